@@ -1,0 +1,144 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: causal grouped-query attention on
+ * NVIDIA GB300 (sm_103a).
+ *
+ *   out[i, h, :] = softmax_j( scale * q[i, h, :] . k[j, g, :] )  v[j, g, :]
+ *
+ * over the keys j that query row i may see, with g = h / (Hq / Hkv) the KV
+ * head shared by a group of query heads.  Query rows are bottom-right
+ * aligned: with R query rows and a context of N keys, row i sits at absolute
+ * position N - R + i and sees keys 0 .. N - R + i.
+ *
+ * Sources (web pages, by title and section):
+ *   [P1] "[Kernel][SM70] Default long-prefill GQA architecture", Purpose:
+ *        causal FP16 prefill, Q=8000, KV=40000..128000, Hq=6, Hkv=1, D=256,
+ *        scale 1/16; Test Result: FP16 envelope max abs <= 1e-3, rel L2 <= 1e-2.
+ *   [P2] "[Perf] Ship the qualified SM70 long-context layout and drop its
+ *        context fences", What / Changes: grouped E4M3 FP32 long-context
+ *        operator, capacity 262144, verifier tails of 1..8 query rows.
+ *   [P3] "[Kernel][SM70] Repair #378 on latest main", Changes: per-row
+ *        selected four-token KV blocks over a page-16 cache whose block table
+ *        is in physical-page units; positions clamped to the row.
+ *
+ * Conventions shared by every entry point
+ *   - Supported family: Hq = 6, Hkv = 1, D = 256 (other values return
+ *     GQA_ERR_UNSUPPORTED).  scale must be finite and > 0.
+ *   - All tensor pointers are DEVICE pointers, contiguous, 16-byte aligned,
+ *     owned by the caller.  fp16 means IEEE binary16.
+ *   - q / out are [rows, Hq, D] fp16; out is fully overwritten.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     never allocate or free memory.  Work that needs scratch space (split
+ *     partials, merge counters) uses the workspace registered with
+ *     gqa_set_workspace for the current device; calls that share one
+ *     workspace must not overlap on the GPU (issue them on one stream).
+ *   - Results are bitwise reproducible from run to run and under CUDA-graph
+ *     replay: the work partition depends only on the shape and the device's
+ *     SM count, and every reduction has a fixed order.
+ *   - The first call of each entry point on a device loads its kernels and
+ *     sets their shared-memory limits; make it before capturing a graph.
+ *   - Return value: a gqa_status.  Argument errors are detected on the host
+ *     before anything is launched.  Errors found on the device (out-of-range
+ *     block ids, a pipeline wait that timed out) set a per-device error word
+ *     read by gqa_get_device_error; the kernel masks the offending input and
+ *     carries on (or returns) instead of trapping.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, rows > context, bad scale */
+    GQA_ERR_UNSUPPORTED = 2,   /* outside Hq=6, Hkv=1, D=256, page=16, query_rows<=8 (paged) */
+    GQA_ERR_WORKSPACE = 3,     /* no workspace registered, or it is too small */
+    GQA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} gqa_status;
+
+/* Bits of the device error word (gqa_get_device_error). */
+#define GQA_DEVERR_WAIT_TIMEOUT 0x1u  /* a pipeline wait exceeded its limit; output invalid */
+#define GQA_DEVERR_BAD_BLOCK_ID 0x2u  /* sel_idx held an id < 0 or past the row's own block */
+#define GQA_DEVERR_BAD_PAGE_ID  0x4u  /* a block-table entry was < 0 or >= num_pages */
+
+/* Dense causal prefill [P1, Purpose].
+ *   q   [Q, Hq, D]  fp16     k, v [KV, Hkv, D] fp16     out [Q, Hq, D] fp16
+ *   1 <= Q <= KV.  Row i sees keys 0 .. KV - Q + i.
+ * FP32 accumulation; P is rounded to fp16 before the P.V product; the output
+ * is rounded to nearest fp16.  Long problems are split over all SMs; the
+ * split partials live in the registered workspace
+ * (gqa_workspace_bytes(GQA_KIND_PREFILL, Q, KV, Hq, D) bytes). */
+int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int Q, int KV,
+                     int Hq, int Hkv, int D, float scale, struct CUstream_st* stream);
+
+/* Paged FP8-E4M3 verifier tail [P2, What / Changes].
+ *   q            [query_rows, Hq, D] fp16, 1 <= query_rows <= 8
+ *   kcache/vcache [num_pages, page, Hkv, D] uint8 E4M3 codes (OCP e4m3fn:
+ *                bias 7, 0x7F/0xFF NaN, max 448); real value = decode(byte) * scale
+ *   kscale/vscale DEVICE pointers to one fp32 each (graph-capturable)
+ *   block_table  [ceil(ctx_len / page)] int32 physical page ids, each in
+ *                [0, num_pages); entries outside it are clamped to page 0 and
+ *                flag GQA_DEVERR_BAD_PAGE_ID
+ *   page = 16; query_rows <= ctx_len <= num_pages * page.
+ * Tail row r sits at position ctx_len - query_rows + r.  The key range is
+ * split over all SMs; each split's (O, m, l) partial goes to the workspace
+ * and the last split to finish merges them in a fixed order. */
+int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                        const float* kscale, const float* vscale, const int32_t* block_table,
+                        int num_pages, int page, int ctx_len, int query_rows, int Hq, int Hkv,
+                        int D, float scale, void* out, struct CUstream_st* stream);
+
+/* Selected-block sparse paged prefill [P3, Changes].
+ *   q            [query_rows, Hq, D] fp16
+ *   kcache/vcache [num_pages, page, Hkv, D] fp16, page = 16
+ *   block_table  [ceil(ctx_len / page)] int32 physical page ids
+ *   sel_idx      [query_rows, max_sel] int32 logical 4-token block ids b
+ *                (tokens 4b .. 4b+3); sel_cnt [query_rows] int32, 0..max_sel
+ * Row i (position p = ctx_len - query_rows + i) attends the tokens of its
+ * first sel_cnt[i] selected blocks that are <= p; the row's own block is
+ * clamped to p.  A row's ids must be distinct.  Ids < 0 or > p / 4 select
+ * nothing and flag GQA_DEVERR_BAD_BLOCK_ID.  A row that selects no visible
+ * token gets a zero output.  Needs no workspace. */
+int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
+                           const int32_t* block_table, const int32_t* sel_idx,
+                           const int32_t* sel_cnt, int max_sel, int num_pages, int page,
+                           int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
+                           void* out, struct CUstream_st* stream);
+
+/* Workspace kinds for gqa_workspace_bytes. */
+#define GQA_KIND_PREFILL 0
+#define GQA_KIND_PAGED_E4M3 1
+#define GQA_KIND_SPARSE 2
+
+/* Bytes of workspace an entry point of `kind` needs for the given shape on
+ * the current device (query_rows = Q or the tail/row count, ctx_or_kv = KV or
+ * ctx_len).  Returns 0 for unsupported arguments. */
+size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D);
+
+/* Register caller-owned device memory as the workspace of `device`
+ * (ptr 256-byte aligned, or NULL to unregister).  The library keeps the
+ * pointer and never frees it.  Registration zeroes the small counter area at
+ * the start of the workspace (a synchronous cudaMemset); kernels leave those
+ * counters at zero when they finish.  After a device error
+ * (gqa_get_device_error != 0) register the workspace again. */
+int gqa_set_workspace(int device, void* ptr, size_t bytes);
+
+/* Synchronise `stream`, then read and clear the current device's error word
+ * (GQA_DEVERR_* bits; 0 = no device-side error since the last read).
+ * Returns -1 if the CUDA calls themselves failed. */
+int gqa_get_device_error(struct CUstream_st* stream);
+
+/* Human-readable name of a gqa_status value. */
+const char* gqa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

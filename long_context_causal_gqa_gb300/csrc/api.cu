@@ -1,0 +1,214 @@
+// api.cu -- the C ABI declared in include/gqa_attn.h: argument validation,
+// per-device state (SM count, error word, registered workspace), tensor-map
+// encoding, and dispatch to the kernel launchers.  No entry point allocates
+// or frees device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
+#include <string.h>
+
+#include "internal.h"
+
+namespace gqa {
+
+// One error word per device (module-scope device memory, not an allocation).
+__device__ unsigned g_err_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    DeviceInfo info{};
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+
+}  // namespace
+
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+        st.info.device = dev;
+        st.info.num_sms = sms;
+        st.info.err_word = static_cast<unsigned*>(p);
+        st.ready = true;
+    }
+    return &st.info;
+}
+
+void current_workspace(void** ptr, size_t* bytes) {
+    int dev = 0;
+    *ptr = nullptr;
+    *bytes = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    *ptr = g_dev[dev].ws;
+    *bytes = g_dev[dev].ws_bytes;
+}
+
+EncodeTiledFn encode_tiled() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_cols) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+namespace {
+
+bool family_ok(int Hq, int Hkv, int D) { return Hq == kHq && Hkv == kHkv && D == kHeadDim; }
+
+bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
+
+}  // namespace
+
+extern "C" {
+
+int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int Q, int KV,
+                     int Hq, int Hkv, int D, float scale, struct CUstream_st* stream) {
+    if (!q || !k || !v || !out) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if (Q < 1 || KV < 1 || Q > KV || !scale_ok(scale)) return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
+    if ((long long)Q * Hq > 0x7fffffffLL - 256) return GQA_ERR_INVALID_ARG;
+    return prefill_launch(q, k, v, out, Q, KV, scale, stream);
+}
+
+int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                        const float* kscale, const float* vscale, const int32_t* block_table,
+                        int num_pages, int page, int ctx_len, int query_rows, int Hq, int Hkv,
+                        int D, float scale, void* out, struct CUstream_st* stream) {
+    if (!q || !kcache || !vcache || !kscale || !vscale || !block_table || !out)
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale) |
+         reinterpret_cast<uintptr_t>(block_table)) & 3u)
+        return GQA_ERR_INVALID_ARG;
+    if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
+    return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, ctx_len,
+                             query_rows, scale, out, stream);
+}
+
+int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
+                           const int32_t* block_table, const int32_t* sel_idx,
+                           const int32_t* sel_cnt, int max_sel, int num_pages, int page,
+                           int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
+                           void* out, struct CUstream_st* stream) {
+    if (!q || !kcache || !vcache || !block_table || !sel_idx || !sel_cnt || !out)
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(sel_idx) |
+         reinterpret_cast<uintptr_t>(sel_cnt)) & 3u)
+        return GQA_ERR_INVALID_ARG;
+    if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || max_sel < 1 ||
+        !scale_ok(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D) || page != kPage) return GQA_ERR_UNSUPPORTED;
+    if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
+    return sparse_launch(q, kcache, vcache, block_table, sel_idx, sel_cnt, max_sel, num_pages,
+                         ctx_len, query_rows, scale, out, stream);
+}
+
+size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {
+    if (Hq != kHq || D != kHeadDim || query_rows < 1 || ctx_or_kv < query_rows) return 0;
+    const DeviceInfo* di = device_info();
+    if (!di) return 0;
+    switch (kind) {
+        case GQA_KIND_PREFILL:
+            return prefill_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
+        case GQA_KIND_PAGED_E4M3:
+            if (query_rows > 8) return 0;
+            return paged_e4m3_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
+        case GQA_KIND_SPARSE:
+            return kWorkspaceCounterBytes;
+        default:
+            return 0;
+    }
+}
+
+int gqa_set_workspace(int device, void* ptr, size_t bytes) {
+    if (device < 0 || device >= 64) return GQA_ERR_INVALID_ARG;
+    if (ptr && ((reinterpret_cast<uintptr_t>(ptr) & 255u) || bytes < kWorkspaceCounterBytes))
+        return GQA_ERR_INVALID_ARG;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return GQA_ERR_CUDA;
+    if (ptr) {
+        if (cudaSetDevice(device) != cudaSuccess) return GQA_ERR_CUDA;
+        cudaError_t e = cudaMemset(ptr, 0, kWorkspaceCounterBytes);
+        cudaSetDevice(prev);
+        if (e != cudaSuccess) return GQA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_dev[device].ws = ptr;
+    g_dev[device].ws_bytes = ptr ? bytes : 0;
+    return GQA_OK;
+}
+
+int gqa_get_device_error(struct CUstream_st* stream) {
+    const DeviceInfo* di = device_info();
+    if (!di) return -1;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof v) != cudaSuccess) return -1;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof zero) != cudaSuccess) return -1;
+    return (int)v;
+}
+
+const char* gqa_status_string(int status) {
+    switch (status) {
+        case GQA_OK: return "GQA_OK";
+        case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG";
+        case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
+        case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE";
+        case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+        default: return "GQA_UNKNOWN_STATUS";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gqa_attn.h"
+
+namespace gqa {
+
+constexpr int kHq = 6;
+constexpr int kHkv = 1;
+constexpr int kHeadDim = 256;
+constexpr int kPage = 16;
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    unsigned* err_word;  // device address of this device's error word
+};
+
+// Per-device facts, looked up once; returns nullptr on a CUDA error.
+const DeviceInfo* device_info();
+
+// Workspace registered for the current device (ptr may be null).
+void current_workspace(void** ptr, size_t* bytes);
+
+// cuTensorMapEncodeTiled, fetched through the runtime's driver entry point.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
+
+// 2D fp16 row-major tensor [rows, cols] with a box of [box_rows, box_cols]
+// (box_cols * 2 bytes <= 128), 128-byte swizzle, zero fill out of bounds.
+bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_cols);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launchers (one per kernel family).  Arguments are validated by the caller.
+int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
+                   float scale, cudaStream_t stream);
+size_t prefill_workspace_bytes(int Q, int KV, int num_sms);
+
+int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                      const float* kscale, const float* vscale, const int32_t* block_table,
+                      int num_pages, int ctx_len, int R, float scale, void* out,
+                      cudaStream_t stream);
+size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms);
+
+int sparse_launch(const void* q, const void* kcache, const void* vcache,
+                  const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
+                  int max_sel, int num_pages, int ctx_len, int rows, float scale, void* out,
+                  cudaStream_t stream);
+
+// Bytes at the start of every workspace reserved for merge counters.
+constexpr size_t kWorkspaceCounterBytes = 4096;
+
+}  // namespace gqa

@@ -1,0 +1,113 @@
+"""GPU parity of the dense causal prefill against the FP64 oracle.
+
+Pass criterion ("[Kernel][SM70] Default long-prefill GQA architecture", Test
+Result): max abs error <= 1e-3 and relative L2 <= 1e-2, all outputs finite.
+Output must also be bitwise reproducible across runs and CUDA-graph replay
+("[Kernel][SM70] Repair #378 on latest main", Test Result: graph replay
+bitwise equal to eager).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_causal_gqa_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-3
+REL_L2 = 1e-2
+
+
+def _check(got, ref, what=""):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all(), what
+    err = np.abs(g - ref).max()
+    rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+    assert err <= MAX_ABS and rel <= REL_L2, f"{what}: max abs {err:.3e} rel L2 {rel:.3e}"
+    return err, rel
+
+
+def _run(lib, d):
+    dev = torch.device("cuda")
+    q, k, v = d.q.to(dev), d.k.to(dev), d.v.to(dev)
+    out = lib.prefill(q, k, v, d.scale)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    return out
+
+
+@pytest.mark.parametrize("Q,KV", [
+    (256, 1024),   # the small configuration, full comparison
+    (1, 1),        # single key
+    (1, 300),      # one row, many keys
+    (7, 7),        # square causal
+    (22, 150),     # one ragged q-tile (132 packed rows)
+    (100, 333),    # several tiles, ragged KV tail
+    (300, 300),    # square, many diagonal tiles
+    (640, 2100),   # enough work to split q-tiles across CTAs
+])
+def test_prefill_matches_oracle(cuda_lib, Q, KV):
+    d = inputs.dense_inputs(Q, KV, seed=Q + KV)
+    out = _run(cuda_lib, d)
+    ref = oracle.dense(d.q, d.k, d.v, d.scale)
+    _check(out, ref, f"Q={Q} KV={KV}")
+
+
+def _sample_rows(Q, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 20, 21, 22, 42, 43, Q // 2, Q - 22, Q - 2, Q - 1]
+    rows = sorted(set([r for r in fixed if 0 <= r < Q] + rng.choice(Q, n, replace=False).tolist()))
+    return np.array(rows, dtype=np.int32)
+
+
+@pytest.mark.parametrize("Q,KV", [(8000, 40000), (8000, 128000)])
+def test_prefill_full_size_sampled_rows(cuda_lib, Q, KV):
+    d = inputs.dense_inputs(Q, KV, seed=1)
+    out = _run(cuda_lib, d)
+    rows = _sample_rows(Q)
+    ref = oracle.dense(d.q, d.k, d.v, d.scale, rows=rows)
+    _check(out[torch.as_tensor(rows, dtype=torch.long)], ref, f"Q={Q} KV={KV}")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_prefill_bitwise_reproducible_and_graph_replay(cuda_lib):
+    dev = torch.device("cuda")
+    d = inputs.dense_inputs(700, 5000, seed=3)
+    q, k, v = d.q.to(dev), d.k.to(dev), d.v.to(dev)
+    a = cuda_lib.prefill(q, k, v, d.scale)
+    b = cuda_lib.prefill(q, k, v, d.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        cuda_lib.prefill(q, k, v, d.scale, out=out)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        cuda_lib.prefill(q, k, v, d.scale, out=out)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), a.view(torch.int16))
+    assert cuda_lib.device_error() == 0
+
+
+def test_prefill_future_keys_do_not_leak(cuda_lib):
+    dev = torch.device("cuda")
+    d = inputs.dense_inputs(200, 700, seed=5)
+    base = cuda_lib.prefill(d.q.to(dev), d.k.to(dev), d.v.to(dev), d.scale)
+    # Change every key/value past row 0's last visible key (finite values: they
+    # are real positions other rows see).  Row 0 must not change at all.
+    k2, v2 = d.k.clone(), d.v.clone()
+    k2[700 - 200 + 1:] = 60000.0
+    v2[700 - 200 + 1:] = -30000.0
+    out = cuda_lib.prefill(d.q.to(dev), k2.to(dev), v2.to(dev), d.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0].view(torch.int16), base[0].view(torch.int16))
