@@ -1,0 +1,452 @@
+"""Benchmark of the causal GQA hot path on GB300.
+
+Headline (one JSON line on stdout, rank 0): causal-visible TFLOP/s of the
+dense prefill at Q=8000 query rows bottom-right aligned to KV=40000 keys,
+Hq=6, Hkv=1, D=256, scale 1/16, fp16 in/out ("[Kernel][SM70] Default
+long-prefill GQA architecture", Purpose and Test Result).  One step = one
+gqa_attn_prefill call (main kernel + split merge) on inputs resident in HBM;
+L2 is flushed before every timed step.  The same line carries:
+
+* ``roofline``: the step's algorithmic FLOPs / measured step time against the
+  measured dense bf16 tensor peak (fp16 runs at the same nominal rate);
+* ``e2e``: the same metric through the C ABI with pinned host buffers and the
+  host<->device copies inside the timed region;
+* ``cpu_baseline``: the FP64 CPU oracle on a bounded sample of query rows;
+* ``secondary``: the KV sweep 40K..128K, the paged E4M3 verifier tail at
+  ctx 261888 (HBM roofline) and the selected-block sparse prefill.
+
+``--impl reference`` times the CPU oracle alone on the same workload (bounded
+sample per step) and prints the same kind of line with "impl": "reference".
+Under torchrun each rank runs its own independent problem (weak scaling);
+rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HQ, D, SCALE = 6, 256, 1.0 / 16
+Q_MAIN, KV_MAIN = 8000, 40000
+
+
+def visible_pairs(Q: int, KV: int) -> int:
+    return Q * (KV - Q) + Q * (Q + 1) // 2
+
+
+def prefill_flops(Q: int, KV: int) -> float:
+    # QK^T and PV: 2 FLOPs per multiply-add each, per head, per visible pair.
+    return 4.0 * D * HQ * visible_pairs(Q, KV)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j.get("hbm_gbs", 6800.0), "bf16_tflops": j.get("bf16_tflops", 1900.0),
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", 1700.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def time_steps(fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) of fn() on `stream`, L2 flushed before each."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    for a, b in evs:
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def make_flush(device):
+    import torch
+    buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        buf.fill_(1.0)
+    return flush
+
+
+def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0):
+    import torch
+    from long_context_causal_gqa_gb300 import inputs
+    d = inputs.dense_inputs(Q, KV, seed=seed)
+    q, k, v = d.q.to(device), d.k.to(device), d.v.to(device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+    binding.prefill(q, k, v, SCALE, out=out)
+    times = time_steps(lambda: binding.prefill(q, k, v, SCALE, out=out), steps, warmup, flush,
+                       stream)
+    return times, (q, k, v, out, d)
+
+
+def bench_e2e_prefill(binding, d, steps, warmup, device):
+    """Prefill through the public API with pinned host inputs: H2D copies of
+    q, k, v, the call, and the D2H copy of out are all inside the timed region."""
+    import torch
+    hq, hk, hv = d.q.pin_memory(), d.k.pin_memory(), d.v.pin_memory()
+    hout = torch.empty_like(d.q).pin_memory()
+    q = torch.empty_like(hq, device=device)
+    k = torch.empty_like(hk, device=device)
+    v = torch.empty_like(hv, device=device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        binding.prefill(q, k, v, SCALE, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    times = time_steps(step, steps, warmup, lambda: None, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size()
+    return times, h2d, d2h
+
+
+def bench_paged(binding, R, device, steps, warmup, flush, ctx_len=261888, seed=0):
+    import torch
+    from long_context_causal_gqa_gb300 import inputs
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx_len, capacity=262144, seed=seed)
+    q = p.q.to(device)
+    kc, vc = p.kcache.to(device), p.vcache.to(device)
+    ks = torch.tensor([p.kscale], dtype=torch.float32, device=device)
+    vs = torch.tensor([p.vscale], dtype=torch.float32, device=device)
+    bt = p.block_table.to(device)
+    out = torch.empty_like(q)
+
+    def call():
+        binding.paged_e4m3(q, kc, vc, ks, vs, bt, ctx_len, SCALE, out=out)
+    call()
+    torch.cuda.synchronize()
+    # Replay the tail from a CUDA graph, as a verifier round would.
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    times = time_steps(g.replay, steps, warmup, flush, torch.cuda.current_stream())
+    kv_bytes = 2 * ctx_len * D  # one E4M3 byte per K and V element, Hkv = 1
+    return times, kv_bytes, 4.0 * D * HQ * visible_pairs(R, ctx_len)
+
+
+def bench_sparse(binding, T, device, steps, warmup, flush, rows=4096, ctx_len=32768, seed=0):
+    import torch
+    from long_context_causal_gqa_gb300 import inputs
+    s = inputs.sparse_inputs(rows=rows, ctx_len=ctx_len, tokens=T, seed=seed)
+    args = [x.to(device) for x in (s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt)]
+    out = torch.empty_like(args[0])
+
+    def call():
+        binding.sparse_blocks(*args, ctx_len, SCALE, out=out)
+    call()
+    times = time_steps(call, steps, warmup, flush, torch.cuda.current_stream())
+    visible = 0
+    for i in range(rows):
+        p = ctx_len - rows + i
+        n = int(s.sel_cnt[i])
+        visible += 4 * n - (3 - p % 4)
+    gathered = rows * T * 2 * D * 2
+    return times, gathered, 4.0 * D * HQ * visible
+
+
+def cpu_baseline_prefill(Q, KV, seconds_target=15.0, seed=0):
+    """Times the FP64 oracle on sampled query rows of the dense workload."""
+    import numpy as np
+    import oracle
+    from long_context_causal_gqa_gb300 import inputs
+    d = inputs.dense_inputs(Q, KV, seed=seed)
+    ncores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    # Calibrate on a few rows, then size the sample to about seconds_target.
+    rows = rng.choice(Q, ncores, replace=False).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.dense(d.q, d.k, d.v, SCALE, rows=rows, nthreads=ncores)
+    dt = time.perf_counter() - t0
+    n = int(max(ncores, min(Q, ncores * max(1, int(seconds_target / max(dt, 1e-3))))))
+    rows = np.sort(rng.choice(Q, n, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.dense(d.q, d.k, d.v, SCALE, rows=rows, nthreads=ncores)
+    dt = time.perf_counter() - t0
+    pairs = sum(KV - Q + int(r) + 1 for r in rows)
+    flops = 4.0 * D * HQ * pairs
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{n} of {Q} query rows x {HQ} heads of Q={Q} KV={KV}, FP64 two-pass"}
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from long_context_causal_gqa_gb300 import binding, build_lib
+    if not build_lib.up_to_date():
+        if rank == 0:
+            build_lib.build()
+        barrier(world)
+    binding.load()
+    peaks = load_peaks()
+    flush = make_flush(device)
+    Q, KV = args.q, args.kv
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    times, keep = bench_prefill(binding, Q, KV, args.steps, args.warmup, flush, device,
+                                seed=rank)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = statistics.mean(times)
+    step_ms_max = max_over_ranks(step_ms, world, device)
+    flops = prefill_flops(Q, KV)
+    value = flops * world / (step_ms_max * 1e-3) / 1e12
+    launches_per_step = 2  # main kernel + split merge
+    achieved = flops / (step_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+
+    e2e_times, h2d, d2h = bench_e2e_prefill(binding, keep[4], args.steps, min(args.warmup, 3),
+                                            device)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times), world, device)
+    assert binding.device_error() == 0
+
+    line = {
+        "metric": "causal-visible TFLOP/s of dense causal GQA prefill (Q=8000, KV=40000, "
+                  "Hq=6, Hkv=1, D=256); % of FP16 tensor-core peak",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "data": "synthetic: seeded i.i.d. N(0,1) fp16 q/k/v",
+        "config": {"workload": f"dense causal GQA prefill Q={Q} KV={KV} Hq=6 Hkv=1 D=256 "
+                               "scale=1/16 batch 1", "Q": Q, "KV": KV,
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"{world} independent problem(s), one per GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peaks['source']} bf16 dense burst (fp16 same nominal rate)",
+                     "traffic": None,
+                     "note": "achieved = causal-visible FLOPs / CUDA-event time of one step "
+                             "(main kernel + merge)"},
+        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    secondary = []
+    if not args.quick:
+        for kv in ([48000, 56000, 64000, 72000, 80000, 88000, 96000, 104000, 112000, 120000,
+                    128000] if args.sweep else [128000]):
+            t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device)
+            ms = statistics.mean(t)
+            secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
+                              "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
+                              "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4)})
+        for R in (1, 2, 8):
+            try:
+                t, nbytes, fl = bench_paged(binding, R, device, 50, 5, flush)
+                derr = binding.device_error()
+            except Exception as e:  # a secondary failure must not lose the headline
+                secondary.append({"what": f"paged_e4m3 R={R}", "error": str(e)[:200]})
+                continue
+            if derr:
+                secondary.append({"what": f"paged_e4m3 R={R}", "error": f"device error {derr}"})
+                continue
+            us = statistics.median(t) * 1e3
+            gbs = nbytes / (us * 1e-6) / 1e9
+            secondary.append({"what": f"paged E4M3 tail R={R} ctx=261888 (graph replay)",
+                              "us": round(us, 2), "GB/s": round(gbs, 1),
+                              "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                              "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 1)})
+        for T in (64, 512, 2048):
+            try:
+                t, gathered, fl = bench_sparse(binding, T, device, 5, 2, flush)
+                derr = binding.device_error()
+            except Exception as e:
+                secondary.append({"what": f"sparse T={T}", "error": str(e)[:200]})
+                continue
+            if derr:
+                secondary.append({"what": f"sparse T={T}", "error": f"device error {derr}"})
+                continue
+            ms = statistics.median(t)
+            secondary.append({"what": f"sparse blocks 4096 rows T={T} ctx=32768", "ms": round(ms, 4),
+                              "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1),
+                              "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2)})
+    line["secondary"] = secondary
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(Q, KV, seconds_target=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    Q, KV = args.q, args.kv
+    for _ in range(args.warmup):
+        cpu_baseline_prefill(Q, KV, seconds_target=1.0)
+    vals, secs = [], []
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline_prefill(Q, KV, seconds_target=args.ref_seconds)
+        vals.append(last["value"])
+        secs.append(last["seconds"])
+    value = statistics.mean(vals)
+    ms_full = prefill_flops(Q, KV) / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference",
+        "metric": "causal-visible TFLOP/s of dense causal GQA prefill (Q=8000, KV=40000, "
+                  "Hq=6, Hkv=1, D=256); % of FP16 tensor-core peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_full, 1),
+        "ms_per_step_note": "extrapolated to the full problem from the sampled rows",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded i.i.d. N(0,1) fp16 q/k/v",
+        "config": {"workload": f"dense causal GQA prefill Q={Q} KV={KV} Hq=6 Hkv=1 D=256 "
+                               "scale=1/16 batch 1", "Q": Q, "KV": KV},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"],
+                         "kind": "oracle", "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--q", type=int, default=Q_MAIN)
+    ap.add_argument("--kv", type=int, default=KV_MAIN)
+    ap.add_argument("--sweep", action="store_true", help="secondary: all 12 KV shapes")
+    ap.add_argument("--quick", action="store_true", help="headline only, no secondary")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -40,6 +40,11 @@ EncodeTiledFn encode_tiled();
 bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols);
 
+// 2D uint8 row-major tensor [rows, cols] with a box of [box_rows, box_cols]
+// (box_cols <= 128), 128-byte swizzle.
+bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows, uint32_t box_cols);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (one per kernel family).  Arguments are validated by the caller.

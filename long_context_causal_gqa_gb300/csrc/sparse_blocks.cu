@@ -1,0 +1,533 @@
+// sparse_blocks.cu -- selected-block sparse paged prefill on sm_103a.
+//
+// Problem ("[Kernel][SM70] Repair #378 on latest main", Changes): each query
+// row i (position p = ctx_len - rows + i, 6 query heads sharing 1 KV head,
+// D = 256) attends its own list of selected four-token KV blocks of an fp16
+// page-16 cache (block table in physical-page units); the row's own block is
+// clamped to p, and an index outside 0 .. p/4 selects nothing.  The page
+// converts the blocks into locality-sorted virtual pages for a V100 paged
+// kernel; here every row's gather feeds the tensor cores directly:
+//
+// * Persistent CTAs, one per SM, walk the rows (row = cta, cta + G, ...).  A
+//   row's keys come in tiles of 128 (32 blocks); all 6 heads share them.
+// * Gather: four warps issue 16-byte cp.async copies, one warp-wide 512-byte
+//   copy per token row of K or V, straight into a 128B-swizzled smem tile;
+//   tokens that are masked (past p, past the list, or a bad id) are
+//   zero-filled, so stale cache contents (even NaN) never reach the MMA.
+//   Completion is counted on mbarriers (cp.async.mbarrier.arrive.noinc).
+// * Swap-AB UMMA with keys as M = 128 and the 6 heads (padded to 16) as N:
+//     S^T[128 x 16] = K[128 x 256] . Q^T,  O^T[256 x 16] += V^T . P^T.
+// * Softmax across TMEM lanes with a lazily moved per-head reference max
+//   (exact cross-lane max only on a row's first tile or when a score exceeds
+//   the reference by more than 8 in log2 units); row sums stay per thread
+//   until the row ends.  The epilogue writes out[i] directly (no split).
+//
+// Warp roles (320 threads): 0..3 gather, 4 TMEM owner + UMMA issuer,
+// 5..8 key warps (softmax + epilogue; thread = TMEM lane), 9 idle helper.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace gqa {
+namespace sparse {
+
+constexpr int D = kHeadDim;
+constexpr int HQ = kHq;
+constexpr int PAGE = kPage;
+constexpr int TILE = 128;            // keys per tile
+constexpr int BLK = 4;               // tokens per selected block
+constexpr int NP = 16;               // 6 heads padded to the UMMA N granule
+constexpr int KV_TILE_BYTES = TILE * D * 2;   // 64 KB
+constexpr int NTHREADS = 320;
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+struct Params {
+    const __half* q;
+    const __half* kcache;
+    const __half* vcache;
+    const int32_t* table;
+    const int32_t* sel_idx;
+    const int32_t* sel_cnt;
+    int max_sel, num_pages, ctx_len, rows, G;
+    float scale_log2;
+    __half* out;
+    unsigned* err;
+};
+
+// smem layout (offsets from a 1024-aligned base)
+constexpr int OFF_K = 0;                                  // 2 x 64 KB
+constexpr int OFF_V = OFF_K + 2 * KV_TILE_BYTES;          // 64 KB
+constexpr int Q_BYTES = NP * D * 2;                       // 8 KB: 4 chunks [16][64]
+constexpr int OFF_Q = OFF_V + KV_TILE_BYTES;              // 2 x 8 KB
+constexpr int PT_BYTES = NP * TILE * 2;                   // 4 KB: 2 chunks [16][64 keys]
+constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;               // 2 x 4 KB
+constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;            // [4][NP] floats
+constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
+constexpr int OFF_FAC = OFF_MREF + NP * 4;
+constexpr int OFF_FLAG = OFF_FAC + NP * 4;                // [2][4] ints
+constexpr int OFF_BAR = (OFF_FLAG + 32 + 7) & ~7;
+enum {
+    B_KFULL = 0,   // [2]
+    B_KEMPTY = 2,  // [2]
+    B_VFULL = 4,
+    B_VEMPTY = 5,
+    B_QFULL = 6,   // [2]
+    B_QEMPTY = 8,  // [2]
+    B_SFULL = 10,  // [2]
+    B_PREADY = 12, // [2]
+    B_PTEMPTY = 14,// [2]
+    B_DRAIN = 16,
+    B_GROUP = 17,  // key-thread group barrier
+    NUM_BARS = 18
+};
+constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM = OFF_TMEM + 16 + 1024;
+constexpr uint32_t S_COL = 0;        // 2 x NP
+constexpr uint32_t O_COL = 2 * NP;   // 2 halves x NP
+constexpr uint32_t TMEM_COLS = 128;
+
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t u) {
+    return r * 128u + ((u ^ (r & 7u)) << 4);
+}
+
+// Barrier among the 128 key threads built on an mbarrier (count 128), so that
+// it shares the bounded, abort-aware wait of the pipeline barriers: a thread
+// that gave up elsewhere cannot leave the others blocked here forever.
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* abort,
+                                           unsigned* err) {
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase, abort, err);
+    phase ^= 1u;
+    return ok;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > 100000000ull) break;
+    }
+}
+
+// 16-byte async copy global -> shared; src_bytes = 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on the mbarrier once all of this thread's earlier cp.async copies land.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ int row_tiles(int cnt) { return (cnt * BLK + TILE - 1) / TILE; }
+
+// Token of key slot `key` (0..127) in tile `t` of row i, or -1 if masked.
+// Flags ids outside 0 .. p/4.
+__device__ __forceinline__ int key_token(const Params& P, int i, int cnt, int t, int key,
+                                         bool flag) {
+    const int li = t * (TILE / BLK) + key / BLK;
+    if (li >= cnt) return -1;
+    const int p = P.ctx_len - P.rows + i;
+    const int b = __ldg(P.sel_idx + (size_t)i * P.max_sel + li);
+    if (b < 0 || b > p / BLK) {
+        if (flag && (key & (BLK - 1)) == 0) atomicOr(P.err, kErrBadBlockId);
+        return -1;
+    }
+    const int tok = b * BLK + (key & (BLK - 1));
+    return tok <= p ? tok : -1;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
+    constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
+    constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (sbase - smem_u32(smem_raw));
+    float* red = reinterpret_cast<float*>(gbase + OFF_RED);
+    float* mref = reinterpret_cast<float*>(gbase + OFF_MREF);
+    float* fac = reinterpret_cast<float*>(gbase + OFF_FAC);
+    volatile int* flags = reinterpret_cast<volatile int*>(gbase + OFF_FLAG);
+    const uint32_t bars = sbase + OFF_BAR;
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(gbase + OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_ptr + 1);
+    auto bar = [&](int i) { return bars + 8u * i; };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_KFULL + b), 128);
+            mbar_init(bar(B_KEMPTY + b), 1);
+            mbar_init(bar(B_QFULL + b), 128);
+            mbar_init(bar(B_QEMPTY + b), 1);
+            mbar_init(bar(B_SFULL + b), 1);
+            mbar_init(bar(B_PREADY + b), 128);
+            mbar_init(bar(B_PTEMPTY + b), 1);
+        }
+        mbar_init(bar(B_VFULL), 128);
+        mbar_init(bar(B_VEMPTY), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_GROUP), 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // Zero both Q buffers once (rows 6..15 stay zero).
+    for (int u = threadIdx.x; u < 2 * Q_BYTES / 16; u += NTHREADS)
+        *reinterpret_cast<uint4*>(gbase + OFF_Q + u * 16) = make_uint4(0, 0, 0, 0);
+    if (warp == 4) {
+        tmem_alloc(smem_u32(tmem_ptr), TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_ptr;
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ gather
+        const int gt = threadIdx.x;        // 0..127
+        uint32_t g = 0;                     // global tile counter
+        int rloc = 0;                       // non-empty rows handled so far
+        bool ok = true;
+        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+            const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
+            const int nt = row_tiles(cnt);
+            if (nt == 0) continue;
+            // Q row i (6 heads x 256 d) -> Q buffer rloc & 1, rows 0..5.
+            const int qb = rloc & 1;
+            if (!mbar_wait(bar(B_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                ok = false;
+                break;
+            }
+            for (int u = gt; u < HQ * (D / 8); u += 128) {
+                const int h = u / (D / 8), c16 = u % (D / 8);
+                const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
+                                     sw128(h, c16 % 8);
+                cp_async16(dst, P.q + ((size_t)i * HQ + h) * D + c16 * 8, 16);
+            }
+            cp_async_arrive(bar(B_QFULL + qb));
+            ++rloc;
+            for (int t = 0; t < nt && ok; ++t, ++g) {
+                // This warp's 32 keys: lane -> token info, then one 512-byte row per key.
+                const int key_l = (warp * 32) + lane;
+                const int tok_l = key_token(P, i, cnt, t, key_l, true);
+                size_t row_l = 0;
+                if (tok_l >= 0) {
+                    int pg = __ldg(P.table + tok_l / PAGE);
+                    if (pg < 0 || pg >= P.num_pages) {
+                        atomicOr(P.err, kErrBadPageId);
+                        pg = 0;
+                    }
+                    row_l = ((size_t)pg * PAGE + (tok_l % PAGE)) * D;
+                }
+                const int kb = g & 1;
+                for (int kv = 0; kv < 2; ++kv) {
+                    if (kv == 0) {
+                        if (!mbar_wait(bar(B_KEMPTY + kb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        if (!mbar_wait(bar(B_VEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const __half* cache = kv == 0 ? P.kcache : P.vcache;
+                    const uint32_t tile = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V);
+#pragma unroll 4
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = warp * 32 + e;
+                        const int tok = __shfl_sync(0xffffffffu, tok_l, e);
+                        const size_t row = __shfl_sync(0xffffffffu, row_l, e);
+                        // lane covers d = 8 lane .. 8 lane + 7: chunk lane / 8, unit lane % 8
+                        const uint32_t dst = tile + (lane >> 3) * (TILE * 128) + sw128(key, lane & 7);
+                        const __half* src = tok >= 0 ? cache + row + lane * 8 : cache;
+                        cp_async16(dst, src, tok >= 0 ? 16u : 0u);
+                    }
+                    cp_async_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
+                }
+            }
+        }
+        if (!ok) asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            uint32_t g = 0;
+            int rloc = 0;
+            bool ok = true;
+            auto issue_pv = [&](uint32_t x, bool first) -> bool {
+                if (!mbar_wait(bar(B_PREADY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
+                    return false;
+                if (!mbar_wait(bar(B_VFULL), x & 1, abort_flag, P.err)) return false;
+                fence_async_shared();
+                tc_fence_after();
+                const uint32_t pt = sbase + OFF_PT + (x & 1) * PT_BYTES;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int ks = 0; ks < TILE / 16; ++ks) {
+                        const uint64_t a = sdesc_sw128(sbase + OFF_V + (2 * h) * (TILE * 128) +
+                                                           ks * 2048,
+                                                       TILE * 128, 1024);
+                        const uint64_t b =
+                            sdesc_sw128(pt + (ks / 4) * (NP * 128) + (ks % 4) * 32, 16, 1024);
+                        umma_ss(tmem + O_COL + h * NP, a, b, IDESC_PV, (!first || ks > 0));
+                    }
+                }
+                umma_commit(bar(B_PTEMPTY + (x & 1)));
+                umma_commit(bar(B_VEMPTY));
+                return true;
+            };
+            for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+                const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
+                const int nt = row_tiles(cnt);
+                if (nt == 0) continue;
+                const int qb = rloc & 1;
+                if (!mbar_wait(bar(B_QFULL + qb), (rloc >> 1) & 1, abort_flag, P.err)) {
+                    ok = false;
+                    break;
+                }
+                ++rloc;
+                // cp.async writes are generic-proxy writes; order them before UMMA reads.
+                fence_async_shared();
+                const uint32_t g0 = g;
+                for (int t = 0; t < nt; ++t, ++g) {
+                    const int kb = g & 1;
+                    if (!mbar_wait(bar(B_KFULL + kb), (g >> 1) & 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_async_shared();
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t a = sdesc_sw128(sbase + OFF_K + kb * KV_TILE_BYTES +
+                                                           (kk / 4) * (TILE * 128) + (kk % 4) * 32,
+                                                       16, 1024);
+                        const uint64_t b = sdesc_sw128(sbase + OFF_Q + qb * Q_BYTES +
+                                                           (kk / 4) * (NP * 128) + (kk % 4) * 32,
+                                                       16, 1024);
+                        umma_ss(tmem + S_COL + (g & 1) * NP, a, b, IDESC_QK, kk > 0);
+                    }
+                    umma_commit(bar(B_SFULL + (g & 1)));
+                    umma_commit(bar(B_KEMPTY + kb));
+                    if (t == nt - 1) umma_commit(bar(B_QEMPTY + qb));
+                    if (t >= 1 && !(ok = issue_pv(g - 1, g - 1 == g0))) break;
+                }
+                if (ok) ok = issue_pv(g - 1, g - 1 == g0);
+            }
+            if (!ok) {
+                umma_commit(bar(B_DRAIN));
+                drain_wait(bar(B_DRAIN), 0);
+            }
+        }
+    } else if (warp < 9) {
+        // ------------------------------------------------------------ key warps
+        const int wq = warp & 3;
+        const int k = wq * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+        const float sl2 = P.scale_log2;
+        uint32_t g = 0;
+        uint32_t gphase = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+            const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
+            const int nt = row_tiles(cnt);
+            if (nt == 0) {
+                // Nothing selected: the row's output is zero.
+                for (int u = k; u < HQ * (D / 8); u += 128)
+                    reinterpret_cast<uint4*>(P.out + (size_t)i * HQ * D)[u] = make_uint4(0, 0, 0, 0);
+                continue;
+            }
+            if (k < NP) mref[k] = -INFINITY;
+            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            float lpart[NP];
+#pragma unroll
+            for (int c = 0; c < NP; ++c) lpart[c] = 0.f;
+            for (int t = 0; t < nt; ++t, ++g) {
+                const int b = g & 1;
+                const bool masked = key_token(P, i, cnt, t, k, false) < 0;
+                ok = mbar_wait(bar(B_SFULL + b), (g >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                float s[NP];
+                {
+                    uint32_t r[NP];
+                    tmem_ld16(t_lane + S_COL + b * NP, r);
+                    tmem_ld_wait<NP>(r);
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) s[c] = masked ? -INFINITY : __uint_as_float(r[c]) * sl2;
+                }
+                bool exceed = false;
+#pragma unroll
+                for (int c = 0; c < HQ; ++c) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
+                const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                volatile int* fl = flags + (g & 1) * 4;
+                if (lane == 0) fl[wq] = vote != 0;
+                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const bool any = fl[0] | fl[1] | fl[2] | fl[3];
+                if (any) {
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) {
+                        float m = s[c];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (lane == 0) red[wq * NP + c] = m;
+                    }
+                    ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (k < HQ) {
+                        const int c = k;
+                        const float tmax = fmaxf(fmaxf(red[c], red[NP + c]),
+                                                 fmaxf(red[2 * NP + c], red[3 * NP + c]));
+                        const float old = mref[c];
+                        float f = 1.0f;
+                        if (tmax > old + RESCALE_THRESHOLD) {
+                            f = (old == -INFINITY) ? 0.f : ex2(old - tmax);
+                            mref[c] = tmax;
+                        }
+                        fac[c] = f;
+                    }
+                    ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (t > 0) {
+                        const uint32_t x = g - 1;
+                        ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t r[NP];
+                            tmem_ld16(t_lane + O_COL + h * NP, r);
+                            tmem_ld_wait<NP>(r);
+#pragma unroll
+                            for (int c = 0; c < HQ; ++c)
+                                r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c]);
+                            tmem_st16(t_lane + O_COL + h * NP, r);
+                        }
+                        tmem_st_wait();
+                    }
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) lpart[c] *= fac[c];
+                }
+                ok = mbar_wait(bar(B_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                uint8_t* pt = gbase + OFF_PT + b * PT_BYTES;
+                const int kc = k >> 6, kin = k & 63;
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    float p = 0.f;
+                    if (c < HQ) {
+                        const float m = mref[c];
+                        p = ex2(s[c] - (m == -INFINITY ? 0.f : m));
+                        lpart[c] += p;
+                    }
+                    const uint32_t off = kc * (NP * 128) + sw128(c, kin >> 3) + (kin & 7) * 2;
+                    *reinterpret_cast<__half*>(pt + off) = __float2half_rn(p);
+                }
+                fence_async_shared();
+                mbar_arrive(bar(B_PREADY + b));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- row epilogue
+            const uint32_t x = g - 1;
+            ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < HQ; ++c) {
+                float v = lpart[c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) red[wq * NP + c] = v;
+            }
+            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            float inv[HQ];
+#pragma unroll
+            for (int c = 0; c < HQ; ++c) {
+                const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
+                inv[c] = l > 0.f ? 1.0f / l : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[NP];
+                tmem_ld16(t_lane + O_COL + h * NP, r);
+                tmem_ld_wait<NP>(r);
+                const int d = h * 128 + k;
+#pragma unroll
+                for (int c = 0; c < HQ; ++c)
+                    P.out[((size_t)i * HQ + c) * D + d] = __float2half_rn(__uint_as_float(r[c]) * inv[c]);
+            }
+            // red / mref are rewritten by the next row only after this barrier.
+            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace sparse
+
+int sparse_launch(const void* q, const void* kcache, const void* vcache,
+                  const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
+                  int max_sel, int num_pages, int ctx_len, int rows, float scale, void* out,
+                  cudaStream_t stream) {
+    using namespace sparse;
+    const DeviceInfo* di = device_info();
+    if (!di) return GQA_ERR_CUDA;
+    Params P;
+    P.q = static_cast<const __half*>(q);
+    P.kcache = static_cast<const __half*>(kcache);
+    P.vcache = static_cast<const __half*>(vcache);
+    P.table = block_table;
+    P.sel_idx = sel_idx;
+    P.sel_cnt = sel_cnt;
+    P.max_sel = max_sel;
+    P.num_pages = num_pages;
+    P.ctx_len = ctx_len;
+    P.rows = rows;
+    P.G = rows < di->num_sms ? rows : di->num_sms;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.out = static_cast<__half*>(out);
+    P.err = di->err_word;
+    static bool attr_done[64] = {false};
+    if (di->device < 64 && !attr_done[di->device]) {
+        if (cudaFuncSetAttribute(sparse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        attr_done[di->device] = true;
+    }
+    sparse_kernel<<<P.G, NTHREADS, SMEM, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    return GQA_OK;
+}
+
+}  // namespace gqa

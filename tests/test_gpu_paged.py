@@ -1,0 +1,105 @@
+"""GPU parity of the paged FP8-E4M3 verifier tail against the FP64 oracle.
+
+Workload ("[Perf] Ship the qualified SM70 long-context layout and drop its
+context fences", What / Changes / Measurement): R query rows (1..8) at the end
+of a context up to the 262144 capacity, E4M3 K/V with one fp32 scale each in
+page-16 blocks under a permuted block table.  Envelope: max abs <= 1e-3,
+rel L2 <= 1e-2 ("[Kernel][SM70] Default long-prefill GQA architecture",
+Test Result).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_causal_gqa_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _to_dev(p, dev):
+    ks = torch.tensor([p.kscale], dtype=torch.float32, device=dev)
+    vs = torch.tensor([p.vscale], dtype=torch.float32, device=dev)
+    return (p.q.to(dev), p.kcache.to(dev), p.vcache.to(dev), ks, vs, p.block_table.to(dev))
+
+
+def _check(got, ref, what):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all(), what
+    err = np.abs(g - ref).max()
+    rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+    assert err <= 1e-3 and rel <= 1e-2, f"{what}: max abs {err:.3e} rel L2 {rel:.3e}"
+
+
+def _run(lib, p):
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    out = lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    return out
+
+
+@pytest.mark.parametrize("R,ctx,cap", [
+    (1, 1, 16), (8, 8, 16), (1, 3000, 4096), (2, 3001, 4096), (8, 2999, 4096),
+    (3, 130, 256), (5, 5000, 8192), (7, 1000, 1024), (4, 40000, 65536), (6, 777, 2048),
+])
+def test_paged_matches_oracle(cuda_lib, R, ctx, cap):
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx, capacity=cap, seed=R * 31 + ctx)
+    out = _run(cuda_lib, p)
+    ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                            p.ctx_len, p.scale)
+    _check(out, ref, f"R={R} ctx={ctx}")
+
+
+@pytest.mark.parametrize("R", [1, 2, 8])
+def test_paged_full_size(cuda_lib, R):
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=261888, capacity=262144, seed=R)
+    out = _run(cuda_lib, p)
+    ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                            p.ctx_len, p.scale)
+    _check(out, ref, f"R={R} ctx=261888")
+
+
+def test_paged_bitwise_reproducible_and_graph_replay(cuda_lib):
+    dev = torch.device("cuda")
+    p = inputs.paged_e4m3_inputs(R=8, ctx_len=50000, capacity=65536, seed=11)
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    a = cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale)
+    b = cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    out = torch.empty_like(q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale, out=out)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), a.view(torch.int16))
+    assert cuda_lib.device_error() == 0
+
+
+def test_paged_scale_is_read_on_device(cuda_lib):
+    """Doubling vscale in device memory doubles the output (graph-capturable scales)."""
+    dev = torch.device("cuda")
+    p = inputs.paged_e4m3_inputs(R=2, ctx_len=4000, capacity=4096, seed=12)
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    a = cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale).float()
+    vs.mul_(2.0)
+    b = cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale).float()
+    torch.cuda.synchronize()
+    assert torch.allclose(b, 2 * a, rtol=2e-3, atol=1e-6)
+
+
+def test_paged_bad_page_id_sets_device_error(cuda_lib):
+    dev = torch.device("cuda")
+    p = inputs.paged_e4m3_inputs(R=1, ctx_len=500, capacity=512, seed=13)
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    bt[3] = kc.shape[0] + 5
+    cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale)
+    err = cuda_lib.device_error()
+    assert err & cuda_lib.DEVERR_BAD_PAGE_ID
+    assert cuda_lib.device_error() == 0  # read clears it
