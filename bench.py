@@ -392,6 +392,32 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """One secondary workload alone (for profiling): --case paged|sparse."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    from long_context_causal_gqa_gb300 import binding, build_lib
+    if not build_lib.up_to_date():
+        build_lib.build()
+    binding.load()
+    peaks = load_peaks()
+    flush = make_flush(device)
+    if args.case == "paged":
+        t, nbytes, fl = bench_paged(binding, args.rows, device, args.steps, args.warmup, flush)
+        us = statistics.median(t) * 1e3
+        line = {"case": f"paged E4M3 tail R={args.rows} ctx=261888", "us": round(us, 2),
+                "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+    else:
+        t, gathered, fl = bench_sparse(binding, args.tokens, device, args.steps, args.warmup, flush)
+        ms = statistics.median(t)
+        line = {"case": f"sparse blocks 4096 rows T={args.tokens}", "ms": round(ms, 4),
+                "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1)}
+    line["device_error"] = binding.device_error()
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -439,11 +465,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--case", default="headline", choices=["headline", "paged", "sparse"],
+                    help="run one secondary workload alone (profiling)")
+    ap.add_argument("--rows", type=int, default=8, help="--case paged: tail rows")
+    ap.add_argument("--tokens", type=int, default=2048, help="--case sparse: tokens per row")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.case != "headline":
+        run_case(args)
     else:
         run_gpu(args)
 

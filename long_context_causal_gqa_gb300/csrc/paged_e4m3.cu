@@ -556,20 +556,70 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 }
 
 // out[c, d] = vscale * 256 * sum_s w_s O_s[c, d] / sum_s w_s l_s, w_s = 2^(m_s - M).
+// Block (c, dg) merges packed row c for d = 32 dg .. 32 dg + 31.  The split
+// weights are computed once per block in shared memory; warp w then sums the
+// splits s = w, w + 8, ... for its lane's d, and the eight warp sums are added
+// in a fixed order, so the result does not depend on timing.
+constexpr int MERGE_MAX_SPLITS = 1024;
+
 __global__ void __launch_bounds__(256) paged_merge_kernel(const Params P) {
+    __shared__ float w_s[MERGE_MAX_SPLITS];
+    __shared__ float red[8][33];
+    __shared__ float stat[2];
     const int c = blockIdx.x;
-    const int d = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = 0; s < P.G; ++s) M = fmaxf(M, P.ws_ml[((size_t)s * P.nq + c) * 2]);
-    float Lsum = 0.f, acc = 0.f;
-    for (int s = 0; s < P.G; ++s) {
+    const int d = blockIdx.y * 32 + (threadIdx.x & 31);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = P.G;
+    // Phase 1: M = max_s m_s, w_s = 2^(m_s - M), L = sum_s w_s l_s.
+    float mx = -INFINITY;
+    for (int s = threadIdx.x; s < G; s += 256) {
         const float m = P.ws_ml[((size_t)s * P.nq + c) * 2];
-        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-        Lsum += P.ws_ml[((size_t)s * P.nq + c) * 2 + 1] * w;
-        acc += P.ws_o[((size_t)s * P.nq + c) * D + d] * w;
+        w_s[s] = m;
+        mx = fmaxf(mx, m);
     }
-    const float vs = *P.vscale * 256.0f;
-    P.out[(size_t)c * D + d] = __float2half_rn(Lsum > 0.f ? acc / Lsum * vs : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp][32] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float M = red[0][32];
+        for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w][32]);
+        stat[0] = M;
+    }
+    __syncthreads();
+    const float M = stat[0];
+    float lsum = 0.f;
+    for (int s = threadIdx.x; s < G; s += 256) {
+        const float m = w_s[s];
+        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+        w_s[s] = w;
+        lsum += w * P.ws_ml[((size_t)s * P.nq + c) * 2 + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    __syncthreads();
+    if (lane == 0) red[warp][32] = lsum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float L = 0.f;
+        for (int w = 0; w < 8; ++w) L += red[w][32];
+        stat[1] = L;
+    }
+    // Phase 2: weighted sum of the partial O over the splits.
+    float acc = 0.f;
+#pragma unroll 4
+    for (int s = warp; s < G; s += 8) acc += w_s[s] * P.ws_o[((size_t)s * P.nq + c) * D + d];
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) a += red[w][lane];
+        const float L = stat[1];
+        const float vs = *P.vscale * 256.0f;
+        P.out[(size_t)c * D + d] = __float2half_rn(L > 0.f ? a / L * vs : 0.f);
+    }
 }
 
 template <int NP>
@@ -586,7 +636,7 @@ int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStrea
     }
     paged_split_kernel<NP><<<P.G, NTHREADS, L::SMEM, stream>>>(tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    paged_merge_kernel<<<P.nq, 256, 0, stream>>>(P);
+    paged_merge_kernel<<<dim3(P.nq, D / 32), 256, 0, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
 }
@@ -620,6 +670,7 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.nq = R * HQ;
     P.n_tiles = (ctx_len + TILE - 1) / TILE;
     P.G = P.n_tiles < di->num_sms ? P.n_tiles : di->num_sms;
+    if (P.G > MERGE_MAX_SPLITS) P.G = MERGE_MAX_SPLITS;
     P.scale = scale;
     P.out = static_cast<__half*>(out);
     P.err = di->err_word;

@@ -490,55 +490,68 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 }
 
-// Combines the partials of every q-tile that was cut between CTAs.  Block c
-// handles the q-tile whose first piece is CTA c's last segment; pieces are
-// read in CTA order, so the result does not depend on timing.
+// A q-tile cut between CTAs c0 .. c_last: its first piece is CTA c0's last
+// segment (partial slot slot0), the others are the first segments (slot 0) of
+// CTAs c0 + 1 .. c_last.  Found on the host from the same shape-only schedule.
+constexpr int kMaxCtas = 160;
+struct MergeTasks {
+    int n;
+    int4 task[kMaxCtas];  // (q-tile, c0, slot0, c_last)
+};
+
+// blockIdx.x picks a cut q-tile, blockIdx.y 8 of its 128 rows; thread
+// (row, lane) merges 8 consecutive d.  Pieces are combined in CTA order (exact
+// log-sum-exp merge), so the result does not depend on timing.
 __global__ void __launch_bounds__(256)
-prefill_merge_kernel(const Params P) {
-    const int c0 = blockIdx.x;
-    long long pos = cta_begin(P.total, P.G, c0);
-    const long long end = cta_begin(P.total, P.G, c0 + 1);
-    int t = 0;
+prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
+    const int4 tk = T.task[blockIdx.x];
+    const int t = tk.x, c0 = tk.y, slot0 = tk.z, c_last = tk.w;
+    const int r = blockIdx.y * 8 + (threadIdx.x >> 5);
+    const int m_row = t * BM + r;
+    if (m_row >= P.M_total) return;
+    const int d0 = (threadIdx.x & 31) * 8;
+    float M = -INFINITY;
+    for (int c = c0; c <= c_last; ++c) {
+        const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM + r;
+        M = fmaxf(M, P.ws_ml[prow * 2]);
+    }
+    float L = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int c = c0; c <= c_last; ++c) {
+        const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM + r;
+        const float mp = P.ws_ml[prow * 2];
+        const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
+        L += P.ws_ml[prow * 2 + 1] * w;
+        const float4* o = reinterpret_cast<const float4*>(P.ws_o + prow * D + d0);
+        const float4 a = o[0], b = o[1];
+        acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
+        acc[4] += b.x * w; acc[5] += b.y * w; acc[6] += b.z * w; acc[7] += b.w * w;
+    }
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    uint4 hv = make_uint4(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv),
+                          pack_half2(acc[4] * inv, acc[5] * inv), pack_half2(acc[6] * inv, acc[7] * inv));
+    *reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + d0) = hv;
+}
+
+// Host side of the schedule: the cut q-tiles and their pieces.
+static void find_cut_tiles(const Params& P, MergeTasks& T) {
+    T.n = 0;
     long long cum = 0;
-    while (t < P.num_qtiles) {
-        int n = kv_tiles(t, P.Q, P.KV, P.M_total);
-        if (cum + n > pos) break;
-        cum += n;
-        ++t;
-    }
-    // Advance to this CTA's last segment (the tile holding iteration end - 1).
-    for (;;) {
+    int c = 0;  // first CTA whose range ends after cum
+    for (int t = 0; t < P.num_qtiles; ++t) {
         const int n = kv_tiles(t, P.Q, P.KV, P.M_total);
-        if (cum + n >= end) break;
-        cum += n;
-        ++t;
-    }
-    const int n = kv_tiles(t, P.Q, P.KV, P.M_total);
-    // The tile starts inside this CTA and continues past its end?
-    if (!(cum >= pos && cum + n > end)) return;
-    const int slot0 = (cum == pos) ? 0 : 1;
-    // Pieces, in CTA order: (c0, slot0), then (c, slot 0) for the following
-    // CTAs up to the one whose range reaches the tile's end.
-    int c_last = c0 + 1;
-    while (c_last + 1 < P.G && cta_begin(P.total, P.G, c_last + 1) < cum + n) ++c_last;
-    const int d = threadIdx.x;
-    for (int r = 0; r < BM; ++r) {
-        const int m_row = t * BM + r;
-        if (m_row >= P.M_total) break;
-        float M = -INFINITY;
-        for (int c = c0; c <= c_last; ++c) {
-            const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM + r;
-            M = fmaxf(M, P.ws_ml[prow * 2]);
+        const long long t_end = cum + n;
+        // CTA holding the tile's first iteration
+        while (c + 1 < P.G && cta_begin(P.total, P.G, c + 1) <= cum) ++c;
+        if (cta_begin(P.total, P.G, c + 1) < t_end) {  // the tile continues past CTA c
+            int c_last = c + 1;
+            while (c_last + 1 < P.G && cta_begin(P.total, P.G, c_last + 1) < t_end) ++c_last;
+            const int slot0 = (cta_begin(P.total, P.G, c) == cum) ? 0 : 1;
+            T.task[T.n++] = make_int4(t, c, slot0, c_last);
         }
-        float L = 0.f, acc = 0.f;
-        for (int c = c0; c <= c_last; ++c) {
-            const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM + r;
-            const float mp = P.ws_ml[prow * 2];
-            const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
-            L += P.ws_ml[prow * 2 + 1] * w;
-            acc += P.ws_o[prow * D + d] * w;
-        }
-        P.out[(size_t)m_row * D + d] = __float2half_rn(L > 0.f ? acc / L : 0.f);
+        cum = t_end;
     }
 }
 
@@ -565,6 +578,7 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     for (int t = 0; t < P.num_qtiles; ++t) total += kv_tiles(t, Q, KV, P.M_total);
     P.total = total;
     P.G = (int)(total < di->num_sms ? total : di->num_sms);
+    if (P.G > kMaxCtas) P.G = kMaxCtas;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.out = static_cast<__half*>(out);
     P.err = di->err_word;
@@ -598,8 +612,10 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     }
     prefill_kernel<<<P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    if (P.G > 1) {
-        prefill_merge_kernel<<<P.G, 256, 0, stream>>>(P);
+    MergeTasks tasks;  // passed to the merge kernel by value
+    find_cut_tiles(P, tasks);
+    if (tasks.n > 0) {
+        prefill_merge_kernel<<<dim3(tasks.n, BM / 8), 256, 0, stream>>>(P, tasks);
         if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
     return GQA_OK;
