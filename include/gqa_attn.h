@@ -94,6 +94,34 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
                         int num_pages, int page, int ctx_len, int query_rows, int Hq, int Hkv,
                         int D, float scale, void* out, struct CUstream_st* stream);
 
+/* Paged FP8-E4M3 verifier tail that allocates nothing (no counterpart in the
+ * pages; an addition of this library).  Some callers cannot call cudaMalloc:
+ * engines whose pooling allocator owns all device memory and must not see
+ * foreign allocations, latency-critical serving loops in which cudaMalloc's
+ * implicit device synchronisation is not acceptable, and plugin code that has
+ * no access to the process's allocator.  This entry point takes the same
+ * arguments, layouts and error codes as gqa_attn_paged_e4m3 and computes the
+ * same result (bitwise equal on devices with at most 160 SMs), but needs no
+ * registered workspace: its split partials live in a static device array
+ * inside the library, at most 160 splits x 48 packed rows x 258 floats
+ * (about 7.9 MB), which every GPU that loads the library holds until the
+ * process exits.  It never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents.  Nothing in it has to start at zero: a call writes every
+ *     partial it reads.  Calls that overlap on the GPU (e.g. on two streams
+ *     without ordering) race on the array and give wrong results.
+ *   - query_rows > 8 returns GQA_ERR_UNSUPPORTED; a shape whose partials would
+ *     not fit the array returns GQA_ERR_WORKSPACE. */
+int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                                const float* kscale, const float* vscale,
+                                const int32_t* block_table, int num_pages, int page,
+                                int ctx_len, int query_rows, int Hq, int Hkv, int D,
+                                float scale, void* out, struct CUstream_st* stream);
+
 /* Selected-block sparse paged prefill [P3, Changes].
  *   q            [query_rows, Hq, D] fp16
  *   kcache/vcache [num_pages, page, Hkv, D] fp16, page = 16

@@ -34,7 +34,8 @@ DEVERR_BAD_BLOCK_ID = 0x2
 DEVERR_BAD_PAGE_ID = 0x4
 
 # Every symbol include/gqa_attn.h declares.
-EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_sparse_blocks",
+EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_noalloc",
+            "gqa_attn_sparse_blocks",
             "gqa_workspace_bytes", "gqa_set_workspace", "gqa_get_device_error",
             "gqa_status_string")
 
@@ -63,6 +64,9 @@ def load():
             lib.gqa_attn_prefill.restype = I
             lib.gqa_attn_paged_e4m3.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
             lib.gqa_attn_paged_e4m3.restype = I
+            lib.gqa_attn_paged_e4m3_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                        F, P, P]
+            lib.gqa_attn_paged_e4m3_noalloc.restype = I
             lib.gqa_attn_sparse_blocks.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                                    P, P]
             lib.gqa_attn_sparse_blocks.restype = I

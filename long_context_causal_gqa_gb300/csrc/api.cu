@@ -148,6 +148,26 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
                              query_rows, scale, out, stream);
 }
 
+int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                                const float* kscale, const float* vscale,
+                                const int32_t* block_table, int num_pages, int page, int ctx_len,
+                                int query_rows, int Hq, int Hkv, int D, float scale, void* out,
+                                struct CUstream_st* stream) {
+    if (!q || !kcache || !vcache || !kscale || !vscale || !block_table || !out)
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale) |
+         reinterpret_cast<uintptr_t>(block_table)) & 3u)
+        return GQA_ERR_INVALID_ARG;
+    if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
+    return paged_e4m3_noalloc_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages,
+                                     ctx_len, query_rows, scale, out, stream);
+}
+
 int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
                            const int32_t* block_table, const int32_t* sel_idx,
                            const int32_t* sel_cnt, int max_sel, int num_pages, int page,

@@ -58,6 +58,12 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
                       cudaStream_t stream);
 size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms);
 
+// Same as paged_e4m3_launch, with the split partials in a static device array.
+int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                              const float* kscale, const float* vscale,
+                              const int32_t* block_table, int num_pages, int ctx_len, int R,
+                              float scale, void* out, cudaStream_t stream);
+
 int sparse_launch(const void* q, const void* kcache, const void* vcache,
                   const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
                   int max_sel, int num_pages, int ctx_len, int rows, float scale, void* out,

@@ -693,3 +693,82 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
 }
 
 }  // namespace gqa
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the paged E4M3 tail.  It runs the same kernels
+// but keeps the split partials in a file-scope device array instead of the
+// caller-registered workspace, for callers that cannot allocate device memory.
+#include <mutex>
+
+namespace gqa {
+namespace paged {
+
+constexpr int kNoAllocMaxSplits = 160;
+constexpr int kNoAllocMaxRows = 8 * HQ;  // query_rows <= 8
+constexpr size_t kNoAllocFloats = (size_t)kNoAllocMaxSplits * kNoAllocMaxRows * (D + 2);
+
+// Split partials (O, then (m, l)) of gqa_attn_paged_e4m3_noalloc: about
+// 7.9 MB of module-scope device memory that every device loading the library
+// holds until the process exits.  Host code must not use this name as a
+// device pointer; the address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_partials[kNoAllocFloats];
+
+}  // namespace paged
+
+size_t paged_e4m3_noalloc_capacity_floats() { return paged::kNoAllocFloats; }
+
+int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                              const float* kscale, const float* vscale,
+                              const int32_t* block_table, int num_pages, int ctx_len, int R,
+                              float scale, void* out, cudaStream_t stream) {
+    using namespace paged;
+    const DeviceInfo* di = device_info();
+    if (!di) return GQA_ERR_CUDA;
+    // Device address of the array, looked up once per device while that
+    // device is current (the first call on a device does this).
+    static float* s_addr[64] = {nullptr};
+    static std::mutex s_mu;
+    if (di->device >= 64) return GQA_ERR_CUDA;
+    float* scratch;
+    {
+        std::lock_guard<std::mutex> lk(s_mu);
+        if (!s_addr[di->device]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p)
+                return GQA_ERR_CUDA;
+            s_addr[di->device] = static_cast<float*>(p);
+        }
+        scratch = s_addr[di->device];
+    }
+    Params P;
+    P.kcache = kcache;
+    P.vcache = vcache;
+    P.kscale = kscale;
+    P.vscale = vscale;
+    P.table = block_table;
+    P.q = static_cast<const __half*>(q);
+    P.num_pages = num_pages;
+    P.ctx_len = ctx_len;
+    P.R = R;
+    P.nq = R * HQ;
+    P.n_tiles = (ctx_len + TILE - 1) / TILE;
+    P.G = P.n_tiles < di->num_sms ? P.n_tiles : di->num_sms;
+    if (P.G > kNoAllocMaxSplits) P.G = kNoAllocMaxSplits;
+    P.scale = scale;
+    P.out = static_cast<__half*>(out);
+    P.err = di->err_word;
+    if (P.nq > kNoAllocMaxRows || (size_t)P.G * P.nq * (D + 2) > kNoAllocFloats)
+        return GQA_ERR_WORKSPACE;
+    P.ws_o = scratch;
+    P.ws_ml = scratch + (size_t)P.G * P.nq * D;
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)num_pages * PAGE;
+    if (!make_map_2d_u8(&tk, kcache, rows, D, PAGE, 128) ||
+        !make_map_2d_u8(&tv, vcache, rows, D, PAGE, 128))
+        return GQA_ERR_CUDA;
+    if (P.nq <= 16) return launch_np<16>(tk, tv, P, stream, di->device);
+    if (P.nq <= 32) return launch_np<32>(tk, tv, P, stream, di->device);
+    return launch_np<48>(tk, tv, P, stream, di->device);
+}
+
+}  // namespace gqa
