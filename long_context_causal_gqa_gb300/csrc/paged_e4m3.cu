@@ -11,26 +11,34 @@
 // * Split-KV: the context is cut into 128-key tiles (8 pages) and the tiles
 //   into one contiguous range per SM.  Each split writes an (O, m, l) partial;
 //   a merge kernel combines them in split order (exact log-sum-exp merge).
-// * Swap-AB UMMA: keys are the M=128 dimension, the packed query rows the N
-//   dimension (padded to NP = 16/32/48), so few rows waste no tensor work.
-//     S^T[128 keys x NP] = K[128 x 256] . Q^T          (A = K in tensor memory)
-//     O^T[256 d x NP]   += V^T[256 x 128] . P^T[128 x NP] (two M=128 halves)
-// * E4M3 -> fp16 is pure bit work: fp16 bits = sign << 15 | (b & 0x7F) << 7
-//   equals the E4M3 value times 2^-8 for every finite code (normal and
-//   subnormal), so the 2^8 is folded into the K and V scales.  K is decoded by
-//   the thread that owns its TMEM lane and stored as the UMMA A operand; V is
-//   decoded into a 128B-swizzled fp16 smem tile.  Raw pages arrive by TMA
-//   tensor copies (128-byte swizzle, so every thread reads its own key's row
-//   without bank conflicts) through a 3-stage ring.
+// * Swap-AB UMMA on the FP8 tensor cores (kind::f8f6f4, K = 32 per
+//   instruction): keys are the M=128 dimension, the packed query rows the N
+//   dimension (NP = 16/32/48).  K and V enter as the raw E4M3 bytes the TMA
+//   brought in, so nothing is decoded:
+//     S^T[128 keys x 3NP] = K[128 x 256] . [Q1 | Q2 | Q3]^T        (K-major A)
+//     O^T[128 d x 3NP]   += V^T[128 d x 128 keys] . [P1 | P2 | P3]^T
+//                           (MN-major A, one UMMA chain per half of d)
+//   Q and P are fp16 / fp32 quantities; each enters as a three-term E4M3
+//   expansion x ~= t1 + t2 / 16 + t3 / 256 (each term the E4M3 rounding of
+//   the scaled remainder), which carries at least fp16's 11 significant bits,
+//   so S = S1 + S2 / 16 + S3 / 256 and likewise O.  Q uses one scale per
+//   packed row (its absmax maps to 256); P <= 256 by the lazy rescale below.
+//   K's and V's fp32 scales are applied to S and to the merged output.
+// * Raw pages arrive by TMA tensor copies (128-byte swizzle, two 128-byte
+//   halves of d per page) through a ring of 32 KB stages (K0, V0, K1, V1,
+//   ...); a stage is released by the commit of the UMMAs that read it.  With
+//   up to 32 packed rows S^T is double-buffered in tensor memory; at 48 the
+//   three-term S^T and O^T leave room for one S^T buffer, which the softmax
+//   releases as soon as it has read it.
 // * Softmax over keys runs across TMEM lanes.  A per-row reference max moves
 //   only when a score exceeds it by more than 8 (log2 units); the common case
-//   is one threshold compare and a CTA-wide vote per tile, and the exact
+//   is one threshold compare and a warpgroup vote per tile, and the exact
 //   cross-lane max is taken only on the first tile or when the vote fires.
 //   Row sums stay per thread until the split's end.
 //
-// Warp roles (320 threads): 0 bulk-copy producer, 1 TMEM owner + UMMA issuer,
-// 2..5 "key" warps (K decode, softmax, epilogue; thread = TMEM lane),
-// 6..9 V decode warps.
+// Warp roles (320 threads): 0 TMA producer, 1 TMEM owner + UMMA issuer,
+// 2..9 softmax warps (two warpgroups, each owning half of the packed query
+// rows; thread = TMEM lane = key).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,9 +58,8 @@ constexpr int TILE = 128;        // keys per tile
 constexpr int PAGES_PER_TILE = TILE / PAGE;
 constexpr int PAGE_BYTES = PAGE * D;            // 4096 (Hkv = 1, one byte per element)
 constexpr int RAW_STAGE = TILE * D;             // 32 KB of E4M3 per K or V tile
-constexpr int NRAW = 3;
-constexpr int V_BYTES = TILE * D * 2;           // fp16 V tile, 64 KB
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 320;   // 10 warps: producer, UMMA, 8 softmax
+constexpr int NKEY = 256;       // softmax threads (two warpgroups)
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Params {
@@ -64,7 +71,7 @@ struct Params {
     const __half* q;
     int num_pages, ctx_len, R, nq, n_tiles, G;
     float scale;
-    float* ws_o;    // [G][nq][D] unnormalised partial O (in units of the fp16 V)
+    float* ws_o;    // [G][nq][D] unnormalised partial O (in units of the E4M3 V)
     float* ws_ml;   // [G][nq][2]  (m in log2 units, l)
     __half* out;
     unsigned* err;
@@ -72,47 +79,81 @@ struct Params {
 
 template <int NP>
 struct Layout {
-    static constexpr int Q_BYTES = NP * D * 2;       // 4 chunks [NP][64] fp16
-    static constexpr int PT_BYTES = NP * TILE * 2;   // 2 chunks [NP][64 keys] fp16
-    static constexpr int OFF_V = 0;
-    static constexpr int OFF_RAW = OFF_V + V_BYTES;
+    static constexpr int NT = 3;                      // E4M3 expansion terms
+    static constexpr int N3 = NT * NP;                // UMMA N
+    static constexpr int NS = (NP <= 32) ? 2 : 1;     // S^T buffers in tensor memory
+    static constexpr int NRAW = (NP <= 32) ? 5 : 4;   // raw K/V stages
+    static constexpr int Q_BYTES = N3 * D;            // [Q1|Q2|Q3]: N3 rows x 256 B, 2 halves
+    static constexpr int PT_BYTES = N3 * TILE;        // [P1|P2|P3]^T: N3 rows x 128 keys
+    static constexpr int OFF_RAW = 0;
     static constexpr int OFF_Q = OFF_RAW + NRAW * RAW_STAGE;
     static constexpr int OFF_PT = OFF_Q + Q_BYTES;
-    static constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;       // [4][NP] floats
-    static constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;        // [NP] floats
+    static constexpr int OFF_QS = OFF_PT + 2 * PT_BYTES;        // [NP] per-row Q scales
+    static constexpr int OFF_RED = OFF_QS + NP * 4;             // [8 warps][NP] floats
+    static constexpr int OFF_MREF = OFF_RED + 8 * NP * 4;        // [NP] floats
     static constexpr int OFF_FAC = OFF_MREF + NP * 4;            // [NP] floats
-    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;            // [2][4] ints
-    static constexpr int OFF_BAR = (OFF_FLAG + 32 + 7) & ~7;
-    static constexpr int NUM_BARS = 2 * NRAW + 12;
+    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;            // [2][8] ints
+    static constexpr int OFF_BAR = (OFF_FLAG + 64 + 7) & ~7;
+    static constexpr int NUM_BARS = 24;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_TMEM + 16;
     static constexpr int SMEM = BYTES + 1024;
     // TMEM columns
-    static constexpr uint32_t K_COL = 0;             // 2 x 128 (fp16 pairs)
-    static constexpr uint32_t S_COL = 256;           // 2 x NP
-    static constexpr uint32_t O_COL = 256 + 2 * NP;  // 2 halves x NP
+    static constexpr uint32_t S_COL = 0;              // NS buffers x N3  (S1 | S2 | S3)
+    static constexpr uint32_t O_COL = NS * N3;        // 2 halves of d x N3 (O1 | O2 | O3)
+    static_assert(O_COL + 2 * N3 <= 512, "tensor memory");
+    static_assert(SMEM <= 232448, "shared memory");
 };
 
 // mbarrier indices
+constexpr int MAX_RAW = 5;
 enum {
-    B_RAW_FULL = 0,          // [NRAW]
-    B_RAW_EMPTY = NRAW,      // [NRAW]
-    B_K_READY = 2 * NRAW,    // [2]
-    B_S_FULL = 2 * NRAW + 2, // [2]
-    B_P_READY = 2 * NRAW + 4,// [2]
-    B_PT_EMPTY = 2 * NRAW + 6, // [2] PV of that P^T buffer done
-    B_V_READY = 2 * NRAW + 8,
-    B_V_EMPTY = 2 * NRAW + 9,
-    B_DRAIN = 2 * NRAW + 10,
-    B_GROUP = 2 * NRAW + 11,  // key-thread group barrier
+    B_RAW_FULL = 0,               // [MAX_RAW]
+    B_RAW_EMPTY = MAX_RAW,        // [MAX_RAW]
+    B_S_FULL = 2 * MAX_RAW,       // [2]
+    B_P_READY = 2 * MAX_RAW + 2,  // [2]
+    B_PT_EMPTY = 2 * MAX_RAW + 4, // [2] P.V of that P^T buffer done
+    B_DRAIN = 2 * MAX_RAW + 6,
+    B_GROUP = 2 * MAX_RAW + 7,    // [2] per softmax warpgroup
+    B_S_FREE = 2 * MAX_RAW + 9,   // single S^T buffer read by the softmax
 };
 
-// 4 E4M3 bytes -> 4 fp16 (value * 2^-8) as two half2 words.
-__device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
-    const uint32_t a = __byte_perm(x, 0u, 0x1404);  // [0, b0, 0, b1]
-    const uint32_t b = __byte_perm(x, 0u, 0x3424);  // [0, b2, 0, b3]
-    lo = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
-    hi = (b & 0x80008000u) | ((b >> 1) & 0x3F803F80u);
+// FP8 UMMA: D (+)= A . B with E4M3 operands from shared memory, f32 accumulator.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two floats -> two E4M3 bytes (round to nearest even, saturating), low byte = a.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+// Value of an E4M3 byte pair (low byte first) as two floats.
+__device__ __forceinline__ void e4m3x2_val(uint32_t v, float& a, float& b) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
+    const __half2 hh = *reinterpret_cast<const __half2*>(&h2);
+    a = __low2float(hh);
+    b = __high2float(hh);
+}
+// x ~= t1 + t2 / 16 + t3 / 256 with t1, t2, t3 E4M3, for two values at once
+// (each result holds the pair's two bytes in its low 16 bits).
+__device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& t1, uint32_t& t2,
+                                              uint32_t& t3) {
+    float a0, a1;
+    t1 = e4m3x2(x0, x1);
+    e4m3x2_val(t1, a0, a1);
+    const float r0 = (x0 - a0) * 16.f, r1 = (x1 - a1) * 16.f;
+    t2 = e4m3x2(r0, r1);
+    e4m3x2_val(t2, a0, a1);
+    t3 = e4m3x2((r0 - a0) * 16.f, (r1 - a1) * 16.f);
 }
 
 // Byte offset of 16-byte unit u (0..7) of row r inside a 128B-swizzled block.
@@ -127,9 +168,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Barrier among the 128 key threads built on an mbarrier (count 128), so that
-// it shares the bounded, abort-aware wait of the pipeline barriers: a thread
-// that gave up elsewhere cannot leave the others blocked here forever.
+// Barrier among the 128 threads of one softmax warpgroup, built on an mbarrier
+// so that it shares the bounded, abort-aware wait of the pipeline barriers: a
+// thread that gave up elsewhere cannot leave the others blocked here forever.
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* abort,
                                            unsigned* err) {
     mbar_arrive(bar);
@@ -138,21 +179,58 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volati
     return ok;
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                   "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+// N consecutive columns (N = 8, 16 or 24) of this thread's TMEM lane.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t* r) {
+    if constexpr (N >= 16) {
+        tmem_ld16(taddr, r);
+        if constexpr (N == 24) tmem_ld8(taddr + 16, r + 16);
+    } else {
+        tmem_ld8(taddr, r);
+    }
+}
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t* r) {
+    if constexpr (N >= 16) {
+        tmem_st16(taddr, r);
+        if constexpr (N == 24) tmem_st8(taddr + 16, r + 16);
+    } else {
+        tmem_st8(taddr, r);
+    }
+}
+
 template <int NP>
 __global__ void __launch_bounds__(NTHREADS, 1)
 paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params P) {
     using L = Layout<NP>;
-    constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
-    constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
+    constexpr int NH = NP / 2;   // packed query rows per softmax warpgroup
+    constexpr int N3 = L::N3;    // UMMA N: three expansion terms
+    constexpr int NS = L::NS;
+    constexpr int NRAW = L::NRAW;
+    // E4M3 x E4M3 -> f32 (format fields 0 = E4M3 for kind::f8f6f4).
+    constexpr uint32_t IDESC_QK = idesc_f16_f32(128, N3, false, false);
+    constexpr uint32_t IDESC_PV = idesc_f16_f32(128, N3, true, false);   // A = V^T, MN-major
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (sbase - smem_u32(smem_raw));
-    const uint32_t s_v = sbase + L::OFF_V;
     const uint32_t s_raw = sbase + L::OFF_RAW;
     const uint32_t s_q = sbase + L::OFF_Q;
     const uint32_t s_pt = sbase + L::OFF_PT;
+    float* qs = reinterpret_cast<float*>(gbase + L::OFF_QS);
     float* red = reinterpret_cast<float*>(gbase + L::OFF_RED);
     float* mref = reinterpret_cast<float*>(gbase + L::OFF_MREF);
     float* fac = reinterpret_cast<float*>(gbase + L::OFF_FAC);
@@ -170,32 +248,61 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int ntl = t_end - t_begin;
     const int n_logical = (P.ctx_len + PAGE - 1) / PAGE;
 
-    // ---- set-up: barriers, Q -> smem (swizzled, zero padding rows), TMEM
     if (threadIdx.x == 0) {
         for (int s = 0; s < NRAW; ++s) {
             mbar_init(bar(B_RAW_FULL + s), 1);
-            mbar_init(bar(B_RAW_EMPTY + s), 128);
+            mbar_init(bar(B_RAW_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_K_READY + b), 128);
             mbar_init(bar(B_S_FULL + b), 1);
-            mbar_init(bar(B_P_READY + b), 128);
+            mbar_init(bar(B_P_READY + b), NKEY);
             mbar_init(bar(B_PT_EMPTY + b), 1);
+            mbar_init(bar(B_GROUP + b), 128);
         }
-        mbar_init(bar(B_V_READY), 128);
-        mbar_init(bar(B_V_EMPTY), 1);
+        mbar_init(bar(B_S_FREE), NKEY);
         mbar_init(bar(B_DRAIN), 1);
-        mbar_init(bar(B_GROUP), 128);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int u = threadIdx.x; u < NP * (D / 8); u += NTHREADS) {
-        const int r = u / (D / 8);          // packed query row
-        const int c16 = u % (D / 8);        // 16-byte unit along d
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < P.nq) val = *reinterpret_cast<const uint4*>(P.q + (size_t)r * D + c16 * 8);
-        const uint32_t dst = s_q + (c16 / 8) * (NP * 128) + sw128(r, c16 % 8);
-        *reinterpret_cast<uint4*>(gbase + L::OFF_Q + (dst - s_q)) = val;
+    // ---- Q -> three-term E4M3 expansion [Q1 | Q2 | Q3] in shared memory
+    // (K-major, 3NP rows of 256 bytes in two 128-byte halves, 128B-swizzled),
+    // one scale per packed row: x / qs ~= t1 + t2 / 16 + t3 / 256, |x / qs| <= 256.
+    for (int r = warp; r < NP; r += NTHREADS / 32) {
+        const int d0 = lane * 8;
+        float x[8];
+        if (r < P.nq) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(P.q + (size_t)r * D + d0);
+            const __half* h = reinterpret_cast<const __half*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __half2float(h[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = amax > 0.f ? amax / 256.0f : 1.0f;
+        const float inv = 1.0f / sc;
+        uint32_t w1[2] = {0, 0}, w2[2] = {0, 0}, w3[2] = {0, 0};
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            uint32_t b1, b2, b3;
+            split3_e4m3x2(x[e] * inv, x[e + 1] * inv, b1, b2, b3);
+            w1[e >> 2] |= b1 << (8 * (e & 3));
+            w2[e >> 2] |= b2 << (8 * (e & 3));
+            w3[e >> 2] |= b3 << (8 * (e & 3));
+        }
+        const int h = d0 >> 7, cin = d0 & 127;
+        uint8_t* qh = gbase + L::OFF_Q + h * (N3 * 128);
+        *reinterpret_cast<uint2*>(qh + sw128(r, cin >> 4) + (cin & 15)) = make_uint2(w1[0], w1[1]);
+        *reinterpret_cast<uint2*>(qh + sw128(NP + r, cin >> 4) + (cin & 15)) =
+            make_uint2(w2[0], w2[1]);
+        *reinterpret_cast<uint2*>(qh + sw128(2 * NP + r, cin >> 4) + (cin & 15)) =
+            make_uint2(w3[0], w3[1]);
+        if (lane == 0) qs[r] = sc;
     }
     for (int c = threadIdx.x; c < NP; c += NTHREADS) mref[c] = -INFINITY;
     if (warp == 1) {
@@ -261,42 +368,56 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0 && ntl > 0) {
             bool ok = true;
+            auto stage_of = [](int item) { return item % NRAW; };
+            auto phase_of = [](int item) { return (uint32_t)((item / NRAW) & 1); };
             auto issue_pv = [&](int x) -> bool {
                 if (!mbar_wait(bar(B_P_READY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
                     return false;
-                if (!mbar_wait(bar(B_V_READY), x & 1, abort_flag, P.err)) return false;
+                const int vi = 2 * x + 1;
+                if (!mbar_wait(bar(B_RAW_FULL + stage_of(vi)), phase_of(vi), abort_flag, P.err))
+                    return false;
                 tc_fence_after();
+                const uint32_t vst = s_raw + stage_of(vi) * RAW_STAGE;
                 const uint32_t pt = s_pt + (x & 1) * L::PT_BYTES;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                    for (int ks = 0; ks < TILE / 16; ++ks) {
-                        const uint64_t a = sdesc_sw128(s_v + (2 * h) * (TILE * 128) + ks * 2048,
-                                                       TILE * 128, 1024);
-                        const uint64_t b =
-                            sdesc_sw128(pt + (ks / 4) * (NP * 128) + (ks % 4) * 32, 16, 1024);
-                        umma_ss(tmem + L::O_COL + h * NP, a, b, IDESC_PV, (x > 0 || ks > 0));
+                    for (int ks = 0; ks < TILE / 32; ++ks) {
+                        // V^T half h: M = 128 d (one 128-byte atom), K = 32 keys (rows)
+                        const uint64_t a = sdesc_sw128(vst + h * (TILE * 128) + ks * 4096, 16384, 1024);
+                        const uint64_t b = sdesc_sw128(pt + ks * 32, 16, 1024);
+                        umma_f8(tmem + L::O_COL + h * N3, a, b, IDESC_PV, (x > 0 || ks > 0));
                     }
                 }
                 umma_commit(bar(B_PT_EMPTY + (x & 1)));
-                umma_commit(bar(B_V_EMPTY));
+                umma_commit(bar(B_RAW_EMPTY + stage_of(vi)));
                 return true;
             };
             for (int jj = 0; jj < ntl && ok; ++jj) {
-                const int b = jj & 1;
-                if (!mbar_wait(bar(B_K_READY + b), (jj >> 1) & 1, abort_flag, P.err)) {
+                const int b = jj % NS;
+                const int ki = 2 * jj;
+                if (!mbar_wait(bar(B_RAW_FULL + stage_of(ki)), phase_of(ki), abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
+                if (NS == 1 && jj > 0) {
+                    // The single S^T buffer: the softmax must have read tile jj - 1.
+                    if (!mbar_wait(bar(B_S_FREE), (uint32_t)((jj - 1) & 1), abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 tc_fence_after();
+                const uint32_t kst = s_raw + stage_of(ki) * RAW_STAGE;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t bq =
-                        sdesc_sw128(s_q + (kk / 4) * (NP * 128) + (kk % 4) * 32, 16, 1024);
-                    umma_ts(tmem + L::S_COL + b * NP, tmem + L::K_COL + b * 128 + kk * 8, bq,
-                            IDESC_QK, kk > 0);
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    const int h = kk >> 2;   // d half
+                    const uint64_t a = sdesc_sw128(kst + h * (TILE * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bq = sdesc_sw128(s_q + h * (N3 * 128) + (kk & 3) * 32, 16, 1024);
+                    umma_f8(tmem + L::S_COL + b * N3, a, bq, IDESC_QK, kk > 0);
                 }
                 umma_commit(bar(B_S_FULL + b));
+                umma_commit(bar(B_RAW_EMPTY + stage_of(ki)));
                 if (jj >= 1) ok = issue_pv(jj - 1);
             }
             if (ok) ok = issue_pv(ntl - 1);
@@ -305,109 +426,89 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 drain_wait(bar(B_DRAIN), 0);
             }
         }
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ key warps
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        // Warpgroup hg owns packed query rows (S^T / O^T columns) hg*NH .. hg*NH+NH-1;
+        // its lazy-rescale state is per column, so the two warpgroups never talk.
+        const int hg = (warp - 2) >> 2;
         const int wq = warp & 3;
+        const int wi = (warp - 2) & 3;                      // warp within the warpgroup
         const int k = wq * 32 + lane;                       // TMEM lane = key in tile = d in O^T half
+        const int c0 = hg * NH;
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        const float sl2 = P.scale * kscale * 256.0f * 1.4426950408889634f;
         const int lim_base = P.ctx_len - P.R;               // row r sees keys <= lim_base + r
-        float lpart[NP];
-#pragma unroll
-        for (int c = 0; c < NP; ++c) lpart[c] = 0.f;
-        uint32_t raw_item = 0;
+        const uint32_t gbar = bar(B_GROUP + hg);
         uint32_t gphase = 0;
+        float sl2[NH];
+#pragma unroll
+        for (int c = 0; c < NH; ++c) sl2[c] = P.scale * kscale * qs[c0 + c] * 1.4426950408889634f;
+        float lpart[NH];
+#pragma unroll
+        for (int c = 0; c < NH; ++c) lpart[c] = 0.f;
         bool ok = ntl > 0;
-
-        // Decode tile jj's K (raw stage) into TMEM K buffer jj & 1.
-        auto decode_k = [&](int jj) -> bool {
-            const int s = raw_item % NRAW;
-            const uint32_t ph = (raw_item / NRAW) & 1u;
-            if (!mbar_wait(bar(B_RAW_FULL + s), ph, abort_flag, P.err)) return false;
-            const int key = (t_begin + jj) * TILE + k;
-            const bool live = key / PAGE < n_logical;   // page loaded (else stale smem)
-            const uint8_t* src = gbase + L::OFF_RAW + s * RAW_STAGE + k * 128;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t w[64];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint4 x = make_uint4(0, 0, 0, 0);
-                    if (live)
-                        x = *reinterpret_cast<const uint4*>(src + half * (TILE * 128) +
-                                                            ((i ^ (k & 7)) << 4));
-                    e4m3x4_to_f16(x.x, w[8 * i + 0], w[8 * i + 1]);
-                    e4m3x4_to_f16(x.y, w[8 * i + 2], w[8 * i + 3]);
-                    e4m3x4_to_f16(x.z, w[8 * i + 4], w[8 * i + 5]);
-                    e4m3x4_to_f16(x.w, w[8 * i + 6], w[8 * i + 7]);
-                }
-                tmem_st32(t_lane + L::K_COL + (jj & 1) * 128 + half * 64, w);
-                tmem_st32(t_lane + L::K_COL + (jj & 1) * 128 + half * 64 + 32, w + 32);
-            }
-            tmem_st_wait();
-            mbar_arrive(bar(B_RAW_EMPTY + s));
-            raw_item += 2;  // skip the V stage of this tile
-            tc_fence_before();
-            mbar_arrive(bar(B_K_READY + (jj & 1)));
-            return true;
-        };
-
-        if (ok) ok = decode_k(0);
         for (int jj = 0; jj < ntl && ok; ++jj) {
-            if (jj + 1 < ntl) {
-                ok = decode_k(jj + 1);
-                if (!ok) break;
-            }
-            const int b = jj & 1;
-            ok = mbar_wait(bar(B_S_FULL + b), (jj >> 1) & 1, abort_flag, P.err);
+            const int b = jj & 1;            // P^T buffer
+            const int sb = jj % NS;          // S^T buffer
+            ok = mbar_wait(bar(B_S_FULL + sb), (uint32_t)((jj / NS) & 1), abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float s[NP];
+            float s[NH];
             {
-                uint32_t r[NP];
+                uint32_t r1[NH], r2[NH], r3[NH];
+                tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + c0, r1);
+                tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + NP + c0, r2);
+                tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + 2 * NP + c0, r3);
+                tmem_ld_wait<NH>(r1);
+                tmem_ld_wait<NH>(r2);
+                tmem_ld_wait<NH>(r3);
+                if (NS == 1) {
+                    // S^T is in registers: the next Q.K^T may overwrite it.
+                    tc_fence_before();
+                    mbar_arrive(bar(B_S_FREE));
+                }
 #pragma unroll
-                for (int c = 0; c < NP; c += 16) tmem_ld16(t_lane + L::S_COL + b * NP + c, r + c);
-                tmem_ld_wait<NP>(r);
-#pragma unroll
-                for (int c = 0; c < NP; ++c) s[c] = __uint_as_float(r[c]) * sl2;
+                for (int c = 0; c < NH; ++c)
+                    s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
+                                fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c]))) *
+                           sl2[c];
             }
             const int key = (t_begin + jj) * TILE + k;
             if ((t_begin + jj) * TILE + TILE - 1 > lim_base) {
 #pragma unroll
-                for (int c = 0; c < NP; ++c) {
-                    const int r = c / HQ;
-                    const bool vis = (c < P.nq) ? (key <= lim_base + r) : (key < P.ctx_len);
+                for (int c = 0; c < NH; ++c) {
+                    const int cg = c0 + c;
+                    const bool vis = (cg < P.nq) ? (key <= lim_base + cg / HQ) : (key < P.ctx_len);
                     if (!vis) s[c] = -INFINITY;
                 }
             }
             // Vote: does any score exceed its row's reference max by > threshold?
             bool exceed = false;
 #pragma unroll
-            for (int c = 0; c < NP; ++c) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
+            for (int c = 0; c < NH; ++c) exceed |= s[c] > mref[c0 + c] + RESCALE_THRESHOLD;
             const unsigned vote = __ballot_sync(0xffffffffu, exceed);
-            volatile int* fl = flags + (jj & 1) * 4;
-            if (lane == 0) fl[wq] = vote != 0;
-            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+            volatile int* fl = flags + (jj & 1) * 8 + hg * 4;
+            if (lane == 0) fl[wi] = vote != 0;
+            ok = group_sync(gbar, gphase, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const bool any = fl[0] | fl[1] | fl[2] | fl[3];
             if (any) {
                 // Exact column max over the 128 keys of this tile.
 #pragma unroll
-                for (int c = 0; c < NP; ++c) {
+                for (int c = 0; c < NH; ++c) {
                     float m = s[c];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if (lane == 0) red[wq * NP + c] = m;
+                    if (lane == 0) red[(hg * 4 + wi) * NP + c0 + c] = m;
                 }
-                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                ok = group_sync(gbar, gphase, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (k < NP) {
-                    const int c = k;
-                    const float tmax = fmaxf(fmaxf(red[c], red[NP + c]),
-                                             fmaxf(red[2 * NP + c], red[3 * NP + c]));
+                if (k < NH) {
+                    const int c = c0 + k;
+                    const float* rr = red + (hg * 4) * NP + c;
+                    const float tmax = fmaxf(fmaxf(rr[0], rr[NP]), fmaxf(rr[2 * NP], rr[3 * NP]));
                     const float old = mref[c];
                     float f = 1.0f;
                     if (tmax > old + RESCALE_THRESHOLD) {
@@ -416,7 +517,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     }
                     fac[c] = f;
                 }
-                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                ok = group_sync(gbar, gphase, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if (jj > 0) {
@@ -427,38 +528,61 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t r[NP];
+                    for (int g6 = 0; g6 < 6; ++g6) {   // (d half, expansion term)
+                        const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * NP + c0;
+                        uint32_t r[NH];
+                        tmem_ldn<NH>(t_lane + col, r);
+                        tmem_ld_wait<NH>(r);
 #pragma unroll
-                        for (int c = 0; c < NP; c += 16)
-                            tmem_ld16(t_lane + L::O_COL + h * NP + c, r + c);
-                        tmem_ld_wait<NP>(r);
-#pragma unroll
-                        for (int c = 0; c < NP; ++c)
-                            r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c]);
-#pragma unroll
-                        for (int c = 0; c < NP; c += 16)
-                            tmem_st16(t_lane + L::O_COL + h * NP + c, r + c);
+                        for (int c = 0; c < NH; ++c)
+                            r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c0 + c]);
+                        tmem_stn<NH>(t_lane + col, r);
                     }
                     tmem_st_wait();
                 }
 #pragma unroll
-                for (int c = 0; c < NP; ++c) lpart[c] *= fac[c];
+                for (int c = 0; c < NH; ++c) lpart[c] *= fac[c0 + c];
+            }
+            // Keys past the context in the last tile (the rest of the last page,
+            // or pages never loaded) hold whatever the cache or shared memory
+            // held, possibly the E4M3 NaN code; zero their V rows so that
+            // P = 0 times V stays 0.  Warpgroup hg clears half hg of d.
+            if (t_begin + jj == P.n_tiles - 1 && (P.ctx_len & (TILE - 1)) != 0) {
+                const int vi = 2 * jj + 1;
+                ok = mbar_wait(bar(B_RAW_FULL + vi % NRAW), (uint32_t)((vi / NRAW) & 1), abort_flag,
+                               P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (key >= P.ctx_len) {
+                    uint4* row = reinterpret_cast<uint4*>(gbase + L::OFF_RAW + (vi % NRAW) * RAW_STAGE +
+                                                          hg * (TILE * 128) + k * 128);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
+                }
             }
             // P^T buffer b is free once the P.V two tiles back has completed.
             ok = mbar_wait(bar(B_PT_EMPTY + b), ((jj >> 1) & 1) ^ 1, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
-            const int kc = k >> 6;          // 64-key chunk
-            const int kin = k & 63;
+            {
+                // [P1 | P2 | P3]^T, K-major: row = term * NP + packed row, byte = key.
+                uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
 #pragma unroll
-            for (int c = 0; c < NP; ++c) {
-                const float m = mref[c];
-                const float p = ex2(s[c] - (m == -INFINITY ? 0.f : m));
-                lpart[c] += p;
-                const uint32_t off = kc * (NP * 128) + sw128(c, kin >> 3) + (kin & 7) * 2;
-                *reinterpret_cast<__half*>(pt + off) = __float2half_rn(p);
+                for (int c = 0; c < NH; c += 2) {
+                    const float m0 = mref[c0 + c], m1 = mref[c0 + c + 1];
+                    const float p0 = ex2(s[c] - (m0 == -INFINITY ? 0.f : m0));
+                    const float p1 = ex2(s[c + 1] - (m1 == -INFINITY ? 0.f : m1));
+                    lpart[c] += p0;
+                    lpart[c + 1] += p1;
+                    uint32_t t[3];
+                    split3_e4m3x2(p0, p1, t[0], t[1], t[2]);
+                    const int r0 = c0 + c;
+#pragma unroll
+                    for (int e = 0; e < 3; ++e) {
+                        pt[sw128(e * NP + r0, k >> 4) + (k & 15)] = (uint8_t)(t[e] & 0xFF);
+                        pt[sw128(e * NP + r0 + 1, k >> 4) + (k & 15)] = (uint8_t)(t[e] >> 8);
+                    }
+                }
             }
             fence_async_shared();
             mbar_arrive(bar(B_P_READY + b));
@@ -473,77 +597,40 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             tc_fence_after();
             // Row sums: reduce the per-thread partial sums over the 128 keys.
 #pragma unroll
-            for (int c = 0; c < NP; ++c) {
+            for (int c = 0; c < NH; ++c) {
                 float v = lpart[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) red[wq * NP + c] = v;
+                if (lane == 0) red[(hg * 4 + wi) * NP + c0 + c] = v;
             }
-            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+            ok = group_sync(gbar, gphase, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok && ntl > 0) {
-            if (k < P.nq) {
-                const int c = k;
-                const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
+            if (k < NH && c0 + k < P.nq) {
+                const int c = c0 + k;
+                const float* rr = red + (hg * 4) * NP + c;
+                const float l = (rr[0] + rr[NP]) + (rr[2 * NP] + rr[3 * NP]);
                 P.ws_ml[((size_t)split * P.nq + c) * 2 + 0] = mref[c];
                 P.ws_ml[((size_t)split * P.nq + c) * 2 + 1] = l;
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                uint32_t r[NP];
-#pragma unroll
-                for (int c = 0; c < NP; c += 16) tmem_ld16(t_lane + L::O_COL + h * NP + c, r + c);
-                tmem_ld_wait<NP>(r);
+                uint32_t r1[NH], r2[NH], r3[NH];
+                tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + c0, r1);
+                tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + NP + c0, r2);
+                tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + 2 * NP + c0, r3);
+                tmem_ld_wait<NH>(r1);
+                tmem_ld_wait<NH>(r2);
+                tmem_ld_wait<NH>(r3);
                 const int d = h * 128 + k;
 #pragma unroll
-                for (int c = 0; c < NP; ++c)
-                    if (c < P.nq) P.ws_o[((size_t)split * P.nq + c) * D + d] = __uint_as_float(r[c]);
+                for (int c = 0; c < NH; ++c)
+                    if (c0 + c < P.nq)
+                        P.ws_o[((size_t)split * P.nq + c0 + c) * D + d] =
+                            fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
+                                 fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c])));
             }
-        }
-    } else {
-        // ------------------------------------------------------------ V decode warps
-        const int t = threadIdx.x - 192;                 // 0..127
-        uint32_t raw_item = 1;                           // V stages are the odd items
-        bool ok = ntl > 0;
-        for (int jj = 0; jj < ntl && ok; ++jj) {
-            const int s = raw_item % NRAW;
-            const uint32_t ph = (raw_item / NRAW) & 1u;
-            ok = mbar_wait(bar(B_RAW_FULL + s), ph, abort_flag, P.err);
-            if (!ok) break;
-            ok = mbar_wait(bar(B_V_EMPTY), (jj & 1) ^ 1, abort_flag, P.err);
-            if (!ok) break;
-            const uint8_t* src = gbase + L::OFF_RAW + s * RAW_STAGE;
-            const int tile_key0 = (t_begin + jj) * TILE;
-            // 128 keys x 16 raw units of 16 bytes (16 d each); thread t handles
-            // units t, t + 128, ...; 8 consecutive threads read one key's half row.
-#pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-                const int unit = i * 128 + t;
-                const int key = unit >> 4;        // 0..127
-                const int u = unit & 15;          // d = 16u .. 16u + 15
-                const int h = u >> 3;
-                uint4 x = make_uint4(0, 0, 0, 0);
-                if ((tile_key0 + key) / PAGE < n_logical)
-                    x = *reinterpret_cast<const uint4*>(src + h * (TILE * 128) + key * 128 +
-                                                        (((u & 7) ^ (key & 7)) << 4));
-                uint32_t w[8];
-                e4m3x4_to_f16(x.x, w[0], w[1]);
-                e4m3x4_to_f16(x.y, w[2], w[3]);
-                e4m3x4_to_f16(x.z, w[4], w[5]);
-                e4m3x4_to_f16(x.w, w[6], w[7]);
-                // fp16 tile: chunk u / 4 (64 d), 16-byte units 2(u%4), 2(u%4)+1
-                const int chunk = u >> 2;
-                const int uu = (u & 3) * 2;
-                uint8_t* dst = gbase + L::OFF_V + chunk * (TILE * 128);
-                *reinterpret_cast<uint4*>(dst + sw128(key, uu)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4*>(dst + sw128(key, uu + 1)) =
-                    make_uint4(w[4], w[5], w[6], w[7]);
-            }
-            fence_async_shared();
-            mbar_arrive(bar(B_RAW_EMPTY + s));
-            mbar_arrive(bar(B_V_READY));
-            raw_item += 2;
         }
     }
 
@@ -555,7 +642,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
 }
 
-// out[c, d] = vscale * 256 * sum_s w_s O_s[c, d] / sum_s w_s l_s, w_s = 2^(m_s - M).
+// out[c, d] = vscale * sum_s w_s O_s[c, d] / sum_s w_s l_s, w_s = 2^(m_s - M).
 // Block (c, dg) merges packed row c for d = 32 dg .. 32 dg + 31.  The split
 // weights are computed once per block in shared memory; warp w then sums the
 // splits s = w, w + 8, ... for its lane's d, and the eight warp sums are added
@@ -617,7 +704,7 @@ __global__ void __launch_bounds__(256) paged_merge_kernel(const Params P) {
 #pragma unroll
         for (int w = 0; w < 8; ++w) a += red[w][lane];
         const float L = stat[1];
-        const float vs = *P.vscale * 256.0f;
+        const float vs = *P.vscale;
         P.out[(size_t)c * D + d] = __float2half_rn(L > 0.f ? a / L * vs : 0.f);
     }
 }
