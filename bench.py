@@ -165,11 +165,19 @@ def time_steps(fn, steps, warmup, flush, stream):
 
 
 def make_flush(device):
+    """L2 flush run before every timed step: write a 256 MB buffer (twice the
+    L2), then read a second 256 MB buffer.  The read replaces the write's dirty
+    lines, so their write-back happens here rather than inside the timed
+    kernel, and L2 holds neither the step's inputs nor its previous outputs."""
     import torch
-    buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    n = 256 * 1024 * 1024 // 4
+    buf = torch.empty(n, dtype=torch.float32, device=device)
+    buf2 = torch.ones(n, dtype=torch.float32, device=device)
+    sink = torch.empty((), dtype=torch.float32, device=device)
 
     def flush():
         buf.fill_(1.0)
+        torch.sum(buf2, dim=0, out=sink)
     return flush
 
 
@@ -329,7 +337,7 @@ def run_gpu(args):
         "data": "synthetic: seeded i.i.d. N(0,1) fp16 q/k/v",
         "config": {"workload": f"dense causal GQA prefill Q={Q} KV={KV} Hq=6 Hkv=1 D=256 "
                                "scale=1/16 batch 1", "Q": Q, "KV": KV,
-                   "l2": "flushed (256 MB write) before every timed step",
+                   "l2": "flushed before every timed step (256 MB write, then 256 MB read of a second buffer)",
                    "parallelism": f"{world} independent problem(s), one per GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),

@@ -10,7 +10,8 @@
 //
 // * Split-KV: the context is cut into 128-key tiles (8 pages) and the tiles
 //   into one contiguous range per SM.  Each split writes an (O, m, l) partial;
-//   a merge kernel combines them in split order (exact log-sum-exp merge).
+//   a merge kernel, launched as a programmatic dependent so that its launch
+//   overlaps this kernel's tail, combines them (exact log-sum-exp merge).
 // * Swap-AB UMMA on the FP8 tensor cores (kind::f8f6f4, K = 32 per
 //   instruction): keys are the M=128 dimension, the packed query rows the N
 //   dimension (NP = 16/32/48).  K and V enter as the raw E4M3 bytes the TMA
@@ -25,8 +26,12 @@
 //   packed row (its absmax maps to 256); P <= 256 by the lazy rescale below.
 //   K's and V's fp32 scales are applied to S and to the merged output.
 // * Raw pages arrive by TMA tensor copies (128-byte swizzle, two 128-byte
-//   halves of d per page) through a ring of 32 KB stages (K0, V0, K1, V1,
-//   ...); a stage is released by the commit of the UMMAs that read it.  With
+//   halves of d per page) through a ring of 32 KB stages (K0, K1, V0, K2,
+//   V1, ...: each V one tile behind its K, so that it arrives when its P is
+//   ready); a stage is released by the commit of the UMMAs that read it.  The
+//   ring is as deep as shared memory allows (6 stages for 16 packed rows):
+//   under full load DRAM latency is several microseconds, and the bytes in
+//   flight per SM set the bandwidth.  With
 //   up to 32 packed rows S^T is double-buffered in tensor memory; at 48 the
 //   three-term S^T and O^T leave room for one S^T buffer, which the softmax
 //   releases as soon as it has read it.
@@ -58,8 +63,9 @@ constexpr int TILE = 128;        // keys per tile
 constexpr int PAGES_PER_TILE = TILE / PAGE;
 constexpr int PAGE_BYTES = PAGE * D;            // 4096 (Hkv = 1, one byte per element)
 constexpr int RAW_STAGE = TILE * D;             // 32 KB of E4M3 per K or V tile
-constexpr int NTHREADS = 320;   // 10 warps: producer, UMMA, 8 softmax
-constexpr int NKEY = 256;       // softmax threads (two warpgroups)
+// Threads of a CTA with NWG softmax warpgroups: producer warp, UMMA warp,
+// then 4 * NWG softmax warps.
+__host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Params {
@@ -77,24 +83,24 @@ struct Params {
     unsigned* err;
 };
 
-template <int NP>
+template <int NP, int NWG>
 struct Layout {
     static constexpr int NT = 3;                      // E4M3 expansion terms
     static constexpr int N3 = NT * NP;                // UMMA N
     static constexpr int NS = (NP <= 32) ? 2 : 1;     // S^T buffers in tensor memory
-    static constexpr int NRAW = (NP <= 32) ? 5 : 4;   // raw K/V stages
+    static constexpr int NRAW = (NP <= 16) ? 6 : (NP <= 32) ? 5 : 4;   // raw K/V stages
     static constexpr int Q_BYTES = N3 * D;            // [Q1|Q2|Q3]: N3 rows x 256 B, 2 halves
     static constexpr int PT_BYTES = N3 * TILE;        // [P1|P2|P3]^T: N3 rows x 128 keys
     static constexpr int OFF_RAW = 0;
     static constexpr int OFF_Q = OFF_RAW + NRAW * RAW_STAGE;
     static constexpr int OFF_PT = OFF_Q + Q_BYTES;
     static constexpr int OFF_QS = OFF_PT + 2 * PT_BYTES;        // [NP] per-row Q scales
-    static constexpr int OFF_RED = OFF_QS + NP * 4;             // [8 warps][NP] floats
-    static constexpr int OFF_MREF = OFF_RED + 8 * NP * 4;        // [NP] floats
+    static constexpr int OFF_RED = OFF_QS + NP * 4;             // [4 NWG warps][NP] floats
+    static constexpr int OFF_MREF = OFF_RED + 4 * NWG * NP * 4;  // [NP] floats
     static constexpr int OFF_FAC = OFF_MREF + NP * 4;            // [NP] floats
-    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;            // [2][8] ints
-    static constexpr int OFF_BAR = (OFF_FLAG + 64 + 7) & ~7;
-    static constexpr int NUM_BARS = 24;
+    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;            // [2][4 NWG] ints
+    static constexpr int OFF_BAR = (OFF_FLAG + 2 * 4 * NWG * 4 + 7) & ~7;
+    static constexpr int NUM_BARS = 32;   // >= NUM_BARRIERS
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_TMEM + 16;
     static constexpr int SMEM = BYTES + 1024;
@@ -106,7 +112,8 @@ struct Layout {
 };
 
 // mbarrier indices
-constexpr int MAX_RAW = 5;
+constexpr int MAX_RAW = 6;
+constexpr int MAX_WG = 6;
 enum {
     B_RAW_FULL = 0,               // [MAX_RAW]
     B_RAW_EMPTY = MAX_RAW,        // [MAX_RAW]
@@ -114,9 +121,19 @@ enum {
     B_P_READY = 2 * MAX_RAW + 2,  // [2]
     B_PT_EMPTY = 2 * MAX_RAW + 4, // [2] P.V of that P^T buffer done
     B_DRAIN = 2 * MAX_RAW + 6,
-    B_GROUP = 2 * MAX_RAW + 7,    // [2] per softmax warpgroup
-    B_S_FREE = 2 * MAX_RAW + 9,   // single S^T buffer read by the softmax
+    B_GROUP = 2 * MAX_RAW + 7,    // [MAX_WG] per softmax warpgroup
+    B_S_FREE = 2 * MAX_RAW + 7 + MAX_WG,  // single S^T buffer read by the softmax
+    NUM_BARRIERS = B_S_FREE + 1,
 };
+
+static_assert(NUM_BARRIERS <= 32, "mbarrier slots");
+
+// Copy order through the raw ring: K0, then K(j), V(j - 1) for j = 1 .. n - 1,
+// then V(n - 1).  V(j) is requested one tile after K(j), so that it lands
+// about when P(j) is ready instead of holding a stage while the softmax of
+// tile j runs.
+__device__ __forceinline__ int item_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int item_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
 // FP8 UMMA: D (+)= A . B with E4M3 operands from shared memory, f32 accumulator.
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -191,32 +208,53 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
                    "r"(r[6]), "r"(r[7])
                  : "memory");
 }
-// N consecutive columns (N = 8, 16 or 24) of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+// N consecutive columns (N a multiple of 4, at most 32) of this thread's TMEM lane.
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t* r) {
+    static_assert(N % 4 == 0 && N > 0 && N <= 32, "column count");
     if constexpr (N >= 16) {
         tmem_ld16(taddr, r);
-        if constexpr (N == 24) tmem_ld8(taddr + 16, r + 16);
-    } else {
+        if constexpr (N > 16) tmem_ldn<N - 16>(taddr + 16, r + 16);
+    } else if constexpr (N >= 8) {
         tmem_ld8(taddr, r);
+        if constexpr (N > 8) tmem_ldn<N - 8>(taddr + 8, r + 8);
+    } else {
+        tmem_ld4(taddr, r);
     }
 }
 template <int N>
 __device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t* r) {
+    static_assert(N % 4 == 0 && N > 0 && N <= 32, "column count");
     if constexpr (N >= 16) {
         tmem_st16(taddr, r);
-        if constexpr (N == 24) tmem_st8(taddr + 16, r + 16);
-    } else {
+        if constexpr (N > 16) tmem_stn<N - 16>(taddr + 16, r + 16);
+    } else if constexpr (N >= 8) {
         tmem_st8(taddr, r);
+        if constexpr (N > 8) tmem_stn<N - 8>(taddr + 8, r + 8);
+    } else {
+        tmem_st4(taddr, r);
     }
 }
 
-template <int NP>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int NP, int NWG>
+__global__ void __launch_bounds__(threads_for(NWG), 1)
 paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params P) {
-    using L = Layout<NP>;
-    constexpr int NH = NP / 2;   // packed query rows per softmax warpgroup
+    using L = Layout<NP, NWG>;
+    constexpr int NTHREADS = threads_for(NWG);
+    constexpr int NKEY = 128 * NWG;   // softmax threads
+    constexpr int NH = NP / NWG;      // packed query rows per softmax warpgroup
+    static_assert(NP % NWG == 0 && NWG <= MAX_WG, "softmax split");
     constexpr int N3 = L::N3;    // UMMA N: three expansion terms
     constexpr int NS = L::NS;
     constexpr int NRAW = L::NRAW;
@@ -257,381 +295,422 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_READY + b), NKEY);
             mbar_init(bar(B_PT_EMPTY + b), 1);
-            mbar_init(bar(B_GROUP + b), 128);
         }
+        for (int g = 0; g < NWG; ++g) mbar_init(bar(B_GROUP + g), 128);
         mbar_init(bar(B_S_FREE), NKEY);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // ---- Q -> three-term E4M3 expansion [Q1 | Q2 | Q3] in shared memory
-    // (K-major, 3NP rows of 256 bytes in two 128-byte halves, 128B-swizzled),
-    // one scale per packed row: x / qs ~= t1 + t2 / 16 + t3 / 256, |x / qs| <= 256.
-    for (int r = warp; r < NP; r += NTHREADS / 32) {
-        const int d0 = lane * 8;
-        float x[8];
-        if (r < P.nq) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(P.q + (size_t)r * D + d0);
-            const __half* h = reinterpret_cast<const __half*>(&raw);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __half2float(h[e]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float sc = amax > 0.f ? amax / 256.0f : 1.0f;
-        const float inv = 1.0f / sc;
-        uint32_t w1[2] = {0, 0}, w2[2] = {0, 0}, w3[2] = {0, 0};
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            uint32_t b1, b2, b3;
-            split3_e4m3x2(x[e] * inv, x[e + 1] * inv, b1, b2, b3);
-            w1[e >> 2] |= b1 << (8 * (e & 3));
-            w2[e >> 2] |= b2 << (8 * (e & 3));
-            w3[e >> 2] |= b3 << (8 * (e & 3));
-        }
-        const int h = d0 >> 7, cin = d0 & 127;
-        uint8_t* qh = gbase + L::OFF_Q + h * (N3 * 128);
-        *reinterpret_cast<uint2*>(qh + sw128(r, cin >> 4) + (cin & 15)) = make_uint2(w1[0], w1[1]);
-        *reinterpret_cast<uint2*>(qh + sw128(NP + r, cin >> 4) + (cin & 15)) =
-            make_uint2(w2[0], w2[1]);
-        *reinterpret_cast<uint2*>(qh + sw128(2 * NP + r, cin >> 4) + (cin & 15)) =
-            make_uint2(w3[0], w3[1]);
-        if (lane == 0) qs[r] = sc;
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
     }
-    for (int c = threadIdx.x; c < NP; c += NTHREADS) mref[c] = -INFINITY;
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_ptr), 512);
-        tmem_relinquish();
-    }
-    fence_async_shared();
-    tc_fence_before();
+    // Barriers are initialised: the producer starts streaming at once, while
+    // warps 1..9 build the Q operand and allocate tensor memory.
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_ptr;
-    const float kscale = *P.kscale;
+    // The merge kernel may be scheduled now; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;");
+    uint32_t tmem = 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && ntl > 0) {
+        // Block-table entries arrive a chunk of four tiles (32 pages, one per
+        // lane) ahead of their use, so their latency stays off the copy
+        // stream; lane 2p + h issues the copy of page p, half h of d.
+        if (ntl > 0) {
+            const int pg_end = min(t_end * PAGES_PER_TILE, n_logical);
+            auto load_chunk = [&](int k) -> int {
+                const int pg = (t_begin + 4 * k) * PAGES_PER_TILE + lane;
+                return pg < pg_end ? __ldg(P.table + pg) : 0;
+            };
+            int cur = load_chunk(0);
+            int nxt = load_chunk(1);
+            const int pp = lane >> 1, hh = lane & 1;
             uint32_t item = 0;
             bool ok = true;
-            for (int jj = 0; jj < ntl && ok; ++jj) {
-                const int tile = t_begin + jj;
-                const int p0 = tile * PAGES_PER_TILE;
-                int phys[PAGES_PER_TILE];
-                int npg = 0;
-#pragma unroll
-                for (int p = 0; p < PAGES_PER_TILE; ++p) {
-                    int id = 0;
-                    if (p0 + p < n_logical) {
-                        id = __ldg(P.table + p0 + p);
-                        if (id < 0 || id >= P.num_pages) {
-                            atomicOr(P.err, kErrBadPageId);
-                            id = 0;
-                        }
-                        npg = p + 1;
-                    }
-                    phys[p] = id;
+            int id_prev = 0, npg_prev = 0;
+            auto issue = [&](const CUtensorMap* tm, int id, int npg) -> bool {
+                const int s = item % NRAW;
+                const uint32_t ph = (item / NRAW) & 1u;
+                int okw = 1;
+                if (lane == 0) {
+                    okw = mbar_wait(bar(B_RAW_EMPTY + s), ph ^ 1u, abort_flag, P.err);
+                    if (okw) mbar_arrive_expect_tx(bar(B_RAW_FULL + s), npg * PAGE_BYTES);
                 }
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int s = item % NRAW;
-                    const uint32_t ph = (item / NRAW) & 1u;
-                    if (!mbar_wait(bar(B_RAW_EMPTY + s), ph ^ 1u, abort_flag, P.err)) {
-                        ok = false;
-                        break;
+                if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
+                // Stage layout: [2 halves of d][128 keys][128 B], 128B-swizzled.
+                if (lane < 2 * npg)
+                    tma_load_2d(s_raw + s * RAW_STAGE + hh * (TILE * 128) + pp * (PAGE * 128), tm,
+                                bar(B_RAW_FULL + s), hh * 128, id * PAGE);
+                ++item;
+                return true;
+            };
+            for (int jj = 0; jj <= ntl && ok; ++jj) {
+                int id = 0, npg = 0;
+                if (jj < ntl) {
+                    const int sub = jj & 3;
+                    if (sub == 0 && jj > 0) {
+                        cur = nxt;
+                        nxt = load_chunk((jj >> 2) + 1);
                     }
-                    const CUtensorMap* tm = kv == 0 ? &tm_k : &tm_v;
-                    mbar_arrive_expect_tx(bar(B_RAW_FULL + s), npg * PAGE_BYTES);
-                    // Stage layout: [2 halves of d][128 keys][128 B], 128B-swizzled.
-                    for (int p = 0; p < npg; ++p)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_2d(s_raw + s * RAW_STAGE + h * (TILE * 128) + p * (PAGE * 128),
-                                        tm, bar(B_RAW_FULL + s), h * 128, phys[p] * PAGE);
-                    ++item;
+                    const int tile = t_begin + jj;
+                    npg = min(PAGES_PER_TILE, n_logical - tile * PAGES_PER_TILE);
+                    id = __shfl_sync(0xffffffffu, cur, sub * PAGES_PER_TILE + pp);
+                    if (lane < 2 * npg && (id < 0 || id >= P.num_pages)) {
+                        atomicOr(P.err, kErrBadPageId);
+                        id = 0;
+                    }
+                    ok = issue(&tm_k, id, npg);
                 }
+                if (ok && jj >= 1) ok = issue(&tm_v, id_prev, npg_prev);
+                id_prev = id;
+                npg_prev = npg;
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 for (int s = 0; s < NRAW; ++s) {
                     const uint32_t fills = item > (uint32_t)s ? (item - s + NRAW - 1) / NRAW : 0;
                     if (fills) drain_wait(bar(B_RAW_FULL + s), (fills - 1) & 1u);
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ UMMA issuer
-        if (lane == 0 && ntl > 0) {
-            bool ok = true;
-            auto stage_of = [](int item) { return item % NRAW; };
-            auto phase_of = [](int item) { return (uint32_t)((item / NRAW) & 1); };
-            auto issue_pv = [&](int x) -> bool {
-                if (!mbar_wait(bar(B_P_READY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
-                    return false;
-                const int vi = 2 * x + 1;
-                if (!mbar_wait(bar(B_RAW_FULL + stage_of(vi)), phase_of(vi), abort_flag, P.err))
-                    return false;
-                tc_fence_after();
-                const uint32_t vst = s_raw + stage_of(vi) * RAW_STAGE;
-                const uint32_t pt = s_pt + (x & 1) * L::PT_BYTES;
+    } else {
+        // ---- Q -> three-term E4M3 expansion [Q1 | Q2 | Q3] in shared memory
+        // (K-major, 3NP rows of 256 bytes in two 128-byte halves, 128B-swizzled),
+        // one scale per packed row: x / qs ~= t1 + t2 / 16 + t3 / 256, |x / qs| <= 256.
+        // Warps 1..9 take rows r = warp - 1, warp + 8, ...; all their loads are
+        // issued before the first conversion.
+        const float kscale = *P.kscale;
+        {
+            constexpr int QW = NTHREADS / 32 - 1;
+            constexpr int RPW = (NP + QW - 1) / QW;
+            const int d0 = lane * 8;
+            uint4 raw[RPW];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+            for (int i = 0; i < RPW; ++i) {
+                const int r = warp - 1 + QW * i;
+                raw[i] = (r < P.nq) ? *reinterpret_cast<const uint4*>(P.q + (size_t)r * D + d0)
+                                    : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-                    for (int ks = 0; ks < TILE / 32; ++ks) {
-                        // V^T half h: M = 128 d (one 128-byte atom), K = 32 keys (rows)
-                        const uint64_t a = sdesc_sw128(vst + h * (TILE * 128) + ks * 4096, 16384, 1024);
-                        const uint64_t b = sdesc_sw128(pt + ks * 32, 16, 1024);
-                        umma_f8(tmem + L::O_COL + h * N3, a, b, IDESC_PV, (x > 0 || ks > 0));
+            for (int i = 0; i < RPW; ++i) {
+                const int r = warp - 1 + QW * i;
+                if (r >= NP) break;
+                float x[8];
+                const __half* hx = reinterpret_cast<const __half*>(&raw[i]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __half2float(hx[e]);
+                float amax = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float sc = amax > 0.f ? amax / 256.0f : 1.0f;
+                const float inv = 1.0f / sc;
+                uint32_t w1[2] = {0, 0}, w2[2] = {0, 0}, w3[2] = {0, 0};
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    uint32_t b1, b2, b3;
+                    split3_e4m3x2(x[e] * inv, x[e + 1] * inv, b1, b2, b3);
+                    w1[e >> 2] |= b1 << (8 * (e & 3));
+                    w2[e >> 2] |= b2 << (8 * (e & 3));
+                    w3[e >> 2] |= b3 << (8 * (e & 3));
+                }
+                const int h = d0 >> 7, cin = d0 & 127;
+                uint8_t* qh = gbase + L::OFF_Q + h * (N3 * 128);
+                *reinterpret_cast<uint2*>(qh + sw128(r, cin >> 4) + (cin & 15)) =
+                    make_uint2(w1[0], w1[1]);
+                *reinterpret_cast<uint2*>(qh + sw128(NP + r, cin >> 4) + (cin & 15)) =
+                    make_uint2(w2[0], w2[1]);
+                *reinterpret_cast<uint2*>(qh + sw128(2 * NP + r, cin >> 4) + (cin & 15)) =
+                    make_uint2(w3[0], w3[1]);
+                if (lane == 0) qs[r] = sc;
+            }
+        }
+        for (int c = threadIdx.x - 32; c < NP; c += NTHREADS - 32) mref[c] = -INFINITY;
+        if (warp == 1) {
+            tmem_alloc(smem_u32(tmem_ptr), 512);
+            tmem_relinquish();
+        }
+        fence_async_shared();
+        tc_fence_before();
+        // Warps 1..9 only (the producer is already streaming); every one of them
+        // reaches this barrier unconditionally.
+        asm volatile("bar.sync 1, %0;" ::"r"(NTHREADS - 32) : "memory");
+        tc_fence_after();
+        tmem = *tmem_ptr;
+        if (warp == 1) {
+            // ------------------------------------------------------------ UMMA issuer
+            if (lane == 0 && ntl > 0) {
+                bool ok = true;
+                auto stage_of = [](int item) { return item % NRAW; };
+                auto phase_of = [](int item) { return (uint32_t)((item / NRAW) & 1); };
+                auto issue_pv = [&](int x) -> bool {
+                    if (!mbar_wait(bar(B_P_READY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
+                        return false;
+                    const int vi = item_v(x, ntl);
+                    if (!mbar_wait(bar(B_RAW_FULL + stage_of(vi)), phase_of(vi), abort_flag, P.err))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t vst = s_raw + stage_of(vi) * RAW_STAGE;
+                    const uint32_t pt = s_pt + (x & 1) * L::PT_BYTES;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int ks = 0; ks < TILE / 32; ++ks) {
+                            // V^T half h: M = 128 d (one 128-byte atom), K = 32 keys (rows)
+                            const uint64_t a = sdesc_sw128(vst + h * (TILE * 128) + ks * 4096, 16384, 1024);
+                            const uint64_t b = sdesc_sw128(pt + ks * 32, 16, 1024);
+                            umma_f8(tmem + L::O_COL + h * N3, a, b, IDESC_PV, (x > 0 || ks > 0));
+                        }
                     }
-                }
-                umma_commit(bar(B_PT_EMPTY + (x & 1)));
-                umma_commit(bar(B_RAW_EMPTY + stage_of(vi)));
-                return true;
-            };
-            for (int jj = 0; jj < ntl && ok; ++jj) {
-                const int b = jj % NS;
-                const int ki = 2 * jj;
-                if (!mbar_wait(bar(B_RAW_FULL + stage_of(ki)), phase_of(ki), abort_flag, P.err)) {
-                    ok = false;
-                    break;
-                }
-                if (NS == 1 && jj > 0) {
-                    // The single S^T buffer: the softmax must have read tile jj - 1.
-                    if (!mbar_wait(bar(B_S_FREE), (uint32_t)((jj - 1) & 1), abort_flag, P.err)) {
+                    umma_commit(bar(B_PT_EMPTY + (x & 1)));
+                    umma_commit(bar(B_RAW_EMPTY + stage_of(vi)));
+                    return true;
+                };
+                for (int jj = 0; jj < ntl && ok; ++jj) {
+                    const int b = jj % NS;
+                    const int ki = item_k(jj);
+                    if (!mbar_wait(bar(B_RAW_FULL + stage_of(ki)), phase_of(ki), abort_flag, P.err)) {
                         ok = false;
                         break;
                     }
-                }
-                tc_fence_after();
-                const uint32_t kst = s_raw + stage_of(ki) * RAW_STAGE;
-#pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    const int h = kk >> 2;   // d half
-                    const uint64_t a = sdesc_sw128(kst + h * (TILE * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bq = sdesc_sw128(s_q + h * (N3 * 128) + (kk & 3) * 32, 16, 1024);
-                    umma_f8(tmem + L::S_COL + b * N3, a, bq, IDESC_QK, kk > 0);
-                }
-                umma_commit(bar(B_S_FULL + b));
-                umma_commit(bar(B_RAW_EMPTY + stage_of(ki)));
-                if (jj >= 1) ok = issue_pv(jj - 1);
-            }
-            if (ok) ok = issue_pv(ntl - 1);
-            if (!ok) {
-                umma_commit(bar(B_DRAIN));
-                drain_wait(bar(B_DRAIN), 0);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ softmax warpgroups
-        // Warpgroup hg owns packed query rows (S^T / O^T columns) hg*NH .. hg*NH+NH-1;
-        // its lazy-rescale state is per column, so the two warpgroups never talk.
-        const int hg = (warp - 2) >> 2;
-        const int wq = warp & 3;
-        const int wi = (warp - 2) & 3;                      // warp within the warpgroup
-        const int k = wq * 32 + lane;                       // TMEM lane = key in tile = d in O^T half
-        const int c0 = hg * NH;
-        const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        const int lim_base = P.ctx_len - P.R;               // row r sees keys <= lim_base + r
-        const uint32_t gbar = bar(B_GROUP + hg);
-        uint32_t gphase = 0;
-        float sl2[NH];
-#pragma unroll
-        for (int c = 0; c < NH; ++c) sl2[c] = P.scale * kscale * qs[c0 + c] * 1.4426950408889634f;
-        float lpart[NH];
-#pragma unroll
-        for (int c = 0; c < NH; ++c) lpart[c] = 0.f;
-        bool ok = ntl > 0;
-        for (int jj = 0; jj < ntl && ok; ++jj) {
-            const int b = jj & 1;            // P^T buffer
-            const int sb = jj % NS;          // S^T buffer
-            ok = mbar_wait(bar(B_S_FULL + sb), (uint32_t)((jj / NS) & 1), abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            float s[NH];
-            {
-                uint32_t r1[NH], r2[NH], r3[NH];
-                tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + c0, r1);
-                tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + NP + c0, r2);
-                tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + 2 * NP + c0, r3);
-                tmem_ld_wait<NH>(r1);
-                tmem_ld_wait<NH>(r2);
-                tmem_ld_wait<NH>(r3);
-                if (NS == 1) {
-                    // S^T is in registers: the next Q.K^T may overwrite it.
-                    tc_fence_before();
-                    mbar_arrive(bar(B_S_FREE));
-                }
-#pragma unroll
-                for (int c = 0; c < NH; ++c)
-                    s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
-                                fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c]))) *
-                           sl2[c];
-            }
-            const int key = (t_begin + jj) * TILE + k;
-            if ((t_begin + jj) * TILE + TILE - 1 > lim_base) {
-#pragma unroll
-                for (int c = 0; c < NH; ++c) {
-                    const int cg = c0 + c;
-                    const bool vis = (cg < P.nq) ? (key <= lim_base + cg / HQ) : (key < P.ctx_len);
-                    if (!vis) s[c] = -INFINITY;
-                }
-            }
-            // Vote: does any score exceed its row's reference max by > threshold?
-            bool exceed = false;
-#pragma unroll
-            for (int c = 0; c < NH; ++c) exceed |= s[c] > mref[c0 + c] + RESCALE_THRESHOLD;
-            const unsigned vote = __ballot_sync(0xffffffffu, exceed);
-            volatile int* fl = flags + (jj & 1) * 8 + hg * 4;
-            if (lane == 0) fl[wi] = vote != 0;
-            ok = group_sync(gbar, gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const bool any = fl[0] | fl[1] | fl[2] | fl[3];
-            if (any) {
-                // Exact column max over the 128 keys of this tile.
-#pragma unroll
-                for (int c = 0; c < NH; ++c) {
-                    float m = s[c];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if (lane == 0) red[(hg * 4 + wi) * NP + c0 + c] = m;
-                }
-                ok = group_sync(gbar, gphase, abort_flag, P.err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                if (k < NH) {
-                    const int c = c0 + k;
-                    const float* rr = red + (hg * 4) * NP + c;
-                    const float tmax = fmaxf(fmaxf(rr[0], rr[NP]), fmaxf(rr[2 * NP], rr[3 * NP]));
-                    const float old = mref[c];
-                    float f = 1.0f;
-                    if (tmax > old + RESCALE_THRESHOLD) {
-                        f = (old == -INFINITY) ? 0.f : ex2(old - tmax);
-                        mref[c] = tmax;
+                    if (NS == 1 && jj > 0) {
+                        // The single S^T buffer: the softmax must have read tile jj - 1.
+                        if (!mbar_wait(bar(B_S_FREE), (uint32_t)((jj - 1) & 1), abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    fac[c] = f;
+                    tc_fence_after();
+                    const uint32_t kst = s_raw + stage_of(ki) * RAW_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const int h = kk >> 2;   // d half
+                        const uint64_t a = sdesc_sw128(kst + h * (TILE * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bq = sdesc_sw128(s_q + h * (N3 * 128) + (kk & 3) * 32, 16, 1024);
+                        umma_f8(tmem + L::S_COL + b * N3, a, bq, IDESC_QK, kk > 0);
+                    }
+                    umma_commit(bar(B_S_FULL + b));
+                    umma_commit(bar(B_RAW_EMPTY + stage_of(ki)));
+                    if (jj >= 1) ok = issue_pv(jj - 1);
                 }
+                if (ok) ok = issue_pv(ntl - 1);
+                if (!ok) {
+                    umma_commit(bar(B_DRAIN));
+                    drain_wait(bar(B_DRAIN), 0);
+                }
+            }
+        } else {
+            // ------------------------------------------------------------ softmax warpgroups
+            // Warpgroup hg owns packed query rows (S^T / O^T columns) hg*NH .. hg*NH+NH-1;
+            // its lazy-rescale state is per column, so the two warpgroups never talk.
+            const int hg = (warp - 2) >> 2;
+            const int wq = warp & 3;
+            const int wi = (warp - 2) & 3;                      // warp within the warpgroup
+            const int k = wq * 32 + lane;                       // TMEM lane = key in tile = d in O^T half
+            const int c0 = hg * NH;
+            const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+            const int lim_base = P.ctx_len - P.R;               // row r sees keys <= lim_base + r
+            const uint32_t gbar = bar(B_GROUP + hg);
+            uint32_t gphase = 0;
+            float sl2[NH];
+#pragma unroll
+            for (int c = 0; c < NH; ++c) sl2[c] = P.scale * kscale * qs[c0 + c] * 1.4426950408889634f;
+            float lpart[NH];
+#pragma unroll
+            for (int c = 0; c < NH; ++c) lpart[c] = 0.f;
+            bool ok = ntl > 0;
+            for (int jj = 0; jj < ntl && ok; ++jj) {
+                const int b = jj & 1;            // P^T buffer
+                const int sb = jj % NS;          // S^T buffer
+                ok = mbar_wait(bar(B_S_FULL + sb), (uint32_t)((jj / NS) & 1), abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                float s[NH];
+                {
+                    uint32_t r1[NH], r2[NH], r3[NH];
+                    tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + c0, r1);
+                    tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + NP + c0, r2);
+                    tmem_ldn<NH>(t_lane + L::S_COL + sb * N3 + 2 * NP + c0, r3);
+                    tmem_ld_wait<NH>(r1);
+                    tmem_ld_wait<NH>(r2);
+                    tmem_ld_wait<NH>(r3);
+                    if (NS == 1) {
+                        // S^T is in registers: the next Q.K^T may overwrite it.
+                        tc_fence_before();
+                        mbar_arrive(bar(B_S_FREE));
+                    }
+#pragma unroll
+                    for (int c = 0; c < NH; ++c)
+                        s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
+                                    fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c]))) *
+                               sl2[c];
+                }
+                const int key = (t_begin + jj) * TILE + k;
+                if ((t_begin + jj) * TILE + TILE - 1 > lim_base) {
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) {
+                        const int cg = c0 + c;
+                        const bool vis = (cg < P.nq) ? (key <= lim_base + cg / HQ) : (key < P.ctx_len);
+                        if (!vis) s[c] = -INFINITY;
+                    }
+                }
+                // Vote: does any score exceed its row's reference max by > threshold?
+                bool exceed = false;
+#pragma unroll
+                for (int c = 0; c < NH; ++c) exceed |= s[c] > mref[c0 + c] + RESCALE_THRESHOLD;
+                const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                volatile int* fl = flags + (jj & 1) * (4 * NWG) + hg * 4;
+                if (lane == 0) fl[wi] = vote != 0;
                 ok = group_sync(gbar, gphase, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (jj > 0) {
-                    // O^T must hold every earlier P.V before it is rescaled.
-                    const int x = jj - 1;
-                    ok = mbar_wait(bar(B_PT_EMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                const bool any = fl[0] | fl[1] | fl[2] | fl[3];
+                if (any) {
+                    // Exact column max over the 128 keys of this tile.
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) {
+                        float m = s[c];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (lane == 0) red[(hg * 4 + wi) * NP + c0 + c] = m;
+                    }
+                    ok = group_sync(gbar, gphase, abort_flag, P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int g6 = 0; g6 < 6; ++g6) {   // (d half, expansion term)
-                        const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * NP + c0;
-                        uint32_t r[NH];
-                        tmem_ldn<NH>(t_lane + col, r);
-                        tmem_ld_wait<NH>(r);
-#pragma unroll
-                        for (int c = 0; c < NH; ++c)
-                            r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c0 + c]);
-                        tmem_stn<NH>(t_lane + col, r);
+                    if (k < NH) {
+                        const int c = c0 + k;
+                        const float* rr = red + (hg * 4) * NP + c;
+                        const float tmax = fmaxf(fmaxf(rr[0], rr[NP]), fmaxf(rr[2 * NP], rr[3 * NP]));
+                        const float old = mref[c];
+                        float f = 1.0f;
+                        if (tmax > old + RESCALE_THRESHOLD) {
+                            f = (old == -INFINITY) ? 0.f : ex2(old - tmax);
+                            mref[c] = tmax;
+                        }
+                        fac[c] = f;
                     }
-                    tmem_st_wait();
-                }
+                    ok = group_sync(gbar, gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (jj > 0) {
+                        // O^T must hold every earlier P.V before it is rescaled.
+                        const int x = jj - 1;
+                        ok = mbar_wait(bar(B_PT_EMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < NH; ++c) lpart[c] *= fac[c0 + c];
-            }
-            // Keys past the context in the last tile (the rest of the last page,
-            // or pages never loaded) hold whatever the cache or shared memory
-            // held, possibly the E4M3 NaN code; zero their V rows so that
-            // P = 0 times V stays 0.  Warpgroup hg clears half hg of d.
-            if (t_begin + jj == P.n_tiles - 1 && (P.ctx_len & (TILE - 1)) != 0) {
-                const int vi = 2 * jj + 1;
-                ok = mbar_wait(bar(B_RAW_FULL + vi % NRAW), (uint32_t)((vi / NRAW) & 1), abort_flag,
-                               P.err);
+                        for (int g6 = 0; g6 < 6; ++g6) {   // (d half, expansion term)
+                            const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * NP + c0;
+                            uint32_t r[NH];
+                            tmem_ldn<NH>(t_lane + col, r);
+                            tmem_ld_wait<NH>(r);
+#pragma unroll
+                            for (int c = 0; c < NH; ++c)
+                                r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c0 + c]);
+                            tmem_stn<NH>(t_lane + col, r);
+                        }
+                        tmem_st_wait();
+                    }
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) lpart[c] *= fac[c0 + c];
+                }
+                // Keys past the context in the last tile (the rest of the last page,
+                // or pages never loaded) hold whatever the cache or shared memory
+                // held, possibly the E4M3 NaN code; zero their V rows so that
+                // P = 0 times V stays 0.  Each warpgroup clears its share of the
+                // row's sixteen 16-byte units (both halves of d).
+                if (t_begin + jj == P.n_tiles - 1 && (P.ctx_len & (TILE - 1)) != 0) {
+                    const int vi = item_v(jj, ntl);
+                    ok = mbar_wait(bar(B_RAW_FULL + vi % NRAW), (uint32_t)((vi / NRAW) & 1), abort_flag,
+                                   P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (key >= P.ctx_len) {
+                        uint8_t* st = gbase + L::OFF_RAW + (vi % NRAW) * RAW_STAGE + k * 128;
+                        for (int u = hg * 16 / NWG; u < (hg + 1) * 16 / NWG; ++u)
+                            *reinterpret_cast<uint4*>(st + (u >> 3) * (TILE * 128) + (u & 7) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                    }
+                }
+                // P^T buffer b is free once the P.V two tiles back has completed.
+                ok = mbar_wait(bar(B_PT_EMPTY + b), ((jj >> 1) & 1) ^ 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (key >= P.ctx_len) {
-                    uint4* row = reinterpret_cast<uint4*>(gbase + L::OFF_RAW + (vi % NRAW) * RAW_STAGE +
-                                                          hg * (TILE * 128) + k * 128);
+                {
+                    // [P1 | P2 | P3]^T, K-major: row = term * NP + packed row, byte = key.
+                    uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
-                }
-            }
-            // P^T buffer b is free once the P.V two tiles back has completed.
-            ok = mbar_wait(bar(B_PT_EMPTY + b), ((jj >> 1) & 1) ^ 1, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            {
-                // [P1 | P2 | P3]^T, K-major: row = term * NP + packed row, byte = key.
-                uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
+                    for (int c = 0; c < NH; c += 2) {
+                        const float m0 = mref[c0 + c], m1 = mref[c0 + c + 1];
+                        const float p0 = ex2(s[c] - (m0 == -INFINITY ? 0.f : m0));
+                        const float p1 = ex2(s[c + 1] - (m1 == -INFINITY ? 0.f : m1));
+                        lpart[c] += p0;
+                        lpart[c + 1] += p1;
+                        uint32_t t[3];
+                        split3_e4m3x2(p0, p1, t[0], t[1], t[2]);
+                        const int r0 = c0 + c;
 #pragma unroll
-                for (int c = 0; c < NH; c += 2) {
-                    const float m0 = mref[c0 + c], m1 = mref[c0 + c + 1];
-                    const float p0 = ex2(s[c] - (m0 == -INFINITY ? 0.f : m0));
-                    const float p1 = ex2(s[c + 1] - (m1 == -INFINITY ? 0.f : m1));
-                    lpart[c] += p0;
-                    lpart[c + 1] += p1;
-                    uint32_t t[3];
-                    split3_e4m3x2(p0, p1, t[0], t[1], t[2]);
-                    const int r0 = c0 + c;
-#pragma unroll
-                    for (int e = 0; e < 3; ++e) {
-                        pt[sw128(e * NP + r0, k >> 4) + (k & 15)] = (uint8_t)(t[e] & 0xFF);
-                        pt[sw128(e * NP + r0 + 1, k >> 4) + (k & 15)] = (uint8_t)(t[e] >> 8);
+                        for (int e = 0; e < 3; ++e) {
+                            pt[sw128(e * NP + r0, k >> 4) + (k & 15)] = (uint8_t)(t[e] & 0xFF);
+                            pt[sw128(e * NP + r0 + 1, k >> 4) + (k & 15)] = (uint8_t)(t[e] >> 8);
+                        }
                     }
                 }
+                fence_async_shared();
+                mbar_arrive(bar(B_P_READY + b));
             }
-            fence_async_shared();
-            mbar_arrive(bar(B_P_READY + b));
-        }
-        // ---------------------------------------------------------- epilogue
-        if (ok && ntl > 0) {
-            const int x = ntl - 1;
-            ok = mbar_wait(bar(B_PT_EMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok && ntl > 0) {
-            tc_fence_after();
-            // Row sums: reduce the per-thread partial sums over the 128 keys.
-#pragma unroll
-            for (int c = 0; c < NH; ++c) {
-                float v = lpart[c];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) red[(hg * 4 + wi) * NP + c0 + c] = v;
+            // ---------------------------------------------------------- epilogue
+            if (ok && ntl > 0) {
+                const int x = ntl - 1;
+                ok = mbar_wait(bar(B_PT_EMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
             }
-            ok = group_sync(gbar, gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok && ntl > 0) {
-            if (k < NH && c0 + k < P.nq) {
-                const int c = c0 + k;
-                const float* rr = red + (hg * 4) * NP + c;
-                const float l = (rr[0] + rr[NP]) + (rr[2 * NP] + rr[3 * NP]);
-                P.ws_ml[((size_t)split * P.nq + c) * 2 + 0] = mref[c];
-                P.ws_ml[((size_t)split * P.nq + c) * 2 + 1] = l;
+            if (ok && ntl > 0) {
+                tc_fence_after();
+                // Row sums: reduce the per-thread partial sums over the 128 keys.
+#pragma unroll
+                for (int c = 0; c < NH; ++c) {
+                    float v = lpart[c];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) red[(hg * 4 + wi) * NP + c0 + c] = v;
+                }
+                ok = group_sync(gbar, gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
             }
+            if (ok && ntl > 0) {
+                if (k < NH && c0 + k < P.nq) {
+                    const int c = c0 + k;
+                    const float* rr = red + (hg * 4) * NP + c;
+                    const float l = (rr[0] + rr[NP]) + (rr[2 * NP] + rr[3 * NP]);
+                    P.ws_ml[((size_t)split * P.nq + c) * 2 + 0] = mref[c];
+                    P.ws_ml[((size_t)split * P.nq + c) * 2 + 1] = l;
+                }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r1[NH], r2[NH], r3[NH];
-                tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + c0, r1);
-                tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + NP + c0, r2);
-                tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + 2 * NP + c0, r3);
-                tmem_ld_wait<NH>(r1);
-                tmem_ld_wait<NH>(r2);
-                tmem_ld_wait<NH>(r3);
-                const int d = h * 128 + k;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r1[NH], r2[NH], r3[NH];
+                    tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + c0, r1);
+                    tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + NP + c0, r2);
+                    tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + 2 * NP + c0, r3);
+                    tmem_ld_wait<NH>(r1);
+                    tmem_ld_wait<NH>(r2);
+                    tmem_ld_wait<NH>(r3);
+                    const int d = h * 128 + k;
 #pragma unroll
-                for (int c = 0; c < NH; ++c)
-                    if (c0 + c < P.nq)
-                        P.ws_o[((size_t)split * P.nq + c0 + c) * D + d] =
-                            fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
-                                 fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c])));
+                    for (int c = 0; c < NH; ++c)
+                        if (c0 + c < P.nq)
+                            P.ws_o[((size_t)split * P.nq + c0 + c) * D + d] =
+                                fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
+                                     fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c])));
+                }
             }
         }
+
     }
 
     tc_fence_before();
@@ -643,89 +722,148 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 }
 
 // out[c, d] = vscale * sum_s w_s O_s[c, d] / sum_s w_s l_s, w_s = 2^(m_s - M).
-// Block (c, dg) merges packed row c for d = 32 dg .. 32 dg + 31.  The split
-// weights are computed once per block in shared memory; warp w then sums the
-// splits s = w, w + 8, ... for its lane's d, and the eight warp sums are added
-// in a fixed order, so the result does not depend on timing.
+// Block (c, dh) merges packed row c for d = 128 dh .. 128 dh + 127, four d per
+// lane.  Warp w owns the splits s = w, w + 16, ...; the first MERGE_PF of them
+// are loaded together with every split's (m, l), so that one round of L2
+// latency covers up to 16 * MERGE_PF splits.  The warp sums are added in warp order,
+// so the result does not depend on timing.  The kernel is launched as a
+// programmatic dependent of the split kernel: everything before
+// griddepcontrol.wait overlaps the split kernel's last CTAs.
 constexpr int MERGE_MAX_SPLITS = 1024;
+constexpr int MERGE_WARPS = 16;
+constexpr int MERGE_PF = 10;
 
-__global__ void __launch_bounds__(256) paged_merge_kernel(const Params P) {
+__global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Params P) {
     __shared__ float w_s[MERGE_MAX_SPLITS];
-    __shared__ float red[8][33];
-    __shared__ float stat[2];
+    __shared__ float4 red[MERGE_WARPS][32];
+    __shared__ float wred[2][MERGE_WARPS];
     const int c = blockIdx.x;
-    const int d = blockIdx.y * 32 + (threadIdx.x & 31);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int d0 = blockIdx.y * 128 + lane * 4;
     const int G = P.G;
-    // Phase 1: M = max_s m_s, w_s = 2^(m_s - M), L = sum_s w_s l_s.
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < G; s += 256) {
-        const float m = P.ws_ml[((size_t)s * P.nq + c) * 2];
-        w_s[s] = m;
-        mx = fmaxf(mx, m);
-    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float vs = *P.vscale;
+    // One round of loads: the O partials of this warp's first MERGE_PF splits
+    // and the (m, l) pairs of the splits threadIdx.x + 512 i.
+    float4 o[MERGE_PF];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp][32] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float M = red[0][32];
-        for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w][32]);
-        stat[0] = M;
+    for (int i = 0; i < MERGE_PF; ++i) {
+        const int s = warp + MERGE_WARPS * i;
+        o[i] = s < G ? __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    constexpr int ML_PT = MERGE_MAX_SPLITS / (MERGE_WARPS * 32);
+    float2 ml[ML_PT];
+#pragma unroll
+    for (int i = 0; i < ML_PT; ++i) {
+        const int s = threadIdx.x + MERGE_WARPS * 32 * i;
+        ml[i] = s < G ? __ldcg(reinterpret_cast<const float2*>(P.ws_ml + ((size_t)s * P.nq + c) * 2))
+                      : make_float2(-INFINITY, 0.f);
+    }
+    // M = max_s m_s.
+    float mx = ml[0].x;
+#pragma unroll
+    for (int i = 1; i < ML_PT; ++i) mx = fmaxf(mx, ml[i].x);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+    if (lane == 0) wred[0][warp] = mx;
     __syncthreads();
-    const float M = stat[0];
+    float M = wred[0][0];
+#pragma unroll
+    for (int w = 1; w < MERGE_WARPS; ++w) M = fmaxf(M, wred[0][w]);
+    // w_s = 2^(m_s - M), L = sum_s w_s l_s.
     float lsum = 0.f;
-    for (int s = threadIdx.x; s < G; s += 256) {
-        const float m = w_s[s];
-        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-        w_s[s] = w;
-        lsum += w * P.ws_ml[((size_t)s * P.nq + c) * 2 + 1];
+#pragma unroll
+    for (int i = 0; i < ML_PT; ++i) {
+        const int s = threadIdx.x + MERGE_WARPS * 32 * i;
+        const float w = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - M);
+        if (s < G) w_s[s] = w;
+        lsum += w * ml[i].y;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    for (int o2 = 16; o2 > 0; o2 >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o2);
+    if (lane == 0) wred[1][warp] = lsum;
     __syncthreads();
-    if (lane == 0) red[warp][32] = lsum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float L = 0.f;
-        for (int w = 0; w < 8; ++w) L += red[w][32];
-        stat[1] = L;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < MERGE_PF; ++i) {
+        const int s = warp + MERGE_WARPS * i;
+        const float w = s < G ? w_s[s] : 0.f;
+        acc.x = fmaf(w, o[i].x, acc.x);
+        acc.y = fmaf(w, o[i].y, acc.y);
+        acc.z = fmaf(w, o[i].z, acc.z);
+        acc.w = fmaf(w, o[i].w, acc.w);
     }
-    // Phase 2: weighted sum of the partial O over the splits.
-    float acc = 0.f;
-#pragma unroll 4
-    for (int s = warp; s < G; s += 8) acc += w_s[s] * P.ws_o[((size_t)s * P.nq + c) * D + d];
+    for (int s = warp + MERGE_WARPS * MERGE_PF; s < G; s += MERGE_WARPS) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0));
+        const float w = w_s[s];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
     red[warp][lane] = acc;
     __syncthreads();
     if (warp == 0) {
-        float a = 0.f;
+        float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) a += red[w][lane];
-        const float L = stat[1];
-        const float vs = *P.vscale;
-        P.out[(size_t)c * D + d] = __float2half_rn(L > 0.f ? a / L * vs : 0.f);
+        for (int w = 0; w < MERGE_WARPS; ++w) L += wred[1][w];
+        float4 a = red[0][lane];
+#pragma unroll
+        for (int w = 1; w < MERGE_WARPS; ++w) {
+            const float4 b = red[w][lane];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        const float f = L > 0.f ? vs / L : 0.f;
+        const __half2 h01 = __floats2half2_rn(a.x * f, a.y * f);
+        const __half2 h23 = __floats2half2_rn(a.z * f, a.w * f);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+        pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+        *reinterpret_cast<uint2*>(P.out + (size_t)c * D + d0) = pk;
     }
 }
 
-template <int NP>
+template <int NP, int NWG>
 int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
               int device) {
-    using L = Layout<NP>;
+    using L = Layout<NP, NWG>;
     static bool attr_done[64] = {false};
     if (device < 64 && !attr_done[device]) {
-        if (cudaFuncSetAttribute(paged_split_kernel<NP>,
+        if (cudaFuncSetAttribute(paged_split_kernel<NP, NWG>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::SMEM) != cudaSuccess)
             return GQA_ERR_CUDA;
         attr_done[device] = true;
     }
-    paged_split_kernel<NP><<<P.G, NTHREADS, L::SMEM, stream>>>(tk, tv, P);
+    paged_split_kernel<NP, NWG><<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    paged_merge_kernel<<<dim3(P.nq, D / 32), 256, 0, stream>>>(P);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.nq, D / 128);
+    cfg.blockDim = dim3(MERGE_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_merge_kernel, P) != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
+}
+
+// Packed query rows -> UMMA N and softmax warpgroups: every softmax thread
+// owns 8 columns (8-aligned in tensor memory), so that the latency-bound
+// softmax chain is spread over 8, 16 or 24 warps.
+int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
+                 int device) {
+    if (P.nq <= 16) return launch_np<16, 2>(tk, tv, P, stream, device);
+    if (P.nq <= 32) return launch_np<32, 4>(tk, tv, P, stream, device);
+    return launch_np<48, 6>(tk, tv, P, stream, device);
 }
 
 }  // namespace paged
@@ -774,9 +912,7 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     if (!make_map_2d_u8(&tk, kcache, rows, D, PAGE, 128) ||
         !make_map_2d_u8(&tv, vcache, rows, D, PAGE, 128))
         return GQA_ERR_CUDA;
-    if (P.nq <= 16) return launch_np<16>(tk, tv, P, stream, di->device);
-    if (P.nq <= 32) return launch_np<32>(tk, tv, P, stream, di->device);
-    return launch_np<48>(tk, tv, P, stream, di->device);
+    return launch_split(tk, tv, P, stream, di->device);
 }
 
 }  // namespace gqa
@@ -853,9 +989,7 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     if (!make_map_2d_u8(&tk, kcache, rows, D, PAGE, 128) ||
         !make_map_2d_u8(&tv, vcache, rows, D, PAGE, 128))
         return GQA_ERR_CUDA;
-    if (P.nq <= 16) return launch_np<16>(tk, tv, P, stream, di->device);
-    if (P.nq <= 32) return launch_np<32>(tk, tv, P, stream, di->device);
-    return launch_np<48>(tk, tv, P, stream, di->device);
+    return launch_split(tk, tv, P, stream, di->device);
 }
 
 }  // namespace gqa
