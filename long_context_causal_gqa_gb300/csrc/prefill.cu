@@ -13,11 +13,14 @@
 // * One CTA per SM, warp-specialised:
 //     warp 0      TMA producer (Q tile, then a ring of 16 KB K / V chunks)
 //     warp 1      tensor-memory allocation and the single UMMA-issuing thread
-//     warps 2..5  softmax + epilogue, one thread per tile row (TMEM lane)
+//     warps 2..9  softmax + epilogue: two warpgroups, each thread one tile row
+//                 (TMEM lane) and half of its columns
 // * Tensor memory (512 columns x 128 lanes): O = 256 fp32 columns; two S
 //   buffers of 128 fp32 columns, so Q.K^T of tile j+1 runs while tile j's
-//   softmax runs.  P (fp16) overwrites the first 64 columns of its S buffer
-//   and feeds P.V straight from tensor memory.
+//   softmax runs.  Each warpgroup's P (fp16) overwrites the first 32 columns
+//   of its own 64-column half of the S buffer and feeds P.V straight from
+//   tensor memory.  The two threads of a row swap their half maxima through
+//   shared memory each tile, so both take the same rescale decisions.
 // * Online softmax with a lazy rescale: the per-row reference max only moves
 //   (and O is rescaled in TMEM) when a tile's max exceeds it by more than
 //   8 (log2 units), which bounds P by 256.
@@ -43,13 +46,16 @@ constexpr int BM = 128;         // packed query rows per tile
 constexpr int BN = 128;         // keys per KV tile
 constexpr int D = kHeadDim;     // 256
 constexpr int HQ = kHq;         // 6
-constexpr int NSLOT = 10;       // ring slots
+constexpr int NSLOT = 9;        // ring slots
 constexpr int SLOT_BYTES = 16384;
 constexpr int Q_BYTES = BM * D * 2;           // 64 KB
 constexpr int RING_BYTES = NSLOT * SLOT_BYTES;
-constexpr int NUM_BARS = 2 * NSLOT + 8;  // full/empty ring, q, s[2], p[2], o, drain
-constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + Q_BYTES + NUM_BARS * 8 + 16;
-constexpr int NTHREADS = 192;
+constexpr int NUM_BARS = 2 * NSLOT + 9;  // full/empty ring, q, s[2], p[2], o, drain, group
+constexpr int XCH_BYTES = (2 * 2 + 2) * BM * 4;  // half maxima [parity][half][row], sums [half][row]
+constexpr int SMEM_BYTES =
+    1024 /*align slack*/ + RING_BYTES + Q_BYTES + XCH_BYTES + NUM_BARS * 8 + 16;
+constexpr int NTHREADS = 320;
+constexpr int NSOFT = 256;      // softmax threads
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 0;
 constexpr uint32_t S_COL0 = 256;
@@ -130,6 +136,17 @@ __device__ __forceinline__ uint32_t bar_pfull(uint32_t b, int i) {
 }
 __device__ __forceinline__ uint32_t bar_ofull(uint32_t b) { return b + 8 * (2 * NSLOT + 6); }
 __device__ __forceinline__ uint32_t bar_drain(uint32_t b) { return b + 8 * (2 * NSLOT + 7); }
+__device__ __forceinline__ uint32_t bar_group(uint32_t b) { return b + 8 * (2 * NSLOT + 8); }
+
+// Barrier of the 256 softmax threads on an mbarrier, so that it shares the
+// bounded, abort-aware wait of the pipeline barriers.
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* abort,
+                                           unsigned* err) {
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase, abort, err);
+    phase ^= 1u;
+    return ok;
+}
 
 // Bounded wait that ignores the abort flag (used only while unwinding).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -147,9 +164,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
     const uint32_t s_ring = base;
     const uint32_t s_q = base + RING_BYTES;
-    const uint32_t s_bars = s_q + Q_BYTES;
+    const uint32_t s_bars = s_q + Q_BYTES + XCH_BYTES;
+    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + Q_BYTES);
     uint32_t* tmem_base_ptr =
-        reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + Q_BYTES + NUM_BARS * 8);
+        reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + Q_BYTES + XCH_BYTES + NUM_BARS * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_ptr + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -164,10 +182,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(bar_qempty(s_bars), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull(s_bars, i), 1);
-            mbar_init(bar_pfull(s_bars, i), 128);
+            mbar_init(bar_pfull(s_bars, i), NSOFT);
         }
         mbar_init(bar_ofull(s_bars), 1);
         mbar_init(bar_drain(s_bars), 1);
+        mbar_init(bar_group(s_bars), NSOFT);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
@@ -288,7 +307,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const uint64_t b = sdesc_sw128(vaddr + ks * 2048, 4096, 1024);
-                        const uint32_t a_tmem = tmem + s_col + (sub * 32 + ks * 16) / 2;
+                        // P of keys kb .. kb + 15: half kb / 64 sits at columns
+                        // 64 (kb / 64) + (kb % 64) / 2 of the S buffer.
+                        const int kb = sub * 32 + ks * 16;
+                        const uint32_t a_tmem = tmem + s_col + (kb >> 6) * 64 + ((kb & 63) >> 1);
                         umma_ts(tmem + O_COL, a_tmem, b, IDESC_PV, (acc0 || sub || ks) ? 1u : 0u);
                     }
                     umma_commit(bar_empty(s_bars, slot));
@@ -334,9 +356,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
+        // Warpgroup hg owns S columns [64 hg, 64 hg + 64) of every tile and O
+        // columns [128 hg, 128 hg + 128).  Row maxima: each thread writes its
+        // half maximum to xch[tile parity][hg][row]; after the group barrier it
+        // reads its partner's, so both threads of a row see the same maximum.
+        const int hg = (warp - 2) >> 2;
         const int wq = warp & 3;           // TMEM lane quarter this warp may access
         const int row = wq * 32 + lane;    // tile row == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+        float* xl = xch + 4 * BM;          // row-sum halves [hg][row]
+        const uint32_t gbar = bar_group(s_bars);
+        uint32_t gphase = 0;
         const float sl2 = P.scale_log2;
         uint32_t g = 0;
         bool ok = true;
@@ -354,27 +384,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sr[BN];
+                uint32_t sr[BN / 2];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    tmem_ld32(t_lane + s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-                tmem_ld_wait<BN>(sr);
+                for (int c = 0; c < BN / 64; ++c)
+                    tmem_ld32(t_lane + s_col + 64 * hg + 32 * c,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+                tmem_ld_wait<BN / 2>(sr);
                 float* s = reinterpret_cast<float*>(sr);
                 if (j >= j_mask) {
-                    const int k0 = j * BN;
+                    const int k0 = j * BN + 64 * hg;
 #pragma unroll
-                    for (int c = 0; c < BN; ++c)
+                    for (int c = 0; c < BN / 2; ++c)
                         if (k0 + c > lim) s[c] = -INFINITY;
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 4; c < BN; c += 4) {
+                for (int c = 4; c < BN / 2; c += 4) {
                     mx0 = fmaxf(mx0, s[c]);
                     mx1 = fmaxf(mx1, s[c + 1]);
                     mx2 = fmaxf(mx2, s[c + 2]);
                     mx3 = fmaxf(mx3, s[c + 3]);
                 }
-                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float hm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                float* xp = xch + (gg & 1) * (2 * BM);
+                xp[hg * BM + row] = hm;
+                ok = group_sync(gbar, gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const float mx = fmaxf(xp[row], xp[BM + row]) * sl2;
                 bool o_seen = false;
                 if (j == jb) {
                     m_ref = mx;
@@ -392,39 +429,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             m_ref = mx;
                         }
 #pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
+                        for (int c = 0; c < D / 64; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(t_lane + O_COL + 32 * c, o);
+                            const uint32_t oc = O_COL + 128 * hg + 32 * c;
+                            tmem_ld32(t_lane + oc, o);
                             tmem_ld_wait<32>(o);
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                            tmem_st32(t_lane + O_COL + 32 * c, o);
+                            tmem_st32(t_lane + oc, o);
                         }
                         tmem_st_wait();
                     }
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                uint32_t pk[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int c = h * 64 + 2 * e;
-                        const float p0 = ex2(fmaf(s[c], sl2, neg));
-                        const float p1 = ex2(fmaf(s[c + 1], sl2, neg));
-                        const float p2 = ex2(fmaf(s[c + 2], sl2, neg));
-                        const float p3 = ex2(fmaf(s[c + 3], sl2, neg));
-                        l0 += p0;
-                        l1 += p1;
-                        l2 += p2;
-                        l3 += p3;
-                        pk[e] = pack_half2(p0, p1);
-                        pk[e + 1] = pack_half2(p2, p3);
-                    }
-                    tmem_st32(t_lane + s_col + 32 * h, pk);
+                for (int e = 0; e < 32; e += 2) {
+                    const int c = 2 * e;
+                    const float p0 = ex2(fmaf(s[c], sl2, neg));
+                    const float p1 = ex2(fmaf(s[c + 1], sl2, neg));
+                    const float p2 = ex2(fmaf(s[c + 2], sl2, neg));
+                    const float p3 = ex2(fmaf(s[c + 3], sl2, neg));
+                    l0 += p0;
+                    l1 += p1;
+                    l2 += p2;
+                    l3 += p3;
+                    pk[e] = pack_half2(p0, p1);
+                    pk[e + 1] = pack_half2(p2, p3);
                 }
+                tmem_st32(t_lane + s_col + 64 * hg, pk);
                 l += (l0 + l1) + (l2 + l3);
                 tmem_st_wait();
                 if (j > jb && !o_seen) {
@@ -442,13 +477,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            // Row sum: the two halves, added in a fixed order.
+            xl[hg * BM + row] = l;
+            ok = group_sync(gbar, gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const float l_row = xl[row] + xl[BM + row];
             if (jb == 0 && je == n) {
-                const float inv = (l > 0.f) ? 1.0f / l : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * D);
+                const float inv = (l_row > 0.f) ? 1.0f / l_row : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + 128 * hg);
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + O_COL + 32 * c, o);
+                    tmem_ld32(t_lane + O_COL + 128 * hg + 32 * c, o);
                     tmem_ld_wait<32>(o);
                     uint32_t hv[16];
 #pragma unroll
@@ -465,18 +506,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             } else {
                 const int slot = is_first ? 0 : 1;
                 const size_t prow = ((size_t)blockIdx.x * 2 + slot) * BM + row;
-                uint4* dst = reinterpret_cast<uint4*>(P.ws_o + prow * D);
+                uint4* dst = reinterpret_cast<uint4*>(P.ws_o + prow * D + 128 * hg);
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + O_COL + 32 * c, o);
+                    tmem_ld32(t_lane + O_COL + 128 * hg + 32 * c, o);
                     tmem_ld_wait<32>(o);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[c * 8 + e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
                 }
-                P.ws_ml[prow * 2 + 0] = m_ref;
-                P.ws_ml[prow * 2 + 1] = l;
+                if (hg == 0) {
+                    P.ws_ml[prow * 2 + 0] = m_ref;
+                    P.ws_ml[prow * 2 + 1] = l_row;
+                }
             }
             g += je - jb;
         }
