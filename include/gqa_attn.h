@@ -162,6 +162,12 @@ int gqa_set_workspace(int device, void* ptr, size_t bytes);
  * Returns -1 if the CUDA calls themselves failed. */
 int gqa_get_device_error(struct CUstream_st* stream);
 
+/* Number of SM pairs (two-CTA clusters) gqa_attn_prefill runs on for the
+ * current device: the clusters of its kernel that can be resident at once,
+ * which the GPC layout can put below half the SM count.  Returns -1 on a CUDA
+ * error.  Informational; the library sizes its grid with the same query. */
+int gqa_prefill_sm_pairs(void);
+
 /* Human-readable name of a gqa_status value. */
 const char* gqa_status_string(int status);
 

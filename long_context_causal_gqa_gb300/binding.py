@@ -37,7 +37,7 @@ DEVERR_BAD_PAGE_ID = 0x4
 EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_noalloc",
             "gqa_attn_sparse_blocks",
             "gqa_workspace_bytes", "gqa_set_workspace", "gqa_get_device_error",
-            "gqa_status_string")
+            "gqa_prefill_sm_pairs", "gqa_status_string")
 
 
 class GQAError(RuntimeError):
@@ -76,6 +76,8 @@ def load():
             lib.gqa_set_workspace.restype = I
             lib.gqa_get_device_error.argtypes = [P]
             lib.gqa_get_device_error.restype = I
+            lib.gqa_prefill_sm_pairs.argtypes = []
+            lib.gqa_prefill_sm_pairs.restype = I
             lib.gqa_status_string.argtypes = [I]
             lib.gqa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -145,6 +147,14 @@ def device_error(stream=None) -> int:
     v = load().gqa_get_device_error(_stream_ptr(stream))
     if v < 0:
         raise GQAError(GQA_ERR_CUDA, "gqa_get_device_error")
+    return v
+
+
+def prefill_sm_pairs() -> int:
+    """SM pairs the dense prefill kernel runs on (co-resident two-CTA clusters)."""
+    v = load().gqa_prefill_sm_pairs()
+    if v < 0:
+        raise GQAError(GQA_ERR_CUDA, "gqa_prefill_sm_pairs")
     return v
 
 

@@ -235,6 +235,8 @@ int gqa_get_device_error(struct CUstream_st* stream) {
     return (int)v;
 }
 
+int gqa_prefill_sm_pairs(void) { return prefill_resident_pairs(); }
+
 const char* gqa_status_string(int status) {
     switch (status) {
         case GQA_OK: return "GQA_OK";

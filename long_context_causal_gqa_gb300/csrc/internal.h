@@ -51,6 +51,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
                    float scale, cudaStream_t stream);
 size_t prefill_workspace_bytes(int Q, int KV, int num_sms);
+int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill kernel
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,

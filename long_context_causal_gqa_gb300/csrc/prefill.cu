@@ -7,29 +7,39 @@
 // causal tail with online-softmax state; both ideas carry over, re-shaped for
 // tcgen05:
 //
-// * Head packing.  q is [Q, 6, 256] = [6Q, 256] row-major, so 128 consecutive
-//   flattened rows (about 21 positions x 6 heads) are one 128-row M tile with
-//   no padding.  Each K/V tile is read once per 128 packed rows.
-// * One CTA per SM, warp-specialised:
-//     warp 0      TMA producer (Q tile, then a ring of 16 KB K / V chunks)
-//     warp 1      tensor-memory allocation and the single UMMA-issuing thread
-//     warps 2..9  softmax + epilogue: two warpgroups, each thread one tile row
-//                 (TMEM lane) and half of its columns
-// * Tensor memory (512 columns x 128 lanes): O = 256 fp32 columns; two S
-//   buffers of 128 fp32 columns, so Q.K^T of tile j+1 runs while tile j's
-//   softmax runs.  Each warpgroup's P (fp16) overwrites the first 32 columns
-//   of its own 64-column half of the S buffer and feeds P.V straight from
-//   tensor memory.  The two threads of a row swap their half maxima through
-//   shared memory each tile, so both take the same rescale decisions.
+// * Head packing.  q is [Q, 6, 256] = [6Q, 256] row-major, so consecutive
+//   flattened rows (positions x 6 heads) form the M tiles with no padding.
+// * CTA pairs (cta_group::2).  A cluster of two CTAs on neighbouring SMs
+//   takes a pair tile of 256 packed rows, 128 per CTA, and runs one M = 256
+//   UMMA stream issued by the even CTA:
+//     S[256 x 128 keys]  = Q[256 x 256] . K^T     (K-major operands)
+//     O[256 x 256 d]    += P[256 x 128] . V        (P from tensor memory)
+//   Each CTA holds its own 128 rows of Q, S, P and O, but only half of every
+//   K tile (64 keys) and half of every V tile (128 of the 256 d), so a K/V
+//   tile costs each SM 64 KB of shared-memory traffic instead of 128 KB and
+//   the copy ring covers twice as many tiles of L2 latency.
+// * Warp roles per CTA: warp 0 loads Q and K, warp 10 loads V (each its
+//   half of every operand; the odd CTA's copies complete on the even CTA's
+//   barriers), warp 1 tensor-memory owner and, in the even CTA, the single
+//   UMMA-issuing thread, warps 2..9 softmax + epilogue in two warpgroups, each
+//   thread one tile row (TMEM lane) and half of its columns.
+// * K and V stream through separate rings of 16 KB slots, so that K of the
+//   next tiles never waits behind V slots held until their P is ready.
+// * Tensor memory (512 columns x 128 lanes per CTA): O = 256 fp32 columns;
+//   two S buffers of 128 fp32 columns, so Q.K^T of tile j+1 runs while tile
+//   j's softmax runs.  Each warpgroup's P (fp16) overwrites the first 32
+//   columns of its own 64-column half of the S buffer.  The two threads of a
+//   row swap their half maxima through shared memory each tile, so both take
+//   the same rescale decisions.
 // * Online softmax with a lazy rescale: the per-row reference max only moves
 //   (and O is rescaled in TMEM) when a tile's max exceeds it by more than
 //   8 (log2 units), which bounds P by 256.
-// * Only the one or two KV tiles on a q-tile's diagonal are masked.
-// * Work split: the causal-visible (q-tile, kv-tile) iterations are laid out
-//   q-tile-major and cut into one contiguous, equal range per CTA (shape-only,
-//   so deterministic).  A q-tile cut between CTAs leaves (O, m, l) partials in
-//   the workspace; a merge kernel combines them in CTA order (exact
-//   log-sum-exp merge).
+// * Only the one or two KV tiles on a pair tile's diagonal are masked.
+// * Work split: the causal-visible (pair tile, kv tile) iterations are laid
+//   out pair-tile-major and cut into one contiguous, equal range per CTA pair
+//   (shape-only, so deterministic).  A pair tile cut between pairs leaves
+//   (O, m, l) partials in the workspace; a merge kernel combines them in pair
+//   order (exact log-sum-exp merge).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -42,73 +52,86 @@
 namespace gqa {
 namespace prefill {
 
-constexpr int BM = 128;         // packed query rows per tile
+constexpr int BM = 128;         // packed query rows per CTA
+constexpr int BM2 = 2 * BM;     // packed query rows per CTA pair
 constexpr int BN = 128;         // keys per KV tile
 constexpr int D = kHeadDim;     // 256
 constexpr int HQ = kHq;         // 6
-constexpr int NSLOT = 9;        // ring slots
+// Ring slots of 16 KB.  A K slot holds this CTA's 64 keys x two 64-wide d
+// chunks (8 KB each); a V slot holds two 32-key sub-tiles x this CTA's 128 d
+// (8 KB each, two 64-wide atoms of 4 KB).  A tile's half of K or V is two slots.
 constexpr int SLOT_BYTES = 16384;
+constexpr int HALF_SLOT = SLOT_BYTES / 2;
+constexpr int NK = 4;                         // K slots (two tiles)
+constexpr int NV = 5;                         // V slots
 constexpr int Q_BYTES = BM * D * 2;           // 64 KB
-constexpr int RING_BYTES = NSLOT * SLOT_BYTES;
-constexpr int NUM_BARS = 2 * NSLOT + 9;  // full/empty ring, q, s[2], p[2], o, drain, group
-constexpr int XCH_BYTES = (2 * 2 + 2) * BM * 4;  // half maxima [parity][half][row], sums [half][row]
+constexpr int RING_BYTES = (NK + NV) * SLOT_BYTES;
+constexpr int NWG = 2;                        // softmax warpgroups per CTA
+constexpr int COLS = BN / NWG;                // S columns per softmax thread
+constexpr int OCOLS = D / NWG;                // O columns per softmax thread
+constexpr int NSOFT = 128 * NWG;              // softmax threads per CTA
+constexpr int NTHREADS = 64 + NSOFT + 32;     // + the V producer warp
+constexpr int V_WARP = 2 + NSOFT / 32;
+// Barriers: K full/empty, V full/empty, q full/empty, s[2], p[2], o, drain, group.
+constexpr int NRING = NK + NV;
+constexpr int NUM_BARS = 2 * NRING + 9;
+constexpr int XCH_BYTES = 3 * NWG * BM * 4;  // part maxima [parity][part][row], sums [part][row]
 constexpr int SMEM_BYTES =
     1024 /*align slack*/ + RING_BYTES + Q_BYTES + XCH_BYTES + NUM_BARS * 8 + 16;
-constexpr int NTHREADS = 320;
-constexpr int NSOFT = 256;      // softmax threads
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 0;
 constexpr uint32_t S_COL0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+constexpr int kMaxClusters = 80;
 
-// UMMA shapes: S[128 x 128] = Q[128 x 16] K^T, both K-major;
-// O[128 x 256] += P[128 x 16] (tensor memory) V[16 x 256], V MN-major.
-constexpr uint32_t IDESC_QK = idesc_f16_f32(128, 128, false, false);
-constexpr uint32_t IDESC_PV = idesc_f16_f32(128, 256, false, true);
+// UMMA shapes (M = 256 over the pair): S[256 x 128] = Q[256 x 16] K^T, both
+// K-major; O[256 x 256] += P[256 x 16] (tensor memory) V[16 x 256], V MN-major.
+constexpr uint32_t IDESC_QK = idesc_f16_f32(256, 128, false, false);
+constexpr uint32_t IDESC_PV = idesc_f16_f32(256, 256, false, true);
 
 struct Params {
-    int Q, KV, M_total, num_qtiles, G;
-    long long total;      // causal-visible (q-tile, kv-tile) iterations
+    int Q, KV, M_total, num_ptiles, G;
+    long long total;      // causal-visible (pair tile, kv tile) iterations
     float scale_log2;     // scale * log2(e)
     __half* out;
-    float* ws_o;          // [G][2][BM][D] unnormalised partial O
-    float* ws_ml;         // [G][2][BM][2] partial (m in log2 units, l)
+    float* ws_o;          // [G][2][BM2][D] unnormalised partial O
+    float* ws_ml;         // [G][2][BM2][2] partial (m in log2 units, l)
     unsigned* err;
 };
 
-// KV tiles q-tile t needs: up to the last visible key of its last valid row.
+// KV tiles pair tile t needs: up to the last visible key of its last valid row.
 __host__ __device__ inline int kv_tiles(int t, int Q, int KV, int M_total) {
-    int last = min(t * BM + BM - 1, M_total - 1);
+    int last = min(t * BM2 + BM2 - 1, M_total - 1);
     return (KV - Q + last / HQ) / BN + 1;
 }
 
-__host__ __device__ inline long long cta_begin(long long total, int G, int c) {
+__host__ __device__ inline long long pair_begin(long long total, int G, int c) {
     return (long long)c * total / G;
 }
 
-// Walks the segments (q-tile, [jb, je)) of one CTA's iteration range.
+// Walks the segments (pair tile, [jb, je)) of one pair's iteration range.
 struct SegIter {
     long long pos, end, cum;
     int t;
     bool first;
-    __device__ void init(const Params& P, int cta) {
-        pos = cta_begin(P.total, P.G, cta);
-        end = cta_begin(P.total, P.G, cta + 1);
+    __device__ void init(const Params& P, int pair) {
+        pos = pair_begin(P.total, P.G, pair);
+        end = pair_begin(P.total, P.G, pair + 1);
         t = 0;
         cum = 0;
         first = true;
-        while (t < P.num_qtiles) {
+        while (t < P.num_ptiles) {
             int n = kv_tiles(t, P.Q, P.KV, P.M_total);
             if (cum + n > pos) break;
             cum += n;
             ++t;
         }
     }
-    // Next segment; is_first tells whether it is this CTA's first segment.
-    __device__ bool next(const Params& P, int& qt, int& jb, int& je, int& n, bool& is_first) {
+    // Next segment; is_first tells whether it is this pair's first segment.
+    __device__ bool next(const Params& P, int& pt, int& jb, int& je, int& n, bool& is_first) {
         if (pos >= end) return false;
         n = kv_tiles(t, P.Q, P.KV, P.M_total);
-        qt = t;
+        pt = t;
         jb = (int)(pos - cum);
         long long e = end - cum;
         je = e < n ? (int)e : n;
@@ -123,29 +146,91 @@ struct SegIter {
     }
 };
 
-
+// Ring slot s: K slots are 0 .. NK-1, V slots NK .. NK+NV-1.
 __device__ __forceinline__ uint32_t bar_full(uint32_t b, int s) { return b + 8 * s; }
-__device__ __forceinline__ uint32_t bar_empty(uint32_t b, int s) { return b + 8 * (NSLOT + s); }
-__device__ __forceinline__ uint32_t bar_qfull(uint32_t b) { return b + 8 * (2 * NSLOT); }
-__device__ __forceinline__ uint32_t bar_qempty(uint32_t b) { return b + 8 * (2 * NSLOT + 1); }
+__device__ __forceinline__ uint32_t bar_empty(uint32_t b, int s) { return b + 8 * (NRING + s); }
+__device__ __forceinline__ uint32_t bar_qfull(uint32_t b) { return b + 8 * (2 * NRING); }
+__device__ __forceinline__ uint32_t bar_qempty(uint32_t b) { return b + 8 * (2 * NRING + 1); }
 __device__ __forceinline__ uint32_t bar_sfull(uint32_t b, int i) {
-    return b + 8 * (2 * NSLOT + 2 + i);
+    return b + 8 * (2 * NRING + 2 + i);
 }
 __device__ __forceinline__ uint32_t bar_pfull(uint32_t b, int i) {
-    return b + 8 * (2 * NSLOT + 4 + i);
+    return b + 8 * (2 * NRING + 4 + i);
 }
-__device__ __forceinline__ uint32_t bar_ofull(uint32_t b) { return b + 8 * (2 * NSLOT + 6); }
-__device__ __forceinline__ uint32_t bar_drain(uint32_t b) { return b + 8 * (2 * NSLOT + 7); }
-__device__ __forceinline__ uint32_t bar_group(uint32_t b) { return b + 8 * (2 * NSLOT + 8); }
+__device__ __forceinline__ uint32_t bar_ofull(uint32_t b) { return b + 8 * (2 * NRING + 6); }
+__device__ __forceinline__ uint32_t bar_drain(uint32_t b) { return b + 8 * (2 * NRING + 7); }
+__device__ __forceinline__ uint32_t bar_group(uint32_t b) { return b + 8 * (2 * NRING + 8); }
 
-// Barrier of the 256 softmax threads on an mbarrier, so that it shares the
-// bounded, abort-aware wait of the pipeline barriers.
-__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* abort,
-                                           unsigned* err) {
-    mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase, abort, err);
-    phase ^= 1u;
-    return ok;
+// One ring (K or V) seen by its producer and by the UMMA issuer: slot
+// position n maps to slot first + n % count, phase (n / count) & 1.
+struct Ring {
+    int first, count;
+    uint32_t n;
+    __device__ int slot() const { return first + (int)(n % (uint32_t)count); }
+    __device__ uint32_t phase() const { return (n / (uint32_t)count) & 1u; }
+};
+
+// ---------------------------------------------------------------- CTA pairs
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// The address of the same shared-memory object in the pair's even CTA.
+__device__ __forceinline__ uint32_t leader_addr(uint32_t a) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                              int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void umma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at this offset in both CTAs of the pair when
+// every UMMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
 }
 
 // Bounded wait that ignores the abort flag (used only while unwinding).
@@ -156,7 +241,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+// Barrier of the softmax threads of one CTA on an mbarrier, so that it shares
+// the bounded, abort-aware wait of the pipeline barriers.
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* abort,
+                                           unsigned* err) {
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase, abort, err);
+    phase ^= 1u;
+    return ok;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params P) {
     extern __shared__ uint8_t smem_raw[];
@@ -172,9 +267,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();      // 0: issues the UMMAs of the pair
+    const bool leader = rank == 0;
+    const int pair = (int)cluster_id_x();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSLOT; ++s) {
+        for (int s = 0; s < NRING; ++s) {
             mbar_init(bar_full(s_bars, s), 1);
             mbar_init(bar_empty(s_bars, s), 1);
         }
@@ -182,7 +280,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(bar_qempty(s_bars), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull(s_bars, i), 1);
-            mbar_init(bar_pfull(s_bars, i), NSOFT);
+            mbar_init(bar_pfull(s_bars, i), 2 * NSOFT / 32);   // one arrival per softmax warp of the pair
         }
         mbar_init(bar_ofull(s_bars), 1);
         mbar_init(bar_drain(s_bars), 1);
@@ -194,131 +292,155 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tma_prefetch_desc(&tm_v);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_base_ptr), TMEM_COLS);
-        tmem_relinquish();
+        // One warp of each CTA of the pair allocates, collectively.
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_base_ptr)),
+                     "r"(TMEM_COLS)
+                     : "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    // Both CTAs' barriers are initialised before either uses the other's.
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_ptr;
+    // The merge kernel may be scheduled now; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;");
 
     SegIter it;
-    it.init(P, blockIdx.x);
-    int qt, jb, je, n;
+    it.init(P, pair);
+    int pt, jb, je, n;
     bool is_first;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == V_WARP) {
+        // ------------------------------------------------------------ producers
+        // Warp 0: Q and K; warp V_WARP: V.  Each loads this CTA's half of
+        // every operand; completions land on the even CTA's full barriers,
+        // whose transaction count the even CTA sets for both halves.
         if (lane == 0) {
-            uint32_t ring = 0;
+            const bool kq = warp == 0;
+            Ring rg{kq ? 0 : NK, kq ? NK : NV, 0u};
             int seg = 0;
             bool ok = true;
-            auto acquire = [&](uint32_t& slot_addr) -> int {
-                const int slot = ring % NSLOT;
-                const uint32_t ph = (ring / NSLOT) & 1u;
-                if (!mbar_wait(bar_empty(s_bars, slot), ph ^ 1u, abort_flag, P.err)) return -1;
-                slot_addr = s_ring + slot * SLOT_BYTES;
-                return slot;
-            };
-            auto load_k = [&](int j) -> bool {
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t dst;
-                    const int slot = acquire(dst);
-                    if (slot < 0) return false;
-                    mbar_arrive_expect_tx(bar_full(s_bars, slot), SLOT_BYTES);
-                    tma_load_2d(dst, &tm_k, bar_full(s_bars, slot), c * 64, j * BN);
-                    ++ring;
-                }
+            // Acquire the next slot of this ring; returns its full barrier.
+            auto acquire = [&](uint32_t& dst, uint32_t& fb) -> bool {
+                const int slot = rg.slot();
+                if (!mbar_wait(bar_empty(s_bars, slot), rg.phase() ^ 1u, abort_flag, P.err))
+                    return false;
+                dst = s_ring + slot * SLOT_BYTES;
+                fb = bar_full(s_bars, slot);
+                if (leader) mbar_arrive_expect_tx(fb, 2 * SLOT_BYTES);
+                fb = leader_addr(fb);
                 return true;
             };
-            auto load_v = [&](int j) -> bool {
-                for (int sub = 0; sub < 4; ++sub) {
-                    uint32_t dst;
-                    const int slot = acquire(dst);
-                    if (slot < 0) return false;
-                    mbar_arrive_expect_tx(bar_full(s_bars, slot), SLOT_BYTES);
+            while (ok && it.next(P, pt, jb, je, n, is_first)) {
+                if (kq) {
+                    if (!mbar_wait(bar_qempty(s_bars), (seg & 1) ^ 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t qb = bar_qfull(s_bars);
+                    if (leader) mbar_arrive_expect_tx(qb, 2 * Q_BYTES);
                     for (int c = 0; c < 4; ++c)
-                        tma_load_2d(dst + c * 4096, &tm_v, bar_full(s_bars, slot), c * 64,
-                                    j * BN + sub * 32);
-                    ++ring;
+                        tma_load_pair(s_q + c * (BM * 128), &tm_q, leader_addr(qb), c * 64,
+                                      pt * BM2 + BM * (int)rank);
                 }
-                return true;
-            };
-            while (ok && it.next(P, qt, jb, je, n, is_first)) {
-                if (!mbar_wait(bar_qempty(s_bars), (seg & 1) ^ 1, abort_flag, P.err)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar_qfull(s_bars), Q_BYTES);
-                for (int c = 0; c < 4; ++c)
-                    tma_load_2d(s_q + c * (BM * 128), &tm_q, bar_qfull(s_bars), c * 64, qt * BM);
-                ok = load_k(jb);
                 for (int j = jb; ok && j < je; ++j) {
-                    if (j + 1 < je) ok = load_k(j + 1);
-                    if (ok) ok = load_v(j);
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        uint32_t dst, fb;
+                        if (!acquire(dst, fb)) {
+                            ok = false;
+                            break;
+                        }
+                        if (kq) {
+                            // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
+                            for (int cc = 0; cc < 2; ++cc)
+                                tma_load_pair(dst + cc * HALF_SLOT, &tm_k, fb, (2 * h + cc) * 64,
+                                              j * BN + 64 * (int)rank);
+                        } else {
+                            // V: sub-tiles 2h, 2h + 1 (32 keys) x this CTA's 128 d
+                            for (int ss = 0; ss < 2; ++ss)
+                                for (int a = 0; a < 2; ++a)
+                                    tma_load_pair(dst + ss * HALF_SLOT + a * 4096, &tm_v, fb,
+                                                  128 * (int)rank + 64 * a,
+                                                  j * BN + (2 * h + ss) * 32);
+                        }
+                        ++rg.n;
+                    }
                 }
                 ++seg;
             }
-            if (!ok) {
-                // Unwind: let every copy still in flight land before the CTA exits.
-                for (int s = 0; s < NSLOT; ++s) {
-                    const uint32_t fills = ring > (uint32_t)s ? (ring - s + NSLOT - 1) / NSLOT : 0;
-                    if (fills) drain_wait(bar_full(s_bars, s), (fills - 1) & 1u);
+            if (!ok && leader) {
+                // Unwind: let every copy still in flight land before the CTA exits
+                // (the even CTA's full barriers count both halves).
+                for (int i = 0; i < rg.count; ++i) {
+                    const uint32_t fills =
+                        rg.n > (uint32_t)i ? (rg.n - i + rg.count - 1) / rg.count : 0;
+                    if (fills) drain_wait(bar_full(s_bars, rg.first + i), (fills - 1) & 1u);
                 }
-                if (seg > 0) drain_wait(bar_qfull(s_bars), (seg - 1) & 1);
+                if (kq && seg > 0) drain_wait(bar_qfull(s_bars), (seg - 1) & 1);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t ring = 0;
+        if (lane == 0 && leader) {
+            Ring kr{0, NK, 0u}, vr{NK, NV, 0u};
             uint32_t g = 0;
             int seg = 0;
             bool ok = true;
-            auto take = [&](int& slot) -> bool {
-                slot = ring % NSLOT;
-                const uint32_t ph = (ring / NSLOT) & 1u;
-                if (!mbar_wait(bar_full(s_bars, slot), ph, abort_flag, P.err)) return false;
+            auto take = [&](Ring& rg, int& slot) -> bool {
+                slot = rg.slot();
+                if (!mbar_wait(bar_full(s_bars, slot), rg.phase(), abort_flag, P.err)) return false;
                 tc_fence_after();
                 return true;
             };
             auto issue_qk = [&](uint32_t s_col) -> bool {
-                for (int c = 0; c < 4; ++c) {
+                for (int h = 0; h < 2; ++h) {
                     int slot;
-                    if (!take(slot)) return false;
+                    if (!take(kr, slot)) return false;
                     const uint32_t kaddr = s_ring + slot * SLOT_BYTES;
-                    const uint32_t qaddr = s_q + c * (BM * 128);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(qaddr + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(kaddr + kk * 32, 16, 1024);
-                        umma_ss(tmem + s_col, a, b, IDESC_QK, (c | kk) != 0);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * h + cc;
+                        const uint32_t qaddr = s_q + c * (BM * 128);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(qaddr + kk * 32, 16, 1024);
+                            const uint64_t b =
+                                sdesc_sw128(kaddr + cc * HALF_SLOT + kk * 32, 16, 1024);
+                            umma_ss_pair(tmem + s_col, a, b, IDESC_QK, (c | kk) != 0);
+                        }
                     }
-                    umma_commit(bar_empty(s_bars, slot));
-                    ++ring;
+                    umma_commit_pair(bar_empty(s_bars, slot));
+                    ++kr.n;
                 }
                 return true;
             };
             auto issue_pv = [&](uint32_t s_col, bool acc0) -> bool {
-                for (int sub = 0; sub < 4; ++sub) {
+                for (int h = 0; h < 2; ++h) {
                     int slot;
-                    if (!take(slot)) return false;
+                    if (!take(vr, slot)) return false;
                     const uint32_t vaddr = s_ring + slot * SLOT_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const uint64_t b = sdesc_sw128(vaddr + ks * 2048, 4096, 1024);
-                        // P of keys kb .. kb + 15: half kb / 64 sits at columns
-                        // 64 (kb / 64) + (kb % 64) / 2 of the S buffer.
-                        const int kb = sub * 32 + ks * 16;
-                        const uint32_t a_tmem = tmem + s_col + (kb >> 6) * 64 + ((kb & 63) >> 1);
-                        umma_ts(tmem + O_COL, a_tmem, b, IDESC_PV, (acc0 || sub || ks) ? 1u : 0u);
+                    for (int ss = 0; ss < 2; ++ss) {
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const uint64_t b =
+                                sdesc_sw128(vaddr + ss * HALF_SLOT + ks * 2048, 4096, 1024);
+                            // P of keys kb .. kb + 15: part kb / COLS sits at columns
+                            // COLS (kb / COLS) + (kb % COLS) / 2 of the S buffer.
+                            const int kb = (2 * h + ss) * 32 + ks * 16;
+                            const uint32_t a_tmem =
+                                tmem + s_col + (kb / COLS) * COLS + (kb % COLS) / 2;
+                            umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV,
+                                         (acc0 || h || ss || ks) ? 1u : 0u);
+                        }
                     }
-                    umma_commit(bar_empty(s_bars, slot));
-                    ++ring;
+                    umma_commit_pair(bar_empty(s_bars, slot));
+                    ++vr.n;
                 }
                 return true;
             };
-            while (ok && it.next(P, qt, jb, je, n, is_first)) {
+            while (ok && it.next(P, pt, jb, je, n, is_first)) {
                 if (!mbar_wait(bar_qfull(s_bars), seg & 1, abort_flag, P.err)) {
                     ok = false;
                     break;
@@ -326,15 +448,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_after();
                 ok = issue_qk(S_COL0 + (g & 1) * BN);
                 if (!ok) break;
-                umma_commit(bar_sfull(s_bars, g & 1));
-                if (je - jb == 1) umma_commit(bar_qempty(s_bars));
+                umma_commit_pair(bar_sfull(s_bars, g & 1));
+                if (je - jb == 1) umma_commit_pair(bar_qempty(s_bars));
                 for (int j = jb; j < je; ++j) {
                     const uint32_t gg = g + (j - jb);
                     if (j + 1 < je) {
                         ok = issue_qk(S_COL0 + ((gg + 1) & 1) * BN);
                         if (!ok) break;
-                        umma_commit(bar_sfull(s_bars, (gg + 1) & 1));
-                        if (j + 1 == je - 1) umma_commit(bar_qempty(s_bars));
+                        umma_commit_pair(bar_sfull(s_bars, (gg + 1) & 1));
+                        if (j + 1 == je - 1) umma_commit_pair(bar_qempty(s_bars));
                     }
                     if (!mbar_wait(bar_pfull(s_bars, gg & 1), (gg >> 1) & 1, abort_flag, P.err)) {
                         ok = false;
@@ -343,38 +465,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tc_fence_after();
                     ok = issue_pv(S_COL0 + (gg & 1) * BN, j > jb);
                     if (!ok) break;
-                    umma_commit(bar_ofull(s_bars));
+                    umma_commit_pair(bar_ofull(s_bars));
                 }
                 g += je - jb;
                 ++seg;
             }
             if (!ok) {
                 // Unwind: wait for every UMMA already issued before TMEM is freed.
-                umma_commit(bar_drain(s_bars));
+                umma_commit_pair(bar_drain(s_bars));
                 drain_wait(bar_drain(s_bars), 0);
             }
         }
-    } else {
+    } else if (warp < V_WARP) {
         // ------------------------------------------------------------ softmax / epilogue
-        // Warpgroup hg owns S columns [64 hg, 64 hg + 64) of every tile and O
-        // columns [128 hg, 128 hg + 128).  Row maxima: each thread writes its
-        // half maximum to xch[tile parity][hg][row]; after the group barrier it
-        // reads its partner's, so both threads of a row see the same maximum.
+        // Warpgroup hg owns S columns [COLS hg, COLS (hg + 1)) of every tile
+        // and O columns [OCOLS hg, OCOLS (hg + 1)).  Row maxima: each thread
+        // writes its part maximum to xch[tile parity][hg][row]; after the group
+        // barrier it reads the others', so all threads of a row see the same
+        // maximum (combined in a fixed order).
         const int hg = (warp - 2) >> 2;
         const int wq = warp & 3;           // TMEM lane quarter this warp may access
         const int row = wq * 32 + lane;    // tile row == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        float* xl = xch + 4 * BM;          // row-sum halves [hg][row]
+        float* xl = xch + 2 * NWG * BM;    // row-sum parts [hg][row]
         const uint32_t gbar = bar_group(s_bars);
         uint32_t gphase = 0;
         const float sl2 = P.scale_log2;
         uint32_t g = 0;
         bool ok = true;
-        while (ok && it.next(P, qt, jb, je, n, is_first)) {
-            const int m_row = qt * BM + row;
+        while (ok && it.next(P, pt, jb, je, n, is_first)) {
+            const int m_row = pt * BM2 + BM * (int)rank + row;
             const bool valid = m_row < P.M_total;
             const int lim = P.KV - P.Q + m_row / HQ;           // last visible key
-            const int j_mask = (P.KV - P.Q + (qt * BM) / HQ + 1) / BN;  // first tile to mask
+            const int j_mask = (P.KV - P.Q + (pt * BM2 + BM * (int)rank) / HQ + 1) / BN;
             float m_ref = -INFINITY;
             float l = 0.f;
             for (int j = jb; j < je; ++j) {
@@ -384,34 +507,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sr[BN / 2];
+                uint32_t sr[COLS];
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c)
-                    tmem_ld32(t_lane + s_col + 64 * hg + 32 * c,
+                for (int c = 0; c < COLS / 32; ++c)
+                    tmem_ld32(t_lane + s_col + COLS * hg + 32 * c,
                               *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-                tmem_ld_wait<BN / 2>(sr);
+                tmem_ld_wait<COLS>(sr);
                 float* s = reinterpret_cast<float*>(sr);
                 if (j >= j_mask) {
-                    const int k0 = j * BN + 64 * hg;
+                    const int k0 = j * BN + COLS * hg;
 #pragma unroll
-                    for (int c = 0; c < BN / 2; ++c)
+                    for (int c = 0; c < COLS; ++c)
                         if (k0 + c > lim) s[c] = -INFINITY;
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 4; c < BN / 2; c += 4) {
+                for (int c = 4; c < COLS; c += 4) {
                     mx0 = fmaxf(mx0, s[c]);
                     mx1 = fmaxf(mx1, s[c + 1]);
                     mx2 = fmaxf(mx2, s[c + 2]);
                     mx3 = fmaxf(mx3, s[c + 3]);
                 }
                 const float hm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-                float* xp = xch + (gg & 1) * (2 * BM);
+                float* xp = xch + (gg & 1) * (NWG * BM);
                 xp[hg * BM + row] = hm;
                 ok = group_sync(gbar, gphase, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const float mx = fmaxf(xp[row], xp[BM + row]) * sl2;
+                float rm = xp[row];
+#pragma unroll
+                for (int h = 1; h < NWG; ++h) rm = fmaxf(rm, xp[h * BM + row]);
+                const float mx = rm * sl2;
                 bool o_seen = false;
                 if (j == jb) {
                     m_ref = mx;
@@ -429,9 +555,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             m_ref = mx;
                         }
 #pragma unroll 1
-                        for (int c = 0; c < D / 64; ++c) {
+                        for (int c = 0; c < OCOLS / 32; ++c) {
                             uint32_t o[32];
-                            const uint32_t oc = O_COL + 128 * hg + 32 * c;
+                            const uint32_t oc = O_COL + OCOLS * hg + 32 * c;
                             tmem_ld32(t_lane + oc, o);
                             tmem_ld_wait<32>(o);
 #pragma unroll
@@ -444,9 +570,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-                uint32_t pk[32];
+                uint32_t pk[COLS / 2];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < COLS / 2; e += 2) {
                     const int c = 2 * e;
                     const float p0 = ex2(fmaf(s[c], sl2, neg));
                     const float p1 = ex2(fmaf(s[c + 1], sl2, neg));
@@ -459,7 +585,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     pk[e] = pack_half2(p0, p1);
                     pk[e + 1] = pack_half2(p2, p3);
                 }
-                tmem_st32(t_lane + s_col + 64 * hg, pk);
+                tmem_st32(t_lane + s_col + COLS * hg, pk);
                 l += (l0 + l1) + (l2 + l3);
                 tmem_st_wait();
                 if (j > jb && !o_seen) {
@@ -468,7 +594,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (!ok) break;
                 }
                 tc_fence_before();
-                mbar_arrive(bar_pfull(s_bars, gg & 1));
+                __syncwarp();
+                if (lane == 0) remote_arrive(leader_addr(bar_pfull(s_bars, gg & 1)));
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
@@ -477,19 +604,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // Row sum: the two halves, added in a fixed order.
+            // Row sum: the parts, added in a fixed order.
             xl[hg * BM + row] = l;
             ok = group_sync(gbar, gphase, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            const float l_row = xl[row] + xl[BM + row];
+            float l_row = xl[row];
+#pragma unroll
+            for (int h = 1; h < NWG; ++h) l_row += xl[h * BM + row];
             if (jb == 0 && je == n) {
                 const float inv = (l_row > 0.f) ? 1.0f / l_row : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + 128 * hg);
+                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + OCOLS * hg);
 #pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
+                for (int c = 0; c < OCOLS / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + O_COL + 128 * hg + 32 * c, o);
+                    tmem_ld32(t_lane + O_COL + OCOLS * hg + 32 * c, o);
                     tmem_ld_wait<32>(o);
                     uint32_t hv[16];
 #pragma unroll
@@ -505,12 +634,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             } else {
                 const int slot = is_first ? 0 : 1;
-                const size_t prow = ((size_t)blockIdx.x * 2 + slot) * BM + row;
-                uint4* dst = reinterpret_cast<uint4*>(P.ws_o + prow * D + 128 * hg);
+                const size_t prow = ((size_t)pair * 2 + slot) * BM2 + BM * rank + row;
+                uint4* dst = reinterpret_cast<uint4*>(P.ws_o + prow * D + OCOLS * hg);
 #pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
+                for (int c = 0; c < OCOLS / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + O_COL + 128 * hg + 32 * c, o);
+                    tmem_ld32(t_lane + O_COL + OCOLS * hg + 32 * c, o);
                     tmem_ld_wait<32>(o);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -525,37 +654,52 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     }
 
-    tc_fence_before();
+    // After an abort, give copies the other CTA of the pair still had in
+    // flight into this CTA's shared memory time to land before it exits.
     __syncthreads();
+    if (*abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+    }
+    tc_fence_before();
+    // Neither CTA leaves while the other may still signal its barriers.
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
     }
 }
 
-// A q-tile cut between CTAs c0 .. c_last: its first piece is CTA c0's last
-// segment (partial slot slot0), the others are the first segments (slot 0) of
-// CTAs c0 + 1 .. c_last.  Found on the host from the same shape-only schedule.
-constexpr int kMaxCtas = 160;
+// A pair tile cut between pairs c0 .. c_last: its first piece is pair c0's
+// last segment (partial slot slot0), the others are the first segments (slot
+// 0) of pairs c0 + 1 .. c_last.  Found on the host from the same shape-only
+// schedule.
 struct MergeTasks {
     int n;
-    int4 task[kMaxCtas];  // (q-tile, c0, slot0, c_last)
+    int4 task[kMaxClusters];  // (pair tile, c0, slot0, c_last)
 };
 
-// blockIdx.x picks a cut q-tile, blockIdx.y 8 of its 128 rows; thread
-// (row, lane) merges 8 consecutive d.  Pieces are combined in CTA order (exact
-// log-sum-exp merge), so the result does not depend on timing.
+// blockIdx.x picks a cut pair tile, blockIdx.y 8 of its 256 rows; thread
+// (row, lane) merges 8 consecutive d.  Pieces are combined in pair order
+// (exact log-sum-exp merge), so the result does not depend on timing.  The
+// kernel is a programmatic dependent of the main kernel: its launch overlaps
+// that kernel's tail, and griddepcontrol.wait holds it until the partials are
+// complete.
 __global__ void __launch_bounds__(256)
 prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     const int4 tk = T.task[blockIdx.x];
     const int t = tk.x, c0 = tk.y, slot0 = tk.z, c_last = tk.w;
     const int r = blockIdx.y * 8 + (threadIdx.x >> 5);
-    const int m_row = t * BM + r;
+    const int m_row = t * BM2 + r;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (m_row >= P.M_total) return;
     const int d0 = (threadIdx.x & 31) * 8;
     float M = -INFINITY;
     for (int c = c0; c <= c_last; ++c) {
-        const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM + r;
+        const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM2 + r;
         M = fmaxf(M, P.ws_ml[prow * 2]);
     }
     float L = 0.f;
@@ -563,7 +707,7 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     for (int c = c0; c <= c_last; ++c) {
-        const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM + r;
+        const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM2 + r;
         const float mp = P.ws_ml[prow * 2];
         const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
         L += P.ws_ml[prow * 2 + 1] * w;
@@ -578,33 +722,69 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     *reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + d0) = hv;
 }
 
-// Host side of the schedule: the cut q-tiles and their pieces.
+// Host side of the schedule: the cut pair tiles and their pieces.
 static void find_cut_tiles(const Params& P, MergeTasks& T) {
     T.n = 0;
     long long cum = 0;
-    int c = 0;  // first CTA whose range ends after cum
-    for (int t = 0; t < P.num_qtiles; ++t) {
+    int c = 0;  // first pair whose range ends after cum
+    for (int t = 0; t < P.num_ptiles; ++t) {
         const int n = kv_tiles(t, P.Q, P.KV, P.M_total);
         const long long t_end = cum + n;
-        // CTA holding the tile's first iteration
-        while (c + 1 < P.G && cta_begin(P.total, P.G, c + 1) <= cum) ++c;
-        if (cta_begin(P.total, P.G, c + 1) < t_end) {  // the tile continues past CTA c
+        // pair holding the tile's first iteration
+        while (c + 1 < P.G && pair_begin(P.total, P.G, c + 1) <= cum) ++c;
+        if (pair_begin(P.total, P.G, c + 1) < t_end) {  // the tile continues past pair c
             int c_last = c + 1;
-            while (c_last + 1 < P.G && cta_begin(P.total, P.G, c_last + 1) < t_end) ++c_last;
-            const int slot0 = (cta_begin(P.total, P.G, c) == cum) ? 0 : 1;
+            while (c_last + 1 < P.G && pair_begin(P.total, P.G, c_last + 1) < t_end) ++c_last;
+            const int slot0 = (pair_begin(P.total, P.G, c) == cum) ? 0 : 1;
             T.task[T.n++] = make_int4(t, c, slot0, c_last);
         }
         cum = t_end;
     }
 }
 
+// Pairs that can be resident at once with this kernel's shared memory (the
+// SMs of a pair must share a GPC, so this can be below num_sms / 2).
+static int max_pairs(int device) {
+    static int cached[64] = {0};
+    if (device < 64 && cached[device]) return cached[device];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (n > kMaxClusters) n = kMaxClusters;
+    if (device < 64) cached[device] = n;
+    return n;
+}
+
 }  // namespace prefill
+
+int prefill_resident_pairs() {
+    const DeviceInfo* di = device_info();
+    if (!di) return -1;
+    if (cudaFuncSetAttribute(prefill::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             prefill::SMEM_BYTES) != cudaSuccess)
+        return -1;
+    return prefill::max_pairs(di->device);
+}
 
 size_t prefill_workspace_bytes(int Q, int KV, int num_sms) {
     (void)Q;
     (void)KV;
-    const size_t per_cta = (size_t)2 * prefill::BM * (prefill::D + 2) * sizeof(float);
-    return kWorkspaceCounterBytes + per_cta * (size_t)num_sms + 256;
+    const size_t per_pair = (size_t)2 * prefill::BM2 * (prefill::D + 2) * sizeof(float);
+    const size_t pairs = (size_t)(num_sms / 2 > 0 ? num_sms / 2 : 1);
+    return kWorkspaceCounterBytes + per_pair * pairs + 256;
 }
 
 int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
@@ -612,40 +792,6 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     using namespace prefill;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
-    Params P;
-    P.Q = Q;
-    P.KV = KV;
-    P.M_total = Q * HQ;
-    P.num_qtiles = (P.M_total + BM - 1) / BM;
-    long long total = 0;
-    for (int t = 0; t < P.num_qtiles; ++t) total += kv_tiles(t, Q, KV, P.M_total);
-    P.total = total;
-    P.G = (int)(total < di->num_sms ? total : di->num_sms);
-    if (P.G > kMaxCtas) P.G = kMaxCtas;
-    P.scale_log2 = scale * 1.4426950408889634f;
-    P.out = static_cast<__half*>(out);
-    P.err = di->err_word;
-
-    void* ws;
-    size_t ws_bytes;
-    current_workspace(&ws, &ws_bytes);
-    const size_t need = kWorkspaceCounterBytes + (size_t)P.G * 2 * BM * (D + 2) * sizeof(float);
-    if (P.G > 1 && (!ws || ws_bytes < need)) return GQA_ERR_WORKSPACE;
-    if (ws) {
-        float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
-        P.ws_o = w;
-        P.ws_ml = w + (size_t)P.G * 2 * BM * D;
-    } else {
-        P.ws_o = nullptr;
-        P.ws_ml = nullptr;
-    }
-
-    CUtensorMap tq, tk, tv;
-    if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, D, BM, 64) ||
-        !make_map_2d_f16(&tk, k, (uint64_t)KV, D, BN, 64) ||
-        !make_map_2d_f16(&tv, v, (uint64_t)KV, D, 32, 64))
-        return GQA_ERR_CUDA;
-
     static bool attr_done[64] = {false};
     if (di->device < 64 && !attr_done[di->device]) {
         if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -653,13 +799,60 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
             return GQA_ERR_CUDA;
         attr_done[di->device] = true;
     }
-    prefill_kernel<<<P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
+    const int pairs_max = max_pairs(di->device);
+    if (pairs_max < 1) return GQA_ERR_CUDA;
+    Params P;
+    P.Q = Q;
+    P.KV = KV;
+    P.M_total = Q * HQ;
+    P.num_ptiles = (P.M_total + BM2 - 1) / BM2;
+    long long total = 0;
+    for (int t = 0; t < P.num_ptiles; ++t) total += kv_tiles(t, Q, KV, P.M_total);
+    P.total = total;
+    int G = pairs_max < di->num_sms / 2 ? pairs_max : di->num_sms / 2;
+    if (G < 1) G = 1;
+    P.G = (int)(total < G ? total : G);
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.out = static_cast<__half*>(out);
+    P.err = di->err_word;
+
+    void* ws;
+    size_t ws_bytes;
+    current_workspace(&ws, &ws_bytes);
+    const size_t need = kWorkspaceCounterBytes + (size_t)P.G * 2 * BM2 * (D + 2) * sizeof(float);
+    if (P.G > 1 && (!ws || ws_bytes < need)) return GQA_ERR_WORKSPACE;
+    if (ws) {
+        float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
+        P.ws_o = w;
+        P.ws_ml = w + (size_t)P.G * 2 * BM2 * D;
+    } else {
+        P.ws_o = nullptr;
+        P.ws_ml = nullptr;
+    }
+
+    CUtensorMap tq, tk, tv;
+    if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, D, BM, 64) ||
+        !make_map_2d_f16(&tk, k, (uint64_t)KV, D, BN / 2, 64) ||
+        !make_map_2d_f16(&tv, v, (uint64_t)KV, D, 32, 64))
+        return GQA_ERR_CUDA;
+
+    prefill_kernel<<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     MergeTasks tasks;  // passed to the merge kernel by value
     find_cut_tiles(P, tasks);
     if (tasks.n > 0) {
-        prefill_merge_kernel<<<dim3(tasks.n, BM / 8), 256, 0, stream>>>(P, tasks);
-        if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(tasks.n, BM2 / 8);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel, P, tasks) != cudaSuccess)
+            return GQA_ERR_CUDA;
     }
     return GQA_OK;
 }
