@@ -191,9 +191,12 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                  ::: "memory");
 }
+// Arrive on an mbarrier of the even CTA (default .release.cta semantics: the
+// tensor-memory writes this signals are ordered by tcgen05.wait::st and
+// tcgen05.fence::before_thread_sync, not by the arrive; a cluster-scope
+// release here costs about a microsecond per tile).
 __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair.
@@ -595,7 +598,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) remote_arrive(leader_addr(bar_pfull(s_bars, gg & 1)));
+                if (lane == 0) {
+                    if (leader) mbar_arrive(bar_pfull(s_bars, gg & 1));
+                    else remote_arrive(leader_addr(bar_pfull(s_bars, gg & 1)));
+                }
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
