@@ -390,11 +390,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             uint32_t g = 0;
             int seg = 0;
             bool ok = true;
+            // A landed K / V slot: the copy and the UMMA that reads it are both
+            // async-proxy operations ordered by the mbarrier's completion, so no
+            // tcgen05 fence is needed here (the issuing thread's time between
+            // UMMAs is what keeps the tensor pipe fed).
             auto take = [&](Ring& rg, int& slot) -> bool {
                 slot = rg.slot();
-                if (!mbar_wait(bar_full(s_bars, slot), rg.phase(), abort_flag, P.err)) return false;
-                tc_fence_after();
-                return true;
+                return mbar_wait(bar_full(s_bars, slot), rg.phase(), abort_flag, P.err);
             };
             auto issue_qk = [&](uint32_t s_col) -> bool {
                 for (int h = 0; h < 2; ++h) {
