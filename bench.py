@@ -164,6 +164,24 @@ def time_steps(fn, steps, warmup, flush, stream):
     return times
 
 
+def profiled_traffic(profile: str, source: str, key: str = "traffic_bytes_per_launch"):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that
+    the ncu summary profiles/<profile> records, or None when the summary is
+    missing or was taken on a different version of the kernel source (its
+    source_sha256 line does not match)."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        digest = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
+    except OSError:
+        return None
+    vals = dict(re.findall(r"^(\w+):\s*(\S+)\s*$", text, re.M))
+    if vals.get("source_sha256") != digest or key not in vals:
+        return None
+    return int(vals[key])
+
+
 def make_flush(device):
     """L2 flush run before every timed step: write a 256 MB buffer (twice the
     L2), then read a second 256 MB buffer.  The read replaces the write's dirty
@@ -342,7 +360,11 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} bf16 dense burst (fp16 same nominal rate)",
-                     "traffic": None,
+                     "traffic": profiled_traffic("prefill_kernel_Q8000_KV40000.md",
+                                                 "long_context_causal_gqa_gb300/csrc/prefill.cu")
+                     if (Q, KV) == (Q_MAIN, KV_MAIN) else None,
+                     "traffic_note": "DRAM bytes per launch of prefill_kernel from the ncu "
+                                     "summary in profiles/, null if taken on other source",
                      "note": "achieved = causal-visible FLOPs / CUDA-event time of one step "
                              "(main kernel + merge)"},
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -375,7 +397,12 @@ def run_gpu(args):
             secondary.append({"what": f"paged E4M3 tail R={R} ctx=261888 (graph replay)",
                               "us": round(us, 2), "GB/s": round(gbs, 1),
                               "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-                              "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 1)})
+                              "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 1),
+                              "algorithmic_bytes": nbytes,
+                              "traffic": profiled_traffic(
+                                  "paged_split_kernel_ctx261888.md",
+                                  "long_context_causal_gqa_gb300/csrc/paged_e4m3.cu",
+                                  f"traffic_bytes_per_launch_R{R}")})
         for T in (64, 512, 2048):
             try:
                 t, gathered, fl = bench_sparse(binding, T, device, 5, 2, flush)
