@@ -62,8 +62,14 @@ constexpr int HQ = kHq;         // 6
 // (8 KB each, two 64-wide atoms of 4 KB).  A tile's half of K or V is two slots.
 constexpr int SLOT_BYTES = 16384;
 constexpr int HALF_SLOT = SLOT_BYTES / 2;
-constexpr int NK = 4;                         // K slots (two tiles)
-constexpr int NV = 5;                         // V slots
+#ifndef GQA_PREFILL_NK
+#define GQA_PREFILL_NK 4
+#endif
+#ifndef GQA_PREFILL_NV
+#define GQA_PREFILL_NV 5
+#endif
+constexpr int NK = GQA_PREFILL_NK;            // K slots (two per tile)
+constexpr int NV = GQA_PREFILL_NV;            // V slots (two per tile)
 constexpr int Q_BYTES = BM * D * 2;           // 64 KB
 constexpr int RING_BYTES = (NK + NV) * SLOT_BYTES;
 constexpr int NWG = 2;                        // softmax warpgroups per CTA
