@@ -88,13 +88,16 @@ struct Layout {
     static constexpr int NT = 3;                      // E4M3 expansion terms
     static constexpr int N3 = NT * NP;                // UMMA N
     static constexpr int NS = (NP <= 32) ? 2 : 1;     // S^T buffers in tensor memory
-    static constexpr int NRAW = (NP <= 16) ? 6 : (NP <= 32) ? 5 : 4;   // raw K/V stages
+    // P^T buffers: two up to 32 packed rows; at 48 one, so that a fifth raw
+    // stage fits (the copy stream's rate is set by its bytes in flight).
+    static constexpr int NPT = (NP <= 32) ? 2 : 1;
+    static constexpr int NRAW = (NP <= 16) ? 6 : 5;   // raw K/V stages
     static constexpr int Q_BYTES = N3 * D;            // [Q1|Q2|Q3]: N3 rows x 256 B, 2 halves
     static constexpr int PT_BYTES = N3 * TILE;        // [P1|P2|P3]^T: N3 rows x 128 keys
     static constexpr int OFF_RAW = 0;
     static constexpr int OFF_Q = OFF_RAW + NRAW * RAW_STAGE;
     static constexpr int OFF_PT = OFF_Q + Q_BYTES;
-    static constexpr int OFF_QS = OFF_PT + 2 * PT_BYTES;        // [NP] per-row Q scales
+    static constexpr int OFF_QS = OFF_PT + NPT * PT_BYTES;      // [NP] per-row Q scales
     static constexpr int OFF_RED = OFF_QS + NP * 4;             // [4 NWG warps][NP] floats
     static constexpr int OFF_MREF = OFF_RED + 4 * NWG * NP * 4;  // [NP] floats
     static constexpr int OFF_FAC = OFF_MREF + NP * 4;            // [NP] floats
@@ -118,8 +121,8 @@ enum {
     B_RAW_FULL = 0,               // [MAX_RAW]
     B_RAW_EMPTY = MAX_RAW,        // [MAX_RAW]
     B_S_FULL = 2 * MAX_RAW,       // [2]
-    B_P_READY = 2 * MAX_RAW + 2,  // [2]
-    B_PT_EMPTY = 2 * MAX_RAW + 4, // [2] P.V of that P^T buffer done
+    B_P_READY = 2 * MAX_RAW + 2,  // [NPT]
+    B_PT_EMPTY = 2 * MAX_RAW + 4, // [NPT] P.V of that P^T buffer done
     B_DRAIN = 2 * MAX_RAW + 6,
     B_GROUP = 2 * MAX_RAW + 7,    // [MAX_WG] per softmax warpgroup
     B_S_FREE = 2 * MAX_RAW + 7 + MAX_WG,  // single S^T buffer read by the softmax
@@ -171,6 +174,30 @@ __device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& t1, 
     t2 = e4m3x2(r0, r1);
     e4m3x2_val(t2, a0, a1);
     t3 = e4m3x2((r0 - a0) * 16.f, (r1 - a1) * 16.f);
+}
+
+// Two fp32 values rounded to fp16, then split as h = t1 + t2 / 16 + t3 / 256
+// with t1, t2, t3 E4M3 (each result holds the pair's two bytes in its low 16
+// bits).  Differences and the scalings by 16 are exact in fp16, and three
+// 4-bit terms cover fp16's 11 significant bits, so the three terms carry the
+// fp16 value (down to E4M3's smallest subnormal in the last term).
+__device__ __forceinline__ void split3_e4m3_h2(float x0, float x1, uint32_t& t1, uint32_t& t2,
+                                               uint32_t& t3) {
+    uint32_t h, b, r;
+    uint16_t a;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(h));
+    t1 = a;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(a));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(b));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x4C004C00u));   // x 16
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(r));
+    t2 = a;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(a));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(b));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x4C004C00u));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(r));
+    t3 = a;
 }
 
 // Byte offset of 16-byte unit u (0..7) of row r inside a 128B-swizzled block.
@@ -258,6 +285,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     constexpr int N3 = L::N3;    // UMMA N: three expansion terms
     constexpr int NS = L::NS;
     constexpr int NRAW = L::NRAW;
+    constexpr int NPT = L::NPT;
     // E4M3 x E4M3 -> f32 (format fields 0 = E4M3 for kind::f8f6f4).
     constexpr uint32_t IDESC_QK = idesc_f16_f32(128, N3, false, false);
     constexpr uint32_t IDESC_PV = idesc_f16_f32(128, N3, true, false);   // A = V^T, MN-major
@@ -447,14 +475,14 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 auto stage_of = [](int item) { return item % NRAW; };
                 auto phase_of = [](int item) { return (uint32_t)((item / NRAW) & 1); };
                 auto issue_pv = [&](int x) -> bool {
-                    if (!mbar_wait(bar(B_P_READY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
+                    if (!mbar_wait(bar(B_P_READY + x % NPT), (x / NPT) & 1, abort_flag, P.err))
                         return false;
                     const int vi = item_v(x, ntl);
                     if (!mbar_wait(bar(B_RAW_FULL + stage_of(vi)), phase_of(vi), abort_flag, P.err))
                         return false;
                     tc_fence_after();
                     const uint32_t vst = s_raw + stage_of(vi) * RAW_STAGE;
-                    const uint32_t pt = s_pt + (x & 1) * L::PT_BYTES;
+                    const uint32_t pt = s_pt + (x % NPT) * L::PT_BYTES;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -465,7 +493,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                             umma_f8(tmem + L::O_COL + h * N3, a, b, IDESC_PV, (x > 0 || ks > 0));
                         }
                     }
-                    umma_commit(bar(B_PT_EMPTY + (x & 1)));
+                    umma_commit(bar(B_PT_EMPTY + x % NPT));
                     umma_commit(bar(B_RAW_EMPTY + stage_of(vi)));
                     return true;
                 };
@@ -521,9 +549,19 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             float lpart[NH];
 #pragma unroll
             for (int c = 0; c < NH; ++c) lpart[c] = 0.f;
+            // P^T store offsets: key k of row r = term * NP + c0 + c sits at byte
+            // r * 128 + (((k >> 4) ^ (r & 7)) << 4) + (k & 15); c0 and NP are
+            // multiples of 8, so r & 7 == c and the swizzled part depends only on
+            // (k, c).
+            static_assert(NH == 8 && NP % 8 == 0, "P^T store layout");
+            const uint32_t p_row0 = (uint32_t)c0 * 128u + ((uint32_t)k & 15u);
+            const uint32_t p_unit = ((uint32_t)k >> 4) << 4;
+            auto pofs = [&](int c) -> uint32_t {
+                return p_row0 + (uint32_t)c * 128u + (p_unit ^ ((uint32_t)c << 4));
+            };
             bool ok = ntl > 0;
             for (int jj = 0; jj < ntl && ok; ++jj) {
-                const int b = jj & 1;            // P^T buffer
+                const int b = jj % NPT;          // P^T buffer
                 const int sb = jj % NS;          // S^T buffer
                 ok = mbar_wait(bar(B_S_FULL + sb), (uint32_t)((jj / NS) & 1), abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
@@ -599,7 +637,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     if (jj > 0) {
                         // O^T must hold every earlier P.V before it is rescaled.
                         const int x = jj - 1;
-                        ok = mbar_wait(bar(B_PT_EMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                        ok = mbar_wait(bar(B_PT_EMPTY + x % NPT), (x / NPT) & 1, abort_flag, P.err);
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                         tc_fence_after();
@@ -637,8 +675,8 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                                 make_uint4(0, 0, 0, 0);
                     }
                 }
-                // P^T buffer b is free once the P.V two tiles back has completed.
-                ok = mbar_wait(bar(B_PT_EMPTY + b), ((jj >> 1) & 1) ^ 1, abort_flag, P.err);
+                // P^T buffer b is free once the P.V NPT tiles back has completed.
+                ok = mbar_wait(bar(B_PT_EMPTY + b), ((jj / NPT) & 1) ^ 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 {
@@ -652,12 +690,11 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                         lpart[c] += p0;
                         lpart[c + 1] += p1;
                         uint32_t t[3];
-                        split3_e4m3x2(p0, p1, t[0], t[1], t[2]);
-                        const int r0 = c0 + c;
+                        split3_e4m3_h2(p0, p1, t[0], t[1], t[2]);
 #pragma unroll
                         for (int e = 0; e < 3; ++e) {
-                            pt[sw128(e * NP + r0, k >> 4) + (k & 15)] = (uint8_t)(t[e] & 0xFF);
-                            pt[sw128(e * NP + r0 + 1, k >> 4) + (k & 15)] = (uint8_t)(t[e] >> 8);
+                            pt[pofs(c) + e * NP * 128] = (uint8_t)(t[e] & 0xFF);
+                            pt[pofs(c + 1) + e * NP * 128] = (uint8_t)(t[e] >> 8);
                         }
                     }
                 }
@@ -667,7 +704,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             // ---------------------------------------------------------- epilogue
             if (ok && ntl > 0) {
                 const int x = ntl - 1;
-                ok = mbar_wait(bar(B_PT_EMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                ok = mbar_wait(bar(B_PT_EMPTY + x % NPT), (x / NPT) & 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
             }
             if (ok && ntl > 0) {
