@@ -232,6 +232,33 @@ __device__ __forceinline__ void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, u
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Shared-memory descriptors split into their two 32-bit words: the high word
+// (SBO = 1024, version bit 46, 128-byte swizzle) is the same for every
+// operand here; the low word is (address >> 4) | (LBO >> 4) << 16, so an
+// operand at a fixed offset from a slot base is one integer add away.
+constexpr uint32_t DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+    return (saddr >> 4) | ((lbo >> 4) << 16);
+}
+__device__ __forceinline__ uint64_t desc64(uint32_t lo) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(DESC_HI));
+    return d;
+}
+// UMMA with a compile-time accumulate flag (no predicate set-up).
+template <bool ACC>
+__device__ __forceinline__ void umma_ss_pair_c(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc) {
+    if constexpr (ACC)
+        asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc)
+                     : "memory");
+    else
+        asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc)
+                     : "memory");
+}
+
 // Arrive once on the mbarrier at this offset in both CTAs of the pair when
 // every UMMA this thread issued before has completed.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
@@ -404,21 +431,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 slot = rg.slot();
                 return mbar_wait(bar_full(s_bars, slot), rg.phase(), abort_flag, P.err);
             };
+            // Descriptor low words: Q chunk c at q_lo + c * (BM * 128 >> 4); a K
+            // slot's chunk cc at + cc * (HALF_SLOT >> 4); a K step of 16
+            // elements (32 bytes) at + 2.
+            const uint32_t q_lo = desc_lo(s_q, 16);
             auto issue_qk = [&](uint32_t s_col) -> bool {
+                const uint32_t d = tmem + s_col;
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     int slot;
                     if (!take(kr, slot)) return false;
-                    const uint32_t kaddr = s_ring + slot * SLOT_BYTES;
+                    const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
                         const int c = 2 * h + cc;
-                        const uint32_t qaddr = s_q + c * (BM * 128);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = sdesc_sw128(qaddr + kk * 32, 16, 1024);
-                            const uint64_t b =
-                                sdesc_sw128(kaddr + cc * HALF_SLOT + kk * 32, 16, 1024);
-                            umma_ss_pair(tmem + s_col, a, b, IDESC_QK, (c | kk) != 0);
+                            const uint64_t a = desc64(q_lo + c * ((BM * 128) >> 4) + kk * 2);
+                            const uint64_t b = desc64(k_lo + cc * (HALF_SLOT >> 4) + kk * 2);
+                            if (c == 0 && kk == 0)
+                                umma_ss_pair_c<false>(d, a, b, IDESC_QK);
+                            else
+                                umma_ss_pair_c<true>(d, a, b, IDESC_QK);
                         }
                     }
                     umma_commit_pair(bar_empty(s_bars, slot));
@@ -427,21 +461,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 return true;
             };
             auto issue_pv = [&](uint32_t s_col, bool acc0) -> bool {
+                const uint32_t p_base = tmem + s_col;
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     int slot;
                     if (!take(vr, slot)) return false;
-                    const uint32_t vaddr = s_ring + slot * SLOT_BYTES;
+                    // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
+                    // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
+                    const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
 #pragma unroll
                     for (int ss = 0; ss < 2; ++ss) {
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks) {
-                            const uint64_t b =
-                                sdesc_sw128(vaddr + ss * HALF_SLOT + ks * 2048, 4096, 1024);
+                            const uint64_t b = desc64(v_lo + ss * (HALF_SLOT >> 4) + ks * (2048 >> 4));
                             // P of keys kb .. kb + 15: part kb / COLS sits at columns
                             // COLS (kb / COLS) + (kb % COLS) / 2 of the S buffer.
                             const int kb = (2 * h + ss) * 32 + ks * 16;
-                            const uint32_t a_tmem =
-                                tmem + s_col + (kb / COLS) * COLS + (kb % COLS) / 2;
+                            const uint32_t a_tmem = p_base + (kb / COLS) * COLS + (kb % COLS) / 2;
                             umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV,
                                          (acc0 || h || ss || ks) ? 1u : 0u);
                         }
