@@ -214,15 +214,6 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void umma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 __device__ __forceinline__ void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -256,6 +247,19 @@ __device__ __forceinline__ void umma_ss_pair_c(uint32_t d_tmem, uint64_t a_desc,
     else
         asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc)
+                     : "memory");
+}
+
+template <bool ACC>
+__device__ __forceinline__ void umma_ts_pair_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc) {
+    if constexpr (ACC)
+        asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+                     "r"(a_tmem), "l"(b_desc), "r"(idesc)
+                     : "memory");
+    else
+        asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
+                     "r"(a_tmem), "l"(b_desc), "r"(idesc)
                      : "memory");
 }
 
@@ -478,8 +482,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             // COLS (kb / COLS) + (kb % COLS) / 2 of the S buffer.
                             const int kb = (2 * h + ss) * 32 + ks * 16;
                             const uint32_t a_tmem = p_base + (kb / COLS) * COLS + (kb % COLS) / 2;
-                            umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV,
-                                         (acc0 || h || ss || ks) ? 1u : 0u);
+                            if (h == 0 && ss == 0 && ks == 0)
+                                umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV, acc0 ? 1u : 0u);
+                            else
+                                umma_ts_pair_c<true>(tmem + O_COL, a_tmem, b, IDESC_PV);
                         }
                     }
                     umma_commit_pair(bar_empty(s_bars, slot));
