@@ -66,6 +66,7 @@ typedef enum {
 #define GQA_DEVERR_WAIT_TIMEOUT 0x1u  /* a pipeline wait exceeded its limit; output invalid */
 #define GQA_DEVERR_BAD_BLOCK_ID 0x2u  /* sel_idx held an id < 0 or past the row's own block */
 #define GQA_DEVERR_BAD_PAGE_ID  0x4u  /* a block-table entry was < 0 or >= num_pages */
+#define GQA_DEVERR_BAD_CTX_LEN  0x8u  /* a device-side ctx_len was < query_rows or > max_ctx_len */
 
 /* Dense causal prefill [P1, Purpose].
  *   q   [Q, Hq, D]  fp16     k, v [KV, Hkv, D] fp16     out [Q, Hq, D] fp16
@@ -88,11 +89,34 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
  *   page = 16; query_rows <= ctx_len <= num_pages * page.
  * Tail row r sits at position ctx_len - query_rows + r.  The key range is
  * split over all SMs; each split's (O, m, l) partial goes to the workspace
- * and the last split to finish merges them in a fixed order. */
+ * and a second kernel on the same stream merges them in a fixed order. */
 int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                         const float* kscale, const float* vscale, const int32_t* block_table,
                         int num_pages, int page, int ctx_len, int query_rows, int Hq, int Hkv,
                         int D, float scale, void* out, struct CUstream_st* stream);
+
+/* Paged FP8-E4M3 verifier tail whose context length is read on the device
+ * when the kernels run ([P2] Changes: the tail CUDA graph is captured once for
+ * a bound and replayed while the context grows).  Same arguments, layouts and
+ * result as gqa_attn_paged_e4m3, except:
+ *   ctx_len_dev  device pointer to one int32, the context length used by this
+ *                launch (and by every replay of a graph that captured it);
+ *                4-byte aligned.
+ *   max_ctx_len  host bound: query_rows <= max_ctx_len <= num_pages * page.
+ *                The grid, the workspace size (gqa_workspace_bytes with
+ *                ctx_or_kv = max_ctx_len) and the part of block_table that may
+ *                be read ([ceil(max_ctx_len / page)] entries) follow it.
+ * A device value below query_rows or above max_ctx_len is clamped into that
+ * range and flags GQA_DEVERR_BAD_CTX_LEN.  Splits that the actual context
+ * leaves without keys publish empty partials, so the result equals
+ * gqa_attn_paged_e4m3 at the same context up to the order of the split merge
+ * (the split boundaries depend on max_ctx_len only through the SM count). */
+int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                               const float* kscale, const float* vscale,
+                               const int32_t* block_table, int num_pages, int page,
+                               const int32_t* ctx_len_dev, int max_ctx_len, int query_rows,
+                               int Hq, int Hkv, int D, float scale, void* out,
+                               struct CUstream_st* stream);
 
 /* Paged FP8-E4M3 verifier tail that allocates nothing (no counterpart in the
  * pages; an addition of this library).  Some callers cannot call cudaMalloc:

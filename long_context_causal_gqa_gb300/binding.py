@@ -32,9 +32,11 @@ KIND_SPARSE = 2
 DEVERR_WAIT_TIMEOUT = 0x1
 DEVERR_BAD_BLOCK_ID = 0x2
 DEVERR_BAD_PAGE_ID = 0x4
+DEVERR_BAD_CTX_LEN = 0x8
 
 # Every symbol include/gqa_attn.h declares.
-EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_noalloc",
+EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_devctx",
+            "gqa_attn_paged_e4m3_noalloc",
             "gqa_attn_sparse_blocks",
             "gqa_workspace_bytes", "gqa_set_workspace", "gqa_get_device_error",
             "gqa_prefill_sm_pairs", "gqa_status_string")
@@ -64,6 +66,9 @@ def load():
             lib.gqa_attn_prefill.restype = I
             lib.gqa_attn_paged_e4m3.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
             lib.gqa_attn_paged_e4m3.restype = I
+            lib.gqa_attn_paged_e4m3_devctx.argtypes = [P, P, P, P, P, P, I, I, P, I, I, I, I, I,
+                                                       F, P, P]
+            lib.gqa_attn_paged_e4m3_devctx.restype = I
             lib.gqa_attn_paged_e4m3_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I,
                                                         F, P, P]
             lib.gqa_attn_paged_e4m3_noalloc.restype = I
@@ -194,6 +199,31 @@ def paged_e4m3(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
                                         int(ctx_len), R, Hq, Hkv, D, float(scale), _ptr(out),
                                         _stream_ptr(stream))
     _check(st, "gqa_attn_paged_e4m3")
+    return out
+
+
+def paged_e4m3_devctx(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                      kscale: torch.Tensor, vscale: torch.Tensor, block_table: torch.Tensor,
+                      ctx_len_dev: torch.Tensor, max_ctx_len: int, scale: float = 1.0 / 16,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Paged E4M3 tail with the context length read on the device when the
+    kernels run: ctx_len_dev is a one-element int32 CUDA tensor, max_ctx_len
+    the host bound that sizes the grid and the workspace."""
+    dev = _need_cuda(q, kcache, vcache, kscale, vscale, block_table, ctx_len_dev)
+    if ctx_len_dev.dtype != torch.int32 or ctx_len_dev.numel() < 1:
+        raise GQAError(GQA_ERR_INVALID_ARG, "ctx_len_dev must be a CUDA int32 tensor")
+    R, Hq, D = q.shape
+    num_pages, page, Hkv, _ = kcache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    with torch.cuda.device(dev):
+        ensure_workspace(workspace_bytes(KIND_PAGED_E4M3, R, max_ctx_len, Hq, D), dev)
+        st = load().gqa_attn_paged_e4m3_devctx(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kscale),
+                                               _ptr(vscale), _ptr(block_table), num_pages, page,
+                                               _ptr(ctx_len_dev), int(max_ctx_len), R, Hq, Hkv, D,
+                                               float(scale), _ptr(out), _stream_ptr(stream))
+    _check(st, "gqa_attn_paged_e4m3_devctx")
     return out
 
 

@@ -145,7 +145,29 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
     if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, ctx_len,
-                             query_rows, scale, out, stream);
+                             nullptr, query_rows, scale, out, stream);
+}
+
+int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                               const float* kscale, const float* vscale,
+                               const int32_t* block_table, int num_pages, int page,
+                               const int32_t* ctx_len_dev, int max_ctx_len, int query_rows,
+                               int Hq, int Hkv, int D, float scale, void* out,
+                               struct CUstream_st* stream) {
+    if (!q || !kcache || !vcache || !kscale || !vscale || !block_table || !ctx_len_dev || !out)
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale) |
+         reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(ctx_len_dev)) &
+        3u)
+        return GQA_ERR_INVALID_ARG;
+    if (query_rows < 1 || max_ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if ((long long)max_ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
+    return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages,
+                             max_ctx_len, ctx_len_dev, query_rows, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,

@@ -55,8 +55,8 @@ int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill k
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
-                      int num_pages, int ctx_len, int R, float scale, void* out,
-                      cudaStream_t stream);
+                      int num_pages, int ctx_len, const int* ctx_dev, int R, float scale,
+                      void* out, cudaStream_t stream);
 size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms);
 
 // Same as paged_e4m3_launch, with the split partials in a static device array.

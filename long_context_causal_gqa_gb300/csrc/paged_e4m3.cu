@@ -75,6 +75,7 @@ struct Params {
     const float* vscale;
     const int32_t* table;
     const __half* q;
+    const int* ctx_dev;   // device-side ctx_len (nullptr: use ctx_len)
     int num_pages, ctx_len, R, nq, n_tiles, G;
     float scale;
     float* ws_o;    // [G][nq][D] unnormalised partial O (in units of the E4M3 V)
@@ -309,10 +310,25 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x;
-    const int t_begin = (int)((long long)split * P.n_tiles / P.G);
-    const int t_end = (int)((long long)(split + 1) * P.n_tiles / P.G);
+    // Context length: the launch's, or read on the device (the grid is then
+    // sized for the largest context, P.ctx_len, and splits past the actual
+    // context get no tiles).  A device value outside [R, P.ctx_len] is
+    // clamped and flagged.
+    int ctx_len = P.ctx_len;
+    if (P.ctx_dev) {
+        const int c = *P.ctx_dev;
+        if (c < P.R || c > P.ctx_len) {
+            if (threadIdx.x == 0 && split == 0) atomicOr(P.err, kErrBadCtxLen);
+            ctx_len = c < P.R ? P.R : P.ctx_len;
+        } else {
+            ctx_len = c;
+        }
+    }
+    const int n_tiles = (ctx_len + TILE - 1) / TILE;
+    const int t_begin = (int)((long long)split * n_tiles / P.G);
+    const int t_end = (int)((long long)(split + 1) * n_tiles / P.G);
     const int ntl = t_end - t_begin;
-    const int n_logical = (P.ctx_len + PAGE - 1) / PAGE;
+    const int n_logical = (ctx_len + PAGE - 1) / PAGE;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NRAW; ++s) {
@@ -540,7 +556,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const int k = wq * 32 + lane;                       // TMEM lane = key in tile = d in O^T half
             const int c0 = hg * NH;
             const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-            const int lim_base = P.ctx_len - P.R;               // row r sees keys <= lim_base + r
+            const int lim_base = ctx_len - P.R;                 // row r sees keys <= lim_base + r
             const uint32_t gbar = bar(B_GROUP + hg);
             uint32_t gphase = 0;
             float sl2[NH];
@@ -592,7 +608,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
                     for (int c = 0; c < NH; ++c) {
                         const int cg = c0 + c;
-                        const bool vis = (cg < P.nq) ? (key <= lim_base + cg / HQ) : (key < P.ctx_len);
+                        const bool vis = (cg < P.nq) ? (key <= lim_base + cg / HQ) : (key < ctx_len);
                         if (!vis) s[c] = -INFINITY;
                     }
                 }
@@ -662,13 +678,13 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 // held, possibly the E4M3 NaN code; zero their V rows so that
                 // P = 0 times V stays 0.  Each warpgroup clears its share of the
                 // row's sixteen 16-byte units (both halves of d).
-                if (t_begin + jj == P.n_tiles - 1 && (P.ctx_len & (TILE - 1)) != 0) {
+                if (t_begin + jj == n_tiles - 1 && (ctx_len & (TILE - 1)) != 0) {
                     const int vi = item_v(jj, ntl);
                     ok = mbar_wait(bar(B_RAW_FULL + vi % NRAW), (uint32_t)((vi / NRAW) & 1), abort_flag,
                                    P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    if (key >= P.ctx_len) {
+                    if (key >= ctx_len) {
                         uint8_t* st = gbase + L::OFF_RAW + (vi % NRAW) * RAW_STAGE + k * 128;
                         for (int u = hg * 16 / NWG; u < (hg + 1) * 16 / NWG; ++u)
                             *reinterpret_cast<uint4*>(st + (u >> 3) * (TILE * 128) + (u & 7) * 16) =
@@ -746,6 +762,13 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                                      fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c])));
                 }
             }
+            if (ntl == 0 && k < NH && c0 + k < P.nq) {
+                // A split with no tiles (a device-side context shorter than the
+                // one the grid was sized for): a partial the merge gives zero
+                // weight; its O is never read.
+                P.ws_ml[((size_t)split * P.nq + c0 + k) * 2 + 0] = -INFINITY;
+                P.ws_ml[((size_t)split * P.nq + c0 + k) * 2 + 1] = 0.f;
+            }
         }
 
     }
@@ -822,23 +845,26 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     for (int o2 = 16; o2 > 0; o2 >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o2);
     if (lane == 0) wred[1][warp] = lsum;
     __syncthreads();
+    // A zero weight (a split that saw no visible key, or none at all) skips
+    // its O, which may hold anything.
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float w, const float4& v) {
+        if (w != 0.f) {
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+    };
 #pragma unroll
     for (int i = 0; i < MERGE_PF; ++i) {
         const int s = warp + MERGE_WARPS * i;
-        const float w = s < G ? w_s[s] : 0.f;
-        acc.x = fmaf(w, o[i].x, acc.x);
-        acc.y = fmaf(w, o[i].y, acc.y);
-        acc.z = fmaf(w, o[i].z, acc.z);
-        acc.w = fmaf(w, o[i].w, acc.w);
+        add(s < G ? w_s[s] : 0.f, o[i]);
     }
     for (int s = warp + MERGE_WARPS * MERGE_PF; s < G; s += MERGE_WARPS) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0));
         const float w = w_s[s];
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        if (w != 0.f)
+            add(w, __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0)));
     }
     red[warp][lane] = acc;
     __syncthreads();
@@ -914,8 +940,8 @@ size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms) {
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
-                      int num_pages, int ctx_len, int R, float scale, void* out,
-                      cudaStream_t stream) {
+                      int num_pages, int ctx_len, const int* ctx_dev, int R, float scale,
+                      void* out, cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -926,6 +952,7 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.vscale = vscale;
     P.table = block_table;
     P.q = static_cast<const __half*>(q);
+    P.ctx_dev = ctx_dev;
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
@@ -1007,6 +1034,7 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.vscale = vscale;
     P.table = block_table;
     P.q = static_cast<const __half*>(q);
+    P.ctx_dev = nullptr;
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;

@@ -16,6 +16,7 @@ namespace gqa {
 constexpr unsigned kErrWaitTimeout = 0x1u;
 constexpr unsigned kErrBadBlockId = 0x2u;
 constexpr unsigned kErrBadPageId = 0x4u;
+constexpr unsigned kErrBadCtxLen = 0x8u;
 
 // A pipeline wait that has not completed after this long means a bug; the
 // kernel records kErrWaitTimeout and unwinds instead of spinning forever.

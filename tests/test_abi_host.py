@@ -81,6 +81,21 @@ def test_paged_rejects_bad_arguments(lib):
     assert _paged(lib, scale=-1.0) == binding.GQA_ERR_INVALID_ARG
 
 
+def _paged_dev(lib, R=2, max_ctx=100, pages=8, ctxp=FAKE, page=16, scale=0.0625):
+    return lib.gqa_attn_paged_e4m3_devctx(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, pages, page, ctxp,
+                                          max_ctx, R, 6, 1, 256, scale, FAKE, None)
+
+
+def test_paged_devctx_rejects_bad_arguments(lib):
+    assert _paged_dev(lib, ctxp=P(0)) == binding.GQA_ERR_INVALID_ARG
+    assert _paged_dev(lib, ctxp=P(0x10002)) == binding.GQA_ERR_INVALID_ARG   # not 4-byte aligned
+    assert _paged_dev(lib, R=3, max_ctx=2) == binding.GQA_ERR_INVALID_ARG
+    assert _paged_dev(lib, max_ctx=200, pages=8) == binding.GQA_ERR_INVALID_ARG
+    assert _paged_dev(lib, R=9, max_ctx=100) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged_dev(lib, page=8) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged_dev(lib, scale=0.0) == binding.GQA_ERR_INVALID_ARG
+
+
 def _sparse(lib, rows=4, ctx=64, pages=4, max_sel=4, sel=FAKE, D=256):
     return lib.gqa_attn_sparse_blocks(FAKE, FAKE, FAKE, FAKE, sel, FAKE, max_sel, pages, 16,
                                       ctx, rows, 6, 1, D, 0.0625, FAKE, None)

@@ -103,3 +103,70 @@ def test_paged_bad_page_id_sets_device_error(cuda_lib):
     err = cuda_lib.device_error()
     assert err & cuda_lib.DEVERR_BAD_PAGE_ID
     assert cuda_lib.device_error() == 0  # read clears it
+
+
+def _poison_past(kc_dev, vc_dev, bt, ctx_len, max_ctx):
+    """Write the E4M3 NaN code into every cached token in [ctx_len, max_ctx)."""
+    t = torch.arange(ctx_len, max_ctx)
+    pg, slot = bt[t // 16].long(), t % 16
+    kc_dev[pg, slot] = 0x7F
+    vc_dev[pg, slot] = 0x7F
+
+
+@pytest.mark.parametrize("R", [1, 5, 8])
+def test_paged_devctx_graph_replay_at_growing_context(cuda_lib, R):
+    """One graph captured at the bound, replayed with the context length
+    changed on the device ([P2] Changes: tail graphs replayed as the context
+    grows); tokens past each context are NaN-poisoned and must not matter."""
+    max_ctx, cap = 9000, 9216
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=max_ctx, capacity=cap, seed=40 + R)
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    ctx_dev = torch.tensor([max_ctx], dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, max_ctx, p.scale, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, max_ctx, p.scale, out=out)
+    kc_host, vc_host = p.kcache.clone(), p.vcache.clone()
+    for ctx in [max_ctx, 8999, 7000, 4097, 4096, 1000, 129, 128, 8 + R]:
+        _poison_past(kc_host, vc_host, p.block_table, ctx, max_ctx)
+        kc.copy_(kc_host)
+        vc.copy_(vc_host)
+        ctx_dev.fill_(ctx)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert cuda_lib.device_error() == 0
+        ref = oracle.paged_e4m3(p.q, kc_host, vc_host, p.kscale, p.vscale, p.block_table, ctx,
+                                p.scale)
+        _check(out, ref, f"R={R} device ctx={ctx}")
+
+
+def test_paged_devctx_equals_host_ctx(cuda_lib):
+    p = inputs.paged_e4m3_inputs(R=4, ctx_len=20000, capacity=20480, seed=77)
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    a = cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale)
+    ctx_dev = torch.tensor([p.ctx_len], dtype=torch.int32, device=dev)
+    b = cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, p.ctx_len, p.scale)
+    torch.cuda.synchronize()
+    # Same grid and split boundaries when max_ctx_len == ctx_len: bitwise equal.
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert cuda_lib.device_error() == 0
+
+
+def test_paged_devctx_out_of_range_is_clamped_and_flagged(cuda_lib):
+    p = inputs.paged_e4m3_inputs(R=2, ctx_len=3000, capacity=3072, seed=78)
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    for bad, used in [(5000, 3000), (1, 2)]:
+        ctx_dev = torch.tensor([bad], dtype=torch.int32, device=dev)
+        out = cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, 3000, p.scale)
+        torch.cuda.synchronize()
+        assert cuda_lib.device_error() & cuda_lib.DEVERR_BAD_CTX_LEN
+        if used == 3000:
+            ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                                    used, p.scale)
+            _check(out, ref, f"clamped ctx {bad} -> {used}")
