@@ -57,7 +57,8 @@ struct CUstream_st; /* cudaStream_t */
 typedef enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, rows > context, bad scale */
-    GQA_ERR_UNSUPPORTED = 2,   /* outside Hq=6, Hkv=1, D=256, page=16, query_rows<=8 (paged) */
+    GQA_ERR_UNSUPPORTED = 2,   /* outside Hq=6, Hkv=1, D=256, page a power of two in [8, 256],
+                                  query_rows<=8 (paged) */
     GQA_ERR_WORKSPACE = 3,     /* no workspace registered, or it is too small */
     GQA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } gqa_status;
@@ -86,7 +87,8 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
  *   block_table  [ceil(ctx_len / page)] int32 physical page ids, each in
  *                [0, num_pages); entries outside it are clamped to page 0 and
  *                flag GQA_DEVERR_BAD_PAGE_ID
- *   page = 16; query_rows <= ctx_len <= num_pages * page.
+ *   page: tokens per cache page, a power of two in [8, 256] (the pages use 16);
+ *   query_rows <= ctx_len <= num_pages * page.
  * Tail row r sits at position ctx_len - query_rows + r.  The key range is
  * split over all SMs; each split's (O, m, l) partial goes to the workspace
  * and a second kernel on the same stream merges them in a fixed order. */
@@ -148,7 +150,8 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
 
 /* Selected-block sparse paged prefill [P3, Changes].
  *   q            [query_rows, Hq, D] fp16
- *   kcache/vcache [num_pages, page, Hkv, D] fp16, page = 16
+ *   kcache/vcache [num_pages, page, Hkv, D] fp16, page a power of two in
+ *                [8, 256] (the pages use 16)
  *   block_table  [ceil(ctx_len / page)] int32 physical page ids
  *   sel_idx      [query_rows, max_sel] int32 logical 4-token block ids b
  *                (tokens 4b .. 4b+3); sel_cnt [query_rows] int32, 0..max_sel

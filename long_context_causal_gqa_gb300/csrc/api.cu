@@ -142,10 +142,10 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
         return GQA_ERR_INVALID_ARG;
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
-    return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, ctx_len,
-                             nullptr, query_rows, scale, out, stream);
+    return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, page,
+                             ctx_len, nullptr, query_rows, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -164,9 +164,9 @@ int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8
         return GQA_ERR_INVALID_ARG;
     if (query_rows < 1 || max_ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8) return GQA_ERR_UNSUPPORTED;
     if ((long long)max_ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
-    return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages,
+    return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, page,
                              max_ctx_len, ctx_len_dev, query_rows, scale, out, stream);
 }
 
@@ -184,10 +184,10 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
         return GQA_ERR_INVALID_ARG;
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || page != kPage || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_noalloc_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages,
-                                     ctx_len, query_rows, scale, out, stream);
+                                     page, ctx_len, query_rows, scale, out, stream);
 }
 
 int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
@@ -205,10 +205,10 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || max_sel < 1 ||
         !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || page != kPage) return GQA_ERR_UNSUPPORTED;
+    if (!family_ok(Hq, Hkv, D) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return sparse_launch(q, kcache, vcache, block_table, sel_idx, sel_cnt, max_sel, num_pages,
-                         ctx_len, query_rows, scale, out, stream);
+                         page, ctx_len, query_rows, scale, out, stream);
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {

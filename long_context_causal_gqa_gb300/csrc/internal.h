@@ -14,7 +14,12 @@ namespace gqa {
 constexpr int kHq = 6;
 constexpr int kHkv = 1;
 constexpr int kHeadDim = 256;
-constexpr int kPage = 16;
+constexpr int kPage = 16;   // the pages' page size; any power of two in [8, 256] is accepted
+
+// Page sizes the paged kernels take: a power of two in [8, 256] (so that a
+// 4-token block never straddles a page and a 128-key tile is whole pages or a
+// slice of one).
+inline bool page_ok(int page) { return page >= 8 && page <= 256 && (page & (page - 1)) == 0; }
 
 struct DeviceInfo {
     int device;
@@ -55,20 +60,20 @@ int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill k
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
-                      int num_pages, int ctx_len, const int* ctx_dev, int R, float scale,
-                      void* out, cudaStream_t stream);
+                      int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
+                      float scale, void* out, cudaStream_t stream);
 size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms);
 
 // Same as paged_e4m3_launch, with the split partials in a static device array.
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                               const float* kscale, const float* vscale,
-                              const int32_t* block_table, int num_pages, int ctx_len, int R,
-                              float scale, void* out, cudaStream_t stream);
+                              const int32_t* block_table, int num_pages, int page, int ctx_len,
+                              int R, float scale, void* out, cudaStream_t stream);
 
 int sparse_launch(const void* q, const void* kcache, const void* vcache,
                   const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
-                  int max_sel, int num_pages, int ctx_len, int rows, float scale, void* out,
-                  cudaStream_t stream);
+                  int max_sel, int num_pages, int page, int ctx_len, int rows, float scale,
+                  void* out, cudaStream_t stream);
 
 // Bytes at the start of every workspace reserved for merge counters.
 constexpr size_t kWorkspaceCounterBytes = 4096;

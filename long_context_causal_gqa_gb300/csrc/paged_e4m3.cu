@@ -58,10 +58,7 @@ namespace paged {
 
 constexpr int D = kHeadDim;      // 256
 constexpr int HQ = kHq;          // 6
-constexpr int PAGE = kPage;      // 16 tokens
 constexpr int TILE = 128;        // keys per tile
-constexpr int PAGES_PER_TILE = TILE / PAGE;
-constexpr int PAGE_BYTES = PAGE * D;            // 4096 (Hkv = 1, one byte per element)
 constexpr int RAW_STAGE = TILE * D;             // 32 KB of E4M3 per K or V tile
 // Threads of a CTA with NWG softmax warpgroups: producer warp, UMMA warp,
 // then 4 * NWG softmax warps.
@@ -76,6 +73,7 @@ struct Params {
     const int32_t* table;
     const __half* q;
     const int* ctx_dev;   // device-side ctx_len (nullptr: use ctx_len)
+    int page, log2_page;  // tokens per cache page, a power of two in [8, 256]
     int num_pages, ctx_len, R, nq, n_tiles, G;
     float scale;
     float* ws_o;    // [G][nq][D] unnormalised partial O (in units of the E4M3 V)
@@ -328,7 +326,8 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int t_begin = (int)((long long)split * n_tiles / P.G);
     const int t_end = (int)((long long)(split + 1) * n_tiles / P.G);
     const int ntl = t_end - t_begin;
-    const int n_logical = (ctx_len + PAGE - 1) / PAGE;
+    const int page = P.page, lpage = P.log2_page;
+    const int n_logical = (ctx_len + page - 1) >> lpage;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NRAW; ++s) {
@@ -359,57 +358,71 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Block-table entries arrive a chunk of four tiles (32 pages, one per
-        // lane) ahead of their use, so their latency stays off the copy
-        // stream; lane 2p + h issues the copy of page p, half h of d.
+        // Block-table entries arrive a chunk of 32 pages (one per lane) ahead
+        // of their use, so their latency stays off the copy stream.  A tile
+        // covers TILE / page pages (page <= TILE, lane 2p + h copies page p,
+        // half h of d) or a TILE-row slice of one page (page > TILE).
         if (ntl > 0) {
-            const int pg_end = min(t_end * PAGES_PER_TILE, n_logical);
+            const int ppt = page >= TILE ? 1 : TILE >> lpage;       // pages per tile, divides 32
+            const int rows_per_copy = page >= TILE ? TILE : page;
+            const int pg_begin = (t_begin * TILE) >> lpage;
+            const int pg_end = min(((t_end * TILE - 1) >> lpage) + 1, n_logical);
             auto load_chunk = [&](int k) -> int {
-                const int pg = (t_begin + 4 * k) * PAGES_PER_TILE + lane;
+                const int pg = pg_begin + 32 * k + lane;
                 return pg < pg_end ? __ldg(P.table + pg) : 0;
             };
             int cur = load_chunk(0);
             int nxt = load_chunk(1);
+            int cur_k = 0;
             const int pp = lane >> 1, hh = lane & 1;
             uint32_t item = 0;
             bool ok = true;
-            int id_prev = 0, npg_prev = 0;
-            auto issue = [&](const CUtensorMap* tm, int id, int npg) -> bool {
+            int id_prev = 0, npg_prev = 0, y_prev = 0;
+            // One K or V stage: npg copies of rows_per_copy rows (row offset y0
+            // inside the page when a tile is a slice of one page).
+            auto issue = [&](const CUtensorMap* tm, int id, int npg, int y0) -> bool {
                 const int s = item % NRAW;
                 const uint32_t ph = (item / NRAW) & 1u;
                 int okw = 1;
                 if (lane == 0) {
                     okw = mbar_wait(bar(B_RAW_EMPTY + s), ph ^ 1u, abort_flag, P.err);
-                    if (okw) mbar_arrive_expect_tx(bar(B_RAW_FULL + s), npg * PAGE_BYTES);
+                    if (okw)
+                        mbar_arrive_expect_tx(bar(B_RAW_FULL + s),
+                                              (uint32_t)(npg * rows_per_copy * D));
                 }
                 if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
                 // Stage layout: [2 halves of d][128 keys][128 B], 128B-swizzled.
                 if (lane < 2 * npg)
-                    tma_load_2d(s_raw + s * RAW_STAGE + hh * (TILE * 128) + pp * (PAGE * 128), tm,
-                                bar(B_RAW_FULL + s), hh * 128, id * PAGE);
+                    tma_load_2d(s_raw + s * RAW_STAGE + hh * (TILE * 128) +
+                                    pp * (rows_per_copy * 128),
+                                tm, bar(B_RAW_FULL + s), hh * 128, id * page + y0);
                 ++item;
                 return true;
             };
             for (int jj = 0; jj <= ntl && ok; ++jj) {
-                int id = 0, npg = 0;
+                int id = 0, npg = 0, y0 = 0;
                 if (jj < ntl) {
-                    const int sub = jj & 3;
-                    if (sub == 0 && jj > 0) {
-                        cur = nxt;
-                        nxt = load_chunk((jj >> 2) + 1);
-                    }
                     const int tile = t_begin + jj;
-                    npg = min(PAGES_PER_TILE, n_logical - tile * PAGES_PER_TILE);
-                    id = __shfl_sync(0xffffffffu, cur, sub * PAGES_PER_TILE + pp);
+                    const int lp0 = (tile * TILE) >> lpage;            // first logical page
+                    const int rel = lp0 - pg_begin;
+                    while ((rel >> 5) > cur_k) {
+                        cur = nxt;
+                        ++cur_k;
+                        nxt = load_chunk(cur_k + 1);
+                    }
+                    npg = min(ppt, n_logical - lp0);
+                    y0 = (tile * TILE) & (page - 1);
+                    id = __shfl_sync(0xffffffffu, cur, (rel & 31) + (pp < ppt ? pp : 0));
                     if (lane < 2 * npg && (id < 0 || id >= P.num_pages)) {
                         atomicOr(P.err, kErrBadPageId);
                         id = 0;
                     }
-                    ok = issue(&tm_k, id, npg);
+                    ok = issue(&tm_k, id, npg, y0);
                 }
-                if (ok && jj >= 1) ok = issue(&tm_v, id_prev, npg_prev);
+                if (ok && jj >= 1) ok = issue(&tm_v, id_prev, npg_prev, y_prev);
                 id_prev = id;
                 npg_prev = npg;
+                y_prev = y0;
             }
             if (!ok && lane == 0) {
                 for (int s = 0; s < NRAW; ++s) {
@@ -940,8 +953,8 @@ size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms) {
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
-                      int num_pages, int ctx_len, const int* ctx_dev, int R, float scale,
-                      void* out, cudaStream_t stream) {
+                      int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
+                      float scale, void* out, cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -953,6 +966,8 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.table = block_table;
     P.q = static_cast<const __half*>(q);
     P.ctx_dev = ctx_dev;
+    P.page = page;
+    P.log2_page = __builtin_ctz((unsigned)page);
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
@@ -972,9 +987,10 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.ws_o = w;
     P.ws_ml = w + (size_t)P.G * P.nq * D;
     CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)num_pages * PAGE;
-    if (!make_map_2d_u8(&tk, kcache, rows, D, PAGE, 128) ||
-        !make_map_2d_u8(&tv, vcache, rows, D, PAGE, 128))
+    const uint64_t rows = (uint64_t)num_pages * page;
+    const uint32_t box_rows = page < TILE ? (uint32_t)page : (uint32_t)TILE;
+    if (!make_map_2d_u8(&tk, kcache, rows, D, box_rows, 128) ||
+        !make_map_2d_u8(&tv, vcache, rows, D, box_rows, 128))
         return GQA_ERR_CUDA;
     return launch_split(tk, tv, P, stream, di->device);
 }
@@ -1006,8 +1022,8 @@ size_t paged_e4m3_noalloc_capacity_floats() { return paged::kNoAllocFloats; }
 
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                               const float* kscale, const float* vscale,
-                              const int32_t* block_table, int num_pages, int ctx_len, int R,
-                              float scale, void* out, cudaStream_t stream) {
+                              const int32_t* block_table, int num_pages, int page, int ctx_len,
+                              int R, float scale, void* out, cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -1035,6 +1051,8 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.table = block_table;
     P.q = static_cast<const __half*>(q);
     P.ctx_dev = nullptr;
+    P.page = page;
+    P.log2_page = __builtin_ctz((unsigned)page);
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
@@ -1050,9 +1068,10 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.ws_o = scratch;
     P.ws_ml = scratch + (size_t)P.G * P.nq * D;
     CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)num_pages * PAGE;
-    if (!make_map_2d_u8(&tk, kcache, rows, D, PAGE, 128) ||
-        !make_map_2d_u8(&tv, vcache, rows, D, PAGE, 128))
+    const uint64_t rows = (uint64_t)num_pages * page;
+    const uint32_t box_rows = page < TILE ? (uint32_t)page : (uint32_t)TILE;
+    if (!make_map_2d_u8(&tk, kcache, rows, D, box_rows, 128) ||
+        !make_map_2d_u8(&tv, vcache, rows, D, box_rows, 128))
         return GQA_ERR_CUDA;
     return launch_split(tk, tv, P, stream, di->device);
 }

@@ -38,7 +38,6 @@ namespace sparse {
 
 constexpr int D = kHeadDim;
 constexpr int HQ = kHq;
-constexpr int PAGE = kPage;
 constexpr int TILE = 128;            // keys per tile
 constexpr int BLK = 4;               // tokens per selected block
 constexpr int NP = 16;               // 6 heads padded to the UMMA N granule
@@ -54,6 +53,7 @@ struct Params {
     const int32_t* sel_idx;
     const int32_t* sel_cnt;
     int max_sel, num_pages, ctx_len, rows, G;
+    int log2_page;   // tokens per cache page = 1 << log2_page (8 .. 256)
     float scale_log2;
     __half* out;
     unsigned* err;
@@ -220,12 +220,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 const int tok_l = key_token(P, i, cnt, t, key_l, true);
                 size_t row_l = 0;
                 if (tok_l >= 0) {
-                    int pg = __ldg(P.table + tok_l / PAGE);
+                    int pg = __ldg(P.table + (tok_l >> P.log2_page));
                     if (pg < 0 || pg >= P.num_pages) {
                         atomicOr(P.err, kErrBadPageId);
                         pg = 0;
                     }
-                    row_l = ((size_t)pg * PAGE + (tok_l % PAGE)) * D;
+                    row_l = (((size_t)pg << P.log2_page) + (tok_l & ((1 << P.log2_page) - 1))) * D;
                 }
                 const int kb = g & 1;
                 for (int kv = 0; kv < 2; ++kv) {
@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 
 int sparse_launch(const void* q, const void* kcache, const void* vcache,
                   const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
-                  int max_sel, int num_pages, int ctx_len, int rows, float scale, void* out,
-                  cudaStream_t stream) {
+                  int max_sel, int num_pages, int page, int ctx_len, int rows, float scale,
+                  void* out, cudaStream_t stream) {
     using namespace sparse;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -512,6 +512,7 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache,
     P.sel_cnt = sel_cnt;
     P.max_sel = max_sel;
     P.num_pages = num_pages;
+    P.log2_page = __builtin_ctz((unsigned)page);
     P.ctx_len = ctx_len;
     P.rows = rows;
     P.G = rows < di->num_sms ? rows : di->num_sms;

@@ -75,7 +75,9 @@ def test_paged_rejects_bad_arguments(lib):
     assert _paged(lib, kscale=P(0)) == binding.GQA_ERR_INVALID_ARG
     assert _paged(lib, R=0) == binding.GQA_ERR_INVALID_ARG
     assert _paged(lib, R=9) == binding.GQA_ERR_UNSUPPORTED
-    assert _paged(lib, page=32) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged(lib, page=12) == binding.GQA_ERR_UNSUPPORTED   # not a power of two
+    assert _paged(lib, page=512) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged(lib, page=4) == binding.GQA_ERR_UNSUPPORTED
     assert _paged(lib, ctx=200, pages=8) == binding.GQA_ERR_INVALID_ARG  # 200 > 8 * 16
     assert _paged(lib, R=8, ctx=5) == binding.GQA_ERR_INVALID_ARG
     assert _paged(lib, scale=-1.0) == binding.GQA_ERR_INVALID_ARG
@@ -92,7 +94,7 @@ def test_paged_devctx_rejects_bad_arguments(lib):
     assert _paged_dev(lib, R=3, max_ctx=2) == binding.GQA_ERR_INVALID_ARG
     assert _paged_dev(lib, max_ctx=200, pages=8) == binding.GQA_ERR_INVALID_ARG
     assert _paged_dev(lib, R=9, max_ctx=100) == binding.GQA_ERR_UNSUPPORTED
-    assert _paged_dev(lib, page=8) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged_dev(lib, page=24) == binding.GQA_ERR_UNSUPPORTED
     assert _paged_dev(lib, scale=0.0) == binding.GQA_ERR_INVALID_ARG
 
 

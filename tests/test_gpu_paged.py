@@ -170,3 +170,39 @@ def test_paged_devctx_out_of_range_is_clamped_and_flagged(cuda_lib):
             ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
                                     used, p.scale)
             _check(out, ref, f"clamped ctx {bad} -> {used}")
+
+
+@pytest.mark.parametrize("page,R,ctx,cap", [
+    (8, 1, 3000, 4096), (8, 8, 777, 1024), (32, 2, 5001, 8192), (64, 5, 4000, 4096),
+    (128, 8, 3333, 4096), (256, 3, 5000, 8192), (256, 1, 129, 256), (64, 8, 40000, 65536),
+])
+def test_paged_other_page_sizes(cuda_lib, page, R, ctx, cap):
+    """Page sizes other than the pages' 16: a 128-key tile is TILE / page pages
+    (page <= 128) or a slice of one page (page 256)."""
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx, capacity=cap, seed=page + R, page=page)
+    out = _run(cuda_lib, p)
+    ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                            p.ctx_len, p.scale)
+    _check(out, ref, f"page={page} R={R} ctx={ctx}")
+
+
+def test_paged_devctx_page_256_graph_replay(cuda_lib):
+    max_ctx, cap = 6000, 6144
+    p = inputs.paged_e4m3_inputs(R=4, ctx_len=max_ctx, capacity=cap, seed=91, page=256)
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    ctx_dev = torch.tensor([max_ctx], dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, max_ctx, p.scale, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, max_ctx, p.scale, out=out)
+    for ctx in [6000, 3001, 256, 255, 100]:
+        ctx_dev.fill_(ctx)
+        g.replay()
+        torch.cuda.synchronize()
+        assert cuda_lib.device_error() == 0
+        ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table, ctx,
+                                p.scale)
+        _check(out, ref, f"page=256 device ctx={ctx}")

@@ -145,3 +145,13 @@ def test_sparse_bitwise_reproducible_and_graph_replay(cuda_lib):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), a.view(torch.int16))
     assert cuda_lib.device_error() == 0
+
+
+@pytest.mark.parametrize("page", [8, 32, 64, 256])
+def test_sparse_other_page_sizes(cuda_lib, page):
+    """Page sizes other than the pages' 16 (any power of two in [8, 256])."""
+    s = inputs.sparse_inputs(rows=96, ctx_len=3000, tokens=128, seed=page, page=page)
+    out = _run(cuda_lib, s)
+    ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
+                               s.ctx_len, s.scale)
+    _check(out, ref, f"page={page}")
