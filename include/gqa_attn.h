@@ -120,6 +120,30 @@ int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8
                                int Hq, int Hkv, int D, float scale, void* out,
                                struct CUstream_st* stream);
 
+/* Several sequences' E4M3 verifier tails in one launch ([P2] Changes; a
+ * serving step verifies a batch of sequences of different lengths): the
+ * batched, variable-length form of gqa_attn_paged_e4m3_devctx.  All
+ * sequences share one cache (kcache/vcache, kscale/vscale, page) and
+ * query_rows; per sequence b:
+ *   q[b], out[b]        q/out [batch, query_rows, Hq, D] fp16
+ *   block_tables[b]     [batch, table_stride] int32 physical page ids;
+ *                       table_stride * page >= max_ctx_len
+ *   ctx_lens_dev[b]     device int32 [batch], read when the kernels run (so a
+ *                       captured graph replays as the contexts grow); each is
+ *                       clamped into [query_rows, max_ctx_len] and flags
+ *                       GQA_DEVERR_BAD_CTX_LEN if it was outside.
+ * 1 <= batch <= 1024.  The grid has max(SM count, batch) splits, divided
+ * between the sequences in proportion to their 128-key tile counts (at least
+ * one each) on the device; each split's partial goes to the workspace
+ * (gqa_workspace_bytes(GQA_KIND_PAGED_E4M3_BATCH, query_rows, batch, ...))
+ * and a second kernel merges every sequence's splits in a fixed order. */
+int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                              const float* kscale, const float* vscale,
+                              const int32_t* block_tables, int table_stride, int num_pages,
+                              int page, const int32_t* ctx_lens_dev, int max_ctx_len, int batch,
+                              int query_rows, int Hq, int Hkv, int D, float scale, void* out,
+                              struct CUstream_st* stream);
+
 /* Paged FP8-E4M3 verifier tail that allocates nothing (no counterpart in the
  * pages; an addition of this library).  Some callers cannot call cudaMalloc:
  * engines whose pooling allocator owns all device memory and must not see
@@ -170,6 +194,7 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
 #define GQA_KIND_PREFILL 0
 #define GQA_KIND_PAGED_E4M3 1
 #define GQA_KIND_SPARSE 2
+#define GQA_KIND_PAGED_E4M3_BATCH 3   /* ctx_or_kv = number of sequences */
 
 /* Bytes of workspace an entry point of `kind` needs for the given shape on
  * the current device (query_rows = Q or the tail/row count, ctx_or_kv = KV or

@@ -29,6 +29,7 @@ GQA_ERR_CUDA = 4
 KIND_PREFILL = 0
 KIND_PAGED_E4M3 = 1
 KIND_SPARSE = 2
+KIND_PAGED_E4M3_BATCH = 3
 DEVERR_WAIT_TIMEOUT = 0x1
 DEVERR_BAD_BLOCK_ID = 0x2
 DEVERR_BAD_PAGE_ID = 0x4
@@ -36,6 +37,7 @@ DEVERR_BAD_CTX_LEN = 0x8
 
 # Every symbol include/gqa_attn.h declares.
 EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_devctx",
+            "gqa_attn_paged_e4m3_batch",
             "gqa_attn_paged_e4m3_noalloc",
             "gqa_attn_sparse_blocks",
             "gqa_workspace_bytes", "gqa_set_workspace", "gqa_get_device_error",
@@ -69,6 +71,9 @@ def load():
             lib.gqa_attn_paged_e4m3_devctx.argtypes = [P, P, P, P, P, P, I, I, P, I, I, I, I, I,
                                                        F, P, P]
             lib.gqa_attn_paged_e4m3_devctx.restype = I
+            lib.gqa_attn_paged_e4m3_batch.argtypes = [P, P, P, P, P, P, I, I, I, P, I, I, I, I, I,
+                                                      I, F, P, P]
+            lib.gqa_attn_paged_e4m3_batch.restype = I
             lib.gqa_attn_paged_e4m3_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I,
                                                         F, P, P]
             lib.gqa_attn_paged_e4m3_noalloc.restype = I
@@ -224,6 +229,34 @@ def paged_e4m3_devctx(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tenso
                                                _ptr(ctx_len_dev), int(max_ctx_len), R, Hq, Hkv, D,
                                                float(scale), _ptr(out), _stream_ptr(stream))
     _check(st, "gqa_attn_paged_e4m3_devctx")
+    return out
+
+
+def paged_e4m3_batch(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                     kscale: torch.Tensor, vscale: torch.Tensor, block_tables: torch.Tensor,
+                     ctx_lens_dev: torch.Tensor, max_ctx_len: int, scale: float = 1.0 / 16,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Batched variable-length E4M3 tails: q [B,R,Hq,D] fp16, one shared page
+    cache, block_tables [B, stride] int32, ctx_lens_dev [B] CUDA int32 read when
+    the kernels run, max_ctx_len the host bound."""
+    dev = _need_cuda(q, kcache, vcache, kscale, vscale, block_tables, ctx_lens_dev)
+    if ctx_lens_dev.dtype != torch.int32 or block_tables.dtype != torch.int32:
+        raise GQAError(GQA_ERR_INVALID_ARG, "ctx_lens_dev and block_tables must be int32")
+    B, R, Hq, D = q.shape
+    if ctx_lens_dev.numel() != B or block_tables.shape[0] != B or not block_tables.is_contiguous():
+        raise GQAError(GQA_ERR_INVALID_ARG, "one context length and table row per sequence")
+    num_pages, page, Hkv, _ = kcache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    with torch.cuda.device(dev):
+        ensure_workspace(workspace_bytes(KIND_PAGED_E4M3_BATCH, R, B, Hq, D), dev)
+        st = load().gqa_attn_paged_e4m3_batch(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kscale),
+                                              _ptr(vscale), _ptr(block_tables),
+                                              block_tables.shape[1], num_pages, page,
+                                              _ptr(ctx_lens_dev), int(max_ctx_len), B, R, Hq, Hkv,
+                                              D, float(scale), _ptr(out), _stream_ptr(stream))
+    _check(st, "gqa_attn_paged_e4m3_batch")
     return out
 
 

@@ -148,6 +148,32 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
                              ctx_len, nullptr, query_rows, scale, out, stream);
 }
 
+int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                              const float* kscale, const float* vscale,
+                              const int32_t* block_tables, int table_stride, int num_pages,
+                              int page, const int32_t* ctx_lens_dev, int max_ctx_len, int batch,
+                              int query_rows, int Hq, int Hkv, int D, float scale, void* out,
+                              struct CUstream_st* stream) {
+    if (!q || !kcache || !vcache || !kscale || !vscale || !block_tables || !ctx_lens_dev || !out)
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale) |
+         reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(ctx_lens_dev)) &
+        3u)
+        return GQA_ERR_INVALID_ARG;
+    if (query_rows < 1 || max_ctx_len < query_rows || num_pages < 1 || batch < 1 ||
+        !scale_ok(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8 || batch > kMaxTailBatch)
+        return GQA_ERR_UNSUPPORTED;
+    if ((long long)max_ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
+    if ((long long)table_stride * page < (long long)max_ctx_len) return GQA_ERR_INVALID_ARG;
+    return paged_e4m3_batch_launch(q, kcache, vcache, kscale, vscale, block_tables, table_stride,
+                                   num_pages, page, ctx_lens_dev, max_ctx_len, batch, query_rows,
+                                   scale, out, stream);
+}
+
 int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                                const float* kscale, const float* vscale,
                                const int32_t* block_table, int num_pages, int page,
@@ -212,9 +238,14 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {
-    if (Hq != kHq || D != kHeadDim || query_rows < 1 || ctx_or_kv < query_rows) return 0;
+    if (Hq != kHq || D != kHeadDim || query_rows < 1 || ctx_or_kv < 1) return 0;
     const DeviceInfo* di = device_info();
     if (!di) return 0;
+    if (kind == GQA_KIND_PAGED_E4M3_BATCH) {   // ctx_or_kv = number of sequences
+        if (query_rows > 8 || ctx_or_kv > kMaxTailBatch) return 0;
+        return paged_e4m3_batch_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
+    }
+    if (ctx_or_kv < query_rows) return 0;
     switch (kind) {
         case GQA_KIND_PREFILL:
             return prefill_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);

@@ -21,6 +21,10 @@ constexpr int kPage = 16;   // the pages' page size; any power of two in [8, 256
 // slice of one).
 inline bool page_ok(int page) { return page >= 8 && page <= 256 && (page & (page - 1)) == 0; }
 
+// Most sequences one batched tail launch takes (its merge reads at most 1024
+// split partials per packed row).
+constexpr int kMaxTailBatch = 1024;
+
 struct DeviceInfo {
     int device;
     int num_sms;
@@ -63,6 +67,12 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
                       int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
                       float scale, void* out, cudaStream_t stream);
 size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms);
+int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                            const float* kscale, const float* vscale,
+                            const int32_t* block_tables, int table_stride, int num_pages,
+                            int page, const int* ctx_lens_dev, int max_ctx_len, int batch,
+                            int R, float scale, void* out, cudaStream_t stream);
+size_t paged_e4m3_batch_workspace_bytes(int R, int batch, int num_sms);
 
 // Same as paged_e4m3_launch, with the split partials in a static device array.
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,

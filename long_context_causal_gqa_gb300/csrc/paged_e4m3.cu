@@ -72,7 +72,9 @@ struct Params {
     const float* vscale;
     const int32_t* table;
     const __half* q;
-    const int* ctx_dev;   // device-side ctx_len (nullptr: use ctx_len)
+    const int* ctx_dev;   // device-side context lengths, one per sequence (nullptr: ctx_len)
+    int batch;            // sequences sharing the grid (1 except for the batched entry point)
+    int table_stride;     // block-table entries per sequence
     int page, log2_page;  // tokens per cache page, a power of two in [8, 256]
     int num_pages, ctx_len, R, nq, n_tiles, G;
     float scale;
@@ -175,30 +177,6 @@ __device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& t1, 
     t3 = e4m3x2((r0 - a0) * 16.f, (r1 - a1) * 16.f);
 }
 
-// Two fp32 values rounded to fp16, then split as h = t1 + t2 / 16 + t3 / 256
-// with t1, t2, t3 E4M3 (each result holds the pair's two bytes in its low 16
-// bits).  Differences and the scalings by 16 are exact in fp16, and three
-// 4-bit terms cover fp16's 11 significant bits, so the three terms carry the
-// fp16 value (down to E4M3's smallest subnormal in the last term).
-__device__ __forceinline__ void split3_e4m3_h2(float x0, float x1, uint32_t& t1, uint32_t& t2,
-                                               uint32_t& t3) {
-    uint32_t h, b, r;
-    uint16_t a;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(h));
-    t1 = a;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(a));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(b));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x4C004C00u));   // x 16
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(r));
-    t2 = a;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(a));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(b));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x4C004C00u));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(r));
-    t3 = a;
-}
-
 // Byte offset of 16-byte unit u (0..7) of row r inside a 128B-swizzled block.
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t u) {
     return r * 128u + ((u ^ (r & 7u)) << 4);
@@ -272,7 +250,113 @@ __device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t* r) {
     }
 }
 
-template <int NP, int NWG>
+// Which sequence, and which of its splits, CTA `split` works on.  With one
+// sequence: all P.G splits.  With several (the batched tail): sequence b gets
+// 1 + floor((G - batch) * tiles_b / total_tiles) splits, laid out in sequence
+// order, from the context lengths read on the device; CTAs past the last
+// sequence's splits get b = -1 and do nothing.  Device context lengths are
+// clamped into [R, ctx_len] (bad = the value was outside).  Every warp runs
+// this itself (lane-parallel over the sequences), so no block-wide step is
+// needed before the CTA knows its work.
+struct SplitOwner {
+    int b, j, g, ctx;
+    bool bad;
+};
+__device__ __forceinline__ int clamp_ctx(const Params& P, int c) {
+    return c < P.R ? P.R : (c > P.ctx_len ? P.ctx_len : c);
+}
+__device__ __forceinline__ long long tiles_of(int ctx) { return (ctx + TILE - 1) / TILE; }
+
+template <bool BATCHED>
+__device__ SplitOwner split_owner(const Params& P, int split) {
+    SplitOwner r;
+    if (!BATCHED) {
+        const int raw = P.ctx_dev ? *P.ctx_dev : P.ctx_len;
+        r.b = 0;
+        r.j = split;
+        r.g = P.G;
+        r.ctx = clamp_ctx(P, raw);
+        r.bad = raw != r.ctx;
+        return r;
+    }
+    const int lane = threadIdx.x & 31;
+    long long total = 0;
+    for (int i = lane; i < P.batch; i += 32) total += tiles_of(clamp_ctx(P, P.ctx_dev[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    const long long spare = P.G - P.batch;
+    int base = 0;
+    for (int i0 = 0; i0 < P.batch; i0 += 32) {
+        const int i = i0 + lane;
+        int ci = 0, gi = 0, bad = 0;
+        if (i < P.batch) {
+            const int raw = P.ctx_dev[i];
+            ci = clamp_ctx(P, raw);
+            bad = raw != ci;
+            gi = 1 + (int)(spare * tiles_of(ci) / total);
+        }
+        int incl = gi;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const int start = base + incl - gi;
+        const unsigned m =
+            __ballot_sync(0xffffffffu, i < P.batch && split >= start && split < start + gi);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            r.b = i0 + src;
+            r.j = split - __shfl_sync(0xffffffffu, start, src);
+            r.g = __shfl_sync(0xffffffffu, gi, src);
+            r.ctx = __shfl_sync(0xffffffffu, ci, src);
+            r.bad = __shfl_sync(0xffffffffu, bad, src) != 0;
+            return r;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    r.b = -1;
+    r.j = r.g = r.ctx = 0;
+    r.bad = false;
+    return r;
+}
+
+// First split and split count of sequence b (the merge's view of split_owner).
+__device__ void seq_splits(const Params& P, int b, int& first, int& count) {
+    if (P.batch == 1) {
+        first = 0;
+        count = P.G;
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    long long total = 0;
+    for (int i = lane; i < P.batch; i += 32) total += tiles_of(clamp_ctx(P, P.ctx_dev[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    const long long spare = P.G - P.batch;
+    int base = 0;
+    for (int i0 = 0; i0 <= b; i0 += 32) {
+        const int i = i0 + lane;
+        const int gi = i < P.batch ? 1 + (int)(spare * tiles_of(clamp_ctx(P, P.ctx_dev[i])) / total)
+                                   : 0;
+        int incl = gi;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (b < i0 + 32) {
+            const int src = b - i0;
+            first = base + __shfl_sync(0xffffffffu, incl - gi, src);
+            count = __shfl_sync(0xffffffffu, gi, src);
+            return;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    first = count = 0;
+}
+
+template <int NP, int NWG, bool BATCHED>
 __global__ void __launch_bounds__(threads_for(NWG), 1)
 paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params P) {
@@ -307,24 +391,18 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int split = blockIdx.x;
+    const int split = blockIdx.x;   // this CTA's partial slot
     // Context length: the launch's, or read on the device (the grid is then
     // sized for the largest context, P.ctx_len, and splits past the actual
-    // context get no tiles).  A device value outside [R, P.ctx_len] is
-    // clamped and flagged.
-    int ctx_len = P.ctx_len;
-    if (P.ctx_dev) {
-        const int c = *P.ctx_dev;
-        if (c < P.R || c > P.ctx_len) {
-            if (threadIdx.x == 0 && split == 0) atomicOr(P.err, kErrBadCtxLen);
-            ctx_len = c < P.R ? P.R : P.ctx_len;
-        } else {
-            ctx_len = c;
-        }
-    }
+    // context get no tiles); with several sequences, this CTA's sequence.
+    const SplitOwner own = split_owner<BATCHED>(P, split);
+    if (own.b < 0) return;   // uniform: no sequence left for this CTA
+    if (own.bad && own.j == 0 && threadIdx.x == 0) atomicOr(P.err, kErrBadCtxLen);
+    const int ctx_len = own.ctx;
     const int n_tiles = (ctx_len + TILE - 1) / TILE;
-    const int t_begin = (int)((long long)split * n_tiles / P.G);
-    const int t_end = (int)((long long)(split + 1) * n_tiles / P.G);
+    const int t_begin = (int)((long long)own.j * n_tiles / own.g);
+    const int t_end = (int)((long long)(own.j + 1) * n_tiles / own.g);
+    const int seq = own.b;
     const int ntl = t_end - t_begin;
     const int page = P.page, lpage = P.log2_page;
     const int n_logical = (ctx_len + page - 1) >> lpage;
@@ -367,9 +445,10 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const int rows_per_copy = page >= TILE ? TILE : page;
             const int pg_begin = (t_begin * TILE) >> lpage;
             const int pg_end = min(((t_end * TILE - 1) >> lpage) + 1, n_logical);
+            const int32_t* table = P.table + (size_t)seq * P.table_stride;
             auto load_chunk = [&](int k) -> int {
                 const int pg = pg_begin + 32 * k + lane;
-                return pg < pg_end ? __ldg(P.table + pg) : 0;
+                return pg < pg_end ? __ldg(table + pg) : 0;
             };
             int cur = load_chunk(0);
             int nxt = load_chunk(1);
@@ -446,7 +525,8 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 const int r = warp - 1 + QW * i;
-                raw[i] = (r < P.nq) ? *reinterpret_cast<const uint4*>(P.q + (size_t)r * D + d0)
+                raw[i] = (r < P.nq) ? *reinterpret_cast<const uint4*>(
+                                          P.q + ((size_t)seq * P.nq + r) * D + d0)
                                     : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
@@ -572,9 +652,14 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const int lim_base = ctx_len - P.R;                 // row r sees keys <= lim_base + r
             const uint32_t gbar = bar(B_GROUP + hg);
             uint32_t gphase = 0;
-            float sl2[NH];
+            // Score scale per packed row (log2 units): scale * kscale * Q row scale;
+            // at 48 packed rows (72 registers per thread) read from shared memory
+            // each tile (a broadcast) instead of held in registers.
+            const float sl2k = P.scale * kscale * 1.4426950408889634f;
+            constexpr bool kSl2InRegs = NP <= 32;
+            float sl2[kSl2InRegs ? NH : 1];
 #pragma unroll
-            for (int c = 0; c < NH; ++c) sl2[c] = P.scale * kscale * qs[c0 + c] * 1.4426950408889634f;
+            for (int c = 0; c < (kSl2InRegs ? NH : 1); ++c) sl2[c] = sl2k * qs[c0 + c];
             float lpart[NH];
 #pragma unroll
             for (int c = 0; c < NH; ++c) lpart[c] = 0.f;
@@ -614,7 +699,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     for (int c = 0; c < NH; ++c)
                         s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
                                     fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c]))) *
-                               sl2[c];
+                               (kSl2InRegs ? sl2[kSl2InRegs ? c : 0] : sl2k * qs[c0 + c]);
                 }
                 const int key = (t_begin + jj) * TILE + k;
                 if ((t_begin + jj) * TILE + TILE - 1 > lim_base) {
@@ -719,7 +804,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                         lpart[c] += p0;
                         lpart[c + 1] += p1;
                         uint32_t t[3];
-                        split3_e4m3_h2(p0, p1, t[0], t[1], t[2]);
+                        split3_e4m3x2(p0, p1, t[0], t[1], t[2]);
 #pragma unroll
                         for (int e = 0; e < 3; ++e) {
                             pt[pofs(c) + e * NP * 128] = (uint8_t)(t[e] & 0xFF);
@@ -810,12 +895,14 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     __shared__ float w_s[MERGE_MAX_SPLITS];
     __shared__ float4 red[MERGE_WARPS][32];
     __shared__ float wred[2][MERGE_WARPS];
-    const int c = blockIdx.x;
+    const int seq = P.batch > 1 ? (int)blockIdx.x / P.nq : 0;   // sequence
+    const int c = (int)blockIdx.x - seq * P.nq;                   // packed row within it
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int d0 = blockIdx.y * 128 + lane * 4;
-    const int G = P.G;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    int S0 = 0, G = P.G;                    // this sequence's splits S0 .. S0 + G - 1
+    if (P.batch > 1) seq_splits(P, seq, S0, G);
     const float vs = *P.vscale;
     // One round of loads: the O partials of this warp's first MERGE_PF splits
     // and the (m, l) pairs of the splits threadIdx.x + 512 i.
@@ -823,7 +910,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
 #pragma unroll
     for (int i = 0; i < MERGE_PF; ++i) {
         const int s = warp + MERGE_WARPS * i;
-        o[i] = s < G ? __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0))
+        o[i] = s < G ? __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)(S0 + s) * P.nq + c) * D + d0))
                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     constexpr int ML_PT = MERGE_MAX_SPLITS / (MERGE_WARPS * 32);
@@ -831,7 +918,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
 #pragma unroll
     for (int i = 0; i < ML_PT; ++i) {
         const int s = threadIdx.x + MERGE_WARPS * 32 * i;
-        ml[i] = s < G ? __ldcg(reinterpret_cast<const float2*>(P.ws_ml + ((size_t)s * P.nq + c) * 2))
+        ml[i] = s < G ? __ldcg(reinterpret_cast<const float2*>(P.ws_ml + ((size_t)(S0 + s) * P.nq + c) * 2))
                       : make_float2(-INFINITY, 0.f);
     }
     // M = max_s m_s.
@@ -877,7 +964,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     for (int s = warp + MERGE_WARPS * MERGE_PF; s < G; s += MERGE_WARPS) {
         const float w = w_s[s];
         if (w != 0.f)
-            add(w, __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0)));
+            add(w, __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)(S0 + s) * P.nq + c) * D + d0)));
     }
     red[warp][lane] = acc;
     __syncthreads();
@@ -900,26 +987,26 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
         uint2 pk;
         pk.x = *reinterpret_cast<const uint32_t*>(&h01);
         pk.y = *reinterpret_cast<const uint32_t*>(&h23);
-        *reinterpret_cast<uint2*>(P.out + (size_t)c * D + d0) = pk;
+        *reinterpret_cast<uint2*>(P.out + ((size_t)seq * P.nq + c) * D + d0) = pk;
     }
 }
 
-template <int NP, int NWG>
-int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
-              int device) {
+template <int NP, int NWG, bool BATCHED>
+int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
+                int device) {
     using L = Layout<NP, NWG>;
     static bool attr_done[64] = {false};
     if (device < 64 && !attr_done[device]) {
-        if (cudaFuncSetAttribute(paged_split_kernel<NP, NWG>,
+        if (cudaFuncSetAttribute(paged_split_kernel<NP, NWG, BATCHED>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::SMEM) != cudaSuccess)
             return GQA_ERR_CUDA;
         attr_done[device] = true;
     }
-    paged_split_kernel<NP, NWG><<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
+    paged_split_kernel<NP, NWG, BATCHED><<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P.nq, D / 128);
+    cfg.gridDim = dim3(P.batch * P.nq, D / 128);
     cfg.blockDim = dim3(MERGE_WARPS * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -935,6 +1022,16 @@ int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStrea
 // Packed query rows -> UMMA N and softmax warpgroups: every softmax thread
 // owns 8 columns (8-aligned in tensor memory), so that the latency-bound
 // softmax chain is spread over 8, 16 or 24 warps.
+template <int NP, int NWG>
+int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
+              int device) {
+    // One sequence (the common tail) or several (the batched entry point):
+    // separate instantiations, so the single-sequence kernel carries none of
+    // the batched bookkeeping.
+    return P.batch > 1 ? launch_np_b<NP, NWG, true>(tk, tv, P, stream, device)
+                       : launch_np_b<NP, NWG, false>(tk, tv, P, stream, device);
+}
+
 int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
                  int device) {
     if (P.nq <= 16) return launch_np<16, 2>(tk, tv, P, stream, device);
@@ -966,6 +1063,8 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.table = block_table;
     P.q = static_cast<const __half*>(q);
     P.ctx_dev = ctx_dev;
+    P.batch = 1;
+    P.table_stride = 0;
     P.page = page;
     P.log2_page = __builtin_ctz((unsigned)page);
     P.num_pages = num_pages;
@@ -982,6 +1081,63 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     size_t ws_bytes;
     current_workspace(&ws, &ws_bytes);
     if (!ws || ws_bytes < paged_e4m3_workspace_bytes(R, ctx_len, di->num_sms))
+        return GQA_ERR_WORKSPACE;
+    float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
+    P.ws_o = w;
+    P.ws_ml = w + (size_t)P.G * P.nq * D;
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)num_pages * page;
+    const uint32_t box_rows = page < TILE ? (uint32_t)page : (uint32_t)TILE;
+    if (!make_map_2d_u8(&tk, kcache, rows, D, box_rows, 128) ||
+        !make_map_2d_u8(&tv, vcache, rows, D, box_rows, 128))
+        return GQA_ERR_CUDA;
+    return launch_split(tk, tv, P, stream, di->device);
+}
+
+size_t paged_e4m3_batch_workspace_bytes(int R, int batch, int num_sms) {
+    const int G = batch > num_sms ? batch : num_sms;
+    const size_t nq = (size_t)R * kHq;
+    return kWorkspaceCounterBytes + (size_t)G * nq * (paged::D + 2) * sizeof(float) + 256;
+}
+
+// Several sequences' tails in one launch: q/out [batch, R, 6, 256], block
+// tables [batch, table_stride], context lengths read on the device.  The grid
+// has max(SMs, batch) splits, shared out between the sequences in proportion
+// to their tile counts (split_owner).
+int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                            const float* kscale, const float* vscale,
+                            const int32_t* block_tables, int table_stride, int num_pages,
+                            int page, const int* ctx_lens_dev, int max_ctx_len, int batch,
+                            int R, float scale, void* out, cudaStream_t stream) {
+    using namespace paged;
+    const DeviceInfo* di = device_info();
+    if (!di) return GQA_ERR_CUDA;
+    Params P;
+    P.kcache = kcache;
+    P.vcache = vcache;
+    P.kscale = kscale;
+    P.vscale = vscale;
+    P.table = block_tables;
+    P.q = static_cast<const __half*>(q);
+    P.ctx_dev = ctx_lens_dev;
+    P.batch = batch;
+    P.table_stride = table_stride;
+    P.page = page;
+    P.log2_page = __builtin_ctz((unsigned)page);
+    P.num_pages = num_pages;
+    P.ctx_len = max_ctx_len;
+    P.R = R;
+    P.nq = R * HQ;
+    P.n_tiles = (max_ctx_len + TILE - 1) / TILE;
+    P.G = batch > di->num_sms ? batch : di->num_sms;
+    if (P.G > MERGE_MAX_SPLITS) return GQA_ERR_UNSUPPORTED;
+    P.scale = scale;
+    P.out = static_cast<__half*>(out);
+    P.err = di->err_word;
+    void* ws;
+    size_t ws_bytes;
+    current_workspace(&ws, &ws_bytes);
+    if (!ws || ws_bytes < paged_e4m3_batch_workspace_bytes(R, batch, di->num_sms))
         return GQA_ERR_WORKSPACE;
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
@@ -1051,6 +1207,8 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.table = block_table;
     P.q = static_cast<const __half*>(q);
     P.ctx_dev = nullptr;
+    P.batch = 1;
+    P.table_stride = 0;
     P.page = page;
     P.log2_page = __builtin_ctz((unsigned)page);
     P.num_pages = num_pages;
