@@ -435,16 +435,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 slot = rg.slot();
                 return mbar_wait(bar_full(s_bars, slot), rg.phase(), abort_flag, P.err);
             };
+            // Non-blocking look at the ring position after the current one; its
+            // latency overlaps the current slot's UMMA issue, and a slot found
+            // full needs no wait later.
+            auto peek_next = [&](const Ring& rg) -> bool {
+                Ring nx = rg;
+                ++nx.n;
+                return mbar_test(bar_full(s_bars, nx.slot()), nx.phase());
+            };
             // Descriptor low words: Q chunk c at q_lo + c * (BM * 128 >> 4); a K
             // slot's chunk cc at + cc * (HALF_SLOT >> 4); a K step of 16
             // elements (32 bytes) at + 2.
             const uint32_t q_lo = desc_lo(s_q, 16);
             auto issue_qk = [&](uint32_t s_col) -> bool {
                 const uint32_t d = tmem + s_col;
+                bool next_ready = false;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    int slot;
-                    if (!take(kr, slot)) return false;
+                    int slot = kr.slot();
+                    if (!next_ready && !take(kr, slot)) return false;
+                    if (h == 0) next_ready = peek_next(kr);
                     const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
@@ -466,10 +476,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             auto issue_pv = [&](uint32_t s_col, bool acc0) -> bool {
                 const uint32_t p_base = tmem + s_col;
+                bool next_ready = false;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    int slot;
-                    if (!take(vr, slot)) return false;
+                    int slot = vr.slot();
+                    if (!next_ready && !take(vr, slot)) return false;
+                    if (h == 0) next_ready = peek_next(vr);
                     // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
                     // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
                     const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
