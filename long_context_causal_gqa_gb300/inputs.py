@@ -138,6 +138,33 @@ def paged_e4m3_inputs(R: int, ctx_len: int, capacity: int = 262144, seed: int = 
 
 
 @dataclasses.dataclass
+class PagedE4M3BatchInputs:
+    cache: PagedE4M3Inputs     # the shared cache, scales and its own (unused) tail q
+    tables: torch.Tensor       # [batch, stride] int32: sequence b's logical pages
+    q: torch.Tensor            # [batch, R, Hq, D] fp16
+    ctx_lens: list             # per-sequence context lengths
+    max_ctx: int
+
+
+def paged_e4m3_batch_inputs(ctx_lens, R: int, max_ctx: int, seed: int = 0, page: int = PAGE,
+                            Hq: int = HQ, Hkv: int = HKV, D: int = HEAD_DIM,
+                            scale: float = SCALE) -> PagedE4M3BatchInputs:
+    """Batched verifier tails over one shared E4M3 cache: sequence b owns a run
+    of ceil(max_ctx / page) consecutive logical pages of one permuted cache
+    (the whole run is addressable, so its context can grow up to max_ctx),
+    reached through row b of the block-table matrix; q per sequence is N(0,1)
+    fp16.  Physical pages that no sequence names hold the poison byte."""
+    assert all(1 <= R <= c <= max_ctx for c in ctx_lens)
+    per = (max_ctx + page - 1) // page
+    total = per * len(ctx_lens) * page
+    cache = paged_e4m3_inputs(R=1, ctx_len=total, capacity=total + 4 * page, seed=seed,
+                              page=page, Hq=Hq, Hkv=Hkv, D=D, scale=scale)
+    tables = cache.block_table[: per * len(ctx_lens)].view(len(ctx_lens), per).clone()
+    q = normal_fp16((len(ctx_lens), R, Hq, D), seed * 5 + 4)
+    return PagedE4M3BatchInputs(cache, tables, q, list(ctx_lens), max_ctx)
+
+
+@dataclasses.dataclass
 class SparseInputs:
     q: torch.Tensor            # [rows, Hq, D] fp16
     kcache: torch.Tensor       # [num_pages, page, Hkv, D] fp16

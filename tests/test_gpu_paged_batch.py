@@ -28,20 +28,8 @@ def _check(got, ref, what):
 
 
 def _batch(ctxs, R, max_ctx, page=16, seed=0):
-    """Sequences as consecutive runs of logical pages of one cache."""
-    n = [(max_ctx + page - 1) // page for _ in ctxs]       # pages reserved per sequence
-    total = sum(n) * page
-    big = inputs.paged_e4m3_inputs(R=1, ctx_len=total, capacity=total + 4 * page, seed=seed,
-                                   page=page)
-    stride = max(n)
-    tables = torch.zeros((len(ctxs), stride), dtype=torch.int32)
-    p0 = 0
-    for b, nb in enumerate(n):
-        tables[b, :nb] = big.block_table[p0:p0 + nb]
-        p0 += nb
-    g = torch.Generator().manual_seed(seed + 1)
-    q = torch.randn((len(ctxs), R, 6, 256), generator=g).to(torch.float16)
-    return big, tables, q
+    bi = inputs.paged_e4m3_batch_inputs(ctxs, R, max_ctx, seed=seed, page=page)
+    return bi.cache, bi.tables, bi.q
 
 
 def _run_and_check(cuda_lib, big, tables, q, ctxs, max_ctx, out=None, what=""):
