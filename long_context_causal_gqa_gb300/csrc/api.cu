@@ -75,11 +75,11 @@ EncodeTiledFn encode_tiled() {
 }
 
 bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, uint32_t box_cols) {
+                     uint64_t row_stride, uint32_t box_rows, uint32_t box_cols) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {row_stride * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
@@ -90,11 +90,11 @@ bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 }
 
 bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows, uint32_t box_cols) {
+                    uint64_t row_stride, uint32_t box_rows, uint32_t box_cols) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols};
+    cuuint64_t strides[1] = {row_stride};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
@@ -112,6 +112,18 @@ namespace {
 
 bool family_ok(int Hq, int Hkv, int D) { return Hq == kHq && Hkv == kHkv && D == kHeadDim; }
 
+// The dense prefill and the E4M3 tail take any grouping with D = 256: Hkv KV
+// heads, each shared by Hq / Hkv query heads.
+bool prefill_family_ok(int Hq, int Hkv, int D) {
+    return D == kHeadDim && Hq >= 1 && Hq <= kMaxHeads && Hkv >= 1 && Hq % Hkv == 0;
+}
+
+// One tail launch packs query_rows x (Hq / Hkv) rows into the UMMA N dimension.
+bool tail_family_ok(int Hq, int Hkv, int D, int query_rows) {
+    return prefill_family_ok(Hq, Hkv, D) &&
+           (long long)query_rows * (Hq / Hkv) <= kMaxTailPackedRows;
+}
+
 bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
 
 }  // namespace
@@ -124,9 +136,9 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return GQA_ERR_INVALID_ARG;
     if (Q < 1 || KV < 1 || Q > KV || !scale_ok(scale)) return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
+    if (!prefill_family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
     if ((long long)Q * Hq > 0x7fffffffLL - 256) return GQA_ERR_INVALID_ARG;
-    return prefill_launch(q, k, v, out, Q, KV, scale, stream);
+    return prefill_launch(q, k, v, out, Q, KV, Hq, Hkv, scale, stream);
 }
 
 int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -142,10 +154,10 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
         return GQA_ERR_INVALID_ARG;
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, page,
-                             ctx_len, nullptr, query_rows, scale, out, stream);
+                             ctx_len, nullptr, query_rows, Hq, Hkv, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -165,13 +177,13 @@ int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_
     if (query_rows < 1 || max_ctx_len < query_rows || num_pages < 1 || batch < 1 ||
         !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8 || batch > kMaxTailBatch)
+    if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page) || batch > kMaxTailBatch)
         return GQA_ERR_UNSUPPORTED;
     if ((long long)max_ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     if ((long long)table_stride * page < (long long)max_ctx_len) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_batch_launch(q, kcache, vcache, kscale, vscale, block_tables, table_stride,
                                    num_pages, page, ctx_lens_dev, max_ctx_len, batch, query_rows,
-                                   scale, out, stream);
+                                   Hq, Hkv, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -190,10 +202,10 @@ int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8
         return GQA_ERR_INVALID_ARG;
     if (query_rows < 1 || max_ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)max_ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, page,
-                             max_ctx_len, ctx_len_dev, query_rows, scale, out, stream);
+                             max_ctx_len, ctx_len_dev, query_rows, Hq, Hkv, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -210,10 +222,10 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
         return GQA_ERR_INVALID_ARG;
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || !page_ok(page) || query_rows > 8) return GQA_ERR_UNSUPPORTED;
+    if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_noalloc_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages,
-                                     page, ctx_len, query_rows, scale, out, stream);
+                                     page, ctx_len, query_rows, Hq, Hkv, scale, out, stream);
 }
 
 int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
@@ -238,20 +250,23 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {
-    if (Hq != kHq || D != kHeadDim || query_rows < 1 || ctx_or_kv < 1) return 0;
+    if (D != kHeadDim || query_rows < 1 || ctx_or_kv < 1) return 0;
+    if (kind == GQA_KIND_SPARSE ? Hq != kHq : (Hq < 1 || Hq > kMaxHeads)) return 0;
     const DeviceInfo* di = device_info();
     if (!di) return 0;
+    // The tail's partials are sized for query_rows x Hq packed rows, enough
+    // for any number of KV heads (one launch takes query_rows x Hq / Hkv).
     if (kind == GQA_KIND_PAGED_E4M3_BATCH) {   // ctx_or_kv = number of sequences
-        if (query_rows > 8 || ctx_or_kv > kMaxTailBatch) return 0;
-        return paged_e4m3_batch_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
+        if (query_rows > kMaxTailPackedRows || ctx_or_kv > kMaxTailBatch) return 0;
+        return paged_e4m3_batch_workspace_bytes(query_rows * Hq, ctx_or_kv, di->num_sms);
     }
     if (ctx_or_kv < query_rows) return 0;
     switch (kind) {
         case GQA_KIND_PREFILL:
             return prefill_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
         case GQA_KIND_PAGED_E4M3:
-            if (query_rows > 8) return 0;
-            return paged_e4m3_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
+            if (query_rows > kMaxTailPackedRows) return 0;
+            return paged_e4m3_workspace_bytes(query_rows * Hq, ctx_or_kv, di->num_sms);
         case GQA_KIND_SPARSE:
             return kWorkspaceCounterBytes;
         default:

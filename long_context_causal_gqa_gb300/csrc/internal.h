@@ -14,6 +14,8 @@ namespace gqa {
 constexpr int kHq = 6;
 constexpr int kHkv = 1;
 constexpr int kHeadDim = 256;
+constexpr int kMaxHeads = 64;          // query heads accepted by the prefill and the E4M3 tail
+constexpr int kMaxTailPackedRows = 48; // query rows x query heads per KV head in one tail launch
 constexpr int kPage = 16;   // the pages' page size; any power of two in [8, 256] is accepted
 
 // Page sizes the paged kernels take: a power of two in [8, 256] (so that a
@@ -44,41 +46,71 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled();
 
-// 2D fp16 row-major tensor [rows, cols] with a box of [box_rows, box_cols]
-// (box_cols * 2 bytes <= 128), 128-byte swizzle, zero fill out of bounds.
+// 2D fp16 tensor [rows, cols], rows row_stride elements apart (a multiple of
+// 8), with a box of [box_rows, box_cols] (box_cols * 2 bytes <= 128), 128-byte
+// swizzle, zero fill out of bounds.
 bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, uint32_t box_cols);
+                     uint64_t row_stride, uint32_t box_rows, uint32_t box_cols);
 
-// 2D uint8 row-major tensor [rows, cols] with a box of [box_rows, box_cols]
-// (box_cols <= 128), 128-byte swizzle.
+// 2D uint8 tensor [rows, cols], rows row_stride bytes apart (a multiple of
+// 16), with a box of [box_rows, box_cols] (box_cols <= 128), 128-byte swizzle.
 bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows, uint32_t box_cols);
+                    uint64_t row_stride, uint32_t box_rows, uint32_t box_cols);
+
+// Exact unsigned division by a divisor fixed per launch, for dividends below
+// 2^31: the multiply-high method of Granlund and Montgomery ("Division by
+// invariant integers using multiplication", 1994, section 4), with
+// l = ceil(log2 d) and mul = floor(2^32 (2^l - d) / d) + 1.
+struct FastDiv {
+    uint32_t mul;
+    int shift;
+    int d;
+    __host__ __device__ int div(int n) const {
+#ifdef __CUDA_ARCH__
+        return (int)((__umulhi(mul, (uint32_t)n) + (uint32_t)n) >> shift);
+#else
+        return n / d;
+#endif
+    }
+};
+
+inline FastDiv make_fastdiv(int d) {
+    FastDiv f;
+    f.d = d;
+    int l = 0;
+    while ((1LL << l) < d) ++l;
+    f.shift = l;
+    f.mul = (uint32_t)((((1ULL << l) - (unsigned long long)d) << 32) / (unsigned long long)d + 1);
+    return f;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (one per kernel family).  Arguments are validated by the caller.
 int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
-                   float scale, cudaStream_t stream);
+                   int Hq, int Hkv, float scale, cudaStream_t stream);
 size_t prefill_workspace_bytes(int Q, int KV, int num_sms);
 int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill kernel
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
                       int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
-                      float scale, void* out, cudaStream_t stream);
-size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms);
+                      int Hq, int Hkv, float scale, void* out, cudaStream_t stream);
+// nq = packed rows of one launch (at most query_rows * Hq).
+size_t paged_e4m3_workspace_bytes(int nq, int ctx_len, int num_sms);
 int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                             const float* kscale, const float* vscale,
                             const int32_t* block_tables, int table_stride, int num_pages,
                             int page, const int* ctx_lens_dev, int max_ctx_len, int batch,
-                            int R, float scale, void* out, cudaStream_t stream);
-size_t paged_e4m3_batch_workspace_bytes(int R, int batch, int num_sms);
+                            int R, int Hq, int Hkv, float scale, void* out, cudaStream_t stream);
+size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms);
 
 // Same as paged_e4m3_launch, with the split partials in a static device array.
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                               const float* kscale, const float* vscale,
                               const int32_t* block_table, int num_pages, int page, int ctx_len,
-                              int R, float scale, void* out, cudaStream_t stream);
+                              int R, int Hq, int Hkv, float scale, void* out,
+                              cudaStream_t stream);
 
 int sparse_launch(const void* q, const void* kcache, const void* vcache,
                   const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,

@@ -57,7 +57,6 @@ namespace gqa {
 namespace paged {
 
 constexpr int D = kHeadDim;      // 256
-constexpr int HQ = kHq;          // 6
 constexpr int TILE = 128;        // keys per tile
 constexpr int RAW_STAGE = TILE * D;             // 32 KB of E4M3 per K or V tile
 // Threads of a CTA with NWG softmax warpgroups: producer warp, UMMA warp,
@@ -77,12 +76,22 @@ struct Params {
     int table_stride;     // block-table entries per sequence
     int page, log2_page;  // tokens per cache page, a power of two in [8, 256]
     int num_pages, ctx_len, R, nq, n_tiles, G;
+    int hq;               // query heads per position in q / out
+    FastDiv grp;          // packed rows per position in one launch (query heads of one KV head)
     float scale;
     float* ws_o;    // [G][nq][D] unnormalised partial O (in units of the E4M3 V)
     float* ws_ml;   // [G][nq][2]  (m in log2 units, l)
     __half* out;
     unsigned* err;
 };
+
+// Element offset of packed row r of sequence seq in q / out.  Packed row r is
+// position r / grp of the sequence's tail and the (r mod grp)-th query head of
+// the launch's KV head; q / out already point at that head group's first head.
+__device__ __forceinline__ size_t row_offset(const Params& P, int seq, int r) {
+    const int pos = P.grp.div(r);
+    return ((size_t)(seq * P.R + pos) * P.hq + (r - pos * P.grp.d)) * D;
+}
 
 template <int NP, int NWG>
 struct Layout {
@@ -526,7 +535,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             for (int i = 0; i < RPW; ++i) {
                 const int r = warp - 1 + QW * i;
                 raw[i] = (r < P.nq) ? *reinterpret_cast<const uint4*>(
-                                          P.q + ((size_t)seq * P.nq + r) * D + d0)
+                                          P.q + row_offset(P, seq, r) + d0)
                                     : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
@@ -706,7 +715,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
                     for (int c = 0; c < NH; ++c) {
                         const int cg = c0 + c;
-                        const bool vis = (cg < P.nq) ? (key <= lim_base + cg / HQ) : (key < ctx_len);
+                        const bool vis = (cg < P.nq) ? (key <= lim_base + P.grp.div(cg)) : (key < ctx_len);
                         if (!vis) s[c] = -INFINITY;
                     }
                 }
@@ -987,7 +996,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
         uint2 pk;
         pk.x = *reinterpret_cast<const uint32_t*>(&h01);
         pk.y = *reinterpret_cast<const uint32_t*>(&h23);
-        *reinterpret_cast<uint2*>(P.out + ((size_t)seq * P.nq + c) * D + d0) = pk;
+        *reinterpret_cast<uint2*>(P.out + row_offset(P, seq, c) + d0) = pk;
     }
 }
 
@@ -1039,19 +1048,49 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaSt
     return launch_np<48, 6>(tk, tv, P, stream, device);
 }
 
+// Grouping fields: Hq query heads per position, Hkv KV heads, each shared by
+// Hq / Hkv query heads; one launch takes one KV head's R * Hq / Hkv packed rows.
+void set_grouping(Params& P, int Hq, int Hkv) {
+    P.hq = Hq;
+    P.grp = make_fastdiv(Hq / Hkv);
+    P.nq = P.R * (Hq / Hkv);
+}
+
+// Split + merge once per KV head.  Head g reads row g of every cache token
+// (the caches [num_pages * page, Hkv, D] seen as rows Hkv * D bytes apart) and
+// writes query heads g * grp .. g * grp + grp - 1.  Launches on one stream run
+// in order, so they can share the split partials.
+int launch_heads(Params& P, const void* q, void* out, const uint8_t* kcache,
+                 const uint8_t* vcache, int Hkv, cudaStream_t stream, int device) {
+    const uint64_t rows = (uint64_t)P.num_pages * P.page;
+    const uint32_t box_rows = P.page < TILE ? (uint32_t)P.page : (uint32_t)TILE;
+    for (int g = 0; g < Hkv; ++g) {
+        CUtensorMap tk, tv;
+        if (!make_map_2d_u8(&tk, kcache + (size_t)g * D, rows, D, (uint64_t)Hkv * D, box_rows,
+                            128) ||
+            !make_map_2d_u8(&tv, vcache + (size_t)g * D, rows, D, (uint64_t)Hkv * D, box_rows,
+                            128))
+            return GQA_ERR_CUDA;
+        P.q = static_cast<const __half*>(q) + (size_t)g * P.grp.d * D;
+        P.out = static_cast<__half*>(out) + (size_t)g * P.grp.d * D;
+        const int rc = launch_split(tk, tv, P, stream, device);
+        if (rc != GQA_OK) return rc;
+    }
+    return GQA_OK;
+}
+
 }  // namespace paged
 
-size_t paged_e4m3_workspace_bytes(int R, int ctx_len, int num_sms) {
+size_t paged_e4m3_workspace_bytes(int nq, int ctx_len, int num_sms) {
     const int n_tiles = (ctx_len + paged::TILE - 1) / paged::TILE;
     const int G = n_tiles < num_sms ? n_tiles : num_sms;
-    const size_t nq = (size_t)R * kHq;
     return kWorkspaceCounterBytes + (size_t)G * nq * (paged::D + 2) * sizeof(float) + 256;
 }
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
                       int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
-                      float scale, void* out, cudaStream_t stream) {
+                      int Hq, int Hkv, float scale, void* out, cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -1070,7 +1109,7 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
-    P.nq = R * HQ;
+    set_grouping(P, Hq, Hkv);
     P.n_tiles = (ctx_len + TILE - 1) / TILE;
     P.G = P.n_tiles < di->num_sms ? P.n_tiles : di->num_sms;
     if (P.G > MERGE_MAX_SPLITS) P.G = MERGE_MAX_SPLITS;
@@ -1080,27 +1119,20 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     void* ws;
     size_t ws_bytes;
     current_workspace(&ws, &ws_bytes);
-    if (!ws || ws_bytes < paged_e4m3_workspace_bytes(R, ctx_len, di->num_sms))
+    if (!ws || ws_bytes < paged_e4m3_workspace_bytes(P.nq, ctx_len, di->num_sms))
         return GQA_ERR_WORKSPACE;
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
     P.ws_ml = w + (size_t)P.G * P.nq * D;
-    CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)num_pages * page;
-    const uint32_t box_rows = page < TILE ? (uint32_t)page : (uint32_t)TILE;
-    if (!make_map_2d_u8(&tk, kcache, rows, D, box_rows, 128) ||
-        !make_map_2d_u8(&tv, vcache, rows, D, box_rows, 128))
-        return GQA_ERR_CUDA;
-    return launch_split(tk, tv, P, stream, di->device);
+    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
-size_t paged_e4m3_batch_workspace_bytes(int R, int batch, int num_sms) {
+size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms) {
     const int G = batch > num_sms ? batch : num_sms;
-    const size_t nq = (size_t)R * kHq;
     return kWorkspaceCounterBytes + (size_t)G * nq * (paged::D + 2) * sizeof(float) + 256;
 }
 
-// Several sequences' tails in one launch: q/out [batch, R, 6, 256], block
+// Several sequences' tails in one launch: q/out [batch, R, Hq, 256], block
 // tables [batch, table_stride], context lengths read on the device.  The grid
 // has max(SMs, batch) splits, shared out between the sequences in proportion
 // to their tile counts (split_owner).
@@ -1108,7 +1140,7 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
                             const float* kscale, const float* vscale,
                             const int32_t* block_tables, int table_stride, int num_pages,
                             int page, const int* ctx_lens_dev, int max_ctx_len, int batch,
-                            int R, float scale, void* out, cudaStream_t stream) {
+                            int R, int Hq, int Hkv, float scale, void* out, cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -1127,7 +1159,7 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
     P.num_pages = num_pages;
     P.ctx_len = max_ctx_len;
     P.R = R;
-    P.nq = R * HQ;
+    set_grouping(P, Hq, Hkv);
     P.n_tiles = (max_ctx_len + TILE - 1) / TILE;
     P.G = batch > di->num_sms ? batch : di->num_sms;
     if (P.G > MERGE_MAX_SPLITS) return GQA_ERR_UNSUPPORTED;
@@ -1137,18 +1169,12 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
     void* ws;
     size_t ws_bytes;
     current_workspace(&ws, &ws_bytes);
-    if (!ws || ws_bytes < paged_e4m3_batch_workspace_bytes(R, batch, di->num_sms))
+    if (!ws || ws_bytes < paged_e4m3_batch_workspace_bytes(P.nq, batch, di->num_sms))
         return GQA_ERR_WORKSPACE;
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
     P.ws_ml = w + (size_t)P.G * P.nq * D;
-    CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)num_pages * page;
-    const uint32_t box_rows = page < TILE ? (uint32_t)page : (uint32_t)TILE;
-    if (!make_map_2d_u8(&tk, kcache, rows, D, box_rows, 128) ||
-        !make_map_2d_u8(&tv, vcache, rows, D, box_rows, 128))
-        return GQA_ERR_CUDA;
-    return launch_split(tk, tv, P, stream, di->device);
+    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
 }  // namespace gqa
@@ -1163,7 +1189,7 @@ namespace gqa {
 namespace paged {
 
 constexpr int kNoAllocMaxSplits = 160;
-constexpr int kNoAllocMaxRows = 8 * HQ;  // query_rows <= 8
+constexpr int kNoAllocMaxRows = 48;  // packed rows per launch
 constexpr size_t kNoAllocFloats = (size_t)kNoAllocMaxSplits * kNoAllocMaxRows * (D + 2);
 
 // Split partials (O, then (m, l)) of gqa_attn_paged_e4m3_noalloc: about
@@ -1179,7 +1205,8 @@ size_t paged_e4m3_noalloc_capacity_floats() { return paged::kNoAllocFloats; }
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                               const float* kscale, const float* vscale,
                               const int32_t* block_table, int num_pages, int page, int ctx_len,
-                              int R, float scale, void* out, cudaStream_t stream) {
+                              int R, int Hq, int Hkv, float scale, void* out,
+                              cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -1214,7 +1241,7 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
-    P.nq = R * HQ;
+    set_grouping(P, Hq, Hkv);
     P.n_tiles = (ctx_len + TILE - 1) / TILE;
     P.G = P.n_tiles < di->num_sms ? P.n_tiles : di->num_sms;
     if (P.G > kNoAllocMaxSplits) P.G = kNoAllocMaxSplits;
@@ -1225,13 +1252,7 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
         return GQA_ERR_WORKSPACE;
     P.ws_o = scratch;
     P.ws_ml = scratch + (size_t)P.G * P.nq * D;
-    CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)num_pages * page;
-    const uint32_t box_rows = page < TILE ? (uint32_t)page : (uint32_t)TILE;
-    if (!make_map_2d_u8(&tk, kcache, rows, D, box_rows, 128) ||
-        !make_map_2d_u8(&tv, vcache, rows, D, box_rows, 128))
-        return GQA_ERR_CUDA;
-    return launch_split(tk, tv, P, stream, di->device);
+    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
 }  // namespace gqa

@@ -9,6 +9,10 @@
 //
 // * Head packing.  q is [Q, 6, 256] = [6Q, 256] row-major, so consecutive
 //   flattened rows (positions x 6 heads) form the M tiles with no padding.
+//   Other groupings at D = 256: with one KV head and Hq query heads the
+//   packed rows are positions x Hq; with Hkv > 1 KV heads the kernel runs once
+//   per query head over strided views (one packed row per position), reading
+//   the KV head h / (Hq / Hkv).
 // * CTA pairs (cta_group::2).  A cluster of two CTAs on neighbouring SMs
 //   takes a pair tile of 256 packed rows, 128 per CTA, and runs one M = 256
 //   UMMA stream issued by the even CTA:
@@ -56,7 +60,6 @@ constexpr int BM = 128;         // packed query rows per CTA
 constexpr int BM2 = 2 * BM;     // packed query rows per CTA pair
 constexpr int BN = 128;         // keys per KV tile
 constexpr int D = kHeadDim;     // 256
-constexpr int HQ = kHq;         // 6
 // Ring slots of 16 KB.  A K slot holds this CTA's 64 keys x two 64-wide d
 // chunks (8 KB each); a V slot holds two 32-key sub-tiles x this CTA's 128 d
 // (8 KB each, two 64-wide atoms of 4 KB).  A tile's half of K or V is two slots.
@@ -97,6 +100,8 @@ constexpr uint32_t IDESC_PV = idesc_f16_f32(256, 256, false, true);
 
 struct Params {
     int Q, KV, M_total, num_ptiles, G;
+    FastDiv grp;          // packed rows per query position
+    int out_stride;       // elements between consecutive packed rows of out
     long long total;      // causal-visible (pair tile, kv tile) iterations
     float scale_log2;     // scale * log2(e)
     __half* out;
@@ -106,9 +111,9 @@ struct Params {
 };
 
 // KV tiles pair tile t needs: up to the last visible key of its last valid row.
-__host__ __device__ inline int kv_tiles(int t, int Q, int KV, int M_total) {
+__host__ __device__ inline int kv_tiles(int t, int Q, int KV, int M_total, const FastDiv& grp) {
     int last = min(t * BM2 + BM2 - 1, M_total - 1);
-    return (KV - Q + last / HQ) / BN + 1;
+    return (KV - Q + grp.div(last)) / BN + 1;
 }
 
 __host__ __device__ inline long long pair_begin(long long total, int G, int c) {
@@ -127,7 +132,7 @@ struct SegIter {
         cum = 0;
         first = true;
         while (t < P.num_ptiles) {
-            int n = kv_tiles(t, P.Q, P.KV, P.M_total);
+            int n = kv_tiles(t, P.Q, P.KV, P.M_total, P.grp);
             if (cum + n > pos) break;
             cum += n;
             ++t;
@@ -136,7 +141,7 @@ struct SegIter {
     // Next segment; is_first tells whether it is this pair's first segment.
     __device__ bool next(const Params& P, int& pt, int& jb, int& je, int& n, bool& is_first) {
         if (pos >= end) return false;
-        n = kv_tiles(t, P.Q, P.KV, P.M_total);
+        n = kv_tiles(t, P.Q, P.KV, P.M_total, P.grp);
         pt = t;
         jb = (int)(pos - cum);
         long long e = end - cum;
@@ -561,8 +566,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         while (ok && it.next(P, pt, jb, je, n, is_first)) {
             const int m_row = pt * BM2 + BM * (int)rank + row;
             const bool valid = m_row < P.M_total;
-            const int lim = P.KV - P.Q + m_row / HQ;           // last visible key
-            const int j_mask = (P.KV - P.Q + (pt * BM2 + BM * (int)rank) / HQ + 1) / BN;
+            const int lim = P.KV - P.Q + P.grp.div(m_row);      // last visible key
+            const int j_mask = (P.KV - P.Q + P.grp.div(pt * BM2 + BM * (int)rank) + 1) / BN;
             float m_ref = -INFINITY;
             float l = 0.f;
             for (int j = jb; j < je; ++j) {
@@ -682,7 +687,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int h = 1; h < NWG; ++h) l_row += xl[h * BM + row];
             if (jb == 0 && je == n) {
                 const float inv = (l_row > 0.f) ? 1.0f / l_row : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + OCOLS * hg);
+                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * P.out_stride + OCOLS * hg);
 #pragma unroll 1
                 for (int c = 0; c < OCOLS / 32; ++c) {
                     uint32_t o[32];
@@ -787,7 +792,7 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     const float inv = L > 0.f ? 1.0f / L : 0.f;
     uint4 hv = make_uint4(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv),
                           pack_half2(acc[4] * inv, acc[5] * inv), pack_half2(acc[6] * inv, acc[7] * inv));
-    *reinterpret_cast<uint4*>(P.out + (size_t)m_row * D + d0) = hv;
+    *reinterpret_cast<uint4*>(P.out + (size_t)m_row * P.out_stride + d0) = hv;
 }
 
 // Host side of the schedule: the cut pair tiles and their pieces.
@@ -796,7 +801,7 @@ static void find_cut_tiles(const Params& P, MergeTasks& T) {
     long long cum = 0;
     int c = 0;  // first pair whose range ends after cum
     for (int t = 0; t < P.num_ptiles; ++t) {
-        const int n = kv_tiles(t, P.Q, P.KV, P.M_total);
+        const int n = kv_tiles(t, P.Q, P.KV, P.M_total, P.grp);
         const long long t_end = cum + n;
         // pair holding the tile's first iteration
         while (c + 1 < P.G && pair_begin(P.total, P.G, c + 1) <= cum) ++c;
@@ -836,6 +841,28 @@ static int max_pairs(int device) {
     return n;
 }
 
+// One main-kernel launch and, when pair tiles were cut, its merge.
+static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const Params& P, const MergeTasks& tasks, cudaStream_t stream) {
+    prefill_kernel<<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    if (tasks.n > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(tasks.n, BM2 / 8);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel, P, tasks) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+
 }  // namespace prefill
 
 int prefill_resident_pairs() {
@@ -856,7 +883,7 @@ size_t prefill_workspace_bytes(int Q, int KV, int num_sms) {
 }
 
 int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
-                   float scale, cudaStream_t stream) {
+                   int Hq, int Hkv, float scale, cudaStream_t stream) {
     using namespace prefill;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -869,19 +896,27 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     }
     const int pairs_max = max_pairs(di->device);
     if (pairs_max < 1) return GQA_ERR_CUDA;
+    // Query heads that share the single KV head are packed (positions x Hq
+    // rows, one launch); with several KV heads each query head is one launch
+    // over strided views of q, out and its KV head's k / v.
+    const bool packed = (Hkv == 1);
+    const int grp = packed ? Hq : 1;
+    const int launches = packed ? 1 : Hq;
+    const uint64_t q_stride = packed ? (uint64_t)D : (uint64_t)Hq * D;
     Params P;
     P.Q = Q;
     P.KV = KV;
-    P.M_total = Q * HQ;
+    P.grp = make_fastdiv(grp);
+    P.out_stride = (int)q_stride;
+    P.M_total = Q * grp;
     P.num_ptiles = (P.M_total + BM2 - 1) / BM2;
     long long total = 0;
-    for (int t = 0; t < P.num_ptiles; ++t) total += kv_tiles(t, Q, KV, P.M_total);
+    for (int t = 0; t < P.num_ptiles; ++t) total += kv_tiles(t, Q, KV, P.M_total, P.grp);
     P.total = total;
     int G = pairs_max < di->num_sms / 2 ? pairs_max : di->num_sms / 2;
     if (G < 1) G = 1;
     P.G = (int)(total < G ? total : G);
     P.scale_log2 = scale * 1.4426950408889634f;
-    P.out = static_cast<__half*>(out);
     P.err = di->err_word;
 
     void* ws;
@@ -897,30 +932,22 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
         P.ws_o = nullptr;
         P.ws_ml = nullptr;
     }
-
-    CUtensorMap tq, tk, tv;
-    if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, D, BM, 64) ||
-        !make_map_2d_f16(&tk, k, (uint64_t)KV, D, BN / 2, 64) ||
-        !make_map_2d_f16(&tv, v, (uint64_t)KV, D, 32, 64))
-        return GQA_ERR_CUDA;
-
-    prefill_kernel<<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    MergeTasks tasks;  // passed to the merge kernel by value
+    MergeTasks tasks;  // passed to the merge kernel by value; shape-only, same for every head
     find_cut_tiles(P, tasks);
-    if (tasks.n > 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(tasks.n, BM2 / 8);
-        cfg.blockDim = dim3(256);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel, P, tasks) != cudaSuccess)
+
+    for (int h = 0; h < launches; ++h) {
+        const int g = packed ? 0 : h / (Hq / Hkv);
+        const __half* qh = static_cast<const __half*>(q) + (packed ? 0 : (size_t)h * D);
+        const __half* kg = static_cast<const __half*>(k) + (size_t)g * D;
+        const __half* vg = static_cast<const __half*>(v) + (size_t)g * D;
+        P.out = static_cast<__half*>(out) + (packed ? 0 : (size_t)h * D);
+        CUtensorMap tq, tk, tv;
+        if (!make_map_2d_f16(&tq, qh, (uint64_t)P.M_total, D, q_stride, BM, 64) ||
+            !make_map_2d_f16(&tk, kg, (uint64_t)KV, D, (uint64_t)Hkv * D, BN / 2, 64) ||
+            !make_map_2d_f16(&tv, vg, (uint64_t)KV, D, (uint64_t)Hkv * D, 32, 64))
             return GQA_ERR_CUDA;
+        const int rc = launch_one(tq, tk, tv, P, tasks, stream);
+        if (rc != GQA_OK) return rc;
     }
     return GQA_OK;
 }

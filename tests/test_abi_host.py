@@ -62,13 +62,17 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, scale=0.0) == binding.GQA_ERR_INVALID_ARG
     assert _prefill(lib, scale=float("nan")) == binding.GQA_ERR_INVALID_ARG
     assert _prefill(lib, D=128) == binding.GQA_ERR_UNSUPPORTED
-    assert _prefill(lib, Hq=8) == binding.GQA_ERR_UNSUPPORTED
-    assert _prefill(lib, Hkv=2) == binding.GQA_ERR_UNSUPPORTED
+    # Any grouping with Hkv | Hq (Hq <= 64) is accepted; these are not.
+    assert _prefill(lib, Hq=7, Hkv=2) == binding.GQA_ERR_UNSUPPORTED
+    assert _prefill(lib, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED
+    assert _prefill(lib, Hq=65, Hkv=1) == binding.GQA_ERR_UNSUPPORTED
+    assert _prefill(lib, Hkv=0) == binding.GQA_ERR_UNSUPPORTED
+    assert _prefill(lib, Hq=0) == binding.GQA_ERR_UNSUPPORTED
 
 
-def _paged(lib, R=8, ctx=100, pages=8, page=16, D=256, kscale=FAKE, scale=0.0625):
+def _paged(lib, R=8, ctx=100, pages=8, page=16, D=256, kscale=FAKE, scale=0.0625, Hq=6, Hkv=1):
     return lib.gqa_attn_paged_e4m3(FAKE, FAKE, FAKE, kscale, FAKE, FAKE, pages, page, ctx, R,
-                                   6, 1, D, scale, FAKE, None)
+                                   Hq, Hkv, D, scale, FAKE, None)
 
 
 def test_paged_rejects_bad_arguments(lib):
@@ -78,6 +82,11 @@ def test_paged_rejects_bad_arguments(lib):
     assert _paged(lib, page=12) == binding.GQA_ERR_UNSUPPORTED   # not a power of two
     assert _paged(lib, page=512) == binding.GQA_ERR_UNSUPPORTED
     assert _paged(lib, page=4) == binding.GQA_ERR_UNSUPPORTED
+    # One launch packs R x Hq / Hkv rows, at most 48; Hkv must divide Hq.
+    assert _paged(lib, R=7, Hq=8, Hkv=1) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged(lib, R=17, Hq=6, Hkv=2) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged(lib, R=2, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged(lib, R=2, Hq=6, Hkv=0) == binding.GQA_ERR_UNSUPPORTED
     assert _paged(lib, ctx=200, pages=8) == binding.GQA_ERR_INVALID_ARG  # 200 > 8 * 16
     assert _paged(lib, R=8, ctx=5) == binding.GQA_ERR_INVALID_ARG
     assert _paged(lib, scale=-1.0) == binding.GQA_ERR_INVALID_ARG

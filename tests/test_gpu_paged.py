@@ -53,6 +53,25 @@ def test_paged_matches_oracle(cuda_lib, R, ctx, cap):
     _check(out, ref, f"R={R} ctx={ctx}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,R,ctx,cap", [
+    (6, 2, 8, 5000, 8192),    # three query heads per KV head: 24 packed rows, two launches
+    (6, 3, 4, 3001, 4096),    # two per KV head
+    (6, 6, 8, 2000, 2048),    # one per KV head: 8 packed rows, six launches
+    (8, 1, 6, 4100, 8192),    # one KV head, 48 packed rows in one launch
+    (4, 1, 3, 1500, 2048),
+    (1, 1, 16, 2222, 4096),   # sixteen rows of a single head
+    (12, 4, 5, 900, 1024),
+    (8, 2, 2, 7000, 8192),
+])
+def test_paged_other_groupings_match_oracle(cuda_lib, Hq, Hkv, R, ctx, cap):
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx, capacity=cap, seed=Hq * 7 + Hkv + R,
+                                 Hq=Hq, Hkv=Hkv)
+    out = _run(cuda_lib, p)
+    ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                            p.ctx_len, p.scale)
+    _check(out, ref, f"Hq={Hq} Hkv={Hkv} R={R} ctx={ctx}")
+
+
 @pytest.mark.parametrize("R", [1, 2, 8])
 def test_paged_full_size(cuda_lib, R):
     p = inputs.paged_e4m3_inputs(R=R, ctx_len=261888, capacity=262144, seed=R)

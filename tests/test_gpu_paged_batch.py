@@ -27,8 +27,8 @@ def _check(got, ref, what):
     assert err <= 1e-3 and rel <= 1e-2, f"{what}: max abs {err:.3e} rel L2 {rel:.3e}"
 
 
-def _batch(ctxs, R, max_ctx, page=16, seed=0):
-    bi = inputs.paged_e4m3_batch_inputs(ctxs, R, max_ctx, seed=seed, page=page)
+def _batch(ctxs, R, max_ctx, page=16, seed=0, Hq=6, Hkv=1):
+    bi = inputs.paged_e4m3_batch_inputs(ctxs, R, max_ctx, seed=seed, page=page, Hq=Hq, Hkv=Hkv)
     return bi.cache, bi.tables, bi.q
 
 
@@ -61,6 +61,19 @@ def test_batch_matches_oracle_per_sequence(cuda_lib, R, ctxs):
     torch.cuda.synchronize()
     assert cuda_lib.device_error() == 0
     _run_and_check(cuda_lib, big, tables, q, ctxs, max_ctx, out.cpu(), f"R={R}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,R", [(6, 2, 4), (8, 1, 6), (6, 6, 3)])
+def test_batch_other_groupings(cuda_lib, Hq, Hkv, R):
+    ctxs = [3000, 70, 9000, 1]
+    ctxs = [max(c, R) for c in ctxs]
+    max_ctx = max(ctxs)
+    big, tables, q = _batch(ctxs, R, max_ctx, seed=Hq + Hkv, Hq=Hq, Hkv=Hkv)
+    qd, kc, vc, ks, vs, bt, cl = _dev(big, tables, q, ctxs)
+    out = cuda_lib.paged_e4m3_batch(qd, kc, vc, ks, vs, bt, cl, max_ctx, big.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    _run_and_check(cuda_lib, big, tables, q, ctxs, max_ctx, out.cpu(), f"Hq={Hq} Hkv={Hkv}")
 
 
 def test_batch_graph_replay_with_changing_contexts(cuda_lib):

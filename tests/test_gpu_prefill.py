@@ -55,6 +55,59 @@ def test_prefill_matches_oracle(cuda_lib, Q, KV):
     _check(out, ref, f"Q={Q} KV={KV}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,Q,KV", [
+    (6, 2, 300, 1000),   # three query heads per KV head: one launch per query head
+    (6, 3, 130, 700),    # two per KV head
+    (6, 6, 257, 900),    # one per KV head (multi-head attention)
+    (8, 2, 64, 400),
+    (12, 4, 200, 650),
+    (8, 1, 100, 777),    # one KV head, eight packed query heads
+    (4, 1, 333, 1200),
+    (1, 1, 513, 1500),   # one packed row per position
+    (16, 1, 40, 90),     # 16 packed rows per position, 8 positions per 128-row tile
+])
+def test_prefill_other_groupings_match_oracle(cuda_lib, Hq, Hkv, Q, KV):
+    d = inputs.dense_inputs(Q, KV, seed=Q + KV + Hq, Hq=Hq, Hkv=Hkv)
+    out = _run(cuda_lib, d)
+    ref = oracle.dense(d.q, d.k, d.v, d.scale)
+    _check(out, ref, f"Hq={Hq} Hkv={Hkv} Q={Q} KV={KV}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 2), (8, 1)])
+def test_prefill_groupings_split_and_replay(cuda_lib, Hq, Hkv):
+    """Enough work per launch that pair tiles are cut between CTA pairs and
+    merged; sampled rows against the oracle, then bitwise equality of a second
+    run and of CUDA-graph replay (several launches per call when Hkv > 1)."""
+    dev = torch.device("cuda")
+    Q, KV = 2000, 9000
+    d = inputs.dense_inputs(Q, KV, seed=11, Hq=Hq, Hkv=Hkv)
+    q, k, v = d.q.to(dev), d.k.to(dev), d.v.to(dev)
+    a = cuda_lib.prefill(q, k, v, d.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    rows = _sample_rows(Q, n=24, seed=Hq)
+    ref = oracle.dense(d.q, d.k, d.v, d.scale, rows=rows)
+    _check(a[torch.as_tensor(rows, dtype=torch.long)], ref, f"Hq={Hq} Hkv={Hkv}")
+    b = cuda_lib.prefill(q, k, v, d.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        cuda_lib.prefill(q, k, v, d.scale, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.prefill(q, k, v, d.scale, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), a.view(torch.int16))
+    assert cuda_lib.device_error() == 0
+
+
 def _sample_rows(Q, n=48, seed=0):
     rng = np.random.default_rng(seed)
     fixed = [0, 1, 20, 21, 22, 42, 43, Q // 2, Q - 22, Q - 2, Q - 1]
