@@ -712,10 +712,13 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 }
                 const int key = (t_begin + jj) * TILE + k;
                 if ((t_begin + jj) * TILE + TILE - 1 > lim_base) {
+                    // Packed row cg (position cg / grp) sees the key iff
+                    // cg / grp >= key - lim_base, i.e. cg >= (key - lim_base) grp.
+                    const int need = (key - lim_base) * P.grp.d;
 #pragma unroll
                     for (int c = 0; c < NH; ++c) {
                         const int cg = c0 + c;
-                        const bool vis = (cg < P.nq) ? (key <= lim_base + P.grp.div(cg)) : (key < ctx_len);
+                        const bool vis = (cg < P.nq) ? (cg >= need) : (key < ctx_len);
                         if (!vis) s[c] = -INFINITY;
                     }
                 }
@@ -906,6 +909,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     __shared__ float wred[2][MERGE_WARPS];
     const int seq = P.batch > 1 ? (int)blockIdx.x / P.nq : 0;   // sequence
     const int c = (int)blockIdx.x - seq * P.nq;                   // packed row within it
+    const size_t out_off = row_offset(P, seq, c);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int d0 = blockIdx.y * 128 + lane * 4;
@@ -996,7 +1000,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
         uint2 pk;
         pk.x = *reinterpret_cast<const uint32_t*>(&h01);
         pk.y = *reinterpret_cast<const uint32_t*>(&h23);
-        *reinterpret_cast<uint2*>(P.out + row_offset(P, seq, c) + d0) = pk;
+        *reinterpret_cast<uint2*>(P.out + out_off + d0) = pk;
     }
 }
 
