@@ -21,8 +21,12 @@
  *        is in physical-page units; positions clamped to the row.
  *
  * Conventions shared by every entry point
- *   - Supported family: Hq = 6, Hkv = 1, D = 256 (other values return
- *     GQA_ERR_UNSUPPORTED).  scale must be finite and > 0.
+ *   - Head groupings: D = 256; Hkv KV heads, each shared by Hq / Hkv query
+ *     heads (Hkv divides Hq, Hq <= 64).  The pages' family is Hq = 6,
+ *     Hkv = 1; other groupings run one launch per query head (prefill,
+ *     Hkv > 1) or per KV head (E4M3 tail, sparse), with per-entry limits
+ *     below.  Anything else returns GQA_ERR_UNSUPPORTED.  scale must be
+ *     finite and > 0.
  *   - All tensor pointers are DEVICE pointers, contiguous, 16-byte aligned,
  *     owned by the caller.  fp16 means IEEE binary16.
  *   - q / out are [rows, Hq, D] fp16; out is fully overwritten.
@@ -57,8 +61,9 @@ struct CUstream_st; /* cudaStream_t */
 typedef enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, rows > context, bad scale */
-    GQA_ERR_UNSUPPORTED = 2,   /* outside Hq=6, Hkv=1, D=256, page a power of two in [8, 256],
-                                  query_rows<=8 (paged) */
+    GQA_ERR_UNSUPPORTED = 2,   /* D != 256, Hkv not dividing Hq, Hq > 64, page not a power of
+                                  two in [8, 256], query_rows * Hq / Hkv > 48 (E4M3 tail),
+                                  Hq / Hkv > 16 (sparse) */
     GQA_ERR_WORKSPACE = 3,     /* no workspace registered, or it is too small */
     GQA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } gqa_status;
@@ -72,7 +77,9 @@ typedef enum {
 /* Dense causal prefill [P1, Purpose].
  *   q   [Q, Hq, D]  fp16     k, v [KV, Hkv, D] fp16     out [Q, Hq, D] fp16
  *   1 <= Q <= KV.  Row i sees keys 0 .. KV - Q + i.
- * FP32 accumulation; P is rounded to fp16 before the P.V product; the output
+ * With Hkv = 1 the Q x Hq rows are packed into 128-row tiles in one launch;
+ * with Hkv > 1 each query head is one launch over strided views (the
+ * launches share the workspace in stream order).  FP32 accumulation; P is rounded to fp16 before the P.V product; the output
  * is rounded to nearest fp16.  Long problems are split over all SMs; the
  * split partials live in the registered workspace
  * (gqa_workspace_bytes(GQA_KIND_PREFILL, Q, KV, Hq, D) bytes). */
@@ -80,7 +87,9 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
                      int Hq, int Hkv, int D, float scale, struct CUstream_st* stream);
 
 /* Paged FP8-E4M3 verifier tail [P2, What / Changes].
- *   q            [query_rows, Hq, D] fp16, 1 <= query_rows <= 8
+ *   q            [query_rows, Hq, D] fp16, 1 <= query_rows, query_rows * Hq / Hkv
+ *                <= 48 (one launch per KV head packs its query heads x rows;
+ *                the pages' tails are 1..8 rows of 6 heads)
  *   kcache/vcache [num_pages, page, Hkv, D] uint8 E4M3 codes (OCP e4m3fn:
  *                bias 7, 0x7F/0xFF NaN, max 448); real value = decode(byte) * scale
  *   kscale/vscale DEVICE pointers to one fp32 each (graph-capturable)
@@ -164,8 +173,8 @@ int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_
  *     contents.  Nothing in it has to start at zero: a call writes every
  *     partial it reads.  Calls that overlap on the GPU (e.g. on two streams
  *     without ordering) race on the array and give wrong results.
- *   - query_rows > 8 returns GQA_ERR_UNSUPPORTED; a shape whose partials would
- *     not fit the array returns GQA_ERR_WORKSPACE. */
+ *   - query_rows * Hq / Hkv > 48 returns GQA_ERR_UNSUPPORTED; a shape whose
+ *     partials would not fit the array returns GQA_ERR_WORKSPACE. */
 int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                                 const float* kscale, const float* vscale,
                                 const int32_t* block_table, int num_pages, int page,
@@ -183,7 +192,9 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
  * first sel_cnt[i] selected blocks that are <= p; the row's own block is
  * clamped to p.  A row's ids must be distinct.  Ids < 0 or > p / 4 select
  * nothing and flag GQA_DEVERR_BAD_BLOCK_ID.  A row that selects no visible
- * token gets a zero output.  Needs no workspace. */
+ * token gets a zero output.  The selection is shared by all heads of the row;
+ * Hq / Hkv <= 16 (the query heads of one KV head are the N columns of one
+ * launch; Hkv > 1 runs one launch per KV head).  Needs no workspace. */
 int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
                            const int32_t* block_table, const int32_t* sel_idx,
                            const int32_t* sel_cnt, int max_sel, int num_pages, int page,
@@ -198,7 +209,8 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
 
 /* Bytes of workspace an entry point of `kind` needs for the given shape on
  * the current device (query_rows = Q or the tail/row count, ctx_or_kv = KV or
- * ctx_len).  Returns 0 for unsupported arguments. */
+ * ctx_len).  The size holds for any Hkv dividing Hq.  Returns 0 for
+ * unsupported arguments. */
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D);
 
 /* Register caller-owned device memory as the workspace of `device`

@@ -110,8 +110,6 @@ using namespace gqa;
 
 namespace {
 
-bool family_ok(int Hq, int Hkv, int D) { return Hq == kHq && Hkv == kHkv && D == kHeadDim; }
-
 // The dense prefill and the E4M3 tail take any grouping with D = 256: Hkv KV
 // heads, each shared by Hq / Hkv query heads.
 bool prefill_family_ok(int Hq, int Hkv, int D) {
@@ -243,15 +241,16 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || max_sel < 1 ||
         !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!family_ok(Hq, Hkv, D) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
+    if (!prefill_family_ok(Hq, Hkv, D) || Hq / Hkv > kMaxSparseGroup || !page_ok(page))
+        return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return sparse_launch(q, kcache, vcache, block_table, sel_idx, sel_cnt, max_sel, num_pages,
-                         page, ctx_len, query_rows, scale, out, stream);
+                         page, ctx_len, query_rows, Hq, Hkv, scale, out, stream);
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {
     if (D != kHeadDim || query_rows < 1 || ctx_or_kv < 1) return 0;
-    if (kind == GQA_KIND_SPARSE ? Hq != kHq : (Hq < 1 || Hq > kMaxHeads)) return 0;
+    if (Hq < 1 || Hq > kMaxHeads) return 0;
     const DeviceInfo* di = device_info();
     if (!di) return 0;
     // The tail's partials are sized for query_rows x Hq packed rows, enough

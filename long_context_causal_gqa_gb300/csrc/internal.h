@@ -16,6 +16,7 @@ constexpr int kHkv = 1;
 constexpr int kHeadDim = 256;
 constexpr int kMaxHeads = 64;          // query heads accepted by the prefill and the E4M3 tail
 constexpr int kMaxTailPackedRows = 48; // query rows x query heads per KV head in one tail launch
+constexpr int kMaxSparseGroup = 16;    // query heads per KV head in one sparse launch
 constexpr int kPage = 16;   // the pages' page size; any power of two in [8, 256] is accepted
 
 // Page sizes the paged kernels take: a power of two in [8, 256] (so that a
@@ -114,8 +115,8 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
 
 int sparse_launch(const void* q, const void* kcache, const void* vcache,
                   const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
-                  int max_sel, int num_pages, int page, int ctx_len, int rows, float scale,
-                  void* out, cudaStream_t stream);
+                  int max_sel, int num_pages, int page, int ctx_len, int rows, int Hq, int Hkv,
+                  float scale, void* out, cudaStream_t stream);
 
 // Bytes at the start of every workspace reserved for merge counters.
 constexpr size_t kWorkspaceCounterBytes = 4096;

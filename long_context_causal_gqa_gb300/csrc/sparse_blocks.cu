@@ -2,7 +2,8 @@
 //
 // Problem ("[Kernel][SM70] Repair #378 on latest main", Changes): each query
 // row i (position p = ctx_len - rows + i, 6 query heads sharing 1 KV head,
-// D = 256) attends its own list of selected four-token KV blocks of an fp16
+// D = 256; other groupings run one launch per KV head with up to 16 query
+// heads each) attends its own list of selected four-token KV blocks of an fp16
 // page-16 cache (block table in physical-page units); the row's own block is
 // clamped to p, and an index outside 0 .. p/4 selects nothing.  The page
 // converts the blocks into locality-sorted virtual pages for a V100 paged
@@ -37,10 +38,9 @@ namespace gqa {
 namespace sparse {
 
 constexpr int D = kHeadDim;
-constexpr int HQ = kHq;
 constexpr int TILE = 128;            // keys per tile
 constexpr int BLK = 4;               // tokens per selected block
-constexpr int NP = 16;               // 6 heads padded to the UMMA N granule
+constexpr int NP = 16;               // the heads of one launch padded to the UMMA N granule
 constexpr int KV_TILE_BYTES = TILE * D * 2;   // 64 KB
 constexpr int NTHREADS = 320;
 constexpr float RESCALE_THRESHOLD = 8.0f;
@@ -54,6 +54,9 @@ struct Params {
     const int32_t* sel_cnt;
     int max_sel, num_pages, ctx_len, rows, G;
     int log2_page;   // tokens per cache page = 1 << log2_page (8 .. 256)
+    int nh;          // query heads of this launch (those of one KV head), <= NP
+    int q_stride;    // elements between consecutive rows of q / out (Hq * D)
+    int kv_stride;   // elements between consecutive tokens of the caches (Hkv * D)
     float scale_log2;
     __half* out;
     unsigned* err;
@@ -143,7 +146,12 @@ __device__ __forceinline__ int key_token(const Params& P, int i, int cnt, int t,
     return tok <= p ? tok : -1;
 }
 
+// HQ: heads per launch known at compile time (6), or NP with the count read
+// from P.nh (any grouping up to 16 query heads per KV head).
+template <int HQ>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
+    const int nh = (HQ == NP) ? P.nh : HQ;
+    const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * D;
     constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
     constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
     extern __shared__ uint8_t smem_raw[];
@@ -200,17 +208,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
             const int nt = row_tiles(cnt);
             if (nt == 0) continue;
-            // Q row i (6 heads x 256 d) -> Q buffer rloc & 1, rows 0..5.
+            // Q row i (nh heads x 256 d) -> Q buffer rloc & 1, rows 0 .. nh - 1.
             const int qb = rloc & 1;
             if (!mbar_wait(bar(B_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err)) {
                 ok = false;
                 break;
             }
-            for (int u = gt; u < HQ * (D / 8); u += 128) {
+            for (int u = gt; u < nh * (D / 8); u += 128) {
                 const int h = u / (D / 8), c16 = u % (D / 8);
                 const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
                                      sw128(h, c16 % 8);
-                cp_async16(dst, P.q + ((size_t)i * HQ + h) * D + c16 * 8, 16);
+                cp_async16(dst, P.q + (size_t)i * q_stride + h * D + c16 * 8, 16);
             }
             cp_async_arrive(bar(B_QFULL + qb));
             ++rloc;
@@ -225,7 +233,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                         atomicOr(P.err, kErrBadPageId);
                         pg = 0;
                     }
-                    row_l = (((size_t)pg << P.log2_page) + (tok_l & ((1 << P.log2_page) - 1))) * D;
+                    row_l = (((size_t)pg << P.log2_page) + (tok_l & ((1 << P.log2_page) - 1))) *
+                            (HQ == NP ? (size_t)P.kv_stride : (size_t)D);
                 }
                 const int kb = g & 1;
                 for (int kv = 0; kv < 2; ++kv) {
@@ -343,8 +352,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             const int nt = row_tiles(cnt);
             if (nt == 0) {
                 // Nothing selected: the row's output is zero.
-                for (int u = k; u < HQ * (D / 8); u += 128)
-                    reinterpret_cast<uint4*>(P.out + (size_t)i * HQ * D)[u] = make_uint4(0, 0, 0, 0);
+                for (int u = k; u < nh * (D / 8); u += 128)
+                    reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
                 continue;
             }
             if (k < NP) mref[k] = -INFINITY;
@@ -371,7 +380,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 }
                 bool exceed = false;
 #pragma unroll
-                for (int c = 0; c < HQ; ++c) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
+                for (int c = 0; c < HQ; ++c)
+                    if (c < nh) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
                 const unsigned vote = __ballot_sync(0xffffffffu, exceed);
                 volatile int* fl = flags + (g & 1) * 4;
                 if (lane == 0) fl[wq] = vote != 0;
@@ -382,6 +392,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 if (any) {
 #pragma unroll
                     for (int c = 0; c < HQ; ++c) {
+                        if (c >= nh) break;
                         float m = s[c];
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    if (k < HQ) {
+                    if (k < nh) {
                         const int c = k;
                         const float tmax = fmaxf(fmaxf(red[c], red[NP + c]),
                                                  fmaxf(red[2 * NP + c], red[3 * NP + c]));
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 #pragma unroll
                 for (int c = 0; c < NP; ++c) {
                     float p = 0.f;
-                    if (c < HQ) {
+                    if (c < nh) {
                         const float m = mref[c];
                         p = ex2(s[c] - (m == -INFINITY ? 0.f : m));
                         lpart[c] += p;
@@ -455,6 +466,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
+                if (c >= nh) break;
                 float v = lpart[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -477,7 +489,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 const int d = h * 128 + k;
 #pragma unroll
                 for (int c = 0; c < HQ; ++c)
-                    P.out[((size_t)i * HQ + c) * D + d] = __float2half_rn(__uint_as_float(r[c]) * inv[c]);
+                    if (c < nh)
+                        P.out[(size_t)i * q_stride + c * D + d] =
+                            __float2half_rn(__uint_as_float(r[c]) * inv[c]);
             }
             // red / mref are rewritten by the next row only after this barrier.
             ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
@@ -498,15 +512,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 
 int sparse_launch(const void* q, const void* kcache, const void* vcache,
                   const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
-                  int max_sel, int num_pages, int page, int ctx_len, int rows, float scale,
-                  void* out, cudaStream_t stream) {
+                  int max_sel, int num_pages, int page, int ctx_len, int rows, int Hq, int Hkv,
+                  float scale, void* out, cudaStream_t stream) {
     using namespace sparse;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
+    const int grp = Hq / Hkv;
     Params P;
-    P.q = static_cast<const __half*>(q);
-    P.kcache = static_cast<const __half*>(kcache);
-    P.vcache = static_cast<const __half*>(vcache);
     P.table = block_table;
     P.sel_idx = sel_idx;
     P.sel_cnt = sel_cnt;
@@ -516,18 +528,34 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache,
     P.ctx_len = ctx_len;
     P.rows = rows;
     P.G = rows < di->num_sms ? rows : di->num_sms;
+    P.nh = grp;
+    P.q_stride = Hq * D;
+    P.kv_stride = Hkv * D;
     P.scale_log2 = scale * 1.4426950408889634f;
-    P.out = static_cast<__half*>(out);
     P.err = di->err_word;
-    static bool attr_done[64] = {false};
-    if (di->device < 64 && !attr_done[di->device]) {
-        if (cudaFuncSetAttribute(sparse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM) != cudaSuccess)
+    // The 6-head instantiation addresses the caches with a stride of D, so it
+    // serves one KV head only.
+    const bool six = (grp == kHq && Hkv == 1);
+    static bool attr_done[2][64] = {{false}};
+    if (di->device < 64 && !attr_done[six][di->device]) {
+        if (cudaFuncSetAttribute(six ? sparse_kernel<kHq> : sparse_kernel<NP>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
             return GQA_ERR_CUDA;
-        attr_done[di->device] = true;
+        attr_done[six][di->device] = true;
     }
-    sparse_kernel<<<P.G, NTHREADS, SMEM, stream>>>(P);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    // One launch per KV head: query heads g * grp .. g * grp + grp - 1 read
+    // token rows of KV head g.
+    for (int g = 0; g < Hkv; ++g) {
+        P.q = static_cast<const __half*>(q) + (size_t)g * grp * D;
+        P.out = static_cast<__half*>(out) + (size_t)g * grp * D;
+        P.kcache = static_cast<const __half*>(kcache) + (size_t)g * D;
+        P.vcache = static_cast<const __half*>(vcache) + (size_t)g * D;
+        if (six)
+            sparse_kernel<kHq><<<P.G, NTHREADS, SMEM, stream>>>(P);
+        else
+            sparse_kernel<NP><<<P.G, NTHREADS, SMEM, stream>>>(P);
+        if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    }
     return GQA_OK;
 }
 

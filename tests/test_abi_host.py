@@ -107,9 +107,9 @@ def test_paged_devctx_rejects_bad_arguments(lib):
     assert _paged_dev(lib, scale=0.0) == binding.GQA_ERR_INVALID_ARG
 
 
-def _sparse(lib, rows=4, ctx=64, pages=4, max_sel=4, sel=FAKE, D=256):
+def _sparse(lib, rows=4, ctx=64, pages=4, max_sel=4, sel=FAKE, D=256, Hq=6, Hkv=1):
     return lib.gqa_attn_sparse_blocks(FAKE, FAKE, FAKE, FAKE, sel, FAKE, max_sel, pages, 16,
-                                      ctx, rows, 6, 1, D, 0.0625, FAKE, None)
+                                      ctx, rows, Hq, Hkv, D, 0.0625, FAKE, None)
 
 
 def test_sparse_rejects_bad_arguments(lib):
@@ -119,6 +119,9 @@ def test_sparse_rejects_bad_arguments(lib):
     assert _sparse(lib, rows=65, ctx=64) == binding.GQA_ERR_INVALID_ARG
     assert _sparse(lib, ctx=65, pages=4) == binding.GQA_ERR_INVALID_ARG
     assert _sparse(lib, D=64) == binding.GQA_ERR_UNSUPPORTED
+    # At most 16 query heads per KV head; Hkv must divide Hq.
+    assert _sparse(lib, Hq=32, Hkv=1) == binding.GQA_ERR_UNSUPPORTED
+    assert _sparse(lib, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED
 
 
 def test_workspace_registration_validates(lib):
@@ -126,7 +129,7 @@ def test_workspace_registration_validates(lib):
     assert lib.gqa_set_workspace(0, P(0x10010), 1 << 20) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_set_workspace(0, P(0x10000), 16) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_workspace_bytes(0, 8, 16, 6, 128) == 0
-    assert lib.gqa_workspace_bytes(1, 9, 100, 6, 256) == 0
+    assert lib.gqa_workspace_bytes(1, 49, 100, 6, 256) == 0
 
 
 def test_oracle_is_not_imported_by_the_product_path():

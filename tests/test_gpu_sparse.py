@@ -52,6 +52,25 @@ def test_sparse_matches_oracle(cuda_lib, rows, ctx, T):
     _check(out, ref, f"rows={rows} ctx={ctx} T={T}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,rows,ctx,T", [
+    (6, 2, 100, 3001, 512),   # three query heads per KV head, two launches
+    (6, 3, 64, 2048, 64),
+    (6, 6, 50, 1500, 200),    # one query head per KV head
+    (8, 1, 120, 4096, 512),   # one KV head, eight query heads (generic instantiation)
+    (16, 1, 40, 1000, 128),   # sixteen query heads: the full N granule
+    (12, 4, 30, 900, 64),
+    (4, 1, 77, 2000, 300),
+    (1, 1, 90, 1200, 96),
+])
+def test_sparse_other_groupings_match_oracle(cuda_lib, Hq, Hkv, rows, ctx, T):
+    s = inputs.sparse_inputs(rows=rows, ctx_len=ctx, tokens=T, seed=Hq * 5 + Hkv, Hq=Hq, Hkv=Hkv)
+    out = _run(cuda_lib, s)
+    assert cuda_lib.device_error() == 0
+    ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
+                               s.ctx_len, s.scale)
+    _check(out, ref, f"Hq={Hq} Hkv={Hkv} rows={rows} T={T}")
+
+
 @pytest.mark.parametrize("T", [64, 512, 2048])
 def test_sparse_full_size_sampled_rows(cuda_lib, T):
     s = inputs.sparse_inputs(rows=4096, ctx_len=32768, tokens=T, seed=T)
