@@ -12,8 +12,10 @@ L2 is flushed before every timed step.  The same line carries:
 * ``e2e``: the same metric through the C ABI with pinned host buffers and the
   host<->device copies inside the timed region;
 * ``cpu_baseline``: the FP64 CPU oracle on a bounded sample of query rows;
-* ``secondary``: the KV sweep 40K..128K, the paged E4M3 verifier tail at
-  ctx 261888 (HBM roofline) and the selected-block sparse prefill.
+* ``secondary``: KV=128000 (the KV sweep 40K..128K with --sweep), two other
+  head groupings of the headline shape, the paged E4M3 verifier tail at ctx
+  261888 (HBM roofline), a batch of variable-length tails, and the
+  selected-block sparse prefill.
 
 ``--impl reference`` times the CPU oracle alone on the same workload (bounded
 sample per step) and prints the same kind of line with "impl": "reference".
@@ -43,9 +45,9 @@ def visible_pairs(Q: int, KV: int) -> int:
     return Q * (KV - Q) + Q * (Q + 1) // 2
 
 
-def prefill_flops(Q: int, KV: int) -> float:
-    # QK^T and PV: 2 FLOPs per multiply-add each, per head, per visible pair.
-    return 4.0 * D * HQ * visible_pairs(Q, KV)
+def prefill_flops(Q: int, KV: int, Hq: int = HQ) -> float:
+    # QK^T and PV: 2 FLOPs per multiply-add each, per query head, per visible pair.
+    return 4.0 * D * Hq * visible_pairs(Q, KV)
 
 
 def load_peaks():
@@ -205,10 +207,10 @@ def make_flush(device):
     return flush
 
 
-def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0):
+def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0, Hq=HQ, Hkv=1):
     import torch
     from long_context_causal_gqa_gb300 import inputs
-    d = inputs.dense_inputs(Q, KV, seed=seed)
+    d = inputs.dense_inputs(Q, KV, seed=seed, Hq=Hq, Hkv=Hkv)
     q, k, v = d.q.to(device), d.k.to(device), d.v.to(device)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
@@ -419,6 +421,15 @@ def run_gpu(args):
             secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
                               "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
                               "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4)})
+        for hq, hkv in ((6, 2), (8, 1)):
+            # Other head groupings: Hkv > 1 runs one launch per query head.
+            t, _ = bench_prefill(binding, Q, KV, max(3, args.steps // 2), 2, flush, device,
+                                 Hq=hq, Hkv=hkv)
+            ms = statistics.mean(t)
+            fl = prefill_flops(Q, KV, hq)
+            secondary.append({"what": f"prefill Q={Q} KV={KV} Hq={hq} Hkv={hkv}",
+                              "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
+                              "frac_of_peak": round(fl / ms / 1e9 / peak, 4)})
         for R in (1, 2, 8):
             try:
                 t, nbytes, fl = bench_paged(binding, R, device, 50, 5, flush)
@@ -478,7 +489,7 @@ def run_gpu(args):
 
 
 def run_case(args):
-    """One secondary workload alone (for profiling): --case paged|sparse."""
+    """One secondary workload alone (for profiling): --case prefill|paged|paged_batch|sparse."""
     import torch
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
@@ -488,7 +499,15 @@ def run_case(args):
     binding.load()
     peaks = load_peaks()
     flush = make_flush(device)
-    if args.case == "paged_batch":
+    if args.case == "prefill":
+        t, _ = bench_prefill(binding, args.q, args.kv, args.steps, args.warmup, flush, device,
+                             Hq=args.hq, Hkv=args.hkv)
+        ms = statistics.median(t)
+        fl = prefill_flops(args.q, args.kv, args.hq)
+        line = {"case": f"prefill Q={args.q} KV={args.kv} Hq={args.hq} Hkv={args.hkv}",
+                "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
+                "frac_of_peak": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)}
+    elif args.case == "paged_batch":
         t, nbytes, ctxs = bench_paged_batch(binding, device, args.steps, args.warmup, flush)
         us = statistics.median(t) * 1e3
         line = {"case": f"paged E4M3 batch of {len(ctxs)} tails R=2 ({sum(ctxs)} tokens)",
@@ -556,10 +575,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=10.0)
-    ap.add_argument("--case", default="headline", choices=["headline", "paged", "paged_batch",
+    ap.add_argument("--case", default="headline", choices=["headline", "prefill", "paged",
+                                                           "paged_batch",
                                                            "sparse"],
                     help="run one secondary workload alone (profiling)")
     ap.add_argument("--rows", type=int, default=8, help="--case paged: tail rows")
+    ap.add_argument("--hq", type=int, default=HQ, help="--case prefill: query heads")
+    ap.add_argument("--hkv", type=int, default=1, help="--case prefill: KV heads")
     ap.add_argument("--tokens", type=int, default=2048, help="--case sparse: tokens per row")
     args = ap.parse_args()
     if args.warmup < 3:
