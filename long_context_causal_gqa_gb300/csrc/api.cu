@@ -89,6 +89,22 @@ bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_3d_f16(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
+                     uint64_t rows, uint64_t head_stride, uint64_t row_stride,
+                     uint32_t box_rows) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {d, heads, rows};
+    cuuint64_t strides[2] = {head_stride, row_stride};
+    cuuint32_t box[3] = {64, 1, box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t row_stride, uint32_t box_rows, uint32_t box_cols) {
     EncodeTiledFn enc = encode_tiled();

@@ -53,6 +53,13 @@ EncodeTiledFn encode_tiled();
 bool make_map_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint64_t row_stride, uint32_t box_rows, uint32_t box_cols);
 
+// 3D fp16 tensor (d, heads, rows) with heads head_stride bytes apart and rows
+// row_stride bytes apart (multiples of 16), a box of 64 d x 1 head x box_rows
+// rows, 128-byte swizzle, zero fill out of bounds.
+bool make_map_3d_f16(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
+                     uint64_t rows, uint64_t head_stride, uint64_t row_stride,
+                     uint32_t box_rows);
+
 // 2D uint8 tensor [rows, cols], rows row_stride bytes apart (a multiple of
 // 16), with a box of [box_rows, box_cols] (box_cols <= 128), 128-byte swizzle.
 bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

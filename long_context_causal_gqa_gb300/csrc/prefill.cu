@@ -10,9 +10,10 @@
 // * Head packing.  q is [Q, 6, 256] = [6Q, 256] row-major, so consecutive
 //   flattened rows (positions x 6 heads) form the M tiles with no padding.
 //   Other groupings at D = 256: with one KV head and Hq query heads the
-//   packed rows are positions x Hq; with Hkv > 1 KV heads the kernel runs once
-//   per query head over strided views (one packed row per position), reading
-//   the KV head h / (Hq / Hkv).
+//   packed rows are positions x Hq; with Hkv > 1 KV heads every query head
+//   has its own pair tiles (one packed row per position) in the same launch,
+//   reading the KV head h / (Hq / Hkv) through 3-D tensor maps
+//   (d, head, row).
 // * CTA pairs (cta_group::2).  A cluster of two CTAs on neighbouring SMs
 //   takes a pair tile of 256 packed rows, 128 per CTA, and runs one M = 256
 //   UMMA stream issued by the even CTA:
@@ -99,12 +100,15 @@ constexpr uint32_t IDESC_QK = idesc_f16_f32(256, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_f16_f32(256, 256, false, true);
 
 struct Params {
-    int Q, KV, M_total, num_ptiles, G;
+    int Q, KV, M_total, num_ptiles, G;   // M_total, num_ptiles: per head of the tile space
+    int heads;            // heads in the tile space: 1 (packed) or Hq (one per query head)
+    int head_group;       // query heads per KV head (maps a head of the tile space to its KV head)
     FastDiv grp;          // packed rows per query position
     int out_stride;       // elements between consecutive packed rows of out
     long long total;      // causal-visible (pair tile, kv tile) iterations
     float scale_log2;     // scale * log2(e)
     __half* out;
+    FastDiv ptiles;       // divides a tile-space index by num_ptiles (its head)
     float* ws_o;          // [G][2][BM2][D] unnormalised partial O
     float* ws_ml;         // [G][2][BM2][2] partial (m in log2 units, l)
     unsigned* err;
@@ -121,28 +125,46 @@ __host__ __device__ inline long long pair_begin(long long total, int G, int c) {
 }
 
 // Walks the segments (pair tile, [jb, je)) of one pair's iteration range.
+// The tile space is heads x num_ptiles pair tiles, head-major; t is the index
+// in it, (hd, lt) its head and pair tile within the head.  With MH false the
+// tile space is one head (packed rows) and hd stays 0.
+template <bool MH>
 struct SegIter {
     long long pos, end, cum;
-    int t;
+    int t, hd, lt;
     bool first;
+    __device__ void advance(const Params& P) {
+        ++t;
+        ++lt;
+        if (MH && lt == P.num_ptiles) {
+            lt = 0;
+            ++hd;
+        }
+    }
     __device__ void init(const Params& P, int pair) {
         pos = pair_begin(P.total, P.G, pair);
         end = pair_begin(P.total, P.G, pair + 1);
         t = 0;
+        hd = 0;
+        lt = 0;
         cum = 0;
         first = true;
-        while (t < P.num_ptiles) {
-            int n = kv_tiles(t, P.Q, P.KV, P.M_total, P.grp);
+        const int tiles = MH ? P.heads * P.num_ptiles : P.num_ptiles;
+        while (t < tiles) {
+            int n = kv_tiles(lt, P.Q, P.KV, P.M_total, P.grp);
             if (cum + n > pos) break;
             cum += n;
-            ++t;
+            advance(P);
         }
     }
-    // Next segment; is_first tells whether it is this pair's first segment.
-    __device__ bool next(const Params& P, int& pt, int& jb, int& je, int& n, bool& is_first) {
+    // Next segment: pair tile pt of head head; is_first tells whether it is
+    // this pair's first segment.
+    __device__ bool next(const Params& P, int& pt, int& head, int& jb, int& je, int& n,
+                         bool& is_first) {
         if (pos >= end) return false;
-        n = kv_tiles(t, P.Q, P.KV, P.M_total, P.grp);
-        pt = t;
+        n = kv_tiles(lt, P.Q, P.KV, P.M_total, P.grp);
+        pt = lt;
+        head = hd;
         jb = (int)(pos - cum);
         long long e = end - cum;
         je = e < n ? (int)e : n;
@@ -151,7 +173,7 @@ struct SegIter {
         pos = cum + je;
         if (je == n) {
             cum += n;
-            ++t;
+            advance(P);
         }
         return true;
     }
@@ -211,13 +233,23 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
 }
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair.
+// Coordinates (x = d, y = row) of a 2-D map (MH false) or (x = d, head,
+// y = row) of a 3-D map (MH true).
+template <bool MH>
 __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                              int32_t x, int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-        "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
+                                              int32_t x, int32_t head, int32_t y) {
+    if (MH)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::"
+            "complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(head), "r"(y), "r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::"
+            "complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+            : "memory");
 }
 __device__ __forceinline__ void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
@@ -296,6 +328,9 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volati
     return ok;
 }
 
+// MH: the tile space holds one pair-tile range per query head (Hkv > 1,
+// 3-D maps); otherwise one range of packed rows (2-D maps).
+template <bool MH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params P) {
@@ -351,9 +386,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // The merge kernel may be scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;");
 
-    SegIter it;
+    SegIter<MH> it;
     it.init(P, pair);
-    int pt, jb, je, n;
+    int pt, hd, jb, je, n;
     bool is_first;
 
     if (warp == 0 || warp == V_WARP) {
@@ -377,7 +412,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 fb = leader_addr(fb);
                 return true;
             };
-            while (ok && it.next(P, pt, jb, je, n, is_first)) {
+            while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
+                const int kvh = MH ? hd / P.head_group : 0;   // KV head of this segment
                 if (kq) {
                     if (!mbar_wait(bar_qempty(s_bars), (seg & 1) ^ 1, abort_flag, P.err)) {
                         ok = false;
@@ -386,7 +422,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const uint32_t qb = bar_qfull(s_bars);
                     if (leader) mbar_arrive_expect_tx(qb, 2 * Q_BYTES);
                     for (int c = 0; c < 4; ++c)
-                        tma_load_pair(s_q + c * (BM * 128), &tm_q, leader_addr(qb), c * 64,
+                        tma_load_pair<MH>(s_q + c * (BM * 128), &tm_q, leader_addr(qb), c * 64, hd,
                                       pt * BM2 + BM * (int)rank);
                 }
                 for (int j = jb; ok && j < je; ++j) {
@@ -399,14 +435,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         if (kq) {
                             // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
                             for (int cc = 0; cc < 2; ++cc)
-                                tma_load_pair(dst + cc * HALF_SLOT, &tm_k, fb, (2 * h + cc) * 64,
-                                              j * BN + 64 * (int)rank);
+                                tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fb, (2 * h + cc) * 64,
+                                              kvh, j * BN + 64 * (int)rank);
                         } else {
                             // V: sub-tiles 2h, 2h + 1 (32 keys) x this CTA's 128 d
                             for (int ss = 0; ss < 2; ++ss)
                                 for (int a = 0; a < 2; ++a)
-                                    tma_load_pair(dst + ss * HALF_SLOT + a * 4096, &tm_v, fb,
-                                                  128 * (int)rank + 64 * a,
+                                    tma_load_pair<MH>(dst + ss * HALF_SLOT + a * 4096, &tm_v, fb,
+                                                  128 * (int)rank + 64 * a, kvh,
                                                   j * BN + (2 * h + ss) * 32);
                         }
                         ++rg.n;
@@ -510,7 +546,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 return true;
             };
-            while (ok && it.next(P, pt, jb, je, n, is_first)) {
+            while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
                 if (!mbar_wait(bar_qfull(s_bars), seg & 1, abort_flag, P.err)) {
                     ok = false;
                     break;
@@ -563,7 +599,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float sl2 = P.scale_log2;
         uint32_t g = 0;
         bool ok = true;
-        while (ok && it.next(P, pt, jb, je, n, is_first)) {
+        while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
             const int m_row = pt * BM2 + BM * (int)rank + row;
             const bool valid = m_row < P.M_total;
             const int lim = P.KV - P.Q + P.grp.div(m_row);      // last visible key
@@ -687,7 +723,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int h = 1; h < NWG; ++h) l_row += xl[h * BM + row];
             if (jb == 0 && je == n) {
                 const float inv = (l_row > 0.f) ? 1.0f / l_row : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(P.out + (size_t)m_row * P.out_stride + OCOLS * hg);
+                uint4* dst = reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * D : 0) + (size_t)m_row * P.out_stride + OCOLS * hg);
 #pragma unroll 1
                 for (int c = 0; c < OCOLS / 32; ++c) {
                     uint32_t o[32];
@@ -752,7 +788,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // schedule.
 struct MergeTasks {
     int n;
-    int4 task[kMaxClusters];  // (pair tile, c0, slot0, c_last)
+    int4 task[kMaxClusters];  // (tile-space index, c0, slot0, c_last)
 };
 
 // blockIdx.x picks a cut pair tile, blockIdx.y 8 of its 256 rows; thread
@@ -761,12 +797,14 @@ struct MergeTasks {
 // kernel is a programmatic dependent of the main kernel: its launch overlaps
 // that kernel's tail, and griddepcontrol.wait holds it until the partials are
 // complete.
+template <bool MH>
 __global__ void __launch_bounds__(256)
 prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     const int4 tk = T.task[blockIdx.x];
     const int t = tk.x, c0 = tk.y, slot0 = tk.z, c_last = tk.w;
+    const int hd = MH ? P.ptiles.div(t) : 0;        // head of tile-space index t
     const int r = blockIdx.y * 8 + (threadIdx.x >> 5);
-    const int m_row = t * BM2 + r;
+    const int m_row = (t - hd * P.num_ptiles) * BM2 + r;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (m_row >= P.M_total) return;
     const int d0 = (threadIdx.x & 31) * 8;
@@ -792,7 +830,7 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     const float inv = L > 0.f ? 1.0f / L : 0.f;
     uint4 hv = make_uint4(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv),
                           pack_half2(acc[4] * inv, acc[5] * inv), pack_half2(acc[6] * inv, acc[7] * inv));
-    *reinterpret_cast<uint4*>(P.out + (size_t)m_row * P.out_stride + d0) = hv;
+    *reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * D : 0) + (size_t)m_row * P.out_stride + d0) = hv;
 }
 
 // Host side of the schedule: the cut pair tiles and their pieces.
@@ -800,8 +838,8 @@ static void find_cut_tiles(const Params& P, MergeTasks& T) {
     T.n = 0;
     long long cum = 0;
     int c = 0;  // first pair whose range ends after cum
-    for (int t = 0; t < P.num_ptiles; ++t) {
-        const int n = kv_tiles(t, P.Q, P.KV, P.M_total, P.grp);
+    for (int t = 0; t < P.heads * P.num_ptiles; ++t) {
+        const int n = kv_tiles(t % P.num_ptiles, P.Q, P.KV, P.M_total, P.grp);
         const long long t_end = cum + n;
         // pair holding the tile's first iteration
         while (c + 1 < P.G && pair_begin(P.total, P.G, c + 1) <= cum) ++c;
@@ -832,7 +870,8 @@ static int max_pairs(int device) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg) != cudaSuccess || n < 1) {
+    // Both instantiations have the same threads, shared memory and clusters.
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<false>, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
         return 0;
     }
@@ -842,9 +881,10 @@ static int max_pairs(int device) {
 }
 
 // One main-kernel launch and, when pair tiles were cut, its merge.
+template <bool MH>
 static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Params& P, const MergeTasks& tasks, cudaStream_t stream) {
-    prefill_kernel<<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
+    prefill_kernel<MH><<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     if (tasks.n > 0) {
         cudaLaunchConfig_t cfg = {};
@@ -857,7 +897,7 @@ static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel, P, tasks) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel<MH>, P, tasks) != cudaSuccess)
             return GQA_ERR_CUDA;
     }
     return GQA_OK;
@@ -868,7 +908,11 @@ static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 int prefill_resident_pairs() {
     const DeviceInfo* di = device_info();
     if (!di) return -1;
-    if (cudaFuncSetAttribute(prefill::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(prefill::prefill_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             prefill::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(prefill::prefill_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              prefill::SMEM_BYTES) != cudaSuccess)
         return -1;
     return prefill::max_pairs(di->device);
@@ -889,7 +933,11 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     if (!di) return GQA_ERR_CUDA;
     static bool attr_done[64] = {false};
     if (di->device < 64 && !attr_done[di->device]) {
-        if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return GQA_ERR_CUDA;
         attr_done[di->device] = true;
@@ -897,27 +945,31 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     const int pairs_max = max_pairs(di->device);
     if (pairs_max < 1) return GQA_ERR_CUDA;
     // Query heads that share the single KV head are packed (positions x Hq
-    // rows, one launch); with several KV heads each query head is one launch
-    // over strided views of q, out and its KV head's k / v.
+    // rows of one head of the tile space); with several KV heads every query
+    // head is a head of the tile space, with one row per position, in the
+    // same launch.  The tensor maps are (d, head, row) either way.
     const bool packed = (Hkv == 1);
     const int grp = packed ? Hq : 1;
-    const int launches = packed ? 1 : Hq;
-    const uint64_t q_stride = packed ? (uint64_t)D : (uint64_t)Hq * D;
     Params P;
     P.Q = Q;
     P.KV = KV;
+    P.heads = packed ? 1 : Hq;
+    P.head_group = packed ? 1 : Hq / Hkv;
     P.grp = make_fastdiv(grp);
-    P.out_stride = (int)q_stride;
+    P.out_stride = packed ? D : Hq * D;
     P.M_total = Q * grp;
     P.num_ptiles = (P.M_total + BM2 - 1) / BM2;
+    P.ptiles = make_fastdiv(P.num_ptiles);
     long long total = 0;
     for (int t = 0; t < P.num_ptiles; ++t) total += kv_tiles(t, Q, KV, P.M_total, P.grp);
+    total *= P.heads;
     P.total = total;
     int G = pairs_max < di->num_sms / 2 ? pairs_max : di->num_sms / 2;
     if (G < 1) G = 1;
     P.G = (int)(total < G ? total : G);
     P.scale_log2 = scale * 1.4426950408889634f;
     P.err = di->err_word;
+    P.out = static_cast<__half*>(out);
 
     void* ws;
     size_t ws_bytes;
@@ -932,24 +984,26 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
         P.ws_o = nullptr;
         P.ws_ml = nullptr;
     }
-    MergeTasks tasks;  // passed to the merge kernel by value; shape-only, same for every head
+    MergeTasks tasks;  // passed to the merge kernel by value
     find_cut_tiles(P, tasks);
 
-    for (int h = 0; h < launches; ++h) {
-        const int g = packed ? 0 : h / (Hq / Hkv);
-        const __half* qh = static_cast<const __half*>(q) + (packed ? 0 : (size_t)h * D);
-        const __half* kg = static_cast<const __half*>(k) + (size_t)g * D;
-        const __half* vg = static_cast<const __half*>(v) + (size_t)g * D;
-        P.out = static_cast<__half*>(out) + (packed ? 0 : (size_t)h * D);
-        CUtensorMap tq, tk, tv;
-        if (!make_map_2d_f16(&tq, qh, (uint64_t)P.M_total, D, q_stride, BM, 64) ||
-            !make_map_2d_f16(&tk, kg, (uint64_t)KV, D, (uint64_t)Hkv * D, BN / 2, 64) ||
-            !make_map_2d_f16(&tv, vg, (uint64_t)KV, D, (uint64_t)Hkv * D, 32, 64))
+    CUtensorMap tq, tk, tv;
+    if (packed) {
+        if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, D, D, BM, 64) ||
+            !make_map_2d_f16(&tk, k, (uint64_t)KV, D, D, BN / 2, 64) ||
+            !make_map_2d_f16(&tv, v, (uint64_t)KV, D, D, 32, 64))
             return GQA_ERR_CUDA;
-        const int rc = launch_one(tq, tk, tv, P, tasks, stream);
-        if (rc != GQA_OK) return rc;
+        return launch_one<false>(tq, tk, tv, P, tasks, stream);
     }
-    return GQA_OK;
+    const uint64_t row_bytes = 2ull * D;
+    if (!make_map_3d_f16(&tq, q, D, (uint64_t)Hq, (uint64_t)Q, row_bytes,
+                         (uint64_t)Hq * row_bytes, BM) ||
+        !make_map_3d_f16(&tk, k, D, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
+                         (uint64_t)Hkv * row_bytes, BN / 2) ||
+        !make_map_3d_f16(&tv, v, D, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
+                         (uint64_t)Hkv * row_bytes, 32))
+        return GQA_ERR_CUDA;
+    return launch_one<true>(tq, tk, tv, P, tasks, stream);
 }
 
 }  // namespace gqa
