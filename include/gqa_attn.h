@@ -23,9 +23,9 @@
  * Conventions shared by every entry point
  *   - Head groupings: D = 256; Hkv KV heads, each shared by Hq / Hkv query
  *     heads (Hkv divides Hq, Hq <= 64).  The pages' family is Hq = 6,
- *     Hkv = 1; other groupings run one launch per query head (prefill,
- *     Hkv > 1) or per KV head (E4M3 tail, sparse), with per-entry limits
- *     below.  Anything else returns GQA_ERR_UNSUPPORTED.  scale must be
+ *     Hkv = 1; with Hkv > 1 the prefill gives every query head its own
+ *     tiles in one launch and the E4M3 tail and sparse entry points run one
+ *     launch per KV head, with per-entry limits below.  Anything else returns GQA_ERR_UNSUPPORTED.  scale must be
  *     finite and > 0.
  *   - All tensor pointers are DEVICE pointers, contiguous, 16-byte aligned,
  *     owned by the caller.  fp16 means IEEE binary16.
@@ -78,8 +78,9 @@ typedef enum {
  *   q   [Q, Hq, D]  fp16     k, v [KV, Hkv, D] fp16     out [Q, Hq, D] fp16
  *   1 <= Q <= KV.  Row i sees keys 0 .. KV - Q + i.
  * With Hkv = 1 the Q x Hq rows are packed into 128-row tiles in one launch;
- * with Hkv > 1 each query head is one launch over strided views (the
- * launches share the workspace in stream order).  FP32 accumulation; P is rounded to fp16 before the P.V product; the output
+ * with Hkv > 1 every query head has its own row tiles (one row per position)
+ * in the same launch, read in place through strided views.  FP32
+ * accumulation; P is rounded to fp16 before the P.V product; the output
  * is rounded to nearest fp16.  Long problems are split over all SMs; the
  * split partials live in the registered workspace
  * (gqa_workspace_bytes(GQA_KIND_PREFILL, Q, KV, Hq, D) bytes). */
