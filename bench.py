@@ -39,6 +39,13 @@ sys.path.insert(0, ROOT)
 
 HQ, D, SCALE = 6, 256, 1.0 / 16
 Q_MAIN, KV_MAIN = 8000, 40000
+KV_SWEEP = list(range(40000, 128001, 8000))      # the 12 prefill shapes
+TAIL_CAPACITY, TAIL_CTX = 262144, 261888          # the E4M3 verifier-tail workload
+
+
+def tail_kv_bytes(ctx_len: int) -> int:
+    """E4M3 K and V bytes a tail reads: one byte per element, Hkv = 1."""
+    return 2 * ctx_len * D
 
 
 def visible_pairs(Q: int, KV: int) -> int:
@@ -305,10 +312,10 @@ def bench_e2e_prefill_overlapped(binding, d, steps, warmup, device):
     return start.elapsed_time(end) / steps
 
 
-def bench_paged(binding, R, device, steps, warmup, flush, ctx_len=261888, seed=0):
+def bench_paged(binding, R, device, steps, warmup, flush, ctx_len=TAIL_CTX, seed=0):
     import torch
     from long_context_causal_gqa_gb300 import inputs
-    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx_len, capacity=262144, seed=seed)
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx_len, capacity=TAIL_CAPACITY, seed=seed)
     q = p.q.to(device)
     kc, vc = p.kcache.to(device), p.vcache.to(device)
     ks = torch.tensor([p.kscale], dtype=torch.float32, device=device)
@@ -325,8 +332,7 @@ def bench_paged(binding, R, device, steps, warmup, flush, ctx_len=261888, seed=0
     with torch.cuda.graph(g):
         call()
     times = time_steps(g.replay, steps, warmup, flush, torch.cuda.current_stream())
-    kv_bytes = 2 * ctx_len * D  # one E4M3 byte per K and V element, Hkv = 1
-    return times, kv_bytes, 4.0 * D * HQ * visible_pairs(R, ctx_len)
+    return times, tail_kv_bytes(ctx_len), 4.0 * D * HQ * visible_pairs(R, ctx_len)
 
 
 def bench_paged_batch(binding, device, steps, warmup, flush, B=8, R=2, max_ctx=65536, seed=0):
@@ -485,8 +491,7 @@ def run_gpu(args):
     }
     secondary = []
     if not args.quick:
-        for kv in ([48000, 56000, 64000, 72000, 80000, 88000, 96000, 104000, 112000, 120000,
-                    128000] if args.sweep else [128000]):
+        for kv in ([x for x in KV_SWEEP if x != KV] if args.sweep else [KV_SWEEP[-1]]):
             t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device)
             ms = statistics.mean(t)
             secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
