@@ -62,6 +62,8 @@ def test_paged_matches_oracle(cuda_lib, R, ctx, cap):
     (1, 1, 16, 2222, 4096),   # sixteen rows of a single head
     (12, 4, 5, 900, 1024),
     (8, 2, 2, 7000, 8192),
+    (6, 2, 1, 1, 16),         # a one-token context
+    (6, 3, 3, 130, 256),      # a ragged last tile
 ])
 def test_paged_other_groupings_match_oracle(cuda_lib, Hq, Hkv, R, ctx, cap):
     p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx, capacity=cap, seed=Hq * 7 + Hkv + R,

@@ -65,6 +65,10 @@ def test_prefill_matches_oracle(cuda_lib, Q, KV):
     (4, 1, 333, 1200),
     (1, 1, 513, 1500),   # one packed row per position
     (16, 1, 40, 90),     # 16 packed rows per position, 8 positions per 128-row tile
+    (6, 2, 1, 1),        # one position, one key, six heads of the tile space
+    (6, 3, 2, 700),
+    (12, 4, 1, 33),
+    (2, 2, 300, 301),    # multi-head attention, square-ish causal
 ])
 def test_prefill_other_groupings_match_oracle(cuda_lib, Hq, Hkv, Q, KV):
     d = inputs.dense_inputs(Q, KV, seed=Q + KV + Hq, Hq=Hq, Hkv=Hkv)

@@ -61,6 +61,8 @@ def test_sparse_matches_oracle(cuda_lib, rows, ctx, T):
     (12, 4, 30, 900, 64),
     (4, 1, 77, 2000, 300),
     (1, 1, 90, 1200, 96),
+    (6, 2, 1, 4, 4),          # one row, one block
+    (6, 6, 5, 41, 12),
 ])
 def test_sparse_other_groupings_match_oracle(cuda_lib, Hq, Hkv, rows, ctx, T):
     s = inputs.sparse_inputs(rows=rows, ctx_len=ctx, tokens=T, seed=Hq * 5 + Hkv, Hq=Hq, Hkv=Hkv)
