@@ -318,6 +318,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// max(a, b, c) in one instruction (no NaN operands occur here: scores are
+// finite or -inf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Barrier of the softmax threads of one CTA on an mbarrier, so that it shares
 // the bounded, abort-aware wait of the pipeline barriers.
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* abort,
@@ -626,15 +634,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int c = 0; c < COLS; ++c)
                         if (k0 + c > lim) s[c] = -INFINITY;
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                // Four independent chains (columns i, i + 4, ..., i + COLS - 4) of
+                // three-input maxima, two columns per instruction.
+                static_assert(COLS % 8 == 0, "row max chains");
+                float cm[4];
 #pragma unroll
-                for (int c = 4; c < COLS; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int i = 0; i < 4; ++i) {
+                    float m = fmax3(s[i], s[i + 4], s[i + 8]);
+#pragma unroll
+                    for (int k = 3; k + 1 < COLS / 4; k += 2)
+                        m = fmax3(m, s[i + 4 * k], s[i + 4 * k + 4]);
+                    cm[i] = fmaxf(m, s[i + COLS - 4]);
                 }
-                const float hm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                const float hm = fmax3(cm[0], cm[1], fmaxf(cm[2], cm[3]));
                 float* xp = xch + (gg & 1) * (NWG * BM);
                 xp[hg * BM + row] = hm;
                 ok = group_sync(gbar, gphase, abort_flag, P.err);
