@@ -189,7 +189,7 @@ def paged_e4m3(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
                kscale: torch.Tensor, vscale: torch.Tensor, block_table: torch.Tensor,
                ctx_len: int, scale: float = 1.0 / 16, out: torch.Tensor | None = None,
                stream=None) -> torch.Tensor:
-    """Paged E4M3 verifier tail: q [R,Hq,D] fp16, caches [pages,16,Hkv,D] uint8,
+    """Paged E4M3 verifier tail: q [R,Hq,D] fp16, caches [pages,page,Hkv,D] uint8,
     kscale/vscale one-element fp32 CUDA tensors, block_table int32."""
     dev = _need_cuda(q, kcache, vcache, kscale, vscale, block_table)
     R, Hq, D = q.shape

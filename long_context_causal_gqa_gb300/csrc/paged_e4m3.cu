@@ -4,7 +4,10 @@
 // context fences", What / Changes): R <= 8 query rows (6R packed rows, Hq=6
 // sharing Hkv=1) at the end of a context of up to 262144 keys; K and V are
 // E4M3 bytes (one fp32 scale each) in page-16 blocks addressed through a
-// block table of physical page ids; FP32 accumulation.  The page's operator
+// block table of physical page ids; FP32 accumulation.  Here the page is any
+// power of two in [8, 256], one launch may carry a batch of sequences with
+// their context lengths read on the device, and other head groupings run one
+// launch per KV head (R x Hq / Hkv <= 48 packed rows).  The page's operator
 // decodes E4M3 through a shared lookup table and specialises the 8-row case;
 // here the work is HBM-bound (one byte per K/V element) and shaped for sm_103a:
 //
@@ -41,9 +44,9 @@
 //   cross-lane max is taken only on the first tile or when the vote fires.
 //   Row sums stay per thread until the split's end.
 //
-// Warp roles (320 threads): 0 TMA producer, 1 TMEM owner + UMMA issuer,
-// 2..9 softmax warps (two warpgroups, each owning half of the packed query
-// rows; thread = TMEM lane = key).
+// Warp roles (64 + 128 NWG threads): 0 TMA producer, 1 TMEM owner + UMMA
+// issuer, then NWG = 2 / 4 / 6 softmax warpgroups for 16 / 32 / 48 packed
+// rows, each owning 8 of them (thread = TMEM lane = key).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
