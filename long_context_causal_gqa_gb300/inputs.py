@@ -237,3 +237,52 @@ def sparse_inputs(rows: int, ctx_len: int, tokens: int, seed: int = 0, page: int
     return SparseInputs(q, caches[0], caches[1], table, sel, cnt, max_sel, ctx_len, rows,
                         page, Hq, Hkv, D, scale)
 
+
+
+@dataclasses.dataclass
+class SparseE4M3Inputs:
+    q: torch.Tensor            # [rows, Hq, D] fp16
+    kcache: torch.Tensor       # [num_pages, page, Hkv, D] uint8 E4M3 codes
+    vcache: torch.Tensor       # [num_pages, page, Hkv, D] uint8 E4M3 codes
+    kscale: float
+    vscale: float
+    block_table: torch.Tensor  # [ceil(ctx_len / page)] int32
+    sel_idx: torch.Tensor      # [rows, max_sel] int32 logical 4-token block ids (-1 padding)
+    sel_cnt: torch.Tensor      # [rows] int32
+    max_sel: int
+    ctx_len: int
+    rows: int
+    page: int
+    Hq: int
+    Hkv: int
+    D: int
+    scale: float
+
+
+def sparse_e4m3_inputs(rows: int, ctx_len: int, tokens: int, seed: int = 0, page: int = PAGE,
+                       Hq: int = HQ, Hkv: int = HKV, D: int = HEAD_DIM, scale: float = SCALE,
+                       num_pages: int | None = None) -> SparseE4M3Inputs:
+    """Selected-block sparse inputs over an E4M3 page cache: q, block table and
+    selections as in ``sparse_inputs``; K and V N(0,1) for the ctx_len live
+    tokens, encoded per tensor as E4M3 with one fp32 scale each (absmax / 448,
+    as the tail's cache); physical pages that no entry names, and slots past
+    ctx_len, hold the poison byte."""
+    assert 1 <= rows <= ctx_len
+    n_logical = (ctx_len + page - 1) // page
+    if num_pages is None:
+        num_pages = n_logical
+    q = normal_fp16((rows, Hq, D), seed * 11 + 0)
+    table = permuted_block_table(n_logical, num_pages, seed * 11 + 3)
+    caches, scales = [], []
+    for i in (1, 2):
+        x = torch.randn(ctx_len, Hkv, D, generator=_gen(seed * 11 + i), dtype=torch.float32)
+        b, sc = e4m3_encode(x)
+        padded = torch.full((n_logical * page, Hkv, D), E4M3_POISON, dtype=torch.uint8)
+        padded[:ctx_len] = b
+        cache = torch.full((num_pages, page, Hkv, D), E4M3_POISON, dtype=torch.uint8)
+        cache[table.long()] = padded.view(n_logical, page, Hkv, D)
+        caches.append(cache)
+        scales.append(sc)
+    sel, cnt, max_sel = sparse_selection(rows, ctx_len, tokens, seed * 11 + 4)
+    return SparseE4M3Inputs(q, caches[0], caches[1], scales[0], scales[1], table, sel, cnt,
+                            max_sel, ctx_len, rows, page, Hq, Hkv, D, scale)

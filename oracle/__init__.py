@@ -54,6 +54,9 @@ def _load():
             lib.oracle_sparse_blocks.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, Dd, P,
                                                  I, P, I]
             lib.oracle_sparse_blocks.restype = I
+            lib.oracle_sparse_blocks_e4m3.argtypes = [P, P, P, Dd, Dd, P, P, P, I, I, I, I, I,
+                                                      I, I, Dd, P, I, P, I]
+            lib.oracle_sparse_blocks_e4m3.restype = I
             lib.oracle_dense_probs.argtypes = [P, P, P, I, I, I, I, I, Dd, I, I, P]
             lib.oracle_dense_probs.restype = I
             _lib = lib
@@ -172,4 +175,29 @@ def sparse_blocks(q, kcache, vcache, block_table, sel_idx, sel_cnt, ctx_len: int
                                       _threads(nthreads))
     if rc:
         raise ValueError("oracle_sparse_blocks: invalid arguments")
+    return out
+
+
+def sparse_blocks_e4m3(q, kcache, vcache, kscale: float, vscale: float, block_table, sel_idx,
+                       sel_cnt, ctx_len: int, scale: float, rows=None, nthreads=None) -> np.ndarray:
+    """Selected-block sparse attention over an E4M3 page cache (uint8 codes,
+    values decode(byte) * kscale / vscale)."""
+    qa = _np(q, np.uint16)
+    kc, vc = _np(kcache, np.uint8), _np(vcache, np.uint8)
+    bt = _np(block_table, np.int32)
+    si, sc = _np(sel_idx, np.int32), _np(sel_cnt, np.int32)
+    n_rows, Hq, D = qa.shape
+    _, page, Hkv, D2 = kc.shape
+    assert D == D2 and vc.shape == kc.shape
+    assert si.shape[0] == n_rows and sc.shape[0] == n_rows
+    assert bt.shape[0] * page >= ctx_len
+    max_sel = si.shape[1]
+    r = _rows(rows, n_rows)
+    out = np.zeros((len(r), Hq, D), dtype=np.float64)
+    rc = _load().oracle_sparse_blocks_e4m3(_ptr(qa), _ptr(kc), _ptr(vc), float(kscale),
+                                           float(vscale), _ptr(bt), _ptr(si), _ptr(sc), max_sel,
+                                           page, int(ctx_len), n_rows, Hq, Hkv, D, float(scale),
+                                           _ptr(r), len(r), _ptr(out), _threads(nthreads))
+    if rc:
+        raise ValueError("oracle_sparse_blocks_e4m3: invalid arguments")
     return out

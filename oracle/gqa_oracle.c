@@ -26,7 +26,10 @@
  *           union over the row's selected four-token blocks b of
  *           {4b .. 4b+3}, intersected with {0 .. p_i}, p_i = ctx_len - rows + i
  *           (positions past the row are clamped away; block ids outside
- *           0 .. p_i/4 select nothing).
+ *           0 .. p_i/4 select nothing).  Its keys and values come from an fp16
+ *           page cache, or from an E4M3 page cache read as in the paged
+ *           variant (the E4M3 storage of the second page applied to this
+ *           workload).
  *
  * Inputs arrive as raw fp16 bit patterns and E4M3 bytes; each is decoded here
  * to its exact double value.  Output is double, never rounded to fp16.
@@ -326,6 +329,32 @@ int oracle_sparse_blocks(const uint16_t* q, const uint16_t* kc, const uint16_t* 
     jb.variant = VAR_SPARSE;
     jb.src.fetch_k = paged16_fetch_k;
     jb.src.fetch_v = paged16_fetch_v;
+    jb.src.ctx = &c;
+    jb.src.D = D;
+    jb.q = q; jb.rows_total = rows_total; jb.n_ctx = ctx_len; jb.Hq = Hq; jb.Hkv = Hkv;
+    jb.D = D; jb.scale = scale; jb.sel_idx = sel_idx; jb.sel_cnt = sel_cnt;
+    jb.max_sel = max_sel; jb.rows = rows; jb.nrows = nrows; jb.out = out;
+    for (int w = 0; w < nrows; ++w) {
+        int i = rows[w];
+        if (i < 0 || i >= rows_total || sel_cnt[i] < 0 || sel_cnt[i] > max_sel) return 1;
+    }
+    return run_job(&jb, nthreads);
+}
+
+/* Selected-block sparse paged prefill over an E4M3 page cache: the sparse
+ * visible sets, keys and values decode(byte) * kscale / vscale. */
+int oracle_sparse_blocks_e4m3(const uint16_t* q, const uint8_t* kc, const uint8_t* vc,
+                              double kscale, double vscale, const int32_t* block_table,
+                              const int32_t* sel_idx, const int32_t* sel_cnt, int max_sel,
+                              int page, int ctx_len, int rows_total, int Hq, int Hkv, int D,
+                              double scale, const int* rows, int nrows, double* out,
+                              int nthreads) {
+    paged_ctx c = {kc, vc, kscale, vscale, block_table, page, Hkv, D};
+    job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.variant = VAR_SPARSE;
+    jb.src.fetch_k = paged_fetch_k;
+    jb.src.fetch_v = paged_fetch_v;
     jb.src.ctx = &c;
     jb.src.D = D;
     jb.q = q; jb.rows_total = rows_total; jb.n_ctx = ctx_len; jb.Hq = Hq; jb.Hkv = Hkv;

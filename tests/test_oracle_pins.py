@@ -357,3 +357,47 @@ def test_e4m3_encoding_uses_absmax_over_448():
 def test_block_table_is_injective():
     t = inputs.permuted_block_table(100, 256, seed=1)
     assert len(set(t.tolist())) == 100 and int(t.min()) >= 0 and int(t.max()) < 256
+
+
+# ---------------------------------------------------------------- sparse over an E4M3 cache
+
+def test_sparse_e4m3_matches_decimal_bruteforce():
+    inp = inputs.sparse_e4m3_inputs(rows=5, ctx_len=41, tokens=12, seed=2, page=16, D=8)
+    got = oracle.sparse_blocks_e4m3(inp.q, inp.kcache, inp.vcache, inp.kscale, inp.vscale,
+                                    inp.block_table, inp.sel_idx, inp.sel_cnt, inp.ctx_len, 0.4)
+    kf = _unpage(_decode_torch(inp.kcache), inp.block_table, 41, 16).numpy() * inp.kscale
+    vf = _unpage(_decode_torch(inp.vcache), inp.block_table, 41, 16).numpy() * inp.vscale
+    ref = _brute(_f64(inp.q), kf, vf, 0.4, _visible_sparse(inp.sel_idx, inp.sel_cnt, 41, 5))
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-15)
+
+
+def test_sparse_e4m3_with_every_block_equals_paged_tail():
+    """Selecting every visible block turns the sparse visible set into the
+    causal one, so the result is the E4M3 tail's over the same cache, bit for
+    bit."""
+    rows, ctx_len = 6, 300
+    inp = inputs.sparse_e4m3_inputs(rows=rows, ctx_len=ctx_len, tokens=8, seed=5, page=16,
+                                    D=32, num_pages=24)
+    sel, cnt = _all_blocks(rows, ctx_len)
+    got = oracle.sparse_blocks_e4m3(inp.q, inp.kcache, inp.vcache, inp.kscale, inp.vscale,
+                                    inp.block_table, sel, cnt, ctx_len, 1 / 16)
+    ref = oracle.paged_e4m3(inp.q, inp.kcache, inp.vcache, inp.kscale, inp.vscale,
+                            inp.block_table, ctx_len, 1 / 16)
+    assert np.array_equal(got, ref)
+
+
+def test_sparse_e4m3_equals_fp16_sparse_on_decoded_values():
+    """With power-of-two scales every decode(byte) * scale is exact in fp16,
+    so the E4M3 sparse result equals the fp16 sparse result on the decoded
+    cache, bit for bit."""
+    inp = inputs.sparse_e4m3_inputs(rows=7, ctx_len=200, tokens=40, seed=6, page=16, D=16)
+    ks, vs = 2.0 ** -4, 2.0 ** -3
+    kd = (_decode_torch(inp.kcache) * ks).to(torch.float16)
+    vd = (_decode_torch(inp.vcache) * vs).to(torch.float16)
+    live = torch.isfinite(_decode_torch(inp.kcache))
+    assert torch.equal(kd.to(torch.float64)[live], (_decode_torch(inp.kcache) * ks)[live])
+    got = oracle.sparse_blocks_e4m3(inp.q, inp.kcache, inp.vcache, ks, vs, inp.block_table,
+                                    inp.sel_idx, inp.sel_cnt, inp.ctx_len, 1 / 16)
+    ref = oracle.sparse_blocks(inp.q, kd, vd, inp.block_table, inp.sel_idx, inp.sel_cnt,
+                               inp.ctx_len, 1 / 16)
+    assert np.array_equal(got, ref)
