@@ -366,15 +366,30 @@ def bench_paged_batch(binding, device, steps, warmup, flush, B=8, R=2, max_ctx=6
     return times, kv_bytes, ctxs
 
 
-def bench_sparse(binding, T, device, steps, warmup, flush, rows=4096, ctx_len=32768, seed=0):
+def bench_sparse(binding, T, device, steps, warmup, flush, rows=4096, ctx_len=32768, seed=0,
+                 e4m3=False):
+    """Selected-block sparse prefill over an fp16 cache, or an E4M3 cache
+    (codes converted to fp16 on the way into shared memory)."""
     import torch
     from long_context_causal_gqa_gb300 import inputs
-    s = inputs.sparse_inputs(rows=rows, ctx_len=ctx_len, tokens=T, seed=seed)
-    args = [x.to(device) for x in (s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt)]
-    out = torch.empty_like(args[0])
+    if e4m3:
+        s = inputs.sparse_e4m3_inputs(rows=rows, ctx_len=ctx_len, tokens=T, seed=seed)
+        ks = torch.tensor([s.kscale], dtype=torch.float32, device=device)
+        vs = torch.tensor([s.vscale], dtype=torch.float32, device=device)
+        q, kc, vc, bt, si, sc = [x.to(device) for x in (s.q, s.kcache, s.vcache, s.block_table,
+                                                         s.sel_idx, s.sel_cnt)]
+        out = torch.empty_like(q)
 
-    def call():
-        binding.sparse_blocks(*args, ctx_len, SCALE, out=out)
+        def call():
+            binding.sparse_blocks_e4m3(q, kc, vc, ks, vs, bt, si, sc, ctx_len, SCALE, out=out)
+    else:
+        s = inputs.sparse_inputs(rows=rows, ctx_len=ctx_len, tokens=T, seed=seed)
+        args = [x.to(device) for x in (s.q, s.kcache, s.vcache, s.block_table, s.sel_idx,
+                                       s.sel_cnt)]
+        out = torch.empty_like(args[0])
+
+        def call():
+            binding.sparse_blocks(*args, ctx_len, SCALE, out=out)
     call()
     times = time_steps(call, steps, warmup, flush, torch.cuda.current_stream())
     visible = 0
@@ -382,7 +397,7 @@ def bench_sparse(binding, T, device, steps, warmup, flush, rows=4096, ctx_len=32
         p = ctx_len - rows + i
         n = int(s.sel_cnt[i])
         visible += 4 * n - (3 - p % 4)
-    gathered = rows * T * 2 * D * 2
+    gathered = rows * T * 2 * D * (1 if e4m3 else 2)   # K and V bytes of the selected tokens
     return times, gathered, 4.0 * D * HQ * visible
 
 
@@ -540,20 +555,24 @@ def run_gpu(args):
                               "device_error": derr})
         except Exception as e:  # a secondary failure must not lose the headline
             secondary.append({"what": "paged_e4m3_batch", "error": str(e)[:200]})
-        for T in (64, 512, 2048):
-            try:
-                t, gathered, fl = bench_sparse(binding, T, device, 5, 2, flush)
-                derr = binding.device_error()
-            except Exception as e:
-                secondary.append({"what": f"sparse T={T}", "error": str(e)[:200]})
-                continue
-            if derr:
-                secondary.append({"what": f"sparse T={T}", "error": f"device error {derr}"})
-                continue
-            ms = statistics.median(t)
-            secondary.append({"what": f"sparse blocks 4096 rows T={T} ctx=32768", "ms": round(ms, 4),
-                              "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1),
-                              "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2)})
+        for e4m3 in (False, True):
+            for T in (64, 512, 2048):
+                kind = "E4M3 cache" if e4m3 else "fp16 cache"
+                try:
+                    t, gathered, fl = bench_sparse(binding, T, device, 5, 2, flush, e4m3=e4m3)
+                    derr = binding.device_error()
+                except Exception as e:
+                    secondary.append({"what": f"sparse {kind} T={T}", "error": str(e)[:200]})
+                    continue
+                if derr:
+                    secondary.append({"what": f"sparse {kind} T={T}",
+                                      "error": f"device error {derr}"})
+                    continue
+                ms = statistics.median(t)
+                secondary.append({"what": f"sparse blocks 4096 rows T={T} ctx=32768, {kind}",
+                                  "ms": round(ms, 4),
+                                  "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1),
+                                  "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2)})
     line["secondary"] = secondary
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(Q, KV, seconds_target=args.cpu_seconds)
@@ -596,10 +615,12 @@ def run_case(args):
                 "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                 "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
     else:
-        t, gathered, fl = bench_sparse(binding, args.tokens, device, args.steps, args.warmup, flush)
+        e4m3 = args.case == "sparse_e4m3"
+        t, gathered, fl = bench_sparse(binding, args.tokens, device, args.steps, args.warmup, flush,
+                                       e4m3=e4m3)
         ms = statistics.median(t)
-        line = {"case": f"sparse blocks 4096 rows T={args.tokens}", "ms": round(ms, 4),
-                "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1)}
+        line = {"case": f"sparse blocks 4096 rows T={args.tokens}" + (" E4M3 cache" if e4m3 else ""),
+                "ms": round(ms, 4), "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1)}
     line["device_error"] = binding.device_error()
     print(json.dumps(line), flush=True)
 
@@ -653,7 +674,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--case", default="headline", choices=["headline", "prefill", "paged",
                                                            "paged_batch",
-                                                           "sparse"],
+                                                           "sparse", "sparse_e4m3"],
                     help="run one secondary workload alone (profiling)")
     ap.add_argument("--rows", type=int, default=8, help="--case paged: tail rows")
     ap.add_argument("--hq", type=int, default=HQ, help="--case prefill: query heads")

@@ -202,6 +202,24 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
                            int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
                            void* out, struct CUstream_st* stream);
 
+/* Selected-block sparse paged prefill over an FP8-E4M3 page cache: the E4M3
+ * storage of [P2, What] applied to the [P3, Changes] workload.  Same
+ * arguments, selection semantics and result as gqa_attn_sparse_blocks,
+ * except:
+ *   kcache/vcache [num_pages, page, Hkv, D] uint8 E4M3 codes (OCP e4m3fn),
+ *                real value = decode(byte) * scale
+ *   kscale/vscale DEVICE pointers to one fp32 each, 4-byte aligned
+ * The codes are converted to fp16 on their way into shared memory (exact:
+ * every E4M3 value is an fp16 value); the K scale multiplies the scores and
+ * the V scale the output.  A selected token's code bytes must not be the
+ * E4M3 NaN code (0x7F / 0xFF).  Needs no workspace. */
+int gqa_attn_sparse_blocks_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                                const float* kscale, const float* vscale,
+                                const int32_t* block_table, const int32_t* sel_idx,
+                                const int32_t* sel_cnt, int max_sel, int num_pages, int page,
+                                int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
+                                void* out, struct CUstream_st* stream);
+
 /* Workspace kinds for gqa_workspace_bytes. */
 #define GQA_KIND_PREFILL 0
 #define GQA_KIND_PAGED_E4M3 1

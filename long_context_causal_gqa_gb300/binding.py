@@ -39,7 +39,7 @@ DEVERR_BAD_CTX_LEN = 0x8
 EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_devctx",
             "gqa_attn_paged_e4m3_batch",
             "gqa_attn_paged_e4m3_noalloc",
-            "gqa_attn_sparse_blocks",
+            "gqa_attn_sparse_blocks", "gqa_attn_sparse_blocks_e4m3",
             "gqa_workspace_bytes", "gqa_set_workspace", "gqa_get_device_error",
             "gqa_prefill_sm_pairs", "gqa_status_string")
 
@@ -80,6 +80,9 @@ def load():
             lib.gqa_attn_sparse_blocks.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                                    P, P]
             lib.gqa_attn_sparse_blocks.restype = I
+            lib.gqa_attn_sparse_blocks_e4m3.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                                        I, I, I, F, P, P]
+            lib.gqa_attn_sparse_blocks_e4m3.restype = I
             lib.gqa_workspace_bytes.argtypes = [I, I, I, I, I]
             lib.gqa_workspace_bytes.restype = Z
             lib.gqa_set_workspace.argtypes = [I, P, Z]
@@ -278,4 +281,28 @@ def sparse_blocks(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
                                            max_sel, num_pages, page, int(ctx_len), rows, Hq,
                                            Hkv, D, float(scale), _ptr(out), _stream_ptr(stream))
     _check(st, "gqa_attn_sparse_blocks")
+    return out
+
+
+def sparse_blocks_e4m3(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                       kscale: torch.Tensor, vscale: torch.Tensor, block_table: torch.Tensor,
+                       sel_idx: torch.Tensor, sel_cnt: torch.Tensor, ctx_len: int,
+                       scale: float = 1.0 / 16, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Selected-block sparse paged prefill over an E4M3 page cache: caches
+    [pages,page,Hkv,D] uint8 codes, kscale/vscale one-element fp32 CUDA tensors."""
+    dev = _need_cuda(q, kcache, vcache, kscale, vscale, block_table, sel_idx, sel_cnt)
+    rows, Hq, D = q.shape
+    num_pages, page, Hkv, _ = kcache.shape
+    max_sel = sel_idx.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    with torch.cuda.device(dev):
+        st = load().gqa_attn_sparse_blocks_e4m3(_ptr(q), _ptr(kcache), _ptr(vcache),
+                                                _ptr(kscale), _ptr(vscale), _ptr(block_table),
+                                                _ptr(sel_idx), _ptr(sel_cnt), max_sel, num_pages,
+                                                page, int(ctx_len), rows, Hq, Hkv, D,
+                                                float(scale), _ptr(out), _stream_ptr(stream))
+    _check(st, "gqa_attn_sparse_blocks_e4m3")
     return out

@@ -142,6 +142,35 @@ bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
 
 }  // namespace
 
+namespace {
+
+int sparse_common(const void* q, const void* kcache, const void* vcache, const float* kscale,
+                  const float* vscale, bool e4m3, const int32_t* block_table,
+                  const int32_t* sel_idx, const int32_t* sel_cnt, int max_sel, int num_pages,
+                  int page, int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
+                  void* out, struct CUstream_st* stream) {
+    if (!q || !kcache || !vcache || !block_table || !sel_idx || !sel_cnt || !out)
+        return GQA_ERR_INVALID_ARG;
+    if (e4m3 && (!kscale || !vscale)) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(sel_idx) |
+         reinterpret_cast<uintptr_t>(sel_cnt) | reinterpret_cast<uintptr_t>(kscale) |
+         reinterpret_cast<uintptr_t>(vscale)) & 3u)
+        return GQA_ERR_INVALID_ARG;
+    if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || max_sel < 1 ||
+        !scale_ok(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (!prefill_family_ok(Hq, Hkv, D) || Hq / Hkv > kMaxSparseGroup || !page_ok(page))
+        return GQA_ERR_UNSUPPORTED;
+    if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
+    return sparse_launch(q, kcache, vcache, kscale, vscale, e4m3, block_table, sel_idx, sel_cnt,
+                         max_sel, num_pages, page, ctx_len, query_rows, Hq, Hkv, scale, out,
+                         stream);
+}
+
+}  // namespace
+
 extern "C" {
 
 int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int Q, int KV,
@@ -247,21 +276,20 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
                            const int32_t* sel_cnt, int max_sel, int num_pages, int page,
                            int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
                            void* out, struct CUstream_st* stream) {
-    if (!q || !kcache || !vcache || !block_table || !sel_idx || !sel_cnt || !out)
-        return GQA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
-        return GQA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(sel_idx) |
-         reinterpret_cast<uintptr_t>(sel_cnt)) & 3u)
-        return GQA_ERR_INVALID_ARG;
-    if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || max_sel < 1 ||
-        !scale_ok(scale))
-        return GQA_ERR_INVALID_ARG;
-    if (!prefill_family_ok(Hq, Hkv, D) || Hq / Hkv > kMaxSparseGroup || !page_ok(page))
-        return GQA_ERR_UNSUPPORTED;
-    if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
-    return sparse_launch(q, kcache, vcache, block_table, sel_idx, sel_cnt, max_sel, num_pages,
-                         page, ctx_len, query_rows, Hq, Hkv, scale, out, stream);
+    return sparse_common(q, kcache, vcache, nullptr, nullptr, false, block_table, sel_idx,
+                         sel_cnt, max_sel, num_pages, page, ctx_len, query_rows, Hq, Hkv, D,
+                         scale, out, stream);
+}
+
+int gqa_attn_sparse_blocks_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
+                                const float* kscale, const float* vscale,
+                                const int32_t* block_table, const int32_t* sel_idx,
+                                const int32_t* sel_cnt, int max_sel, int num_pages, int page,
+                                int ctx_len, int query_rows, int Hq, int Hkv, int D, float scale,
+                                void* out, struct CUstream_st* stream) {
+    return sparse_common(q, kcache, vcache, kscale, vscale, true, block_table, sel_idx, sel_cnt,
+                         max_sel, num_pages, page, ctx_len, query_rows, Hq, Hkv, D, scale, out,
+                         stream);
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {

@@ -120,10 +120,13 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
                               int R, int Hq, int Hkv, float scale, void* out,
                               cudaStream_t stream);
 
-int sparse_launch(const void* q, const void* kcache, const void* vcache,
-                  const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
-                  int max_sel, int num_pages, int page, int ctx_len, int rows, int Hq, int Hkv,
-                  float scale, void* out, cudaStream_t stream);
+// kcache / vcache: fp16 elements, or E4M3 codes with kscale / vscale (device
+// pointers to one fp32 each) when e4m3 is set.
+int sparse_launch(const void* q, const void* kcache, const void* vcache, const float* kscale,
+                  const float* vscale, bool e4m3, const int32_t* block_table,
+                  const int32_t* sel_idx, const int32_t* sel_cnt, int max_sel, int num_pages,
+                  int page, int ctx_len, int rows, int Hq, int Hkv, float scale, void* out,
+                  cudaStream_t stream);
 
 // Bytes at the start of every workspace reserved for merge counters.
 constexpr size_t kWorkspaceCounterBytes = 4096;

@@ -23,6 +23,13 @@
 //   the reference by more than 8 in log2 units); row sums stay per thread
 //   until the row ends.  The epilogue writes out[i] directly (no split).
 //
+// * An E4M3 cache (the tail's storage applied to this workload) halves the
+//   gathered bytes: the gather lanes load the code bytes of their token rows
+//   (16 loads in flight per lane), convert them to fp16 with
+//   cvt.rn.f16x2.e4m3x2 and store them into the same swizzled tile the fp16
+//   path copies into, so the MMAs are unchanged; the K scale joins the score
+//   scale and the V scale the final 1 / l.
+//
 // Warp roles (320 threads): 0..3 gather, 4 TMEM owner + UMMA issuer,
 // 5..8 key warps (softmax + epilogue; thread = TMEM lane), 9 idle helper.
 #include <cuda.h>
@@ -47,8 +54,12 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Params {
     const __half* q;
-    const __half* kcache;
+    const __half* kcache;     // fp16 cache (F8 false)
     const __half* vcache;
+    const uint8_t* kcache8;   // E4M3 cache (F8 true)
+    const uint8_t* vcache8;
+    const float* kscale;      // E4M3 scales (device, one fp32 each)
+    const float* vscale;
     const int32_t* table;
     const int32_t* sel_idx;
     const int32_t* sel_cnt;
@@ -146,9 +157,17 @@ __device__ __forceinline__ int key_token(const Params& P, int i, int cnt, int t,
     return tok <= p ? tok : -1;
 }
 
+// Two E4M3 codes (low 16 bits of v, low byte first) -> fp16x2 (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)v));
+    return r;
+}
+
 // HQ: heads per launch known at compile time (6), or NP with the count read
-// from P.nh (any grouping up to 16 query heads per KV head).
-template <int HQ>
+// from P.nh (any grouping up to 16 query heads per KV head).  F8: the cache
+// holds E4M3 codes, converted to fp16 on the way into shared memory.
+template <int HQ, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     const int nh = (HQ == NP) ? P.nh : HQ;
     const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * D;
@@ -249,19 +268,57 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                             break;
                         }
                     }
-                    const __half* cache = kv == 0 ? P.kcache : P.vcache;
                     const uint32_t tile = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V);
+                    if constexpr (F8) {
+                        // A token row is 256 code bytes: half-warp `half` takes key
+                        // 2e + half, lane u of it the codes of d = 16u .. 16u + 15,
+                        // which become fp16 units 2u, 2u + 1 of the row (chunk u / 4,
+                        // units 2 (u % 4) and 2 (u % 4) + 1 within it).  Masked
+                        // tokens are stored as zeros.
+                        const uint8_t* cache = kv == 0 ? P.kcache8 : P.vcache8;
+                        const int u = lane & 15, half = lane >> 4;
+                        uint4 raw[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int src_lane = 2 * e + half;
+                            const int tok = __shfl_sync(0xffffffffu, tok_l, src_lane);
+                            const size_t row = __shfl_sync(0xffffffffu, row_l, src_lane);
+                            raw[e] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(cache + row) + u)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        const uint32_t chunk = tile + (uint32_t)(u >> 2) * (TILE * 128);
+                        const uint32_t unit = 2u * (uint32_t)(u & 3);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const uint32_t key = (uint32_t)(warp * 32 + 2 * e + half);
+                            const uint4 lo = make_uint4(e4m3x2_to_f16x2(raw[e].x),
+                                                        e4m3x2_to_f16x2(raw[e].x >> 16),
+                                                        e4m3x2_to_f16x2(raw[e].y),
+                                                        e4m3x2_to_f16x2(raw[e].y >> 16));
+                            const uint4 hi = make_uint4(e4m3x2_to_f16x2(raw[e].z),
+                                                        e4m3x2_to_f16x2(raw[e].z >> 16),
+                                                        e4m3x2_to_f16x2(raw[e].w),
+                                                        e4m3x2_to_f16x2(raw[e].w >> 16));
+                            *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit) - sbase)) = lo;
+                            *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit + 1) - sbase)) = hi;
+                        }
+                        // Generic-proxy stores, read by the tensor cores (async proxy).
+                        fence_async_shared();
+                        mbar_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
+                    } else {
+                        const __half* cache = kv == 0 ? P.kcache : P.vcache;
 #pragma unroll 4
-                    for (int e = 0; e < 32; ++e) {
-                        const int key = warp * 32 + e;
-                        const int tok = __shfl_sync(0xffffffffu, tok_l, e);
-                        const size_t row = __shfl_sync(0xffffffffu, row_l, e);
-                        // lane covers d = 8 lane .. 8 lane + 7: chunk lane / 8, unit lane % 8
-                        const uint32_t dst = tile + (lane >> 3) * (TILE * 128) + sw128(key, lane & 7);
-                        const __half* src = tok >= 0 ? cache + row + lane * 8 : cache;
-                        cp_async16(dst, src, tok >= 0 ? 16u : 0u);
+                        for (int e = 0; e < 32; ++e) {
+                            const int key = warp * 32 + e;
+                            const int tok = __shfl_sync(0xffffffffu, tok_l, e);
+                            const size_t row = __shfl_sync(0xffffffffu, row_l, e);
+                            // lane covers d = 8 lane .. 8 lane + 7: chunk lane / 8, unit lane % 8
+                            const uint32_t dst = tile + (lane >> 3) * (TILE * 128) + sw128(key, lane & 7);
+                            const __half* src = tok >= 0 ? cache + row + lane * 8 : cache;
+                            cp_async16(dst, src, tok >= 0 ? 16u : 0u);
+                        }
+                        cp_async_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
                     }
-                    cp_async_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
                 }
             }
         }
@@ -343,7 +400,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         const int wq = warp & 3;
         const int k = wq * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        const float sl2 = P.scale_log2;
+        // E4M3: the keys are the codes' values; their scale joins the score scale.
+        const float sl2 = F8 ? P.scale_log2 * __ldg(P.kscale) : P.scale_log2;
         uint32_t g = 0;
         uint32_t gphase = 0;
         bool ok = true;
@@ -479,7 +537,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
                 const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
-                inv[c] = l > 0.f ? 1.0f / l : 0.f;
+                if constexpr (F8)
+                    inv[c] = l > 0.f ? __ldg(P.vscale) / l : 0.f;
+                else
+                    inv[c] = l > 0.f ? 1.0f / l : 0.f;
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -510,10 +571,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 
 }  // namespace sparse
 
-int sparse_launch(const void* q, const void* kcache, const void* vcache,
-                  const int32_t* block_table, const int32_t* sel_idx, const int32_t* sel_cnt,
-                  int max_sel, int num_pages, int page, int ctx_len, int rows, int Hq, int Hkv,
-                  float scale, void* out, cudaStream_t stream) {
+int sparse_launch(const void* q, const void* kcache, const void* vcache, const float* kscale,
+                  const float* vscale, bool e4m3, const int32_t* block_table,
+                  const int32_t* sel_idx, const int32_t* sel_cnt, int max_sel, int num_pages,
+                  int page, int ctx_len, int rows, int Hq, int Hkv, float scale, void* out,
+                  cudaStream_t stream) {
     using namespace sparse;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -531,29 +593,37 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache,
     P.nh = grp;
     P.q_stride = Hq * D;
     P.kv_stride = Hkv * D;
+    P.kscale = kscale;
+    P.vscale = vscale;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.err = di->err_word;
-    // The 6-head instantiation addresses the caches with a stride of D, so it
-    // serves one KV head only.
+    // The 6-head instantiations address the caches with a stride of D, so
+    // they serve one KV head only.
     const bool six = (grp == kHq && Hkv == 1);
-    static bool attr_done[2][64] = {{false}};
-    if (di->device < 64 && !attr_done[six][di->device]) {
-        if (cudaFuncSetAttribute(six ? sparse_kernel<kHq> : sparse_kernel<NP>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+    using KernelFn = void (*)(Params);
+    const KernelFn fn = e4m3 ? (six ? sparse_kernel<kHq, true> : sparse_kernel<NP, true>)
+                             : (six ? sparse_kernel<kHq, false> : sparse_kernel<NP, false>);
+    const int which = (e4m3 ? 2 : 0) + (six ? 1 : 0);
+    static bool attr_done[4][64] = {{false}};
+    if (di->device < 64 && !attr_done[which][di->device]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
+            cudaSuccess)
             return GQA_ERR_CUDA;
-        attr_done[six][di->device] = true;
+        attr_done[which][di->device] = true;
     }
     // One launch per KV head: query heads g * grp .. g * grp + grp - 1 read
     // token rows of KV head g.
+    const size_t esz = e4m3 ? 1 : 2;   // bytes per cache element
     for (int g = 0; g < Hkv; ++g) {
         P.q = static_cast<const __half*>(q) + (size_t)g * grp * D;
         P.out = static_cast<__half*>(out) + (size_t)g * grp * D;
-        P.kcache = static_cast<const __half*>(kcache) + (size_t)g * D;
-        P.vcache = static_cast<const __half*>(vcache) + (size_t)g * D;
-        if (six)
-            sparse_kernel<kHq><<<P.G, NTHREADS, SMEM, stream>>>(P);
-        else
-            sparse_kernel<NP><<<P.G, NTHREADS, SMEM, stream>>>(P);
+        const uint8_t* kb = static_cast<const uint8_t*>(kcache) + (size_t)g * D * esz;
+        const uint8_t* vb = static_cast<const uint8_t*>(vcache) + (size_t)g * D * esz;
+        P.kcache = reinterpret_cast<const __half*>(kb);
+        P.vcache = reinterpret_cast<const __half*>(vb);
+        P.kcache8 = kb;
+        P.vcache8 = vb;
+        fn<<<P.G, NTHREADS, SMEM, stream>>>(P);
         if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
     return GQA_OK;

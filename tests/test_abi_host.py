@@ -124,6 +124,18 @@ def test_sparse_rejects_bad_arguments(lib):
     assert _sparse(lib, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED
 
 
+def _sparse8(lib, ks=FAKE, D=256, Hq=6, Hkv=1):
+    return lib.gqa_attn_sparse_blocks_e4m3(FAKE, FAKE, FAKE, ks, FAKE, FAKE, FAKE, FAKE, 4, 4,
+                                           16, 64, 4, Hq, Hkv, D, 0.0625, FAKE, None)
+
+
+def test_sparse_e4m3_rejects_bad_arguments(lib):
+    assert _sparse8(lib, ks=P(0)) == binding.GQA_ERR_INVALID_ARG
+    assert _sparse8(lib, ks=P(0x10002)) == binding.GQA_ERR_INVALID_ARG
+    assert _sparse8(lib, D=128) == binding.GQA_ERR_UNSUPPORTED
+    assert _sparse8(lib, Hq=32, Hkv=1) == binding.GQA_ERR_UNSUPPORTED
+
+
 def test_workspace_registration_validates(lib):
     assert lib.gqa_set_workspace(-1, None, 0) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_set_workspace(0, P(0x10010), 1 << 20) == binding.GQA_ERR_INVALID_ARG
