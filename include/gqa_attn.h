@@ -195,7 +195,8 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
  * nothing and flag GQA_DEVERR_BAD_BLOCK_ID.  A row that selects no visible
  * token gets a zero output.  The selection is shared by all heads of the row;
  * Hq / Hkv <= 16 (the query heads of one KV head are the N columns of one
- * launch; Hkv > 1 runs one launch per KV head).  Needs no workspace. */
+ * launch; Hkv > 1 runs one launch per KV head).  num_pages * page must be
+ * below 2^31 (GQA_ERR_UNSUPPORTED otherwise).  Needs no workspace. */
 int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
                            const int32_t* block_table, const int32_t* sel_idx,
                            const int32_t* sel_cnt, int max_sel, int num_pages, int page,

@@ -163,6 +163,8 @@ int sparse_common(const void* q, const void* kcache, const void* vcache, const f
         return GQA_ERR_INVALID_ARG;
     if (!prefill_family_ok(Hq, Hkv, D) || Hq / Hkv > kMaxSparseGroup || !page_ok(page))
         return GQA_ERR_UNSUPPORTED;
+    // Cache token rows are 32-bit indices inside the kernel.
+    if ((long long)num_pages * page > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return sparse_launch(q, kcache, vcache, kscale, vscale, e4m3, block_table, sel_idx, sel_cnt,
                          max_sel, num_pages, page, ctx_len, query_rows, Hq, Hkv, scale, out,

@@ -30,8 +30,13 @@
 //   path copies into, so the MMAs are unchanged; the K scale joins the score
 //   scale and the V scale the final 1 / l.
 //
+// * Token index warp: block-table lookups (a selected id, then a page id, two
+//   dependent loads per key) are taken off the gather warps' path: warp 9
+//   resolves each tile's keys to cache token rows ahead of them, through a
+//   ring of NI shared-memory slots.
+//
 // Warp roles (320 threads): 0..3 gather, 4 TMEM owner + UMMA issuer,
-// 5..8 key warps (softmax + epilogue; thread = TMEM lane), 9 idle helper.
+// 5..8 key warps (softmax + epilogue; thread = TMEM lane), 9 token index.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -84,7 +89,9 @@ constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;            // [4][NP] floats
 constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
 constexpr int OFF_FAC = OFF_MREF + NP * 4;
 constexpr int OFF_FLAG = OFF_FAC + NP * 4;                // [2][4] ints
-constexpr int OFF_BAR = (OFF_FLAG + 32 + 7) & ~7;
+constexpr int NI = 4;                                     // token-index ring slots
+constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;       // [NI][TILE] int token rows
+constexpr int OFF_BAR = (OFF_IDX + NI * TILE * 4 + 7) & ~7;
 enum {
     B_KFULL = 0,   // [2]
     B_KEMPTY = 2,  // [2]
@@ -97,7 +104,9 @@ enum {
     B_PTEMPTY = 14,// [2]
     B_DRAIN = 16,
     B_GROUP = 17,  // key-thread group barrier
-    NUM_BARS = 18
+    B_IFULL = 18,  // [NI] token-index slot written
+    B_IEMPTY = 22, // [NI] token-index slot read
+    NUM_BARS = 26
 };
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM = OFF_TMEM + 16 + 1024;
@@ -201,6 +210,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         mbar_init(bar(B_VEMPTY), 1);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_GROUP), 128);
+        for (int b = 0; b < NI; ++b) {
+            mbar_init(bar(B_IFULL + b), 32);
+            mbar_init(bar(B_IEMPTY + b), 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -220,6 +233,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     if (warp < 4) {
         // ------------------------------------------------------------ gather
         const int gt = threadIdx.x;        // 0..127
+        const int* idx = reinterpret_cast<const int*>(gbase + OFF_IDX);
+        const size_t tok_stride = HQ == NP ? (size_t)P.kv_stride : (size_t)D;
+        // Cache row offset of this lane's key in tile-counter position gg, read
+        // from the index ring; tok < 0 for a masked key.
+        auto take_index = [&](uint32_t gg, int& tok, size_t& row) -> bool {
+            const int slot = (int)(gg % NI);
+            if (!mbar_wait(bar(B_IFULL + slot), (gg / NI) & 1, abort_flag, P.err)) return false;
+            tok = idx[slot * TILE + warp * 32 + lane];
+            mbar_arrive(bar(B_IEMPTY + slot));
+            row = tok >= 0 ? (size_t)tok * tok_stride : 0;
+            return true;
+        };
         uint32_t g = 0;                     // global tile counter
         int rloc = 0;                       // non-empty rows handled so far
         bool ok = true;
@@ -241,71 +266,102 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             }
             cp_async_arrive(bar(B_QFULL + qb));
             ++rloc;
-            for (int t = 0; t < nt && ok; ++t, ++g) {
-                // This warp's 32 keys: lane -> token info, then one 512-byte row per key.
-                const int key_l = (warp * 32) + lane;
-                const int tok_l = key_token(P, i, cnt, t, key_l, true);
-                size_t row_l = 0;
-                if (tok_l >= 0) {
-                    int pg = __ldg(P.table + (tok_l >> P.log2_page));
-                    if (pg < 0 || pg >= P.num_pages) {
-                        atomicOr(P.err, kErrBadPageId);
-                        pg = 0;
-                    }
-                    row_l = (((size_t)pg << P.log2_page) + (tok_l & ((1 << P.log2_page) - 1))) *
-                            (HQ == NP ? (size_t)P.kv_stride : (size_t)D);
+            if constexpr (F8) {
+                // E4M3 codes, software-pipelined over the row's steps (tile t, K
+                // or V): while a lane converts one step's codes into its shared
+                // memory tile it issues the next step's loads into the registers
+                // it frees, so one step (32 KB per CTA) is always in flight.  A
+                // token row is 256 code bytes: half-warp `half` takes key 2e +
+                // half, lane u of it the codes of d = 16u .. 16u + 15, which
+                // become fp16 units 2u, 2u + 1 of the row (chunk u / 4, units
+                // 2 (u % 4) and 2 (u % 4) + 1 within it).  Masked tokens are
+                // stored as zeros.
+                const int u = lane & 15, half = lane >> 4;
+                const uint32_t unit = 2u * (uint32_t)(u & 3);
+                auto load = [&](const uint8_t* cache, int tok_l, size_t row_l, int e) -> uint4 {
+                    const int src = 2 * e + half;
+                    const int tok = __shfl_sync(0xffffffffu, tok_l, src);
+                    const size_t row = __shfl_sync(0xffffffffu, row_l, src);
+                    return tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(cache + row) + u)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                };
+                int tok_l;
+                size_t row_l;
+                if (!take_index(g, tok_l, row_l)) {
+                    ok = false;
+                    break;
                 }
-                const int kb = g & 1;
-                for (int kv = 0; kv < 2; ++kv) {
+                uint4 raw[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) raw[e] = load(P.kcache8, tok_l, row_l, e);
+                for (int n = 0; n < 2 * nt && ok; ++n) {
+                    const int t = n >> 1, kv = n & 1;
+                    const uint32_t gt = g + (uint32_t)t;
+                    const int kb = gt & 1;
                     if (kv == 0) {
-                        if (!mbar_wait(bar(B_KEMPTY + kb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                        if (!mbar_wait(bar(B_KEMPTY + kb), ((gt >> 1) & 1) ^ 1, abort_flag, P.err)) {
                             ok = false;
                             break;
                         }
                     } else {
-                        if (!mbar_wait(bar(B_VEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
+                        if (!mbar_wait(bar(B_VEMPTY), (gt & 1) ^ 1, abort_flag, P.err)) {
                             ok = false;
                             break;
                         }
                     }
-                    const uint32_t tile = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V);
-                    if constexpr (F8) {
-                        // A token row is 256 code bytes: half-warp `half` takes key
-                        // 2e + half, lane u of it the codes of d = 16u .. 16u + 15,
-                        // which become fp16 units 2u, 2u + 1 of the row (chunk u / 4,
-                        // units 2 (u % 4) and 2 (u % 4) + 1 within it).  Masked
-                        // tokens are stored as zeros.
-                        const uint8_t* cache = kv == 0 ? P.kcache8 : P.vcache8;
-                        const int u = lane & 15, half = lane >> 4;
-                        uint4 raw[16];
+                    const uint32_t chunk = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V) +
+                                           (uint32_t)(u >> 2) * (TILE * 128);
+                    // The next step: V of this tile (same tokens) or K of the next.
+                    const bool more = n + 1 < 2 * nt;
+                    int ntok = tok_l;
+                    size_t nrow = row_l;
+                    if (kv == 1 && more && !take_index(gt + 1, ntok, nrow)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* ncache = kv == 0 ? P.vcache8 : P.kcache8;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int src_lane = 2 * e + half;
-                            const int tok = __shfl_sync(0xffffffffu, tok_l, src_lane);
-                            const size_t row = __shfl_sync(0xffffffffu, row_l, src_lane);
-                            raw[e] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(cache + row) + u)
-                                              : make_uint4(0u, 0u, 0u, 0u);
+                    for (int e = 0; e < 16; ++e) {
+                        const uint32_t key = (uint32_t)(warp * 32 + 2 * e + half);
+                        const uint4 r = raw[e];
+                        if (more) raw[e] = load(ncache, ntok, nrow, e);
+                        const uint4 lo = make_uint4(e4m3x2_to_f16x2(r.x), e4m3x2_to_f16x2(r.x >> 16),
+                                                    e4m3x2_to_f16x2(r.y), e4m3x2_to_f16x2(r.y >> 16));
+                        const uint4 hi = make_uint4(e4m3x2_to_f16x2(r.z), e4m3x2_to_f16x2(r.z >> 16),
+                                                    e4m3x2_to_f16x2(r.w), e4m3x2_to_f16x2(r.w >> 16));
+                        *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit) - sbase)) = lo;
+                        *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit + 1) - sbase)) = hi;
+                    }
+                    // Generic-proxy stores, read by the tensor cores (async proxy).
+                    fence_async_shared();
+                    mbar_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
+                    tok_l = ntok;
+                    row_l = nrow;
+                }
+                g += (uint32_t)nt;
+            } else {
+                for (int t = 0; t < nt && ok; ++t, ++g) {
+                    // This warp's 32 keys: lane -> cache row, then one 512-byte row per key.
+                    int tok_l;
+                    size_t row_l;
+                    if (!take_index(g, tok_l, row_l)) {
+                        ok = false;
+                        break;
+                    }
+                    const int kb = g & 1;
+                    for (int kv = 0; kv < 2; ++kv) {
+                        if (kv == 0) {
+                            if (!mbar_wait(bar(B_KEMPTY + kb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                                ok = false;
+                                break;
+                            }
+                        } else {
+                            if (!mbar_wait(bar(B_VEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
+                                ok = false;
+                                break;
+                            }
                         }
-                        const uint32_t chunk = tile + (uint32_t)(u >> 2) * (TILE * 128);
-                        const uint32_t unit = 2u * (uint32_t)(u & 3);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const uint32_t key = (uint32_t)(warp * 32 + 2 * e + half);
-                            const uint4 lo = make_uint4(e4m3x2_to_f16x2(raw[e].x),
-                                                        e4m3x2_to_f16x2(raw[e].x >> 16),
-                                                        e4m3x2_to_f16x2(raw[e].y),
-                                                        e4m3x2_to_f16x2(raw[e].y >> 16));
-                            const uint4 hi = make_uint4(e4m3x2_to_f16x2(raw[e].z),
-                                                        e4m3x2_to_f16x2(raw[e].z >> 16),
-                                                        e4m3x2_to_f16x2(raw[e].w),
-                                                        e4m3x2_to_f16x2(raw[e].w >> 16));
-                            *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit) - sbase)) = lo;
-                            *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit + 1) - sbase)) = hi;
-                        }
-                        // Generic-proxy stores, read by the tensor cores (async proxy).
-                        fence_async_shared();
-                        mbar_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
-                    } else {
+                        const uint32_t tile = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V);
                         const __half* cache = kv == 0 ? P.kcache : P.vcache;
 #pragma unroll 4
                         for (int e = 0; e < 32; ++e) {
@@ -558,6 +614,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+        }
+    }
+
+    if (warp == 9) {
+        // ------------------------------------------------------------ token index
+        // Same walk as the gather warps (rows of this CTA, tiles of each
+        // non-empty row); each lane resolves 4 of a tile's 128 keys: selected
+        // id -> token (clamped to the row, flagging bad ids) -> physical page
+        // (flagging bad pages) -> cache token row, or -1 for a masked key.
+        int* idx = reinterpret_cast<int*>(gbase + OFF_IDX);
+        const int lp = P.log2_page, pmask = (1 << P.log2_page) - 1;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+            const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
+            const int nt = row_tiles(cnt);
+            for (int t = 0; t < nt; ++t, ++g) {
+                const int slot = (int)(g % NI);
+                if (!mbar_wait(bar(B_IEMPTY + slot), ((g / NI) & 1) ^ 1, abort_flag, P.err)) {
+                    ok = false;
+                    break;
+                }
+                int tok[TILE / 32];
+#pragma unroll
+                for (int kk = 0; kk < TILE / 32; ++kk)
+                    tok[kk] = key_token(P, i, cnt, t, kk * 32 + lane, true);
+                int pg[TILE / 32];
+#pragma unroll
+                for (int kk = 0; kk < TILE / 32; ++kk)
+                    pg[kk] = tok[kk] >= 0 ? __ldg(P.table + (tok[kk] >> lp)) : 0;
+#pragma unroll
+                for (int kk = 0; kk < TILE / 32; ++kk) {
+                    int r = -1;
+                    if (tok[kk] >= 0) {
+                        int p = pg[kk];
+                        if (p < 0 || p >= P.num_pages) {
+                            atomicOr(P.err, kErrBadPageId);
+                            p = 0;
+                        }
+                        r = (p << lp) + (tok[kk] & pmask);
+                    }
+                    idx[slot * TILE + kk * 32 + lane] = r;
+                }
+                mbar_arrive(bar(B_IFULL + slot));
+            }
         }
     }
 
