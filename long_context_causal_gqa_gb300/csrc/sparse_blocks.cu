@@ -180,6 +180,12 @@ template <int HQ, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     const int nh = (HQ == NP) ? P.nh : HQ;
     const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * D;
+    // Tile buffers: two fp16 K tiles and one V tile; with E4M3 codes one K
+    // tile, the V tile, and 64 KB of code staging in the second K tile's place.
+    constexpr int NKB = F8 ? 1 : 2;
+    constexpr uint32_t KOFF = OFF_K;
+    constexpr uint32_t VOFF = F8 ? (uint32_t)KV_TILE_BYTES : (uint32_t)OFF_V;
+    constexpr uint32_t SOFF = 2u * KV_TILE_BYTES;
     constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
     constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
     extern __shared__ uint8_t smem_raw[];
@@ -248,6 +254,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         uint32_t g = 0;                     // global tile counter
         int rloc = 0;                       // non-empty rows handled so far
         bool ok = true;
+        // E4M3: the first K codes of a row are staged by the previous row's last
+        // step, so that the copy pipeline does not drain between rows.
+        bool staged = false;
+        int f8_tok = -1;
+        size_t f8_row = 0;
         for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
             const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
             const int nt = row_tiles(cnt);
@@ -267,64 +278,91 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             cp_async_arrive(bar(B_QFULL + qb));
             ++rloc;
             if constexpr (F8) {
-                // E4M3 codes, software-pipelined over the row's steps (tile t, K
-                // or V): while a lane converts one step's codes into its shared
-                // memory tile it issues the next step's loads into the registers
-                // it frees, so one step (32 KB per CTA) is always in flight.  A
-                // token row is 256 code bytes: half-warp `half` takes key 2e +
-                // half, lane u of it the codes of d = 16u .. 16u + 15, which
-                // become fp16 units 2u, 2u + 1 of the row (chunk u / 4, units
-                // 2 (u % 4) and 2 (u % 4) + 1 within it).  Masked tokens are
-                // stored as zeros.
+                // E4M3 codes.  Each gather lane copies the 16-byte code chunks it
+                // will convert into a private, double-buffered staging area
+                // (buffer b, pass e: byte (b * 16 + e) * 2048 + 16 gt), one step
+                // (tile t, K or V) ahead of the step it converts; it then waits
+                // for its own copies of the current step, converts them to fp16
+                // into the step's tile and signals it.  A token row is 256 code
+                // bytes: half-warp `half` takes key 2e + half, lane u of it the
+                // codes of d = 16u .. 16u + 15, which become fp16 units 2u, 2u + 1
+                // of the row (chunk u / 4, units 2 (u % 4) and 2 (u % 4) + 1
+                // within it).  Masked tokens are zero-filled by the copy.
                 const int u = lane & 15, half = lane >> 4;
                 const uint32_t unit = 2u * (uint32_t)(u & 3);
-                auto load = [&](const uint8_t* cache, int tok_l, size_t row_l, int e) -> uint4 {
-                    const int src = 2 * e + half;
-                    const int tok = __shfl_sync(0xffffffffu, tok_l, src);
-                    const size_t row = __shfl_sync(0xffffffffu, row_l, src);
-                    return tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(cache + row) + u)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+                auto stage_addr = [&](int b, int e) -> uint32_t {
+                    return sbase + SOFF + (uint32_t)((b * 16 + e) * 2048 + gt * 16);
                 };
-                int tok_l;
-                size_t row_l;
-                if (!take_index(g, tok_l, row_l)) {
-                    ok = false;
-                    break;
-                }
-                uint4 raw[16];
+                auto issue = [&](int b, const uint8_t* cache, int tok_l, size_t row_l) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) raw[e] = load(P.kcache8, tok_l, row_l, e);
+                    for (int e = 0; e < 16; ++e) {
+                        const int src = 2 * e + half;
+                        const int tok = __shfl_sync(0xffffffffu, tok_l, src);
+                        const size_t row = __shfl_sync(0xffffffffu, row_l, src);
+                        const uint8_t* p = tok >= 0 ? cache + row + 16 * u : cache;
+                        cp_async16(stage_addr(b, e), p, tok >= 0 ? 16u : 0u);
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                };
+                if (!staged) {
+                    if (!take_index(g, f8_tok, f8_row)) {
+                        ok = false;
+                        break;
+                    }
+                    issue(0, P.kcache8, f8_tok, f8_row);
+                }
+                staged = false;
                 for (int n = 0; n < 2 * nt && ok; ++n) {
                     const int t = n >> 1, kv = n & 1;
-                    const uint32_t gt = g + (uint32_t)t;
-                    const int kb = gt & 1;
+                    const uint32_t tg = g + (uint32_t)t;      // tile counter of this step
+                    // The next step's codes (V of this tile, or K of the next) go
+                    // into the other staging buffer, converted one step ago.
+                    if (n + 1 < 2 * nt) {
+                        if (kv == 1 && !take_index(tg + 1, f8_tok, f8_row)) {
+                            ok = false;
+                            break;
+                        }
+                        issue((n + 1) & 1, kv == 0 ? P.vcache8 : P.kcache8, f8_tok, f8_row);
+                        asm volatile("cp.async.wait_group 1;" ::: "memory");
+                    } else {
+                        // The row's last step: stage the first K codes of this
+                        // CTA's next non-empty row (its first tile is tile
+                        // counter tg + 1; 2 nt steps per row keep the buffer
+                        // parity at 0).
+                        int i2 = i + P.G;
+                        while (i2 < P.rows &&
+                               row_tiles(min(max(__ldg(P.sel_cnt + i2), 0), P.max_sel)) == 0)
+                            i2 += P.G;
+                        if (i2 < P.rows) {
+                            if (!take_index(tg + 1, f8_tok, f8_row)) {
+                                ok = false;
+                                break;
+                            }
+                            issue(0, P.kcache8, f8_tok, f8_row);
+                            staged = true;
+                            asm volatile("cp.async.wait_group 1;" ::: "memory");
+                        } else {
+                            asm volatile("cp.async.wait_group 0;" ::: "memory");
+                        }
+                    }
                     if (kv == 0) {
-                        if (!mbar_wait(bar(B_KEMPTY + kb), ((gt >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                        if (!mbar_wait(bar(B_KEMPTY), (tg & 1) ^ 1, abort_flag, P.err)) {
                             ok = false;
                             break;
                         }
                     } else {
-                        if (!mbar_wait(bar(B_VEMPTY), (gt & 1) ^ 1, abort_flag, P.err)) {
+                        if (!mbar_wait(bar(B_VEMPTY), (tg & 1) ^ 1, abort_flag, P.err)) {
                             ok = false;
                             break;
                         }
                     }
-                    const uint32_t chunk = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V) +
+                    const uint32_t chunk = sbase + (kv == 0 ? KOFF : VOFF) +
                                            (uint32_t)(u >> 2) * (TILE * 128);
-                    // The next step: V of this tile (same tokens) or K of the next.
-                    const bool more = n + 1 < 2 * nt;
-                    int ntok = tok_l;
-                    size_t nrow = row_l;
-                    if (kv == 1 && more && !take_index(gt + 1, ntok, nrow)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint8_t* ncache = kv == 0 ? P.vcache8 : P.kcache8;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const uint32_t key = (uint32_t)(warp * 32 + 2 * e + half);
-                        const uint4 r = raw[e];
-                        if (more) raw[e] = load(ncache, ntok, nrow, e);
+                        const uint4 r = *reinterpret_cast<const uint4*>(
+                            gbase + (stage_addr(n & 1, e) - sbase));
                         const uint4 lo = make_uint4(e4m3x2_to_f16x2(r.x), e4m3x2_to_f16x2(r.x >> 16),
                                                     e4m3x2_to_f16x2(r.y), e4m3x2_to_f16x2(r.y >> 16));
                         const uint4 hi = make_uint4(e4m3x2_to_f16x2(r.z), e4m3x2_to_f16x2(r.z >> 16),
@@ -334,9 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     }
                     // Generic-proxy stores, read by the tensor cores (async proxy).
                     fence_async_shared();
-                    mbar_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
-                    tok_l = ntok;
-                    row_l = nrow;
+                    mbar_arrive(bar(kv == 0 ? B_KFULL : B_VFULL));
                 }
                 g += (uint32_t)nt;
             } else {
@@ -396,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
                     for (int ks = 0; ks < TILE / 16; ++ks) {
-                        const uint64_t a = sdesc_sw128(sbase + OFF_V + (2 * h) * (TILE * 128) +
+                        const uint64_t a = sdesc_sw128(sbase + VOFF + (2 * h) * (TILE * 128) +
                                                            ks * 2048,
                                                        TILE * 128, 1024);
                         const uint64_t b =
@@ -422,8 +458,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 fence_async_shared();
                 const uint32_t g0 = g;
                 for (int t = 0; t < nt; ++t, ++g) {
-                    const int kb = g & 1;
-                    if (!mbar_wait(bar(B_KFULL + kb), (g >> 1) & 1, abort_flag, P.err)) {
+                    const int kb = (int)(g % NKB);
+                    if (!mbar_wait(bar(B_KFULL + kb), (g / NKB) & 1, abort_flag, P.err)) {
                         ok = false;
                         break;
                     }
@@ -431,7 +467,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(sbase + OFF_K + kb * KV_TILE_BYTES +
+                        const uint64_t a = sdesc_sw128(sbase + KOFF + kb * KV_TILE_BYTES +
                                                            (kk / 4) * (TILE * 128) + (kk % 4) * 32,
                                                        16, 1024);
                         const uint64_t b = sdesc_sw128(sbase + OFF_Q + qb * Q_BYTES +
