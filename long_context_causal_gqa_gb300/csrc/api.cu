@@ -7,6 +7,7 @@
 #include <math.h>
 #include <mutex>
 #include <string.h>
+#include <vector>
 
 #include "internal.h"
 
@@ -28,6 +29,8 @@ struct DeviceState {
 
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+// Kernels whose dynamic shared-memory limit was raised, per device.
+std::vector<const void*> g_smem_done[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 
 }  // namespace
@@ -49,6 +52,20 @@ const DeviceInfo* device_info() {
         st.ready = true;
     }
     return &st.info;
+}
+
+int ensure_smem_limit(const void* kernel, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    std::vector<const void*>& done = g_smem_done[dev];
+    for (const void* k : done)
+        if (k == kernel) return GQA_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return GQA_ERR_CUDA;
+    done.push_back(kernel);
+    return GQA_OK;
 }
 
 void current_workspace(void** ptr, size_t* bytes) {

@@ -92,6 +92,10 @@ inline FastDiv make_fastdiv(int d) {
     return f;
 }
 
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe.  GQA_OK or GQA_ERR_CUDA.
+int ensure_smem_limit(const void* kernel, int bytes);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (one per kernel family).  Arguments are validated by the caller.

@@ -1011,14 +1011,10 @@ template <int NP, int NWG, bool BATCHED>
 int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
                 int device) {
     using L = Layout<NP, NWG>;
-    static bool attr_done[64] = {false};
-    if (device < 64 && !attr_done[device]) {
-        if (cudaFuncSetAttribute(paged_split_kernel<NP, NWG, BATCHED>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::SMEM) != cudaSuccess)
-            return GQA_ERR_CUDA;
-        attr_done[device] = true;
-    }
+    (void)device;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, BATCHED>),
+                          L::SMEM) != GQA_OK)
+        return GQA_ERR_CUDA;
     paged_split_kernel<NP, NWG, BATCHED><<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};

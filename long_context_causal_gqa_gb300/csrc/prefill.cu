@@ -45,6 +45,7 @@
 //   (shape-only, so deterministic).  A pair tile cut between pairs leaves
 //   (O, m, l) partials in the workspace; a merge kernel combines them in pair
 //   order (exact log-sum-exp merge).
+#include <atomic>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -868,8 +869,11 @@ static void find_cut_tiles(const Params& P, MergeTasks& T) {
 // Pairs that can be resident at once with this kernel's shared memory (the
 // SMs of a pair must share a GPC, so this can be below num_sms / 2).
 static int max_pairs(int device) {
-    static int cached[64] = {0};
-    if (device < 64 && cached[device]) return cached[device];
+    static std::atomic<int> cached[64];   // 0 until known (static storage starts at 0)
+    if (device < 64) {
+        const int c = cached[device].load(std::memory_order_relaxed);
+        if (c) return c;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(NTHREADS, 1, 1);
@@ -888,7 +892,7 @@ static int max_pairs(int device) {
         return 0;
     }
     if (n > kMaxClusters) n = kMaxClusters;
-    if (device < 64) cached[device] = n;
+    if (device < 64) cached[device].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -920,12 +924,10 @@ static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 int prefill_resident_pairs() {
     const DeviceInfo* di = device_info();
     if (!di) return -1;
-    if (cudaFuncSetAttribute(prefill::prefill_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             prefill::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(prefill::prefill_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             prefill::SMEM_BYTES) != cudaSuccess)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<false>),
+                          prefill::SMEM_BYTES) != GQA_OK ||
+        ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<true>),
+                          prefill::SMEM_BYTES) != GQA_OK)
         return -1;
     return prefill::max_pairs(di->device);
 }
@@ -943,17 +945,11 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     using namespace prefill;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
-    static bool attr_done[64] = {false};
-    if (di->device < 64 && !attr_done[di->device]) {
-        if (cudaFuncSetAttribute(prefill_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return GQA_ERR_CUDA;
-        attr_done[di->device] = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<false>), SMEM_BYTES) !=
+            GQA_OK ||
+        ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<true>), SMEM_BYTES) !=
+            GQA_OK)
+        return GQA_ERR_CUDA;
     const int pairs_max = max_pairs(di->device);
     if (pairs_max < 1) return GQA_ERR_CUDA;
     // Query heads that share the single KV head are packed (positions x Hq

@@ -740,14 +740,8 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
     using KernelFn = void (*)(Params);
     const KernelFn fn = e4m3 ? (six ? sparse_kernel<kHq, true> : sparse_kernel<NP, true>)
                              : (six ? sparse_kernel<kHq, false> : sparse_kernel<NP, false>);
-    const int which = (e4m3 ? 2 : 0) + (six ? 1 : 0);
-    static bool attr_done[4][64] = {{false}};
-    if (di->device < 64 && !attr_done[which][di->device]) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
-            cudaSuccess)
-            return GQA_ERR_CUDA;
-        attr_done[which][di->device] = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(fn), SMEM) != GQA_OK)
+        return GQA_ERR_CUDA;
     // One launch per KV head: query heads g * grp .. g * grp + grp - 1 read
     // token rows of KV head g.
     const size_t esz = e4m3 ? 1 : 2;   // bytes per cache element
