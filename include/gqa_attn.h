@@ -241,9 +241,11 @@ size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int 
  * (gqa_get_device_error != 0) register the workspace again. */
 int gqa_set_workspace(int device, void* ptr, size_t bytes);
 
-/* Synchronise `stream`, then read and clear the current device's error word
- * (GQA_DEVERR_* bits; 0 = no device-side error since the last read).
- * Returns -1 if the CUDA calls themselves failed. */
+/* After the work already queued on `stream`, read and clear the current
+ * device's error word in one atomic step (a one-thread kernel on `stream`),
+ * then synchronise `stream` and return it (GQA_DEVERR_* bits; 0 = no
+ * device-side error since the last read).  Returns -1 if the CUDA calls
+ * themselves failed. */
 int gqa_get_device_error(struct CUstream_st* stream);
 
 /* Number of SM pairs (two-CTA clusters) gqa_attn_prefill runs on for the

@@ -13,8 +13,13 @@
 
 namespace gqa {
 
-// One error word per device (module-scope device memory, not an allocation).
+// One error word per device (module-scope device memory, not an allocation),
+// and where gqa_get_device_error's exchange leaves its old value.
 __device__ unsigned g_err_word;
+__device__ unsigned g_err_snapshot;
+
+// Reads and clears the error word in one atomic step.
+__global__ void err_exchange_kernel() { g_err_snapshot = atomicExch(&g_err_word, 0u); }
 
 namespace {
 
@@ -357,11 +362,16 @@ int gqa_set_workspace(int device, void* ptr, size_t bytes) {
 int gqa_get_device_error(struct CUstream_st* stream) {
     const DeviceInfo* di = device_info();
     if (!di) return -1;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+    // After the stream's earlier work, swap the word for 0 on the device (a
+    // bit set concurrently by a kernel on another stream is never lost), then
+    // read the old value back.
+    err_exchange_kernel<<<1, 1, 0, stream>>>();
+    if (cudaGetLastError() != cudaSuccess) return -1;
     unsigned v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof v) != cudaSuccess) return -1;
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof zero) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbolAsync(&v, g_err_snapshot, sizeof v, 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
     return (int)v;
 }
 
