@@ -2,8 +2,8 @@
 
 Each translation unit under csrc/ is compiled in parallel, then linked into
 ``long_context_causal_gqa_gb300/libgqa_attn.so``.  No cmake, no torch
-extension machinery; the runtime is linked statically so the library only needs
-the driver at run time.
+extension machinery; the CUDA runtime is linked statically so the library only
+needs the NVIDIA driver (libcuda) at run time.
 """
 
 from __future__ import annotations
