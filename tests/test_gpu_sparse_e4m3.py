@@ -114,3 +114,35 @@ def test_sparse_e4m3_scales_are_read_on_the_device(cuda_lib):
     ref = oracle.sparse_blocks_e4m3(s.q, s.kcache, s.vcache, 2.0 * s.kscale, 0.5 * s.vscale,
                                     s.block_table, s.sel_idx, s.sel_cnt, s.ctx_len, s.scale)
     _check(out, ref, "scales x2 / x0.5")
+
+
+def test_sparse_e4m3_empty_rows_and_bad_ids(cuda_lib):
+    """400 rows (more than one row per CTA, so the copy pipeline runs across
+    rows) with every third row selecting nothing: those rows are zero, the
+    others match the oracle.  Then out-of-range ids: masked and flagged."""
+    s = inputs.sparse_e4m3_inputs(rows=400, ctx_len=4000, tokens=64, seed=12)
+    cnt0 = s.sel_cnt.clone()
+    cnt0[::3] = 0
+    s0 = inputs.SparseE4M3Inputs(**{**s.__dict__, "sel_cnt": cnt0})
+    out = _run(cuda_lib, s0)
+    empty = torch.arange(400)[::3]
+    assert torch.count_nonzero(out[empty]) == 0
+    keep = np.array([i for i in range(400) if i % 3], dtype=np.int32)
+    _check(out[torch.as_tensor(keep, dtype=torch.long)], _ref(s0, rows=keep), "empty rows")
+    # Out-of-range ids select nothing and flag an error; the result is unchanged.
+    sel, cnt = s.sel_idx, s.sel_cnt
+    wide = torch.full((400, sel.shape[1] + 2), -1, dtype=torch.int32)
+    wide[:, : sel.shape[1]] = sel
+    cntw = cnt.clone()
+    for i in range(400):
+        n = int(cnt[i])
+        wide[i, n] = (4000 - 400 + i) // 4 + 5
+        wide[i, n + 1] = -7
+        cntw[i] = n + 2
+    sw = inputs.SparseE4M3Inputs(**{**s.__dict__, "sel_idx": wide, "sel_cnt": cntw,
+                                    "max_sel": wide.shape[1]})
+    q, kc, vc, ks, vs, bt, si, sc = _dev(sw)
+    outw = cuda_lib.sparse_blocks_e4m3(q, kc, vc, ks, vs, bt, si, sc, sw.ctx_len, sw.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() & cuda_lib.DEVERR_BAD_BLOCK_ID
+    _check(outw, _ref(s), "with bad ids")
