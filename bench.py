@@ -52,9 +52,9 @@ def visible_pairs(Q: int, KV: int) -> int:
     return Q * (KV - Q) + Q * (Q + 1) // 2
 
 
-def prefill_flops(Q: int, KV: int, Hq: int = HQ) -> float:
+def prefill_flops(Q: int, KV: int, Hq: int = HQ, Dh: int = D) -> float:
     # QK^T and PV: 2 FLOPs per multiply-add each, per query head, per visible pair.
-    return 4.0 * D * Hq * visible_pairs(Q, KV)
+    return 4.0 * Dh * Hq * visible_pairs(Q, KV)
 
 
 def load_peaks():
@@ -228,10 +228,10 @@ def make_flush(device):
     return flush
 
 
-def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0, Hq=HQ, Hkv=1):
+def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0, Hq=HQ, Hkv=1, Dh=D):
     import torch
     from long_context_causal_gqa_gb300 import inputs
-    d = inputs.dense_inputs(Q, KV, seed=seed, Hq=Hq, Hkv=Hkv)
+    d = inputs.dense_inputs(Q, KV, seed=seed, Hq=Hq, Hkv=Hkv, D=Dh)
     q, k, v = d.q.to(device), d.k.to(device), d.v.to(device)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
@@ -596,10 +596,10 @@ def run_case(args):
     flush = make_flush(device)
     if args.case == "prefill":
         t, _ = bench_prefill(binding, args.q, args.kv, args.steps, args.warmup, flush, device,
-                             Hq=args.hq, Hkv=args.hkv)
+                             Hq=args.hq, Hkv=args.hkv, Dh=args.d)
         ms = statistics.median(t)
-        fl = prefill_flops(args.q, args.kv, args.hq)
-        line = {"case": f"prefill Q={args.q} KV={args.kv} Hq={args.hq} Hkv={args.hkv}",
+        fl = prefill_flops(args.q, args.kv, args.hq, args.d)
+        line = {"case": f"prefill Q={args.q} KV={args.kv} Hq={args.hq} Hkv={args.hkv} D={args.d}",
                 "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
                 "frac_of_peak": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)}
     elif args.case == "paged_batch":
@@ -679,6 +679,7 @@ def main():
     ap.add_argument("--rows", type=int, default=8, help="--case paged: tail rows")
     ap.add_argument("--hq", type=int, default=HQ, help="--case prefill: query heads")
     ap.add_argument("--hkv", type=int, default=1, help="--case prefill: KV heads")
+    ap.add_argument("--d", type=int, default=D, help="--case prefill: head size (256 or 128)")
     ap.add_argument("--tokens", type=int, default=2048, help="--case sparse: tokens per row")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -203,9 +203,10 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return GQA_ERR_INVALID_ARG;
     if (Q < 1 || KV < 1 || Q > KV || !scale_ok(scale)) return GQA_ERR_INVALID_ARG;
-    if (!prefill_family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
+    // The dense prefill also takes head size 128.
+    if (!prefill_family_ok(Hq, Hkv, D == 128 ? kHeadDim : D)) return GQA_ERR_UNSUPPORTED;
     if ((long long)Q * Hq > 0x7fffffffLL - 256) return GQA_ERR_INVALID_ARG;
-    return prefill_launch(q, k, v, out, Q, KV, Hq, Hkv, scale, stream);
+    return prefill_launch(q, k, v, out, Q, KV, Hq, Hkv, D, scale, stream);
 }
 
 int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -317,7 +318,9 @@ int gqa_attn_sparse_blocks_e4m3(const void* q, const uint8_t* kcache, const uint
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {
-    if (D != kHeadDim || query_rows < 1 || ctx_or_kv < 1) return 0;
+    if ((D != kHeadDim && !(kind == GQA_KIND_PREFILL && D == 128)) || query_rows < 1 ||
+        ctx_or_kv < 1)
+        return 0;
     if (Hq < 1 || Hq > kMaxHeads) return 0;
     const DeviceInfo* di = device_info();
     if (!di) return 0;

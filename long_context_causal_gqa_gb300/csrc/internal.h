@@ -99,8 +99,9 @@ int ensure_smem_limit(const void* kernel, int bytes);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (one per kernel family).  Arguments are validated by the caller.
+// Dh: head size, 256 or 128.
 int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
-                   int Hq, int Hkv, float scale, cudaStream_t stream);
+                   int Hq, int Hkv, int Dh, float scale, cudaStream_t stream);
 size_t prefill_workspace_bytes(int Q, int KV, int num_sms);
 int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill kernel
 

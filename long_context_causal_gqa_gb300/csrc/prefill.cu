@@ -61,10 +61,11 @@ namespace prefill {
 constexpr int BM = 128;         // packed query rows per CTA
 constexpr int BM2 = 2 * BM;     // packed query rows per CTA pair
 constexpr int BN = 128;         // keys per KV tile
-constexpr int D = kHeadDim;     // 256
+constexpr int D = kHeadDim;     // 256, the largest head size; shared memory is laid out for it
 // Ring slots of 16 KB.  A K slot holds this CTA's 64 keys x two 64-wide d
-// chunks (8 KB each); a V slot holds two 32-key sub-tiles x this CTA's 128 d
-// (8 KB each, two 64-wide atoms of 4 KB).  A tile's half of K or V is two slots.
+// chunks (8 KB each); a V slot holds 32-key sub-tiles x this CTA's DH / 2 d
+// (64-wide atoms of 4 KB: two sub-tiles of two atoms at DH = 256, four of
+// one at DH = 128).  A tile's half of K or V is DH / 128 slots.
 constexpr int SLOT_BYTES = 16384;
 constexpr int HALF_SLOT = SLOT_BYTES / 2;
 #ifndef GQA_PREFILL_NK
@@ -73,13 +74,12 @@ constexpr int HALF_SLOT = SLOT_BYTES / 2;
 #ifndef GQA_PREFILL_NV
 #define GQA_PREFILL_NV 5
 #endif
-constexpr int NK = GQA_PREFILL_NK;            // K slots (two per tile)
-constexpr int NV = GQA_PREFILL_NV;            // V slots (two per tile)
-constexpr int Q_BYTES = BM * D * 2;           // 64 KB
+constexpr int NK = GQA_PREFILL_NK;            // K slots (DH / 128 per tile)
+constexpr int NV = GQA_PREFILL_NV;            // V slots (DH / 128 per tile)
+constexpr int Q_BYTES = BM * D * 2;           // 64 KB (the DH = 256 Q tile)
 constexpr int RING_BYTES = (NK + NV) * SLOT_BYTES;
 constexpr int NWG = 2;                        // softmax warpgroups per CTA
 constexpr int COLS = BN / NWG;                // S columns per softmax thread
-constexpr int OCOLS = D / NWG;                // O columns per softmax thread
 constexpr int NSOFT = 128 * NWG;              // softmax threads per CTA
 constexpr int NTHREADS = 64 + NSOFT + 32;     // + the V producer warp
 constexpr int V_WARP = 2 + NSOFT / 32;
@@ -96,9 +96,8 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr int kMaxClusters = 80;
 
 // UMMA shapes (M = 256 over the pair): S[256 x 128] = Q[256 x 16] K^T, both
-// K-major; O[256 x 256] += P[256 x 16] (tensor memory) V[16 x 256], V MN-major.
+// K-major; O[256 x DH] += P[256 x 16] (tensor memory) V[16 x DH], V MN-major.
 constexpr uint32_t IDESC_QK = idesc_f16_f32(256, 128, false, false);
-constexpr uint32_t IDESC_PV = idesc_f16_f32(256, 256, false, true);
 
 struct Params {
     int Q, KV, M_total, num_ptiles, G;   // M_total, num_ptiles: per head of the tile space
@@ -110,7 +109,7 @@ struct Params {
     float scale_log2;     // scale * log2(e)
     __half* out;
     FastDiv ptiles;       // divides a tile-space index by num_ptiles (its head)
-    float* ws_o;          // [G][2][BM2][D] unnormalised partial O
+    float* ws_o;          // [G][2][BM2][DH] unnormalised partial O
     float* ws_ml;         // [G][2][BM2][2] partial (m in log2 units, l)
     unsigned* err;
 };
@@ -338,11 +337,21 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volati
 }
 
 // MH: the tile space holds one pair-tile range per query head (Hkv > 1,
-// 3-D maps); otherwise one range of packed rows (2-D maps).
-template <bool MH>
+// 3-D maps); otherwise one range of packed rows (2-D maps).  DH: head size,
+// 256 or 128.
+template <bool MH, int DH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params P) {
+    static_assert(DH == 256 || DH == 128, "head size");
+    constexpr int SLOTS = DH / 128;                 // ring slots per tile, K and V each
+    constexpr int QCH = DH / 64;                    // 64-wide chunks of a Q / K row
+    constexpr int QB = BM * DH * 2;                 // this CTA's Q tile bytes
+    constexpr int VATOMS = DH / 128;                // 64-wide d atoms of this CTA's V half
+    constexpr int SUB_BYTES = 32 * VATOMS * 128;    // one 32-key V sub-tile
+    constexpr int SUBS = SLOT_BYTES / SUB_BYTES;    // V sub-tiles per slot
+    constexpr int OCOLS = DH / NWG;                 // O columns per softmax thread
+    constexpr uint32_t IDESC_PV = idesc_f16_f32(256, DH, false, true);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
@@ -429,13 +438,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         break;
                     }
                     const uint32_t qb = bar_qfull(s_bars);
-                    if (leader) mbar_arrive_expect_tx(qb, 2 * Q_BYTES);
-                    for (int c = 0; c < 4; ++c)
+                    if (leader) mbar_arrive_expect_tx(qb, 2 * QB);
+                    for (int c = 0; c < QCH; ++c)
                         tma_load_pair<MH>(s_q + c * (BM * 128), &tm_q, leader_addr(qb), c * 64, hd,
                                       pt * BM2 + BM * (int)rank);
                 }
                 for (int j = jb; ok && j < je; ++j) {
-                    for (int h = 0; h < 2 && ok; ++h) {
+                    for (int h = 0; h < SLOTS && ok; ++h) {
                         uint32_t dst, fb;
                         if (!acquire(dst, fb)) {
                             ok = false;
@@ -447,12 +456,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fb, (2 * h + cc) * 64,
                                               kvh, j * BN + 64 * (int)rank);
                         } else {
-                            // V: sub-tiles 2h, 2h + 1 (32 keys) x this CTA's 128 d
-                            for (int ss = 0; ss < 2; ++ss)
-                                for (int a = 0; a < 2; ++a)
-                                    tma_load_pair<MH>(dst + ss * HALF_SLOT + a * 4096, &tm_v, fb,
-                                                  128 * (int)rank + 64 * a, kvh,
-                                                  j * BN + (2 * h + ss) * 32);
+                            // V: sub-tiles SUBS h .. SUBS h + SUBS - 1 (32 keys)
+                            // x this CTA's DH / 2 d
+                            for (int ss = 0; ss < SUBS; ++ss)
+                                for (int a = 0; a < VATOMS; ++a)
+                                    tma_load_pair<MH>(dst + ss * SUB_BYTES + a * 4096, &tm_v, fb,
+                                                  (DH / 2) * (int)rank + 64 * a, kvh,
+                                                  j * BN + (SUBS * h + ss) * 32);
                         }
                         ++rg.n;
                     }
@@ -501,10 +511,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const uint32_t d = tmem + s_col;
                 bool next_ready = false;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < SLOTS; ++h) {
                     int slot = kr.slot();
                     if (!next_ready && !take(kr, slot)) return false;
-                    if (h == 0) next_ready = peek_next(kr);
+                    if (SLOTS > 1 && h == 0) next_ready = peek_next(kr);
                     const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
@@ -528,21 +538,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const uint32_t p_base = tmem + s_col;
                 bool next_ready = false;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < SLOTS; ++h) {
                     int slot = vr.slot();
                     if (!next_ready && !take(vr, slot)) return false;
-                    if (h == 0) next_ready = peek_next(vr);
+                    if (SLOTS > 1 && h == 0) next_ready = peek_next(vr);
                     // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
                     // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
                     const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
 #pragma unroll
-                    for (int ss = 0; ss < 2; ++ss) {
+                    for (int ss = 0; ss < SUBS; ++ss) {
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks) {
-                            const uint64_t b = desc64(v_lo + ss * (HALF_SLOT >> 4) + ks * (2048 >> 4));
+                            const uint64_t b = desc64(v_lo + ss * (SUB_BYTES >> 4) + ks * (2048 >> 4));
                             // P of keys kb .. kb + 15: part kb / COLS sits at columns
                             // COLS (kb / COLS) + (kb % COLS) / 2 of the S buffer.
-                            const int kb = (2 * h + ss) * 32 + ks * 16;
+                            const int kb = (SUBS * h + ss) * 32 + ks * 16;
                             const uint32_t a_tmem = p_base + (kb / COLS) * COLS + (kb % COLS) / 2;
                             if (h == 0 && ss == 0 && ks == 0)
                                 umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV, acc0 ? 1u : 0u);
@@ -736,7 +746,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int h = 1; h < NWG; ++h) l_row += xl[h * BM + row];
             if (jb == 0 && je == n) {
                 const float inv = (l_row > 0.f) ? 1.0f / l_row : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * D : 0) + (size_t)m_row * P.out_stride + OCOLS * hg);
+                uint4* dst = reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * DH : 0) + (size_t)m_row * P.out_stride + OCOLS * hg);
 #pragma unroll 1
                 for (int c = 0; c < OCOLS / 32; ++c) {
                     uint32_t o[32];
@@ -757,7 +767,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             } else {
                 const int slot = is_first ? 0 : 1;
                 const size_t prow = ((size_t)pair * 2 + slot) * BM2 + BM * rank + row;
-                uint4* dst = reinterpret_cast<uint4*>(P.ws_o + prow * D + OCOLS * hg);
+                uint4* dst = reinterpret_cast<uint4*>(P.ws_o + prow * DH + OCOLS * hg);
 #pragma unroll 1
                 for (int c = 0; c < OCOLS / 32; ++c) {
                     uint32_t o[32];
@@ -805,12 +815,13 @@ struct MergeTasks {
 };
 
 // blockIdx.x picks a cut pair tile, blockIdx.y 8 of its 256 rows; thread
-// (row, lane) merges 8 consecutive d.  Pieces are combined in pair order
+// (row, lane) merges 8 consecutive d (lanes past DH / 8 have none).  Pieces
+// are combined in pair order
 // (exact log-sum-exp merge), so the result does not depend on timing.  The
 // kernel is a programmatic dependent of the main kernel: its launch overlaps
 // that kernel's tail, and griddepcontrol.wait holds it until the partials are
 // complete.
-template <bool MH>
+template <bool MH, int DH>
 __global__ void __launch_bounds__(256)
 prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     const int4 tk = T.task[blockIdx.x];
@@ -821,6 +832,7 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (m_row >= P.M_total) return;
     const int d0 = (threadIdx.x & 31) * 8;
+    if (d0 >= DH) return;
     float M = -INFINITY;
     for (int c = c0; c <= c_last; ++c) {
         const size_t prow = ((size_t)c * 2 + (c == c0 ? slot0 : 0)) * BM2 + r;
@@ -835,7 +847,7 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
         const float mp = P.ws_ml[prow * 2];
         const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
         L += P.ws_ml[prow * 2 + 1] * w;
-        const float4* o = reinterpret_cast<const float4*>(P.ws_o + prow * D + d0);
+        const float4* o = reinterpret_cast<const float4*>(P.ws_o + prow * DH + d0);
         const float4 a = o[0], b = o[1];
         acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
         acc[4] += b.x * w; acc[5] += b.y * w; acc[6] += b.z * w; acc[7] += b.w * w;
@@ -843,7 +855,7 @@ prefill_merge_kernel(const Params P, const __grid_constant__ MergeTasks T) {
     const float inv = L > 0.f ? 1.0f / L : 0.f;
     uint4 hv = make_uint4(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv),
                           pack_half2(acc[4] * inv, acc[5] * inv), pack_half2(acc[6] * inv, acc[7] * inv));
-    *reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * D : 0) + (size_t)m_row * P.out_stride + d0) = hv;
+    *reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * DH : 0) + (size_t)m_row * P.out_stride + d0) = hv;
 }
 
 // Host side of the schedule: the cut pair tiles and their pieces.
@@ -886,8 +898,9 @@ static int max_pairs(int device) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    // Both instantiations have the same threads, shared memory and clusters.
-    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<false>, &cfg) != cudaSuccess || n < 1) {
+    // All instantiations have the same threads, shared memory and clusters.
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<false, 256>, &cfg) != cudaSuccess ||
+        n < 1) {
         cudaGetLastError();
         return 0;
     }
@@ -897,10 +910,13 @@ static int max_pairs(int device) {
 }
 
 // One main-kernel launch and, when pair tiles were cut, its merge.
-template <bool MH>
+template <bool MH, int DH>
 static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Params& P, const MergeTasks& tasks, cudaStream_t stream) {
-    prefill_kernel<MH><<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<MH, DH>), SMEM_BYTES) !=
+        GQA_OK)
+        return GQA_ERR_CUDA;
+    prefill_kernel<MH, DH><<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     if (tasks.n > 0) {
         cudaLaunchConfig_t cfg = {};
@@ -913,7 +929,7 @@ static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel<MH>, P, tasks) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, prefill_merge_kernel<MH, DH>, P, tasks) != cudaSuccess)
             return GQA_ERR_CUDA;
     }
     return GQA_OK;
@@ -924,9 +940,7 @@ static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 int prefill_resident_pairs() {
     const DeviceInfo* di = device_info();
     if (!di) return -1;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<false>),
-                          prefill::SMEM_BYTES) != GQA_OK ||
-        ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<true>),
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<false, 256>),
                           prefill::SMEM_BYTES) != GQA_OK)
         return -1;
     return prefill::max_pairs(di->device);
@@ -941,14 +955,12 @@ size_t prefill_workspace_bytes(int Q, int KV, int num_sms) {
 }
 
 int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
-                   int Hq, int Hkv, float scale, cudaStream_t stream) {
+                   int Hq, int Hkv, int Dh, float scale, cudaStream_t stream) {
     using namespace prefill;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<false>), SMEM_BYTES) !=
-            GQA_OK ||
-        ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<true>), SMEM_BYTES) !=
-            GQA_OK)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<false, 256>), SMEM_BYTES) !=
+        GQA_OK)
         return GQA_ERR_CUDA;
     const int pairs_max = max_pairs(di->device);
     if (pairs_max < 1) return GQA_ERR_CUDA;
@@ -964,7 +976,7 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     P.heads = packed ? 1 : Hq;
     P.head_group = packed ? 1 : Hq / Hkv;
     P.grp = make_fastdiv(grp);
-    P.out_stride = packed ? D : Hq * D;
+    P.out_stride = packed ? Dh : Hq * Dh;
     P.M_total = Q * grp;
     P.num_ptiles = (P.M_total + BM2 - 1) / BM2;
     P.ptiles = make_fastdiv(P.num_ptiles);
@@ -997,21 +1009,23 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
 
     CUtensorMap tq, tk, tv;
     if (packed) {
-        if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, D, D, BM, 64) ||
-            !make_map_2d_f16(&tk, k, (uint64_t)KV, D, D, BN / 2, 64) ||
-            !make_map_2d_f16(&tv, v, (uint64_t)KV, D, D, 32, 64))
+        if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, Dh, Dh, BM, 64) ||
+            !make_map_2d_f16(&tk, k, (uint64_t)KV, Dh, Dh, BN / 2, 64) ||
+            !make_map_2d_f16(&tv, v, (uint64_t)KV, Dh, Dh, 32, 64))
             return GQA_ERR_CUDA;
-        return launch_one<false>(tq, tk, tv, P, tasks, stream);
+        return Dh == 256 ? launch_one<false, 256>(tq, tk, tv, P, tasks, stream)
+                         : launch_one<false, 128>(tq, tk, tv, P, tasks, stream);
     }
-    const uint64_t row_bytes = 2ull * D;
-    if (!make_map_3d_f16(&tq, q, D, (uint64_t)Hq, (uint64_t)Q, row_bytes,
+    const uint64_t row_bytes = 2ull * Dh;
+    if (!make_map_3d_f16(&tq, q, Dh, (uint64_t)Hq, (uint64_t)Q, row_bytes,
                          (uint64_t)Hq * row_bytes, BM) ||
-        !make_map_3d_f16(&tk, k, D, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
+        !make_map_3d_f16(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
                          (uint64_t)Hkv * row_bytes, BN / 2) ||
-        !make_map_3d_f16(&tv, v, D, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
+        !make_map_3d_f16(&tv, v, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
                          (uint64_t)Hkv * row_bytes, 32))
         return GQA_ERR_CUDA;
-    return launch_one<true>(tq, tk, tv, P, tasks, stream);
+    return Dh == 256 ? launch_one<true, 256>(tq, tk, tv, P, tasks, stream)
+                     : launch_one<true, 128>(tq, tk, tv, P, tasks, stream);
 }
 
 }  // namespace gqa

@@ -61,7 +61,8 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, Q=0) == binding.GQA_ERR_INVALID_ARG
     assert _prefill(lib, scale=0.0) == binding.GQA_ERR_INVALID_ARG
     assert _prefill(lib, scale=float("nan")) == binding.GQA_ERR_INVALID_ARG
-    assert _prefill(lib, D=128) == binding.GQA_ERR_UNSUPPORTED
+    assert _prefill(lib, D=64) == binding.GQA_ERR_UNSUPPORTED    # 128 and 256 are accepted
+    assert _prefill(lib, D=192) == binding.GQA_ERR_UNSUPPORTED
     # Any grouping with Hkv | Hq (Hq <= 64) is accepted; these are not.
     assert _prefill(lib, Hq=7, Hkv=2) == binding.GQA_ERR_UNSUPPORTED
     assert _prefill(lib, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED

@@ -112,6 +112,48 @@ def test_prefill_groupings_split_and_replay(cuda_lib, Hq, Hkv):
     assert cuda_lib.device_error() == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,Q,KV", [
+    (6, 1, 256, 1024),   # the small configuration at head size 128
+    (6, 1, 1, 1),
+    (6, 1, 22, 150),     # one ragged q-tile
+    (6, 1, 300, 300),
+    (8, 2, 100, 777),    # several KV heads: one launch, 3-D maps
+    (4, 4, 257, 900),
+])
+def test_prefill_head_size_128_matches_oracle(cuda_lib, Hq, Hkv, Q, KV):
+    d = inputs.dense_inputs(Q, KV, seed=Q + KV + 128, Hq=Hq, Hkv=Hkv, D=128)
+    out = _run(cuda_lib, d)
+    ref = oracle.dense(d.q, d.k, d.v, d.scale)
+    _check(out, ref, f"D=128 Hq={Hq} Hkv={Hkv} Q={Q} KV={KV}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 1), (6, 2)])
+def test_prefill_head_size_128_split_and_replay(cuda_lib, Hq, Hkv):
+    """Pair tiles cut between CTA pairs and merged, at head size 128; sampled
+    rows against the oracle, bitwise equal on a second run and on graph replay."""
+    dev = torch.device("cuda")
+    Q, KV = 2000, 9000
+    d = inputs.dense_inputs(Q, KV, seed=13, Hq=Hq, Hkv=Hkv, D=128)
+    q, k, v = d.q.to(dev), d.k.to(dev), d.v.to(dev)
+    a = cuda_lib.prefill(q, k, v, d.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    rows = _sample_rows(Q, n=24, seed=Hq + 128)
+    ref = oracle.dense(d.q, d.k, d.v, d.scale, rows=rows)
+    _check(a[torch.as_tensor(rows, dtype=torch.long)], ref, f"D=128 Hq={Hq} Hkv={Hkv}")
+    b = cuda_lib.prefill(q, k, v, d.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    out = torch.empty_like(q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.prefill(q, k, v, d.scale, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), a.view(torch.int16))
+
+
 def _sample_rows(Q, n=48, seed=0):
     rng = np.random.default_rng(seed)
     fixed = [0, 1, 20, 21, 22, 42, 43, Q // 2, Q - 22, Q - 2, Q - 1]
