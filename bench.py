@@ -13,7 +13,7 @@ L2 is flushed before every timed step.  The same line carries:
   host<->device copies inside the timed region;
 * ``cpu_baseline``: the FP64 CPU oracle on a bounded sample of query rows;
 * ``secondary``: KV=128000 (the KV sweep 40K..128K with --sweep), two other
-  head groupings of the headline shape, the paged E4M3 verifier tail at ctx
+  head groupings and head size 128 of the headline shape, the paged E4M3 verifier tail at ctx
   261888 (HBM roofline), a batch of variable-length tails, and the
   selected-block sparse prefill.
 
@@ -512,13 +512,14 @@ def run_gpu(args):
             secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
                               "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
                               "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4)})
-        for hq, hkv in ((6, 2), (8, 1)):
-            # Other head groupings: Hkv > 1 runs one launch per query head.
+        for hq, hkv, dh in ((6, 2, D), (8, 1, D), (6, 1, 128)):
+            # Other head groupings (every query head's tiles in one launch when
+            # Hkv > 1) and head size 128.
             t, _ = bench_prefill(binding, Q, KV, max(3, args.steps // 2), 2, flush, device,
-                                 Hq=hq, Hkv=hkv)
+                                 Hq=hq, Hkv=hkv, Dh=dh)
             ms = statistics.mean(t)
-            fl = prefill_flops(Q, KV, hq)
-            secondary.append({"what": f"prefill Q={Q} KV={KV} Hq={hq} Hkv={hkv}",
+            fl = prefill_flops(Q, KV, hq, dh)
+            secondary.append({"what": f"prefill Q={Q} KV={KV} Hq={hq} Hkv={hkv} D={dh}",
                               "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
                               "frac_of_peak": round(fl / ms / 1e9 / peak, 4)})
         for R in (1, 2, 8):
