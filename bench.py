@@ -12,10 +12,14 @@ L2 is flushed before every timed step.  The same line carries:
 * ``e2e``: the same metric through the C ABI with pinned host buffers and the
   host<->device copies inside the timed region;
 * ``cpu_baseline``: the FP64 CPU oracle on a bounded sample of query rows;
-* ``secondary``: KV=128000 (the KV sweep 40K..128K with --sweep), two other
-  head groupings and head size 128 of the headline shape, the paged E4M3 verifier tail at ctx
-  261888 (HBM roofline), a batch of variable-length tails, and the
-  selected-block sparse prefill.
+  ``cpu_baselines`` times it on the other workloads as well (the small
+  prefill in full, the E4M3 tails in full, the sparse prefill in full at 64
+  and 512 tokens and on 512 sampled rows at 2048);
+* ``secondary``: the rest of the 12-shape KV sweep (40K..128K), two other
+  head groupings and head size 128 of the headline shape, the paged E4M3
+  verifier tail at ctx 261888 (HBM roofline; one call alone, and calls back
+  to back over distinct caches as the layers of a model run them), a batch of
+  variable-length tails, and the selected-block sparse prefill.
 
 ``--impl reference`` times the CPU oracle alone on the same workload (bounded
 sample per step) and prints the same kind of line with "impl": "reference".
@@ -335,6 +339,35 @@ def bench_paged(binding, R, device, steps, warmup, flush, ctx_len=TAIL_CTX, seed
     return times, tail_kv_bytes(ctx_len), 4.0 * D * HQ * visible_pairs(R, ctx_len)
 
 
+def bench_paged_layers(binding, R, device, steps, warmup, flush, layers=4, ctx_len=TAIL_CTX,
+                       seed=0):
+    """`layers` tail calls back to back in one CUDA graph, each over its own
+    cache (a model's layers: 4 x 134 MB, so no call finds the previous one's
+    bytes in L2), L2 flushed before each replay; returns per-call times."""
+    import torch
+    from long_context_causal_gqa_gb300 import inputs
+    sets = []
+    for l in range(layers):
+        p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx_len, capacity=TAIL_CAPACITY,
+                                     seed=seed * 16 + l)
+        sets.append((p.q.to(device), p.kcache.to(device), p.vcache.to(device),
+                     torch.tensor([p.kscale], dtype=torch.float32, device=device),
+                     torch.tensor([p.vscale], dtype=torch.float32, device=device),
+                     p.block_table.to(device)))
+    outs = [torch.empty_like(st[0]) for st in sets]
+
+    def call():
+        for st, o in zip(sets, outs):
+            binding.paged_e4m3(*st, ctx_len, SCALE, out=o)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    times = time_steps(g.replay, steps, warmup, flush, torch.cuda.current_stream())
+    return [t / layers for t in times], tail_kv_bytes(ctx_len)
+
+
 def bench_paged_batch(binding, device, steps, warmup, flush, B=8, R=2, max_ctx=65536, seed=0):
     """B verifier tails of seeded lengths (about 262K tokens in all) in one
     gqa_attn_paged_e4m3_batch call, replayed from a CUDA graph with the
@@ -426,6 +459,67 @@ def cpu_baseline_prefill(Q, KV, seconds_target=15.0, seed=0):
             "sample": f"{n} of {Q} query rows x {HQ} heads of Q={Q} KV={KV}, FP64 two-pass"}
 
 
+def _timed(fn):
+    t0 = time.perf_counter()
+    r = fn()
+    return r, time.perf_counter() - t0
+
+
+def cpu_baselines_other(seed=0):
+    """The FP64 oracle, as it stands, timed on the small prefill (in full), the
+    E4M3 verifier tails at ctx 261888 (in full, R = 1, 2, 8) and the sparse
+    prefill (in full at T = 64 and 512, 512 sampled rows at T = 2048).  The
+    oracle runs one thread per query row, so `cores` is min(rows, host cores)."""
+    import numpy as np
+    import oracle
+    from long_context_causal_gqa_gb300 import inputs
+    ncores = os.cpu_count() or 1
+    res = []
+    d = inputs.dense_inputs(256, 1024, seed=seed)
+    _, dt = _timed(lambda: oracle.dense(d.q, d.k, d.v, SCALE, nthreads=ncores))
+    fl = prefill_flops(256, 1024)
+    res.append({"what": "dense prefill Q=256 KV=1024 (full)", "seconds": round(dt, 3),
+                "TFLOP/s": fl / dt / 1e12, "cores": min(ncores, 256), "kind": "oracle"})
+    for R in (1, 2, 8):
+        p = inputs.paged_e4m3_inputs(R=R, ctx_len=TAIL_CTX, capacity=TAIL_CAPACITY, seed=seed)
+        _, dt = _timed(lambda: oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale,
+                                                 p.block_table, p.ctx_len, SCALE,
+                                                 nthreads=ncores))
+        nbytes = tail_kv_bytes(TAIL_CTX)
+        res.append({"what": f"paged E4M3 tail R={R} ctx={TAIL_CTX} (full)",
+                    "seconds": round(dt, 3), "GB/s": nbytes / dt / 1e9,
+                    "TFLOP/s": 4.0 * D * HQ * visible_pairs(R, TAIL_CTX) / dt / 1e12,
+                    "cores": min(ncores, R), "kind": "oracle"})
+    for T in (64, 512, 2048):
+        s = inputs.sparse_inputs(rows=4096, ctx_len=32768, tokens=T, seed=seed)
+        rows = None
+        n_rows = 4096
+        if T == 2048:
+            rows = np.sort(np.random.default_rng(T).choice(4096, 512, replace=False)).astype(
+                np.int32)
+            n_rows = 512
+        _, dt = _timed(lambda: oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table,
+                                                    s.sel_idx, s.sel_cnt, s.ctx_len, SCALE,
+                                                    rows=rows, nthreads=ncores))
+        rr = range(4096) if rows is None else rows
+        visible = sum(4 * int(s.sel_cnt[i]) - (3 - (32768 - 4096 + int(i)) % 4) for i in rr)
+        res.append({"what": f"sparse blocks T={T} ctx=32768, "
+                            + ("4096 rows (full)" if rows is None else "512 of 4096 rows"),
+                    "seconds": round(dt, 3),
+                    "TFLOP/s": 4.0 * D * HQ * visible / dt / 1e12,
+                    "cores": min(ncores, n_rows), "kind": "oracle"})
+    return res
+
+
+def config_of(Q, KV, world):
+    """The `config` both arms report for the headline workload."""
+    return {"workload": f"dense causal GQA prefill Q={Q} KV={KV} Hq=6 Hkv=1 D=256 "
+                        "scale=1/16 batch 1", "Q": Q, "KV": KV,
+            "l2": "flushed before every timed GPU step (256 MB write, then 256 MB read of a "
+                  "second buffer)",
+            "parallelism": f"{world} independent problem(s), one per GPU"}
+
+
 def run_gpu(args):
     import torch
     rank, world, local = dist_env()
@@ -476,11 +570,9 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
         "data": "synthetic: seeded i.i.d. N(0,1) fp16 q/k/v",
-        "config": {"workload": f"dense causal GQA prefill Q={Q} KV={KV} Hq=6 Hkv=1 D=256 "
-                               "scale=1/16 batch 1", "Q": Q, "KV": KV,
-                   "l2": "flushed before every timed step (256 MB write, then 256 MB read of a second buffer)",
-                   "prewarm": f"untimed steps for >= {PREWARM_S} s before the W warm-up steps",
-                   "parallelism": f"{world} independent problem(s), one per GPU"},
+        "config": config_of(Q, KV, world),
+        "timing": {"prewarm": f"untimed steps for >= {PREWARM_S} s before the W warm-up steps",
+                   "clock": "CUDA events on the launching stream, mean over the K timed steps"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} bf16 dense burst (fp16 same nominal rate)",
@@ -506,7 +598,7 @@ def run_gpu(args):
     }
     secondary = []
     if not args.quick:
-        for kv in ([x for x in KV_SWEEP if x != KV] if args.sweep else [KV_SWEEP[-1]]):
+        for kv in ([x for x in KV_SWEEP if x != KV] if not args.no_sweep else [KV_SWEEP[-1]]):
             t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device)
             ms = statistics.mean(t)
             secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
@@ -543,6 +635,19 @@ def run_gpu(args):
                                   "paged_split_kernel_ctx261888.md",
                                   "long_context_causal_gqa_gb300/csrc/paged_e4m3.cu",
                                   f"traffic_bytes_per_launch_R{R}")})
+        for R in (1, 8):
+            try:
+                t, nbytes = bench_paged_layers(binding, R, device, 30, 5, flush)
+                derr = binding.device_error()
+                us = statistics.median(t) * 1e3
+                gbs = nbytes / (us * 1e-6) / 1e9
+                secondary.append({"what": f"paged E4M3 tail R={R} ctx=261888, 4 calls back to "
+                                          "back over 4 distinct caches (graph replay), per call",
+                                  "us": round(us, 2), "GB/s": round(gbs, 1),
+                                  "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                                  "device_error": derr})
+            except Exception as e:  # a secondary failure must not lose the headline
+                secondary.append({"what": f"paged_e4m3 layers R={R}", "error": str(e)[:200]})
         try:
             t, nbytes, ctxs = bench_paged_batch(binding, device, 50, 5, flush)
             derr = binding.device_error()
@@ -577,6 +682,11 @@ def run_gpu(args):
     line["secondary"] = secondary
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(Q, KV, seconds_target=args.cpu_seconds)
+        if not args.quick:
+            try:
+                line["cpu_baselines"] = cpu_baselines_other()
+            except Exception as e:
+                line["cpu_baselines"] = [{"error": str(e)[:200]}]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -627,6 +737,11 @@ def run_case(args):
 
 
 def run_reference(args):
+    """The reference arm: the FP64 oracle, as it stands, on the host cores.
+    Each step times the oracle on a bounded sample of the headline workload's
+    query rows; `value` is the causal-visible FLOP rate of that sampled work,
+    and `ms_per_step` the mean time of a step as run (the time the whole
+    problem would take at that rate is reported separately)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -646,12 +761,12 @@ def run_reference(args):
         "metric": "causal-visible TFLOP/s of dense causal GQA prefill (Q=8000, KV=40000, "
                   "Hq=6, Hkv=1, D=256); % of FP16 tensor-core peak",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_full, 1),
-        "ms_per_step_note": "extrapolated to the full problem from the sampled rows",
+        "warmup": args.warmup, "ms_per_step": round(statistics.mean(secs) * 1e3, 1),
+        "ms_per_step_note": "wall time of one step as run: the oracle on the sampled rows",
+        "ms_full_problem_extrapolated": round(ms_full, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic: seeded i.i.d. N(0,1) fp16 q/k/v",
-        "config": {"workload": f"dense causal GQA prefill Q={Q} KV={KV} Hq=6 Hkv=1 D=256 "
-                               "scale=1/16 batch 1", "Q": Q, "KV": KV},
+        "config": config_of(Q, KV, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"],
                          "kind": "oracle", "sample": last["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -668,7 +783,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--q", type=int, default=Q_MAIN)
     ap.add_argument("--kv", type=int, default=KV_MAIN)
-    ap.add_argument("--sweep", action="store_true", help="secondary: all 12 KV shapes")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="secondary: only KV=128000 of the 12-shape KV sweep")
     ap.add_argument("--quick", action="store_true", help="headline only, no secondary")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -74,6 +74,7 @@ typedef enum {
 #define GQA_DEVERR_BAD_BLOCK_ID 0x2u  /* sel_idx held an id < 0 or past the row's own block */
 #define GQA_DEVERR_BAD_PAGE_ID  0x4u  /* a block-table entry was < 0 or >= num_pages */
 #define GQA_DEVERR_BAD_CTX_LEN  0x8u  /* a device-side ctx_len was < query_rows or > max_ctx_len */
+#define GQA_DEVERR_DUP_BLOCK_ID 0x10u /* sel_idx held an id an earlier position of its row holds */
 
 /* Dense causal prefill [P1, Purpose].
  *   q   [Q, Hq, D]  fp16     k, v [KV, Hkv, D] fp16     out [Q, Hq, D] fp16
@@ -192,9 +193,12 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
  *                (tokens 4b .. 4b+3); sel_cnt [query_rows] int32, 0..max_sel
  * Row i (position p = ctx_len - query_rows + i) attends the tokens of its
  * first sel_cnt[i] selected blocks that are <= p; the row's own block is
- * clamped to p.  A row's ids must be distinct.  Ids < 0 or > p / 4 select
- * nothing and flag GQA_DEVERR_BAD_BLOCK_ID.  A row that selects no visible
- * token gets a zero output.  The selection is shared by all heads of the row;
+ * clamped to p.  Selection has set semantics ([P3] Changes: stale or padded
+ * entries are masked, not attended): an id that an earlier position of the
+ * row already holds selects nothing more and flags GQA_DEVERR_DUP_BLOCK_ID;
+ * ids < 0 or > p / 4 select nothing and flag GQA_DEVERR_BAD_BLOCK_ID.  The
+ * order of a row's ids changes the result only within rounding.  A row that
+ * selects no visible token gets a zero output.  The selection is shared by all heads of the row;
  * Hq / Hkv <= 16 (the query heads of one KV head are the N columns of one
  * launch; Hkv > 1 runs one launch per KV head).  num_pages * page must be
  * below 2^31 (GQA_ERR_UNSUPPORTED otherwise).  Needs no workspace. */

@@ -34,6 +34,7 @@ DEVERR_WAIT_TIMEOUT = 0x1
 DEVERR_BAD_BLOCK_ID = 0x2
 DEVERR_BAD_PAGE_ID = 0x4
 DEVERR_BAD_CTX_LEN = 0x8
+DEVERR_DUP_BLOCK_ID = 0x10
 
 # Every symbol include/gqa_attn.h declares.
 EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_devctx",

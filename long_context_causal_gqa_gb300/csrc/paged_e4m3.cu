@@ -23,10 +23,13 @@
 //     O^T[128 d x 3NP]   += V^T[128 d x 128 keys] . [P1 | P2 | P3]^T
 //                           (MN-major A, one UMMA chain per half of d)
 //   Q and P are fp16 / fp32 quantities; each enters as a three-term E4M3
-//   expansion x ~= t1 + t2 / 16 + t3 / 256 (each term the E4M3 rounding of
+//   expansion x ~= t1 + t2 / 32 + t3 / 1024 (each term the E4M3 rounding of
 //   the scaled remainder), which carries at least fp16's 11 significant bits,
-//   so S = S1 + S2 / 16 + S3 / 256 and likewise O.  Q uses one scale per
+//   so S = S1 + S2 / 32 + S3 / 1024 and likewise O.  Q uses one scale per
 //   packed row (its absmax maps to 256); P <= 256 by the lazy rescale below.
+//   With |x| <= 256 a remainder is at most half an E4M3 unit of x (<= 8), so
+//   32 times it stays inside E4M3's range (448), and the smallest x the
+//   expansion keeps is 2^-19 (E4M3's smallest subnormal, 2^-9, over 32^2).
 //   K's and V's fp32 scales are applied to S and to the merged output.
 // * Raw pages arrive by TMA tensor copies (128-byte swizzle, two 128-byte
 //   halves of d per page) through a ring of 32 KB stages (K0, K1, V0, K2,
@@ -38,11 +41,15 @@
 //   up to 32 packed rows S^T is double-buffered in tensor memory; at 48 the
 //   three-term S^T and O^T leave room for one S^T buffer, which the softmax
 //   releases as soon as it has read it.
-// * Softmax over keys runs across TMEM lanes.  A per-row reference max moves
-//   only when a score exceeds it by more than 8 (log2 units); the common case
-//   is one threshold compare and a warpgroup vote per tile, and the exact
-//   cross-lane max is taken only on the first tile or when the vote fires.
-//   Row sums stay per thread until the split's end.
+// * Softmax over keys runs across TMEM lanes.  A per-row reference moves only
+//   when a score exceeds it by more than 8 (log2 units, so P <= 256); it is
+//   then set REF_SHIFT = 6 below the tile's exact max, so that right after a
+//   move the largest P is 64 and the expansion's floor of 2^-19 sits at least
+//   25 binades below the row's maximum (the fp16 P of the dense kernels
+//   reaches 2^-24 below theirs).  The common case is one threshold compare and
+//   a warpgroup vote per tile; the exact cross-lane max is taken only on the
+//   first tile or when the vote fires.  Row sums stay per thread until the
+//   split's end.
 //
 // Warp roles (64 + 128 NWG threads): 0 TMA producer, 1 TMEM owner + UMMA
 // issuer, then NWG = 2 / 4 / 6 softmax warpgroups for 16 / 32 / 48 packed
@@ -66,6 +73,10 @@ constexpr int RAW_STAGE = TILE * D;             // 32 KB of E4M3 per K or V tile
 // then 4 * NWG softmax warps.
 __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// A moved reference sits this far below the tile's max (log2 units).
+constexpr float REF_SHIFT = 6.0f;
+// Ratio between consecutive terms of the three-term E4M3 expansions.
+constexpr float XRATIO = 32.0f;
 
 struct Params {
     const uint8_t* kcache;
@@ -176,17 +187,17 @@ __device__ __forceinline__ void e4m3x2_val(uint32_t v, float& a, float& b) {
     a = __low2float(hh);
     b = __high2float(hh);
 }
-// x ~= t1 + t2 / 16 + t3 / 256 with t1, t2, t3 E4M3, for two values at once
-// (each result holds the pair's two bytes in its low 16 bits).
+// x ~= t1 + t2 / 32 + t3 / 1024 with t1, t2, t3 E4M3, for two values at
+// once, |x| <= 256 (each result holds the pair's two bytes in its low 16 bits).
 __device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& t1, uint32_t& t2,
                                               uint32_t& t3) {
     float a0, a1;
     t1 = e4m3x2(x0, x1);
     e4m3x2_val(t1, a0, a1);
-    const float r0 = (x0 - a0) * 16.f, r1 = (x1 - a1) * 16.f;
+    const float r0 = (x0 - a0) * XRATIO, r1 = (x1 - a1) * XRATIO;
     t2 = e4m3x2(r0, r1);
     e4m3x2_val(t2, a0, a1);
-    t3 = e4m3x2((r0 - a0) * 16.f, (r1 - a1) * 16.f);
+    t3 = e4m3x2((r0 - a0) * XRATIO, (r1 - a1) * XRATIO);
 }
 
 // Byte offset of 16-byte unit u (0..7) of row r inside a 128B-swizzled block.
@@ -525,7 +536,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     } else {
         // ---- Q -> three-term E4M3 expansion [Q1 | Q2 | Q3] in shared memory
         // (K-major, 3NP rows of 256 bytes in two 128-byte halves, 128B-swizzled),
-        // one scale per packed row: x / qs ~= t1 + t2 / 16 + t3 / 256, |x / qs| <= 256.
+        // one scale per packed row: x / qs ~= t1 + t2 / 32 + t3 / 1024, |x / qs| <= 256.
         // Warps 1..9 take rows r = warp - 1, warp + 8, ...; all their loads are
         // issued before the first conversion.
         const float kscale = *P.kscale;
@@ -709,8 +720,9 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     }
 #pragma unroll
                     for (int c = 0; c < NH; ++c)
-                        s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
-                                    fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c]))) *
+                        s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / (XRATIO * XRATIO),
+                                    fmaf(__uint_as_float(r2[c]), 1.0f / XRATIO,
+                                         __uint_as_float(r1[c]))) *
                                (kSl2InRegs ? sl2[kSl2InRegs ? c : 0] : sl2k * qs[c0 + c]);
                 }
                 const int key = (t_begin + jj) * TILE + k;
@@ -755,8 +767,9 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                         const float old = mref[c];
                         float f = 1.0f;
                         if (tmax > old + RESCALE_THRESHOLD) {
-                            f = (old == -INFINITY) ? 0.f : ex2(old - tmax);
-                            mref[c] = tmax;
+                            const float ref = tmax - REF_SHIFT;
+                            f = (old == -INFINITY) ? 0.f : ex2(old - ref);
+                            mref[c] = ref;
                         }
                         fac[c] = f;
                     }
@@ -871,8 +884,9 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     for (int c = 0; c < NH; ++c)
                         if (c0 + c < P.nq)
                             P.ws_o[((size_t)split * P.nq + c0 + c) * D + d] =
-                                fmaf(__uint_as_float(r3[c]), 1.0f / 256.0f,
-                                     fmaf(__uint_as_float(r2[c]), 0.0625f, __uint_as_float(r1[c])));
+                                fmaf(__uint_as_float(r3[c]), 1.0f / (XRATIO * XRATIO),
+                                     fmaf(__uint_as_float(r2[c]), 1.0f / XRATIO,
+                                          __uint_as_float(r1[c])));
                 }
             }
             if (ntl == 0 && k < NH && c0 + k < P.nq) {

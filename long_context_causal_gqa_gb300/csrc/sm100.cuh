@@ -17,6 +17,7 @@ constexpr unsigned kErrWaitTimeout = 0x1u;
 constexpr unsigned kErrBadBlockId = 0x2u;
 constexpr unsigned kErrBadPageId = 0x4u;
 constexpr unsigned kErrBadCtxLen = 0x8u;
+constexpr unsigned kErrDupBlockId = 0x10u;
 
 // A pipeline wait that has not completed after this long means a bug; the
 // kernel records kErrWaitTimeout and unwinds instead of spinning forever.

@@ -33,7 +33,13 @@
 // * Token index warp: block-table lookups (a selected id, then a page id, two
 //   dependent loads per key) are taken off the gather warps' path: warp 9
 //   resolves each tile's keys to cache token rows ahead of them, through a
-//   ring of NI shared-memory slots.
+//   ring of NI shared-memory slots that the gather warps and the key warps
+//   both read (a key whose row is -1 is masked in the copy and the softmax).
+// * Selection has set semantics: an id that an earlier position of the row
+//   already holds selects nothing more.  The index warp keeps a bitmap of the
+//   row's ids seen so far (exact for rows whose own block is below
+//   SEEN_BITS; beyond that a hash of the id, with a hit confirmed against the
+//   earlier positions), masks the repeat and flags it on the device.
 //
 // Warp roles (320 threads): 0..3 gather, 4 TMEM owner + UMMA issuer,
 // 5..8 key warps (softmax + epilogue; thread = TMEM lane), 9 token index.
@@ -89,9 +95,11 @@ constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;            // [4][NP] floats
 constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
 constexpr int OFF_FAC = OFF_MREF + NP * 4;
 constexpr int OFF_FLAG = OFF_FAC + NP * 4;                // [2][4] ints
-constexpr int NI = 4;                                     // token-index ring slots
+constexpr int NI = 8;                                     // token-index ring slots
 constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;       // [NI][TILE] int token rows
-constexpr int OFF_BAR = (OFF_IDX + NI * TILE * 4 + 7) & ~7;
+constexpr int SEEN_BITS = 16384;                          // block ids seen in the row
+constexpr int OFF_SEEN = OFF_IDX + NI * TILE * 4;         // [SEEN_BITS / 32] words
+constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
 enum {
     B_KFULL = 0,   // [2]
     B_KEMPTY = 2,  // [2]
@@ -104,9 +112,9 @@ enum {
     B_PTEMPTY = 14,// [2]
     B_DRAIN = 16,
     B_GROUP = 17,  // key-thread group barrier
-    B_IFULL = 18,  // [NI] token-index slot written
-    B_IEMPTY = 22, // [NI] token-index slot read
-    NUM_BARS = 26
+    B_IFULL = 18,       // [NI] token-index slot written
+    B_IEMPTY = 18 + NI, // [NI] token-index slot read by the gather and the key warps
+    NUM_BARS = 18 + 2 * NI
 };
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM = OFF_TMEM + 16 + 1024;
@@ -149,22 +157,6 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 }
 
 __device__ __forceinline__ int row_tiles(int cnt) { return (cnt * BLK + TILE - 1) / TILE; }
-
-// Token of key slot `key` (0..127) in tile `t` of row i, or -1 if masked.
-// Flags ids outside 0 .. p/4.
-__device__ __forceinline__ int key_token(const Params& P, int i, int cnt, int t, int key,
-                                         bool flag) {
-    const int li = t * (TILE / BLK) + key / BLK;
-    if (li >= cnt) return -1;
-    const int p = P.ctx_len - P.rows + i;
-    const int b = __ldg(P.sel_idx + (size_t)i * P.max_sel + li);
-    if (b < 0 || b > p / BLK) {
-        if (flag && (key & (BLK - 1)) == 0) atomicOr(P.err, kErrBadBlockId);
-        return -1;
-    }
-    const int tok = b * BLK + (key & (BLK - 1));
-    return tok <= p ? tok : -1;
-}
 
 // Two E4M3 codes (low 16 bits of v, low byte first) -> fp16x2 (low half first).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
@@ -218,7 +210,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         mbar_init(bar(B_GROUP), 128);
         for (int b = 0; b < NI; ++b) {
             mbar_init(bar(B_IFULL + b), 32);
-            mbar_init(bar(B_IEMPTY + b), 128);
+            mbar_init(bar(B_IEMPTY + b), 256);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -515,7 +507,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             for (int c = 0; c < NP; ++c) lpart[c] = 0.f;
             for (int t = 0; t < nt; ++t, ++g) {
                 const int b = g & 1;
-                const bool masked = key_token(P, i, cnt, t, k, false) < 0;
+                bool masked;
+                {
+                    // The index warp's verdict on this key (-1: masked).
+                    const int slot = (int)(g % NI);
+                    ok = mbar_wait(bar(B_IFULL + slot), (g / NI) & 1, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    masked = reinterpret_cast<const int*>(gbase + OFF_IDX)[slot * TILE + k] < 0;
+                    mbar_arrive(bar(B_IEMPTY + slot));
+                }
                 ok = mbar_wait(bar(B_SFULL + b), (g >> 1) & 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -656,43 +657,83 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     if (warp == 9) {
         // ------------------------------------------------------------ token index
         // Same walk as the gather warps (rows of this CTA, tiles of each
-        // non-empty row); each lane resolves 4 of a tile's 128 keys: selected
-        // id -> token (clamped to the row, flagging bad ids) -> physical page
-        // (flagging bad pages) -> cache token row, or -1 for a masked key.
+        // non-empty row).  Lane l resolves selected position 32 t + l of the
+        // row, i.e. keys 4 l .. 4 l + 3 of tile t: id -> set membership ->
+        // physical page -> cache token rows, -1 for masked keys (past the
+        // list, a bad id, a repeat, or past the row's position).
         int* idx = reinterpret_cast<int*>(gbase + OFF_IDX);
+        uint32_t* seen = reinterpret_cast<uint32_t*>(gbase + OFF_SEEN);
         const int lp = P.log2_page, pmask = (1 << P.log2_page) - 1;
         uint32_t g = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
             const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
             const int nt = row_tiles(cnt);
+            if (nt == 0) continue;
+            const int p = P.ctx_len - P.rows + i;
+            const int own = p / BLK;                     // the row's own block
+            const bool exact = own < SEEN_BITS;          // bit = id, no collisions
+            const int32_t* sel = P.sel_idx + (size_t)i * P.max_sel;
+            for (int w = lane; w < SEEN_BITS / 32; w += 32) seen[w] = 0u;
+            __syncwarp();
             for (int t = 0; t < nt; ++t, ++g) {
                 const int slot = (int)(g % NI);
                 if (!mbar_wait(bar(B_IEMPTY + slot), ((g / NI) & 1) ^ 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
-                int tok[TILE / 32];
-#pragma unroll
-                for (int kk = 0; kk < TILE / 32; ++kk)
-                    tok[kk] = key_token(P, i, cnt, t, kk * 32 + lane, true);
-                int pg[TILE / 32];
-#pragma unroll
-                for (int kk = 0; kk < TILE / 32; ++kk)
-                    pg[kk] = tok[kk] >= 0 ? __ldg(P.table + (tok[kk] >> lp)) : 0;
-#pragma unroll
-                for (int kk = 0; kk < TILE / 32; ++kk) {
-                    int r = -1;
-                    if (tok[kk] >= 0) {
-                        int p = pg[kk];
-                        if (p < 0 || p >= P.num_pages) {
-                            atomicOr(P.err, kErrBadPageId);
-                            p = 0;
-                        }
-                        r = (p << lp) + (tok[kk] & pmask);
-                    }
-                    idx[slot * TILE + kk * 32 + lane] = r;
+                const int li = t * (TILE / BLK) + lane;
+                int b = -1;
+                bool valid = false;
+                if (li < cnt) {
+                    b = __ldg(sel + li);
+                    valid = b >= 0 && b <= own;
                 }
+                const unsigned bad = __ballot_sync(0xffffffffu, li < cnt && !valid);
+                if (bad && lane == 0) atomicOr(P.err, kErrBadBlockId);
+                // A repeat within this tile: a lower lane holds the same id.
+                const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+                bool dup = false;
+                if (valid) {
+                    const unsigned same = __match_any_sync(vmask, b);
+                    dup = (same & ((1u << lane) - 1u)) != 0u;
+                }
+                // A repeat of an earlier tile: the id's bit is set (exact), or
+                // its hash bit is set and an earlier position holds it.
+                const uint32_t h = (uint32_t)b & (uint32_t)(SEEN_BITS - 1);
+                bool cand = valid && !dup && ((seen[h >> 5] >> (h & 31u)) & 1u);
+                if (cand && exact) {
+                    dup = true;
+                    cand = false;
+                }
+                unsigned cm = __ballot_sync(0xffffffffu, cand);
+                while (cm) {
+                    const int src = __ffs(cm) - 1;
+                    cm &= cm - 1u;
+                    const int bb = __shfl_sync(0xffffffffu, b, src);
+                    bool found = false;
+                    for (int j0 = 0; j0 < t * (TILE / BLK) && !found; j0 += 32)
+                        found = __any_sync(0xffffffffu, __ldg(sel + j0 + lane) == bb);
+                    if (lane == src) dup = found;
+                }
+                __syncwarp();
+                if (valid && !dup) atomicOr(seen + (h >> 5), 1u << (h & 31u));
+                if (__ballot_sync(0xffffffffu, dup) && lane == 0) atomicOr(P.err, kErrDupBlockId);
+                const bool use = valid && !dup;
+                const int tok0 = b * BLK;
+                int pg = use ? __ldg(P.table + (tok0 >> lp)) : 0;   // a block never straddles a page
+                if (use && (pg < 0 || pg >= P.num_pages)) {
+                    atomicOr(P.err, kErrBadPageId);
+                    pg = 0;
+                }
+                const int r0 = (pg << lp) + (tok0 & pmask);
+                int4 r;
+                r.x = (use && tok0 + 0 <= p) ? r0 + 0 : -1;
+                r.y = (use && tok0 + 1 <= p) ? r0 + 1 : -1;
+                r.z = (use && tok0 + 2 <= p) ? r0 + 2 : -1;
+                r.w = (use && tok0 + 3 <= p) ? r0 + 3 : -1;
+                reinterpret_cast<int4*>(idx + slot * TILE)[lane] = r;
+                __syncwarp();   // the set's bits are read by every lane in the next tile
                 mbar_arrive(bar(B_IFULL + slot));
             }
         }

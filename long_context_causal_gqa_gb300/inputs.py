@@ -286,3 +286,66 @@ def sparse_e4m3_inputs(rows: int, ctx_len: int, tokens: int, seed: int = 0, page
     sel, cnt, max_sel = sparse_selection(rows, ctx_len, tokens, seed * 11 + 4)
     return SparseE4M3Inputs(q, caches[0], caches[1], scales[0], scales[1], table, sel, cnt,
                             max_sel, ctx_len, rows, page, Hq, Hkv, D, scale)
+
+
+def paged_e4m3_from_values(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, capacity: int,
+                           seed: int = 0, page: int = PAGE,
+                           scale: float = SCALE) -> PagedE4M3Inputs:
+    """Paged E4M3 tail inputs laid out from given values: q [R, Hq, D] fp16,
+    k / v [ctx_len, Hkv, D] real values, each tensor encoded as E4M3 with one
+    scale (absmax / 448) and stored in page-``page`` blocks under a seeded
+    permuted block table; unnamed pages and slots past ctx_len hold the poison
+    byte.  Used for structured inputs (ramps, dominant keys, constant values)."""
+    ctx_len, Hkv, D = k.shape
+    R, Hq, _ = q.shape
+    assert capacity % page == 0 and ctx_len <= capacity and 1 <= R <= ctx_len
+    num_pages = capacity // page
+    n_logical = (ctx_len + page - 1) // page
+    table = permuted_block_table(n_logical, num_pages, seed * 5 + 3)
+    caches, scales = [], []
+    for x in (k, v):
+        b, sc = e4m3_encode(x.to(torch.float32))
+        cache = torch.full((num_pages, page, Hkv, D), E4M3_POISON, dtype=torch.uint8)
+        padded = torch.full((n_logical * page, Hkv, D), E4M3_POISON, dtype=torch.uint8)
+        padded[:ctx_len] = b
+        cache[table.long()] = padded.view(n_logical, page, Hkv, D)
+        caches.append(cache)
+        scales.append(sc)
+    return PagedE4M3Inputs(q.to(torch.float16).contiguous(), caches[0], caches[1], scales[0],
+                           scales[1], table, ctx_len, R, page, Hq, Hkv, D, scale)
+
+
+def sparse_from_values(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, tokens: int,
+                       seed: int = 0, page: int = PAGE, scale: float = SCALE,
+                       e4m3: bool = False):
+    """Selected-block sparse inputs laid out from given values: q [rows, Hq, D],
+    k / v [ctx_len, Hkv, D]; an fp16 cache (or, with e4m3, E4M3 codes with one
+    scale per tensor) in a seeded permuted page table, NaN / poison past
+    ctx_len and in unnamed pages, and seeded selections as ``sparse_inputs``."""
+    ctx_len, Hkv, D = k.shape
+    rows, Hq, _ = q.shape
+    assert 1 <= rows <= ctx_len
+    n_logical = (ctx_len + page - 1) // page
+    num_pages = n_logical
+    table = permuted_block_table(n_logical, num_pages, seed * 7 + 3)
+    caches, scales = [], []
+    for x in (k, v):
+        if e4m3:
+            b, sc = e4m3_encode(x.to(torch.float32))
+            padded = torch.full((n_logical * page, Hkv, D), E4M3_POISON, dtype=torch.uint8)
+            padded[:ctx_len] = b
+            cache = torch.full((num_pages, page, Hkv, D), E4M3_POISON, dtype=torch.uint8)
+            scales.append(sc)
+        else:
+            padded = torch.full((n_logical * page, Hkv, D), float("nan"), dtype=torch.float16)
+            padded[:ctx_len] = x.to(torch.float16)
+            cache = torch.full((num_pages, page, Hkv, D), float("nan"), dtype=torch.float16)
+        cache[table.long()] = padded.view(n_logical, page, Hkv, D)
+        caches.append(cache)
+    sel, cnt, max_sel = sparse_selection(rows, ctx_len, tokens, seed * 7 + 4)
+    qh = q.to(torch.float16).contiguous()
+    if e4m3:
+        return SparseE4M3Inputs(qh, caches[0], caches[1], scales[0], scales[1], table, sel, cnt,
+                                max_sel, ctx_len, rows, page, Hq, Hkv, D, scale)
+    return SparseInputs(qh, caches[0], caches[1], table, sel, cnt, max_sel, ctx_len, rows, page,
+                        Hq, Hkv, D, scale)

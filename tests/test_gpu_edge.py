@@ -1,0 +1,287 @@
+"""GPU parity on inputs that reach the online softmax's edge paths.
+
+The seeded N(0,1) workloads of the other parity tests keep every score within
+a few log2 units of its row maximum, so the branch that moves a row's
+reference maximum and rescales O in tensor memory, and the smallest
+probabilities, are never exercised there.  These inputs are built to reach
+them, for all four kernels (dense prefill, paged E4M3 tail, selected-block
+sparse over an fp16 and over an E4M3 cache):
+
+  ramp      scores that rise by 10 log2 units per 128 keys (more than the
+            rescale threshold) in runs of 8 tiles, so the reference moves
+            (and O is rescaled) on most tiles, while every score stays
+            within ~100 log2 units;
+  dominant  one key per row far above the rest, the rest 12..24 log2 units
+            below it, up to the full context;
+  constant  V equal to one constant: the output is that constant for any
+            weights;
+  same_k    every key identical: the output is the mean of the visible V rows;
+  outlier   query rows with one element 10^3 times the others;
+  scale1    the score scale 1 instead of 1/16 (scores spread over ~100 log2
+            units).
+
+Every case is compared element by element with the FP64 oracle within the
+pages' FP16 envelope, max abs <= 1e-3 and rel L2 <= 1e-2 ("[Kernel][SM70]
+Default long-prefill GQA architecture", Test Result); the invariants the
+oracle itself is pinned to (constant V, identical keys) are also checked
+against their closed forms.  Values are kept within |v| <= 2 so that the fp16
+output's own rounding stays inside the envelope.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_causal_gqa_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+LOG2E = 1.4426950408889634
+KINDS = ["ramp", "dominant", "constant", "same_k", "outlier", "scale1"]
+SEEDS = {k: 101 + 17 * i for i, k in enumerate(KINDS)}
+
+
+def _check(got, ref, what):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all(), what
+    err = np.abs(g - ref).max()
+    rel = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert err <= 1e-3 and rel <= 1e-2, f"{what}: max abs {err:.3e} rel L2 {rel:.3e}"
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def _alphas(Hq):
+    # q = alpha_h * ones(D): a different score slope per head
+    return [1.0 + 0.1 * h for h in range(Hq)]
+
+
+def _keys_for_scores(s, D, scale, seed, noise=0.3):
+    """Keys whose dot with ones(D), times scale * log2(e), is about s (log2
+    units) plus a zero-mean spread of ~noise * 16 * scale * log2(e)."""
+    s = torch.as_tensor(s, dtype=torch.float64)
+    base = s / (D * scale * LOG2E)
+    k = base[:, None] + noise * torch.randn(len(s), D, generator=_gen(seed), dtype=torch.float64)
+    return k.view(len(s), 1, D)
+
+
+def _values(n, D, seed, kind):
+    if kind == "constant":
+        return torch.full((n, 1, D), 0.75, dtype=torch.float64)
+    return (torch.rand(n, 1, D, generator=_gen(seed), dtype=torch.float64) * 4.0 - 2.0)
+
+
+def structured(kind, rows, n, D=256, Hq=6, seed=0, dominant_at=None, dominant_rows_tail=False):
+    """(q [rows, Hq, D], k [n, 1, D], v [n, 1, D], scale) as float64 tensors.
+
+    Positions are absolute key indices; query row i sits at n - rows + i."""
+    scale = 1.0 / 16
+    g = _gen(seed)
+    ones_q = torch.tensor(_alphas(Hq), dtype=torch.float64)[None, :, None].expand(rows, Hq, D)
+    if kind == "ramp":
+        q = ones_q.clone()
+        j = torch.arange(n, dtype=torch.float64)
+        s = 10.0 * (torch.floor(j / 128) % 8) + 10.0 * (j % 128) / 128
+        k = _keys_for_scores(s, D, scale, seed + 1)
+    elif kind in ("dominant", "constant"):
+        q = ones_q.clone()
+        s = 8.0 - (12.0 + 12.0 * torch.rand(n, generator=g, dtype=torch.float64))
+        if dominant_rows_tail:
+            s[n - rows:] = 8.0            # every row's own position dominates
+        else:
+            s[dominant_at if dominant_at is not None else 5] = 8.0
+        k = _keys_for_scores(s, D, scale, seed + 1)
+    elif kind == "same_k":
+        q = torch.randn(rows, Hq, D, generator=g, dtype=torch.float64)
+        k = torch.randn(1, 1, D, generator=g, dtype=torch.float64).expand(n, 1, D).clone()
+    elif kind == "outlier":
+        q = torch.randn(rows, Hq, D, generator=g, dtype=torch.float64)
+        for i in range(rows):
+            for h in range(Hq):
+                q[i, h, (37 * h + 11 * i) % D] = 1000.0 * (1 if (i + h) % 2 == 0 else -1)
+        k = torch.randn(n, 1, D, generator=g, dtype=torch.float64)
+    elif kind == "scale1":
+        scale = 1.0
+        q = torch.randn(rows, Hq, D, generator=g, dtype=torch.float64)
+        k = torch.randn(n, 1, D, generator=g, dtype=torch.float64)
+    else:
+        raise ValueError(kind)
+    v = _values(n, D, seed + 2, kind)
+    return q, k, v, scale
+
+
+def _closed_forms(kind, got, v_real, rows, n):
+    """Closed forms the output must also meet: V = c gives c; identical keys
+    give the mean of the row's visible V (rows see keys 0 .. n - rows + i)."""
+    g = got.float().cpu().numpy().astype(np.float64)
+    if kind == "constant":
+        c = float(v_real.reshape(-1)[0])
+        assert np.abs(g - c).max() <= 1e-3
+    elif kind == "same_k":
+        vv = v_real.reshape(n, -1)
+        cs = np.cumsum(vv, axis=0)
+        for i in range(0, rows, max(1, rows // 7)):
+            last = n - rows + i
+            mean = cs[last] / (last + 1)
+            assert np.abs(g[i] - mean[None, :]).max() <= 1e-3
+
+
+# ------------------------------------------------------------------ dense prefill
+@pytest.mark.parametrize("kind", KINDS)
+def test_prefill_edge_cases(cuda_lib, kind):
+    Q, KV = 300, 2100
+    q, k, v, scale = structured(kind, Q, KV, seed=SEEDS[kind])
+    qh, kh, vh = q.half(), k.half(), v.half()
+    dev = torch.device("cuda")
+    out = cuda_lib.prefill(qh.to(dev), kh.to(dev), vh.to(dev), scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    ref = oracle.dense(qh, kh, vh, scale)
+    _check(out, ref, f"prefill {kind}")
+    _closed_forms(kind, out, vh.double().numpy(), Q, KV)
+
+
+@pytest.mark.parametrize("kind", ["dominant", "constant"])
+def test_prefill_dominant_key_full_context(cuda_lib, kind):
+    """One dominant key (visible to every row) and 127999 keys 12..24 log2
+    units below it at Q=8000, KV=128000; sampled rows against the oracle."""
+    Q, KV = 8000, 128000
+    q, k, v, scale = structured(kind, Q, KV, seed=7, dominant_at=100)
+    qh, kh, vh = q.half(), k.half(), v.half()
+    dev = torch.device("cuda")
+    out = cuda_lib.prefill(qh.to(dev), kh.to(dev), vh.to(dev), scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    rows = np.array([0, 1, 20, 21, 255, 256, 4000, 7998, 7999], dtype=np.int32)
+    ref = oracle.dense(qh, kh, vh, scale, rows=rows)
+    _check(out[torch.as_tensor(rows, dtype=torch.long)], ref, f"prefill full {kind}")
+
+
+def test_prefill_changed_future_keys_match_oracle_on_every_row(cuda_lib):
+    """Keys past row 0's last visible key replaced by large constant keys that
+    later rows see (their scores reach tens of log2 units above the rest, so the
+    reference moves and O is rescaled): row 0 stays bit-identical and every row
+    matches the oracle."""
+    dev = torch.device("cuda")
+    d = inputs.dense_inputs(200, 700, seed=5)
+    base = cuda_lib.prefill(d.q.to(dev), d.k.to(dev), d.v.to(dev), d.scale)
+    k2, v2 = d.k.clone(), d.v.clone()
+    k2[700 - 200 + 1:] = 4.0
+    v2[700 - 200 + 1:] = (torch.rand(199, 1, 256, generator=_gen(3)) * 2 - 1).half()
+    out = cuda_lib.prefill(d.q.to(dev), k2.to(dev), v2.to(dev), d.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    assert torch.equal(out[0].view(torch.int16), base[0].view(torch.int16))
+    ref = oracle.dense(d.q, k2, v2, d.scale)
+    _check(out, ref, "prefill changed future keys")
+
+
+# ------------------------------------------------------------------ paged E4M3 tail
+def _run_paged(lib, p):
+    dev = torch.device("cuda")
+    ks = torch.tensor([p.kscale], dtype=torch.float32, device=dev)
+    vs = torch.tensor([p.vscale], dtype=torch.float32, device=dev)
+    out = lib.paged_e4m3(p.q.to(dev), p.kcache.to(dev), p.vcache.to(dev), ks, vs,
+                         p.block_table.to(dev), p.ctx_len, p.scale)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    return out
+
+
+def _paged_ref(p):
+    return oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                             p.ctx_len, p.scale)
+
+
+def _decoded_v(p):
+    n_log = (p.ctx_len + p.page - 1) // p.page
+    codes = p.vcache[p.block_table[:n_log].long()].reshape(-1, p.Hkv, p.D)[: p.ctx_len]
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy() * p.vscale
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("R", [1, 8])
+def test_paged_edge_cases(cuda_lib, kind, R):
+    # 40000 keys: 313 tiles, so every split of the key range holds two or
+    # three tiles and the reference can move inside a split.
+    ctx = 40000
+    q, k, v, scale = structured(kind, R, ctx, seed=R + SEEDS[kind])
+    p = inputs.paged_e4m3_from_values(q.half(), k, v, capacity=40960, seed=R, scale=scale)
+    out = _run_paged(cuda_lib, p)
+    _check(out, _paged_ref(p), f"paged {kind} R={R}")
+    _closed_forms(kind, out, _decoded_v(p), R, ctx)
+
+
+@pytest.mark.parametrize("kind", ["dominant", "constant"])
+@pytest.mark.parametrize("R", [1, 8])
+def test_paged_dominant_key_full_context(cuda_lib, kind, R):
+    """One dominant key and 261887 keys 12..24 log2 units below it at the
+    pages' tail context (261888 of 262144): the small probabilities, which the
+    E4M3 expansion of P must keep, carry most of the mass."""
+    ctx = 261888
+    q, k, v, scale = structured(kind, R, ctx, seed=11 + R, dominant_at=123457)
+    p = inputs.paged_e4m3_from_values(q.half(), k, v, capacity=262144, seed=R, scale=scale)
+    out = _run_paged(cuda_lib, p)
+    _check(out, _paged_ref(p), f"paged full {kind} R={R}")
+    _closed_forms(kind, out, _decoded_v(p), R, ctx)
+
+
+# ------------------------------------------------------------------ sparse
+def _run_sparse(lib, s, e4m3):
+    dev = torch.device("cuda")
+    args = [s.q.to(dev), s.kcache.to(dev), s.vcache.to(dev)]
+    if e4m3:
+        args += [torch.tensor([s.kscale], dtype=torch.float32, device=dev),
+                 torch.tensor([s.vscale], dtype=torch.float32, device=dev)]
+    args += [s.block_table.to(dev), s.sel_idx.to(dev), s.sel_cnt.to(dev), s.ctx_len, s.scale]
+    out = (lib.sparse_blocks_e4m3 if e4m3 else lib.sparse_blocks)(*args)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    return out
+
+
+def _sparse_ref(s, e4m3, rows=None):
+    if e4m3:
+        return oracle.sparse_blocks_e4m3(s.q, s.kcache, s.vcache, s.kscale, s.vscale,
+                                         s.block_table, s.sel_idx, s.sel_cnt, s.ctx_len, s.scale,
+                                         rows=rows)
+    return oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
+                                s.ctx_len, s.scale, rows=rows)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("e4m3", [False, True])
+def test_sparse_edge_cases(cuda_lib, kind, e4m3):
+    rows, ctx, T = 200, 4096, 512
+    q, k, v, scale = structured(kind, rows, ctx, seed=SEEDS[kind] + e4m3, dominant_rows_tail=True)
+    s = inputs.sparse_from_values(q.half(), k if e4m3 else k.half(), v if e4m3 else v.half(),
+                                  tokens=T, seed=3, scale=scale, e4m3=e4m3)
+    out = _run_sparse(cuda_lib, s, e4m3)
+    _check(out, _sparse_ref(s, e4m3), f"sparse {'e4m3' if e4m3 else 'fp16'} {kind}")
+    if kind == "constant":
+        # every live value is the same code (or fp16 number): the output is it
+        live = s.vcache[s.block_table[0].long(), 0, 0, 0:1]
+        c = (live.view(torch.float8_e4m3fn).double() * s.vscale if e4m3 else live.double())
+        _closed_forms(kind, out, c.numpy(), rows, ctx)
+
+
+@pytest.mark.parametrize("kind", ["dominant", "constant"])
+@pytest.mark.parametrize("e4m3", [False, True])
+def test_sparse_dominant_keys_full_size(cuda_lib, kind, e4m3):
+    """4096 rows at the end of a 32768-token cache, 2048 selected tokens per
+    row: every row's own position dominates, the other selected tokens are
+    12..24 log2 units below; sampled rows against the oracle."""
+    rows, ctx, T = 4096, 32768, 2048
+    q, k, v, scale = structured(kind, rows, ctx, seed=21 + e4m3, dominant_rows_tail=True)
+    s = inputs.sparse_from_values(q.half(), k if e4m3 else k.half(), v if e4m3 else v.half(),
+                                  tokens=T, seed=5, scale=scale, e4m3=e4m3)
+    out = _run_sparse(cuda_lib, s, e4m3)
+    sample = np.array([0, 1, 2, 3, 777, 2048, 4093, 4094, 4095], dtype=np.int32)
+    ref = _sparse_ref(s, e4m3, rows=sample)
+    _check(out[torch.as_tensor(sample, dtype=torch.long)], ref,
+           f"sparse full {'e4m3' if e4m3 else 'fp16'} {kind}")

@@ -176,3 +176,60 @@ def test_sparse_other_page_sizes(cuda_lib, page):
     ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
                                s.ctx_len, s.scale)
     _check(out, ref, f"page={page}")
+
+
+def _with_duplicates(sel, cnt, seed, extra=8):
+    """Each row's ids shuffled, then `extra` copies of randomly chosen ids of
+    the row inserted at random positions (repeats within one 32-block tile
+    and across tiles)."""
+    g = torch.Generator().manual_seed(seed)
+    rows = sel.shape[0]
+    out = torch.full((rows, sel.shape[1] + extra), -1, dtype=torch.int32)
+    cnt2 = cnt.clone()
+    for i in range(rows):
+        c = int(cnt[i])
+        ids = sel[i, :c][torch.randperm(c, generator=g)]
+        dups = ids[torch.randint(0, c, (extra,), generator=g)]
+        allv = torch.cat([ids, dups])[torch.randperm(c + extra, generator=g)]
+        out[i, : c + extra] = allv
+        cnt2[i] = c + extra
+    return out, cnt2
+
+
+@pytest.mark.parametrize("ctx,e4m3", [(4096, False), (4096, True), (70000, False)])
+def test_sparse_duplicate_ids_are_masked_and_flagged(cuda_lib, ctx, e4m3):
+    """Selection has set semantics ("[Kernel][SM70] Repair #378 on latest
+    main", Changes: stale or repeated entries are masked, not attended): a
+    repeated id selects nothing more and sets GQA_DEVERR_DUP_BLOCK_ID.  Rows
+    are shuffled and given repeats; the result equals the oracle's (which
+    builds each row's visible set) and the error bit is set.  At ctx 70000
+    the later rows' block ids exceed the kernel's exact 16384-bit set, so its
+    hashed set with confirmation is exercised."""
+    rows, T = 300, 512
+    mk = inputs.sparse_e4m3_inputs if e4m3 else inputs.sparse_inputs
+    s = mk(rows=rows, ctx_len=ctx, tokens=T, seed=31 + e4m3)
+    sel, cnt = _with_duplicates(s.sel_idx, s.sel_cnt, seed=ctx + e4m3)
+    dev = torch.device("cuda")
+    if e4m3:
+        ks = torch.tensor([s.kscale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([s.vscale], dtype=torch.float32, device=dev)
+        out = cuda_lib.sparse_blocks_e4m3(s.q.to(dev), s.kcache.to(dev), s.vcache.to(dev), ks, vs,
+                                          s.block_table.to(dev), sel.to(dev), cnt.to(dev),
+                                          s.ctx_len, s.scale)
+        ref = oracle.sparse_blocks_e4m3(s.q, s.kcache, s.vcache, s.kscale, s.vscale,
+                                        s.block_table, sel, cnt, s.ctx_len, s.scale)
+    else:
+        out = _run(cuda_lib, s, sel, cnt)
+        ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, sel, cnt, s.ctx_len,
+                                   s.scale)
+    torch.cuda.synchronize()
+    err = cuda_lib.device_error()
+    assert err & cuda_lib.DEVERR_DUP_BLOCK_ID
+    assert not err & cuda_lib.DEVERR_BAD_BLOCK_ID
+    _check(out, ref, f"duplicates ctx={ctx} e4m3={e4m3}")
+    # Without repeats, shuffled ids give the same result within rounding and no error.
+    sel1, cnt1 = _with_duplicates(s.sel_idx, s.sel_cnt, seed=7, extra=0)
+    if not e4m3:
+        out1 = _run(cuda_lib, s, sel1, cnt1)
+        assert cuda_lib.device_error() == 0
+        _check(out1, ref, "shuffled ids")
