@@ -719,11 +719,16 @@ def run_case(args):
         line = {"case": f"paged E4M3 batch of {len(ctxs)} tails R=2 ({sum(ctxs)} tokens)",
                 "us": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                 "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
-    elif args.case == "paged":
-        t, nbytes, fl = bench_paged(binding, args.rows, device, args.steps, args.warmup, flush)
+    elif args.case in ("paged", "paged_layers"):
+        if args.case == "paged":
+            t, nbytes, fl = bench_paged(binding, args.rows, device, args.steps, args.warmup, flush)
+        else:
+            t, nbytes = bench_paged_layers(binding, args.rows, device, args.steps, args.warmup,
+                                           flush)
         us = statistics.median(t) * 1e3
-        line = {"case": f"paged E4M3 tail R={args.rows} ctx=261888", "us": round(us, 2),
-                "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+        line = {"case": f"paged E4M3 tail R={args.rows} ctx=261888"
+                        + (", 4 calls back to back, per call" if args.case != "paged" else ""),
+                "us": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                 "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
     else:
         e4m3 = args.case == "sparse_e4m3"
@@ -790,7 +795,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--case", default="headline", choices=["headline", "prefill", "paged",
-                                                           "paged_batch",
+                                                           "paged_layers", "paged_batch",
                                                            "sparse", "sparse_e4m3"],
                     help="run one secondary workload alone (profiling)")
     ap.add_argument("--rows", type=int, default=8, help="--case paged: tail rows")
