@@ -103,11 +103,7 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
  *   query_rows <= ctx_len <= num_pages * page.
  * Tail row r sits at position ctx_len - query_rows + r.  The key range is
  * split over all SMs; each split's (O, m, l) partial goes to the workspace
- * and the same kernel merges them in a fixed order after a grid-wide barrier
- * (one cooperative launch per KV head, its CTAs resident together; the
- * barrier's two words live in the workspace's counter area).  If the device
- * cannot hold the whole grid at once, a second kernel on the same stream does
- * the merge instead. */
+ * and a second kernel on the same stream merges them in a fixed order. */
 int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                         const float* kscale, const float* vscale, const int32_t* block_table,
                         int num_pages, int page, int ctx_len, int query_rows, int Hq, int Hkv,
@@ -169,19 +165,17 @@ int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_
  * arguments, layouts and error codes as gqa_attn_paged_e4m3 and computes the
  * same result (bitwise equal on devices with at most 160 SMs), but needs no
  * registered workspace: its split partials live in a static device array
- * inside the library, 256 bytes plus at most 160 splits x 48 packed rows x
- * 258 floats (about 7.9 MB), which every GPU that loads the library holds until the
+ * inside the library, at most 160 splits x 48 packed rows x 258 floats
+ * (about 7.9 MB), which every GPU that loads the library holds until the
  * process exits.  It never calls cudaMalloc, cudaFree or any allocating
  * routine.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
  *   - All calls on a device share the one array, which keeps the last call's
- *     contents.  Its first 256 bytes hold the words of the kernel's grid-wide
- *     barrier, which are zero when the library is loaded and which every call
- *     leaves at zero; the partials after them need no clearing, since a call
- *     writes every partial it reads.  Calls that overlap on the GPU (e.g. on
- *     two streams without ordering) race on the array and give wrong results.
+ *     contents.  Nothing in it has to start at zero: a call writes every
+ *     partial it reads.  Calls that overlap on the GPU (e.g. on two streams
+ *     without ordering) race on the array and give wrong results.
  *   - query_rows * Hq / Hkv > 48 returns GQA_ERR_UNSUPPORTED; a shape whose
  *     partials would not fit the array returns GQA_ERR_WORKSPACE. */
 int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,

@@ -12,14 +12,9 @@
 // here the work is HBM-bound (one byte per K/V element) and shaped for sm_103a:
 //
 // * Split-KV: the context is cut into 128-key tiles (8 pages) and the tiles
-//   into one contiguous range per SM.  Each split writes an (O, m, l) partial
-//   and the partials are combined by an exact log-sum-exp merge in a fixed
-//   order.  For one sequence the merge runs in the same kernel: the grid (one
-//   CTA per SM, launched cooperatively so all are resident) meets at a
-//   grid-wide barrier once every partial is written, then every warp of every
-//   CTA merges a share of the (row, 4 d) outputs.  Batches of sequences, whose
-//   split count can exceed the SM count, use a separate merge kernel launched
-//   as a programmatic dependent.
+//   into one contiguous range per SM.  Each split writes an (O, m, l) partial;
+//   a merge kernel, launched as a programmatic dependent so that its launch
+//   overlaps this kernel's tail, combines them (exact log-sum-exp merge).
 // * Swap-AB UMMA on the FP8 tensor cores (kind::f8f6f4, K = 32 per
 //   instruction): keys are the M=128 dimension, the packed query rows the N
 //   dimension (NP = 16/32/48).  K and V enter as the raw E4M3 bytes the TMA
@@ -59,7 +54,6 @@
 // Warp roles (64 + 128 NWG threads): 0 TMA producer, 1 TMEM owner + UMMA
 // issuer, then NWG = 2 / 4 / 6 softmax warpgroups for 16 / 32 / 48 packed
 // rows, each owning 8 of them (thread = TMEM lane = key).
-#include <atomic>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -103,7 +97,6 @@ struct Params {
     float* ws_ml;   // [G][nq][2]  (m in log2 units, l)
     __half* out;
     unsigned* err;
-    unsigned* gbar;  // grid barrier words (arrivals, generation), zero between launches
 };
 
 // Element offset of packed row r of sequence seq in q / out.  Packed row r is
@@ -386,127 +379,7 @@ __device__ void seq_splits(const Params& P, int b, int& first, int& count) {
     first = count = 0;
 }
 
-// Grid-wide barrier of a cooperative launch: thread 0 of each CTA arrives on
-// gbar[0]; the last arrival resets it to zero and advances the generation
-// gbar[1], which the others wait for (bounded: after kWaitTimeoutNs the wait
-// flags kErrWaitTimeout and gives up).  The usual fence / __syncthreads
-// pattern makes every CTA's earlier global writes visible to every CTA after
-// the barrier.  Returns false if the wait gave up.
-__device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned nblocks, unsigned* err,
-                                             volatile int* result) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        volatile unsigned* gen = gbar + 1;
-        const unsigned g0 = *gen;
-        __threadfence();
-        int ok = 1;
-        if (atomicAdd(gbar, 1u) == nblocks - 1) {
-            atomicExch(gbar, 0u);
-            __threadfence();
-            atomicAdd(gbar + 1, 1u);
-        } else {
-            const uint64_t t0 = global_timer_ns();
-            while (*gen == g0) {
-                __nanosleep(32);
-                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                    atomicOr(err, kErrWaitTimeout);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        __threadfence();
-        *result = ok;
-    }
-    __syncthreads();
-    return *result != 0;
-}
-
-// The merge of one sequence's G split partials, shared by the whole grid:
-// unit u = (packed row c, d = 4 (u mod 64) .. + 3) goes to warp u of the grid
-// (strided); lane l takes the splits l, l + 32, ...; the lanes' sums are
-// combined by a fixed butterfly, so the result does not depend on timing.
-//   out[c, d] = vscale * sum_s w_s O_s[c, d] / sum_s w_s l_s,  w_s = 2^(m_s - M).
-// A zero weight (a split that saw no visible key, or none at all) skips its O,
-// which may hold anything.
-template <int NTHREADS>
-__device__ void grid_merge(const Params& P) {
-    constexpr int NW = NTHREADS / 32;
-    constexpr int PER = 5;   // splits per lane kept in registers (G <= 160)
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = P.G;
-    const float vs = *P.vscale;
-    const int units = P.nq * (D / 4);
-    for (int u = blockIdx.x * NW + warp; u < units; u += gridDim.x * NW) {
-        const int c = u / (D / 4);
-        const int d0 = (u - c * (D / 4)) * 4;
-        auto ml_at = [&](int s) {
-            return __ldcg(reinterpret_cast<const float2*>(P.ws_ml + ((size_t)s * P.nq + c) * 2));
-        };
-        auto o_at = [&](int s) {
-            return __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)s * P.nq + c) * D + d0));
-        };
-        float M = -INFINITY, L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        auto add = [&](float w, const float2& m, const float4& o) {
-            if (w != 0.f) {
-                L = fmaf(w, m.y, L);
-                acc.x = fmaf(w, o.x, acc.x);
-                acc.y = fmaf(w, o.y, acc.y);
-                acc.z = fmaf(w, o.z, acc.z);
-                acc.w = fmaf(w, o.w, acc.w);
-            }
-        };
-        if (G <= 32 * PER) {
-            // One round of loads: every split's (m, l) and O of this unit.
-            float2 ml[PER];
-            float4 o[PER];
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int s = lane + 32 * i;
-                ml[i] = s < G ? ml_at(s) : make_float2(-INFINITY, 0.f);
-                o[i] = s < G ? o_at(s) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 0; i < PER; ++i) M = fmaxf(M, ml[i].x);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-#pragma unroll
-            for (int i = 0; i < PER; ++i)
-                add(ml[i].x == -INFINITY ? 0.f : exp2f(ml[i].x - M), ml[i], o[i]);
-        } else {
-            for (int s = lane; s < G; s += 32) M = fmaxf(M, ml_at(s).x);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-            for (int s = lane; s < G; s += 32) {
-                const float2 m = ml_at(s);
-                const float w = m.x == -INFINITY ? 0.f : exp2f(m.x - M);
-                if (w != 0.f) add(w, m, o_at(s));
-            }
-        }
-#pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) {
-            L += __shfl_xor_sync(0xffffffffu, L, o2);
-            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o2);
-            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o2);
-            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o2);
-            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o2);
-        }
-        if (lane == 0) {
-            const float f = L > 0.f ? vs / L : 0.f;
-            const __half2 h01 = __floats2half2_rn(acc.x * f, acc.y * f);
-            const __half2 h23 = __floats2half2_rn(acc.z * f, acc.w * f);
-            uint2 pk;
-            pk.x = *reinterpret_cast<const uint32_t*>(&h01);
-            pk.y = *reinterpret_cast<const uint32_t*>(&h23);
-            *reinterpret_cast<uint2*>(P.out + row_offset(P, 0, c) + d0) = pk;
-        }
-    }
-}
-
-// FUSED (one sequence, cooperative launch): the grid merges its own partials
-// after a grid-wide barrier; otherwise paged_merge_kernel follows.
-template <int NP, int NWG, bool BATCHED, bool FUSED>
+template <int NP, int NWG, bool BATCHED>
 __global__ void __launch_bounds__(threads_for(NWG), 1)
 paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params P) {
@@ -1038,10 +911,6 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    if constexpr (FUSED) {
-        static_assert(!BATCHED, "the fused merge serves one sequence");
-        if (grid_barrier(P.gbar, gridDim.x, P.err, abort_flag + 1)) grid_merge<NTHREADS>(P);
-    }
 }
 
 // out[c, d] = vscale * sum_s w_s O_s[c, d] / sum_s w_s l_s, w_s = 2^(m_s - M).
@@ -1157,61 +1026,15 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     }
 }
 
-// Whether `G` CTAs of the fused single-sequence kernel can all be resident at
-// once on the current device (a cooperative launch needs that); cached per
-// device.
-template <int NP, int NWG>
-bool fused_fits(int G, int device, int num_sms) {
-    static std::atomic<int> cached[64];   // resident CTAs + 1, 0 until known
-    int cap = 0;
-    if (device < 64) cap = cached[device].load(std::memory_order_relaxed) - 1;
-    if (cap < 0) {
-        int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &nb, paged_split_kernel<NP, NWG, false, true>, threads_for(NWG),
-                Layout<NP, NWG>::SMEM) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
-        }
-        cap = nb * num_sms;
-        if (device < 64) cached[device].store(cap + 1, std::memory_order_relaxed);
-    }
-    return G <= cap;
-}
-
 template <int NP, int NWG, bool BATCHED>
 int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
-                int device, int num_sms) {
+                int device) {
     using L = Layout<NP, NWG>;
-    if constexpr (!BATCHED) {
-        // One sequence: split and merge in one cooperative launch when the
-        // grid fits on the device at once (it always does when nothing else
-        // limits residency: G <= SM count, one CTA per SM).
-        if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, false, true>),
-                              L::SMEM) != GQA_OK)
-            return GQA_ERR_CUDA;
-        if (P.gbar && fused_fits<NP, NWG>(P.G, device, num_sms)) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(P.G);
-            cfg.blockDim = dim3(threads_for(NWG));
-            cfg.dynamicSmemBytes = L::SMEM;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeCooperative;
-            attr[0].val.cooperative = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if (cudaLaunchKernelEx(&cfg, paged_split_kernel<NP, NWG, false, true>, tk, tv, P) !=
-                cudaSuccess)
-                return GQA_ERR_CUDA;
-            return GQA_OK;
-        }
-    }
-    if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, BATCHED, false>),
+    (void)device;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, BATCHED>),
                           L::SMEM) != GQA_OK)
         return GQA_ERR_CUDA;
-    paged_split_kernel<NP, NWG, BATCHED, false>
-        <<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
+    paged_split_kernel<NP, NWG, BATCHED><<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.batch * P.nq, D / 128);
@@ -1232,19 +1055,19 @@ int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStr
 // softmax chain is spread over 8, 16 or 24 warps.
 template <int NP, int NWG>
 int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
-              int device, int num_sms) {
+              int device) {
     // One sequence (the common tail) or several (the batched entry point):
     // separate instantiations, so the single-sequence kernel carries none of
     // the batched bookkeeping.
-    return P.batch > 1 ? launch_np_b<NP, NWG, true>(tk, tv, P, stream, device, num_sms)
-                       : launch_np_b<NP, NWG, false>(tk, tv, P, stream, device, num_sms);
+    return P.batch > 1 ? launch_np_b<NP, NWG, true>(tk, tv, P, stream, device)
+                       : launch_np_b<NP, NWG, false>(tk, tv, P, stream, device);
 }
 
 int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
-                 int device, int num_sms) {
-    if (P.nq <= 16) return launch_np<16, 2>(tk, tv, P, stream, device, num_sms);
-    if (P.nq <= 32) return launch_np<32, 4>(tk, tv, P, stream, device, num_sms);
-    return launch_np<48, 6>(tk, tv, P, stream, device, num_sms);
+                 int device) {
+    if (P.nq <= 16) return launch_np<16, 2>(tk, tv, P, stream, device);
+    if (P.nq <= 32) return launch_np<32, 4>(tk, tv, P, stream, device);
+    return launch_np<48, 6>(tk, tv, P, stream, device);
 }
 
 // Grouping fields: Hq query heads per position, Hkv KV heads, each shared by
@@ -1260,7 +1083,7 @@ void set_grouping(Params& P, int Hq, int Hkv) {
 // writes query heads g * grp .. g * grp + grp - 1.  Launches on one stream run
 // in order, so they can share the split partials.
 int launch_heads(Params& P, const void* q, void* out, const uint8_t* kcache,
-                 const uint8_t* vcache, int Hkv, cudaStream_t stream, int device, int num_sms) {
+                 const uint8_t* vcache, int Hkv, cudaStream_t stream, int device) {
     const uint64_t rows = (uint64_t)P.num_pages * P.page;
     const uint32_t box_rows = P.page < TILE ? (uint32_t)P.page : (uint32_t)TILE;
     for (int g = 0; g < Hkv; ++g) {
@@ -1272,7 +1095,7 @@ int launch_heads(Params& P, const void* q, void* out, const uint8_t* kcache,
             return GQA_ERR_CUDA;
         P.q = static_cast<const __half*>(q) + (size_t)g * P.grp.d * D;
         P.out = static_cast<__half*>(out) + (size_t)g * P.grp.d * D;
-        const int rc = launch_split(tk, tv, P, stream, device, num_sms);
+        const int rc = launch_split(tk, tv, P, stream, device);
         if (rc != GQA_OK) return rc;
     }
     return GQA_OK;
@@ -1323,10 +1146,7 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
     P.ws_ml = w + (size_t)P.G * P.nq * D;
-    // The grid barrier's two words live in the workspace's counter area
-    // (zeroed when the workspace is registered, left at zero by every launch).
-    P.gbar = static_cast<unsigned*>(ws);
-    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device, di->num_sms);
+    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
 size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms) {
@@ -1376,8 +1196,7 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
     P.ws_ml = w + (size_t)P.G * P.nq * D;
-    P.gbar = nullptr;
-    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device, di->num_sms);
+    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
 }  // namespace gqa
@@ -1393,9 +1212,7 @@ namespace paged {
 
 constexpr int kNoAllocMaxSplits = 160;
 constexpr int kNoAllocMaxRows = 48;  // packed rows per launch
-constexpr size_t kNoAllocHead = 64;   // grid barrier words, then padding to 256 bytes
-constexpr size_t kNoAllocFloats =
-    kNoAllocHead + (size_t)kNoAllocMaxSplits * kNoAllocMaxRows * (D + 2);
+constexpr size_t kNoAllocFloats = (size_t)kNoAllocMaxSplits * kNoAllocMaxRows * (D + 2);
 
 // Split partials (O, then (m, l)) of gqa_attn_paged_e4m3_noalloc: about
 // 7.9 MB of module-scope device memory that every device loading the library
@@ -1453,14 +1270,11 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.scale = scale;
     P.out = static_cast<__half*>(out);
     P.err = di->err_word;
-    if (P.nq > kNoAllocMaxRows || kNoAllocHead + (size_t)P.G * P.nq * (D + 2) > kNoAllocFloats)
+    if (P.nq > kNoAllocMaxRows || (size_t)P.G * P.nq * (D + 2) > kNoAllocFloats)
         return GQA_ERR_WORKSPACE;
-    // The first words hold the grid barrier (zero at load, left at zero by
-    // every launch); the partials follow.
-    P.gbar = reinterpret_cast<unsigned*>(scratch);
-    P.ws_o = scratch + kNoAllocHead;
-    P.ws_ml = P.ws_o + (size_t)P.G * P.nq * D;
-    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device, di->num_sms);
+    P.ws_o = scratch;
+    P.ws_ml = scratch + (size_t)P.G * P.nq * D;
+    return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
 }  // namespace gqa
