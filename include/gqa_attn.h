@@ -21,12 +21,13 @@
  *        is in physical-page units; positions clamped to the row.
  *
  * Conventions shared by every entry point
- *   - Head groupings: D = 256 (the dense prefill also D = 128); Hkv KV heads,
- *     each shared by Hq / Hkv query heads (Hkv divides Hq, Hq <= 64).  The pages' family is Hq = 6,
- *     Hkv = 1; with Hkv > 1 the prefill gives every query head its own
- *     tiles in one launch and the E4M3 tail and sparse entry points run one
- *     launch per KV head, with per-entry limits below.  Anything else returns GQA_ERR_UNSUPPORTED.  scale must be
- *     finite and > 0.
+ *   - Head sizes and groupings: D = 256 or 128 for every entry point; Hkv KV
+ *     heads, each shared by Hq / Hkv query heads (Hkv divides Hq, Hq <= 64).
+ *     The pages' family is Hq = 6, Hkv = 1, D = 256; with Hkv > 1 the
+ *     prefill gives every query head its own tiles in one launch and the
+ *     E4M3 tail and sparse entry points run one launch per KV head, with
+ *     per-entry limits below.  Anything else returns GQA_ERR_UNSUPPORTED.
+ *     scale must be finite and > 0.
  *   - All tensor pointers are DEVICE pointers, contiguous, 16-byte aligned,
  *     owned by the caller.  fp16 means IEEE binary16.
  *   - q / out are [rows, Hq, D] fp16; out is fully overwritten.
@@ -61,7 +62,7 @@ struct CUstream_st; /* cudaStream_t */
 typedef enum {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, rows > context, bad scale */
-    GQA_ERR_UNSUPPORTED = 2,   /* D != 256 (prefill: D not 128 or 256), Hkv not dividing Hq,
+    GQA_ERR_UNSUPPORTED = 2,   /* D not 128 or 256, Hkv not dividing Hq,
                                   Hq > 64, page not a power of
                                   two in [8, 256], query_rows * Hq / Hkv > 48 (E4M3 tail),
                                   Hq / Hkv > 16 (sparse) */

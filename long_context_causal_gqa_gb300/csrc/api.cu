@@ -148,16 +148,16 @@ using namespace gqa;
 
 namespace {
 
-// The dense prefill and the E4M3 tail take any grouping with D = 256: Hkv KV
+// Every entry point takes any grouping with head size 256 or 128: Hkv KV
 // heads, each shared by Hq / Hkv query heads.
-bool prefill_family_ok(int Hq, int Hkv, int D) {
-    return D == kHeadDim && Hq >= 1 && Hq <= kMaxHeads && Hkv >= 1 && Hq % Hkv == 0;
+bool family_ok(int Hq, int Hkv, int D) {
+    return (D == kHeadDim || D == 128) && Hq >= 1 && Hq <= kMaxHeads && Hkv >= 1 &&
+           Hq % Hkv == 0;
 }
 
 // One tail launch packs query_rows x (Hq / Hkv) rows into the UMMA N dimension.
 bool tail_family_ok(int Hq, int Hkv, int D, int query_rows) {
-    return prefill_family_ok(Hq, Hkv, D) &&
-           (long long)query_rows * (Hq / Hkv) <= kMaxTailPackedRows;
+    return family_ok(Hq, Hkv, D) && (long long)query_rows * (Hq / Hkv) <= kMaxTailPackedRows;
 }
 
 bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
@@ -183,13 +183,13 @@ int sparse_common(const void* q, const void* kcache, const void* vcache, const f
     if (query_rows < 1 || ctx_len < query_rows || num_pages < 1 || max_sel < 1 ||
         !scale_ok(scale))
         return GQA_ERR_INVALID_ARG;
-    if (!prefill_family_ok(Hq, Hkv, D) || Hq / Hkv > kMaxSparseGroup || !page_ok(page))
+    if (!family_ok(Hq, Hkv, D) || Hq / Hkv > kMaxSparseGroup || !page_ok(page))
         return GQA_ERR_UNSUPPORTED;
     // Cache token rows are 32-bit indices inside the kernel.
     if ((long long)num_pages * page > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return sparse_launch(q, kcache, vcache, kscale, vscale, e4m3, block_table, sel_idx, sel_cnt,
-                         max_sel, num_pages, page, ctx_len, query_rows, Hq, Hkv, scale, out,
+                         max_sel, num_pages, page, ctx_len, query_rows, Hq, Hkv, D, scale, out,
                          stream);
 }
 
@@ -203,8 +203,7 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return GQA_ERR_INVALID_ARG;
     if (Q < 1 || KV < 1 || Q > KV || !scale_ok(scale)) return GQA_ERR_INVALID_ARG;
-    // The dense prefill also takes head size 128.
-    if (!prefill_family_ok(Hq, Hkv, D == 128 ? kHeadDim : D)) return GQA_ERR_UNSUPPORTED;
+    if (!family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
     if ((long long)Q * Hq > 0x7fffffffLL - 256) return GQA_ERR_INVALID_ARG;
     return prefill_launch(q, k, v, out, Q, KV, Hq, Hkv, D, scale, stream);
 }
@@ -225,7 +224,7 @@ int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vca
     if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, page,
-                             ctx_len, nullptr, query_rows, Hq, Hkv, scale, out, stream);
+                             ctx_len, nullptr, query_rows, Hq, Hkv, D, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -251,7 +250,7 @@ int gqa_attn_paged_e4m3_batch(const void* q, const uint8_t* kcache, const uint8_
     if ((long long)table_stride * page < (long long)max_ctx_len) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_batch_launch(q, kcache, vcache, kscale, vscale, block_tables, table_stride,
                                    num_pages, page, ctx_lens_dev, max_ctx_len, batch, query_rows,
-                                   Hq, Hkv, scale, out, stream);
+                                   Hq, Hkv, D, scale, out, stream);
 }
 
 int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -273,7 +272,8 @@ int gqa_attn_paged_e4m3_devctx(const void* q, const uint8_t* kcache, const uint8
     if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)max_ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages, page,
-                             max_ctx_len, ctx_len_dev, query_rows, Hq, Hkv, scale, out, stream);
+                             max_ctx_len, ctx_len_dev, query_rows, Hq, Hkv, D, scale, out,
+                             stream);
 }
 
 int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint8_t* vcache,
@@ -293,7 +293,7 @@ int gqa_attn_paged_e4m3_noalloc(const void* q, const uint8_t* kcache, const uint
     if (!tail_family_ok(Hq, Hkv, D, query_rows) || !page_ok(page)) return GQA_ERR_UNSUPPORTED;
     if ((long long)ctx_len > (long long)num_pages * page) return GQA_ERR_INVALID_ARG;
     return paged_e4m3_noalloc_launch(q, kcache, vcache, kscale, vscale, block_table, num_pages,
-                                     page, ctx_len, query_rows, Hq, Hkv, scale, out, stream);
+                                     page, ctx_len, query_rows, Hq, Hkv, D, scale, out, stream);
 }
 
 int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache,
@@ -318,9 +318,7 @@ int gqa_attn_sparse_blocks_e4m3(const void* q, const uint8_t* kcache, const uint
 }
 
 size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int D) {
-    if ((D != kHeadDim && !(kind == GQA_KIND_PREFILL && D == 128)) || query_rows < 1 ||
-        ctx_or_kv < 1)
-        return 0;
+    if ((D != kHeadDim && D != 128) || query_rows < 1 || ctx_or_kv < 1) return 0;
     if (Hq < 1 || Hq > kMaxHeads) return 0;
     const DeviceInfo* di = device_info();
     if (!di) return 0;
@@ -328,7 +326,7 @@ size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int 
     // for any number of KV heads (one launch takes query_rows x Hq / Hkv).
     if (kind == GQA_KIND_PAGED_E4M3_BATCH) {   // ctx_or_kv = number of sequences
         if (query_rows > kMaxTailPackedRows || ctx_or_kv > kMaxTailBatch) return 0;
-        return paged_e4m3_batch_workspace_bytes(query_rows * Hq, ctx_or_kv, di->num_sms);
+        return paged_e4m3_batch_workspace_bytes(query_rows * Hq, ctx_or_kv, di->num_sms, D);
     }
     if (ctx_or_kv < query_rows) return 0;
     switch (kind) {
@@ -336,7 +334,7 @@ size_t gqa_workspace_bytes(int kind, int query_rows, int ctx_or_kv, int Hq, int 
             return prefill_workspace_bytes(query_rows, ctx_or_kv, di->num_sms);
         case GQA_KIND_PAGED_E4M3:
             if (query_rows > kMaxTailPackedRows) return 0;
-            return paged_e4m3_workspace_bytes(query_rows * Hq, ctx_or_kv, di->num_sms);
+            return paged_e4m3_workspace_bytes(query_rows * Hq, ctx_or_kv, di->num_sms, D);
         case GQA_KIND_SPARSE:
             return kWorkspaceCounterBytes;
         default:

@@ -108,21 +108,22 @@ int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill k
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
                       int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
-                      int Hq, int Hkv, float scale, void* out, cudaStream_t stream);
-// nq = packed rows of one launch (at most query_rows * Hq).
-size_t paged_e4m3_workspace_bytes(int nq, int ctx_len, int num_sms);
+                      int Hq, int Hkv, int Dh, float scale, void* out, cudaStream_t stream);
+// nq = packed rows of one launch (at most query_rows * Hq); Dh = head size.
+size_t paged_e4m3_workspace_bytes(int nq, int ctx_len, int num_sms, int Dh);
 int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                             const float* kscale, const float* vscale,
                             const int32_t* block_tables, int table_stride, int num_pages,
                             int page, const int* ctx_lens_dev, int max_ctx_len, int batch,
-                            int R, int Hq, int Hkv, float scale, void* out, cudaStream_t stream);
-size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms);
+                            int R, int Hq, int Hkv, int Dh, float scale, void* out,
+                            cudaStream_t stream);
+size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms, int Dh);
 
 // Same as paged_e4m3_launch, with the split partials in a static device array.
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                               const float* kscale, const float* vscale,
                               const int32_t* block_table, int num_pages, int page, int ctx_len,
-                              int R, int Hq, int Hkv, float scale, void* out,
+                              int R, int Hq, int Hkv, int Dh, float scale, void* out,
                               cudaStream_t stream);
 
 // kcache / vcache: fp16 elements, or E4M3 codes with kscale / vscale (device
@@ -130,8 +131,8 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
 int sparse_launch(const void* q, const void* kcache, const void* vcache, const float* kscale,
                   const float* vscale, bool e4m3, const int32_t* block_table,
                   const int32_t* sel_idx, const int32_t* sel_cnt, int max_sel, int num_pages,
-                  int page, int ctx_len, int rows, int Hq, int Hkv, float scale, void* out,
-                  cudaStream_t stream);
+                  int page, int ctx_len, int rows, int Hq, int Hkv, int Dh, float scale,
+                  void* out, cudaStream_t stream);
 
 // Bytes at the start of every workspace reserved for merge counters.
 constexpr size_t kWorkspaceCounterBytes = 4096;

@@ -59,6 +59,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <type_traits>
 
 #include "internal.h"
 #include "sm100.cuh"
@@ -66,9 +67,8 @@
 namespace gqa {
 namespace paged {
 
-constexpr int D = kHeadDim;      // 256
+constexpr int D = kHeadDim;      // 256, the largest head size (sizes the static partials)
 constexpr int TILE = 128;        // keys per tile
-constexpr int RAW_STAGE = TILE * D;             // 32 KB of E4M3 per K or V tile
 // Threads of a CTA with NWG softmax warpgroups: producer warp, UMMA warp,
 // then 4 * NWG softmax warps.
 __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
@@ -93,7 +93,8 @@ struct Params {
     int hq;               // query heads per position in q / out
     FastDiv grp;          // packed rows per position in one launch (query heads of one KV head)
     float scale;
-    float* ws_o;    // [G][nq][D] unnormalised partial O (in units of the E4M3 V)
+    int dh;         // head size, 256 or 128
+    float* ws_o;    // [G][nq][dh] unnormalised partial O (in units of the E4M3 V)
     float* ws_ml;   // [G][nq][2]  (m in log2 units, l)
     __half* out;
     unsigned* err;
@@ -104,19 +105,28 @@ struct Params {
 // the launch's KV head; q / out already point at that head group's first head.
 __device__ __forceinline__ size_t row_offset(const Params& P, int seq, int r) {
     const int pos = P.grp.div(r);
-    return ((size_t)(seq * P.R + pos) * P.hq + (r - pos * P.grp.d)) * D;
+    return ((size_t)(seq * P.R + pos) * P.hq + (r - pos * P.grp.d)) * P.dh;
 }
 
-template <int NP, int NWG>
+// DH: head size, 256 or 128.  A K or V tile is TILE rows of DH E4M3 bytes:
+// DH / 128 swizzle atoms ("halves") of 128 bytes per row.
+template <int NP, int NWG, int DH>
 struct Layout {
+    static constexpr int HALVES = DH / 128;
+    static constexpr int RAW_STAGE = TILE * DH;       // 32 KB (DH 256) or 16 KB per K or V tile
     static constexpr int NT = 3;                      // E4M3 expansion terms
     static constexpr int N3 = NT * NP;                // UMMA N
-    static constexpr int NS = (NP <= 32) ? 2 : 1;     // S^T buffers in tensor memory
-    // P^T buffers: two up to 32 packed rows; at 48 one, so that a fifth raw
-    // stage fits (the copy stream's rate is set by its bytes in flight).
-    static constexpr int NPT = (NP <= 32) ? 2 : 1;
-    static constexpr int NRAW = (NP <= 16) ? 6 : 5;   // raw K/V stages
-    static constexpr int Q_BYTES = N3 * D;            // [Q1|Q2|Q3]: N3 rows x 256 B, 2 halves
+    // S^T buffers in tensor memory: two, except at 48 packed rows and DH 256,
+    // where the three-term S^T and O^T leave room for one.
+    static constexpr int NS = (NP <= 32 || DH == 128) ? 2 : 1;
+    // P^T buffers: two, except at 48 rows and DH 256, where one buffer lets a
+    // fifth raw stage fit (the copy stream's rate is set by its bytes in flight).
+    static constexpr int NPT = (NP <= 32 || DH == 128) ? 2 : 1;
+    // Raw K/V stages: 192 / 160 KB of 32 KB stages at DH 256; at DH 128 the
+    // 16 KB stages come twice as many (the bytes in flight are what count).
+    static constexpr int NRAW = DH == 256 ? ((NP <= 16) ? 6 : 5)
+                                          : ((NP <= 16) ? 12 : (NP <= 32 ? 11 : 10));
+    static constexpr int Q_BYTES = N3 * DH;           // [Q1|Q2|Q3]: N3 rows x DH B, in halves
     static constexpr int PT_BYTES = N3 * TILE;        // [P1|P2|P3]^T: N3 rows x 128 keys
     static constexpr int OFF_RAW = 0;
     static constexpr int OFF_Q = OFF_RAW + NRAW * RAW_STAGE;
@@ -127,19 +137,20 @@ struct Layout {
     static constexpr int OFF_FAC = OFF_MREF + NP * 4;            // [NP] floats
     static constexpr int OFF_FLAG = OFF_FAC + NP * 4;            // [2][4 NWG] ints
     static constexpr int OFF_BAR = (OFF_FLAG + 2 * 4 * NWG * 4 + 7) & ~7;
-    static constexpr int NUM_BARS = 32;   // >= NUM_BARRIERS
+    static constexpr int NUM_BARS = 40;   // >= NUM_BARRIERS
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_TMEM + 16;
     static constexpr int SMEM = BYTES + 1024;
     // TMEM columns
     static constexpr uint32_t S_COL = 0;              // NS buffers x N3  (S1 | S2 | S3)
-    static constexpr uint32_t O_COL = NS * N3;        // 2 halves of d x N3 (O1 | O2 | O3)
-    static_assert(O_COL + 2 * N3 <= 512, "tensor memory");
+    static constexpr uint32_t O_COL = NS * N3;        // HALVES x N3 (O1 | O2 | O3)
+    static_assert(O_COL + HALVES * N3 <= 512, "tensor memory");
     static_assert(SMEM <= 232448, "shared memory");
+    static_assert(NRAW <= 12, "raw stage barriers");
 };
 
 // mbarrier indices
-constexpr int MAX_RAW = 6;
+constexpr int MAX_RAW = 12;
 constexpr int MAX_WG = 6;
 enum {
     B_RAW_FULL = 0,               // [MAX_RAW]
@@ -153,7 +164,7 @@ enum {
     NUM_BARRIERS = B_S_FREE + 1,
 };
 
-static_assert(NUM_BARRIERS <= 32, "mbarrier slots");
+static_assert(NUM_BARRIERS <= 40, "mbarrier slots");
 
 // Copy order through the raw ring: K0, then K(j), V(j - 1) for j = 1 .. n - 1,
 // then V(n - 1).  V(j) is requested one tile after K(j), so that it lands
@@ -379,11 +390,13 @@ __device__ void seq_splits(const Params& P, int b, int& first, int& count) {
     first = count = 0;
 }
 
-template <int NP, int NWG, bool BATCHED>
+template <int NP, int NWG, bool BATCHED, int DH>
 __global__ void __launch_bounds__(threads_for(NWG), 1)
 paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params P) {
-    using L = Layout<NP, NWG>;
+    using L = Layout<NP, NWG, DH>;
+    constexpr int HALVES = L::HALVES;
+    constexpr int RAW_STAGE = L::RAW_STAGE;
     constexpr int NTHREADS = threads_for(NWG);
     constexpr int NKEY = 128 * NWG;   // softmax threads
     constexpr int NH = NP / NWG;      // packed query rows per softmax warpgroup
@@ -481,7 +494,8 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const int ppt = page >= TILE ? 1 : TILE >> lpage;       // pages per tile, divides 32
             const int rows_per_copy = page >= TILE ? TILE : page;
             int cur_k = 0;
-            const int pp = lane >> 1, hh = lane & 1;
+            // Lane HALVES * p + h copies page p, half h of d.
+            const int pp = lane / HALVES, hh = lane % HALVES;
             uint32_t item = 0;
             bool ok = true;
             int id_prev = 0, npg_prev = 0, y_prev = 0;
@@ -495,11 +509,11 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     okw = mbar_wait(bar(B_RAW_EMPTY + s), ph ^ 1u, abort_flag, P.err);
                     if (okw)
                         mbar_arrive_expect_tx(bar(B_RAW_FULL + s),
-                                              (uint32_t)(npg * rows_per_copy * D));
+                                              (uint32_t)(npg * rows_per_copy * DH));
                 }
                 if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
                 // Stage layout: [2 halves of d][128 keys][128 B], 128B-swizzled.
-                if (lane < 2 * npg)
+                if (lane < HALVES * npg)
                     tma_load_2d(s_raw + s * RAW_STAGE + hh * (TILE * 128) +
                                     pp * (rows_per_copy * 128),
                                 tm, bar(B_RAW_FULL + s), hh * 128, id * page + y0);
@@ -520,7 +534,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     npg = min(ppt, n_logical - lp0);
                     y0 = (tile * TILE) & (page - 1);
                     id = __shfl_sync(0xffffffffu, cur, (rel & 31) + (pp < ppt ? pp : 0));
-                    if (lane < 2 * npg && (id < 0 || id >= P.num_pages)) {
+                    if (lane < HALVES * npg && (id < 0 || id >= P.num_pages)) {
                         atomicOr(P.err, kErrBadPageId);
                         id = 0;
                     }
@@ -540,7 +554,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
     } else {
         // ---- Q -> three-term E4M3 expansion [Q1 | Q2 | Q3] in shared memory
-        // (K-major, 3NP rows of 256 bytes in two 128-byte halves, 128B-swizzled),
+        // (K-major, 3NP rows of DH bytes in 128-byte halves, 128B-swizzled),
         // one scale per packed row: x / qs ~= t1 + t2 / 32 + t3 / 1024, |x / qs| <= 256.
         // Warps 1..9 take rows r = warp - 1, warp + 8, ...; all their loads are
         // issued before the first conversion.
@@ -548,26 +562,27 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         {
             constexpr int QW = NTHREADS / 32 - 1;
             constexpr int RPW = (NP + QW - 1) / QW;
-            const int d0 = lane * 8;
-            uint4 raw[RPW];
+            constexpr int EPL = DH / 32;   // elements of a row per lane: 8 or 4
+            using QV = typename std::conditional<EPL == 8, uint4, uint2>::type;
+            const int d0 = lane * EPL;
+            QV raw[RPW];
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 const int r = warp - 1 + QW * i;
-                raw[i] = (r < P.nq) ? *reinterpret_cast<const uint4*>(
-                                          P.q + row_offset(P, seq, r) + d0)
-                                    : make_uint4(0, 0, 0, 0);
+                raw[i] = (r < P.nq) ? *reinterpret_cast<const QV*>(P.q + row_offset(P, seq, r) + d0)
+                                    : QV{};
             }
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 const int r = warp - 1 + QW * i;
                 if (r >= NP) break;
-                float x[8];
+                float x[EPL];
                 const __half* hx = reinterpret_cast<const __half*>(&raw[i]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = __half2float(hx[e]);
+                for (int e = 0; e < EPL; ++e) x[e] = __half2float(hx[e]);
                 float amax = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+                for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -575,7 +590,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 const float inv = 1.0f / sc;
                 uint32_t w1[2] = {0, 0}, w2[2] = {0, 0}, w3[2] = {0, 0};
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
+                for (int e = 0; e < EPL; e += 2) {
                     uint32_t b1, b2, b3;
                     split3_e4m3x2(x[e] * inv, x[e + 1] * inv, b1, b2, b3);
                     w1[e >> 2] |= b1 << (8 * (e & 3));
@@ -584,12 +599,19 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 }
                 const int h = d0 >> 7, cin = d0 & 127;
                 uint8_t* qh = gbase + L::OFF_Q + h * (N3 * 128);
-                *reinterpret_cast<uint2*>(qh + sw128(r, cin >> 4) + (cin & 15)) =
-                    make_uint2(w1[0], w1[1]);
-                *reinterpret_cast<uint2*>(qh + sw128(NP + r, cin >> 4) + (cin & 15)) =
-                    make_uint2(w2[0], w2[1]);
-                *reinterpret_cast<uint2*>(qh + sw128(2 * NP + r, cin >> 4) + (cin & 15)) =
-                    make_uint2(w3[0], w3[1]);
+                if constexpr (EPL == 8) {
+                    *reinterpret_cast<uint2*>(qh + sw128(r, cin >> 4) + (cin & 15)) =
+                        make_uint2(w1[0], w1[1]);
+                    *reinterpret_cast<uint2*>(qh + sw128(NP + r, cin >> 4) + (cin & 15)) =
+                        make_uint2(w2[0], w2[1]);
+                    *reinterpret_cast<uint2*>(qh + sw128(2 * NP + r, cin >> 4) + (cin & 15)) =
+                        make_uint2(w3[0], w3[1]);
+                } else {
+                    *reinterpret_cast<uint32_t*>(qh + sw128(r, cin >> 4) + (cin & 15)) = w1[0];
+                    *reinterpret_cast<uint32_t*>(qh + sw128(NP + r, cin >> 4) + (cin & 15)) = w2[0];
+                    *reinterpret_cast<uint32_t*>(qh + sw128(2 * NP + r, cin >> 4) + (cin & 15)) =
+                        w3[0];
+                }
                 if (lane == 0) qs[r] = sc;
             }
         }
@@ -621,7 +643,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     const uint32_t vst = s_raw + stage_of(vi) * RAW_STAGE;
                     const uint32_t pt = s_pt + (x % NPT) * L::PT_BYTES;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < HALVES; ++h) {
 #pragma unroll
                         for (int ks = 0; ks < TILE / 32; ++ks) {
                             // V^T half h: M = 128 d (one 128-byte atom), K = 32 keys (rows)
@@ -651,7 +673,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     tc_fence_after();
                     const uint32_t kst = s_raw + stage_of(ki) * RAW_STAGE;
 #pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk) {
+                    for (int kk = 0; kk < DH / 32; ++kk) {
                         const int h = kk >> 2;   // d half
                         const uint64_t a = sdesc_sw128(kst + h * (TILE * 128) + (kk & 3) * 32, 16, 1024);
                         const uint64_t bq = sdesc_sw128(s_q + h * (N3 * 128) + (kk & 3) * 32, 16, 1024);
@@ -789,7 +811,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
-                        for (int g6 = 0; g6 < 6; ++g6) {   // (d half, expansion term)
+                        for (int g6 = 0; g6 < 3 * HALVES; ++g6) {   // (d half, expansion term)
                             const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * NP + c0;
                             uint32_t r[NH];
                             tmem_ldn<NH>(t_lane + col, r);
@@ -808,7 +830,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 // or pages never loaded) hold whatever the cache or shared memory
                 // held, possibly the E4M3 NaN code; zero their V rows so that
                 // P = 0 times V stays 0.  Each warpgroup clears its share of the
-                // row's sixteen 16-byte units (both halves of d).
+                // row's 16-byte units (8 per half of d).
                 if (t_begin + jj == n_tiles - 1 && (ctx_len & (TILE - 1)) != 0) {
                     const int vi = item_v(jj, ntl);
                     ok = mbar_wait(bar(B_RAW_FULL + vi % NRAW), (uint32_t)((vi / NRAW) & 1), abort_flag,
@@ -817,7 +839,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     if (!ok) break;
                     if (key >= ctx_len) {
                         uint8_t* st = gbase + L::OFF_RAW + (vi % NRAW) * RAW_STAGE + k * 128;
-                        for (int u = hg * 16 / NWG; u < (hg + 1) * 16 / NWG; ++u)
+                        for (int u = hg * 8 * HALVES / NWG; u < (hg + 1) * 8 * HALVES / NWG; ++u)
                             *reinterpret_cast<uint4*>(st + (u >> 3) * (TILE * 128) + (u & 7) * 16) =
                                 make_uint4(0, 0, 0, 0);
                     }
@@ -876,7 +898,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     P.ws_ml[((size_t)split * P.nq + c) * 2 + 1] = l;
                 }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < HALVES; ++h) {
                     uint32_t r1[NH], r2[NH], r3[NH];
                     tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + c0, r1);
                     tmem_ldn<NH>(t_lane + L::O_COL + h * N3 + NP + c0, r2);
@@ -888,7 +910,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
                     for (int c = 0; c < NH; ++c)
                         if (c0 + c < P.nq)
-                            P.ws_o[((size_t)split * P.nq + c0 + c) * D + d] =
+                            P.ws_o[((size_t)split * P.nq + c0 + c) * DH + d] =
                                 fmaf(__uint_as_float(r3[c]), 1.0f / (XRATIO * XRATIO),
                                      fmaf(__uint_as_float(r2[c]), 1.0f / XRATIO,
                                           __uint_as_float(r1[c])));
@@ -945,7 +967,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
 #pragma unroll
     for (int i = 0; i < MERGE_PF; ++i) {
         const int s = warp + MERGE_WARPS * i;
-        o[i] = s < G ? __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)(S0 + s) * P.nq + c) * D + d0))
+        o[i] = s < G ? __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)(S0 + s) * P.nq + c) * P.dh + d0))
                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     constexpr int ML_PT = MERGE_MAX_SPLITS / (MERGE_WARPS * 32);
@@ -999,7 +1021,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     for (int s = warp + MERGE_WARPS * MERGE_PF; s < G; s += MERGE_WARPS) {
         const float w = w_s[s];
         if (w != 0.f)
-            add(w, __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)(S0 + s) * P.nq + c) * D + d0)));
+            add(w, __ldcg(reinterpret_cast<const float4*>(P.ws_o + ((size_t)(S0 + s) * P.nq + c) * P.dh + d0)));
     }
     red[warp][lane] = acc;
     __syncthreads();
@@ -1026,18 +1048,19 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     }
 }
 
-template <int NP, int NWG, bool BATCHED>
+template <int NP, int NWG, bool BATCHED, int DH>
 int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
                 int device) {
-    using L = Layout<NP, NWG>;
+    using L = Layout<NP, NWG, DH>;
     (void)device;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, BATCHED>),
+    if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, BATCHED, DH>),
                           L::SMEM) != GQA_OK)
         return GQA_ERR_CUDA;
-    paged_split_kernel<NP, NWG, BATCHED><<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
+    paged_split_kernel<NP, NWG, BATCHED, DH>
+        <<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P.batch * P.nq, D / 128);
+    cfg.gridDim = dim3(P.batch * P.nq, P.dh / 128);
     cfg.blockDim = dim3(MERGE_WARPS * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -1053,21 +1076,28 @@ int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStr
 // Packed query rows -> UMMA N and softmax warpgroups: every softmax thread
 // owns 8 columns (8-aligned in tensor memory), so that the latency-bound
 // softmax chain is spread over 8, 16 or 24 warps.
-template <int NP, int NWG>
+template <int NP, int NWG, int DH>
 int launch_np(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
               int device) {
     // One sequence (the common tail) or several (the batched entry point):
     // separate instantiations, so the single-sequence kernel carries none of
     // the batched bookkeeping.
-    return P.batch > 1 ? launch_np_b<NP, NWG, true>(tk, tv, P, stream, device)
-                       : launch_np_b<NP, NWG, false>(tk, tv, P, stream, device);
+    return P.batch > 1 ? launch_np_b<NP, NWG, true, DH>(tk, tv, P, stream, device)
+                       : launch_np_b<NP, NWG, false, DH>(tk, tv, P, stream, device);
+}
+
+template <int DH>
+int launch_split_dh(const CUtensorMap& tk, const CUtensorMap& tv, Params& P,
+                    cudaStream_t stream, int device) {
+    if (P.nq <= 16) return launch_np<16, 2, DH>(tk, tv, P, stream, device);
+    if (P.nq <= 32) return launch_np<32, 4, DH>(tk, tv, P, stream, device);
+    return launch_np<48, 6, DH>(tk, tv, P, stream, device);
 }
 
 int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStream_t stream,
                  int device) {
-    if (P.nq <= 16) return launch_np<16, 2>(tk, tv, P, stream, device);
-    if (P.nq <= 32) return launch_np<32, 4>(tk, tv, P, stream, device);
-    return launch_np<48, 6>(tk, tv, P, stream, device);
+    return P.dh == 128 ? launch_split_dh<128>(tk, tv, P, stream, device)
+                       : launch_split_dh<256>(tk, tv, P, stream, device);
 }
 
 // Grouping fields: Hq query heads per position, Hkv KV heads, each shared by
@@ -1079,22 +1109,23 @@ void set_grouping(Params& P, int Hq, int Hkv) {
 }
 
 // Split + merge once per KV head.  Head g reads row g of every cache token
-// (the caches [num_pages * page, Hkv, D] seen as rows Hkv * D bytes apart) and
+// (the caches [num_pages * page, Hkv, dh] seen as rows Hkv * dh bytes apart) and
 // writes query heads g * grp .. g * grp + grp - 1.  Launches on one stream run
 // in order, so they can share the split partials.
 int launch_heads(Params& P, const void* q, void* out, const uint8_t* kcache,
                  const uint8_t* vcache, int Hkv, cudaStream_t stream, int device) {
     const uint64_t rows = (uint64_t)P.num_pages * P.page;
     const uint32_t box_rows = P.page < TILE ? (uint32_t)P.page : (uint32_t)TILE;
+    const int dh = P.dh;
     for (int g = 0; g < Hkv; ++g) {
         CUtensorMap tk, tv;
-        if (!make_map_2d_u8(&tk, kcache + (size_t)g * D, rows, D, (uint64_t)Hkv * D, box_rows,
+        if (!make_map_2d_u8(&tk, kcache + (size_t)g * dh, rows, dh, (uint64_t)Hkv * dh, box_rows,
                             128) ||
-            !make_map_2d_u8(&tv, vcache + (size_t)g * D, rows, D, (uint64_t)Hkv * D, box_rows,
+            !make_map_2d_u8(&tv, vcache + (size_t)g * dh, rows, dh, (uint64_t)Hkv * dh, box_rows,
                             128))
             return GQA_ERR_CUDA;
-        P.q = static_cast<const __half*>(q) + (size_t)g * P.grp.d * D;
-        P.out = static_cast<__half*>(out) + (size_t)g * P.grp.d * D;
+        P.q = static_cast<const __half*>(q) + (size_t)g * P.grp.d * dh;
+        P.out = static_cast<__half*>(out) + (size_t)g * P.grp.d * dh;
         const int rc = launch_split(tk, tv, P, stream, device);
         if (rc != GQA_OK) return rc;
     }
@@ -1103,16 +1134,16 @@ int launch_heads(Params& P, const void* q, void* out, const uint8_t* kcache,
 
 }  // namespace paged
 
-size_t paged_e4m3_workspace_bytes(int nq, int ctx_len, int num_sms) {
+size_t paged_e4m3_workspace_bytes(int nq, int ctx_len, int num_sms, int Dh) {
     const int n_tiles = (ctx_len + paged::TILE - 1) / paged::TILE;
     const int G = n_tiles < num_sms ? n_tiles : num_sms;
-    return kWorkspaceCounterBytes + (size_t)G * nq * (paged::D + 2) * sizeof(float) + 256;
+    return kWorkspaceCounterBytes + (size_t)G * nq * (Dh + 2) * sizeof(float) + 256;
 }
 
 int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                       const float* kscale, const float* vscale, const int32_t* block_table,
                       int num_pages, int page, int ctx_len, const int* ctx_dev, int R,
-                      int Hq, int Hkv, float scale, void* out, cudaStream_t stream) {
+                      int Hq, int Hkv, int Dh, float scale, void* out, cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -1131,6 +1162,7 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
+    P.dh = Dh;
     set_grouping(P, Hq, Hkv);
     P.n_tiles = (ctx_len + TILE - 1) / TILE;
     P.G = P.n_tiles < di->num_sms ? P.n_tiles : di->num_sms;
@@ -1141,17 +1173,17 @@ int paged_e4m3_launch(const void* q, const uint8_t* kcache, const uint8_t* vcach
     void* ws;
     size_t ws_bytes;
     current_workspace(&ws, &ws_bytes);
-    if (!ws || ws_bytes < paged_e4m3_workspace_bytes(P.nq, ctx_len, di->num_sms))
+    if (!ws || ws_bytes < paged_e4m3_workspace_bytes(P.nq, ctx_len, di->num_sms, Dh))
         return GQA_ERR_WORKSPACE;
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
-    P.ws_ml = w + (size_t)P.G * P.nq * D;
+    P.ws_ml = w + (size_t)P.G * P.nq * Dh;
     return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
-size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms) {
+size_t paged_e4m3_batch_workspace_bytes(int nq, int batch, int num_sms, int Dh) {
     const int G = batch > num_sms ? batch : num_sms;
-    return kWorkspaceCounterBytes + (size_t)G * nq * (paged::D + 2) * sizeof(float) + 256;
+    return kWorkspaceCounterBytes + (size_t)G * nq * (Dh + 2) * sizeof(float) + 256;
 }
 
 // Several sequences' tails in one launch: q/out [batch, R, Hq, 256], block
@@ -1162,7 +1194,8 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
                             const float* kscale, const float* vscale,
                             const int32_t* block_tables, int table_stride, int num_pages,
                             int page, const int* ctx_lens_dev, int max_ctx_len, int batch,
-                            int R, int Hq, int Hkv, float scale, void* out, cudaStream_t stream) {
+                            int R, int Hq, int Hkv, int Dh, float scale, void* out,
+                            cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -1181,6 +1214,7 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
     P.num_pages = num_pages;
     P.ctx_len = max_ctx_len;
     P.R = R;
+    P.dh = Dh;
     set_grouping(P, Hq, Hkv);
     P.n_tiles = (max_ctx_len + TILE - 1) / TILE;
     P.G = batch > di->num_sms ? batch : di->num_sms;
@@ -1191,11 +1225,11 @@ int paged_e4m3_batch_launch(const void* q, const uint8_t* kcache, const uint8_t*
     void* ws;
     size_t ws_bytes;
     current_workspace(&ws, &ws_bytes);
-    if (!ws || ws_bytes < paged_e4m3_batch_workspace_bytes(P.nq, batch, di->num_sms))
+    if (!ws || ws_bytes < paged_e4m3_batch_workspace_bytes(P.nq, batch, di->num_sms, Dh))
         return GQA_ERR_WORKSPACE;
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceCounterBytes);
     P.ws_o = w;
-    P.ws_ml = w + (size_t)P.G * P.nq * D;
+    P.ws_ml = w + (size_t)P.G * P.nq * Dh;
     return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 
@@ -1227,7 +1261,7 @@ size_t paged_e4m3_noalloc_capacity_floats() { return paged::kNoAllocFloats; }
 int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                               const float* kscale, const float* vscale,
                               const int32_t* block_table, int num_pages, int page, int ctx_len,
-                              int R, int Hq, int Hkv, float scale, void* out,
+                              int R, int Hq, int Hkv, int Dh, float scale, void* out,
                               cudaStream_t stream) {
     using namespace paged;
     const DeviceInfo* di = device_info();
@@ -1263,6 +1297,7 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.num_pages = num_pages;
     P.ctx_len = ctx_len;
     P.R = R;
+    P.dh = Dh;
     set_grouping(P, Hq, Hkv);
     P.n_tiles = (ctx_len + TILE - 1) / TILE;
     P.G = P.n_tiles < di->num_sms ? P.n_tiles : di->num_sms;
@@ -1270,10 +1305,10 @@ int paged_e4m3_noalloc_launch(const void* q, const uint8_t* kcache, const uint8_
     P.scale = scale;
     P.out = static_cast<__half*>(out);
     P.err = di->err_word;
-    if (P.nq > kNoAllocMaxRows || (size_t)P.G * P.nq * (D + 2) > kNoAllocFloats)
+    if (P.nq > kNoAllocMaxRows || (size_t)P.G * P.nq * (Dh + 2) > kNoAllocFloats)
         return GQA_ERR_WORKSPACE;
     P.ws_o = scratch;
-    P.ws_ml = scratch + (size_t)P.G * P.nq * D;
+    P.ws_ml = scratch + (size_t)P.G * P.nq * Dh;
     return launch_heads(P, q, out, kcache, vcache, Hkv, stream, di->device);
 }
 

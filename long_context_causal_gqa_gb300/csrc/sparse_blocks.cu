@@ -55,11 +55,9 @@
 namespace gqa {
 namespace sparse {
 
-constexpr int D = kHeadDim;
 constexpr int TILE = 128;            // keys per tile
 constexpr int BLK = 4;               // tokens per selected block
 constexpr int NP = 16;               // the heads of one launch padded to the UMMA N granule
-constexpr int KV_TILE_BYTES = TILE * D * 2;   // 64 KB
 constexpr int NTHREADS = 320;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
@@ -77,29 +75,34 @@ struct Params {
     int max_sel, num_pages, ctx_len, rows, G;
     int log2_page;   // tokens per cache page = 1 << log2_page (8 .. 256)
     int nh;          // query heads of this launch (those of one KV head), <= NP
-    int q_stride;    // elements between consecutive rows of q / out (Hq * D)
-    int kv_stride;   // elements between consecutive tokens of the caches (Hkv * D)
+    int q_stride;    // elements between consecutive rows of q / out (Hq * head size)
+    int kv_stride;   // elements between consecutive tokens of the caches (Hkv * head size)
     float scale_log2;
     __half* out;
     unsigned* err;
 };
 
-// smem layout (offsets from a 1024-aligned base)
-constexpr int OFF_K = 0;                                  // 2 x 64 KB
-constexpr int OFF_V = OFF_K + 2 * KV_TILE_BYTES;          // 64 KB
-constexpr int Q_BYTES = NP * D * 2;                       // 8 KB: 4 chunks [16][64]
-constexpr int OFF_Q = OFF_V + KV_TILE_BYTES;              // 2 x 8 KB
 constexpr int PT_BYTES = NP * TILE * 2;                   // 4 KB: 2 chunks [16][64 keys]
-constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;               // 2 x 4 KB
-constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;            // [4][NP] floats
-constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
-constexpr int OFF_FAC = OFF_MREF + NP * 4;
-constexpr int OFF_FLAG = OFF_FAC + NP * 4;                // [2][4] ints
 constexpr int NI = 8;                                     // token-index ring slots
-constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;       // [NI][TILE] int token rows
 constexpr int SEEN_BITS = 16384;                          // block ids seen in the row
-constexpr int OFF_SEEN = OFF_IDX + NI * TILE * 4;         // [SEEN_BITS / 32] words
-constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
+
+// smem layout (offsets from a 1024-aligned base) for head size DH (256 or 128)
+template <int DH>
+struct SL {
+    static constexpr int KV_TILE_BYTES = TILE * DH * 2;            // 64 / 32 KB
+    static constexpr int OFF_K = 0;                                // 2 K tiles
+    static constexpr int OFF_V = OFF_K + 2 * KV_TILE_BYTES;        // 1 V tile
+    static constexpr int Q_BYTES = NP * DH * 2;                    // DH / 64 chunks [16][64]
+    static constexpr int OFF_Q = OFF_V + KV_TILE_BYTES;            // 2 Q buffers
+    static constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;             // 2 P^T buffers
+    static constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;          // [4][NP] floats
+    static constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
+    static constexpr int OFF_FAC = OFF_MREF + NP * 4;
+    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;              // [2][4] ints
+    static constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;     // [NI][TILE] int token rows
+    static constexpr int OFF_SEEN = OFF_IDX + NI * TILE * 4;       // [SEEN_BITS / 32] words
+    static constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
+};
 enum {
     B_KFULL = 0,   // [2]
     B_KEMPTY = 2,  // [2]
@@ -116,10 +119,12 @@ enum {
     B_IEMPTY = 18 + NI, // [NI] token-index slot read by the gather and the key warps
     NUM_BARS = 18 + 2 * NI
 };
-constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM = OFF_TMEM + 16 + 1024;
+template <int DH>
+constexpr int off_tmem() { return SL<DH>::OFF_BAR + NUM_BARS * 8; }
+template <int DH>
+constexpr int smem_bytes() { return off_tmem<DH>() + 16 + 1024; }
 constexpr uint32_t S_COL = 0;        // 2 x NP
-constexpr uint32_t O_COL = 2 * NP;   // 2 halves x NP
+constexpr uint32_t O_COL = 2 * NP;   // DH / 128 halves x NP
 constexpr uint32_t TMEM_COLS = 128;
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t u) {
@@ -167,13 +172,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
 
 // HQ: heads per launch known at compile time (6), or NP with the count read
 // from P.nh (any grouping up to 16 query heads per KV head).  F8: the cache
-// holds E4M3 codes, converted to fp16 on the way into shared memory.
-template <int HQ, bool F8>
+// holds E4M3 codes, converted to fp16 on the way into shared memory.  DH: head
+// size, 256 or 128.
+template <int HQ, bool F8, int DH>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
+    using L = SL<DH>;
+    constexpr int HALVES = DH / 128;   // 128-d halves of a row (one M = 128 P.V each)
+    constexpr int KV_TILE_BYTES = L::KV_TILE_BYTES;
+    constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, Q_BYTES = L::Q_BYTES, OFF_Q = L::OFF_Q;
+    constexpr int OFF_PT = L::OFF_PT, OFF_RED = L::OFF_RED, OFF_MREF = L::OFF_MREF;
+    constexpr int OFF_FAC = L::OFF_FAC, OFF_FLAG = L::OFF_FLAG, OFF_IDX = L::OFF_IDX;
+    constexpr int OFF_SEEN = L::OFF_SEEN, OFF_BAR = L::OFF_BAR, OFF_TMEM = off_tmem<DH>();
     const int nh = (HQ == NP) ? P.nh : HQ;
-    const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * D;
+    const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * DH;
     // Tile buffers: two fp16 K tiles and one V tile; with E4M3 codes one K
-    // tile, the V tile, and 64 KB of code staging in the second K tile's place.
+    // tile, the V tile, and the code staging in the second K tile's place.
     constexpr int NKB = F8 ? 1 : 2;
     constexpr uint32_t KOFF = OFF_K;
     constexpr uint32_t VOFF = F8 ? (uint32_t)KV_TILE_BYTES : (uint32_t)OFF_V;
@@ -232,7 +245,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         // ------------------------------------------------------------ gather
         const int gt = threadIdx.x;        // 0..127
         const int* idx = reinterpret_cast<const int*>(gbase + OFF_IDX);
-        const size_t tok_stride = HQ == NP ? (size_t)P.kv_stride : (size_t)D;
+        const size_t tok_stride = HQ == NP ? (size_t)P.kv_stride : (size_t)DH;
         // Cache row offset of this lane's key in tile-counter position gg, read
         // from the index ring; tok < 0 for a masked key.
         auto take_index = [&](uint32_t gg, int& tok, size_t& row) -> bool {
@@ -261,34 +274,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 ok = false;
                 break;
             }
-            for (int u = gt; u < nh * (D / 8); u += 128) {
-                const int h = u / (D / 8), c16 = u % (D / 8);
+            for (int u = gt; u < nh * (DH / 8); u += 128) {
+                const int h = u / (DH / 8), c16 = u % (DH / 8);
                 const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
                                      sw128(h, c16 % 8);
-                cp_async16(dst, P.q + (size_t)i * q_stride + h * D + c16 * 8, 16);
+                cp_async16(dst, P.q + (size_t)i * q_stride + h * DH + c16 * 8, 16);
             }
             cp_async_arrive(bar(B_QFULL + qb));
             ++rloc;
             if constexpr (F8) {
                 // E4M3 codes.  Each gather lane copies the 16-byte code chunks it
                 // will convert into a private, double-buffered staging area
-                // (buffer b, pass e: byte (b * 16 + e) * 2048 + 16 gt), one step
-                // (tile t, K or V) ahead of the step it converts; it then waits
-                // for its own copies of the current step, converts them to fp16
-                // into the step's tile and signals it.  A token row is 256 code
-                // bytes: half-warp `half` takes key 2e + half, lane u of it the
-                // codes of d = 16u .. 16u + 15, which become fp16 units 2u, 2u + 1
-                // of the row (chunk u / 4, units 2 (u % 4) and 2 (u % 4) + 1
-                // within it).  Masked tokens are zero-filled by the copy.
-                const int u = lane & 15, half = lane >> 4;
+                // (buffer b, pass e: byte (b * NPASS + e) * 2048 + 16 gt), one
+                // step (tile t, K or V) ahead of the step it converts; it then
+                // waits for its own copies of the current step, converts them to
+                // fp16 into the step's tile and signals it.  A token row is DH
+                // code bytes: a group of LPK = DH / 16 lanes takes key KPP e +
+                // group, lane u of it the codes of d = 16u .. 16u + 15, which
+                // become fp16 units 2u, 2u + 1 of the row (chunk u / 4, units
+                // 2 (u % 4) and 2 (u % 4) + 1 within it).  Masked tokens are
+                // zero-filled by the copy.
+                constexpr int LPK = DH / 16;      // lanes per key row: 16 or 8
+                constexpr int KPP = 32 / LPK;     // keys per pass: 2 or 4
+                constexpr int NPASS = 32 / KPP;   // passes per warp's 32 keys: 16 or 8
+                const int u = lane % LPK, half = lane / LPK;
                 const uint32_t unit = 2u * (uint32_t)(u & 3);
                 auto stage_addr = [&](int b, int e) -> uint32_t {
-                    return sbase + SOFF + (uint32_t)((b * 16 + e) * 2048 + gt * 16);
+                    return sbase + SOFF + (uint32_t)((b * NPASS + e) * 2048 + gt * 16);
                 };
                 auto issue = [&](int b, const uint8_t* cache, int tok_l, size_t row_l) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int src = 2 * e + half;
+                    for (int e = 0; e < NPASS; ++e) {
+                        const int src = KPP * e + half;
                         const int tok = __shfl_sync(0xffffffffu, tok_l, src);
                         const size_t row = __shfl_sync(0xffffffffu, row_l, src);
                         const uint8_t* p = tok >= 0 ? cache + row + 16 * u : cache;
@@ -351,8 +368,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     const uint32_t chunk = sbase + (kv == 0 ? KOFF : VOFF) +
                                            (uint32_t)(u >> 2) * (TILE * 128);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const uint32_t key = (uint32_t)(warp * 32 + 2 * e + half);
+                    for (int e = 0; e < NPASS; ++e) {
+                        const uint32_t key = (uint32_t)(warp * 32 + KPP * e + half);
                         const uint4 r = *reinterpret_cast<const uint4*>(
                             gbase + (stage_addr(n & 1, e) - sbase));
                         const uint4 lo = make_uint4(e4m3x2_to_f16x2(r.x), e4m3x2_to_f16x2(r.x >> 16),
@@ -369,7 +386,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 g += (uint32_t)nt;
             } else {
                 for (int t = 0; t < nt && ok; ++t, ++g) {
-                    // This warp's 32 keys: lane -> cache row, then one 512-byte row per key.
+                    // This warp's 32 keys: lane -> cache row, then the DH * 2-byte
+                    // row of each key (one warp-wide copy covers 512 / (DH * 2) keys).
                     int tok_l;
                     size_t row_l;
                     if (!take_index(g, tok_l, row_l)) {
@@ -391,14 +409,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                         }
                         const uint32_t tile = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V);
                         const __half* cache = kv == 0 ? P.kcache : P.vcache;
+                        constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
+                        constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
 #pragma unroll 4
-                        for (int e = 0; e < 32; ++e) {
-                            const int key = warp * 32 + e;
-                            const int tok = __shfl_sync(0xffffffffu, tok_l, e);
-                            const size_t row = __shfl_sync(0xffffffffu, row_l, e);
-                            // lane covers d = 8 lane .. 8 lane + 7: chunk lane / 8, unit lane % 8
-                            const uint32_t dst = tile + (lane >> 3) * (TILE * 128) + sw128(key, lane & 7);
-                            const __half* src = tok >= 0 ? cache + row + lane * 8 : cache;
+                        for (int e = 0; e < 32 / KPI; ++e) {
+                            const int src_lane = KPI * e + lane / LPK;
+                            const int key = warp * 32 + src_lane;
+                            const int ul = lane % LPK;
+                            const int tok = __shfl_sync(0xffffffffu, tok_l, src_lane);
+                            const size_t row = __shfl_sync(0xffffffffu, row_l, src_lane);
+                            // lane covers d = 8 ul .. 8 ul + 7: chunk ul / 8, unit ul % 8
+                            const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
+                            const __half* src = tok >= 0 ? cache + row + ul * 8 : cache;
                             cp_async16(dst, src, tok >= 0 ? 16u : 0u);
                         }
                         cp_async_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
@@ -421,7 +443,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 tc_fence_after();
                 const uint32_t pt = sbase + OFF_PT + (x & 1) * PT_BYTES;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < HALVES; ++h) {
 #pragma unroll
                     for (int ks = 0; ks < TILE / 16; ++ks) {
                         const uint64_t a = sdesc_sw128(sbase + VOFF + (2 * h) * (TILE * 128) +
@@ -458,7 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     fence_async_shared();
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
+                    for (int kk = 0; kk < DH / 16; ++kk) {
                         const uint64_t a = sdesc_sw128(sbase + KOFF + kb * KV_TILE_BYTES +
                                                            (kk / 4) * (TILE * 128) + (kk % 4) * 32,
                                                        16, 1024);
@@ -494,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             const int nt = row_tiles(cnt);
             if (nt == 0) {
                 // Nothing selected: the row's output is zero.
-                for (int u = k; u < nh * (D / 8); u += 128)
+                for (int u = k; u < nh * (DH / 8); u += 128)
                     reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
                 continue;
             }
@@ -575,7 +597,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
+                        for (int h = 0; h < HALVES; ++h) {
                             uint32_t r[NP];
                             tmem_ld16(t_lane + O_COL + h * NP, r);
                             tmem_ld_wait<NP>(r);
@@ -636,7 +658,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     inv[c] = l > 0.f ? 1.0f / l : 0.f;
             }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < HALVES; ++h) {
                 uint32_t r[NP];
                 tmem_ld16(t_lane + O_COL + h * NP, r);
                 tmem_ld_wait<NP>(r);
@@ -644,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 #pragma unroll
                 for (int c = 0; c < HQ; ++c)
                     if (c < nh)
-                        P.out[(size_t)i * q_stride + c * D + d] =
+                        P.out[(size_t)i * q_stride + c * DH + d] =
                             __float2half_rn(__uint_as_float(r[c]) * inv[c]);
             }
             // red / mref are rewritten by the next row only after this barrier.
@@ -752,8 +774,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 int sparse_launch(const void* q, const void* kcache, const void* vcache, const float* kscale,
                   const float* vscale, bool e4m3, const int32_t* block_table,
                   const int32_t* sel_idx, const int32_t* sel_cnt, int max_sel, int num_pages,
-                  int page, int ctx_len, int rows, int Hq, int Hkv, float scale, void* out,
-                  cudaStream_t stream) {
+                  int page, int ctx_len, int rows, int Hq, int Hkv, int Dh, float scale,
+                  void* out, cudaStream_t stream) {
     using namespace sparse;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
@@ -769,33 +791,42 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
     P.rows = rows;
     P.G = rows < di->num_sms ? rows : di->num_sms;
     P.nh = grp;
-    P.q_stride = Hq * D;
-    P.kv_stride = Hkv * D;
+    P.q_stride = Hq * Dh;
+    P.kv_stride = Hkv * Dh;
     P.kscale = kscale;
     P.vscale = vscale;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.err = di->err_word;
-    // The 6-head instantiations address the caches with a stride of D, so
-    // they serve one KV head only.
+    // The 6-head instantiations address the caches with a stride of one head,
+    // so they serve one KV head only.
     const bool six = (grp == kHq && Hkv == 1);
     using KernelFn = void (*)(Params);
-    const KernelFn fn = e4m3 ? (six ? sparse_kernel<kHq, true> : sparse_kernel<NP, true>)
-                             : (six ? sparse_kernel<kHq, false> : sparse_kernel<NP, false>);
-    if (ensure_smem_limit(reinterpret_cast<const void*>(fn), SMEM) != GQA_OK)
+    KernelFn fn;
+    int smem;
+    if (Dh == 128) {
+        fn = e4m3 ? (six ? sparse_kernel<kHq, true, 128> : sparse_kernel<NP, true, 128>)
+                  : (six ? sparse_kernel<kHq, false, 128> : sparse_kernel<NP, false, 128>);
+        smem = smem_bytes<128>();
+    } else {
+        fn = e4m3 ? (six ? sparse_kernel<kHq, true, 256> : sparse_kernel<NP, true, 256>)
+                  : (six ? sparse_kernel<kHq, false, 256> : sparse_kernel<NP, false, 256>);
+        smem = smem_bytes<256>();
+    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(fn), smem) != GQA_OK)
         return GQA_ERR_CUDA;
     // One launch per KV head: query heads g * grp .. g * grp + grp - 1 read
     // token rows of KV head g.
     const size_t esz = e4m3 ? 1 : 2;   // bytes per cache element
     for (int g = 0; g < Hkv; ++g) {
-        P.q = static_cast<const __half*>(q) + (size_t)g * grp * D;
-        P.out = static_cast<__half*>(out) + (size_t)g * grp * D;
-        const uint8_t* kb = static_cast<const uint8_t*>(kcache) + (size_t)g * D * esz;
-        const uint8_t* vb = static_cast<const uint8_t*>(vcache) + (size_t)g * D * esz;
+        P.q = static_cast<const __half*>(q) + (size_t)g * grp * Dh;
+        P.out = static_cast<__half*>(out) + (size_t)g * grp * Dh;
+        const uint8_t* kb = static_cast<const uint8_t*>(kcache) + (size_t)g * Dh * esz;
+        const uint8_t* vb = static_cast<const uint8_t*>(vcache) + (size_t)g * Dh * esz;
         P.kcache = reinterpret_cast<const __half*>(kb);
         P.vcache = reinterpret_cast<const __half*>(vb);
         P.kcache8 = kb;
         P.vcache8 = vb;
-        fn<<<P.G, NTHREADS, SMEM, stream>>>(P);
+        fn<<<P.G, NTHREADS, smem, stream>>>(P);
         if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
     return GQA_OK;

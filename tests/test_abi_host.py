@@ -80,6 +80,8 @@ def test_paged_rejects_bad_arguments(lib):
     assert _paged(lib, kscale=P(0)) == binding.GQA_ERR_INVALID_ARG
     assert _paged(lib, R=0) == binding.GQA_ERR_INVALID_ARG
     assert _paged(lib, R=9) == binding.GQA_ERR_UNSUPPORTED
+    assert _paged(lib, D=64) == binding.GQA_ERR_UNSUPPORTED      # 128 and 256 are accepted
+    assert _paged(lib, D=192) == binding.GQA_ERR_UNSUPPORTED
     assert _paged(lib, page=12) == binding.GQA_ERR_UNSUPPORTED   # not a power of two
     assert _paged(lib, page=512) == binding.GQA_ERR_UNSUPPORTED
     assert _paged(lib, page=4) == binding.GQA_ERR_UNSUPPORTED
@@ -119,7 +121,8 @@ def test_sparse_rejects_bad_arguments(lib):
     assert _sparse(lib, max_sel=0) == binding.GQA_ERR_INVALID_ARG
     assert _sparse(lib, rows=65, ctx=64) == binding.GQA_ERR_INVALID_ARG
     assert _sparse(lib, ctx=65, pages=4) == binding.GQA_ERR_INVALID_ARG
-    assert _sparse(lib, D=64) == binding.GQA_ERR_UNSUPPORTED
+    assert _sparse(lib, D=64) == binding.GQA_ERR_UNSUPPORTED     # 128 and 256 are accepted
+    assert _sparse(lib, D=512) == binding.GQA_ERR_UNSUPPORTED
     # At most 16 query heads per KV head; Hkv must divide Hq.
     assert _sparse(lib, Hq=32, Hkv=1) == binding.GQA_ERR_UNSUPPORTED
     assert _sparse(lib, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED

@@ -227,3 +227,64 @@ def test_paged_devctx_page_256_graph_replay(cuda_lib):
         ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table, ctx,
                                 p.scale)
         _check(out, ref, f"page=256 device ctx={ctx}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,R,ctx,cap,page", [
+    (6, 1, 1, 3000, 4096, 16),
+    (6, 1, 8, 5000, 8192, 16),    # 48 packed rows
+    (6, 1, 2, 1, 16, 16),         # a one-token context
+    (6, 2, 8, 4000, 4096, 16),    # two launches of 24 packed rows
+    (8, 1, 6, 3001, 4096, 32),
+    (6, 3, 4, 777, 1024, 8),
+    (4, 4, 5, 2000, 2048, 64),
+    (6, 1, 8, 40000, 65536, 256),
+    (6, 1, 3, 130, 256, 128),     # a ragged last tile
+])
+def test_paged_head_size_128_matches_oracle(cuda_lib, Hq, Hkv, R, ctx, cap, page):
+    """Head size 128 (one 128-byte swizzle atom per cache row, 16 KB stages)."""
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=ctx, capacity=cap, seed=Hq + R + page, page=page,
+                                 Hq=Hq, Hkv=Hkv, D=128)
+    out = _run(cuda_lib, p)
+    _check(out, oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                                  p.ctx_len, p.scale), f"D=128 Hq={Hq} Hkv={Hkv} R={R} ctx={ctx}")
+
+
+@pytest.mark.parametrize("R", [1, 8])
+def test_paged_head_size_128_full_size_and_replay(cuda_lib, R):
+    p = inputs.paged_e4m3_inputs(R=R, ctx_len=261888, capacity=262144, seed=70 + R, D=128)
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    a = cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    _check(a, oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table,
+                                p.ctx_len, p.scale), f"D=128 R={R} ctx=261888")
+    out = torch.empty_like(q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.paged_e4m3(q, kc, vc, ks, vs, bt, p.ctx_len, p.scale, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), a.view(torch.int16))
+
+
+def test_paged_head_size_128_devctx_replay(cuda_lib):
+    max_ctx, cap = 9000, 9216
+    p = inputs.paged_e4m3_inputs(R=4, ctx_len=max_ctx, capacity=cap, seed=93, D=128)
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, bt = _to_dev(p, dev)
+    ctx_dev = torch.tensor([max_ctx], dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, max_ctx, p.scale, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.paged_e4m3_devctx(q, kc, vc, ks, vs, bt, ctx_dev, max_ctx, p.scale, out=out)
+    for ctx in [9000, 4097, 128, 5]:
+        ctx_dev.fill_(ctx)
+        g.replay()
+        torch.cuda.synchronize()
+        assert cuda_lib.device_error() == 0
+        ref = oracle.paged_e4m3(p.q, p.kcache, p.vcache, p.kscale, p.vscale, p.block_table, ctx,
+                                p.scale)
+        _check(out, ref, f"D=128 device ctx={ctx}")

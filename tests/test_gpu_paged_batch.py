@@ -125,3 +125,27 @@ def test_batch_bitwise_reproducible_and_bad_context_flagged(cuda_lib):
     torch.cuda.synchronize()
     assert cuda_lib.device_error() & cuda_lib.DEVERR_BAD_CTX_LEN
     _run_and_check(cuda_lib, big, tables, q, [4000, 4000, 2000], max_ctx, c.cpu(), "clamped")
+
+
+def test_batch_head_size_128_matches_oracle(cuda_lib):
+    """Batched variable-length tails at head size 128."""
+    ctxs = [300, 5000, 12345, 64, 9000]
+    R, max_ctx = 3, 16384
+    bi = inputs.paged_e4m3_batch_inputs(ctxs, R, max_ctx, seed=128, D=128)
+    c = bi.cache
+    dev = torch.device("cuda")
+    ks = torch.tensor([c.kscale], dtype=torch.float32, device=dev)
+    vs = torch.tensor([c.vscale], dtype=torch.float32, device=dev)
+    out = cuda_lib.paged_e4m3_batch(bi.q.to(dev), c.kcache.to(dev), c.vcache.to(dev), ks, vs,
+                                    bi.tables.to(dev),
+                                    torch.tensor(ctxs, dtype=torch.int32, device=dev), max_ctx,
+                                    c.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    for b, ctx in enumerate(ctxs):
+        ref = oracle.paged_e4m3(bi.q[b], c.kcache, c.vcache, c.kscale, c.vscale, bi.tables[b],
+                                ctx, c.scale)
+        g = out[b].float().cpu().numpy().astype(np.float64)
+        err = np.abs(g - ref).max()
+        rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+        assert err <= 1e-3 and rel <= 1e-2, f"D=128 seq {b}: {err:.3e} {rel:.3e}"

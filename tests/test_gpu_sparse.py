@@ -233,3 +233,48 @@ def test_sparse_duplicate_ids_are_masked_and_flagged(cuda_lib, ctx, e4m3):
         out1 = _run(cuda_lib, s, sel1, cnt1)
         assert cuda_lib.device_error() == 0
         _check(out1, ref, "shuffled ids")
+
+
+@pytest.mark.parametrize("Hq,Hkv,rows,ctx,T,page,e4m3", [
+    (6, 1, 200, 4096, 512, 16, False),
+    (6, 1, 200, 4096, 512, 16, True),
+    (6, 1, 1, 4, 4, 16, False),          # one row, one block
+    (6, 2, 100, 3001, 256, 32, False),   # two KV heads
+    (8, 1, 120, 4096, 128, 8, True),     # generic 16-column instantiation
+    (4, 4, 60, 2000, 64, 64, False),
+    (6, 1, 300, 5000, 2048, 256, True),
+    (16, 1, 40, 1000, 128, 16, False),
+])
+def test_sparse_head_size_128_matches_oracle(cuda_lib, Hq, Hkv, rows, ctx, T, page, e4m3):
+    """Head size 128: a fp16 token row is 256 bytes (16 lanes, two keys per
+    warp-wide copy), an E4M3 row 128 code bytes (8 lanes, four keys per pass)."""
+    dev = torch.device("cuda")
+    if e4m3:
+        s = inputs.sparse_e4m3_inputs(rows=rows, ctx_len=ctx, tokens=T, seed=Hq + T, page=page,
+                                      Hq=Hq, Hkv=Hkv, D=128)
+        ks = torch.tensor([s.kscale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([s.vscale], dtype=torch.float32, device=dev)
+        out = cuda_lib.sparse_blocks_e4m3(s.q.to(dev), s.kcache.to(dev), s.vcache.to(dev), ks, vs,
+                                          s.block_table.to(dev), s.sel_idx.to(dev),
+                                          s.sel_cnt.to(dev), s.ctx_len, s.scale)
+        ref = oracle.sparse_blocks_e4m3(s.q, s.kcache, s.vcache, s.kscale, s.vscale,
+                                        s.block_table, s.sel_idx, s.sel_cnt, s.ctx_len, s.scale)
+    else:
+        s = inputs.sparse_inputs(rows=rows, ctx_len=ctx, tokens=T, seed=Hq + T, page=page, Hq=Hq,
+                                 Hkv=Hkv, D=128)
+        out = _run(cuda_lib, s)
+        ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
+                                   s.ctx_len, s.scale)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_error() == 0
+    _check(out, ref, f"D=128 Hq={Hq} Hkv={Hkv} T={T} page={page} e4m3={e4m3}")
+
+
+def test_sparse_head_size_128_full_size_sampled_rows(cuda_lib):
+    s = inputs.sparse_inputs(rows=4096, ctx_len=32768, tokens=2048, seed=128, D=128)
+    out = _run(cuda_lib, s)
+    assert cuda_lib.device_error() == 0
+    rows = np.array([0, 1, 2, 3, 1000, 2047, 4094, 4095], dtype=np.int32)
+    ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
+                               s.ctx_len, s.scale, rows=rows)
+    _check(out[torch.as_tensor(rows, dtype=torch.long)], ref, "D=128 T=2048")
