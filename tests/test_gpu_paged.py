@@ -232,7 +232,7 @@ def test_paged_devctx_page_256_graph_replay(cuda_lib):
 @pytest.mark.parametrize("Hq,Hkv,R,ctx,cap,page", [
     (6, 1, 1, 3000, 4096, 16),
     (6, 1, 8, 5000, 8192, 16),    # 48 packed rows
-    (6, 1, 2, 1, 16, 16),         # a one-token context
+    (6, 1, 1, 1, 16, 16),         # a one-token context
     (6, 2, 8, 4000, 4096, 16),    # two launches of 24 packed rows
     (8, 1, 6, 3001, 4096, 32),
     (6, 3, 4, 777, 1024, 8),
