@@ -67,6 +67,32 @@ def dense_inputs(Q: int, KV: int, seed: int = 0, Hq: int = HQ, Hkv: int = HKV,
     return DenseInputs(q, k, v, Q, KV, Hq, Hkv, D, scale)
 
 
+@dataclasses.dataclass
+class DenseE4M3Inputs:
+    q: torch.Tensor  # [Q, Hq, D] fp16
+    k: torch.Tensor  # [KV, Hkv, D] uint8 E4M3 codes
+    v: torch.Tensor  # [KV, Hkv, D] uint8 E4M3 codes
+    kscale: float
+    vscale: float
+    Q: int
+    KV: int
+    Hq: int
+    Hkv: int
+    D: int
+    scale: float
+
+
+def dense_e4m3_inputs(Q: int, KV: int, seed: int = 0, Hq: int = HQ, Hkv: int = HKV,
+                      D: int = HEAD_DIM, scale: float = SCALE) -> "DenseE4M3Inputs":
+    """Dense causal prefill over an E4M3 K/V cache: q i.i.d. N(0,1) in fp16; K and
+    V i.i.d. N(0,1), each tensor encoded as E4M3 with one scale (absmax / 448),
+    the storage of the E4M3 tail applied to the dense workload."""
+    q = normal_fp16((Q, Hq, D), seed * 13 + 0)
+    k, ks = e4m3_encode(torch.randn(KV, Hkv, D, generator=_gen(seed * 13 + 1)))
+    v, vs = e4m3_encode(torch.randn(KV, Hkv, D, generator=_gen(seed * 13 + 2)))
+    return DenseE4M3Inputs(q, k.contiguous(), v.contiguous(), ks, vs, Q, KV, Hq, Hkv, D, scale)
+
+
 def e4m3_encode(x: torch.Tensor):
     """Per-tensor E4M3 encoding: scale = absmax / 448, byte = RNE(x / scale).
 

@@ -154,6 +154,22 @@ def paged_e4m3(q, kcache, vcache, kscale: float, vscale: float, block_table, ctx
     return out
 
 
+def dense_e4m3(q, k, v, kscale: float, vscale: float, scale: float, rows=None,
+               nthreads=None) -> np.ndarray:
+    """Dense bottom-right causal attention over E4M3 keys and values: the E4M3
+    storage of "[Perf] Ship the qualified SM70 long-context layout and drop its
+    context fences" (What) applied to the dense prefill of "[Kernel][SM70]
+    Default long-prefill GQA architecture" (Purpose).  q [Q, Hq, D] fp16, k / v
+    [KV, Hkv, D] uint8 E4M3 codes with real value decode(byte) * kscale /
+    vscale.  The same arithmetic as the paged tail with the whole context in
+    one page (block table [0]), so row i sees keys 0 .. KV - Q + i."""
+    ka, va = _np(k, np.uint8), _np(v, np.uint8)
+    KV, Hkv, D = ka.shape
+    table = np.zeros(1, dtype=np.int32)
+    return paged_e4m3(q, ka.reshape(1, KV, Hkv, D), va.reshape(1, KV, Hkv, D), kscale, vscale,
+                      table, KV, scale, rows=rows, nthreads=nthreads)
+
+
 def sparse_blocks(q, kcache, vcache, block_table, sel_idx, sel_cnt, ctx_len: int,
                   scale: float, rows=None, nthreads=None) -> np.ndarray:
     """Selected-block sparse attention over an fp16 page cache."""

@@ -401,3 +401,40 @@ def test_sparse_e4m3_equals_fp16_sparse_on_decoded_values():
     ref = oracle.sparse_blocks(inp.q, kd, vd, inp.block_table, inp.sel_idx, inp.sel_cnt,
                                inp.ctx_len, 1 / 16)
     assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- dense over E4M3
+
+def test_dense_e4m3_matches_decimal_bruteforce():
+    inp = inputs.dense_e4m3_inputs(Q=3, KV=11, seed=9, D=8)
+    got = oracle.dense_e4m3(inp.q, inp.k, inp.v, inp.kscale, inp.vscale, 0.3)
+    kf = _decode_torch(inp.k).numpy() * inp.kscale
+    vf = _decode_torch(inp.v).numpy() * inp.vscale
+    ref = _brute(_f64(inp.q), kf, vf, 0.3, lambda i: range(11 - 3 + i + 1))
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-15)
+
+
+def test_dense_e4m3_unit_scales_equal_dense_on_decoded_values():
+    """With scales 1 the E4M3 values are exact fp16 values: the dense fp16
+    oracle on them gives bit-identical results."""
+    inp = inputs.dense_e4m3_inputs(Q=40, KV=300, seed=10, Hq=6, Hkv=2, D=32)
+    got = oracle.dense_e4m3(inp.q, inp.k, inp.v, 1.0, 1.0, 1 / 16)
+    ref = oracle.dense(inp.q, _decode_torch(inp.k).to(torch.float16),
+                       _decode_torch(inp.v).to(torch.float16), 1 / 16)
+    assert np.array_equal(got, ref)
+
+
+def test_dense_e4m3_equals_paged_tail_on_a_permuted_layout():
+    """The same codes stored in permuted page-16 blocks and read through the
+    block table give bit-identical rows (the paged tail's arithmetic)."""
+    inp = inputs.dense_e4m3_inputs(Q=5, KV=77, seed=11, D=16)
+    page, n_log = 16, (77 + 15) // 16
+    table = inputs.permuted_block_table(n_log, n_log + 3, seed=12)
+    kc = torch.full((n_log + 3, page, 1, 16), 0x7F, dtype=torch.uint8)
+    vc = torch.full((n_log + 3, page, 1, 16), 0x7F, dtype=torch.uint8)
+    for t in range(77):
+        kc[table[t // page], t % page] = inp.k[t]
+        vc[table[t // page], t % page] = inp.v[t]
+    a = oracle.dense_e4m3(inp.q, inp.k, inp.v, inp.kscale, inp.vscale, 1 / 16)
+    b = oracle.paged_e4m3(inp.q, kc, vc, inp.kscale, inp.vscale, table, 77, 1 / 16)
+    assert np.array_equal(a, b)
