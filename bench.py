@@ -232,13 +232,24 @@ def make_flush(device):
     return flush
 
 
-def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0, Hq=HQ, Hkv=1, Dh=D):
+def bench_prefill(binding, Q, KV, steps, warmup, flush, device, seed=0, Hq=HQ, Hkv=1, Dh=D,
+                  e4m3=False):
     import torch
     from long_context_causal_gqa_gb300 import inputs
+    stream = torch.cuda.current_stream()
+    if e4m3:
+        d = inputs.dense_e4m3_inputs(Q, KV, seed=seed, Hq=Hq, Hkv=Hkv, D=Dh)
+        q, k, v = d.q.to(device), d.k.to(device), d.v.to(device)
+        ks = torch.tensor([d.kscale], dtype=torch.float32, device=device)
+        vs = torch.tensor([d.vscale], dtype=torch.float32, device=device)
+        out = torch.empty_like(q)
+        binding.prefill_e4m3(q, k, v, ks, vs, SCALE, out=out)
+        times = time_steps(lambda: binding.prefill_e4m3(q, k, v, ks, vs, SCALE, out=out), steps,
+                           warmup, flush, stream)
+        return times, (q, k, v, out, d)
     d = inputs.dense_inputs(Q, KV, seed=seed, Hq=Hq, Hkv=Hkv, D=Dh)
     q, k, v = d.q.to(device), d.k.to(device), d.v.to(device)
     out = torch.empty_like(q)
-    stream = torch.cuda.current_stream()
     binding.prefill(q, k, v, SCALE, out=out)
     times = time_steps(lambda: binding.prefill(q, k, v, SCALE, out=out), steps, warmup, flush,
                        stream)
@@ -604,6 +615,15 @@ def run_gpu(args):
             secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
                               "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
                               "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4)})
+        for kv in (KV, KV_SWEEP[-1]):
+            # K / V stored as E4M3 codes (converted to fp16 in shared memory).
+            t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device,
+                                 e4m3=True)
+            ms = statistics.mean(t)
+            secondary.append({"what": f"prefill Q={Q} KV={kv}, E4M3 K/V cache", "ms": round(ms, 4),
+                              "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
+                              "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4),
+                              "device_error": binding.device_error()})
         for hq, hkv, dh in ((6, 2, D), (8, 1, D), (6, 1, 128)):
             # Other head groupings (every query head's tiles in one launch when
             # Hkv > 1) and head size 128.
@@ -733,10 +753,11 @@ def run_case(args):
     flush = make_flush(device)
     if args.case == "prefill":
         t, _ = bench_prefill(binding, args.q, args.kv, args.steps, args.warmup, flush, device,
-                             Hq=args.hq, Hkv=args.hkv, Dh=args.d)
+                             Hq=args.hq, Hkv=args.hkv, Dh=args.d, e4m3=args.e4m3)
         ms = statistics.median(t)
         fl = prefill_flops(args.q, args.kv, args.hq, args.d)
-        line = {"case": f"prefill Q={args.q} KV={args.kv} Hq={args.hq} Hkv={args.hkv} D={args.d}",
+        line = {"case": f"prefill Q={args.q} KV={args.kv} Hq={args.hq} Hkv={args.hkv} D={args.d}"
+                        + (" E4M3 K/V" if args.e4m3 else ""),
                 "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
                 "frac_of_peak": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)}
     elif args.case == "paged_batch":
@@ -830,6 +851,7 @@ def main():
     ap.add_argument("--hkv", type=int, default=1, help="--case prefill: KV heads")
     ap.add_argument("--d", type=int, default=D, help="--case prefill|paged|sparse: head size (256 or 128)")
     ap.add_argument("--tokens", type=int, default=2048, help="--case sparse: tokens per row")
+    ap.add_argument("--e4m3", action="store_true", help="--case prefill: E4M3 K/V cache")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -90,6 +90,23 @@ typedef enum {
 int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int Q, int KV,
                      int Hq, int Hkv, int D, float scale, struct CUstream_st* stream);
 
+/* Dense causal prefill over an FP8-E4M3 K/V cache: the E4M3 storage of
+ * [P2, What] applied to the dense workload of [P1, Purpose].  Same arguments,
+ * layouts and result as gqa_attn_prefill, except:
+ *   k, v          [KV, Hkv, D] uint8 E4M3 codes (OCP e4m3fn: bias 7, 0x7F /
+ *                 0xFF NaN, max 448); real value = decode(byte) * scale; no
+ *                 code may be the NaN code
+ *   kscale/vscale DEVICE pointers to one fp32 each, 4-byte aligned
+ *                 (graph-capturable)
+ * Each CTA's tensor-memory copies bring the codes into shared memory, where
+ * two converter warps write them as fp16 (exact: every E4M3 value is an fp16
+ * value) into the slots the fp16 UMMAs read; the K scale joins the score
+ * scale and the V scale multiplies the output.  Half the K/V bytes of the
+ * fp16 prefill; the workspace is the same (GQA_KIND_PREFILL). */
+int gqa_attn_prefill_e4m3(const void* q, const uint8_t* k, const uint8_t* v, const float* kscale,
+                          const float* vscale, void* out, int Q, int KV, int Hq, int Hkv, int D,
+                          float scale, struct CUstream_st* stream);
+
 /* Paged FP8-E4M3 verifier tail [P2, What / Changes].
  *   q            [query_rows, Hq, D] fp16, 1 <= query_rows, query_rows * Hq / Hkv
  *                <= 48 (one launch per KV head packs its query heads x rows;

@@ -37,7 +37,7 @@ DEVERR_BAD_CTX_LEN = 0x8
 DEVERR_DUP_BLOCK_ID = 0x10
 
 # Every symbol include/gqa_attn.h declares.
-EXPORTED = ("gqa_attn_prefill", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_devctx",
+EXPORTED = ("gqa_attn_prefill", "gqa_attn_prefill_e4m3", "gqa_attn_paged_e4m3", "gqa_attn_paged_e4m3_devctx",
             "gqa_attn_paged_e4m3_batch",
             "gqa_attn_paged_e4m3_noalloc",
             "gqa_attn_sparse_blocks", "gqa_attn_sparse_blocks_e4m3",
@@ -67,6 +67,8 @@ def load():
             P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             lib.gqa_attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, F, P]
             lib.gqa_attn_prefill.restype = I
+            lib.gqa_attn_prefill_e4m3.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+            lib.gqa_attn_prefill_e4m3.restype = I
             lib.gqa_attn_paged_e4m3.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
             lib.gqa_attn_paged_e4m3.restype = I
             lib.gqa_attn_paged_e4m3_devctx.argtypes = [P, P, P, P, P, P, I, I, P, I, I, I, I, I,
@@ -186,6 +188,26 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float = 1.
         st = load().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), Q, KV, Hq, Hkv, D,
                                      float(scale), _stream_ptr(stream))
     _check(st, "gqa_attn_prefill")
+    return out
+
+
+def prefill_e4m3(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kscale: torch.Tensor,
+                 vscale: torch.Tensor, scale: float = 1.0 / 16, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Dense causal GQA prefill over an E4M3 K/V cache: q [Q,Hq,D] fp16, k/v
+    [KV,Hkv,D] uint8 codes, kscale/vscale one-element fp32 CUDA tensors."""
+    dev = _need_cuda(q, k, v, kscale, vscale)
+    Q, Hq, D = q.shape
+    KV, Hkv, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda(out)
+    with torch.cuda.device(dev):
+        ensure_workspace(workspace_bytes(KIND_PREFILL, Q, KV, Hq, D), dev)
+        st = load().gqa_attn_prefill_e4m3(_ptr(q), _ptr(k), _ptr(v), _ptr(kscale), _ptr(vscale),
+                                          _ptr(out), Q, KV, Hq, Hkv, D, float(scale),
+                                          _stream_ptr(stream))
+    _check(st, "gqa_attn_prefill_e4m3")
     return out
 
 

@@ -142,6 +142,32 @@ bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_u8_plain(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
+                       uint64_t rows, uint64_t head_stride, uint64_t row_stride, uint32_t box_d,
+                       uint32_t box_rows, bool three_d) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    CUresult r;
+    if (three_d) {
+        cuuint64_t dims[3] = {d, heads, rows};
+        cuuint64_t strides[2] = {head_stride, row_stride};
+        cuuint32_t box[3] = {box_d, 1, box_rows};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {d, rows};
+        cuuint64_t strides[1] = {row_stride};
+        cuuint32_t box[2] = {box_d, box_rows};
+        cuuint32_t estr[2] = {1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace gqa
 
 using namespace gqa;
@@ -205,7 +231,21 @@ int gqa_attn_prefill(const void* q, const void* k, const void* v, void* out, int
     if (Q < 1 || KV < 1 || Q > KV || !scale_ok(scale)) return GQA_ERR_INVALID_ARG;
     if (!family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
     if ((long long)Q * Hq > 0x7fffffffLL - 256) return GQA_ERR_INVALID_ARG;
-    return prefill_launch(q, k, v, out, Q, KV, Hq, Hkv, D, scale, stream);
+    return prefill_launch(q, k, v, nullptr, nullptr, out, Q, KV, Hq, Hkv, D, scale, stream);
+}
+
+int gqa_attn_prefill_e4m3(const void* q, const uint8_t* k, const uint8_t* v, const float* kscale,
+                          const float* vscale, void* out, int Q, int KV, int Hq, int Hkv, int D,
+                          float scale, struct CUstream_st* stream) {
+    if (!q || !k || !v || !kscale || !vscale || !out) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale)) & 3u)
+        return GQA_ERR_INVALID_ARG;
+    if (Q < 1 || KV < 1 || Q > KV || !scale_ok(scale)) return GQA_ERR_INVALID_ARG;
+    if (!family_ok(Hq, Hkv, D)) return GQA_ERR_UNSUPPORTED;
+    if ((long long)Q * Hq > 0x7fffffffLL - 256) return GQA_ERR_INVALID_ARG;
+    return prefill_launch(q, k, v, kscale, vscale, out, Q, KV, Hq, Hkv, D, scale, stream);
 }
 
 int gqa_attn_paged_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,

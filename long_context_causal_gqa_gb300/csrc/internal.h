@@ -65,6 +65,14 @@ bool make_map_3d_f16(CUtensorMap* map, const void* base, uint64_t d, uint64_t he
 bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t row_stride, uint32_t box_rows, uint32_t box_cols);
 
+// uint8 tensor (d, heads, rows) -- or (d, rows) when three_d is false -- with
+// heads head_stride bytes apart and rows row_stride bytes apart (multiples of
+// 16), a box of box_d bytes x 1 head x box_rows rows, no swizzle (rows land
+// box_d bytes apart in shared memory).
+bool make_map_u8_plain(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
+                       uint64_t rows, uint64_t head_stride, uint64_t row_stride, uint32_t box_d,
+                       uint32_t box_rows, bool three_d);
+
 // Exact unsigned division by a divisor fixed per launch, for dividends below
 // 2^31: the multiply-high method of Granlund and Montgomery ("Division by
 // invariant integers using multiplication", 1994, section 4), with
@@ -100,8 +108,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Launchers (one per kernel family).  Arguments are validated by the caller.
 // Dh: head size, 256 or 128.
-int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
-                   int Hq, int Hkv, int Dh, float scale, cudaStream_t stream);
+// kscale / vscale: null for fp16 k / v; device pointers to one fp32 each when
+// k / v hold E4M3 codes.
+int prefill_launch(const void* q, const void* k, const void* v, const float* kscale,
+                   const float* vscale, void* out, int Q, int KV, int Hq, int Hkv, int Dh,
+                   float scale, cudaStream_t stream);
 size_t prefill_workspace_bytes(int Q, int KV, int num_sms);
 int prefill_resident_pairs();   // co-resident two-CTA clusters of the prefill kernel
 

@@ -74,21 +74,37 @@ constexpr int HALF_SLOT = SLOT_BYTES / 2;
 #ifndef GQA_PREFILL_NV
 #define GQA_PREFILL_NV 5
 #endif
-constexpr int NK = GQA_PREFILL_NK;            // K slots (DH / 128 per tile)
-constexpr int NV = GQA_PREFILL_NV;            // V slots (DH / 128 per tile)
 constexpr int Q_BYTES = BM * D * 2;           // 64 KB (the DH = 256 Q tile)
-constexpr int RING_BYTES = (NK + NV) * SLOT_BYTES;
 constexpr int NWG = 2;                        // softmax warpgroups per CTA
 constexpr int COLS = BN / NWG;                // S columns per softmax thread
 constexpr int NSOFT = 128 * NWG;              // softmax threads per CTA
-constexpr int NTHREADS = 64 + NSOFT + 32;     // + the V producer warp
 constexpr int V_WARP = 2 + NSOFT / 32;
-// Barriers: K full/empty, V full/empty, q full/empty, s[2], p[2], o, drain, group.
-constexpr int NRING = NK + NV;
-constexpr int NUM_BARS = 2 * NRING + 9;
 constexpr int XCH_BYTES = 3 * NWG * BM * 4;  // part maxima [parity][part][row], sums [part][row]
-constexpr int SMEM_BYTES =
-    1024 /*align slack*/ + RING_BYTES + Q_BYTES + XCH_BYTES + NUM_BARS * 8 + 16;
+// E4M3 staging slot: this CTA's codes of one fp16 ring slot (8 KB).
+constexpr int STG_SLOT = 8192;
+
+// Per-variant sizes.  F8 (K and V stored as FP8-E4M3 codes): each CTA's TMA
+// brings its codes into staging slots, and two converter warps (one for K,
+// one for V) write them as fp16 into the ring slots the UMMAs read; the fp16
+// ring shrinks to make room for the staging ring.
+// Barriers: ring full/empty, q full/empty, s[2], p[2], o, drain, group, then
+// staging full/empty (F8).
+template <bool F8>
+struct Cfg {
+    static constexpr int NK = F8 ? 3 : GQA_PREFILL_NK;   // K slots (DH / 128 per tile)
+    static constexpr int NV = F8 ? 3 : GQA_PREFILL_NV;   // V slots (DH / 128 per tile)
+    static constexpr int NRING = NK + NV;
+    static constexpr int NSK = F8 ? 3 : 0;               // K staging slots
+    static constexpr int NSV = F8 ? 3 : 0;               // V staging slots
+    static constexpr int NSTG = NSK + NSV;
+    static constexpr int RING_BYTES = NRING * SLOT_BYTES;
+    static constexpr int STG_BYTES = NSTG * STG_SLOT;
+    static constexpr int NUM_BARS = 2 * NRING + 9 + 2 * NSTG;
+    static constexpr int NTHREADS = 64 + NSOFT + 32 + (F8 ? 64 : 0);
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + STG_BYTES + Q_BYTES +
+                                      XCH_BYTES + NUM_BARS * 8 + 16;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 0;
 constexpr uint32_t S_COL0 = 256;
@@ -107,6 +123,8 @@ struct Params {
     int out_stride;       // elements between consecutive packed rows of out
     long long total;      // causal-visible (pair tile, kv tile) iterations
     float scale_log2;     // scale * log2(e)
+    const float* kscale;  // E4M3 K / V scales (device, one fp32 each); null for fp16 K / V
+    const float* vscale;
     __half* out;
     FastDiv ptiles;       // divides a tile-space index by num_ptiles (its head)
     float* ws_o;          // [G][2][BM2][DH] unnormalised partial O
@@ -179,20 +197,23 @@ struct SegIter {
     }
 };
 
-// Ring slot s: K slots are 0 .. NK-1, V slots NK .. NK+NV-1.
-__device__ __forceinline__ uint32_t bar_full(uint32_t b, int s) { return b + 8 * s; }
-__device__ __forceinline__ uint32_t bar_empty(uint32_t b, int s) { return b + 8 * (NRING + s); }
-__device__ __forceinline__ uint32_t bar_qfull(uint32_t b) { return b + 8 * (2 * NRING); }
-__device__ __forceinline__ uint32_t bar_qempty(uint32_t b) { return b + 8 * (2 * NRING + 1); }
-__device__ __forceinline__ uint32_t bar_sfull(uint32_t b, int i) {
-    return b + 8 * (2 * NRING + 2 + i);
-}
-__device__ __forceinline__ uint32_t bar_pfull(uint32_t b, int i) {
-    return b + 8 * (2 * NRING + 4 + i);
-}
-__device__ __forceinline__ uint32_t bar_ofull(uint32_t b) { return b + 8 * (2 * NRING + 6); }
-__device__ __forceinline__ uint32_t bar_drain(uint32_t b) { return b + 8 * (2 * NRING + 7); }
-__device__ __forceinline__ uint32_t bar_group(uint32_t b) { return b + 8 * (2 * NRING + 8); }
+// Barrier addresses for a ring of NR slots (K slots 0 .. NK-1, V slots
+// NK .. NR-1) and NS staging slots.
+template <int NR>
+struct Bars {
+    uint32_t b;
+    __device__ uint32_t full(int s) const { return b + 8 * s; }
+    __device__ uint32_t empty(int s) const { return b + 8 * (NR + s); }
+    __device__ uint32_t qfull() const { return b + 8 * (2 * NR); }
+    __device__ uint32_t qempty() const { return b + 8 * (2 * NR + 1); }
+    __device__ uint32_t sfull(int i) const { return b + 8 * (2 * NR + 2 + i); }
+    __device__ uint32_t pfull(int i) const { return b + 8 * (2 * NR + 4 + i); }
+    __device__ uint32_t ofull() const { return b + 8 * (2 * NR + 6); }
+    __device__ uint32_t drain() const { return b + 8 * (2 * NR + 7); }
+    __device__ uint32_t group() const { return b + 8 * (2 * NR + 8); }
+    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 9 + i); }
+    __device__ uint32_t stg_empty(int i, int ns) const { return b + 8 * (2 * NR + 9 + ns + i); }
+};
 
 // One ring (K or V) seen by its producer and by the UMMA issuer: slot
 // position n maps to slot first + n % count, phase (n / count) & 1.
@@ -336,11 +357,90 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volati
     return ok;
 }
 
+// Cluster-scope forms of the barrier operations, for ring slots that the
+// converter warps of both CTAs fill with generic stores: the arrive releases
+// (and the wait acquires) at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait as mbar_wait, with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             unsigned* err) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cl(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                *abort = 1;
+                atomicOr(err, kErrWaitTimeout);
+                return false;
+            }
+        }
+    }
+}
+// Arrive with cluster-scope release on an mbarrier of this CTA (local) or of
+// the pair's even CTA (remote, address from mapa).
+__device__ __forceinline__ void arrive_cl_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void arrive_cl_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+// TMA load into this CTA's shared memory, completion on a barrier of this CTA.
+template <bool MH>
+__device__ __forceinline__ void tma_load_self(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                              int32_t x, int32_t head, int32_t y) {
+    if (MH)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(head), "r"(y), "r"(bar)
+            : "memory");
+    else
+        tma_load_2d(dst, map, bar, x, y);
+}
+// Two E4M3 codes (low 16 bits of v, low byte first) -> fp16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)v));
+    return r;
+}
+// 16 E4M3 codes -> two 16-byte units of 8 fp16 each.
+__device__ __forceinline__ void e4m3x16_f16(const uint4& c, uint4& lo, uint4& hi) {
+    lo = make_uint4(e4m3x2_f16x2(c.x), e4m3x2_f16x2(c.x >> 16), e4m3x2_f16x2(c.y),
+                    e4m3x2_f16x2(c.y >> 16));
+    hi = make_uint4(e4m3x2_f16x2(c.z), e4m3x2_f16x2(c.z >> 16), e4m3x2_f16x2(c.w),
+                    e4m3x2_f16x2(c.w >> 16));
+}
+
 // MH: the tile space holds one pair-tile range per query head (Hkv > 1,
 // 3-D maps); otherwise one range of packed rows (2-D maps).  DH: head size,
-// 256 or 128.
-template <bool MH, int DH>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+// 256 or 128.  F8: K and V are E4M3 codes (tm_k / tm_v map the code bytes),
+// converted to fp16 in shared memory by two extra warps.
+template <bool MH, int DH, bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<F8>::NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params P) {
     static_assert(DH == 256 || DH == 128, "head size");
@@ -352,15 +452,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr int SUBS = SLOT_BYTES / SUB_BYTES;    // V sub-tiles per slot
     constexpr int OCOLS = DH / NWG;                 // O columns per softmax thread
     constexpr uint32_t IDESC_PV = idesc_f16_f32(256, DH, false, true);
+    using C = Cfg<F8>;
+    constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING, NSK = C::NSK, NSV = C::NSV;
+    constexpr int NSTG = C::NSTG;
+    constexpr int RING_BYTES = C::RING_BYTES, STG_BYTES = C::STG_BYTES, NUM_BARS = C::NUM_BARS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
+    // Layout: fp16 ring | E4M3 staging (F8) | Q | exchange | barriers | tmem address.
     const uint32_t s_ring = base;
-    const uint32_t s_q = base + RING_BYTES;
+    const uint32_t s_stg = base + RING_BYTES;
+    const uint32_t s_q = s_stg + STG_BYTES;
     const uint32_t s_bars = s_q + Q_BYTES + XCH_BYTES;
-    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + Q_BYTES);
-    uint32_t* tmem_base_ptr =
-        reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + Q_BYTES + XCH_BYTES + NUM_BARS * 8);
+    const Bars<NRING> BR{s_bars};
+    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + STG_BYTES + Q_BYTES);
+    uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + STG_BYTES +
+                                                          Q_BYTES + XCH_BYTES + NUM_BARS * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_ptr + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -371,18 +478,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NRING; ++s) {
-            mbar_init(bar_full(s_bars, s), 1);
-            mbar_init(bar_empty(s_bars, s), 1);
+            // fp16 path: one arrival (with the pair's transaction bytes); F8: one
+            // arrival per CTA's converter warp.
+            mbar_init(BR.full(s), F8 ? 2 : 1);
+            mbar_init(BR.empty(s), 1);
         }
-        mbar_init(bar_qfull(s_bars), 1);
-        mbar_init(bar_qempty(s_bars), 1);
+        for (int s = 0; s < NSTG; ++s) {
+            mbar_init(BR.stg_full(s), 1);
+            mbar_init(BR.stg_empty(s, NSTG), 1);
+        }
+        mbar_init(BR.qfull(), 1);
+        mbar_init(BR.qempty(), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_sfull(s_bars, i), 1);
-            mbar_init(bar_pfull(s_bars, i), 2 * NSOFT / 32);   // one arrival per softmax warp of the pair
+            mbar_init(BR.sfull(i), 1);
+            mbar_init(BR.pfull(i), 2 * NSOFT / 32);   // one arrival per softmax warp of the pair
         }
-        mbar_init(bar_ofull(s_bars), 1);
-        mbar_init(bar_drain(s_bars), 1);
-        mbar_init(bar_group(s_bars), NSOFT);
+        mbar_init(BR.ofull(), 1);
+        mbar_init(BR.drain(), 1);
+        mbar_init(BR.group(), NSOFT);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
@@ -413,19 +526,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // ------------------------------------------------------------ producers
         // Warp 0: Q and K; warp V_WARP: V.  Each loads this CTA's half of
         // every operand; completions land on the even CTA's full barriers,
-        // whose transaction count the even CTA sets for both halves.
+        // whose transaction count the even CTA sets for both halves.  F8: K / V
+        // codes go to this CTA's own staging slots (8 KB each, unswizzled rows),
+        // completing on its own staging barriers, for the converter warps.
         if (lane == 0) {
             const bool kq = warp == 0;
-            Ring rg{kq ? 0 : NK, kq ? NK : NV, 0u};
+            Ring rg = F8 ? Ring{kq ? 0 : NSK, kq ? NSK : NSV, 0u}
+                         : Ring{kq ? 0 : NK, kq ? NK : NV, 0u};
             int seg = 0;
             bool ok = true;
             // Acquire the next slot of this ring; returns its full barrier.
             auto acquire = [&](uint32_t& dst, uint32_t& fb) -> bool {
                 const int slot = rg.slot();
-                if (!mbar_wait(bar_empty(s_bars, slot), rg.phase() ^ 1u, abort_flag, P.err))
+                if constexpr (F8) {
+                    if (!mbar_wait(BR.stg_empty(slot, NSTG), rg.phase() ^ 1u, abort_flag, P.err))
+                        return false;
+                    dst = s_stg + slot * STG_SLOT;
+                    fb = BR.stg_full(slot);
+                    mbar_arrive_expect_tx(fb, STG_SLOT);
+                    return true;
+                }
+                if (!mbar_wait(BR.empty(slot), rg.phase() ^ 1u, abort_flag, P.err))
                     return false;
                 dst = s_ring + slot * SLOT_BYTES;
-                fb = bar_full(s_bars, slot);
+                fb = BR.full(slot);
                 if (leader) mbar_arrive_expect_tx(fb, 2 * SLOT_BYTES);
                 fb = leader_addr(fb);
                 return true;
@@ -433,11 +557,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
                 const int kvh = MH ? hd / P.head_group : 0;   // KV head of this segment
                 if (kq) {
-                    if (!mbar_wait(bar_qempty(s_bars), (seg & 1) ^ 1, abort_flag, P.err)) {
+                    if (!mbar_wait(BR.qempty(), (seg & 1) ^ 1, abort_flag, P.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t qb = bar_qfull(s_bars);
+                    const uint32_t qb = BR.qfull();
                     if (leader) mbar_arrive_expect_tx(qb, 2 * QB);
                     for (int c = 0; c < QCH; ++c)
                         tma_load_pair<MH>(s_q + c * (BM * 128), &tm_q, leader_addr(qb), c * 64, hd,
@@ -450,7 +574,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             ok = false;
                             break;
                         }
-                        if (kq) {
+                        if (F8) {
+                            // Codes of the same keys and d: K, this CTA's 64 keys x
+                            // d 128 h .. 128 h + 127; V, keys (BN / SLOTS) h ..
+                            // + BN / SLOTS - 1 x this CTA's DH / 2 d.
+                            if (kq)
+                                tma_load_self<MH>(dst, &tm_k, fb, 128 * h, kvh,
+                                                  j * BN + 64 * (int)rank);
+                            else
+                                tma_load_self<MH>(dst, &tm_v, fb, (DH / 2) * (int)rank, kvh,
+                                                  j * BN + h * (BN / SLOTS));
+                        } else if (kq) {
                             // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
                             for (int cc = 0; cc < 2; ++cc)
                                 tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fb, (2 * h + cc) * 64,
@@ -469,15 +603,74 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 ++seg;
             }
-            if (!ok && leader) {
+            if (!ok && (leader || F8)) {
                 // Unwind: let every copy still in flight land before the CTA exits
-                // (the even CTA's full barriers count both halves).
+                // (the even CTA's full barriers count both halves; F8 staging
+                // copies complete on each CTA's own barriers).
                 for (int i = 0; i < rg.count; ++i) {
                     const uint32_t fills =
                         rg.n > (uint32_t)i ? (rg.n - i + rg.count - 1) / rg.count : 0;
-                    if (fills) drain_wait(bar_full(s_bars, rg.first + i), (fills - 1) & 1u);
+                    if (fills)
+                        drain_wait(F8 ? BR.stg_full(rg.first + i) : BR.full(rg.first + i),
+                                   (fills - 1) & 1u);
                 }
-                if (kq && seg > 0) drain_wait(bar_qfull(s_bars), (seg - 1) & 1);
+                if (kq && seg > 0 && leader) drain_wait(BR.qfull(), (seg - 1) & 1);
+            }
+        }
+    } else if (F8 && (warp == V_WARP + 1 || warp == V_WARP + 2)) {
+        // ------------------------------------------------------------ converters (F8)
+        // Warp V_WARP + 1 converts K, V_WARP + 2 V: for every ring slot, in
+        // the order the producer filled the staging slots, wait for the codes
+        // and for the fp16 slot to be free (its UMMAs done), write the fp16
+        // values exactly where the fp16 path's TMA would have put them
+        // (128-byte-swizzled rows), make them visible to the tensor cores'
+        // async proxy, free the staging slot and arrive (cluster scope) on the
+        // even CTA's full barrier.  E4M3 -> fp16 is exact.
+        const bool kc = warp == V_WARP + 1;
+        Ring sg{kc ? 0 : NSK, kc ? NSK : NSV, 0u};
+        Ring rg{kc ? 0 : NK, kc ? NK : NV, 0u};
+        // Staging rows: K 64 keys x 128 codes; V (BN / SLOTS) keys x DH / 2 codes.
+        const int rb = kc ? 128 : DH / 2;            // code bytes per staging row
+        const int cpr = rb / 16;                     // 16-code chunks per row
+        const int rpi = 32 / cpr;                    // rows per warp pass
+        const int rows = kc ? 64 : BN / SLOTS;
+        bool ok = true;
+        while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
+            for (int j = jb; ok && j < je; ++j) {
+                for (int h = 0; h < SLOTS && ok; ++h) {
+                    const int ss = sg.slot(), fs = rg.slot();
+                    ok = mbar_wait(BR.stg_full(ss), sg.phase(), abort_flag, P.err);
+                    if (ok) ok = mbar_wait(BR.empty(fs), rg.phase() ^ 1u, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    const uint8_t* src = base_ptr + RING_BYTES + ss * STG_SLOT;
+                    uint8_t* dst = base_ptr + fs * SLOT_BYTES;
+                    for (int r0 = 0; r0 < rows; r0 += rpi) {
+                        const int r = r0 + lane / cpr, c = lane % cpr;   // 16 codes: d 16c ..
+                        uint4 lo, hi;
+                        e4m3x16_f16(*reinterpret_cast<const uint4*>(src + r * rb + c * 16), lo, hi);
+                        uint32_t o;
+                        if (kc) {
+                            // K slot: chunk c / 4 (64 d) of HALF_SLOT, row r, units 2 (c % 4) ..
+                            o = (uint32_t)((c >> 2) * HALF_SLOT + r * 128);
+                        } else {
+                            // V slot: sub-tile r / 32, atom c / 4 (64 d), row r % 32
+                            o = (uint32_t)((r >> 5) * SUB_BYTES + (c >> 2) * 4096 + (r & 31) * 128);
+                        }
+                        const uint32_t u0 = 2u * (uint32_t)(c & 3), sw = (uint32_t)(r & 7);
+                        *reinterpret_cast<uint4*>(dst + o + ((u0 ^ sw) << 4)) = lo;
+                        *reinterpret_cast<uint4*>(dst + o + (((u0 + 1) ^ sw) << 4)) = hi;
+                    }
+                    asm volatile("fence.proxy.async;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(BR.stg_empty(ss, NSTG));
+                        if (leader) arrive_cl_local(BR.full(fs));
+                        else arrive_cl_remote(leader_addr(BR.full(fs)));
+                    }
+                    ++sg.n;
+                    ++rg.n;
+                }
             }
         }
     } else if (warp == 1) {
@@ -491,9 +684,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // async-proxy operations ordered by the mbarrier's completion, so no
             // tcgen05 fence is needed here (the issuing thread's time between
             // UMMAs is what keeps the tensor pipe fed).
+            // F8: the slots were filled by generic stores of both CTAs' converter
+            // warps, which arrive with cluster-scope release; acquire at cluster
+            // scope to match.
             auto take = [&](Ring& rg, int& slot) -> bool {
                 slot = rg.slot();
-                return mbar_wait(bar_full(s_bars, slot), rg.phase(), abort_flag, P.err);
+                if constexpr (F8) return mbar_wait_cl(BR.full(slot), rg.phase(), abort_flag, P.err);
+                return mbar_wait(BR.full(slot), rg.phase(), abort_flag, P.err);
             };
             // Non-blocking look at the ring position after the current one; its
             // latency overlaps the current slot's UMMA issue, and a slot found
@@ -501,7 +698,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto peek_next = [&](const Ring& rg) -> bool {
                 Ring nx = rg;
                 ++nx.n;
-                return mbar_test(bar_full(s_bars, nx.slot()), nx.phase());
+                if constexpr (F8) return mbar_test_cl(BR.full(nx.slot()), nx.phase());
+                return mbar_test(BR.full(nx.slot()), nx.phase());
             };
             // Descriptor low words: Q chunk c at q_lo + c * (BM * 128 >> 4); a K
             // slot's chunk cc at + cc * (HALF_SLOT >> 4); a K step of 16
@@ -529,7 +727,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 umma_ss_pair_c<true>(d, a, b, IDESC_QK);
                         }
                     }
-                    umma_commit_pair(bar_empty(s_bars, slot));
+                    umma_commit_pair(BR.empty(slot));
                     ++kr.n;
                 }
                 return true;
@@ -560,45 +758,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 umma_ts_pair_c<true>(tmem + O_COL, a_tmem, b, IDESC_PV);
                         }
                     }
-                    umma_commit_pair(bar_empty(s_bars, slot));
+                    umma_commit_pair(BR.empty(slot));
                     ++vr.n;
                 }
                 return true;
             };
             while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
-                if (!mbar_wait(bar_qfull(s_bars), seg & 1, abort_flag, P.err)) {
+                if (!mbar_wait(BR.qfull(), seg & 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 ok = issue_qk(S_COL0 + (g & 1) * BN);
                 if (!ok) break;
-                umma_commit_pair(bar_sfull(s_bars, g & 1));
-                if (je - jb == 1) umma_commit_pair(bar_qempty(s_bars));
+                umma_commit_pair(BR.sfull(g & 1));
+                if (je - jb == 1) umma_commit_pair(BR.qempty());
                 for (int j = jb; j < je; ++j) {
                     const uint32_t gg = g + (j - jb);
                     if (j + 1 < je) {
                         ok = issue_qk(S_COL0 + ((gg + 1) & 1) * BN);
                         if (!ok) break;
-                        umma_commit_pair(bar_sfull(s_bars, (gg + 1) & 1));
-                        if (j + 1 == je - 1) umma_commit_pair(bar_qempty(s_bars));
+                        umma_commit_pair(BR.sfull((gg + 1) & 1));
+                        if (j + 1 == je - 1) umma_commit_pair(BR.qempty());
                     }
-                    if (!mbar_wait(bar_pfull(s_bars, gg & 1), (gg >> 1) & 1, abort_flag, P.err)) {
+                    if (!mbar_wait(BR.pfull(gg & 1), (gg >> 1) & 1, abort_flag, P.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     ok = issue_pv(S_COL0 + (gg & 1) * BN, j > jb);
                     if (!ok) break;
-                    umma_commit_pair(bar_ofull(s_bars));
+                    umma_commit_pair(BR.ofull());
                 }
                 g += je - jb;
                 ++seg;
             }
             if (!ok) {
                 // Unwind: wait for every UMMA already issued before TMEM is freed.
-                umma_commit_pair(bar_drain(s_bars));
-                drain_wait(bar_drain(s_bars), 0);
+                umma_commit_pair(BR.drain());
+                drain_wait(BR.drain(), 0);
             }
         }
     } else if (warp < V_WARP) {
@@ -613,9 +811,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int row = wq * 32 + lane;    // tile row == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
         float* xl = xch + 2 * NWG * BM;    // row-sum parts [hg][row]
-        const uint32_t gbar = bar_group(s_bars);
+        const uint32_t gbar = BR.group();
         uint32_t gphase = 0;
-        const float sl2 = P.scale_log2;
+        // F8: the K scale joins the score scale; the V scale multiplies O.
+        const float sl2 = F8 ? P.scale_log2 * __ldg(P.kscale) : P.scale_log2;
+        const float vsc = F8 ? __ldg(P.vscale) : 1.0f;
         uint32_t g = 0;
         bool ok = true;
         while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
@@ -628,7 +828,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int j = jb; j < je; ++j) {
                 const uint32_t gg = g + (j - jb);
                 const uint32_t s_col = S_COL0 + (gg & 1) * BN;
-                ok = mbar_wait(bar_sfull(s_bars, gg & 1), (gg >> 1) & 1, abort_flag, P.err);
+                ok = mbar_wait(BR.sfull(gg & 1), (gg >> 1) & 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -673,7 +873,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 } else {
                     const bool need = mx > m_ref + RESCALE_THRESHOLD;
                     if (__any_sync(0xffffffffu, need)) {
-                        ok = mbar_wait(bar_ofull(s_bars), (gg - 1) & 1, abort_flag, P.err);
+                        ok = mbar_wait(BR.ofull(), (gg - 1) & 1, abort_flag, P.err);
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                         tc_fence_after();
@@ -718,21 +918,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 l += (l0 + l1) + (l2 + l3);
                 tmem_st_wait();
                 if (j > jb && !o_seen) {
-                    ok = mbar_wait(bar_ofull(s_bars), (gg - 1) & 1, abort_flag, P.err);
+                    ok = mbar_wait(BR.ofull(), (gg - 1) & 1, abort_flag, P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if (leader) mbar_arrive(bar_pfull(s_bars, gg & 1));
-                    else remote_arrive(leader_addr(bar_pfull(s_bars, gg & 1)));
+                    if (leader) mbar_arrive(BR.pfull(gg & 1));
+                    else remote_arrive(leader_addr(BR.pfull(gg & 1)));
                 }
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
             const uint32_t gl = g + (je - jb) - 1;
-            ok = mbar_wait(bar_ofull(s_bars), gl & 1, abort_flag, P.err);
+            ok = mbar_wait(BR.ofull(), gl & 1, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -745,7 +945,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int h = 1; h < NWG; ++h) l_row += xl[h * BM + row];
             if (jb == 0 && je == n) {
-                const float inv = (l_row > 0.f) ? 1.0f / l_row : 0.f;
+                const float inv = (l_row > 0.f) ? vsc / l_row : 0.f;
                 uint4* dst = reinterpret_cast<uint4*>(P.out + (MH ? (size_t)hd * DH : 0) + (size_t)m_row * P.out_stride + OCOLS * hg);
 #pragma unroll 1
                 for (int c = 0; c < OCOLS / 32; ++c) {
@@ -773,6 +973,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     uint32_t o[32];
                     tmem_ld32(t_lane + O_COL + OCOLS * hg + 32 * c, o);
                     tmem_ld_wait<32>(o);
+                    if (F8) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * vsc);
+                    }
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[c * 8 + e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
@@ -888,8 +1093,8 @@ static int max_pairs(int device) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(NTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.blockDim = dim3(Cfg<false>::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<false>::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -898,8 +1103,9 @@ static int max_pairs(int device) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    // All instantiations have the same threads, shared memory and clusters.
-    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<false, 256>, &cfg) != cudaSuccess ||
+    // All instantiations use one CTA per SM (their shared memory allows no
+    // second), so the fp16 kernel's count holds for all.
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<false, 256, false>, &cfg) != cudaSuccess ||
         n < 1) {
         cudaGetLastError();
         return 0;
@@ -910,13 +1116,14 @@ static int max_pairs(int device) {
 }
 
 // One main-kernel launch and, when pair tiles were cut, its merge.
-template <bool MH, int DH>
+template <bool MH, int DH, bool F8>
 static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Params& P, const MergeTasks& tasks, cudaStream_t stream) {
-    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<MH, DH>), SMEM_BYTES) !=
-        GQA_OK)
+    using C = Cfg<F8>;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<MH, DH, F8>),
+                          C::SMEM_BYTES) != GQA_OK)
         return GQA_ERR_CUDA;
-    prefill_kernel<MH, DH><<<2 * P.G, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, P);
+    prefill_kernel<MH, DH, F8><<<2 * P.G, C::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, P);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     if (tasks.n > 0) {
         cudaLaunchConfig_t cfg = {};
@@ -940,8 +1147,8 @@ static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 int prefill_resident_pairs() {
     const DeviceInfo* di = device_info();
     if (!di) return -1;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<false, 256>),
-                          prefill::SMEM_BYTES) != GQA_OK)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<false, 256, false>),
+                          prefill::Cfg<false>::SMEM_BYTES) != GQA_OK)
         return -1;
     return prefill::max_pairs(di->device);
 }
@@ -954,13 +1161,15 @@ size_t prefill_workspace_bytes(int Q, int KV, int num_sms) {
     return kWorkspaceCounterBytes + per_pair * pairs + 256;
 }
 
-int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q, int KV,
-                   int Hq, int Hkv, int Dh, float scale, cudaStream_t stream) {
+int prefill_launch(const void* q, const void* k, const void* v, const float* kscale,
+                   const float* vscale, void* out, int Q, int KV, int Hq, int Hkv, int Dh,
+                   float scale, cudaStream_t stream) {
     using namespace prefill;
     const DeviceInfo* di = device_info();
     if (!di) return GQA_ERR_CUDA;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<false, 256>), SMEM_BYTES) !=
-        GQA_OK)
+    const bool f8 = kscale != nullptr;   // K / V are E4M3 codes with device-side scales
+    if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<false, 256, false>),
+                          Cfg<false>::SMEM_BYTES) != GQA_OK)
         return GQA_ERR_CUDA;
     const int pairs_max = max_pairs(di->device);
     if (pairs_max < 1) return GQA_ERR_CUDA;
@@ -988,6 +1197,8 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     if (G < 1) G = 1;
     P.G = (int)(total < G ? total : G);
     P.scale_log2 = scale * 1.4426950408889634f;
+    P.kscale = kscale;
+    P.vscale = vscale;
     P.err = di->err_word;
     P.out = static_cast<__half*>(out);
 
@@ -1008,24 +1219,44 @@ int prefill_launch(const void* q, const void* k, const void* v, void* out, int Q
     find_cut_tiles(P, tasks);
 
     CUtensorMap tq, tk, tv;
+    // E4M3 code maps (unswizzled staging rows): K boxes of 128 codes x 64 keys,
+    // V boxes of Dh / 2 codes x (128 / (Dh / 128)) keys, one KV head per box.
+    auto code_maps = [&](bool three_d) -> bool {
+        const uint32_t v_rows = (uint32_t)(BN / (Dh / 128));
+        return make_map_u8_plain(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, (uint64_t)Dh,
+                                 (uint64_t)Hkv * Dh, 128, 64, three_d) &&
+               make_map_u8_plain(&tv, v, Dh, (uint64_t)Hkv, (uint64_t)KV, (uint64_t)Dh,
+                                 (uint64_t)Hkv * Dh, (uint32_t)(Dh / 2), v_rows, three_d);
+    };
     if (packed) {
-        if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, Dh, Dh, BM, 64) ||
-            !make_map_2d_f16(&tk, k, (uint64_t)KV, Dh, Dh, BN / 2, 64) ||
+        if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, Dh, Dh, BM, 64)) return GQA_ERR_CUDA;
+        if (f8) {
+            if (!code_maps(false)) return GQA_ERR_CUDA;
+            return Dh == 256 ? launch_one<false, 256, true>(tq, tk, tv, P, tasks, stream)
+                             : launch_one<false, 128, true>(tq, tk, tv, P, tasks, stream);
+        }
+        if (!make_map_2d_f16(&tk, k, (uint64_t)KV, Dh, Dh, BN / 2, 64) ||
             !make_map_2d_f16(&tv, v, (uint64_t)KV, Dh, Dh, 32, 64))
             return GQA_ERR_CUDA;
-        return Dh == 256 ? launch_one<false, 256>(tq, tk, tv, P, tasks, stream)
-                         : launch_one<false, 128>(tq, tk, tv, P, tasks, stream);
+        return Dh == 256 ? launch_one<false, 256, false>(tq, tk, tv, P, tasks, stream)
+                         : launch_one<false, 128, false>(tq, tk, tv, P, tasks, stream);
     }
     const uint64_t row_bytes = 2ull * Dh;
     if (!make_map_3d_f16(&tq, q, Dh, (uint64_t)Hq, (uint64_t)Q, row_bytes,
-                         (uint64_t)Hq * row_bytes, BM) ||
-        !make_map_3d_f16(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
+                         (uint64_t)Hq * row_bytes, BM))
+        return GQA_ERR_CUDA;
+    if (f8) {
+        if (!code_maps(true)) return GQA_ERR_CUDA;
+        return Dh == 256 ? launch_one<true, 256, true>(tq, tk, tv, P, tasks, stream)
+                         : launch_one<true, 128, true>(tq, tk, tv, P, tasks, stream);
+    }
+    if (!make_map_3d_f16(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
                          (uint64_t)Hkv * row_bytes, BN / 2) ||
         !make_map_3d_f16(&tv, v, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
                          (uint64_t)Hkv * row_bytes, 32))
         return GQA_ERR_CUDA;
-    return Dh == 256 ? launch_one<true, 256>(tq, tk, tv, P, tasks, stream)
-                     : launch_one<true, 128>(tq, tk, tv, P, tasks, stream);
+    return Dh == 256 ? launch_one<true, 256, false>(tq, tk, tv, P, tasks, stream)
+                     : launch_one<true, 128, false>(tq, tk, tv, P, tasks, stream);
 }
 
 }  // namespace gqa

@@ -156,3 +156,17 @@ def test_oracle_is_not_imported_by_the_product_path():
                 text = open(os.path.join(dirpath, f), errors="ignore").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "gqa_oracle" not in text and "liboracle" not in text, f
+
+
+def _prefill8(lib, Q=8, KV=16, D=256, Hq=6, Hkv=1, ks=FAKE, scale=0.0625):
+    return lib.gqa_attn_prefill_e4m3(FAKE, FAKE, FAKE, ks, FAKE, FAKE, Q, KV, Hq, Hkv, D, scale,
+                                     None)
+
+
+def test_prefill_e4m3_rejects_bad_arguments(lib):
+    assert _prefill8(lib, ks=P(0)) == binding.GQA_ERR_INVALID_ARG
+    assert _prefill8(lib, ks=P(0x10002)) == binding.GQA_ERR_INVALID_ARG   # not 4-byte aligned
+    assert _prefill8(lib, Q=17, KV=16) == binding.GQA_ERR_INVALID_ARG
+    assert _prefill8(lib, scale=0.0) == binding.GQA_ERR_INVALID_ARG
+    assert _prefill8(lib, D=64) == binding.GQA_ERR_UNSUPPORTED     # 128 and 256 are accepted
+    assert _prefill8(lib, Hq=6, Hkv=4) == binding.GQA_ERR_UNSUPPORTED
