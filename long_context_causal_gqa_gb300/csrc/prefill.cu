@@ -84,9 +84,11 @@ constexpr int XCH_BYTES = 3 * NWG * BM * 4;  // part maxima [parity][part][row],
 constexpr int STG_SLOT = 8192;
 
 // Per-variant sizes.  F8 (K and V stored as FP8-E4M3 codes): each CTA's TMA
-// brings its codes into staging slots, and two converter warps (one for K,
-// one for V) write them as fp16 into the ring slots the UMMAs read; the fp16
-// ring shrinks to make room for the staging ring.
+// brings its codes into staging slots, and four converter warps (two for K,
+// two for V, each half of a slot) write them as fp16 into the ring slots the
+// UMMAs read; the fp16 ring shrinks to make room for the staging ring.  Up to
+// 16 warps share the same register limit (128 per thread at 4 warps per
+// scheduler), so the converters cost no registers beyond 13 warps.
 // Barriers: ring full/empty, q full/empty, s[2], p[2], o, drain, group, then
 // staging full/empty (F8).
 template <bool F8>
@@ -100,7 +102,8 @@ struct Cfg {
     static constexpr int RING_BYTES = NRING * SLOT_BYTES;
     static constexpr int STG_BYTES = NSTG * STG_SLOT;
     static constexpr int NUM_BARS = 2 * NRING + 9 + 2 * NSTG;
-    static constexpr int NTHREADS = 64 + NSOFT + 32 + (F8 ? 64 : 0);
+    static constexpr int NCONV = F8 ? 4 : 0;              // converter warps: 2 for K, 2 for V
+    static constexpr int NTHREADS = 64 + NSOFT + 32 + 32 * NCONV;
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + STG_BYTES + Q_BYTES +
                                       XCH_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -479,13 +482,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < NRING; ++s) {
             // fp16 path: one arrival (with the pair's transaction bytes); F8: one
-            // arrival per CTA's converter warp.
-            mbar_init(BR.full(s), F8 ? 2 : 1);
+            // arrival per converter warp of the role in either CTA.
+            mbar_init(BR.full(s), F8 ? 4 : 1);
             mbar_init(BR.empty(s), 1);
         }
         for (int s = 0; s < NSTG; ++s) {
             mbar_init(BR.stg_full(s), 1);
-            mbar_init(BR.stg_empty(s, NSTG), 1);
+            mbar_init(BR.stg_empty(s, NSTG), 2);   // both converter warps of the role
         }
         mbar_init(BR.qfull(), 1);
         mbar_init(BR.qempty(), 1);
@@ -617,23 +620,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (kq && seg > 0 && leader) drain_wait(BR.qfull(), (seg - 1) & 1);
             }
         }
-    } else if (F8 && (warp == V_WARP + 1 || warp == V_WARP + 2)) {
+    } else if (F8 && warp > V_WARP) {
         // ------------------------------------------------------------ converters (F8)
-        // Warp V_WARP + 1 converts K, V_WARP + 2 V: for every ring slot, in
-        // the order the producer filled the staging slots, wait for the codes
-        // and for the fp16 slot to be free (its UMMAs done), write the fp16
-        // values exactly where the fp16 path's TMA would have put them
-        // (128-byte-swizzled rows), make them visible to the tensor cores'
-        // async proxy, free the staging slot and arrive (cluster scope) on the
-        // even CTA's full barrier.  E4M3 -> fp16 is exact.
-        const bool kc = warp == V_WARP + 1;
+        // Warps V_WARP + 1, + 2 convert K, V_WARP + 3, + 4 V, each half of
+        // every slot: in the order the producer filled the staging slots, wait
+        // for the codes and for the fp16 slot to be free (its UMMAs done),
+        // write the fp16 values exactly where the fp16 path's TMA would have
+        // put them (128-byte-swizzled rows), make them visible to the tensor
+        // cores' async proxy, free the staging slot and arrive (cluster scope)
+        // on the even CTA's full barrier.  E4M3 -> fp16 is exact.  All eight
+        // 16-byte code loads of a lane are issued before the first conversion.
+        const int cw = warp - V_WARP - 1;           // 0..3
+        const bool kc = cw < 2;
+        const int part = cw & 1;                    // which half of the slot's rows
         Ring sg{kc ? 0 : NSK, kc ? NSK : NSV, 0u};
         Ring rg{kc ? 0 : NK, kc ? NK : NV, 0u};
         // Staging rows: K 64 keys x 128 codes; V (BN / SLOTS) keys x DH / 2 codes.
-        const int rb = kc ? 128 : DH / 2;            // code bytes per staging row
-        const int cpr = rb / 16;                     // 16-code chunks per row
-        const int rpi = 32 / cpr;                    // rows per warp pass
-        const int rows = kc ? 64 : BN / SLOTS;
+        constexpr int RBV = DH / 2;                 // V code bytes per staging row
+        constexpr int RPIK = 32 / (128 / 16);       // K rows per warp pass (4)
+        constexpr int RPIV = 32 / (RBV / 16);       // V rows per warp pass (4 or 8)
+        constexpr int PASSES = 8;                   // passes per warp per slot (half a slot)
+        static_assert(64 / 2 == RPIK * PASSES && (BN / SLOTS) / 2 == RPIV * PASSES, "passes");
+        const int rb = kc ? 128 : RBV;
+        const int cpr = rb / 16;                    // 16-code chunks per row
+        const int rpi = kc ? RPIK : RPIV;
+        const int rbase = part * rpi * PASSES + lane / cpr;
+        const int c = lane % cpr;                   // 16 codes: d 16c .. 16c + 15 of the row
         bool ok = true;
         while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
             for (int j = jb; ok && j < je; ++j) {
@@ -645,18 +657,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (!ok) break;
                     const uint8_t* src = base_ptr + RING_BYTES + ss * STG_SLOT;
                     uint8_t* dst = base_ptr + fs * SLOT_BYTES;
-                    for (int r0 = 0; r0 < rows; r0 += rpi) {
-                        const int r = r0 + lane / cpr, c = lane % cpr;   // 16 codes: d 16c ..
+                    uint4 code[PASSES];
+#pragma unroll
+                    for (int i = 0; i < PASSES; ++i)
+                        code[i] = *reinterpret_cast<const uint4*>(src + (rbase + i * rpi) * rb +
+                                                                  c * 16);
+#pragma unroll
+                    for (int i = 0; i < PASSES; ++i) {
+                        const int r = rbase + i * rpi;
                         uint4 lo, hi;
-                        e4m3x16_f16(*reinterpret_cast<const uint4*>(src + r * rb + c * 16), lo, hi);
-                        uint32_t o;
-                        if (kc) {
-                            // K slot: chunk c / 4 (64 d) of HALF_SLOT, row r, units 2 (c % 4) ..
-                            o = (uint32_t)((c >> 2) * HALF_SLOT + r * 128);
-                        } else {
-                            // V slot: sub-tile r / 32, atom c / 4 (64 d), row r % 32
-                            o = (uint32_t)((r >> 5) * SUB_BYTES + (c >> 2) * 4096 + (r & 31) * 128);
-                        }
+                        e4m3x16_f16(code[i], lo, hi);
+                        // K slot: chunk c / 4 (64 d) of HALF_SLOT, row r; V slot:
+                        // sub-tile r / 32, atom c / 4 (64 d), row r % 32.
+                        const uint32_t o =
+                            kc ? (uint32_t)((c >> 2) * HALF_SLOT + r * 128)
+                               : (uint32_t)((r >> 5) * SUB_BYTES + (c >> 2) * 4096 + (r & 31) * 128);
                         const uint32_t u0 = 2u * (uint32_t)(c & 3), sw = (uint32_t)(r & 7);
                         *reinterpret_cast<uint4*>(dst + o + ((u0 ^ sw) << 4)) = lo;
                         *reinterpret_cast<uint4*>(dst + o + (((u0 + 1) ^ sw) << 4)) = hi;
