@@ -676,7 +676,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         *reinterpret_cast<uint4*>(dst + o + ((u0 ^ sw) << 4)) = lo;
                         *reinterpret_cast<uint4*>(dst + o + (((u0 + 1) ^ sw) << 4)) = hi;
                     }
-                    asm volatile("fence.proxy.async;" ::: "memory");
+                    // Order the generic stores before the tensor cores' reads of this
+                    // CTA's shared memory (reached through the cluster window by the
+                    // even CTA's UMMAs); a shared-memory-only proxy fence.
+                    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(BR.stg_empty(ss, NSTG));
