@@ -80,32 +80,32 @@ constexpr int COLS = BN / NWG;                // S columns per softmax thread
 constexpr int NSOFT = 128 * NWG;              // softmax threads per CTA
 constexpr int V_WARP = 2 + NSOFT / 32;
 constexpr int XCH_BYTES = 3 * NWG * BM * 4;  // part maxima [parity][part][row], sums [part][row]
-// E4M3 codes of one fp16 ring slot for this CTA (8 KB), as two boxes of half
-// the slot's rows, one per converter warp.
-constexpr int CODE_BYTES = 8192;
+// E4M3 staging slot: this CTA's codes of one fp16 ring slot (8 KB).
+constexpr int STG_SLOT = 8192;
 
 // Per-variant sizes.  F8 (K and V stored as FP8-E4M3 codes): each CTA's TMA
-// brings its codes straight into the ring slot they will become (8 of its 16
-// KB), and four converter warps (two for K, two for V) rewrite each slot in
-// place as the fp16 rows the UMMAs read: warp `part` of a role owns half of
-// the slot's rows, and its codes are placed inside the bytes it writes
-// itself, so a warp that holds all its codes in registers before writing
-// needs no other warp.  The ring is the fp16 path's.  Up to 16 warps share the
-// same register limit (128 per thread at 4 warps per scheduler), so the
-// converters cost no registers beyond 13 warps.
+// brings its codes into staging slots, and four converter warps (two for K,
+// two for V, each half of a slot) write them as fp16 into the ring slots the
+// UMMAs read; the fp16 ring shrinks to make room for the staging ring.  Up to
+// 16 warps share the same register limit (128 per thread at 4 warps per
+// scheduler), so the converters cost no registers beyond 13 warps.
 // Barriers: ring full/empty, q full/empty, s[2], p[2], o, drain, group, then
-// (F8) one codes-landed barrier per ring slot.
+// staging full/empty (F8).
 template <bool F8>
 struct Cfg {
-    static constexpr int NK = GQA_PREFILL_NK;            // K slots (DH / 128 per tile)
-    static constexpr int NV = GQA_PREFILL_NV;            // V slots (DH / 128 per tile)
+    static constexpr int NK = F8 ? 3 : GQA_PREFILL_NK;   // K slots (DH / 128 per tile)
+    static constexpr int NV = F8 ? 3 : GQA_PREFILL_NV;   // V slots (DH / 128 per tile)
     static constexpr int NRING = NK + NV;
+    static constexpr int NSK = F8 ? 3 : 0;               // K staging slots
+    static constexpr int NSV = F8 ? 3 : 0;               // V staging slots
+    static constexpr int NSTG = NSK + NSV;
     static constexpr int RING_BYTES = NRING * SLOT_BYTES;
-    static constexpr int NUM_BARS = 2 * NRING + 9 + (F8 ? NRING : 0);
+    static constexpr int STG_BYTES = NSTG * STG_SLOT;
+    static constexpr int NUM_BARS = 2 * NRING + 9 + 2 * NSTG;
     static constexpr int NCONV = F8 ? 4 : 0;              // converter warps: 2 for K, 2 for V
     static constexpr int NTHREADS = 64 + NSOFT + 32 + 32 * NCONV;
-    static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + RING_BYTES + Q_BYTES + XCH_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + STG_BYTES + Q_BYTES +
+                                      XCH_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 constexpr uint32_t TMEM_COLS = 512;
@@ -214,7 +214,8 @@ struct Bars {
     __device__ uint32_t ofull() const { return b + 8 * (2 * NR + 6); }
     __device__ uint32_t drain() const { return b + 8 * (2 * NR + 7); }
     __device__ uint32_t group() const { return b + 8 * (2 * NR + 8); }
-    __device__ uint32_t code_full(int s) const { return b + 8 * (2 * NR + 9 + s); }
+    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 9 + i); }
+    __device__ uint32_t stg_empty(int i, int ns) const { return b + 8 * (2 * NR + 9 + ns + i); }
 };
 
 // One ring (K or V) seen by its producer and by the UMMA issuer: slot
@@ -455,27 +456,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr int OCOLS = DH / NWG;                 // O columns per softmax thread
     constexpr uint32_t IDESC_PV = idesc_f16_f32(256, DH, false, true);
     using C = Cfg<F8>;
-    constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING;
-    constexpr int RING_BYTES = C::RING_BYTES, NUM_BARS = C::NUM_BARS;
-    // F8: where a slot's two code boxes (rows of half `part`) land inside it,
-    // within the bytes that part's converter warp writes: K slot chunk c
-    // (64 d) of half p occupies c * HALF_SLOT + p * 4096 (rows 32p .. 32p + 31),
-    // so half p's codes go to HALF_SLOT + 4096 p; a V slot's half p of the
-    // rows is its bytes [8192 p, 8192 p + 8192), and its codes go to the upper
-    // 4 KB of that.
-    auto k_code_off = [](int part) { return HALF_SLOT + 4096 * part; };
-    auto v_code_off = [](int part) { return 4096 + HALF_SLOT * part; };
+    constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING, NSK = C::NSK, NSV = C::NSV;
+    constexpr int NSTG = C::NSTG;
+    constexpr int RING_BYTES = C::RING_BYTES, STG_BYTES = C::STG_BYTES, NUM_BARS = C::NUM_BARS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
-    // Layout: ring | Q | exchange | barriers | tmem address.
+    // Layout: fp16 ring | E4M3 staging (F8) | Q | exchange | barriers | tmem address.
     const uint32_t s_ring = base;
-    const uint32_t s_q = base + RING_BYTES;
+    const uint32_t s_stg = base + RING_BYTES;
+    const uint32_t s_q = s_stg + STG_BYTES;
     const uint32_t s_bars = s_q + Q_BYTES + XCH_BYTES;
     const Bars<NRING> BR{s_bars};
-    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + Q_BYTES);
-    uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + Q_BYTES +
-                                                          XCH_BYTES + NUM_BARS * 8);
+    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + STG_BYTES + Q_BYTES);
+    uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + STG_BYTES +
+                                                          Q_BYTES + XCH_BYTES + NUM_BARS * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_ptr + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -491,8 +486,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(BR.full(s), F8 ? 4 : 1);
             mbar_init(BR.empty(s), 1);
         }
-        if (F8)
-            for (int s = 0; s < NRING; ++s) mbar_init(BR.code_full(s), 1);
+        for (int s = 0; s < NSTG; ++s) {
+            mbar_init(BR.stg_full(s), 1);
+            mbar_init(BR.stg_empty(s, NSTG), 2);   // both converter warps of the role
+        }
         mbar_init(BR.qfull(), 1);
         mbar_init(BR.qempty(), 1);
         for (int i = 0; i < 2; ++i) {
@@ -532,26 +529,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // ------------------------------------------------------------ producers
         // Warp 0: Q and K; warp V_WARP: V.  Each loads this CTA's half of
         // every operand; completions land on the even CTA's full barriers,
-        // whose transaction count the even CTA sets for both halves.  F8: the
-        // K / V codes go into the slot itself (two unswizzled boxes of half the
-        // rows), completing on this CTA's own codes-landed barrier for the
-        // converter warps.
+        // whose transaction count the even CTA sets for both halves.  F8: K / V
+        // codes go to this CTA's own staging slots (8 KB each, unswizzled rows),
+        // completing on its own staging barriers, for the converter warps.
         if (lane == 0) {
             const bool kq = warp == 0;
-            Ring rg{kq ? 0 : NK, kq ? NK : NV, 0u};
+            Ring rg = F8 ? Ring{kq ? 0 : NSK, kq ? NSK : NSV, 0u}
+                         : Ring{kq ? 0 : NK, kq ? NK : NV, 0u};
             int seg = 0;
             bool ok = true;
             // Acquire the next slot of this ring; returns its full barrier.
             auto acquire = [&](uint32_t& dst, uint32_t& fb) -> bool {
                 const int slot = rg.slot();
+                if constexpr (F8) {
+                    if (!mbar_wait(BR.stg_empty(slot, NSTG), rg.phase() ^ 1u, abort_flag, P.err))
+                        return false;
+                    dst = s_stg + slot * STG_SLOT;
+                    fb = BR.stg_full(slot);
+                    mbar_arrive_expect_tx(fb, STG_SLOT);
+                    return true;
+                }
                 if (!mbar_wait(BR.empty(slot), rg.phase() ^ 1u, abort_flag, P.err))
                     return false;
                 dst = s_ring + slot * SLOT_BYTES;
-                if constexpr (F8) {
-                    fb = BR.code_full(slot);
-                    mbar_arrive_expect_tx(fb, CODE_BYTES);
-                    return true;
-                }
                 fb = BR.full(slot);
                 if (leader) mbar_arrive_expect_tx(fb, 2 * SLOT_BYTES);
                 fb = leader_addr(fb);
@@ -578,19 +578,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             break;
                         }
                         if (F8) {
-                            // Codes of the same keys and d, half the rows per box: K,
-                            // this CTA's 64 keys x d 128 h .. 128 h + 127; V, keys
-                            // (BN / SLOTS) h .. + BN / SLOTS - 1 x this CTA's DH / 2 d.
-                            for (int part = 0; part < 2; ++part) {
-                                if (kq)
-                                    tma_load_self<MH>(dst + k_code_off(part), &tm_k, fb, 128 * h,
-                                                      kvh, j * BN + 64 * (int)rank + 32 * part);
-                                else
-                                    tma_load_self<MH>(dst + v_code_off(part), &tm_v, fb,
-                                                      (DH / 2) * (int)rank, kvh,
-                                                      j * BN + h * (BN / SLOTS) +
-                                                          part * (BN / SLOTS / 2));
-                            }
+                            // Codes of the same keys and d: K, this CTA's 64 keys x
+                            // d 128 h .. 128 h + 127; V, keys (BN / SLOTS) h ..
+                            // + BN / SLOTS - 1 x this CTA's DH / 2 d.
+                            if (kq)
+                                tma_load_self<MH>(dst, &tm_k, fb, 128 * h, kvh,
+                                                  j * BN + 64 * (int)rank);
+                            else
+                                tma_load_self<MH>(dst, &tm_v, fb, (DH / 2) * (int)rank, kvh,
+                                                  j * BN + h * (BN / SLOTS));
                         } else if (kq) {
                             // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
                             for (int cc = 0; cc < 2; ++cc)
@@ -618,7 +614,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const uint32_t fills =
                         rg.n > (uint32_t)i ? (rg.n - i + rg.count - 1) / rg.count : 0;
                     if (fills)
-                        drain_wait(F8 ? BR.code_full(rg.first + i) : BR.full(rg.first + i),
+                        drain_wait(F8 ? BR.stg_full(rg.first + i) : BR.full(rg.first + i),
                                    (fills - 1) & 1u);
                 }
                 if (kq && seg > 0 && leader) drain_wait(BR.qfull(), (seg - 1) & 1);
@@ -626,20 +622,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else if (F8 && warp > V_WARP) {
         // ------------------------------------------------------------ converters (F8)
-        // Warps V_WARP + 1, + 2 convert K, V_WARP + 3, + 4 V; warp `part` of a
-        // role owns half of every slot's rows.  In the order the producer
-        // filled the slots, it waits for its CTA's codes, loads all of its own
-        // (eight 16-byte chunks per lane), then writes the fp16 values exactly
-        // where the fp16 path's TMA would have put them (128-byte-swizzled
-        // rows) -- over its own codes only -- makes them visible to the tensor
-        // cores' async proxy and arrives (cluster scope) on the even CTA's full
-        // barrier.  E4M3 -> fp16 is exact.
+        // Warps V_WARP + 1, + 2 convert K, V_WARP + 3, + 4 V, each half of
+        // every slot: in the order the producer filled the staging slots, wait
+        // for the codes and for the fp16 slot to be free (its UMMAs done),
+        // write the fp16 values exactly where the fp16 path's TMA would have
+        // put them (128-byte-swizzled rows), make them visible to the tensor
+        // cores' async proxy, free the staging slot and arrive (cluster scope)
+        // on the even CTA's full barrier.  E4M3 -> fp16 is exact.  All eight
+        // 16-byte code loads of a lane are issued before the first conversion.
         const int cw = warp - V_WARP - 1;           // 0..3
         const bool kc = cw < 2;
         const int part = cw & 1;                    // which half of the slot's rows
+        Ring sg{kc ? 0 : NSK, kc ? NSK : NSV, 0u};
         Ring rg{kc ? 0 : NK, kc ? NK : NV, 0u};
-        // Code rows: K 64 keys x 128 codes; V (BN / SLOTS) keys x DH / 2 codes.
-        constexpr int RBV = DH / 2;                 // V code bytes per row
+        // Staging rows: K 64 keys x 128 codes; V (BN / SLOTS) keys x DH / 2 codes.
+        constexpr int RBV = DH / 2;                 // V code bytes per staging row
         constexpr int RPIK = 32 / (128 / 16);       // K rows per warp pass (4)
         constexpr int RPIV = 32 / (RBV / 16);       // V rows per warp pass (4 or 8)
         constexpr int PASSES = 8;                   // passes per warp per slot (half a slot)
@@ -647,28 +644,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int rb = kc ? 128 : RBV;
         const int cpr = rb / 16;                    // 16-code chunks per row
         const int rpi = kc ? RPIK : RPIV;
-        const int half_rows = rpi * PASSES;         // rows of this warp's half
-        const int code_off = kc ? k_code_off(part) : v_code_off(part);
-        const int rsub = lane / cpr;                // row within a pass
+        const int rbase = part * rpi * PASSES + lane / cpr;
         const int c = lane % cpr;                   // 16 codes: d 16c .. 16c + 15 of the row
         bool ok = true;
         while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
             for (int j = jb; ok && j < je; ++j) {
                 for (int h = 0; h < SLOTS && ok; ++h) {
-                    const int fs = rg.slot();
-                    ok = mbar_wait(BR.code_full(fs), rg.phase(), abort_flag, P.err);
+                    const int ss = sg.slot(), fs = rg.slot();
+                    ok = mbar_wait(BR.stg_full(ss), sg.phase(), abort_flag, P.err);
+                    if (ok) ok = mbar_wait(BR.empty(fs), rg.phase() ^ 1u, abort_flag, P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    uint8_t* slot = base_ptr + fs * SLOT_BYTES;
+                    const uint8_t* src = base_ptr + RING_BYTES + ss * STG_SLOT;
+                    uint8_t* dst = base_ptr + fs * SLOT_BYTES;
                     uint4 code[PASSES];
 #pragma unroll
                     for (int i = 0; i < PASSES; ++i)
-                        code[i] = *reinterpret_cast<const uint4*>(
-                            slot + code_off + (rsub + i * rpi) * rb + c * 16);
-                    __syncwarp();   // every lane's codes are in registers before any store
+                        code[i] = *reinterpret_cast<const uint4*>(src + (rbase + i * rpi) * rb +
+                                                                  c * 16);
 #pragma unroll
                     for (int i = 0; i < PASSES; ++i) {
-                        const int r = part * half_rows + rsub + i * rpi;   // row of the slot
+                        const int r = rbase + i * rpi;
                         uint4 lo, hi;
                         e4m3x16_f16(code[i], lo, hi);
                         // K slot: chunk c / 4 (64 d) of HALF_SLOT, row r; V slot:
@@ -677,8 +673,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             kc ? (uint32_t)((c >> 2) * HALF_SLOT + r * 128)
                                : (uint32_t)((r >> 5) * SUB_BYTES + (c >> 2) * 4096 + (r & 31) * 128);
                         const uint32_t u0 = 2u * (uint32_t)(c & 3), sw = (uint32_t)(r & 7);
-                        *reinterpret_cast<uint4*>(slot + o + ((u0 ^ sw) << 4)) = lo;
-                        *reinterpret_cast<uint4*>(slot + o + (((u0 + 1) ^ sw) << 4)) = hi;
+                        *reinterpret_cast<uint4*>(dst + o + ((u0 ^ sw) << 4)) = lo;
+                        *reinterpret_cast<uint4*>(dst + o + (((u0 + 1) ^ sw) << 4)) = hi;
                     }
                     // Order the generic stores before the tensor cores' reads of this
                     // CTA's shared memory (reached through the cluster window by the
@@ -686,9 +682,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
+                        mbar_arrive(BR.stg_empty(ss, NSTG));
                         if (leader) arrive_cl_local(BR.full(fs));
                         else arrive_cl_remote(leader_addr(BR.full(fs)));
                     }
+                    ++sg.n;
                     ++rg.n;
                 }
             }
@@ -1239,13 +1237,12 @@ int prefill_launch(const void* q, const void* k, const void* v, const float* ksc
     find_cut_tiles(P, tasks);
 
     CUtensorMap tq, tk, tv;
-    // E4M3 code maps (unswizzled rows, half a ring slot's rows per box): K
-    // boxes of 128 codes x 32 keys, V boxes of Dh / 2 codes x 64 / (Dh / 128)
-    // keys, one KV head per box; 4 KB each.
+    // E4M3 code maps (unswizzled staging rows): K boxes of 128 codes x 64 keys,
+    // V boxes of Dh / 2 codes x (128 / (Dh / 128)) keys, one KV head per box.
     auto code_maps = [&](bool three_d) -> bool {
-        const uint32_t v_rows = (uint32_t)(BN / (Dh / 128) / 2);
+        const uint32_t v_rows = (uint32_t)(BN / (Dh / 128));
         return make_map_u8_plain(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, (uint64_t)Dh,
-                                 (uint64_t)Hkv * Dh, 128, 32, three_d) &&
+                                 (uint64_t)Hkv * Dh, 128, 64, three_d) &&
                make_map_u8_plain(&tv, v, Dh, (uint64_t)Hkv, (uint64_t)KV, (uint64_t)Dh,
                                  (uint64_t)Hkv * Dh, (uint32_t)(Dh / 2), v_rows, three_d);
     };
