@@ -90,10 +90,10 @@ constexpr int SEEN_BITS = 16384;                          // block ids seen in t
 template <int DH>
 struct SL {
     static constexpr int KV_TILE_BYTES = TILE * DH * 2;            // 64 / 32 KB
-    static constexpr int OFF_K = 0;                                // 2 K tiles
-    static constexpr int OFF_V = OFF_K + 2 * KV_TILE_BYTES;        // 1 V tile
+    static constexpr int OFF_K = 0;                                // 1 K tile
+    static constexpr int OFF_V = OFF_K + KV_TILE_BYTES;            // 2 V tiles (fp16 cache)
     static constexpr int Q_BYTES = NP * DH * 2;                    // DH / 64 chunks [16][64]
-    static constexpr int OFF_Q = OFF_V + KV_TILE_BYTES;            // 2 Q buffers
+    static constexpr int OFF_Q = OFF_V + 2 * KV_TILE_BYTES;        // 2 Q buffers
     static constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;             // 2 P^T buffers
     static constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;          // [4][NP] floats
     static constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
@@ -104,10 +104,10 @@ struct SL {
     static constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
 };
 enum {
-    B_KFULL = 0,   // [2]
-    B_KEMPTY = 2,  // [2]
-    B_VFULL = 4,
-    B_VEMPTY = 5,
+    B_KFULL = 0,
+    B_KEMPTY = 1,
+    B_VFULL = 2,   // [2] (one slot with an E4M3 cache)
+    B_VEMPTY = 4,  // [2]
     B_QFULL = 6,   // [2]
     B_QEMPTY = 8,  // [2]
     B_SFULL = 10,  // [2]
@@ -185,11 +185,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     constexpr int OFF_SEEN = L::OFF_SEEN, OFF_BAR = L::OFF_BAR, OFF_TMEM = off_tmem<DH>();
     const int nh = (HQ == NP) ? P.nh : HQ;
     const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * DH;
-    // Tile buffers: two fp16 K tiles and one V tile; with E4M3 codes one K
-    // tile, the V tile, and the code staging in the second K tile's place.
-    constexpr int NKB = F8 ? 1 : 2;
+    // Tile buffers: one K tile and two V tiles (the K tile is free again as
+    // soon as its Q.K^T is done, a V tile only after the softmax and P.V);
+    // with E4M3 codes one K tile, one V tile, and the code staging in the
+    // second V tile's place.
+    constexpr int NVB = F8 ? 1 : 2;
     constexpr uint32_t KOFF = OFF_K;
-    constexpr uint32_t VOFF = F8 ? (uint32_t)KV_TILE_BYTES : (uint32_t)OFF_V;
+    constexpr uint32_t VOFF = OFF_V;
+    // Copy completions counted per tile: fp16, two warps of 32 lanes per K or
+    // V tile (and the K warps load Q); E4M3, all four gather warps.
+    constexpr int NGATHER = F8 ? 128 : 64;
     constexpr uint32_t SOFF = 2u * KV_TILE_BYTES;
     constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
     constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
@@ -208,17 +213,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        mbar_init(bar(B_KFULL), NGATHER);
+        mbar_init(bar(B_KEMPTY), 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_KFULL + b), 128);
-            mbar_init(bar(B_KEMPTY + b), 1);
-            mbar_init(bar(B_QFULL + b), 128);
+            mbar_init(bar(B_VFULL + b), NGATHER);
+            mbar_init(bar(B_VEMPTY + b), 1);
+            mbar_init(bar(B_QFULL + b), NGATHER);
             mbar_init(bar(B_QEMPTY + b), 1);
             mbar_init(bar(B_SFULL + b), 1);
             mbar_init(bar(B_PREADY + b), 128);
             mbar_init(bar(B_PTEMPTY + b), 1);
         }
-        mbar_init(bar(B_VFULL), 128);
-        mbar_init(bar(B_VEMPTY), 1);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_GROUP), 128);
         for (int b = 0; b < NI; ++b) {
@@ -256,6 +261,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             row = tok >= 0 ? (size_t)tok * tok_stride : 0;
             return true;
         };
+        // fp16 gather: the rows of keys kbase + lane and kbase + 32 + lane.
+        auto take_index2 = [&](uint32_t gg, int kbase, int (&tok)[2], size_t (&row)[2]) -> bool {
+            const int slot = (int)(gg % NI);
+            if (!mbar_wait(bar(B_IFULL + slot), (gg / NI) & 1, abort_flag, P.err)) return false;
+            tok[0] = idx[slot * TILE + kbase + lane];
+            tok[1] = idx[slot * TILE + kbase + 32 + lane];
+            mbar_arrive(bar(B_IEMPTY + slot));
+            row[0] = tok[0] >= 0 ? (size_t)tok[0] * tok_stride : 0;
+            row[1] = tok[1] >= 0 ? (size_t)tok[1] * tok_stride : 0;
+            return true;
+        };
         uint32_t g = 0;                     // global tile counter
         int rloc = 0;                       // non-empty rows handled so far
         bool ok = true;
@@ -268,19 +284,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
             const int nt = row_tiles(cnt);
             if (nt == 0) continue;
-            // Q row i (nh heads x 256 d) -> Q buffer rloc & 1, rows 0 .. nh - 1.
+            // Q row i (nh heads x DH d) -> Q buffer rloc & 1, rows 0 .. nh - 1,
+            // by the NGATHER threads that count on QFULL (the K warps with an
+            // fp16 cache, all four gather warps with E4M3 codes).
             const int qb = rloc & 1;
-            if (!mbar_wait(bar(B_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err)) {
-                ok = false;
-                break;
+            if (gt < NGATHER) {
+                if (!mbar_wait(bar(B_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                    ok = false;
+                    break;
+                }
+                for (int u = gt; u < nh * (DH / 8); u += NGATHER) {
+                    const int h = u / (DH / 8), c16 = u % (DH / 8);
+                    const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
+                                         sw128(h, c16 % 8);
+                    cp_async16(dst, P.q + (size_t)i * q_stride + h * DH + c16 * 8, 16);
+                }
+                cp_async_arrive(bar(B_QFULL + qb));
             }
-            for (int u = gt; u < nh * (DH / 8); u += 128) {
-                const int h = u / (DH / 8), c16 = u % (DH / 8);
-                const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
-                                     sw128(h, c16 % 8);
-                cp_async16(dst, P.q + (size_t)i * q_stride + h * DH + c16 * 8, 16);
-            }
-            cp_async_arrive(bar(B_QFULL + qb));
             ++rloc;
             if constexpr (F8) {
                 // E4M3 codes.  Each gather lane copies the 16-byte code chunks it
@@ -385,46 +405,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 }
                 g += (uint32_t)nt;
             } else {
+                // fp16: warps 0, 1 gather K and warps 2, 3 V, each warp the keys
+                // kbase .. kbase + 63 of every tile, so the K stream runs ahead of
+                // the V stream (K's single buffer frees once its Q.K^T is done, V's
+                // two buffers after each P.V).  A key's row is DH * 2 bytes, one
+                // warp-wide copy per 512 / (DH * 2) keys.
+                const bool kg = warp < 2;
+                const int kbase = (warp & 1) * 64;
+                constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
+                constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
+                const int ul = lane % LPK;        // lane covers d = 8 ul .. 8 ul + 7
+                const __half* cache = kg ? P.kcache : P.vcache;
                 for (int t = 0; t < nt && ok; ++t, ++g) {
-                    // This warp's 32 keys: lane -> cache row, then the DH * 2-byte
-                    // row of each key (one warp-wide copy covers 512 / (DH * 2) keys).
-                    int tok_l;
-                    size_t row_l;
-                    if (!take_index(g, tok_l, row_l)) {
+                    int tok2[2];
+                    size_t row2[2];
+                    if (!take_index2(g, kbase, tok2, row2)) {
                         ok = false;
                         break;
                     }
-                    const int kb = g & 1;
-                    for (int kv = 0; kv < 2; ++kv) {
-                        if (kv == 0) {
-                            if (!mbar_wait(bar(B_KEMPTY + kb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
-                                ok = false;
-                                break;
-                            }
-                        } else {
-                            if (!mbar_wait(bar(B_VEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
-                                ok = false;
-                                break;
-                            }
+                    uint32_t tile, fullb;
+                    if (kg) {
+                        if (!mbar_wait(bar(B_KEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
+                            ok = false;
+                            break;
                         }
-                        const uint32_t tile = sbase + (kv == 0 ? OFF_K + kb * KV_TILE_BYTES : OFF_V);
-                        const __half* cache = kv == 0 ? P.kcache : P.vcache;
-                        constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
-                        constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
+                        tile = sbase + OFF_K;
+                        fullb = bar(B_KFULL);
+                    } else {
+                        const int vb = g & 1;
+                        if (!mbar_wait(bar(B_VEMPTY + vb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tile = sbase + OFF_V + vb * KV_TILE_BYTES;
+                        fullb = bar(B_VFULL + vb);
+                    }
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll 4
                         for (int e = 0; e < 32 / KPI; ++e) {
-                            const int src_lane = KPI * e + lane / LPK;
-                            const int key = warp * 32 + src_lane;
-                            const int ul = lane % LPK;
-                            const int tok = __shfl_sync(0xffffffffu, tok_l, src_lane);
-                            const size_t row = __shfl_sync(0xffffffffu, row_l, src_lane);
-                            // lane covers d = 8 ul .. 8 ul + 7: chunk ul / 8, unit ul % 8
+                            const int src = KPI * e + lane / LPK;   // lane holding this key's row
+                            const int key = kbase + 32 * hf + src;
+                            const int tok = __shfl_sync(0xffffffffu, tok2[hf], src);
+                            const size_t row = __shfl_sync(0xffffffffu, row2[hf], src);
+                            // chunk ul / 8, unit ul % 8 of the key's swizzled row
                             const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
-                            const __half* src = tok >= 0 ? cache + row + ul * 8 : cache;
-                            cp_async16(dst, src, tok >= 0 ? 16u : 0u);
+                            const __half* sp = tok >= 0 ? cache + row + ul * 8 : cache;
+                            cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
                         }
-                        cp_async_arrive(bar(kv == 0 ? B_KFULL + kb : B_VFULL));
                     }
+                    cp_async_arrive(fullb);
                 }
             }
         }
@@ -438,7 +468,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             auto issue_pv = [&](uint32_t x, bool first) -> bool {
                 if (!mbar_wait(bar(B_PREADY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
                     return false;
-                if (!mbar_wait(bar(B_VFULL), x & 1, abort_flag, P.err)) return false;
+                const int vb = (int)(x % NVB);
+                if (!mbar_wait(bar(B_VFULL + vb), (x / NVB) & 1, abort_flag, P.err)) return false;
                 fence_async_shared();
                 tc_fence_after();
                 const uint32_t pt = sbase + OFF_PT + (x & 1) * PT_BYTES;
@@ -446,7 +477,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 for (int h = 0; h < HALVES; ++h) {
 #pragma unroll
                     for (int ks = 0; ks < TILE / 16; ++ks) {
-                        const uint64_t a = sdesc_sw128(sbase + VOFF + (2 * h) * (TILE * 128) +
+                        const uint64_t a = sdesc_sw128(sbase + VOFF + vb * KV_TILE_BYTES +
+                                                           (2 * h) * (TILE * 128) +
                                                            ks * 2048,
                                                        TILE * 128, 1024);
                         const uint64_t b =
@@ -455,7 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     }
                 }
                 umma_commit(bar(B_PTEMPTY + (x & 1)));
-                umma_commit(bar(B_VEMPTY));
+                umma_commit(bar(B_VEMPTY + vb));
                 return true;
             };
             for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
@@ -472,8 +504,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 fence_async_shared();
                 const uint32_t g0 = g;
                 for (int t = 0; t < nt; ++t, ++g) {
-                    const int kb = (int)(g % NKB);
-                    if (!mbar_wait(bar(B_KFULL + kb), (g / NKB) & 1, abort_flag, P.err)) {
+                    if (!mbar_wait(bar(B_KFULL), g & 1, abort_flag, P.err)) {
                         ok = false;
                         break;
                     }
@@ -481,7 +512,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < DH / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(sbase + KOFF + kb * KV_TILE_BYTES +
+                        const uint64_t a = sdesc_sw128(sbase + KOFF +
                                                            (kk / 4) * (TILE * 128) + (kk % 4) * 32,
                                                        16, 1024);
                         const uint64_t b = sdesc_sw128(sbase + OFF_Q + qb * Q_BYTES +
@@ -490,7 +521,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                         umma_ss(tmem + S_COL + (g & 1) * NP, a, b, IDESC_QK, kk > 0);
                     }
                     umma_commit(bar(B_SFULL + (g & 1)));
-                    umma_commit(bar(B_KEMPTY + kb));
+                    umma_commit(bar(B_KEMPTY));
                     if (t == nt - 1) umma_commit(bar(B_QEMPTY + qb));
                     if (t >= 1 && !(ok = issue_pv(g - 1, g - 1 == g0))) break;
                 }
