@@ -623,6 +623,10 @@ def run_gpu(args):
             secondary.append({"what": f"prefill Q={Q} KV={kv}, E4M3 K/V cache", "ms": round(ms, 4),
                               "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
                               "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4),
+                              "traffic": profiled_traffic(
+                                  "prefill_kernel_e4m3_Q8000_KV40000.md",
+                                  "long_context_causal_gqa_gb300/csrc/prefill.cu")
+                              if (Q, kv) == (Q_MAIN, KV_MAIN) else None,
                               "device_error": binding.device_error()})
         for hq, hkv, dh in ((6, 2, D), (8, 1, D), (6, 1, 128)):
             # Other head groupings (every query head's tiles in one launch when
@@ -710,7 +714,12 @@ def run_gpu(args):
                 secondary.append({"what": f"sparse blocks 4096 rows T={T} ctx=32768, {kind}",
                                   "ms": round(ms, 4),
                                   "gathered_GB/s": round(gathered / (ms * 1e-3) / 1e9, 1),
-                                  "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2)})
+                                  "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2),
+                                  "traffic": profiled_traffic(
+                                      "sparse_kernel_T512_rows4096.md",
+                                      "long_context_causal_gqa_gb300/csrc/sparse_blocks.cu",
+                                      "traffic_bytes_per_launch_e4m3" if e4m3
+                                      else "traffic_bytes_per_launch") if T == 512 else None})
         for e4m3 in (False, True):
             kind = "E4M3 cache" if e4m3 else "fp16 cache"
             try:
