@@ -428,6 +428,11 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x;   // this CTA's partial slot
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream (the previous call's merge, in a model's consecutive layers): the
+    // CTA launch overlaps that kernel, and nothing of global memory is read or
+    // written before it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Context length: the launch's, or read on the device (the grid is then
     // sized for the largest context, P.ctx_len, and splits past the actual
     // context get no tiles); with several sequences, this CTA's sequence.
@@ -957,6 +962,10 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) paged_merge_kernel(const Par
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int d0 = blockIdx.y * 128 + lane * 4;
+    // The next call's split kernel may launch now (it occupies no SM this
+    // kernel needs until these blocks are resident, and reads nothing before
+    // this grid has completed).
+    asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int S0 = 0, G = P.G;                    // this sequence's splits S0 .. S0 + G - 1
     if (P.batch > 1) seq_splits(P, seq, S0, G);
@@ -1056,19 +1065,23 @@ int launch_np_b(const CUtensorMap& tk, const CUtensorMap& tv, Params& P, cudaStr
     if (ensure_smem_limit(reinterpret_cast<const void*>(paged_split_kernel<NP, NWG, BATCHED, DH>),
                           L::SMEM) != GQA_OK)
         return GQA_ERR_CUDA;
-    paged_split_kernel<NP, NWG, BATCHED, DH>
-        <<<P.G, threads_for(NWG), L::SMEM, stream>>>(tk, tv, P);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P.batch * P.nq, P.dh / 128);
-    cfg.blockDim = dim3(MERGE_WARPS * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
+    // Both kernels are programmatic dependents of the kernel before them.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.G);
+    cfg.blockDim = dim3(threads_for(NWG));
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_split_kernel<NP, NWG, BATCHED, DH>, tk, tv, P) !=
+        cudaSuccess)
+        return GQA_ERR_CUDA;
+    cfg.gridDim = dim3(P.batch * P.nq, P.dh / 128);
+    cfg.blockDim = dim3(MERGE_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
     if (cudaLaunchKernelEx(&cfg, paged_merge_kernel, P) != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
 }
