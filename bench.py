@@ -637,7 +637,11 @@ def run_gpu(args):
             fl = prefill_flops(Q, KV, hq, dh)
             secondary.append({"what": f"prefill Q={Q} KV={KV} Hq={hq} Hkv={hkv} D={dh}",
                               "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
-                              "frac_of_peak": round(fl / ms / 1e9 / peak, 4)})
+                              "frac_of_peak": round(fl / ms / 1e9 / peak, 4),
+                              "traffic": profiled_traffic(
+                                  "prefill_kernel_d128_Q8000_KV40000.md",
+                                  "long_context_causal_gqa_gb300/csrc/prefill.cu")
+                              if (hq, hkv, dh, Q, KV) == (6, 1, 128, Q_MAIN, KV_MAIN) else None})
         for R in (1, 2, 8):
             try:
                 t, nbytes, fl = bench_paged(binding, R, device, 50, 5, flush)

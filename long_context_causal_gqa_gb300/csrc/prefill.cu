@@ -25,14 +25,16 @@
 //   the copy ring covers twice as many tiles of L2 latency.
 // * Warp roles per CTA: warp 0 loads Q and K, warp 10 loads V (each its
 //   half of every operand; the odd CTA's copies complete on the even CTA's
-//   barriers), warp 1 tensor-memory owner and, in the even CTA, the single
-//   UMMA-issuing thread, warps 2..9 softmax + epilogue in two warpgroups, each
-//   thread one tile row (TMEM lane) and half of its columns.
+//   barriers), warp 1 tensor-memory owner and, in the even CTA, the thread
+//   that issues the UMMAs, warps 2..9 softmax + epilogue in two warpgroups,
+//   each thread one tile row (TMEM lane) and half of its columns.  At head
+//   size 128 one more warp's first thread (even CTA) issues every P.V while
+//   warp 1 issues every Q.K^T (see the issuer section).
 // * K and V stream through separate rings of 16 KB slots, so that K of the
 //   next tiles never waits behind V slots held until their P is ready.
-// * Tensor memory (512 columns x 128 lanes per CTA): O = 256 fp32 columns;
-//   two S buffers of 128 fp32 columns, so Q.K^T of tile j+1 runs while tile
-//   j's softmax runs.  Each warpgroup's P (fp16) overwrites the first 32
+// * Tensor memory (512 columns x 128 lanes per CTA): O = DH fp32 columns,
+//   then two (DH = 256) or three (DH = 128) S buffers of 128 fp32 columns, so
+//   Q.K^T of tile j+1 runs while tile j's softmax runs.  Each warpgroup's P (fp16) overwrites the first 32
 //   columns of its own 64-column half of the S buffer.  The two threads of a
 //   row swap their half maxima through shared memory each tile, so both take
 //   the same rescale decisions.
@@ -89,9 +91,9 @@ constexpr int STG_SLOT = 8192;
 // UMMAs read; the fp16 ring shrinks to make room for the staging ring.  Up to
 // 16 warps share the same register limit (128 per thread at 4 warps per
 // scheduler), so the converters cost no registers beyond 13 warps.
-// Barriers: ring full/empty, q full/empty, s[2], p[2], o, drain, group, then
-// staging full/empty (F8).
-template <bool F8>
+// Barriers: ring full/empty, q full/empty, s / p / s-free [3], o, drain[2],
+// group, then staging full/empty (F8).
+template <bool F8, int DH>
 struct Cfg {
     static constexpr int NK = F8 ? 3 : GQA_PREFILL_NK;   // K slots (DH / 128 per tile)
     static constexpr int NV = F8 ? 3 : GQA_PREFILL_NV;   // V slots (DH / 128 per tile)
@@ -101,16 +103,25 @@ struct Cfg {
     static constexpr int NSTG = NSK + NSV;
     static constexpr int RING_BYTES = NRING * SLOT_BYTES;
     static constexpr int STG_BYTES = NSTG * STG_SLOT;
-    static constexpr int NUM_BARS = 2 * NRING + 9 + 2 * NSTG;
+    static constexpr int NUM_BARS = 2 * NRING + 15 + 2 * NSTG;
     static constexpr int NCONV = F8 ? 4 : 0;              // converter warps: 2 for K, 2 for V
-    static constexpr int NTHREADS = 64 + NSOFT + 32 + 32 * NCONV;
+    // DH = 128 (three S buffers): one more warp, whose first thread issues the
+    // P.V UMMAs; DH = 256: none (-1).
+    static constexpr int PV_WARP = DH == 128 ? V_WARP + 1 + NCONV : -1;
+    static constexpr int NTHREADS = 32 * (V_WARP + 1 + NCONV + (DH == 128 ? 1 : 0));
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + STG_BYTES + Q_BYTES +
                                       XCH_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 0;
-constexpr uint32_t S_COL0 = 256;
+// S buffers follow O in tensor memory: two of 128 columns after a 256-column
+// O (DH = 256), three after a 128-column O (DH = 128).
+template <int DH>
+struct SBuf {
+    static constexpr int N = DH == 128 ? 3 : 2;
+    static constexpr uint32_t COL0 = DH;
+};
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr int kMaxClusters = 80;
 
@@ -202,20 +213,24 @@ struct SegIter {
 
 // Barrier addresses for a ring of NR slots (K slots 0 .. NK-1, V slots
 // NK .. NR-1) and NS staging slots.
-template <int NR>
+template <int NR, int NS>
 struct Bars {
     uint32_t b;
     __device__ uint32_t full(int s) const { return b + 8 * s; }
     __device__ uint32_t empty(int s) const { return b + 8 * (NR + s); }
     __device__ uint32_t qfull() const { return b + 8 * (2 * NR); }
     __device__ uint32_t qempty() const { return b + 8 * (2 * NR + 1); }
+    // S buffer i (up to three): scores ready, P ready, free again (the P.V
+    // that read its P has completed).
     __device__ uint32_t sfull(int i) const { return b + 8 * (2 * NR + 2 + i); }
-    __device__ uint32_t pfull(int i) const { return b + 8 * (2 * NR + 4 + i); }
-    __device__ uint32_t ofull() const { return b + 8 * (2 * NR + 6); }
-    __device__ uint32_t drain() const { return b + 8 * (2 * NR + 7); }
-    __device__ uint32_t group() const { return b + 8 * (2 * NR + 8); }
-    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 9 + i); }
-    __device__ uint32_t stg_empty(int i, int ns) const { return b + 8 * (2 * NR + 9 + ns + i); }
+    __device__ uint32_t pfull(int i) const { return b + 8 * (2 * NR + 5 + i); }
+    __device__ uint32_t sfree(int i) const { return b + 8 * (2 * NR + 8 + i); }
+    __device__ uint32_t ofull() const { return b + 8 * (2 * NR + 11); }
+    __device__ uint32_t drain() const { return b + 8 * (2 * NR + 12); }
+    __device__ uint32_t drain2() const { return b + 8 * (2 * NR + 13); }
+    __device__ uint32_t group() const { return b + 8 * (2 * NR + 14); }
+    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 15 + i); }
+    __device__ uint32_t stg_empty(int i) const { return b + 8 * (2 * NR + 15 + NS + i); }
 };
 
 // One ring (K or V) seen by its producer and by the UMMA issuer: slot
@@ -443,7 +458,7 @@ __device__ __forceinline__ void e4m3x16_f16(const uint4& c, uint4& lo, uint4& hi
 // 256 or 128.  F8: K and V are E4M3 codes (tm_k / tm_v map the code bytes),
 // converted to fp16 in shared memory by two extra warps.
 template <bool MH, int DH, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<F8>::NTHREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<F8, DH>::NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params P) {
     static_assert(DH == 256 || DH == 128, "head size");
@@ -454,8 +469,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr int SUB_BYTES = 32 * VATOMS * 128;    // one 32-key V sub-tile
     constexpr int SUBS = SLOT_BYTES / SUB_BYTES;    // V sub-tiles per slot
     constexpr int OCOLS = DH / NWG;                 // O columns per softmax thread
+    constexpr uint32_t NSB = SBuf<DH>::N;           // S buffers in tensor memory
+    // Three S buffers: Q.K^T and P.V come from two threads; two: from one.
+    constexpr bool TWO_ISSUERS = NSB == 3;
     constexpr uint32_t IDESC_PV = idesc_f16_f32(256, DH, false, true);
-    using C = Cfg<F8>;
+    using C = Cfg<F8, DH>;
     constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING, NSK = C::NSK, NSV = C::NSV;
     constexpr int NSTG = C::NSTG;
     constexpr int RING_BYTES = C::RING_BYTES, STG_BYTES = C::STG_BYTES, NUM_BARS = C::NUM_BARS;
@@ -467,7 +485,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t s_stg = base + RING_BYTES;
     const uint32_t s_q = s_stg + STG_BYTES;
     const uint32_t s_bars = s_q + Q_BYTES + XCH_BYTES;
-    const Bars<NRING> BR{s_bars};
+    const Bars<NRING, NSTG> BR{s_bars};
     float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + STG_BYTES + Q_BYTES);
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + STG_BYTES +
                                                           Q_BYTES + XCH_BYTES + NUM_BARS * 8);
@@ -488,16 +506,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         for (int s = 0; s < NSTG; ++s) {
             mbar_init(BR.stg_full(s), 1);
-            mbar_init(BR.stg_empty(s, NSTG), 2);   // both converter warps of the role
+            mbar_init(BR.stg_empty(s), 2);   // both converter warps of the role
         }
         mbar_init(BR.qfull(), 1);
         mbar_init(BR.qempty(), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 3; ++i) {
             mbar_init(BR.sfull(i), 1);
             mbar_init(BR.pfull(i), 2 * NSOFT / 32);   // one arrival per softmax warp of the pair
+            mbar_init(BR.sfree(i), 1);
         }
         mbar_init(BR.ofull(), 1);
         mbar_init(BR.drain(), 1);
+        mbar_init(BR.drain2(), 1);
         mbar_init(BR.group(), NSOFT);
         *abort_flag = 0;
         fence_mbar_init();
@@ -542,7 +562,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto acquire = [&](uint32_t& dst, uint32_t& fb) -> bool {
                 const int slot = rg.slot();
                 if constexpr (F8) {
-                    if (!mbar_wait(BR.stg_empty(slot, NSTG), rg.phase() ^ 1u, abort_flag, P.err))
+                    if (!mbar_wait(BR.stg_empty(slot), rg.phase() ^ 1u, abort_flag, P.err))
                         return false;
                     dst = s_stg + slot * STG_SLOT;
                     fb = BR.stg_full(slot);
@@ -620,7 +640,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (kq && seg > 0 && leader) drain_wait(BR.qfull(), (seg - 1) & 1);
             }
         }
-    } else if (F8 && warp > V_WARP) {
+    } else if (F8 && warp > V_WARP && warp <= V_WARP + C::NCONV) {
         // ------------------------------------------------------------ converters (F8)
         // Warps V_WARP + 1, + 2 convert K, V_WARP + 3, + 4 V, each half of
         // every slot: in the order the producer filled the staging slots, wait
@@ -682,7 +702,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(BR.stg_empty(ss, NSTG));
+                        mbar_arrive(BR.stg_empty(ss));
                         if (leader) arrive_cl_local(BR.full(fs));
                         else arrive_cl_remote(leader_addr(BR.full(fs)));
                     }
@@ -691,110 +711,157 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && leader) {
-            Ring kr{0, NK, 0u}, vr{NK, NV, 0u};
-            uint32_t g = 0;
-            int seg = 0;
-            bool ok = true;
-            // A landed K / V slot: the copy and the UMMA that reads it are both
-            // async-proxy operations ordered by the mbarrier's completion, so no
-            // tcgen05 fence is needed here (the issuing thread's time between
-            // UMMAs is what keeps the tensor pipe fed).
-            // F8: the slots were filled by generic stores of both CTAs' converter
-            // warps, which arrive with cluster-scope release; acquire at cluster
-            // scope to match.
-            auto take = [&](Ring& rg, int& slot) -> bool {
-                slot = rg.slot();
-                if constexpr (F8) return mbar_wait_cl(BR.full(slot), rg.phase(), abort_flag, P.err);
-                return mbar_wait(BR.full(slot), rg.phase(), abort_flag, P.err);
-            };
-            // Non-blocking look at the ring position after the current one; its
-            // latency overlaps the current slot's UMMA issue, and a slot found
-            // full needs no wait later.
-            auto peek_next = [&](const Ring& rg) -> bool {
-                Ring nx = rg;
-                ++nx.n;
-                if constexpr (F8) return mbar_test_cl(BR.full(nx.slot()), nx.phase());
-                return mbar_test(BR.full(nx.slot()), nx.phase());
-            };
-            // Descriptor low words: Q chunk c at q_lo + c * (BM * 128 >> 4); a K
-            // slot's chunk cc at + cc * (HALF_SLOT >> 4); a K step of 16
-            // elements (32 bytes) at + 2.
-            const uint32_t q_lo = desc_lo(s_q, 16);
-            auto issue_qk = [&](uint32_t s_col) -> bool {
-                const uint32_t d = tmem + s_col;
-                bool next_ready = false;
+    } else if (warp == 1 || warp == C::PV_WARP) {
+      if (lane == 0 && leader && (TWO_ISSUERS || warp == 1)) {
+        // ------------------------------------------------------------ UMMA issuers
+        // Each UMMA issues at about the tensor pipe's own rate, so the issuing
+        // thread's barrier waits and commits (several hundred cycles per tile)
+        // leave the pipe idle unless something else issues meanwhile.  With
+        // three S buffers (DH = 128) two threads of the even CTA issue: warp 1
+        // every Q.K^T, warp PV_WARP every P.V, and Q.K^T of tile g waits only
+        // for the P.V of tile g - 3 (sfree), so the chain softmax -> P.V ->
+        // Q.K^T spans three tiles.  With two (DH = 256, where O takes half of
+        // tensor memory) warp 1 issues both in one stream: Q.K^T of tile g + 1,
+        // then P.V of tile g, the tensor pipe's order keeping Q.K^T of tile
+        // g + 2 behind the P.V of tile g that reads the same buffer.
+        const bool qk_role = warp == 1;
+        Ring kr{0, NK, 0u}, vr{NK, NV, 0u};   // each thread uses the ring(s) of its UMMAs
+        uint32_t g = 0;
+        int seg = 0;
+        bool ok = true;
+        // A landed K / V slot: the copy and the UMMA that reads it are both
+        // async-proxy operations ordered by the mbarrier's completion, so no
+        // tcgen05 fence is needed here.
+        // F8: the slots were filled by generic stores of both CTAs' converter
+        // warps, which arrive with cluster-scope release; acquire at cluster
+        // scope to match.
+        auto take = [&](const Ring& rg, int& slot) -> bool {
+            slot = rg.slot();
+            if constexpr (F8) return mbar_wait_cl(BR.full(slot), rg.phase(), abort_flag, P.err);
+            return mbar_wait(BR.full(slot), rg.phase(), abort_flag, P.err);
+        };
+        // Non-blocking look at the ring position after the current one; its
+        // latency overlaps the current slot's UMMA issue, and a slot found
+        // full needs no wait later.
+        auto peek_next = [&](const Ring& rg) -> bool {
+            Ring nx = rg;
+            ++nx.n;
+            if constexpr (F8) return mbar_test_cl(BR.full(nx.slot()), nx.phase());
+            return mbar_test(BR.full(nx.slot()), nx.phase());
+        };
+        // Descriptor low words: Q chunk c at q_lo + c * (BM * 128 >> 4); a K
+        // slot's chunk cc at + cc * (HALF_SLOT >> 4); a K step of 16
+        // elements (32 bytes) at + 2.
+        const uint32_t q_lo = desc_lo(s_q, 16);
+        auto issue_qk = [&](uint32_t s_col) -> bool {
+            const uint32_t d = tmem + s_col;
+            bool next_ready = false;
 #pragma unroll
-                for (int h = 0; h < SLOTS; ++h) {
-                    int slot = kr.slot();
-                    if (!next_ready && !take(kr, slot)) return false;
-                    if (SLOTS > 1 && h == 0) next_ready = peek_next(kr);
-                    const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
+            for (int h = 0; h < SLOTS; ++h) {
+                int slot = kr.slot();
+                if (!next_ready && !take(kr, slot)) return false;
+                if (SLOTS > 1 && h == 0) next_ready = peek_next(kr);
+                const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * h + cc;
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * h + cc;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = desc64(q_lo + c * ((BM * 128) >> 4) + kk * 2);
-                            const uint64_t b = desc64(k_lo + cc * (HALF_SLOT >> 4) + kk * 2);
-                            if (c == 0 && kk == 0)
-                                umma_ss_pair_c<false>(d, a, b, IDESC_QK);
-                            else
-                                umma_ss_pair_c<true>(d, a, b, IDESC_QK);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = desc64(q_lo + c * ((BM * 128) >> 4) + kk * 2);
+                        const uint64_t b = desc64(k_lo + cc * (HALF_SLOT >> 4) + kk * 2);
+                        if (c == 0 && kk == 0)
+                            umma_ss_pair_c<false>(d, a, b, IDESC_QK);
+                        else
+                            umma_ss_pair_c<true>(d, a, b, IDESC_QK);
                     }
-                    umma_commit_pair(BR.empty(slot));
-                    ++kr.n;
                 }
-                return true;
-            };
-            auto issue_pv = [&](uint32_t s_col, bool acc0) -> bool {
-                const uint32_t p_base = tmem + s_col;
-                bool next_ready = false;
+                umma_commit_pair(BR.empty(slot));
+                ++kr.n;
+            }
+            return true;
+        };
+        auto issue_pv = [&](uint32_t s_col, bool acc0) -> bool {
+            const uint32_t p_base = tmem + s_col;
+            bool next_ready = false;
 #pragma unroll
-                for (int h = 0; h < SLOTS; ++h) {
-                    int slot = vr.slot();
-                    if (!next_ready && !take(vr, slot)) return false;
-                    if (SLOTS > 1 && h == 0) next_ready = peek_next(vr);
-                    // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
-                    // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
-                    const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
+            for (int h = 0; h < SLOTS; ++h) {
+                int slot = vr.slot();
+                if (!next_ready && !take(vr, slot)) return false;
+                if (SLOTS > 1 && h == 0) next_ready = peek_next(vr);
+                // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
+                // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
+                const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
 #pragma unroll
-                    for (int ss = 0; ss < SUBS; ++ss) {
+                for (int ss = 0; ss < SUBS; ++ss) {
 #pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const uint64_t b = desc64(v_lo + ss * (SUB_BYTES >> 4) + ks * (2048 >> 4));
-                            // P of keys kb .. kb + 15: part kb / COLS sits at columns
-                            // COLS (kb / COLS) + (kb % COLS) / 2 of the S buffer.
-                            const int kb = (SUBS * h + ss) * 32 + ks * 16;
-                            const uint32_t a_tmem = p_base + (kb / COLS) * COLS + (kb % COLS) / 2;
-                            if (h == 0 && ss == 0 && ks == 0)
-                                umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV, acc0 ? 1u : 0u);
-                            else
-                                umma_ts_pair_c<true>(tmem + O_COL, a_tmem, b, IDESC_PV);
-                        }
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const uint64_t b = desc64(v_lo + ss * (SUB_BYTES >> 4) + ks * (2048 >> 4));
+                        // P of keys kb .. kb + 15: part kb / COLS sits at columns
+                        // COLS (kb / COLS) + (kb % COLS) / 2 of the S buffer.
+                        const int kb = (SUBS * h + ss) * 32 + ks * 16;
+                        const uint32_t a_tmem = p_base + (kb / COLS) * COLS + (kb % COLS) / 2;
+                        if (h == 0 && ss == 0 && ks == 0)
+                            umma_ts_pair(tmem + O_COL, a_tmem, b, IDESC_PV, acc0 ? 1u : 0u);
+                        else
+                            umma_ts_pair_c<true>(tmem + O_COL, a_tmem, b, IDESC_PV);
                     }
-                    umma_commit_pair(BR.empty(slot));
-                    ++vr.n;
                 }
-                return true;
-            };
-            while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
+                umma_commit_pair(BR.empty(slot));
+                ++vr.n;
+            }
+            return true;
+        };
+        auto s_col_of = [&](uint32_t gg) { return SBuf<DH>::COL0 + (gg % NSB) * BN; };
+        // Q.K^T of tile gg into its S buffer, then the scores-ready commit (and
+        // the Q-free commit after the segment's last one).
+        auto qk_step = [&](uint32_t gg, bool last_of_seg) -> bool {
+            if (!issue_qk(s_col_of(gg))) return false;
+            umma_commit_pair(BR.sfull(gg % NSB));
+            if (last_of_seg) umma_commit_pair(BR.qempty());
+            return true;
+        };
+        // P.V of tile gg once its P is ready, then the O-ready (and, with two
+        // issuers, the S-buffer-free) commits.
+        auto pv_step = [&](uint32_t gg, bool acc) -> bool {
+            if (!mbar_wait(BR.pfull(gg % NSB), (gg / NSB) & 1, abort_flag, P.err)) return false;
+            tc_fence_after();
+            if (!issue_pv(s_col_of(gg), acc)) return false;
+            umma_commit_pair(BR.ofull());
+            if (TWO_ISSUERS) umma_commit_pair(BR.sfree(gg % NSB));
+            return true;
+        };
+        while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
+            if (qk_role) {
                 if (!mbar_wait(BR.qfull(), seg & 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                ok = issue_qk(S_COL0 + (g & 1) * BN);
+            }
+            if (TWO_ISSUERS) {
+                for (int j = jb; ok && j < je; ++j) {
+                    const uint32_t gg = g + (j - jb);
+                    if (qk_role) {
+                        if (gg >= NSB) {
+                            ok = mbar_wait(BR.sfree(gg % NSB), ((gg - NSB) / NSB) & 1, abort_flag,
+                                           P.err);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        ok = qk_step(gg, j == je - 1);
+                    } else {
+                        ok = pv_step(gg, j > jb);
+                    }
+                }
+            } else {
+                ok = issue_qk(s_col_of(g));
                 if (!ok) break;
                 umma_commit_pair(BR.sfull(g & 1));
                 if (je - jb == 1) umma_commit_pair(BR.qempty());
                 for (int j = jb; j < je; ++j) {
                     const uint32_t gg = g + (j - jb);
                     if (j + 1 < je) {
-                        ok = issue_qk(S_COL0 + ((gg + 1) & 1) * BN);
+                        ok = issue_qk(s_col_of(gg + 1));
                         if (!ok) break;
                         umma_commit_pair(BR.sfull((gg + 1) & 1));
                         if (j + 1 == je - 1) umma_commit_pair(BR.qempty());
@@ -804,19 +871,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
-                    ok = issue_pv(S_COL0 + (gg & 1) * BN, j > jb);
+                    ok = issue_pv(s_col_of(gg), j > jb);
                     if (!ok) break;
                     umma_commit_pair(BR.ofull());
                 }
-                g += je - jb;
-                ++seg;
             }
-            if (!ok) {
-                // Unwind: wait for every UMMA already issued before TMEM is freed.
-                umma_commit_pair(BR.drain());
-                drain_wait(BR.drain(), 0);
-            }
+            g += je - jb;
+            ++seg;
         }
+        if (!ok) {
+            // Unwind: wait for every UMMA this thread issued before TMEM is freed.
+            const uint32_t db = qk_role ? BR.drain() : BR.drain2();
+            umma_commit_pair(db);
+            drain_wait(db, 0);
+        }
+      }
     } else if (warp < V_WARP) {
         // ------------------------------------------------------------ softmax / epilogue
         // Warpgroup hg owns S columns [COLS hg, COLS (hg + 1)) of every tile
@@ -845,8 +914,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float l = 0.f;
             for (int j = jb; j < je; ++j) {
                 const uint32_t gg = g + (j - jb);
-                const uint32_t s_col = S_COL0 + (gg & 1) * BN;
-                ok = mbar_wait(BR.sfull(gg & 1), (gg >> 1) & 1, abort_flag, P.err);
+                const uint32_t sb = gg % NSB;
+                const uint32_t s_col = SBuf<DH>::COL0 + sb * BN;
+                ok = mbar_wait(BR.sfull(sb), (gg / NSB) & 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -943,8 +1013,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if (leader) mbar_arrive(BR.pfull(gg & 1));
-                    else remote_arrive(leader_addr(BR.pfull(gg & 1)));
+                    if (leader) mbar_arrive(BR.pfull(sb));
+                    else remote_arrive(leader_addr(BR.pfull(sb)));
                 }
             }
             if (!ok) break;
@@ -1111,8 +1181,8 @@ static int max_pairs(int device) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(Cfg<false>::NTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<false>::SMEM_BYTES;
+    cfg.blockDim = dim3(Cfg<false, 256>::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<false, 256>::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -1137,7 +1207,7 @@ static int max_pairs(int device) {
 template <bool MH, int DH, bool F8>
 static int launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Params& P, const MergeTasks& tasks, cudaStream_t stream) {
-    using C = Cfg<F8>;
+    using C = Cfg<F8, DH>;
     if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<MH, DH, F8>),
                           C::SMEM_BYTES) != GQA_OK)
         return GQA_ERR_CUDA;
@@ -1166,7 +1236,7 @@ int prefill_resident_pairs() {
     const DeviceInfo* di = device_info();
     if (!di) return -1;
     if (ensure_smem_limit(reinterpret_cast<const void*>(prefill::prefill_kernel<false, 256, false>),
-                          prefill::Cfg<false>::SMEM_BYTES) != GQA_OK)
+                          prefill::Cfg<false, 256>::SMEM_BYTES) != GQA_OK)
         return -1;
     return prefill::max_pairs(di->device);
 }
@@ -1187,7 +1257,7 @@ int prefill_launch(const void* q, const void* k, const void* v, const float* ksc
     if (!di) return GQA_ERR_CUDA;
     const bool f8 = kscale != nullptr;   // K / V are E4M3 codes with device-side scales
     if (ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel<false, 256, false>),
-                          Cfg<false>::SMEM_BYTES) != GQA_OK)
+                          Cfg<false, 256>::SMEM_BYTES) != GQA_OK)
         return GQA_ERR_CUDA;
     const int pairs_max = max_pairs(di->device);
     if (pairs_max < 1) return GQA_ERR_CUDA;
