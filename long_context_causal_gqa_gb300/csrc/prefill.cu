@@ -31,7 +31,14 @@
 //   size 128 one more warp's first thread (even CTA) issues every P.V while
 //   warp 1 issues every Q.K^T (see the issuer section).
 // * K and V stream through separate rings of 16 KB slots, so that K of the
-//   next tiles never waits behind V slots held until their P is ready.
+//   next tiles never waits behind V slots held until their P is ready.  With
+//   fp16 K / V each ring holds one tile per S buffer: a tile's K slots are
+//   refilled after the Q.K^T into the same-numbered S buffer completes and
+//   its V slots after that tile's P.V does, signalled by the scores-ready and
+//   O-ready barriers the softmax waits on anyway, so the issuing thread
+//   commits no per-slot releases and takes one barrier per tile and operand
+//   (with one issuing thread, half of each tile's issue time had been
+//   barrier operations).
 // * Tensor memory (512 columns x 128 lanes per CTA): O = DH fp32 columns,
 //   then two (DH = 256) or three (DH = 128) S buffers of 128 fp32 columns, so
 //   Q.K^T of tile j+1 runs while tile j's softmax runs.  Each warpgroup's P (fp16) overwrites the first 32
@@ -70,12 +77,6 @@ constexpr int D = kHeadDim;     // 256, the largest head size; shared memory is 
 // one at DH = 128).  A tile's half of K or V is DH / 128 slots.
 constexpr int SLOT_BYTES = 16384;
 constexpr int HALF_SLOT = SLOT_BYTES / 2;
-#ifndef GQA_PREFILL_NK
-#define GQA_PREFILL_NK 4
-#endif
-#ifndef GQA_PREFILL_NV
-#define GQA_PREFILL_NV 5
-#endif
 constexpr int Q_BYTES = BM * D * 2;           // 64 KB (the DH = 256 Q tile)
 constexpr int NWG = 2;                        // softmax warpgroups per CTA
 constexpr int COLS = BN / NWG;                // S columns per softmax thread
@@ -85,25 +86,38 @@ constexpr int XCH_BYTES = 3 * NWG * BM * 4;  // part maxima [parity][part][row],
 // E4M3 staging slot: this CTA's codes of one fp16 ring slot (8 KB).
 constexpr int STG_SLOT = 8192;
 
-// Per-variant sizes.  F8 (K and V stored as FP8-E4M3 codes): each CTA's TMA
+// S buffers follow O in tensor memory: two of 128 columns after a 256-column
+// O (DH = 256), three after a 128-column O (DH = 128).
+template <int DH>
+struct SBuf {
+    static constexpr int N = DH == 128 ? 3 : 2;
+    static constexpr uint32_t COL0 = DH;
+};
+
+// Per-variant sizes.  fp16 K / V: the K and V rings hold one tile per S
+// buffer (DH / 128 slots each), so a K tile's slots are free again exactly
+// when the Q.K^T into the same-numbered S buffer has completed (its
+// scores-ready barrier) and a V tile's when the P.V of that tile has (its
+// O-ready barrier): no per-slot release barriers or commits.
+// F8 (K and V stored as FP8-E4M3 codes): each CTA's TMA
 // brings its codes into staging slots, and four converter warps (two for K,
 // two for V, each half of a slot) write them as fp16 into the ring slots the
 // UMMAs read; the fp16 ring shrinks to make room for the staging ring.  Up to
 // 16 warps share the same register limit (128 per thread at 4 warps per
 // scheduler), so the converters cost no registers beyond 13 warps.
-// Barriers: ring full/empty, q full/empty, s / p / s-free [3], o, drain[2],
-// group, then staging full/empty (F8).
+// Barriers: ring full/empty (empty: F8 only), q full/empty, s / p / o [3],
+// drain[2], group, then staging full/empty (F8).
 template <bool F8, int DH>
 struct Cfg {
-    static constexpr int NK = F8 ? 3 : GQA_PREFILL_NK;   // K slots (DH / 128 per tile)
-    static constexpr int NV = F8 ? 3 : GQA_PREFILL_NV;   // V slots (DH / 128 per tile)
+    static constexpr int NK = F8 ? 3 : (DH / 128) * SBuf<DH>::N;   // K slots (DH / 128 per tile)
+    static constexpr int NV = F8 ? 3 : (DH / 128) * SBuf<DH>::N;   // V slots (DH / 128 per tile)
     static constexpr int NRING = NK + NV;
     static constexpr int NSK = F8 ? 3 : 0;               // K staging slots
     static constexpr int NSV = F8 ? 3 : 0;               // V staging slots
     static constexpr int NSTG = NSK + NSV;
     static constexpr int RING_BYTES = NRING * SLOT_BYTES;
     static constexpr int STG_BYTES = NSTG * STG_SLOT;
-    static constexpr int NUM_BARS = 2 * NRING + 15 + 2 * NSTG;
+    static constexpr int NUM_BARS = 2 * NRING + 14 + 2 * NSTG;
     static constexpr int NCONV = F8 ? 4 : 0;              // converter warps: 2 for K, 2 for V
     // DH = 128 (three S buffers): one more warp, whose first thread issues the
     // P.V UMMAs; DH = 256: none (-1).
@@ -115,13 +129,6 @@ struct Cfg {
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 0;
-// S buffers follow O in tensor memory: two of 128 columns after a 256-column
-// O (DH = 256), three after a 128-column O (DH = 128).
-template <int DH>
-struct SBuf {
-    static constexpr int N = DH == 128 ? 3 : 2;
-    static constexpr uint32_t COL0 = DH;
-};
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr int kMaxClusters = 80;
 
@@ -220,17 +227,17 @@ struct Bars {
     __device__ uint32_t empty(int s) const { return b + 8 * (NR + s); }
     __device__ uint32_t qfull() const { return b + 8 * (2 * NR); }
     __device__ uint32_t qempty() const { return b + 8 * (2 * NR + 1); }
-    // S buffer i (up to three): scores ready, P ready, free again (the P.V
-    // that read its P has completed).
+    // S buffer i (up to three): scores ready (Q.K^T into it complete), P
+    // ready, and O ready (the P.V of the buffer's tile complete, so also its
+    // P and, with fp16 K / V, that tile's V slots free again).
     __device__ uint32_t sfull(int i) const { return b + 8 * (2 * NR + 2 + i); }
     __device__ uint32_t pfull(int i) const { return b + 8 * (2 * NR + 5 + i); }
-    __device__ uint32_t sfree(int i) const { return b + 8 * (2 * NR + 8 + i); }
-    __device__ uint32_t ofull() const { return b + 8 * (2 * NR + 11); }
-    __device__ uint32_t drain() const { return b + 8 * (2 * NR + 12); }
-    __device__ uint32_t drain2() const { return b + 8 * (2 * NR + 13); }
-    __device__ uint32_t group() const { return b + 8 * (2 * NR + 14); }
-    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 15 + i); }
-    __device__ uint32_t stg_empty(int i) const { return b + 8 * (2 * NR + 15 + NS + i); }
+    __device__ uint32_t ofull(int i) const { return b + 8 * (2 * NR + 8 + i); }
+    __device__ uint32_t drain() const { return b + 8 * (2 * NR + 11); }
+    __device__ uint32_t drain2() const { return b + 8 * (2 * NR + 12); }
+    __device__ uint32_t group() const { return b + 8 * (2 * NR + 13); }
+    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 14 + i); }
+    __device__ uint32_t stg_empty(int i) const { return b + 8 * (2 * NR + 14 + NS + i); }
 };
 
 // One ring (K or V) seen by its producer and by the UMMA issuer: slot
@@ -513,9 +520,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int i = 0; i < 3; ++i) {
             mbar_init(BR.sfull(i), 1);
             mbar_init(BR.pfull(i), 2 * NSOFT / 32);   // one arrival per softmax warp of the pair
-            mbar_init(BR.sfree(i), 1);
+            mbar_init(BR.ofull(i), 1);
         }
-        mbar_init(BR.ofull(), 1);
         mbar_init(BR.drain(), 1);
         mbar_init(BR.drain2(), 1);
         mbar_init(BR.group(), NSOFT);
@@ -556,25 +562,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool kq = warp == 0;
             Ring rg = F8 ? Ring{kq ? 0 : NSK, kq ? NSK : NSV, 0u}
                          : Ring{kq ? 0 : NK, kq ? NK : NV, 0u};
+            uint32_t t = 0;   // fp16: tiles loaded so far (tile t uses S buffer t % NSB)
             int seg = 0;
             bool ok = true;
-            // Acquire the next slot of this ring; returns its full barrier.
-            auto acquire = [&](uint32_t& dst, uint32_t& fb) -> bool {
+            // F8: acquire the next staging slot; returns its full barrier.
+            auto acquire_stg = [&](uint32_t& dst, uint32_t& fb) -> bool {
                 const int slot = rg.slot();
-                if constexpr (F8) {
-                    if (!mbar_wait(BR.stg_empty(slot), rg.phase() ^ 1u, abort_flag, P.err))
-                        return false;
-                    dst = s_stg + slot * STG_SLOT;
-                    fb = BR.stg_full(slot);
-                    mbar_arrive_expect_tx(fb, STG_SLOT);
-                    return true;
-                }
-                if (!mbar_wait(BR.empty(slot), rg.phase() ^ 1u, abort_flag, P.err))
-                    return false;
-                dst = s_ring + slot * SLOT_BYTES;
-                fb = BR.full(slot);
-                if (leader) mbar_arrive_expect_tx(fb, 2 * SLOT_BYTES);
-                fb = leader_addr(fb);
+                if (!mbar_wait(BR.stg_empty(slot), rg.phase() ^ 1u, abort_flag, P.err)) return false;
+                dst = s_stg + slot * STG_SLOT;
+                fb = BR.stg_full(slot);
+                mbar_arrive_expect_tx(fb, STG_SLOT);
                 return true;
             };
             while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
@@ -591,13 +588,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                       pt * BM2 + BM * (int)rank);
                 }
                 for (int j = jb; ok && j < je; ++j) {
-                    for (int h = 0; h < SLOTS && ok; ++h) {
-                        uint32_t dst, fb;
-                        if (!acquire(dst, fb)) {
-                            ok = false;
-                            break;
-                        }
-                        if (F8) {
+                    if constexpr (F8) {
+                        for (int h = 0; h < SLOTS && ok; ++h) {
+                            uint32_t dst, fb;
+                            if (!acquire_stg(dst, fb)) {
+                                ok = false;
+                                break;
+                            }
                             // Codes of the same keys and d: K, this CTA's 64 keys x
                             // d 128 h .. 128 h + 127; V, keys (BN / SLOTS) h ..
                             // + BN / SLOTS - 1 x this CTA's DH / 2 d.
@@ -607,21 +604,42 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             else
                                 tma_load_self<MH>(dst, &tm_v, fb, (DH / 2) * (int)rank, kvh,
                                                   j * BN + h * (BN / SLOTS));
-                        } else if (kq) {
-                            // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
-                            for (int cc = 0; cc < 2; ++cc)
-                                tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fb, (2 * h + cc) * 64,
-                                              kvh, j * BN + 64 * (int)rank);
-                        } else {
-                            // V: sub-tiles SUBS h .. SUBS h + SUBS - 1 (32 keys)
-                            // x this CTA's DH / 2 d
-                            for (int ss = 0; ss < SUBS; ++ss)
-                                for (int a = 0; a < VATOMS; ++a)
-                                    tma_load_pair<MH>(dst + ss * SUB_BYTES + a * 4096, &tm_v, fb,
-                                                  (DH / 2) * (int)rank + 64 * a, kvh,
-                                                  j * BN + (SUBS * h + ss) * 32);
+                            ++rg.n;
                         }
-                        ++rg.n;
+                    } else {
+                        // Tile t's slots are free once the UMMAs of tile t - NSB that
+                        // read them have completed: Q.K^T (scores ready) for K, P.V
+                        // (O ready) for V, both committed to this CTA's barriers too.
+                        const uint32_t u = t % NSB;
+                        if (t >= NSB &&
+                            !mbar_wait(kq ? BR.sfull(u) : BR.ofull(u), ((t - NSB) / NSB) & 1,
+                                       abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
+                        const int slot0 = rg.first + (int)u * SLOTS;
+                        const uint32_t fb = BR.full(slot0);
+                        if (leader) mbar_arrive_expect_tx(fb, 2 * SLOTS * SLOT_BYTES);
+                        const uint32_t fbl = leader_addr(fb);
+                        for (int h = 0; h < SLOTS; ++h) {
+                            const uint32_t dst = s_ring + (slot0 + h) * SLOT_BYTES;
+                            if (kq) {
+                                // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
+                                for (int cc = 0; cc < 2; ++cc)
+                                    tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fbl,
+                                                      (2 * h + cc) * 64, kvh,
+                                                      j * BN + 64 * (int)rank);
+                            } else {
+                                // V: sub-tiles SUBS h .. SUBS h + SUBS - 1 (32 keys)
+                                // x this CTA's DH / 2 d
+                                for (int ss = 0; ss < SUBS; ++ss)
+                                    for (int a = 0; a < VATOMS; ++a)
+                                        tma_load_pair<MH>(dst + ss * SUB_BYTES + a * 4096, &tm_v,
+                                                          fbl, (DH / 2) * (int)rank + 64 * a, kvh,
+                                                          j * BN + (SUBS * h + ss) * 32);
+                            }
+                        }
+                        ++t;
                     }
                 }
                 ++seg;
@@ -630,12 +648,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // Unwind: let every copy still in flight land before the CTA exits
                 // (the even CTA's full barriers count both halves; F8 staging
                 // copies complete on each CTA's own barriers).
-                for (int i = 0; i < rg.count; ++i) {
-                    const uint32_t fills =
-                        rg.n > (uint32_t)i ? (rg.n - i + rg.count - 1) / rg.count : 0;
-                    if (fills)
-                        drain_wait(F8 ? BR.stg_full(rg.first + i) : BR.full(rg.first + i),
-                                   (fills - 1) & 1u);
+                if constexpr (F8) {
+                    for (int i = 0; i < rg.count; ++i) {
+                        const uint32_t fills =
+                            rg.n > (uint32_t)i ? (rg.n - i + rg.count - 1) / rg.count : 0;
+                        if (fills) drain_wait(BR.stg_full(rg.first + i), (fills - 1) & 1u);
+                    }
+                } else {
+                    for (uint32_t u = 0; u < NSB; ++u) {
+                        const uint32_t fills = t > u ? (t - u + NSB - 1) / NSB : 0;
+                        if (fills) drain_wait(BR.full(rg.first + (int)u * SLOTS), (fills - 1) & 1u);
+                    }
                 }
                 if (kq && seg > 0 && leader) drain_wait(BR.qfull(), (seg - 1) & 1);
             }
@@ -719,8 +742,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // leave the pipe idle unless something else issues meanwhile.  With
         // three S buffers (DH = 128) two threads of the even CTA issue: warp 1
         // every Q.K^T, warp PV_WARP every P.V, and Q.K^T of tile g waits only
-        // for the P.V of tile g - 3 (sfree), so the chain softmax -> P.V ->
-        // Q.K^T spans three tiles.  With two (DH = 256, where O takes half of
+        // for the P.V of tile g - 3 (its buffer's O-ready barrier), so the chain
+        // softmax -> P.V -> Q.K^T spans three tiles.  With two (DH = 256, where O takes half of
         // tensor memory) warp 1 issues both in one stream: Q.K^T of tile g + 1,
         // then P.V of tile g, the tensor pipe's order keeping Q.K^T of tile
         // g + 2 behind the P.V of tile g that reads the same buffer.
@@ -749,18 +772,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if constexpr (F8) return mbar_test_cl(BR.full(nx.slot()), nx.phase());
             return mbar_test(BR.full(nx.slot()), nx.phase());
         };
+        // fp16 K / V: tile gg's K (V) slots are first + (gg % NSB) * SLOTS ..,
+        // landed when the first one's full barrier completes phase gg / NSB.
+        auto take_tile = [&](int first, uint32_t gg, int& slot0) -> bool {
+            slot0 = first + (int)(gg % NSB) * SLOTS;
+            return mbar_wait(BR.full(slot0), (gg / NSB) & 1, abort_flag, P.err);
+        };
+        auto s_col_of = [&](uint32_t gg) { return SBuf<DH>::COL0 + (gg % NSB) * BN; };
         // Descriptor low words: Q chunk c at q_lo + c * (BM * 128 >> 4); a K
         // slot's chunk cc at + cc * (HALF_SLOT >> 4); a K step of 16
         // elements (32 bytes) at + 2.
         const uint32_t q_lo = desc_lo(s_q, 16);
-        auto issue_qk = [&](uint32_t s_col) -> bool {
-            const uint32_t d = tmem + s_col;
+        auto issue_qk = [&](uint32_t gg) -> bool {
+            const uint32_t d = tmem + s_col_of(gg);
             bool next_ready = false;
+            int slot0 = 0;
+            if constexpr (!F8) {
+                if (!take_tile(0, gg, slot0)) return false;
+            }
 #pragma unroll
             for (int h = 0; h < SLOTS; ++h) {
-                int slot = kr.slot();
-                if (!next_ready && !take(kr, slot)) return false;
-                if (SLOTS > 1 && h == 0) next_ready = peek_next(kr);
+                int slot = slot0 + h;
+                if constexpr (F8) {
+                    slot = kr.slot();
+                    if (!next_ready && !take(kr, slot)) return false;
+                    if (SLOTS > 1 && h == 0) next_ready = peek_next(kr);
+                }
                 const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
@@ -775,19 +812,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             umma_ss_pair_c<true>(d, a, b, IDESC_QK);
                     }
                 }
-                umma_commit_pair(BR.empty(slot));
-                ++kr.n;
+                if constexpr (F8) {
+                    umma_commit_pair(BR.empty(slot));
+                    ++kr.n;
+                }
             }
             return true;
         };
-        auto issue_pv = [&](uint32_t s_col, bool acc0) -> bool {
-            const uint32_t p_base = tmem + s_col;
+        auto issue_pv = [&](uint32_t gg, bool acc0) -> bool {
+            const uint32_t p_base = tmem + s_col_of(gg);
             bool next_ready = false;
+            int slot0 = 0;
+            if constexpr (!F8) {
+                if (!take_tile(NK, gg, slot0)) return false;
+            }
 #pragma unroll
             for (int h = 0; h < SLOTS; ++h) {
-                int slot = vr.slot();
-                if (!next_ready && !take(vr, slot)) return false;
-                if (SLOTS > 1 && h == 0) next_ready = peek_next(vr);
+                int slot = slot0 + h;
+                if constexpr (F8) {
+                    slot = vr.slot();
+                    if (!next_ready && !take(vr, slot)) return false;
+                    if (SLOTS > 1 && h == 0) next_ready = peek_next(vr);
+                }
                 // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
                 // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
                 const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
@@ -806,28 +852,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             umma_ts_pair_c<true>(tmem + O_COL, a_tmem, b, IDESC_PV);
                     }
                 }
-                umma_commit_pair(BR.empty(slot));
-                ++vr.n;
+                if constexpr (F8) {
+                    umma_commit_pair(BR.empty(slot));
+                    ++vr.n;
+                }
             }
-            return true;
-        };
-        auto s_col_of = [&](uint32_t gg) { return SBuf<DH>::COL0 + (gg % NSB) * BN; };
-        // Q.K^T of tile gg into its S buffer, then the scores-ready commit (and
-        // the Q-free commit after the segment's last one).
-        auto qk_step = [&](uint32_t gg, bool last_of_seg) -> bool {
-            if (!issue_qk(s_col_of(gg))) return false;
-            umma_commit_pair(BR.sfull(gg % NSB));
-            if (last_of_seg) umma_commit_pair(BR.qempty());
-            return true;
-        };
-        // P.V of tile gg once its P is ready, then the O-ready (and, with two
-        // issuers, the S-buffer-free) commits.
-        auto pv_step = [&](uint32_t gg, bool acc) -> bool {
-            if (!mbar_wait(BR.pfull(gg % NSB), (gg / NSB) & 1, abort_flag, P.err)) return false;
-            tc_fence_after();
-            if (!issue_pv(s_col_of(gg), acc)) return false;
-            umma_commit_pair(BR.ofull());
-            if (TWO_ISSUERS) umma_commit_pair(BR.sfree(gg % NSB));
             return true;
         };
         while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
@@ -842,26 +871,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int j = jb; ok && j < je; ++j) {
                     const uint32_t gg = g + (j - jb);
                     if (qk_role) {
+                        // S buffer gg % NSB is free once the P.V of tile gg - NSB
+                        // (which read its P) has completed.
                         if (gg >= NSB) {
-                            ok = mbar_wait(BR.sfree(gg % NSB), ((gg - NSB) / NSB) & 1, abort_flag,
+                            ok = mbar_wait(BR.ofull(gg % NSB), ((gg - NSB) / NSB) & 1, abort_flag,
                                            P.err);
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        ok = qk_step(gg, j == je - 1);
+                        ok = issue_qk(gg);
+                        if (!ok) break;
+                        umma_commit_pair(BR.sfull(gg % NSB));
+                        if (j == je - 1) umma_commit_pair(BR.qempty());
                     } else {
-                        ok = pv_step(gg, j > jb);
+                        ok = mbar_wait(BR.pfull(gg % NSB), (gg / NSB) & 1, abort_flag, P.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        ok = issue_pv(gg, j > jb);
+                        if (!ok) break;
+                        umma_commit_pair(BR.ofull(gg % NSB));
                     }
                 }
             } else {
-                ok = issue_qk(s_col_of(g));
+                ok = issue_qk(g);
                 if (!ok) break;
                 umma_commit_pair(BR.sfull(g & 1));
                 if (je - jb == 1) umma_commit_pair(BR.qempty());
                 for (int j = jb; j < je; ++j) {
                     const uint32_t gg = g + (j - jb);
                     if (j + 1 < je) {
-                        ok = issue_qk(s_col_of(gg + 1));
+                        ok = issue_qk(gg + 1);
                         if (!ok) break;
                         umma_commit_pair(BR.sfull((gg + 1) & 1));
                         if (j + 1 == je - 1) umma_commit_pair(BR.qempty());
@@ -871,9 +910,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
-                    ok = issue_pv(s_col_of(gg), j > jb);
+                    ok = issue_pv(gg, j > jb);
                     if (!ok) break;
-                    umma_commit_pair(BR.ofull());
+                    umma_commit_pair(BR.ofull(gg & 1));
                 }
             }
             g += je - jb;
@@ -961,7 +1000,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 } else {
                     const bool need = mx > m_ref + RESCALE_THRESHOLD;
                     if (__any_sync(0xffffffffu, need)) {
-                        ok = mbar_wait(BR.ofull(), (gg - 1) & 1, abort_flag, P.err);
+                        ok = mbar_wait(BR.ofull((gg - 1) % NSB), ((gg - 1) / NSB) & 1,
+                                       abort_flag, P.err);
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                         tc_fence_after();
@@ -1006,7 +1046,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 l += (l0 + l1) + (l2 + l3);
                 tmem_st_wait();
                 if (j > jb && !o_seen) {
-                    ok = mbar_wait(BR.ofull(), (gg - 1) & 1, abort_flag, P.err);
+                    ok = mbar_wait(BR.ofull((gg - 1) % NSB), ((gg - 1) / NSB) & 1, abort_flag,
+                                   P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
@@ -1020,7 +1061,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
             const uint32_t gl = g + (je - jb) - 1;
-            ok = mbar_wait(BR.ofull(), gl & 1, abort_flag, P.err);
+            ok = mbar_wait(BR.ofull(gl % NSB), (gl / NSB) & 1, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
