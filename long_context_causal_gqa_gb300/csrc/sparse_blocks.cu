@@ -11,8 +11,11 @@
 //
 // * Persistent CTAs, one per SM, walk the rows (row = cta, cta + G, ...).  A
 //   row's keys come in tiles of 128 (32 blocks); all 6 heads share them.
-// * Gather: four warps issue 16-byte cp.async copies, one warp-wide 512-byte
-//   copy per token row of K or V, straight into a 128B-swizzled smem tile;
+// * Gather: sixteen warps (eight for K, eight for V; eight in all at head
+//   size 128 or for up to 16 heads) issue 16-byte cp.async copies, one
+//   warp-wide 512-byte copy per token row, straight into a
+//   128B-swizzled smem tile (a warp's copies issue at about 8 bytes per cycle,
+//   so the rate grows with the warps that issue them);
 //   tokens that are masked (past p, past the list, or a bad id) are
 //   zero-filled, so stale cache contents (even NaN) never reach the MMA.
 //   Completion is counted on mbarriers (cp.async.mbarrier.arrive.noinc).
@@ -31,7 +34,7 @@
 //   scale and the V scale the final 1 / l.
 //
 // * Token index warp: block-table lookups (a selected id, then a page id, two
-//   dependent loads per key) are taken off the gather warps' path: warp 9
+//   dependent loads per key) are taken off the gather warps' path: the index warp
 //   resolves each tile's keys to cache token rows ahead of them, through a
 //   ring of NI shared-memory slots that the gather warps and the key warps
 //   both read (a key whose row is -1 is masked in the copy and the softmax).
@@ -41,8 +44,9 @@
 //   SEEN_BITS; beyond that a hash of the id, with a hit confirmed against the
 //   earlier positions), masks the repeat and flags it on the device.
 //
-// Warp roles (320 threads): 0..3 gather, 4 TMEM owner + UMMA issuer,
-// 5..8 key warps (softmax + epilogue; thread = TMEM lane), 9 token index.
+// Warp roles: gather warps (sixteen or eight for an fp16 cache, four for
+// E4M3), then the TMEM owner + UMMA issuer, four key warps (softmax +
+// epilogue; thread = TMEM lane) and the token index warp.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -58,7 +62,18 @@ namespace sparse {
 constexpr int TILE = 128;            // keys per tile
 constexpr int BLK = 4;               // tokens per selected block
 constexpr int NP = 16;               // the heads of one launch padded to the UMMA N granule
-constexpr int NTHREADS = 320;
+// Gather warps: a warp-wide 16-byte cp.async copy issues at about 8 bytes per
+// cycle per warp, whatever the number of warps (measured: 4 warps move 32, 8
+// warps 50, 16 warps 69 bytes per cycle per SM of 512-byte rows from L2), so
+// the fp16 path gathers with sixteen warps (eight for K, eight for V) at head
+// size 256 with 6 heads, eight at head size 128 (sixteen measured no faster)
+// and for up to 16 heads (whose key warps need the registers); the E4M3
+// path's four warps load, convert and store their codes themselves.
+template <int HQ, bool F8, int DH>
+constexpr int gather_warps() { return F8 ? 4 : (DH == 256 && HQ != NP ? 16 : 8); }
+// Warps: gather warps, then the UMMA issuer, four key warps, the index warp.
+template <int HQ, bool F8, int DH>
+constexpr int nthreads() { return 32 * (gather_warps<HQ, F8, DH>() + 6); }
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Params {
@@ -175,7 +190,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
 // holds E4M3 codes, converted to fp16 on the way into shared memory.  DH: head
 // size, 256 or 128.
 template <int HQ, bool F8, int DH>
-__global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
+__global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const Params P) {
     using L = SL<DH>;
     constexpr int HALVES = DH / 128;   // 128-d halves of a row (one M = 128 P.V each)
     constexpr int KV_TILE_BYTES = L::KV_TILE_BYTES;
@@ -194,7 +209,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     constexpr uint32_t VOFF = OFF_V;
     // Copy completions counted per tile: fp16, two warps of 32 lanes per K or
     // V tile (and the K warps load Q); E4M3, all four gather warps.
-    constexpr int NGATHER = F8 ? 128 : 64;
+    constexpr int NGW = gather_warps<HQ, F8, DH>();
+    constexpr int NTHREADS = nthreads<HQ, F8, DH>();
+    constexpr int MMA_WARP = NGW, KEY_WARP0 = NGW + 1, IDX_WARP = NGW + 5;
+    // Arrivals per K or V tile: every gather thread of the operand (fp16: the
+    // operand's NGW / 2 warps; E4M3: all four warps handle both operands).
+    constexpr int NGATHER = F8 ? 128 : 32 * (NGW / 2);
+    constexpr int NQLOAD = 128;   // threads that load Q and arrive on its barrier
     constexpr uint32_t SOFF = 2u * KV_TILE_BYTES;
     constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
     constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
@@ -218,7 +239,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_VFULL + b), NGATHER);
             mbar_init(bar(B_VEMPTY + b), 1);
-            mbar_init(bar(B_QFULL + b), NGATHER);
+            mbar_init(bar(B_QFULL + b), NQLOAD);
             mbar_init(bar(B_QEMPTY + b), 1);
             mbar_init(bar(B_SFULL + b), 1);
             mbar_init(bar(B_PREADY + b), 128);
@@ -228,7 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         mbar_init(bar(B_GROUP), 128);
         for (int b = 0; b < NI; ++b) {
             mbar_init(bar(B_IFULL + b), 32);
-            mbar_init(bar(B_IEMPTY + b), 256);
+            mbar_init(bar(B_IEMPTY + b), 32 * NGW + 128);   // gather and key threads
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -236,7 +257,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     // Zero both Q buffers once (rows 6..15 stay zero).
     for (int u = threadIdx.x; u < 2 * Q_BYTES / 16; u += NTHREADS)
         *reinterpret_cast<uint4*>(gbase + OFF_Q + u * 16) = make_uint4(0, 0, 0, 0);
-    if (warp == 4) {
+    if (warp == MMA_WARP) {
         tmem_alloc(smem_u32(tmem_ptr), TMEM_COLS);
         tmem_relinquish();
     }
@@ -246,30 +267,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
     tc_fence_after();
     const uint32_t tmem = *tmem_ptr;
 
-    if (warp < 4) {
+    if (warp < NGW) {
         // ------------------------------------------------------------ gather
-        const int gt = threadIdx.x;        // 0..127
+        const int gt = threadIdx.x;        // 0 .. 32 NGW - 1
         const int* idx = reinterpret_cast<const int*>(gbase + OFF_IDX);
         const size_t tok_stride = HQ == NP ? (size_t)P.kv_stride : (size_t)DH;
-        // Cache row offset of this lane's key in tile-counter position gg, read
+        // Cache row offset of key kbase + lane of tile-counter position gg, read
         // from the index ring; tok < 0 for a masked key.
-        auto take_index = [&](uint32_t gg, int& tok, size_t& row) -> bool {
+        auto take_index = [&](uint32_t gg, int kbase, int& tok, size_t& row) -> bool {
             const int slot = (int)(gg % NI);
             if (!mbar_wait(bar(B_IFULL + slot), (gg / NI) & 1, abort_flag, P.err)) return false;
-            tok = idx[slot * TILE + warp * 32 + lane];
+            tok = idx[slot * TILE + min(kbase + lane, TILE - 1)];
             mbar_arrive(bar(B_IEMPTY + slot));
             row = tok >= 0 ? (size_t)tok * tok_stride : 0;
-            return true;
-        };
-        // fp16 gather: the rows of keys kbase + lane and kbase + 32 + lane.
-        auto take_index2 = [&](uint32_t gg, int kbase, int (&tok)[2], size_t (&row)[2]) -> bool {
-            const int slot = (int)(gg % NI);
-            if (!mbar_wait(bar(B_IFULL + slot), (gg / NI) & 1, abort_flag, P.err)) return false;
-            tok[0] = idx[slot * TILE + kbase + lane];
-            tok[1] = idx[slot * TILE + kbase + 32 + lane];
-            mbar_arrive(bar(B_IEMPTY + slot));
-            row[0] = tok[0] >= 0 ? (size_t)tok[0] * tok_stride : 0;
-            row[1] = tok[1] >= 0 ? (size_t)tok[1] * tok_stride : 0;
             return true;
         };
         uint32_t g = 0;                     // global tile counter
@@ -285,15 +295,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
             const int nt = row_tiles(cnt);
             if (nt == 0) continue;
             // Q row i (nh heads x DH d) -> Q buffer rloc & 1, rows 0 .. nh - 1,
-            // by the NGATHER threads that count on QFULL (the K warps with an
-            // fp16 cache, all four gather warps with E4M3 codes).
+            // by the NQLOAD threads that count on QFULL (the first gather warps).
             const int qb = rloc & 1;
-            if (gt < NGATHER) {
+            if (gt < NQLOAD) {
                 if (!mbar_wait(bar(B_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
-                for (int u = gt; u < nh * (DH / 8); u += NGATHER) {
+                for (int u = gt; u < nh * (DH / 8); u += NQLOAD) {
                     const int h = u / (DH / 8), c16 = u % (DH / 8);
                     const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
                                          sw128(h, c16 % 8);
@@ -334,7 +343,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     asm volatile("cp.async.commit_group;" ::: "memory");
                 };
                 if (!staged) {
-                    if (!take_index(g, f8_tok, f8_row)) {
+                    if (!take_index(g, warp * 32, f8_tok, f8_row)) {
                         ok = false;
                         break;
                     }
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                     // The next step's codes (V of this tile, or K of the next) go
                     // into the other staging buffer, converted one step ago.
                     if (n + 1 < 2 * nt) {
-                        if (kv == 1 && !take_index(tg + 1, f8_tok, f8_row)) {
+                        if (kv == 1 && !take_index(tg + 1, warp * 32, f8_tok, f8_row)) {
                             ok = false;
                             break;
                         }
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                                row_tiles(min(max(__ldg(P.sel_cnt + i2), 0), P.max_sel)) == 0)
                             i2 += P.G;
                         if (i2 < P.rows) {
-                            if (!take_index(tg + 1, f8_tok, f8_row)) {
+                            if (!take_index(tg + 1, warp * 32, f8_tok, f8_row)) {
                                 ok = false;
                                 break;
                             }
@@ -405,24 +414,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 }
                 g += (uint32_t)nt;
             } else {
-                // fp16: warps 0, 1 gather K and warps 2, 3 V, each warp the keys
-                // kbase .. kbase + 63 of every tile, so the K stream runs ahead of
-                // the V stream (K's single buffer frees once its Q.K^T is done, V's
-                // two buffers after each P.V).  A key's row is DH * 2 bytes, one
+                // fp16: warps 0 .. NGW / 2 - 1 gather K and the others V, each
+                // warp KPW keys of every tile, so the K stream runs ahead of the V
+                // stream (K's single buffer frees once its Q.K^T is done, V's two
+                // buffers after each P.V).  A key's row is DH * 2 bytes, one
                 // warp-wide copy per 512 / (DH * 2) keys.
-                const bool kg = warp < 2;
-                const int kbase = (warp & 1) * 64;
+                constexpr int KW = NGW / 2;        // warps per operand
+                constexpr int KPW = TILE / KW;     // keys per warp: 32 or 16
+                static_assert(KPW <= 32 && TILE == KPW * KW, "keys per warp");
+                const bool kg = warp < KW;
+                const int kbase = (warp % KW) * KPW;
                 constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
                 constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
                 const int ul = lane % LPK;        // lane covers d = 8 ul .. 8 ul + 7
                 const __half* cache = kg ? P.kcache : P.vcache;
                 for (int t = 0; t < nt && ok; ++t, ++g) {
-                    int tok2[2];
-                    size_t row2[2];
-                    if (!take_index2(g, kbase, tok2, row2)) {
+                    int tok1;
+                    size_t row1;
+                    if (!take_index(g, kbase, tok1, row1)) {
                         ok = false;
                         break;
                     }
+                    // (lanes KPW .. 31 read keys of the next warp; their values are unused)
                     uint32_t tile, fullb;
                     if (kg) {
                         if (!mbar_wait(bar(B_KEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
@@ -440,26 +453,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                         tile = sbase + OFF_V + vb * KV_TILE_BYTES;
                         fullb = bar(B_VFULL + vb);
                     }
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll 4
-                        for (int e = 0; e < 32 / KPI; ++e) {
-                            const int src = KPI * e + lane / LPK;   // lane holding this key's row
-                            const int key = kbase + 32 * hf + src;
-                            const int tok = __shfl_sync(0xffffffffu, tok2[hf], src);
-                            const size_t row = __shfl_sync(0xffffffffu, row2[hf], src);
-                            // chunk ul / 8, unit ul % 8 of the key's swizzled row
-                            const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
-                            const __half* sp = tok >= 0 ? cache + row + ul * 8 : cache;
-                            cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
-                        }
+                    for (int e = 0; e < KPW / KPI; ++e) {
+                        const int src = KPI * e + lane / LPK;   // lane holding this key's row
+                        const int key = kbase + src;
+                        const int tok = __shfl_sync(0xffffffffu, tok1, src);
+                        const size_t row = __shfl_sync(0xffffffffu, row1, src);
+                        // chunk ul / 8, unit ul % 8 of the key's swizzled row
+                        const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
+                        const __half* sp = tok >= 0 ? cache + row + ul * 8 : cache;
+                        cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
                     }
                     cp_async_arrive(fullb);
                 }
             }
         }
         if (!ok) asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 4) {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
             uint32_t g = 0;
@@ -532,7 +542,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
                 drain_wait(bar(B_DRAIN), 0);
             }
         }
-    } else if (warp < 9) {
+    } else if (warp < KEY_WARP0 + 4) {
         // ------------------------------------------------------------ key warps
         const int wq = warp & 3;
         const int k = wq * 32 + lane;
@@ -707,7 +717,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
         }
     }
 
-    if (warp == 9) {
+    if (warp == IDX_WARP) {
         // ------------------------------------------------------------ token index
         // Same walk as the gather warps (rows of this CTA, tiles of each
         // non-empty row).  Lane l resolves selected position 32 t + l of the
@@ -794,7 +804,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_kernel(const Params P) {
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -833,14 +843,18 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
     const bool six = (grp == kHq && Hkv == 1);
     using KernelFn = void (*)(Params);
     KernelFn fn;
-    int smem;
+    int smem, threads;
     if (Dh == 128) {
         fn = e4m3 ? (six ? sparse_kernel<kHq, true, 128> : sparse_kernel<NP, true, 128>)
                   : (six ? sparse_kernel<kHq, false, 128> : sparse_kernel<NP, false, 128>);
+        threads = e4m3 ? (six ? nthreads<kHq, true, 128>() : nthreads<NP, true, 128>())
+                       : (six ? nthreads<kHq, false, 128>() : nthreads<NP, false, 128>());
         smem = smem_bytes<128>();
     } else {
         fn = e4m3 ? (six ? sparse_kernel<kHq, true, 256> : sparse_kernel<NP, true, 256>)
                   : (six ? sparse_kernel<kHq, false, 256> : sparse_kernel<NP, false, 256>);
+        threads = e4m3 ? (six ? nthreads<kHq, true, 256>() : nthreads<NP, true, 256>())
+                       : (six ? nthreads<kHq, false, 256>() : nthreads<NP, false, 256>());
         smem = smem_bytes<256>();
     }
     if (ensure_smem_limit(reinterpret_cast<const void*>(fn), smem) != GQA_OK)
@@ -857,7 +871,7 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
         P.vcache = reinterpret_cast<const __half*>(vb);
         P.kcache8 = kb;
         P.vcache8 = vb;
-        fn<<<P.G, NTHREADS, smem, stream>>>(P);
+        fn<<<P.G, threads, smem, stream>>>(P);
         if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
     return GQA_OK;
