@@ -28,7 +28,8 @@
 //
 // * An E4M3 cache (the tail's storage applied to this workload) halves the
 //   gathered bytes: the gather lanes load the code bytes of their token rows
-//   (16 loads in flight per lane), convert them to fp16 with
+//   into registers (a tile's loads all in flight before the lane waits for
+//   the tile buffer), convert them to fp16 with
 //   cvt.rn.f16x2.e4m3x2 and store them into the same swizzled tile the fp16
 //   path copies into, so the MMAs are unchanged; the K scale joins the score
 //   scale and the V scale the final 1 / l.
@@ -70,7 +71,7 @@ constexpr int NP = 16;               // the heads of one launch padded to the UM
 // and for up to 16 heads (whose key warps need the registers); the E4M3
 // path's four warps load, convert and store their codes themselves.
 template <int HQ, bool F8, int DH>
-constexpr int gather_warps() { return F8 ? 4 : (DH == 256 && HQ != NP ? 16 : 8); }
+constexpr int gather_warps() { return DH == 256 && HQ != NP ? 16 : 8; }
 // Warps: gather warps, then the UMMA issuer, four key warps, the index warp.
 template <int HQ, bool F8, int DH>
 constexpr int nthreads() { return 32 * (gather_warps<HQ, F8, DH>() + 6); }
@@ -106,7 +107,7 @@ template <int DH>
 struct SL {
     static constexpr int KV_TILE_BYTES = TILE * DH * 2;            // 64 / 32 KB
     static constexpr int OFF_K = 0;                                // 1 K tile
-    static constexpr int OFF_V = OFF_K + KV_TILE_BYTES;            // 2 V tiles (fp16 cache)
+    static constexpr int OFF_V = OFF_K + KV_TILE_BYTES;            // 2 V tiles
     static constexpr int Q_BYTES = NP * DH * 2;                    // DH / 64 chunks [16][64]
     static constexpr int OFF_Q = OFF_V + 2 * KV_TILE_BYTES;        // 2 Q buffers
     static constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;             // 2 P^T buffers
@@ -200,23 +201,18 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
     constexpr int OFF_SEEN = L::OFF_SEEN, OFF_BAR = L::OFF_BAR, OFF_TMEM = off_tmem<DH>();
     const int nh = (HQ == NP) ? P.nh : HQ;
     const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * DH;
-    // Tile buffers: one K tile and two V tiles (the K tile is free again as
-    // soon as its Q.K^T is done, a V tile only after the softmax and P.V);
-    // with E4M3 codes one K tile, one V tile, and the code staging in the
-    // second V tile's place.
-    constexpr int NVB = F8 ? 1 : 2;
+    // Tile buffers (fp16, whatever the cache holds): one K tile and two V
+    // tiles (the K tile is free again as soon as its Q.K^T is done, a V tile
+    // only after the softmax and P.V).
+    constexpr int NVB = 2;
     constexpr uint32_t KOFF = OFF_K;
     constexpr uint32_t VOFF = OFF_V;
-    // Copy completions counted per tile: fp16, two warps of 32 lanes per K or
-    // V tile (and the K warps load Q); E4M3, all four gather warps.
     constexpr int NGW = gather_warps<HQ, F8, DH>();
     constexpr int NTHREADS = nthreads<HQ, F8, DH>();
     constexpr int MMA_WARP = NGW, KEY_WARP0 = NGW + 1, IDX_WARP = NGW + 5;
-    // Arrivals per K or V tile: every gather thread of the operand (fp16: the
-    // operand's NGW / 2 warps; E4M3: all four warps handle both operands).
-    constexpr int NGATHER = F8 ? 128 : 32 * (NGW / 2);
+    // Arrivals per K or V tile: every thread of the operand's NGW / 2 gather warps.
+    constexpr int NGATHER = 32 * (NGW / 2);
     constexpr int NQLOAD = 128;   // threads that load Q and arrive on its barrier
-    constexpr uint32_t SOFF = 2u * KV_TILE_BYTES;
     constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
     constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, false);
     extern __shared__ uint8_t smem_raw[];
@@ -285,11 +281,6 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
         uint32_t g = 0;                     // global tile counter
         int rloc = 0;                       // non-empty rows handled so far
         bool ok = true;
-        // E4M3: the first K codes of a row are staged by the previous row's last
-        // step, so that the copy pipeline does not drain between rows.
-        bool staged = false;
-        int f8_tok = -1;
-        size_t f8_row = 0;
         for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
             const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
             const int nt = row_tiles(cnt);
@@ -311,119 +302,81 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
                 cp_async_arrive(bar(B_QFULL + qb));
             }
             ++rloc;
+            // Warps 0 .. NGW / 2 - 1 gather K and the others V, each warp KPW
+            // keys of every tile, so the K stream runs ahead of the V stream
+            // (K's single buffer frees once its Q.K^T is done, V's two buffers
+            // after each P.V).
+            constexpr int KW = NGW / 2;        // warps per operand
+            constexpr int KPW = TILE / KW;     // keys per warp: 32 or 16
+            static_assert(KPW <= 32 && TILE == KPW * KW, "keys per warp");
+            const bool kg = warp < KW;
+            const int kbase = (warp % KW) * KPW;
             if constexpr (F8) {
-                // E4M3 codes.  Each gather lane copies the 16-byte code chunks it
-                // will convert into a private, double-buffered staging area
-                // (buffer b, pass e: byte (b * NPASS + e) * 2048 + 16 gt), one
-                // step (tile t, K or V) ahead of the step it converts; it then
-                // waits for its own copies of the current step, converts them to
-                // fp16 into the step's tile and signals it.  A token row is DH
-                // code bytes: a group of LPK = DH / 16 lanes takes key KPP e +
-                // group, lane u of it the codes of d = 16u .. 16u + 15, which
-                // become fp16 units 2u, 2u + 1 of the row (chunk u / 4, units
-                // 2 (u % 4) and 2 (u % 4) + 1 within it).  Masked tokens are
-                // zero-filled by the copy.
+                // E4M3 codes: a token row is DH code bytes; a group of LPK = DH / 16
+                // lanes takes key KPP e + group, lane u of it the codes of d = 16u ..
+                // 16u + 15, which become fp16 units 2u, 2u + 1 of the row (chunk
+                // u / 4, units 2 (u % 4) and 2 (u % 4) + 1 within it).  A warp loads
+                // all its code chunks of a tile into registers before it waits for
+                // the tile buffer, so the loads' latency overlaps the wait; masked
+                // tokens convert from zero codes.
                 constexpr int LPK = DH / 16;      // lanes per key row: 16 or 8
-                constexpr int KPP = 32 / LPK;     // keys per pass: 2 or 4
-                constexpr int NPASS = 32 / KPP;   // passes per warp's 32 keys: 16 or 8
+                constexpr int KPP = 32 / LPK;     // keys per load: 2 or 4
+                constexpr int NPASS = KPW / KPP;  // loads per lane per tile
                 const int u = lane % LPK, half = lane / LPK;
                 const uint32_t unit = 2u * (uint32_t)(u & 3);
-                auto stage_addr = [&](int b, int e) -> uint32_t {
-                    return sbase + SOFF + (uint32_t)((b * NPASS + e) * 2048 + gt * 16);
-                };
-                auto issue = [&](int b, const uint8_t* cache, int tok_l, size_t row_l) {
-#pragma unroll
-                    for (int e = 0; e < NPASS; ++e) {
-                        const int src = KPP * e + half;
-                        const int tok = __shfl_sync(0xffffffffu, tok_l, src);
-                        const size_t row = __shfl_sync(0xffffffffu, row_l, src);
-                        const uint8_t* p = tok >= 0 ? cache + row + 16 * u : cache;
-                        cp_async16(stage_addr(b, e), p, tok >= 0 ? 16u : 0u);
-                    }
-                    asm volatile("cp.async.commit_group;" ::: "memory");
-                };
-                if (!staged) {
-                    if (!take_index(g, warp * 32, f8_tok, f8_row)) {
+                const uint8_t* cache = kg ? P.kcache8 : P.vcache8;
+                for (int t = 0; t < nt && ok; ++t, ++g) {
+                    int tok1;
+                    size_t row1;
+                    if (!take_index(g, kbase, tok1, row1)) {
                         ok = false;
                         break;
                     }
-                    issue(0, P.kcache8, f8_tok, f8_row);
-                }
-                staged = false;
-                for (int n = 0; n < 2 * nt && ok; ++n) {
-                    const int t = n >> 1, kv = n & 1;
-                    const uint32_t tg = g + (uint32_t)t;      // tile counter of this step
-                    // The next step's codes (V of this tile, or K of the next) go
-                    // into the other staging buffer, converted one step ago.
-                    if (n + 1 < 2 * nt) {
-                        if (kv == 1 && !take_index(tg + 1, warp * 32, f8_tok, f8_row)) {
-                            ok = false;
-                            break;
-                        }
-                        issue((n + 1) & 1, kv == 0 ? P.vcache8 : P.kcache8, f8_tok, f8_row);
-                        asm volatile("cp.async.wait_group 1;" ::: "memory");
-                    } else {
-                        // The row's last step: stage the first K codes of this
-                        // CTA's next non-empty row (its first tile is tile
-                        // counter tg + 1; 2 nt steps per row keep the buffer
-                        // parity at 0).
-                        int i2 = i + P.G;
-                        while (i2 < P.rows &&
-                               row_tiles(min(max(__ldg(P.sel_cnt + i2), 0), P.max_sel)) == 0)
-                            i2 += P.G;
-                        if (i2 < P.rows) {
-                            if (!take_index(tg + 1, warp * 32, f8_tok, f8_row)) {
-                                ok = false;
-                                break;
-                            }
-                            issue(0, P.kcache8, f8_tok, f8_row);
-                            staged = true;
-                            asm volatile("cp.async.wait_group 1;" ::: "memory");
-                        } else {
-                            asm volatile("cp.async.wait_group 0;" ::: "memory");
-                        }
-                    }
-                    if (kv == 0) {
-                        if (!mbar_wait(bar(B_KEMPTY), (tg & 1) ^ 1, abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                    } else {
-                        if (!mbar_wait(bar(B_VEMPTY), (tg & 1) ^ 1, abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    const uint32_t chunk = sbase + (kv == 0 ? KOFF : VOFF) +
-                                           (uint32_t)(u >> 2) * (TILE * 128);
+                    uint4 code[NPASS];
 #pragma unroll
                     for (int e = 0; e < NPASS; ++e) {
-                        const uint32_t key = (uint32_t)(warp * 32 + KPP * e + half);
-                        const uint4 r = *reinterpret_cast<const uint4*>(
-                            gbase + (stage_addr(n & 1, e) - sbase));
+                        const int src = KPP * e + half;
+                        const int tok = __shfl_sync(0xffffffffu, tok1, src);
+                        const size_t row = __shfl_sync(0xffffffffu, row1, src);
+                        code[e] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(cache + row + 16 * u))
+                                           : make_uint4(0, 0, 0, 0);
+                    }
+                    uint32_t tile, fullb;
+                    if (kg) {
+                        if (!mbar_wait(bar(B_KEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tile = OFF_K;
+                        fullb = bar(B_KFULL);
+                    } else {
+                        const int vb = g & 1;
+                        if (!mbar_wait(bar(B_VEMPTY + vb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tile = OFF_V + vb * KV_TILE_BYTES;
+                        fullb = bar(B_VFULL + vb);
+                    }
+                    const uint32_t chunk = tile + (uint32_t)(u >> 2) * (TILE * 128);
+#pragma unroll
+                    for (int e = 0; e < NPASS; ++e) {
+                        const uint32_t key = (uint32_t)(kbase + KPP * e + half);
+                        const uint4 r = code[e];
                         const uint4 lo = make_uint4(e4m3x2_to_f16x2(r.x), e4m3x2_to_f16x2(r.x >> 16),
                                                     e4m3x2_to_f16x2(r.y), e4m3x2_to_f16x2(r.y >> 16));
                         const uint4 hi = make_uint4(e4m3x2_to_f16x2(r.z), e4m3x2_to_f16x2(r.z >> 16),
                                                     e4m3x2_to_f16x2(r.w), e4m3x2_to_f16x2(r.w >> 16));
-                        *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit) - sbase)) = lo;
-                        *reinterpret_cast<uint4*>(gbase + (chunk + sw128(key, unit + 1) - sbase)) = hi;
+                        *reinterpret_cast<uint4*>(gbase + chunk + sw128(key, unit)) = lo;
+                        *reinterpret_cast<uint4*>(gbase + chunk + sw128(key, unit + 1)) = hi;
                     }
                     // Generic-proxy stores, read by the tensor cores (async proxy).
                     fence_async_shared();
-                    mbar_arrive(bar(kv == 0 ? B_KFULL : B_VFULL));
+                    mbar_arrive(fullb);
                 }
-                g += (uint32_t)nt;
             } else {
-                // fp16: warps 0 .. NGW / 2 - 1 gather K and the others V, each
-                // warp KPW keys of every tile, so the K stream runs ahead of the V
-                // stream (K's single buffer frees once its Q.K^T is done, V's two
-                // buffers after each P.V).  A key's row is DH * 2 bytes, one
-                // warp-wide copy per 512 / (DH * 2) keys.
-                constexpr int KW = NGW / 2;        // warps per operand
-                constexpr int KPW = TILE / KW;     // keys per warp: 32 or 16
-                static_assert(KPW <= 32 && TILE == KPW * KW, "keys per warp");
-                const bool kg = warp < KW;
-                const int kbase = (warp % KW) * KPW;
+                // fp16: a key's row is DH * 2 bytes, one warp-wide 16-byte-per-lane
+                // copy per 512 / (DH * 2) keys, straight into the swizzled tile.
                 constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
                 constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
                 const int ul = lane % LPK;        // lane covers d = 8 ul .. 8 ul + 7
