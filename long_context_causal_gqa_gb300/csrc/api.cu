@@ -142,32 +142,6 @@ bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
-bool make_map_u8_plain(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
-                       uint64_t rows, uint64_t head_stride, uint64_t row_stride, uint32_t box_d,
-                       uint32_t box_rows, bool three_d) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    CUresult r;
-    if (three_d) {
-        cuuint64_t dims[3] = {d, heads, rows};
-        cuuint64_t strides[2] = {head_stride, row_stride};
-        cuuint32_t box[3] = {box_d, 1, box_rows};
-        cuuint32_t estr[3] = {1, 1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        cuuint64_t dims[2] = {d, rows};
-        cuuint64_t strides[1] = {row_stride};
-        cuuint32_t box[2] = {box_d, box_rows};
-        cuuint32_t estr[2] = {1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace gqa
 
 using namespace gqa;

@@ -65,14 +65,6 @@ bool make_map_3d_f16(CUtensorMap* map, const void* base, uint64_t d, uint64_t he
 bool make_map_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t row_stride, uint32_t box_rows, uint32_t box_cols);
 
-// uint8 tensor (d, heads, rows) -- or (d, rows) when three_d is false -- with
-// heads head_stride bytes apart and rows row_stride bytes apart (multiples of
-// 16), a box of box_d bytes x 1 head x box_rows rows, no swizzle (rows land
-// box_d bytes apart in shared memory).
-bool make_map_u8_plain(CUtensorMap* map, const void* base, uint64_t d, uint64_t heads,
-                       uint64_t rows, uint64_t head_stride, uint64_t row_stride, uint32_t box_d,
-                       uint32_t box_rows, bool three_d);
-
 // Exact unsigned division by a divisor fixed per launch, for dividends below
 // 2^31: the multiply-high method of Granlund and Montgomery ("Division by
 // invariant integers using multiplication", 1994, section 4), with

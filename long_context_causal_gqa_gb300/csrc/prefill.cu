@@ -83,8 +83,6 @@ constexpr int COLS = BN / NWG;                // S columns per softmax thread
 constexpr int NSOFT = 128 * NWG;              // softmax threads per CTA
 constexpr int V_WARP = 2 + NSOFT / 32;
 constexpr int XCH_BYTES = 3 * NWG * BM * 4;  // part maxima [parity][part][row], sums [part][row]
-// E4M3 staging slot: this CTA's codes of one fp16 ring slot (8 KB).
-constexpr int STG_SLOT = 8192;
 
 // S buffers follow O in tensor memory: two of 128 columns after a 256-column
 // O (DH = 256), three after a 128-column O (DH = 128).
@@ -99,31 +97,27 @@ struct SBuf {
 // when the Q.K^T into the same-numbered S buffer has completed (its
 // scores-ready barrier) and a V tile's when the P.V of that tile has (its
 // O-ready barrier): no per-slot release barriers or commits.
-// F8 (K and V stored as FP8-E4M3 codes): each CTA's TMA
-// brings its codes into staging slots, and four converter warps (two for K,
-// two for V, each half of a slot) write them as fp16 into the ring slots the
-// UMMAs read; the fp16 ring shrinks to make room for the staging ring.  Up to
-// 16 warps share the same register limit (128 per thread at 4 warps per
-// scheduler), so the converters cost no registers beyond 13 warps.
-// Barriers: ring full/empty (empty: F8 only), q full/empty, s / p / o [3],
-// drain[2], group, then staging full/empty (F8).
+// F8 (K and V stored as FP8-E4M3 codes): four converter warps (two for K,
+// two for V, each half of a slot's rows) load each CTA's codes of a tile from
+// global memory into registers and write them as fp16 into the same ring
+// slots, released the same way.  Up to 16 warps share the same register
+// limit (128 per thread at 4 warps per scheduler), so the converters cost no
+// registers beyond 13 warps.
+// Barriers: ring full/empty (empty: unused), q full/empty, s / p / o [3],
+// drain[2], group.
 template <bool F8, int DH>
 struct Cfg {
-    static constexpr int NK = F8 ? 3 : (DH / 128) * SBuf<DH>::N;   // K slots (DH / 128 per tile)
-    static constexpr int NV = F8 ? 3 : (DH / 128) * SBuf<DH>::N;   // V slots (DH / 128 per tile)
+    static constexpr int NK = (DH / 128) * SBuf<DH>::N;   // K slots (DH / 128 per tile)
+    static constexpr int NV = (DH / 128) * SBuf<DH>::N;   // V slots (DH / 128 per tile)
     static constexpr int NRING = NK + NV;
-    static constexpr int NSK = F8 ? 3 : 0;               // K staging slots
-    static constexpr int NSV = F8 ? 3 : 0;               // V staging slots
-    static constexpr int NSTG = NSK + NSV;
     static constexpr int RING_BYTES = NRING * SLOT_BYTES;
-    static constexpr int STG_BYTES = NSTG * STG_SLOT;
-    static constexpr int NUM_BARS = 2 * NRING + 14 + 2 * NSTG;
+    static constexpr int NUM_BARS = 2 * NRING + 14;
     static constexpr int NCONV = F8 ? 4 : 0;              // converter warps: 2 for K, 2 for V
     // DH = 128 (three S buffers): one more warp, whose first thread issues the
     // P.V UMMAs; DH = 256: none (-1).
     static constexpr int PV_WARP = DH == 128 ? V_WARP + 1 + NCONV : -1;
     static constexpr int NTHREADS = 32 * (V_WARP + 1 + NCONV + (DH == 128 ? 1 : 0));
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + STG_BYTES + Q_BYTES +
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + RING_BYTES + Q_BYTES +
                                       XCH_BYTES + NUM_BARS * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -146,6 +140,9 @@ struct Params {
     float scale_log2;     // scale * log2(e)
     const float* kscale;  // E4M3 K / V scales (device, one fp32 each); null for fp16 K / V
     const float* vscale;
+    const uint8_t* k8;    // E4M3 K / V codes [KV][Hkv][DH] (F8 only)
+    const uint8_t* v8;
+    int kv_rs;            // bytes between consecutive keys of k8 / v8 (Hkv * DH)
     __half* out;
     FastDiv ptiles;       // divides a tile-space index by num_ptiles (its head)
     float* ws_o;          // [G][2][BM2][DH] unnormalised partial O
@@ -219,8 +216,8 @@ struct SegIter {
 };
 
 // Barrier addresses for a ring of NR slots (K slots 0 .. NK-1, V slots
-// NK .. NR-1) and NS staging slots.
-template <int NR, int NS>
+// NK .. NR-1).
+template <int NR>
 struct Bars {
     uint32_t b;
     __device__ uint32_t full(int s) const { return b + 8 * s; }
@@ -236,17 +233,6 @@ struct Bars {
     __device__ uint32_t drain() const { return b + 8 * (2 * NR + 11); }
     __device__ uint32_t drain2() const { return b + 8 * (2 * NR + 12); }
     __device__ uint32_t group() const { return b + 8 * (2 * NR + 13); }
-    __device__ uint32_t stg_full(int i) const { return b + 8 * (2 * NR + 14 + i); }
-    __device__ uint32_t stg_empty(int i) const { return b + 8 * (2 * NR + 14 + NS + i); }
-};
-
-// One ring (K or V) seen by its producer and by the UMMA issuer: slot
-// position n maps to slot first + n % count, phase (n / count) & 1.
-struct Ring {
-    int first, count;
-    uint32_t n;
-    __device__ int slot() const { return first + (int)(n % (uint32_t)count); }
-    __device__ uint32_t phase() const { return (n / (uint32_t)count) & 1u; }
 };
 
 // ---------------------------------------------------------------- CTA pairs
@@ -396,17 +382,6 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) 
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_test_cl(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // Bounded wait as mbar_wait, with cluster-scope acquire.
 __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort,
                                              unsigned* err) {
@@ -433,19 +408,6 @@ __device__ __forceinline__ void arrive_cl_remote(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
 }
-// TMA load into this CTA's shared memory, completion on a barrier of this CTA.
-template <bool MH>
-__device__ __forceinline__ void tma_load_self(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                              int32_t x, int32_t head, int32_t y) {
-    if (MH)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(head), "r"(y), "r"(bar)
-            : "memory");
-    else
-        tma_load_2d(dst, map, bar, x, y);
-}
 // Two E4M3 codes (low 16 bits of v, low byte first) -> fp16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v) {
     uint32_t r;
@@ -462,8 +424,9 @@ __device__ __forceinline__ void e4m3x16_f16(const uint4& c, uint4& lo, uint4& hi
 
 // MH: the tile space holds one pair-tile range per query head (Hkv > 1,
 // 3-D maps); otherwise one range of packed rows (2-D maps).  DH: head size,
-// 256 or 128.  F8: K and V are E4M3 codes (tm_k / tm_v map the code bytes),
-// converted to fp16 in shared memory by two extra warps.
+// 256 or 128.  F8: K and V are E4M3 codes (read through P.k8 / P.v8; tm_k
+// and tm_v are unused), converted to fp16 in shared memory by four extra
+// warps.
 template <bool MH, int DH, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<F8, DH>::NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -481,21 +444,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr bool TWO_ISSUERS = NSB == 3;
     constexpr uint32_t IDESC_PV = idesc_f16_f32(256, DH, false, true);
     using C = Cfg<F8, DH>;
-    constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING, NSK = C::NSK, NSV = C::NSV;
-    constexpr int NSTG = C::NSTG;
-    constexpr int RING_BYTES = C::RING_BYTES, STG_BYTES = C::STG_BYTES, NUM_BARS = C::NUM_BARS;
+    constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING;
+    constexpr int RING_BYTES = C::RING_BYTES, NUM_BARS = C::NUM_BARS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
-    // Layout: fp16 ring | E4M3 staging (F8) | Q | exchange | barriers | tmem address.
+    // Layout: fp16 ring | Q | exchange | barriers | tmem address.
     const uint32_t s_ring = base;
-    const uint32_t s_stg = base + RING_BYTES;
-    const uint32_t s_q = s_stg + STG_BYTES;
+    const uint32_t s_q = base + RING_BYTES;
     const uint32_t s_bars = s_q + Q_BYTES + XCH_BYTES;
-    const Bars<NRING, NSTG> BR{s_bars};
-    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + STG_BYTES + Q_BYTES);
-    uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + STG_BYTES +
-                                                          Q_BYTES + XCH_BYTES + NUM_BARS * 8);
+    const Bars<NRING> BR{s_bars};
+    float* xch = reinterpret_cast<float*>(base_ptr + RING_BYTES + Q_BYTES);
+    uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(base_ptr + RING_BYTES + Q_BYTES +
+                                                          XCH_BYTES + NUM_BARS * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_ptr + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -510,10 +471,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // arrival per converter warp of the role in either CTA.
             mbar_init(BR.full(s), F8 ? 4 : 1);
             mbar_init(BR.empty(s), 1);
-        }
-        for (int s = 0; s < NSTG; ++s) {
-            mbar_init(BR.stg_full(s), 1);
-            mbar_init(BR.stg_empty(s), 2);   // both converter warps of the role
         }
         mbar_init(BR.qfull(), 1);
         mbar_init(BR.qempty(), 1);
@@ -555,25 +512,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // ------------------------------------------------------------ producers
         // Warp 0: Q and K; warp V_WARP: V.  Each loads this CTA's half of
         // every operand; completions land on the even CTA's full barriers,
-        // whose transaction count the even CTA sets for both halves.  F8: K / V
-        // codes go to this CTA's own staging slots (8 KB each, unswizzled rows),
-        // completing on its own staging barriers, for the converter warps.
-        if (lane == 0) {
+        // whose transaction count the even CTA sets for both halves.  F8: warp
+        // 0 loads Q only (the converter warps fill the K / V slots).
+        if (lane == 0 && (!F8 || warp == 0)) {
             const bool kq = warp == 0;
-            Ring rg = F8 ? Ring{kq ? 0 : NSK, kq ? NSK : NSV, 0u}
-                         : Ring{kq ? 0 : NK, kq ? NK : NV, 0u};
-            uint32_t t = 0;   // fp16: tiles loaded so far (tile t uses S buffer t % NSB)
+            const int first = kq ? 0 : NK;
+            uint32_t t = 0;   // tiles loaded so far (tile t uses S buffer t % NSB)
             int seg = 0;
             bool ok = true;
-            // F8: acquire the next staging slot; returns its full barrier.
-            auto acquire_stg = [&](uint32_t& dst, uint32_t& fb) -> bool {
-                const int slot = rg.slot();
-                if (!mbar_wait(BR.stg_empty(slot), rg.phase() ^ 1u, abort_flag, P.err)) return false;
-                dst = s_stg + slot * STG_SLOT;
-                fb = BR.stg_full(slot);
-                mbar_arrive_expect_tx(fb, STG_SLOT);
-                return true;
-            };
             while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
                 const int kvh = MH ? hd / P.head_group : 0;   // KV head of this segment
                 if (kq) {
@@ -587,99 +533,71 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tma_load_pair<MH>(s_q + c * (BM * 128), &tm_q, leader_addr(qb), c * 64, hd,
                                       pt * BM2 + BM * (int)rank);
                 }
-                for (int j = jb; ok && j < je; ++j) {
-                    if constexpr (F8) {
-                        for (int h = 0; h < SLOTS && ok; ++h) {
-                            uint32_t dst, fb;
-                            if (!acquire_stg(dst, fb)) {
-                                ok = false;
-                                break;
-                            }
-                            // Codes of the same keys and d: K, this CTA's 64 keys x
-                            // d 128 h .. 128 h + 127; V, keys (BN / SLOTS) h ..
-                            // + BN / SLOTS - 1 x this CTA's DH / 2 d.
-                            if (kq)
-                                tma_load_self<MH>(dst, &tm_k, fb, 128 * h, kvh,
-                                                  j * BN + 64 * (int)rank);
-                            else
-                                tma_load_self<MH>(dst, &tm_v, fb, (DH / 2) * (int)rank, kvh,
-                                                  j * BN + h * (BN / SLOTS));
-                            ++rg.n;
-                        }
-                    } else {
-                        // Tile t's slots are free once the UMMAs of tile t - NSB that
-                        // read them have completed: Q.K^T (scores ready) for K, P.V
-                        // (O ready) for V, both committed to this CTA's barriers too.
-                        const uint32_t u = t % NSB;
-                        if (t >= NSB &&
-                            !mbar_wait(kq ? BR.sfull(u) : BR.ofull(u), ((t - NSB) / NSB) & 1,
-                                       abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                        const int slot0 = rg.first + (int)u * SLOTS;
-                        const uint32_t fb = BR.full(slot0);
-                        if (leader) mbar_arrive_expect_tx(fb, 2 * SLOTS * SLOT_BYTES);
-                        const uint32_t fbl = leader_addr(fb);
-                        for (int h = 0; h < SLOTS; ++h) {
-                            const uint32_t dst = s_ring + (slot0 + h) * SLOT_BYTES;
-                            if (kq) {
-                                // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
-                                for (int cc = 0; cc < 2; ++cc)
-                                    tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fbl,
-                                                      (2 * h + cc) * 64, kvh,
-                                                      j * BN + 64 * (int)rank);
-                            } else {
-                                // V: sub-tiles SUBS h .. SUBS h + SUBS - 1 (32 keys)
-                                // x this CTA's DH / 2 d
-                                for (int ss = 0; ss < SUBS; ++ss)
-                                    for (int a = 0; a < VATOMS; ++a)
-                                        tma_load_pair<MH>(dst + ss * SUB_BYTES + a * 4096, &tm_v,
-                                                          fbl, (DH / 2) * (int)rank + 64 * a, kvh,
-                                                          j * BN + (SUBS * h + ss) * 32);
-                            }
-                        }
-                        ++t;
+                for (int j = jb; !F8 && ok && j < je; ++j) {
+                    // Tile t's slots are free once the UMMAs of tile t - NSB that
+                    // read them have completed: Q.K^T (scores ready) for K, P.V
+                    // (O ready) for V, both committed to this CTA's barriers too.
+                    const uint32_t u = t % NSB;
+                    if (t >= NSB &&
+                        !mbar_wait(kq ? BR.sfull(u) : BR.ofull(u), ((t - NSB) / NSB) & 1,
+                                   abort_flag, P.err)) {
+                        ok = false;
+                        break;
                     }
+                    const int slot0 = first + (int)u * SLOTS;
+                    const uint32_t fb = BR.full(slot0);
+                    if (leader) mbar_arrive_expect_tx(fb, 2 * SLOTS * SLOT_BYTES);
+                    const uint32_t fbl = leader_addr(fb);
+                    for (int h = 0; h < SLOTS; ++h) {
+                        const uint32_t dst = s_ring + (slot0 + h) * SLOT_BYTES;
+                        if (kq) {
+                            // K: d chunks 2h, 2h + 1 of this CTA's 64 keys
+                            for (int cc = 0; cc < 2; ++cc)
+                                tma_load_pair<MH>(dst + cc * HALF_SLOT, &tm_k, fbl,
+                                                  (2 * h + cc) * 64, kvh,
+                                                  j * BN + 64 * (int)rank);
+                        } else {
+                            // V: sub-tiles SUBS h .. SUBS h + SUBS - 1 (32 keys)
+                            // x this CTA's DH / 2 d
+                            for (int ss = 0; ss < SUBS; ++ss)
+                                for (int a = 0; a < VATOMS; ++a)
+                                    tma_load_pair<MH>(dst + ss * SUB_BYTES + a * 4096, &tm_v,
+                                                      fbl, (DH / 2) * (int)rank + 64 * a, kvh,
+                                                      j * BN + (SUBS * h + ss) * 32);
+                        }
+                    }
+                    ++t;
                 }
                 ++seg;
             }
-            if (!ok && (leader || F8)) {
+            if (!ok && leader) {
                 // Unwind: let every copy still in flight land before the CTA exits
-                // (the even CTA's full barriers count both halves; F8 staging
-                // copies complete on each CTA's own barriers).
-                if constexpr (F8) {
-                    for (int i = 0; i < rg.count; ++i) {
-                        const uint32_t fills =
-                            rg.n > (uint32_t)i ? (rg.n - i + rg.count - 1) / rg.count : 0;
-                        if (fills) drain_wait(BR.stg_full(rg.first + i), (fills - 1) & 1u);
-                    }
-                } else {
+                // (the even CTA's full barriers count both halves).
+                if (!F8) {
                     for (uint32_t u = 0; u < NSB; ++u) {
                         const uint32_t fills = t > u ? (t - u + NSB - 1) / NSB : 0;
-                        if (fills) drain_wait(BR.full(rg.first + (int)u * SLOTS), (fills - 1) & 1u);
+                        if (fills) drain_wait(BR.full(first + (int)u * SLOTS), (fills - 1) & 1u);
                     }
                 }
-                if (kq && seg > 0 && leader) drain_wait(BR.qfull(), (seg - 1) & 1);
+                if (kq && seg > 0) drain_wait(BR.qfull(), (seg - 1) & 1);
             }
         }
     } else if (F8 && warp > V_WARP && warp <= V_WARP + C::NCONV) {
         // ------------------------------------------------------------ converters (F8)
-        // Warps V_WARP + 1, + 2 convert K, V_WARP + 3, + 4 V, each half of
-        // every slot: in the order the producer filled the staging slots, wait
-        // for the codes and for the fp16 slot to be free (its UMMAs done),
-        // write the fp16 values exactly where the fp16 path's TMA would have
-        // put them (128-byte-swizzled rows), make them visible to the tensor
-        // cores' async proxy, free the staging slot and arrive (cluster scope)
-        // on the even CTA's full barrier.  E4M3 -> fp16 is exact.  All eight
-        // 16-byte code loads of a lane are issued before the first conversion.
+        // Warps V_WARP + 1, + 2 convert K, V_WARP + 3, + 4 V, each half of the
+        // rows of every slot of a tile.  A lane loads all its 16-byte code
+        // chunks of the tile from global memory (L2) first, then waits for the
+        // tile's slots to be free (the scores-ready / O-ready barrier of the UMMAs
+        // NSB tiles back, as the fp16 copies do), writes the fp16 values exactly
+        // where the fp16 path's TMA would have put them (128-byte-swizzled rows),
+        // makes them visible to the tensor cores' async proxy and arrives
+        // (cluster scope) on the even CTA's full barrier.  E4M3 -> fp16 is
+        // exact; keys past KV are zero codes, as the TMA's fill would be.
         const int cw = warp - V_WARP - 1;           // 0..3
         const bool kc = cw < 2;
         const int part = cw & 1;                    // which half of the slot's rows
-        Ring sg{kc ? 0 : NSK, kc ? NSK : NSV, 0u};
-        Ring rg{kc ? 0 : NK, kc ? NK : NV, 0u};
-        // Staging rows: K 64 keys x 128 codes; V (BN / SLOTS) keys x DH / 2 codes.
-        constexpr int RBV = DH / 2;                 // V code bytes per staging row
+        // Slot rows: K 64 keys x 128 codes; V (BN / SLOTS) keys x DH / 2 codes.
+        constexpr int RBV = DH / 2;                 // V code bytes per row
         constexpr int RPIK = 32 / (128 / 16);       // K rows per warp pass (4)
         constexpr int RPIV = 32 / (RBV / 16);       // V rows per warp pass (4 or 8)
         constexpr int PASSES = 8;                   // passes per warp per slot (half a slot)
@@ -689,27 +607,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int rpi = kc ? RPIK : RPIV;
         const int rbase = part * rpi * PASSES + lane / cpr;
         const int c = lane % cpr;                   // 16 codes: d 16c .. 16c + 15 of the row
+        const uint8_t* codes = kc ? P.k8 : P.v8;
+        const int first = kc ? 0 : NK;
+        uint32_t t = 0;
         bool ok = true;
         while (ok && it.next(P, pt, hd, jb, je, n, is_first)) {
+            const int kvh = MH ? hd / P.head_group : 0;
             for (int j = jb; ok && j < je; ++j) {
-                for (int h = 0; h < SLOTS && ok; ++h) {
-                    const int ss = sg.slot(), fs = rg.slot();
-                    ok = mbar_wait(BR.stg_full(ss), sg.phase(), abort_flag, P.err);
-                    if (ok) ok = mbar_wait(BR.empty(fs), rg.phase() ^ 1u, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    const uint8_t* src = base_ptr + RING_BYTES + ss * STG_SLOT;
-                    uint8_t* dst = base_ptr + fs * SLOT_BYTES;
-                    uint4 code[PASSES];
+                uint4 code[SLOTS][PASSES];
 #pragma unroll
-                    for (int i = 0; i < PASSES; ++i)
-                        code[i] = *reinterpret_cast<const uint4*>(src + (rbase + i * rpi) * rb +
-                                                                  c * 16);
+                for (int h = 0; h < SLOTS; ++h) {
+                    // K slot h: this CTA's keys j BN + 64 rank + r, d 128 h ..; V slot h:
+                    // keys j BN + h (BN / SLOTS) + r, this CTA's d (DH / 2) rank ..
+                    const int key0 = kc ? j * BN + 64 * (int)rank : j * BN + h * (BN / SLOTS);
+                    const int d0 = (kc ? 128 * h : (DH / 2) * (int)rank) + 16 * c;
+#pragma unroll
+                    for (int i = 0; i < PASSES; ++i) {
+                        const int key = key0 + rbase + i * rpi;
+                        code[h][i] = key < P.KV
+                                         ? __ldg(reinterpret_cast<const uint4*>(
+                                               codes + (size_t)key * P.kv_rs + kvh * DH + d0))
+                                         : make_uint4(0, 0, 0, 0);
+                    }
+                }
+                const uint32_t u = t % NSB;
+                if (t >= NSB)
+                    ok = mbar_wait(kc ? BR.sfull(u) : BR.ofull(u), ((t - NSB) / NSB) & 1,
+                                   abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const int slot0 = first + (int)u * SLOTS;
+#pragma unroll
+                for (int h = 0; h < SLOTS; ++h) {
+                    uint8_t* dst = base_ptr + (slot0 + h) * SLOT_BYTES;
 #pragma unroll
                     for (int i = 0; i < PASSES; ++i) {
                         const int r = rbase + i * rpi;
                         uint4 lo, hi;
-                        e4m3x16_f16(code[i], lo, hi);
+                        e4m3x16_f16(code[h][i], lo, hi);
                         // K slot: chunk c / 4 (64 d) of HALF_SLOT, row r; V slot:
                         // sub-tile r / 32, atom c / 4 (64 d), row r % 32.
                         const uint32_t o =
@@ -719,19 +654,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         *reinterpret_cast<uint4*>(dst + o + ((u0 ^ sw) << 4)) = lo;
                         *reinterpret_cast<uint4*>(dst + o + (((u0 + 1) ^ sw) << 4)) = hi;
                     }
-                    // Order the generic stores before the tensor cores' reads of this
-                    // CTA's shared memory (reached through the cluster window by the
-                    // even CTA's UMMAs); a shared-memory-only proxy fence.
-                    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(BR.stg_empty(ss));
-                        if (leader) arrive_cl_local(BR.full(fs));
-                        else arrive_cl_remote(leader_addr(BR.full(fs)));
-                    }
-                    ++sg.n;
-                    ++rg.n;
                 }
+                // Order the generic stores before the tensor cores' reads of this
+                // CTA's shared memory (reached through the cluster window by the
+                // even CTA's UMMAs); a shared-memory-only proxy fence.
+                asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) arrive_cl_local(BR.full(slot0));
+                    else arrive_cl_remote(leader_addr(BR.full(slot0)));
+                }
+                ++t;
             }
         }
     } else if (warp == 1 || warp == C::PV_WARP) {
@@ -748,34 +681,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // then P.V of tile g, the tensor pipe's order keeping Q.K^T of tile
         // g + 2 behind the P.V of tile g that reads the same buffer.
         const bool qk_role = warp == 1;
-        Ring kr{0, NK, 0u}, vr{NK, NV, 0u};   // each thread uses the ring(s) of its UMMAs
         uint32_t g = 0;
         int seg = 0;
         bool ok = true;
-        // A landed K / V slot: the copy and the UMMA that reads it are both
-        // async-proxy operations ordered by the mbarrier's completion, so no
-        // tcgen05 fence is needed here.
-        // F8: the slots were filled by generic stores of both CTAs' converter
-        // warps, which arrive with cluster-scope release; acquire at cluster
-        // scope to match.
-        auto take = [&](const Ring& rg, int& slot) -> bool {
-            slot = rg.slot();
-            if constexpr (F8) return mbar_wait_cl(BR.full(slot), rg.phase(), abort_flag, P.err);
-            return mbar_wait(BR.full(slot), rg.phase(), abort_flag, P.err);
-        };
-        // Non-blocking look at the ring position after the current one; its
-        // latency overlaps the current slot's UMMA issue, and a slot found
-        // full needs no wait later.
-        auto peek_next = [&](const Ring& rg) -> bool {
-            Ring nx = rg;
-            ++nx.n;
-            if constexpr (F8) return mbar_test_cl(BR.full(nx.slot()), nx.phase());
-            return mbar_test(BR.full(nx.slot()), nx.phase());
-        };
-        // fp16 K / V: tile gg's K (V) slots are first + (gg % NSB) * SLOTS ..,
-        // landed when the first one's full barrier completes phase gg / NSB.
+        // Tile gg's K (V) slots are first + (gg % NSB) * SLOTS .., landed when
+        // the first one's full barrier completes phase gg / NSB.  A TMA copy and
+        // the UMMA that reads it are both async-proxy operations ordered by the
+        // mbarrier's completion, so no tcgen05 fence is needed; F8: the slots
+        // were filled by generic stores of both CTAs' converter warps, which
+        // arrive with cluster-scope release, so acquire at cluster scope.
         auto take_tile = [&](int first, uint32_t gg, int& slot0) -> bool {
             slot0 = first + (int)(gg % NSB) * SLOTS;
+            if constexpr (F8) return mbar_wait_cl(BR.full(slot0), (gg / NSB) & 1, abort_flag, P.err);
             return mbar_wait(BR.full(slot0), (gg / NSB) & 1, abort_flag, P.err);
         };
         auto s_col_of = [&](uint32_t gg) { return SBuf<DH>::COL0 + (gg % NSB) * BN; };
@@ -785,19 +702,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t q_lo = desc_lo(s_q, 16);
         auto issue_qk = [&](uint32_t gg) -> bool {
             const uint32_t d = tmem + s_col_of(gg);
-            bool next_ready = false;
             int slot0 = 0;
-            if constexpr (!F8) {
-                if (!take_tile(0, gg, slot0)) return false;
-            }
+            if (!take_tile(0, gg, slot0)) return false;
 #pragma unroll
             for (int h = 0; h < SLOTS; ++h) {
-                int slot = slot0 + h;
-                if constexpr (F8) {
-                    slot = kr.slot();
-                    if (!next_ready && !take(kr, slot)) return false;
-                    if (SLOTS > 1 && h == 0) next_ready = peek_next(kr);
-                }
+                const int slot = slot0 + h;
                 const uint32_t k_lo = desc_lo(s_ring + slot * SLOT_BYTES, 16);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
@@ -812,28 +721,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             umma_ss_pair_c<true>(d, a, b, IDESC_QK);
                     }
                 }
-                if constexpr (F8) {
-                    umma_commit_pair(BR.empty(slot));
-                    ++kr.n;
-                }
             }
             return true;
         };
         auto issue_pv = [&](uint32_t gg, bool acc0) -> bool {
             const uint32_t p_base = tmem + s_col_of(gg);
-            bool next_ready = false;
             int slot0 = 0;
-            if constexpr (!F8) {
-                if (!take_tile(NK, gg, slot0)) return false;
-            }
+            if (!take_tile(NK, gg, slot0)) return false;
 #pragma unroll
             for (int h = 0; h < SLOTS; ++h) {
-                int slot = slot0 + h;
-                if constexpr (F8) {
-                    slot = vr.slot();
-                    if (!next_ready && !take(vr, slot)) return false;
-                    if (SLOTS > 1 && h == 0) next_ready = peek_next(vr);
-                }
+                const int slot = slot0 + h;
                 // V: MN-major, 64-element atoms 4096 B apart (LBO), 8-key groups
                 // 1024 B apart (SBO); a K step of 16 keys is 2048 B.
                 const uint32_t v_lo = desc_lo(s_ring + slot * SLOT_BYTES, 4096);
@@ -851,10 +748,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         else
                             umma_ts_pair_c<true>(tmem + O_COL, a_tmem, b, IDESC_PV);
                     }
-                }
-                if constexpr (F8) {
-                    umma_commit_pair(BR.empty(slot));
-                    ++vr.n;
                 }
             }
             return true;
@@ -1328,6 +1221,9 @@ int prefill_launch(const void* q, const void* k, const void* v, const float* ksc
     P.scale_log2 = scale * 1.4426950408889634f;
     P.kscale = kscale;
     P.vscale = vscale;
+    P.k8 = f8 ? static_cast<const uint8_t*>(k) : nullptr;
+    P.v8 = f8 ? static_cast<const uint8_t*>(v) : nullptr;
+    P.kv_rs = Hkv * Dh;
     P.err = di->err_word;
     P.out = static_cast<__half*>(out);
 
@@ -1347,23 +1243,14 @@ int prefill_launch(const void* q, const void* k, const void* v, const float* ksc
     MergeTasks tasks;  // passed to the merge kernel by value
     find_cut_tiles(P, tasks);
 
+    // E4M3 K / V are read by the converter warps through P.k8 / P.v8; their
+    // kernels take the Q map in the K / V map arguments, unused.
     CUtensorMap tq, tk, tv;
-    // E4M3 code maps (unswizzled staging rows): K boxes of 128 codes x 64 keys,
-    // V boxes of Dh / 2 codes x (128 / (Dh / 128)) keys, one KV head per box.
-    auto code_maps = [&](bool three_d) -> bool {
-        const uint32_t v_rows = (uint32_t)(BN / (Dh / 128));
-        return make_map_u8_plain(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, (uint64_t)Dh,
-                                 (uint64_t)Hkv * Dh, 128, 64, three_d) &&
-               make_map_u8_plain(&tv, v, Dh, (uint64_t)Hkv, (uint64_t)KV, (uint64_t)Dh,
-                                 (uint64_t)Hkv * Dh, (uint32_t)(Dh / 2), v_rows, three_d);
-    };
     if (packed) {
         if (!make_map_2d_f16(&tq, q, (uint64_t)P.M_total, Dh, Dh, BM, 64)) return GQA_ERR_CUDA;
-        if (f8) {
-            if (!code_maps(false)) return GQA_ERR_CUDA;
-            return Dh == 256 ? launch_one<false, 256, true>(tq, tk, tv, P, tasks, stream)
-                             : launch_one<false, 128, true>(tq, tk, tv, P, tasks, stream);
-        }
+        if (f8)
+            return Dh == 256 ? launch_one<false, 256, true>(tq, tq, tq, P, tasks, stream)
+                             : launch_one<false, 128, true>(tq, tq, tq, P, tasks, stream);
         if (!make_map_2d_f16(&tk, k, (uint64_t)KV, Dh, Dh, BN / 2, 64) ||
             !make_map_2d_f16(&tv, v, (uint64_t)KV, Dh, Dh, 32, 64))
             return GQA_ERR_CUDA;
@@ -1374,11 +1261,9 @@ int prefill_launch(const void* q, const void* k, const void* v, const float* ksc
     if (!make_map_3d_f16(&tq, q, Dh, (uint64_t)Hq, (uint64_t)Q, row_bytes,
                          (uint64_t)Hq * row_bytes, BM))
         return GQA_ERR_CUDA;
-    if (f8) {
-        if (!code_maps(true)) return GQA_ERR_CUDA;
-        return Dh == 256 ? launch_one<true, 256, true>(tq, tk, tv, P, tasks, stream)
-                         : launch_one<true, 128, true>(tq, tk, tv, P, tasks, stream);
-    }
+    if (f8)
+        return Dh == 256 ? launch_one<true, 256, true>(tq, tq, tq, P, tasks, stream)
+                         : launch_one<true, 128, true>(tq, tq, tq, P, tasks, stream);
     if (!make_map_3d_f16(&tk, k, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
                          (uint64_t)Hkv * row_bytes, BN / 2) ||
         !make_map_3d_f16(&tv, v, Dh, (uint64_t)Hkv, (uint64_t)KV, row_bytes,
