@@ -609,39 +609,38 @@ def run_gpu(args):
     }
     secondary = []
     if not args.quick:
-        for kv in ([x for x in KV_SWEEP if x != KV] if not args.no_sweep else [KV_SWEEP[-1]]):
-            t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device)
+        # Prefill secondaries, each with the SM clock sampled while it runs: they
+        # follow one another for tens of seconds, and under that sustained load
+        # the GPU's power cap can lower the clock (reported, not corrected).
+        def prefill_secondary(what, kv, **kw):
+            clk2 = ClockSampler(local)
+            clk2.start()
+            t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device, **kw)
+            c2 = clk2.stop()
             ms = statistics.mean(t)
-            secondary.append({"what": f"prefill Q={Q} KV={kv}", "ms": round(ms, 4),
-                              "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
-                              "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4)})
-        for kv in (KV, KV_SWEEP[-1]):
-            # K / V stored as E4M3 codes (converted to fp16 in shared memory).
-            t, _ = bench_prefill(binding, Q, kv, max(3, args.steps // 2), 2, flush, device,
-                                 e4m3=True)
-            ms = statistics.mean(t)
-            secondary.append({"what": f"prefill Q={Q} KV={kv}, E4M3 K/V cache", "ms": round(ms, 4),
-                              "TFLOP/s": round(prefill_flops(Q, kv) / ms / 1e9, 1),
-                              "frac_of_peak": round(prefill_flops(Q, kv) / ms / 1e9 / peak, 4),
-                              "traffic": profiled_traffic(
-                                  "prefill_kernel_e4m3_Q8000_KV40000.md",
-                                  "long_context_causal_gqa_gb300/csrc/prefill.cu")
-                              if (Q, kv) == (Q_MAIN, KV_MAIN) else None,
-                              "device_error": binding.device_error()})
+            fl = prefill_flops(Q, kv, kw.get("Hq", HQ), kw.get("Dh", D))
+            return {"what": what, "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
+                    "frac_of_peak": round(fl / ms / 1e9 / peak, 4),
+                    "sm_mhz": c2.get("sm_mhz"), "clock_reasons": c2.get("reasons")}
         for hq, hkv, dh in ((6, 2, D), (8, 1, D), (6, 1, 128)):
             # Other head groupings (every query head's tiles in one launch when
             # Hkv > 1) and head size 128.
-            t, _ = bench_prefill(binding, Q, KV, max(3, args.steps // 2), 2, flush, device,
-                                 Hq=hq, Hkv=hkv, Dh=dh)
-            ms = statistics.mean(t)
-            fl = prefill_flops(Q, KV, hq, dh)
-            secondary.append({"what": f"prefill Q={Q} KV={KV} Hq={hq} Hkv={hkv} D={dh}",
-                              "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
-                              "frac_of_peak": round(fl / ms / 1e9 / peak, 4),
-                              "traffic": profiled_traffic(
-                                  "prefill_kernel_d128_Q8000_KV40000.md",
-                                  "long_context_causal_gqa_gb300/csrc/prefill.cu")
-                              if (hq, hkv, dh, Q, KV) == (6, 1, 128, Q_MAIN, KV_MAIN) else None})
+            e = prefill_secondary(f"prefill Q={Q} KV={KV} Hq={hq} Hkv={hkv} D={dh}", KV,
+                                  Hq=hq, Hkv=hkv, Dh=dh)
+            e["traffic"] = (profiled_traffic("prefill_kernel_d128_Q8000_KV40000.md",
+                                             "long_context_causal_gqa_gb300/csrc/prefill.cu")
+                            if (hq, hkv, dh, Q, KV) == (6, 1, 128, Q_MAIN, KV_MAIN) else None)
+            secondary.append(e)
+        for kv in (KV, KV_SWEEP[-1]):
+            # K / V stored as E4M3 codes (converted to fp16 in shared memory).
+            e = prefill_secondary(f"prefill Q={Q} KV={kv}, E4M3 K/V cache", kv, e4m3=True)
+            e["traffic"] = (profiled_traffic("prefill_kernel_e4m3_Q8000_KV40000.md",
+                                             "long_context_causal_gqa_gb300/csrc/prefill.cu")
+                            if (Q, kv) == (Q_MAIN, KV_MAIN) else None)
+            e["device_error"] = binding.device_error()
+            secondary.append(e)
+        for kv in ([x for x in KV_SWEEP if x != KV] if not args.no_sweep else [KV_SWEEP[-1]]):
+            secondary.append(prefill_secondary(f"prefill Q={Q} KV={kv}", kv))
         for R in (1, 2, 8):
             try:
                 t, nbytes, fl = bench_paged(binding, R, device, 50, 5, flush)
