@@ -887,7 +887,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int h = 1; h < NWG; ++h) rm = fmaxf(rm, xp[h * BM + row]);
                 const float mx = rm * sl2;
-                bool o_seen = false;
                 if (j == jb) {
                     m_ref = mx;
                 } else {
@@ -898,7 +897,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                         tc_fence_after();
-                        o_seen = true;
                         const float f = need ? ex2(m_ref - mx) : 1.0f;
                         if (need) {
                             l *= f;
@@ -938,12 +936,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_st32(t_lane + s_col + COLS * hg, pk);
                 l += (l0 + l1) + (l2 + l3);
                 tmem_st_wait();
-                if (j > jb && !o_seen) {
-                    ok = mbar_wait(BR.ofull((gg - 1) % NSB), ((gg - 1) / NSB) & 1, abort_flag,
-                                   P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                }
+                // No wait for the previous tile's P.V here unless O was rescaled
+                // above: P(j) goes into S buffer j % NSB, whose last reader (the
+                // P.V of tile j - NSB) had completed before the Q.K^T of tile j
+                // was issued, and the O-ready barriers cannot run more than one
+                // phase ahead of this thread (their next phase needs its P).
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
