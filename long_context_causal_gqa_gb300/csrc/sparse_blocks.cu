@@ -54,6 +54,9 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
+#include "e4m3_umma.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -66,22 +69,21 @@ constexpr int NP = 16;               // the heads of one launch padded to the UM
 // Gather warps: a warp-wide 16-byte cp.async copy issues at about 8 bytes per
 // cycle per warp, whatever the number of warps (measured: 4 warps move 32, 8
 // warps 50, 16 warps 69 bytes per cycle per SM of 512-byte rows from L2), so
-// the fp16 path gathers with sixteen warps (eight for K, eight for V) at head
-// size 256 with 6 heads, eight at head size 128 (sixteen measured no faster)
-// and for up to 16 heads (whose key warps need the registers); the E4M3
-// path's four warps load, convert and store their codes themselves.
-template <int HQ, bool F8, int DH>
+// the fp16 kernel gathers with sixteen warps (eight for K, eight for V) at
+// head size 256 with 6 heads, eight at head size 128 (sixteen measured no
+// faster) and for up to 16 heads (whose key warps need the registers).
+template <int HQ, int DH>
 constexpr int gather_warps() { return DH == 256 && HQ != NP ? 16 : 8; }
 // Warps: gather warps, then the UMMA issuer, four key warps, the index warp.
-template <int HQ, bool F8, int DH>
-constexpr int nthreads() { return 32 * (gather_warps<HQ, F8, DH>() + 6); }
+template <int HQ, int DH>
+constexpr int nthreads() { return 32 * (gather_warps<HQ, DH>() + 6); }
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Params {
     const __half* q;
-    const __half* kcache;     // fp16 cache (F8 false)
+    const __half* kcache;     // fp16 cache
     const __half* vcache;
-    const uint8_t* kcache8;   // E4M3 cache (F8 true)
+    const uint8_t* kcache8;   // E4M3 cache
     const uint8_t* vcache8;
     const float* kscale;      // E4M3 scales (device, one fp32 each)
     const float* vscale;
@@ -179,19 +181,100 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 
 __device__ __forceinline__ int row_tiles(int cnt) { return (cnt * BLK + TILE - 1) / TILE; }
 
-// Two E4M3 codes (low 16 bits of v, low byte first) -> fp16x2 (low half first).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)v));
-    return r;
+// ------------------------------------------------------------ token index warp
+// (both kernels).  idx: the ring of NI slots of TILE token rows; seen: the
+// row's id bitmap; ifull / iempty: the full and empty mbarriers of slot 0
+// (each further slot's 8 bytes on).
+__device__ __forceinline__ void index_warp(const Params& P, int* idx, uint32_t* seen,
+                                           uint32_t ifull, uint32_t iempty,
+                                           volatile int* abort_flag) {
+    // Same walk as the gather warps (rows of this CTA, tiles of each
+    // non-empty row).  Lane l resolves selected position 32 t + l of the
+    // row, i.e. keys 4 l .. 4 l + 3 of tile t: id -> set membership ->
+    // physical page -> cache token rows, -1 for masked keys (past the
+    // list, a bad id, a repeat, or past the row's position).
+    const int lane = threadIdx.x & 31;
+    const int lp = P.log2_page, pmask = (1 << P.log2_page) - 1;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+        const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
+        const int nt = row_tiles(cnt);
+        if (nt == 0) continue;
+        const int p = P.ctx_len - P.rows + i;
+        const int own = p / BLK;                     // the row's own block
+        const bool exact = own < SEEN_BITS;          // bit = id, no collisions
+        const int32_t* sel = P.sel_idx + (size_t)i * P.max_sel;
+        for (int w = lane; w < SEEN_BITS / 32; w += 32) seen[w] = 0u;
+        __syncwarp();
+        for (int t = 0; t < nt; ++t, ++g) {
+            const int slot = (int)(g % NI);
+            if (!mbar_wait(iempty + 8u * slot, ((g / NI) & 1) ^ 1, abort_flag, P.err)) {
+                ok = false;
+                break;
+            }
+            const int li = t * (TILE / BLK) + lane;
+            int b = -1;
+            bool valid = false;
+            if (li < cnt) {
+                b = __ldg(sel + li);
+                valid = b >= 0 && b <= own;
+            }
+            const unsigned bad = __ballot_sync(0xffffffffu, li < cnt && !valid);
+            if (bad && lane == 0) atomicOr(P.err, kErrBadBlockId);
+            // A repeat within this tile: a lower lane holds the same id.
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            bool dup = false;
+            if (valid) {
+                const unsigned same = __match_any_sync(vmask, b);
+                dup = (same & ((1u << lane) - 1u)) != 0u;
+            }
+            // A repeat of an earlier tile: the id's bit is set (exact), or
+            // its hash bit is set and an earlier position holds it.
+            const uint32_t h = (uint32_t)b & (uint32_t)(SEEN_BITS - 1);
+            bool cand = valid && !dup && ((seen[h >> 5] >> (h & 31u)) & 1u);
+            if (cand && exact) {
+                dup = true;
+                cand = false;
+            }
+            unsigned cm = __ballot_sync(0xffffffffu, cand);
+            while (cm) {
+                const int src = __ffs(cm) - 1;
+                cm &= cm - 1u;
+                const int bb = __shfl_sync(0xffffffffu, b, src);
+                bool found = false;
+                for (int j0 = 0; j0 < t * (TILE / BLK) && !found; j0 += 32)
+                    found = __any_sync(0xffffffffu, __ldg(sel + j0 + lane) == bb);
+                if (lane == src) dup = found;
+            }
+            __syncwarp();
+            if (valid && !dup) atomicOr(seen + (h >> 5), 1u << (h & 31u));
+            if (__ballot_sync(0xffffffffu, dup) && lane == 0) atomicOr(P.err, kErrDupBlockId);
+            const bool use = valid && !dup;
+            const int tok0 = b * BLK;
+            int pg = use ? __ldg(P.table + (tok0 >> lp)) : 0;   // a block never straddles a page
+            if (use && (pg < 0 || pg >= P.num_pages)) {
+                atomicOr(P.err, kErrBadPageId);
+                pg = 0;
+            }
+            const int r0 = (pg << lp) + (tok0 & pmask);
+            int4 r;
+            r.x = (use && tok0 + 0 <= p) ? r0 + 0 : -1;
+            r.y = (use && tok0 + 1 <= p) ? r0 + 1 : -1;
+            r.z = (use && tok0 + 2 <= p) ? r0 + 2 : -1;
+            r.w = (use && tok0 + 3 <= p) ? r0 + 3 : -1;
+            reinterpret_cast<int4*>(idx + slot * TILE)[lane] = r;
+            __syncwarp();   // the set's bits are read by every lane in the next tile
+            mbar_arrive(ifull + 8u * slot);
+        }
+    }
 }
 
-// HQ: heads per launch known at compile time (6), or NP with the count read
-// from P.nh (any grouping up to 16 query heads per KV head).  F8: the cache
-// holds E4M3 codes, converted to fp16 on the way into shared memory.  DH: head
-// size, 256 or 128.
-template <int HQ, bool F8, int DH>
-__global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const Params P) {
+// fp16 cache.  HQ: heads per launch known at compile time (6), or NP with the
+// count read from P.nh (any grouping up to 16 query heads per KV head).  DH:
+// head size, 256 or 128.
+template <int HQ, int DH>
+__global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Params P) {
     using L = SL<DH>;
     constexpr int HALVES = DH / 128;   // 128-d halves of a row (one M = 128 P.V each)
     constexpr int KV_TILE_BYTES = L::KV_TILE_BYTES;
@@ -207,8 +290,8 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
     constexpr int NVB = 2;
     constexpr uint32_t KOFF = OFF_K;
     constexpr uint32_t VOFF = OFF_V;
-    constexpr int NGW = gather_warps<HQ, F8, DH>();
-    constexpr int NTHREADS = nthreads<HQ, F8, DH>();
+    constexpr int NGW = gather_warps<HQ, DH>();
+    constexpr int NTHREADS = nthreads<HQ, DH>();
     constexpr int MMA_WARP = NGW, KEY_WARP0 = NGW + 1, IDX_WARP = NGW + 5;
     // Arrivals per K or V tile: every thread of the operand's NGW / 2 gather warps.
     constexpr int NGATHER = 32 * (NGW / 2);
@@ -311,114 +394,49 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
             static_assert(KPW <= 32 && TILE == KPW * KW, "keys per warp");
             const bool kg = warp < KW;
             const int kbase = (warp % KW) * KPW;
-            if constexpr (F8) {
-                // E4M3 codes: a token row is DH code bytes; a group of LPK = DH / 16
-                // lanes takes key KPP e + group, lane u of it the codes of d = 16u ..
-                // 16u + 15, which become fp16 units 2u, 2u + 1 of the row (chunk
-                // u / 4, units 2 (u % 4) and 2 (u % 4) + 1 within it).  A warp loads
-                // all its code chunks of a tile into registers before it waits for
-                // the tile buffer, so the loads' latency overlaps the wait; masked
-                // tokens convert from zero codes.
-                constexpr int LPK = DH / 16;      // lanes per key row: 16 or 8
-                constexpr int KPP = 32 / LPK;     // keys per load: 2 or 4
-                constexpr int NPASS = KPW / KPP;  // loads per lane per tile
-                const int u = lane % LPK, half = lane / LPK;
-                const uint32_t unit = 2u * (uint32_t)(u & 3);
-                const uint8_t* cache = kg ? P.kcache8 : P.vcache8;
-                for (int t = 0; t < nt && ok; ++t, ++g) {
-                    int tok1;
-                    size_t row1;
-                    if (!take_index(g, kbase, tok1, row1)) {
-                        ok = false;
-                        break;
-                    }
-                    uint4 code[NPASS];
-#pragma unroll
-                    for (int e = 0; e < NPASS; ++e) {
-                        const int src = KPP * e + half;
-                        const int tok = __shfl_sync(0xffffffffu, tok1, src);
-                        const size_t row = __shfl_sync(0xffffffffu, row1, src);
-                        code[e] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(cache + row + 16 * u))
-                                           : make_uint4(0, 0, 0, 0);
-                    }
-                    uint32_t tile, fullb;
-                    if (kg) {
-                        if (!mbar_wait(bar(B_KEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tile = OFF_K;
-                        fullb = bar(B_KFULL);
-                    } else {
-                        const int vb = g & 1;
-                        if (!mbar_wait(bar(B_VEMPTY + vb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tile = OFF_V + vb * KV_TILE_BYTES;
-                        fullb = bar(B_VFULL + vb);
-                    }
-                    const uint32_t chunk = tile + (uint32_t)(u >> 2) * (TILE * 128);
-#pragma unroll
-                    for (int e = 0; e < NPASS; ++e) {
-                        const uint32_t key = (uint32_t)(kbase + KPP * e + half);
-                        const uint4 r = code[e];
-                        const uint4 lo = make_uint4(e4m3x2_to_f16x2(r.x), e4m3x2_to_f16x2(r.x >> 16),
-                                                    e4m3x2_to_f16x2(r.y), e4m3x2_to_f16x2(r.y >> 16));
-                        const uint4 hi = make_uint4(e4m3x2_to_f16x2(r.z), e4m3x2_to_f16x2(r.z >> 16),
-                                                    e4m3x2_to_f16x2(r.w), e4m3x2_to_f16x2(r.w >> 16));
-                        *reinterpret_cast<uint4*>(gbase + chunk + sw128(key, unit)) = lo;
-                        *reinterpret_cast<uint4*>(gbase + chunk + sw128(key, unit + 1)) = hi;
-                    }
-                    // Generic-proxy stores, read by the tensor cores (async proxy).
-                    fence_async_shared();
-                    mbar_arrive(fullb);
+            // fp16: a key's row is DH * 2 bytes, one warp-wide 16-byte-per-lane
+            // copy per 512 / (DH * 2) keys, straight into the swizzled tile.
+            constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
+            constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
+            const int ul = lane % LPK;        // lane covers d = 8 ul .. 8 ul + 7
+            const __half* cache = kg ? P.kcache : P.vcache;
+            for (int t = 0; t < nt && ok; ++t, ++g) {
+                int tok1;
+                size_t row1;
+                if (!take_index(g, kbase, tok1, row1)) {
+                    ok = false;
+                    break;
                 }
-            } else {
-                // fp16: a key's row is DH * 2 bytes, one warp-wide 16-byte-per-lane
-                // copy per 512 / (DH * 2) keys, straight into the swizzled tile.
-                constexpr int LPK = DH / 8;       // lanes per key row: 32 or 16
-                constexpr int KPI = 32 / LPK;     // keys per copy instruction: 1 or 2
-                const int ul = lane % LPK;        // lane covers d = 8 ul .. 8 ul + 7
-                const __half* cache = kg ? P.kcache : P.vcache;
-                for (int t = 0; t < nt && ok; ++t, ++g) {
-                    int tok1;
-                    size_t row1;
-                    if (!take_index(g, kbase, tok1, row1)) {
+                // (lanes KPW .. 31 read keys of the next warp; their values are unused)
+                uint32_t tile, fullb;
+                if (kg) {
+                    if (!mbar_wait(bar(B_KEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
                         ok = false;
                         break;
                     }
-                    // (lanes KPW .. 31 read keys of the next warp; their values are unused)
-                    uint32_t tile, fullb;
-                    if (kg) {
-                        if (!mbar_wait(bar(B_KEMPTY), (g & 1) ^ 1, abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tile = sbase + OFF_K;
-                        fullb = bar(B_KFULL);
-                    } else {
-                        const int vb = g & 1;
-                        if (!mbar_wait(bar(B_VEMPTY + vb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tile = sbase + OFF_V + vb * KV_TILE_BYTES;
-                        fullb = bar(B_VFULL + vb);
+                    tile = sbase + OFF_K;
+                    fullb = bar(B_KFULL);
+                } else {
+                    const int vb = g & 1;
+                    if (!mbar_wait(bar(B_VEMPTY + vb), ((g >> 1) & 1) ^ 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
                     }
+                    tile = sbase + OFF_V + vb * KV_TILE_BYTES;
+                    fullb = bar(B_VFULL + vb);
+                }
 #pragma unroll 4
-                    for (int e = 0; e < KPW / KPI; ++e) {
-                        const int src = KPI * e + lane / LPK;   // lane holding this key's row
-                        const int key = kbase + src;
-                        const int tok = __shfl_sync(0xffffffffu, tok1, src);
-                        const size_t row = __shfl_sync(0xffffffffu, row1, src);
-                        // chunk ul / 8, unit ul % 8 of the key's swizzled row
-                        const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
-                        const __half* sp = tok >= 0 ? cache + row + ul * 8 : cache;
-                        cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
-                    }
-                    cp_async_arrive(fullb);
+                for (int e = 0; e < KPW / KPI; ++e) {
+                    const int src = KPI * e + lane / LPK;   // lane holding this key's row
+                    const int key = kbase + src;
+                    const int tok = __shfl_sync(0xffffffffu, tok1, src);
+                    const size_t row = __shfl_sync(0xffffffffu, row1, src);
+                    // chunk ul / 8, unit ul % 8 of the key's swizzled row
+                    const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
+                    const __half* sp = tok >= 0 ? cache + row + ul * 8 : cache;
+                    cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
                 }
+                cp_async_arrive(fullb);
             }
         }
         if (!ok) asm volatile("cp.async.wait_all;" ::: "memory");
@@ -500,8 +518,7 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
         const int wq = warp & 3;
         const int k = wq * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        // E4M3: the keys are the codes' values; their scale joins the score scale.
-        const float sl2 = F8 ? P.scale_log2 * __ldg(P.kscale) : P.scale_log2;
+        const float sl2 = P.scale_log2;
         uint32_t g = 0;
         uint32_t gphase = 0;
         bool ok = true;
@@ -646,10 +663,7 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
                 const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
-                if constexpr (F8)
-                    inv[c] = l > 0.f ? __ldg(P.vscale) / l : 0.f;
-                else
-                    inv[c] = l > 0.f ? 1.0f / l : 0.f;
+                inv[c] = l > 0.f ? 1.0f / l : 0.f;
             }
 #pragma unroll
             for (int h = 0; h < HALVES; ++h) {
@@ -670,88 +684,590 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
         }
     }
 
-    if (warp == IDX_WARP) {
-        // ------------------------------------------------------------ token index
-        // Same walk as the gather warps (rows of this CTA, tiles of each
-        // non-empty row).  Lane l resolves selected position 32 t + l of the
-        // row, i.e. keys 4 l .. 4 l + 3 of tile t: id -> set membership ->
-        // physical page -> cache token rows, -1 for masked keys (past the
-        // list, a bad id, a repeat, or past the row's position).
-        int* idx = reinterpret_cast<int*>(gbase + OFF_IDX);
-        uint32_t* seen = reinterpret_cast<uint32_t*>(gbase + OFF_SEEN);
-        const int lp = P.log2_page, pmask = (1 << P.log2_page) - 1;
+    if (warp == IDX_WARP)
+        index_warp(P, reinterpret_cast<int*>(gbase + OFF_IDX),
+                   reinterpret_cast<uint32_t*>(gbase + OFF_SEEN), bar(B_IFULL), bar(B_IEMPTY),
+                   abort_flag);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ======================================================================
+// E4M3 cache: raw codes on the FP8 tensor cores.
+//
+// The gather copies a selected token's E4M3 code row (DH bytes) unchanged
+// into a 128B-swizzled tile, in 128-byte halves of d, the layout a TMA copy
+// of a cache page would give.  Q.K^T and P.V then run as tcgen05.mma
+// kind::f8f6f4 on those bytes, so nothing is decoded: Q (one scale per head,
+// x / qs within +-256) and P (<= 256) enter as three-term E4M3 expansions laid
+// side by side along N (term e of head c is row e * TS + c of the operand),
+// and the key threads combine the three partial products of S^T and O^T.
+// The K scale joins the score scale and the V scale the final 1 / l.
+// A moved reference max sits REF_SHIFT below the tile's max, so that P stays
+// far above the expansion's floor of 2^-19 (the paged tail's rule).
+// Warps: gather warps (half K, half V), the UMMA issuer, four key warps, the
+// token index warp, then F8_QWARPS warps that build each row's Q expansion
+// one row ahead (two Q buffers).  Two K and two V buffers: the gather of
+// tile t + 1 never waits for the Q.K^T of tile t.
+// ======================================================================
+constexpr float REF_SHIFT = 6.0f;
+constexpr int F8_QWARPS = 2;
+constexpr int F8_NKB = 2, F8_NVB = 2;   // K / V tile buffers
+// Rows per expansion term (the heads of the launch, padded to 8) and the UMMA
+// N: three terms, rounded up to the N granule of 16.
+template <int HQ>
+constexpr int f8_ts() { return HQ == NP ? NP : 8; }
+template <int HQ>
+constexpr int f8_n() { return (3 * f8_ts<HQ>() + 15) / 16 * 16; }
+// Half the bytes of the fp16 rows: eight gather warps move a tile's codes in
+// about the time sixteen take for fp16.
+template <int HQ, int DH>
+constexpr int f8_gather_warps() { return 8; }
+template <int HQ, int DH>
+constexpr int f8_nthreads() { return 32 * (f8_gather_warps<HQ, DH>() + 6 + F8_QWARPS); }
+enum {
+    F_KFULL = 0,      // [F8_NKB]
+    F_KEMPTY = 2,     // [F8_NKB]
+    F_VFULL = 4,      // [F8_NVB]
+    F_VEMPTY = 7,     // [F8_NVB]
+    F_QFULL = 10,     // [2]
+    F_QEMPTY = 12,    // [2] the row's last Q.K^T and its key threads' epilogue
+    F_SFULL = 14,     // [2]
+    F_PREADY = 16,    // [2]
+    F_PTEMPTY = 18,   // [2]
+    F_DRAIN = 20,
+    F_GROUP = 21,
+    F_IFULL = 22,          // [NI]
+    F_IEMPTY = 22 + NI,    // [NI]
+    F_NUM_BARS = 22 + 2 * NI
+};
+static_assert(F8_NKB <= 2 && F8_NVB <= 3, "barrier slots");
+// smem layout (offsets from a 1024-aligned base)
+template <int HQ, int DH>
+struct SL8 {
+    static constexpr int TS = f8_ts<HQ>();
+    static constexpr int N3 = f8_n<HQ>();
+    static constexpr int RAW_TILE = TILE * DH;                     // 32 / 16 KB of codes
+    static constexpr int OFF_K = 0;                                // [F8_NKB][DH / 128][TILE][128]
+    static constexpr int OFF_V = OFF_K + F8_NKB * RAW_TILE;        // [F8_NVB][DH / 128][TILE][128]
+    static constexpr int Q_BYTES = N3 * DH;                        // [DH / 128][N3][128]
+    static constexpr int OFF_Q = OFF_V + F8_NVB * RAW_TILE;        // 2 Q expansions
+    static constexpr int PT_BYTES = N3 * TILE;                     // [N3][128 keys]
+    static constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;             // 2 P^T expansions
+    static constexpr int OFF_QS = OFF_PT + 2 * PT_BYTES;           // [2][NP] Q scales
+    static constexpr int OFF_RED = OFF_QS + 2 * NP * 4;            // [4][NP]
+    static constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
+    static constexpr int OFF_FAC = OFF_MREF + NP * 4;
+    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;              // [2][4] ints
+    static constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;     // [NI][TILE] token rows
+    static constexpr int OFF_SEEN = OFF_IDX + NI * TILE * 4;
+    static constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
+    static constexpr int OFF_TMEM = OFF_BAR + F_NUM_BARS * 8;
+    static constexpr int SMEM = OFF_TMEM + 16 + 1024;
+    static constexpr uint32_t S_COL = 0;            // 2 x N3
+    static constexpr uint32_t O_COL = 2 * N3;       // DH / 128 halves x N3
+    static_assert(OFF_Q % 1024 == 0 && OFF_PT % 1024 == 0 && Q_BYTES % 1024 == 0 &&
+                  PT_BYTES % 1024 == 0, "swizzle atoms");
+    static_assert(O_COL + (DH / 128) * N3 <= 256, "tensor memory columns");
+};
+constexpr uint32_t F8_TMEM_COLS = 256;
+
+template <int HQ, int DH>
+__global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(const Params P) {
+    using L = SL8<HQ, DH>;
+    constexpr int HALVES = DH / 128;
+    constexpr int TS = L::TS, N3 = L::N3, RAW_TILE = L::RAW_TILE;
+    constexpr int NGW = f8_gather_warps<HQ, DH>();
+    constexpr int NTHREADS = f8_nthreads<HQ, DH>();
+    constexpr int MMA_WARP = NGW, KEY_WARP0 = NGW + 1, IDX_WARP = NGW + 5, Q_WARP0 = NGW + 6;
+    constexpr int NGATHER = 32 * (NGW / 2);   // arrivals per K or V tile
+    // E4M3 x E4M3 -> f32 (format fields 0 = E4M3 for kind::f8f6f4); A = K
+    // (K-major) for Q.K^T, A = V^T (MN-major) for P.V.
+    constexpr uint32_t IDESC_QK = idesc_f16_f32(128, N3, false, false);
+    constexpr uint32_t IDESC_PV = idesc_f16_f32(128, N3, true, false);
+    const int nh = (HQ == NP) ? P.nh : HQ;
+    const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * DH;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (sbase - smem_u32(smem_raw));
+    float* qs = reinterpret_cast<float*>(gbase + L::OFF_QS);
+    float* red = reinterpret_cast<float*>(gbase + L::OFF_RED);
+    float* mref = reinterpret_cast<float*>(gbase + L::OFF_MREF);
+    float* fac = reinterpret_cast<float*>(gbase + L::OFF_FAC);
+    volatile int* flags = reinterpret_cast<volatile int*>(gbase + L::OFF_FLAG);
+    const uint32_t bars = sbase + L::OFF_BAR;
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(gbase + L::OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_ptr + 1);
+    auto bar = [&](int i) { return bars + 8u * i; };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < F8_NKB; ++b) {
+            mbar_init(bar(F_KFULL + b), NGATHER);
+            mbar_init(bar(F_KEMPTY + b), 1);
+        }
+        for (int b = 0; b < F8_NVB; ++b) {
+            mbar_init(bar(F_VFULL + b), NGATHER);
+            mbar_init(bar(F_VEMPTY + b), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(F_QFULL + b), 32 * F8_QWARPS);
+            mbar_init(bar(F_QEMPTY + b), 2);
+            mbar_init(bar(F_SFULL + b), 1);
+            mbar_init(bar(F_PREADY + b), 128);
+            mbar_init(bar(F_PTEMPTY + b), 1);
+        }
+        mbar_init(bar(F_DRAIN), 1);
+        mbar_init(bar(F_GROUP), 128);
+        for (int b = 0; b < NI; ++b) {
+            mbar_init(bar(F_IFULL + b), 32);
+            mbar_init(bar(F_IEMPTY + b), 32 * NGW + 128);   // gather and key threads
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // Zero the Q and P^T expansions once: rows no head writes (heads past nh,
+    // the padding of N) stay zero.
+    for (int u = threadIdx.x; u < (2 * L::Q_BYTES + 2 * L::PT_BYTES) / 16; u += NTHREADS)
+        *reinterpret_cast<uint4*>(gbase + L::OFF_Q + u * 16) = make_uint4(0, 0, 0, 0);
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_ptr), F8_TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_ptr;
+
+    if (warp < NGW) {
+        // ------------------------------------------------------------ gather
+        // Warps 0 .. NGW / 2 - 1 copy K code rows, the others V, KPW keys of
+        // every tile each; a code row is DH bytes, LPK lanes of 16 bytes.
+        const int* idx = reinterpret_cast<const int*>(gbase + L::OFF_IDX);
+        const size_t tok_stride = HQ == NP ? (size_t)P.kv_stride : (size_t)DH;
+        constexpr int KW = NGW / 2;
+        constexpr int KPW = TILE / KW;
+        static_assert(KPW <= 32 && TILE == KPW * KW, "keys per warp");
+        constexpr int LPK = DH / 16;      // lanes per key row: 16 or 8
+        constexpr int KPI = 32 / LPK;     // keys per copy instruction: 2 or 4
+        const bool kg = warp < KW;
+        const int kbase = (warp % KW) * KPW;
+        const int ul = lane % LPK;        // lane covers bytes 16 ul .. 16 ul + 15
+        const uint8_t* cache = kg ? P.kcache8 : P.vcache8;
         uint32_t g = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-            const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
-            const int nt = row_tiles(cnt);
-            if (nt == 0) continue;
-            const int p = P.ctx_len - P.rows + i;
-            const int own = p / BLK;                     // the row's own block
-            const bool exact = own < SEEN_BITS;          // bit = id, no collisions
-            const int32_t* sel = P.sel_idx + (size_t)i * P.max_sel;
-            for (int w = lane; w < SEEN_BITS / 32; w += 32) seen[w] = 0u;
-            __syncwarp();
-            for (int t = 0; t < nt; ++t, ++g) {
+            const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+            for (int t = 0; t < nt && ok; ++t, ++g) {
                 const int slot = (int)(g % NI);
-                if (!mbar_wait(bar(B_IEMPTY + slot), ((g / NI) & 1) ^ 1, abort_flag, P.err)) {
+                if (!mbar_wait(bar(F_IFULL + slot), (g / NI) & 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
-                const int li = t * (TILE / BLK) + lane;
-                int b = -1;
-                bool valid = false;
-                if (li < cnt) {
-                    b = __ldg(sel + li);
-                    valid = b >= 0 && b <= own;
+                const int tok1 = idx[slot * TILE + kbase + lane];
+                mbar_arrive(bar(F_IEMPTY + slot));
+                const size_t row1 = tok1 >= 0 ? (size_t)tok1 * tok_stride : 0;
+                uint32_t tile, fullb;
+                if (kg) {
+                    const int kb = (int)(g % F8_NKB);
+                    if (!mbar_wait(bar(F_KEMPTY + kb), ((g / F8_NKB) & 1) ^ 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tile = sbase + L::OFF_K + kb * RAW_TILE;
+                    fullb = bar(F_KFULL + kb);
+                } else {
+                    const int vb = (int)(g % F8_NVB);
+                    if (!mbar_wait(bar(F_VEMPTY + vb), ((g / F8_NVB) & 1) ^ 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tile = sbase + L::OFF_V + vb * RAW_TILE;
+                    fullb = bar(F_VFULL + vb);
                 }
-                const unsigned bad = __ballot_sync(0xffffffffu, li < cnt && !valid);
-                if (bad && lane == 0) atomicOr(P.err, kErrBadBlockId);
-                // A repeat within this tile: a lower lane holds the same id.
-                const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-                bool dup = false;
-                if (valid) {
-                    const unsigned same = __match_any_sync(vmask, b);
-                    dup = (same & ((1u << lane) - 1u)) != 0u;
+#pragma unroll 4
+                for (int e = 0; e < KPW / KPI; ++e) {
+                    const int src = KPI * e + lane / LPK;   // lane holding this key's row
+                    const int key = kbase + src;
+                    const int tok = __shfl_sync(0xffffffffu, tok1, src);
+                    const size_t row = __shfl_sync(0xffffffffu, row1, src);
+                    // half ul / 8, unit ul % 8 of the key's swizzled row
+                    const uint32_t dst = tile + (ul >> 3) * (TILE * 128) + sw128(key, ul & 7);
+                    const uint8_t* sp = tok >= 0 ? cache + row + ul * 16 : cache;
+                    cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
                 }
-                // A repeat of an earlier tile: the id's bit is set (exact), or
-                // its hash bit is set and an earlier position holds it.
-                const uint32_t h = (uint32_t)b & (uint32_t)(SEEN_BITS - 1);
-                bool cand = valid && !dup && ((seen[h >> 5] >> (h & 31u)) & 1u);
-                if (cand && exact) {
-                    dup = true;
-                    cand = false;
-                }
-                unsigned cm = __ballot_sync(0xffffffffu, cand);
-                while (cm) {
-                    const int src = __ffs(cm) - 1;
-                    cm &= cm - 1u;
-                    const int bb = __shfl_sync(0xffffffffu, b, src);
-                    bool found = false;
-                    for (int j0 = 0; j0 < t * (TILE / BLK) && !found; j0 += 32)
-                        found = __any_sync(0xffffffffu, __ldg(sel + j0 + lane) == bb);
-                    if (lane == src) dup = found;
-                }
-                __syncwarp();
-                if (valid && !dup) atomicOr(seen + (h >> 5), 1u << (h & 31u));
-                if (__ballot_sync(0xffffffffu, dup) && lane == 0) atomicOr(P.err, kErrDupBlockId);
-                const bool use = valid && !dup;
-                const int tok0 = b * BLK;
-                int pg = use ? __ldg(P.table + (tok0 >> lp)) : 0;   // a block never straddles a page
-                if (use && (pg < 0 || pg >= P.num_pages)) {
-                    atomicOr(P.err, kErrBadPageId);
-                    pg = 0;
-                }
-                const int r0 = (pg << lp) + (tok0 & pmask);
-                int4 r;
-                r.x = (use && tok0 + 0 <= p) ? r0 + 0 : -1;
-                r.y = (use && tok0 + 1 <= p) ? r0 + 1 : -1;
-                r.z = (use && tok0 + 2 <= p) ? r0 + 2 : -1;
-                r.w = (use && tok0 + 3 <= p) ? r0 + 3 : -1;
-                reinterpret_cast<int4*>(idx + slot * TILE)[lane] = r;
-                __syncwarp();   // the set's bits are read by every lane in the next tile
-                mbar_arrive(bar(B_IFULL + slot));
+                cp_async_arrive(fullb);
             }
+        }
+        if (!ok) asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------------------ UMMA issuer
+        // Tiles of all this CTA's rows in one stream: Q.K^T(g), then P.V(g - 1),
+        // so the first Q.K^T of a row is issued while the previous row's last
+        // softmax runs.
+        if (lane == 0) {
+            bool ok = true;
+            auto issue_pv = [&](uint32_t x, bool first) -> bool {
+                if (!mbar_wait(bar(F_PREADY + (x & 1)), (x >> 1) & 1, abort_flag, P.err))
+                    return false;
+                const int vb = (int)(x % F8_NVB);
+                if (!mbar_wait(bar(F_VFULL + vb), (x / F8_NVB) & 1, abort_flag, P.err)) return false;
+                // cp.async writes are generic-proxy writes; order them before UMMA reads.
+                fence_async_shared();
+                tc_fence_after();
+                const uint32_t vst = sbase + L::OFF_V + vb * RAW_TILE;
+                const uint32_t pt = sbase + L::OFF_PT + (x & 1) * L::PT_BYTES;
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+#pragma unroll
+                    for (int ks = 0; ks < TILE / 32; ++ks) {
+                        // V^T half h: M = 128 d (one 128-byte atom), K = 32 keys (rows)
+                        const uint64_t a = sdesc_sw128(vst + h * (TILE * 128) + ks * 4096, TILE * 128, 1024);
+                        const uint64_t b = sdesc_sw128(pt + ks * 32, 16, 1024);
+                        umma_f8(tmem + L::O_COL + h * N3, a, b, IDESC_PV, (!first || ks > 0));
+                    }
+                }
+                umma_commit(bar(F_PTEMPTY + (x & 1)));
+                umma_commit(bar(F_VEMPTY + vb));
+                return true;
+            };
+            uint32_t g = 0, xprev = 0;
+            int rloc = 0;
+            bool have_prev = false, prev_first = false;
+            for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+                const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+                if (nt == 0) continue;
+                const int qb = rloc & 1;
+                if (!mbar_wait(bar(F_QFULL + qb), (rloc >> 1) & 1, abort_flag, P.err)) {
+                    ok = false;
+                    break;
+                }
+                ++rloc;
+                const uint32_t sq = sbase + L::OFF_Q + qb * L::Q_BYTES;
+                for (int t = 0; t < nt; ++t, ++g) {
+                    const int kb = (int)(g % F8_NKB);
+                    if (!mbar_wait(bar(F_KFULL + kb), (g / F8_NKB) & 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_async_shared();
+                    tc_fence_after();
+                    const uint32_t kst = sbase + L::OFF_K + kb * RAW_TILE;
+#pragma unroll
+                    for (int kk = 0; kk < DH / 32; ++kk) {
+                        const int h = kk >> 2;   // d half
+                        const uint64_t a = sdesc_sw128(kst + h * (TILE * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(sq + h * (N3 * 128) + (kk & 3) * 32, 16, 1024);
+                        umma_f8(tmem + L::S_COL + (g & 1) * N3, a, b, IDESC_QK, kk > 0);
+                    }
+                    umma_commit(bar(F_SFULL + (g & 1)));
+                    umma_commit(bar(F_KEMPTY + kb));
+                    if (t == nt - 1) umma_commit(bar(F_QEMPTY + qb));
+                    if (have_prev && !(ok = issue_pv(xprev, prev_first))) break;
+                    xprev = g;
+                    prev_first = t == 0;
+                    have_prev = true;
+                }
+            }
+            if (ok && have_prev) ok = issue_pv(xprev, prev_first);
+            if (!ok) {
+                umma_commit(bar(F_DRAIN));
+                drain_wait(bar(F_DRAIN), 0);
+            }
+        }
+    } else if (warp < KEY_WARP0 + 4) {
+        // ------------------------------------------------------------ key warps
+        const int wq = warp & 3;
+        const int k = wq * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+        // The keys are the codes' values: the K scale joins the score scale.
+        const float sl2k = P.scale_log2 * __ldg(P.kscale);
+        const float vsc = __ldg(P.vscale);
+        // P^T row r, key k: byte r * 128 + (((k >> 4) ^ (r & 7)) << 4) + (k & 15).
+        const uint32_t p_key = (uint32_t)k & 15u, p_unit = (uint32_t)k >> 4;
+        auto pofs = [&](int r) -> uint32_t {
+            return (uint32_t)r * 128u + ((p_unit ^ ((uint32_t)r & 7u)) << 4) + p_key;
+        };
+        uint32_t g = 0;
+        uint32_t gphase = 0;
+        int rloc = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+            const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+            if (nt == 0) {
+                // Nothing selected: the row's output is zero.
+                for (int u = k; u < nh * (DH / 8); u += 128)
+                    reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
+                continue;
+            }
+            const int qb = rloc & 1;
+            ok = mbar_wait(bar(F_QFULL + qb), (rloc >> 1) & 1, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ++rloc;
+            // Score scale per head (log2 units): scale * kscale * the head's Q scale.
+            float sl2[HQ];
+#pragma unroll
+            for (int c = 0; c < HQ; ++c) sl2[c] = c < nh ? sl2k * qs[qb * NP + c] : 0.f;
+            if (k < NP) mref[k] = -INFINITY;
+            ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            float lpart[HQ];
+#pragma unroll
+            for (int c = 0; c < HQ; ++c) lpart[c] = 0.f;
+            for (int t = 0; t < nt; ++t, ++g) {
+                const int b = g & 1;
+                bool masked;
+                {
+                    // The index warp's verdict on this key (-1: masked).
+                    const int slot = (int)(g % NI);
+                    ok = mbar_wait(bar(F_IFULL + slot), (g / NI) & 1, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    masked = reinterpret_cast<const int*>(gbase + L::OFF_IDX)[slot * TILE + k] < 0;
+                    mbar_arrive(bar(F_IEMPTY + slot));
+                }
+                ok = mbar_wait(bar(F_SFULL + b), (g >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                float s[HQ];
+                {
+                    uint32_t r1[TS], r2[TS], r3[TS];
+                    const uint32_t sc = t_lane + L::S_COL + b * N3;
+                    tmem_ldn<TS>(sc, r1);
+                    tmem_ldn<TS>(sc + TS, r2);
+                    tmem_ldn<TS>(sc + 2 * TS, r3);
+                    tmem_ld_wait<TS>(r1);
+                    tmem_ld_wait<TS>(r2);
+                    tmem_ld_wait<TS>(r3);
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c)
+                        s[c] = masked ? -INFINITY : combine3(r1[c], r2[c], r3[c]) * sl2[c];
+                }
+                bool exceed = false;
+#pragma unroll
+                for (int c = 0; c < HQ; ++c)
+                    if (c < nh) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
+                const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                volatile int* fl = flags + (g & 1) * 4;
+                if (lane == 0) fl[wq] = vote != 0;
+                ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const bool any = fl[0] | fl[1] | fl[2] | fl[3];
+                if (any) {
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) {
+                        if (c >= nh) break;
+                        float m = s[c];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (lane == 0) red[wq * NP + c] = m;
+                    }
+                    ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (k < NP) {
+                        float f = 1.0f;
+                        if (k < nh) {
+                            const int c = k;
+                            const float tmax = fmaxf(fmaxf(red[c], red[NP + c]),
+                                                     fmaxf(red[2 * NP + c], red[3 * NP + c]));
+                            const float old = mref[c];
+                            if (tmax > old + RESCALE_THRESHOLD) {
+                                const float ref = tmax - REF_SHIFT;
+                                f = (old == -INFINITY) ? 0.f : ex2(old - ref);
+                                mref[c] = ref;
+                            }
+                        }
+                        fac[k] = f;
+                    }
+                    ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (t > 0) {
+                        // O^T must hold every earlier P.V of the row before it is rescaled.
+                        const uint32_t x = g - 1;
+                        ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int g6 = 0; g6 < 3 * HALVES; ++g6) {   // (d half, expansion term)
+                            const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * TS;
+                            uint32_t r[TS];
+                            tmem_ldn<TS>(t_lane + col, r);
+                            tmem_ld_wait<TS>(r);
+#pragma unroll
+                            for (int c = 0; c < HQ; ++c)
+                                r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c]);
+                            tmem_stn<TS>(t_lane + col, r);
+                        }
+                        tmem_st_wait();
+                    }
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) lpart[c] *= fac[c];
+                }
+                // P^T buffer b is free once the P.V two tiles back has completed.
+                ok = mbar_wait(bar(F_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                {
+                    // [P1 | P2 | P3]^T, K-major: row = term * TS + head, byte = key.
+                    uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
+#pragma unroll
+                    for (int c = 0; c < HQ; c += 2) {
+                        if (c >= nh) break;
+                        const float m0 = mref[c], m1 = mref[c + 1];
+                        const float p0 = ex2(s[c] - (m0 == -INFINITY ? 0.f : m0));
+                        const float p1 = c + 1 < nh ? ex2(s[c + 1] - (m1 == -INFINITY ? 0.f : m1)) : 0.f;
+                        lpart[c] += p0;
+                        lpart[c + 1] += p1;
+                        uint32_t t3[3];
+                        split3_e4m3x2(p0, p1, t3[0], t3[1], t3[2]);
+#pragma unroll
+                        for (int e = 0; e < 3; ++e) {
+                            pt[pofs(e * TS + c)] = (uint8_t)(t3[e] & 0xFF);
+                            pt[pofs(e * TS + c + 1)] = (uint8_t)(t3[e] >> 8);
+                        }
+                    }
+                }
+                fence_async_shared();
+                mbar_arrive(bar(F_PREADY + b));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- row epilogue
+            const uint32_t x = g - 1;
+            ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < HQ; ++c) {
+                if (c >= nh) break;
+                float v = lpart[c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) red[wq * NP + c] = v;
+            }
+            ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            float inv[HQ];
+#pragma unroll
+            for (int c = 0; c < HQ; ++c) {
+                const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
+                inv[c] = l > 0.f ? vsc / l : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+                uint32_t r1[TS], r2[TS], r3[TS];
+                const uint32_t oc = t_lane + L::O_COL + h * N3;
+                tmem_ldn<TS>(oc, r1);
+                tmem_ldn<TS>(oc + TS, r2);
+                tmem_ldn<TS>(oc + 2 * TS, r3);
+                tmem_ld_wait<TS>(r1);
+                tmem_ld_wait<TS>(r2);
+                tmem_ld_wait<TS>(r3);
+                const int d = h * 128 + k;
+#pragma unroll
+                for (int c = 0; c < HQ; ++c)
+                    if (c < nh)
+                        P.out[(size_t)i * q_stride + c * DH + d] =
+                            __float2half_rn(combine3(r1[c], r2[c], r3[c]) * inv[c]);
+            }
+            // red / mref are rewritten by the next row, and the Q scales of this
+            // row's buffer by the Q warps, only after this barrier.
+            ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (k == 0) mbar_arrive(bar(F_QEMPTY + qb));
+        }
+    } else if (warp == IDX_WARP) {
+        index_warp(P, reinterpret_cast<int*>(gbase + L::OFF_IDX),
+                   reinterpret_cast<uint32_t*>(gbase + L::OFF_SEEN), bar(F_IFULL), bar(F_IEMPTY),
+                   abort_flag);
+    } else {
+        // ------------------------------------------------------------ Q expansion
+        // Warp qw takes heads qw, qw + F8_QWARPS, ...: each lane loads EPL
+        // values of a head's row (all of the row's loads issued before the
+        // wait for the buffer), the head's scale is its absolute max / 256, and
+        // the three E4M3 terms of x / scale go to rows head, TS + head and
+        // 2 TS + head of the K-major, 128B-swizzled expansion.
+        const int qw = warp - Q_WARP0;
+        constexpr int RPW = (HQ + F8_QWARPS - 1) / F8_QWARPS;
+        constexpr int EPL = DH / 32;   // elements of a row per lane: 8 or 4
+        using QV = typename std::conditional<EPL == 8, uint4, uint2>::type;
+        const int d0 = lane * EPL;
+        int rloc = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
+            const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+            if (nt == 0) continue;
+            const int qb = rloc & 1;
+            QV raw[RPW];
+#pragma unroll
+            for (int j = 0; j < RPW; ++j) {
+                const int c = qw + F8_QWARPS * j;
+                raw[j] = c < nh ? *reinterpret_cast<const QV*>(P.q + (size_t)i * q_stride + c * DH + d0)
+                                : QV{};
+            }
+            ok = mbar_wait(bar(F_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            uint8_t* qbuf = gbase + L::OFF_Q + qb * L::Q_BYTES;
+#pragma unroll
+            for (int j = 0; j < RPW; ++j) {
+                const int c = qw + F8_QWARPS * j;
+                if (c >= nh) break;
+                float x[EPL];
+                const __half* hx = reinterpret_cast<const __half*>(&raw[j]);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) x[e] = __half2float(hx[e]);
+                float amax = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float sc = amax > 0.f ? amax / 256.0f : 1.0f;
+                const float inv = 1.0f / sc;
+                uint32_t w1[2] = {0, 0}, w2[2] = {0, 0}, w3[2] = {0, 0};
+#pragma unroll
+                for (int e = 0; e < EPL; e += 2) {
+                    uint32_t b1, b2, b3;
+                    split3_e4m3x2(x[e] * inv, x[e + 1] * inv, b1, b2, b3);
+                    w1[e >> 2] |= b1 << (8 * (e & 3));
+                    w2[e >> 2] |= b2 << (8 * (e & 3));
+                    w3[e >> 2] |= b3 << (8 * (e & 3));
+                }
+                const int h = d0 >> 7, cin = d0 & 127;
+                uint8_t* qh = qbuf + h * (N3 * 128) + (cin & 15);
+                if constexpr (EPL == 8) {
+                    *reinterpret_cast<uint2*>(qh + sw128(c, cin >> 4)) = make_uint2(w1[0], w1[1]);
+                    *reinterpret_cast<uint2*>(qh + sw128(TS + c, cin >> 4)) = make_uint2(w2[0], w2[1]);
+                    *reinterpret_cast<uint2*>(qh + sw128(2 * TS + c, cin >> 4)) = make_uint2(w3[0], w3[1]);
+                } else {
+                    *reinterpret_cast<uint32_t*>(qh + sw128(c, cin >> 4)) = w1[0];
+                    *reinterpret_cast<uint32_t*>(qh + sw128(TS + c, cin >> 4)) = w2[0];
+                    *reinterpret_cast<uint32_t*>(qh + sw128(2 * TS + c, cin >> 4)) = w3[0];
+                }
+                if (lane == 0) qs[qb * NP + c] = sc;
+            }
+            // Generic-proxy stores, read by the tensor cores (async proxy).
+            fence_async_shared();
+            mbar_arrive(bar(F_QFULL + qb));
+            ++rloc;
         }
     }
 
@@ -759,7 +1275,7 @@ __global__ void __launch_bounds__(nthreads<HQ, F8, DH>(), 1) sparse_kernel(const
     __syncthreads();
     if (warp == MMA_WARP) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, F8_TMEM_COLS);
     }
 }
 
@@ -797,17 +1313,23 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
     using KernelFn = void (*)(Params);
     KernelFn fn;
     int smem, threads;
-    if (Dh == 128) {
-        fn = e4m3 ? (six ? sparse_kernel<kHq, true, 128> : sparse_kernel<NP, true, 128>)
-                  : (six ? sparse_kernel<kHq, false, 128> : sparse_kernel<NP, false, 128>);
-        threads = e4m3 ? (six ? nthreads<kHq, true, 128>() : nthreads<NP, true, 128>())
-                       : (six ? nthreads<kHq, false, 128>() : nthreads<NP, false, 128>());
+    if (e4m3) {
+        if (Dh == 128) {
+            fn = six ? sparse_f8_kernel<kHq, 128> : sparse_f8_kernel<NP, 128>;
+            threads = six ? f8_nthreads<kHq, 128>() : f8_nthreads<NP, 128>();
+            smem = six ? SL8<kHq, 128>::SMEM : SL8<NP, 128>::SMEM;
+        } else {
+            fn = six ? sparse_f8_kernel<kHq, 256> : sparse_f8_kernel<NP, 256>;
+            threads = six ? f8_nthreads<kHq, 256>() : f8_nthreads<NP, 256>();
+            smem = six ? SL8<kHq, 256>::SMEM : SL8<NP, 256>::SMEM;
+        }
+    } else if (Dh == 128) {
+        fn = six ? sparse_kernel<kHq, 128> : sparse_kernel<NP, 128>;
+        threads = six ? nthreads<kHq, 128>() : nthreads<NP, 128>();
         smem = smem_bytes<128>();
     } else {
-        fn = e4m3 ? (six ? sparse_kernel<kHq, true, 256> : sparse_kernel<NP, true, 256>)
-                  : (six ? sparse_kernel<kHq, false, 256> : sparse_kernel<NP, false, 256>);
-        threads = e4m3 ? (six ? nthreads<kHq, true, 256>() : nthreads<NP, true, 256>())
-                       : (six ? nthreads<kHq, false, 256>() : nthreads<NP, false, 256>());
+        fn = six ? sparse_kernel<kHq, 256> : sparse_kernel<NP, 256>;
+        threads = six ? nthreads<kHq, 256>() : nthreads<NP, 256>();
         smem = smem_bytes<256>();
     }
     if (ensure_smem_limit(reinterpret_cast<const void*>(fn), smem) != GQA_OK)
