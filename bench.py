@@ -413,7 +413,7 @@ def bench_paged_batch(binding, device, steps, warmup, flush, B=8, R=2, max_ctx=6
 def bench_sparse(binding, T, device, steps, warmup, flush, rows=4096, ctx_len=32768, seed=0,
                  e4m3=False, Dh=D):
     """Selected-block sparse prefill over an fp16 cache, or an E4M3 cache
-    (codes converted to fp16 on the way into shared memory)."""
+    (the raw codes on the FP8 tensor cores)."""
     import torch
     from long_context_causal_gqa_gb300 import inputs
     if e4m3:

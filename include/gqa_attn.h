@@ -233,10 +233,11 @@ int gqa_attn_sparse_blocks(const void* q, const void* kcache, const void* vcache
  *   kcache/vcache [num_pages, page, Hkv, D] uint8 E4M3 codes (OCP e4m3fn),
  *                real value = decode(byte) * scale
  *   kscale/vscale DEVICE pointers to one fp32 each, 4-byte aligned
- * The codes are converted to fp16 on their way into shared memory (exact:
- * every E4M3 value is an fp16 value); the K scale multiplies the scores and
- * the V scale the output.  A selected token's code bytes must not be the
- * E4M3 NaN code (0x7F / 0xFF).  Needs no workspace. */
+ * The codes feed the FP8 tensor cores as they are; Q (one scale per head)
+ * and the softmax weights P enter those products as three-term E4M3
+ * expansions (at least fp16's 11 significant bits); the K scale multiplies
+ * the scores and the V scale the output.  A selected token's code bytes must
+ * not be the E4M3 NaN code (0x7F / 0xFF).  Needs no workspace. */
 int gqa_attn_sparse_blocks_e4m3(const void* q, const uint8_t* kcache, const uint8_t* vcache,
                                 const float* kscale, const float* vscale,
                                 const int32_t* block_table, const int32_t* sel_idx,

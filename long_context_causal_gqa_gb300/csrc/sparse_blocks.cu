@@ -27,12 +27,10 @@
 //   until the row ends.  The epilogue writes out[i] directly (no split).
 //
 // * An E4M3 cache (the tail's storage applied to this workload) halves the
-//   gathered bytes: the gather lanes load the code bytes of their token rows
-//   into registers (a tile's loads all in flight before the lane waits for
-//   the tile buffer), convert them to fp16 with
-//   cvt.rn.f16x2.e4m3x2 and store them into the same swizzled tile the fp16
-//   path copies into, so the MMAs are unchanged; the K scale joins the score
-//   scale and the V scale the final 1 / l.
+//   gathered bytes and has a kernel of its own (sparse_f8_kernel): the codes
+//   are gathered unchanged and consumed by FP8 UMMAs (kind::f8f6f4), Q and P
+//   entering as three-term E4M3 expansions (see e4m3_umma.cuh); the K scale
+//   joins the score scale and the V scale the final 1 / l.
 //
 // * Token index warp: block-table lookups (a selected id, then a page id, two
 //   dependent loads per key) are taken off the gather warps' path: the index warp
@@ -45,9 +43,9 @@
 //   SEEN_BITS; beyond that a hash of the id, with a hit confirmed against the
 //   earlier positions), masks the repeat and flags it on the device.
 //
-// Warp roles: gather warps (sixteen or eight for an fp16 cache, four for
-// E4M3), then the TMEM owner + UMMA issuer, four key warps (softmax +
-// epilogue; thread = TMEM lane) and the token index warp.
+// Warp roles: gather warps, then the TMEM owner + UMMA issuer, four key warps
+// (softmax + epilogue; thread = TMEM lane) and the token index warp (and, in
+// the E4M3 kernel, two warps that build the Q expansions).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -718,6 +716,7 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
 constexpr float REF_SHIFT = 6.0f;
 constexpr int F8_QWARPS = 2;
 constexpr int F8_NKB = 2, F8_NVB = 2;   // K / V tile buffers
+constexpr int F8_NQB = 2;               // Q expansion buffers
 // Rows per expansion term (the heads of the launch, padded to 8) and the UMMA
 // N: three terms, rounded up to the N granule of 16.
 template <int HQ>
@@ -735,18 +734,18 @@ enum {
     F_KEMPTY = 2,     // [F8_NKB]
     F_VFULL = 4,      // [F8_NVB]
     F_VEMPTY = 7,     // [F8_NVB]
-    F_QFULL = 10,     // [2]
-    F_QEMPTY = 12,    // [2] the row's last Q.K^T and its key threads' epilogue
-    F_SFULL = 14,     // [2]
-    F_PREADY = 16,    // [2]
-    F_PTEMPTY = 18,   // [2]
-    F_DRAIN = 20,
-    F_GROUP = 21,
-    F_IFULL = 22,          // [NI]
-    F_IEMPTY = 22 + NI,    // [NI]
-    F_NUM_BARS = 22 + 2 * NI
+    F_QFULL = 10,     // [F8_NQB]
+    F_QEMPTY = 13,    // [F8_NQB] the row's last Q.K^T and its key threads' epilogue
+    F_SFULL = 16,     // [2]
+    F_PREADY = 18,    // [2]
+    F_PTEMPTY = 20,   // [2]
+    F_DRAIN = 22,
+    F_GROUP = 23,
+    F_IFULL = 24,          // [NI]
+    F_IEMPTY = 24 + NI,    // [NI]
+    F_NUM_BARS = 24 + 2 * NI
 };
-static_assert(F8_NKB <= 2 && F8_NVB <= 3, "barrier slots");
+static_assert(F8_NKB <= 2 && F8_NVB <= 3 && F8_NQB <= 3, "barrier slots");
 // smem layout (offsets from a 1024-aligned base)
 template <int HQ, int DH>
 struct SL8 {
@@ -756,14 +755,13 @@ struct SL8 {
     static constexpr int OFF_K = 0;                                // [F8_NKB][DH / 128][TILE][128]
     static constexpr int OFF_V = OFF_K + F8_NKB * RAW_TILE;        // [F8_NVB][DH / 128][TILE][128]
     static constexpr int Q_BYTES = N3 * DH;                        // [DH / 128][N3][128]
-    static constexpr int OFF_Q = OFF_V + F8_NVB * RAW_TILE;        // 2 Q expansions
+    static constexpr int OFF_Q = OFF_V + F8_NVB * RAW_TILE;        // F8_NQB Q expansions
     static constexpr int PT_BYTES = N3 * TILE;                     // [N3][128 keys]
-    static constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;             // 2 P^T expansions
-    static constexpr int OFF_QS = OFF_PT + 2 * PT_BYTES;           // [2][NP] Q scales
-    static constexpr int OFF_RED = OFF_QS + 2 * NP * 4;            // [4][NP]
-    static constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
-    static constexpr int OFF_FAC = OFF_MREF + NP * 4;
-    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;              // [2][4] ints
+    static constexpr int OFF_PT = OFF_Q + F8_NQB * Q_BYTES;        // 2 P^T expansions
+    static constexpr int OFF_QS = OFF_PT + 2 * PT_BYTES;           // [F8_NQB][NP] Q scales
+    static constexpr int OFF_RED = OFF_QS + F8_NQB * NP * 4;       // [2][4][NP] tile maxima
+    static constexpr int OFF_REDL = OFF_RED + 2 * 4 * NP * 4;      // [2][4][NP] row sums
+    static constexpr int OFF_FLAG = OFF_REDL + 2 * 4 * NP * 4;     // [2][4] ints
     static constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;     // [NI][TILE] token rows
     static constexpr int OFF_SEEN = OFF_IDX + NI * TILE * 4;
     static constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
@@ -797,8 +795,7 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
     uint8_t* gbase = smem_raw + (sbase - smem_u32(smem_raw));
     float* qs = reinterpret_cast<float*>(gbase + L::OFF_QS);
     float* red = reinterpret_cast<float*>(gbase + L::OFF_RED);
-    float* mref = reinterpret_cast<float*>(gbase + L::OFF_MREF);
-    float* fac = reinterpret_cast<float*>(gbase + L::OFF_FAC);
+    float* redl = reinterpret_cast<float*>(gbase + L::OFF_REDL);
     volatile int* flags = reinterpret_cast<volatile int*>(gbase + L::OFF_FLAG);
     const uint32_t bars = sbase + L::OFF_BAR;
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(gbase + L::OFF_TMEM);
@@ -816,9 +813,11 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
             mbar_init(bar(F_VFULL + b), NGATHER);
             mbar_init(bar(F_VEMPTY + b), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < F8_NQB; ++b) {
             mbar_init(bar(F_QFULL + b), 32 * F8_QWARPS);
             mbar_init(bar(F_QEMPTY + b), 2);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(bar(F_SFULL + b), 1);
             mbar_init(bar(F_PREADY + b), 128);
             mbar_init(bar(F_PTEMPTY + b), 1);
@@ -834,7 +833,7 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
     }
     // Zero the Q and P^T expansions once: rows no head writes (heads past nh,
     // the padding of N) stay zero.
-    for (int u = threadIdx.x; u < (2 * L::Q_BYTES + 2 * L::PT_BYTES) / 16; u += NTHREADS)
+    for (int u = threadIdx.x; u < (F8_NQB * L::Q_BYTES + 2 * L::PT_BYTES) / 16; u += NTHREADS)
         *reinterpret_cast<uint4*>(gbase + L::OFF_Q + u * 16) = make_uint4(0, 0, 0, 0);
     if (warp == MMA_WARP) {
         tmem_alloc(smem_u32(tmem_ptr), F8_TMEM_COLS);
@@ -909,9 +908,8 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
         if (!ok) asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ UMMA issuer
-        // Tiles of all this CTA's rows in one stream: Q.K^T(g), then P.V(g - 1),
-        // so the first Q.K^T of a row is issued while the previous row's last
-        // softmax runs.
+        // Per row: Q.K^T(g), then P.V(g - 1) once its P is ready; the row's
+        // last P.V before the next row's first Q.K^T.
         if (lane == 0) {
             bool ok = true;
             auto issue_pv = [&](uint32_t x, bool first) -> bool {
@@ -938,19 +936,19 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                 umma_commit(bar(F_VEMPTY + vb));
                 return true;
             };
-            uint32_t g = 0, xprev = 0;
+            uint32_t g = 0;
             int rloc = 0;
-            bool have_prev = false, prev_first = false;
             for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
                 const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
                 if (nt == 0) continue;
-                const int qb = rloc & 1;
-                if (!mbar_wait(bar(F_QFULL + qb), (rloc >> 1) & 1, abort_flag, P.err)) {
+                const int qb = rloc % F8_NQB;
+                if (!mbar_wait(bar(F_QFULL + qb), (rloc / F8_NQB) & 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
                 ++rloc;
                 const uint32_t sq = sbase + L::OFF_Q + qb * L::Q_BYTES;
+                const uint32_t g0 = g;
                 for (int t = 0; t < nt; ++t, ++g) {
                     const int kb = (int)(g % F8_NKB);
                     if (!mbar_wait(bar(F_KFULL + kb), (g / F8_NKB) & 1, abort_flag, P.err)) {
@@ -970,13 +968,10 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                     umma_commit(bar(F_SFULL + (g & 1)));
                     umma_commit(bar(F_KEMPTY + kb));
                     if (t == nt - 1) umma_commit(bar(F_QEMPTY + qb));
-                    if (have_prev && !(ok = issue_pv(xprev, prev_first))) break;
-                    xprev = g;
-                    prev_first = t == 0;
-                    have_prev = true;
+                    if (t >= 1 && !(ok = issue_pv(g - 1, g - 1 == g0))) break;
                 }
+                if (ok) ok = issue_pv(g - 1, g - 1 == g0);
             }
-            if (ok && have_prev) ok = issue_pv(xprev, prev_first);
             if (!ok) {
                 umma_commit(bar(F_DRAIN));
                 drain_wait(bar(F_DRAIN), 0);
@@ -984,6 +979,9 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
         }
     } else if (warp < KEY_WARP0 + 4) {
         // ------------------------------------------------------------ key warps
+        // Each thread keeps every head's reference max in registers: after a
+        // vote fires, the warps' partial maxima go through shared memory and
+        // one barrier, and every thread derives the same new references.
         const int wq = warp & 3;
         const int k = wq * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
@@ -1007,22 +1005,19 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                     reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
                 continue;
             }
-            const int qb = rloc & 1;
-            ok = mbar_wait(bar(F_QFULL + qb), (rloc >> 1) & 1, abort_flag, P.err);
+            const int qb = rloc % F8_NQB;
+            ok = mbar_wait(bar(F_QFULL + qb), (rloc / F8_NQB) & 1, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ++rloc;
             // Score scale per head (log2 units): scale * kscale * the head's Q scale.
-            float sl2[HQ];
+            float sl2[HQ], mr[HQ], lpart[HQ];
 #pragma unroll
-            for (int c = 0; c < HQ; ++c) sl2[c] = c < nh ? sl2k * qs[qb * NP + c] : 0.f;
-            if (k < NP) mref[k] = -INFINITY;
-            ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            float lpart[HQ];
-#pragma unroll
-            for (int c = 0; c < HQ; ++c) lpart[c] = 0.f;
+            for (int c = 0; c < HQ; ++c) {
+                sl2[c] = c < nh ? sl2k * qs[qb * NP + c] : 0.f;
+                mr[c] = -INFINITY;
+                lpart[c] = 0.f;
+            }
             for (int t = 0; t < nt; ++t, ++g) {
                 const int b = g & 1;
                 bool masked;
@@ -1053,18 +1048,26 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                     for (int c = 0; c < HQ; ++c)
                         s[c] = masked ? -INFINITY : combine3(r1[c], r2[c], r3[c]) * sl2[c];
                 }
-                bool exceed = false;
+                // A row's first tile always takes the exact max (its references
+                // are -inf); later tiles only when a score crosses its reference.
+                bool any = t == 0;
+                if (!any) {
+                    bool exceed = false;
 #pragma unroll
-                for (int c = 0; c < HQ; ++c)
-                    if (c < nh) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
-                const unsigned vote = __ballot_sync(0xffffffffu, exceed);
-                volatile int* fl = flags + (g & 1) * 4;
-                if (lane == 0) fl[wq] = vote != 0;
-                ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                const bool any = fl[0] | fl[1] | fl[2] | fl[3];
+                    for (int c = 0; c < HQ; ++c)
+                        if (c < nh) exceed |= s[c] > mr[c] + RESCALE_THRESHOLD;
+                    const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                    volatile int* fl = flags + (g & 1) * 4;
+                    if (lane == 0) fl[wq] = vote != 0;
+                    ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    any = fl[0] | fl[1] | fl[2] | fl[3];
+                }
                 if (any) {
+                    // The tile's max per head: warp maxima -> red (its slot of
+                    // this tile parity) -> one barrier -> every thread.
+                    float* rd = red + (g & 1) * (4 * NP);
 #pragma unroll
                     for (int c = 0; c < HQ; ++c) {
                         if (c >= nh) break;
@@ -1072,29 +1075,25 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
                             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                        if (lane == 0) red[wq * NP + c] = m;
+                        if (lane == 0) rd[wq * NP + c] = m;
                     }
                     ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    if (k < NP) {
-                        float f = 1.0f;
-                        if (k < nh) {
-                            const int c = k;
-                            const float tmax = fmaxf(fmaxf(red[c], red[NP + c]),
-                                                     fmaxf(red[2 * NP + c], red[3 * NP + c]));
-                            const float old = mref[c];
-                            if (tmax > old + RESCALE_THRESHOLD) {
+                    float f[HQ];
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) {
+                        f[c] = 1.0f;
+                        if (c < nh) {
+                            const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
+                                                     fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
+                            if (tmax > mr[c] + RESCALE_THRESHOLD) {
                                 const float ref = tmax - REF_SHIFT;
-                                f = (old == -INFINITY) ? 0.f : ex2(old - ref);
-                                mref[c] = ref;
+                                f[c] = (mr[c] == -INFINITY) ? 0.f : ex2(mr[c] - ref);
+                                mr[c] = ref;
                             }
                         }
-                        fac[k] = f;
                     }
-                    ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
                     if (t > 0) {
                         // O^T must hold every earlier P.V of the row before it is rescaled.
                         const uint32_t x = g - 1;
@@ -1110,13 +1109,13 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                             tmem_ld_wait<TS>(r);
 #pragma unroll
                             for (int c = 0; c < HQ; ++c)
-                                r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c]);
+                                r[c] = __float_as_uint(__uint_as_float(r[c]) * f[c]);
                             tmem_stn<TS>(t_lane + col, r);
                         }
                         tmem_st_wait();
                     }
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) lpart[c] *= fac[c];
+                    for (int c = 0; c < HQ; ++c) lpart[c] *= f[c];
                 }
                 // P^T buffer b is free once the P.V two tiles back has completed.
                 ok = mbar_wait(bar(F_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
@@ -1128,9 +1127,9 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
 #pragma unroll
                     for (int c = 0; c < HQ; c += 2) {
                         if (c >= nh) break;
-                        const float m0 = mref[c], m1 = mref[c + 1];
-                        const float p0 = ex2(s[c] - (m0 == -INFINITY ? 0.f : m0));
-                        const float p1 = c + 1 < nh ? ex2(s[c + 1] - (m1 == -INFINITY ? 0.f : m1)) : 0.f;
+                        const float p0 = ex2(s[c] - (mr[c] == -INFINITY ? 0.f : mr[c]));
+                        const float p1 = c + 1 < nh ? ex2(s[c + 1] - (mr[c + 1] == -INFINITY ? 0.f : mr[c + 1]))
+                                                    : 0.f;
                         lpart[c] += p0;
                         lpart[c + 1] += p1;
                         uint32_t t3[3];
@@ -1152,21 +1151,28 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            // Row sums: warp sums -> redl (its slot of this row parity) -> one
+            // barrier.  The next write to the same slot comes two rows later,
+            // behind barriers every thread passes after its reads here.
+            float* rl = redl + (rloc & 1) * (4 * NP);
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
                 if (c >= nh) break;
                 float v = lpart[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) red[wq * NP + c] = v;
+                if (lane == 0) rl[wq * NP + c] = v;
             }
             ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+            // Every thread has read this row's Q scales (row start) and passed
+            // the barrier above: the Q buffer may be refilled.
+            if (k == 0) mbar_arrive(bar(F_QEMPTY + qb));
             float inv[HQ];
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
-                const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
+                const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
                 inv[c] = l > 0.f ? vsc / l : 0.f;
             }
 #pragma unroll
@@ -1186,12 +1192,6 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                         P.out[(size_t)i * q_stride + c * DH + d] =
                             __float2half_rn(combine3(r1[c], r2[c], r3[c]) * inv[c]);
             }
-            // red / mref are rewritten by the next row, and the Q scales of this
-            // row's buffer by the Q warps, only after this barrier.
-            ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            if (k == 0) mbar_arrive(bar(F_QEMPTY + qb));
         }
     } else if (warp == IDX_WARP) {
         index_warp(P, reinterpret_cast<int*>(gbase + L::OFF_IDX),
@@ -1214,7 +1214,7 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
         for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
             const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
             if (nt == 0) continue;
-            const int qb = rloc & 1;
+            const int qb = rloc % F8_NQB;
             QV raw[RPW];
 #pragma unroll
             for (int j = 0; j < RPW; ++j) {
@@ -1222,7 +1222,7 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                 raw[j] = c < nh ? *reinterpret_cast<const QV*>(P.q + (size_t)i * q_stride + c * DH + d0)
                                 : QV{};
             }
-            ok = mbar_wait(bar(F_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err);
+            ok = mbar_wait(bar(F_QEMPTY + qb), ((rloc / F8_NQB) & 1) ^ 1, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             uint8_t* qbuf = gbase + L::OFF_Q + qb * L::Q_BYTES;
