@@ -111,10 +111,9 @@ struct SL {
     static constexpr int Q_BYTES = NP * DH * 2;                    // DH / 64 chunks [16][64]
     static constexpr int OFF_Q = OFF_V + 2 * KV_TILE_BYTES;        // 2 Q buffers
     static constexpr int OFF_PT = OFF_Q + 2 * Q_BYTES;             // 2 P^T buffers
-    static constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;          // [4][NP] floats
-    static constexpr int OFF_MREF = OFF_RED + 4 * NP * 4;
-    static constexpr int OFF_FAC = OFF_MREF + NP * 4;
-    static constexpr int OFF_FLAG = OFF_FAC + NP * 4;              // [2][4] ints
+    static constexpr int OFF_RED = OFF_PT + 2 * PT_BYTES;          // [2][4][NP] tile maxima
+    static constexpr int OFF_REDL = OFF_RED + 2 * 4 * NP * 4;      // [2][4][NP] row sums
+    static constexpr int OFF_FLAG = OFF_REDL + 2 * 4 * NP * 4;     // [2][4] ints
     static constexpr int OFF_IDX = (OFF_FLAG + 32 + 15) & ~15;     // [NI][TILE] int token rows
     static constexpr int OFF_SEEN = OFF_IDX + NI * TILE * 4;       // [SEEN_BITS / 32] words
     static constexpr int OFF_BAR = (OFF_SEEN + SEEN_BITS / 8 + 7) & ~7;
@@ -277,8 +276,8 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
     constexpr int HALVES = DH / 128;   // 128-d halves of a row (one M = 128 P.V each)
     constexpr int KV_TILE_BYTES = L::KV_TILE_BYTES;
     constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, Q_BYTES = L::Q_BYTES, OFF_Q = L::OFF_Q;
-    constexpr int OFF_PT = L::OFF_PT, OFF_RED = L::OFF_RED, OFF_MREF = L::OFF_MREF;
-    constexpr int OFF_FAC = L::OFF_FAC, OFF_FLAG = L::OFF_FLAG, OFF_IDX = L::OFF_IDX;
+    constexpr int OFF_PT = L::OFF_PT, OFF_RED = L::OFF_RED, OFF_REDL = L::OFF_REDL;
+    constexpr int OFF_FLAG = L::OFF_FLAG, OFF_IDX = L::OFF_IDX;
     constexpr int OFF_SEEN = L::OFF_SEEN, OFF_BAR = L::OFF_BAR, OFF_TMEM = off_tmem<DH>();
     const int nh = (HQ == NP) ? P.nh : HQ;
     const size_t q_stride = (HQ == NP) ? (size_t)P.q_stride : (size_t)HQ * DH;
@@ -300,8 +299,7 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (sbase - smem_u32(smem_raw));
     float* red = reinterpret_cast<float*>(gbase + OFF_RED);
-    float* mref = reinterpret_cast<float*>(gbase + OFF_MREF);
-    float* fac = reinterpret_cast<float*>(gbase + OFF_FAC);
+    float* redl = reinterpret_cast<float*>(gbase + OFF_REDL);
     volatile int* flags = reinterpret_cast<volatile int*>(gbase + OFF_FLAG);
     const uint32_t bars = sbase + OFF_BAR;
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(gbase + OFF_TMEM);
@@ -513,12 +511,16 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
         }
     } else if (warp < KEY_WARP0 + 4) {
         // ------------------------------------------------------------ key warps
+        // Each thread keeps every head's reference max in registers: after a
+        // vote fires, the warps' partial maxima go through shared memory and
+        // one barrier, and every thread derives the same new references.
         const int wq = warp & 3;
         const int k = wq * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
         const float sl2 = P.scale_log2;
         uint32_t g = 0;
         uint32_t gphase = 0;
+        int rpar = 0;   // parity of the non-empty rows handled (row-sum slot)
         bool ok = true;
         for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
             const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
@@ -529,13 +531,12 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
                     reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
                 continue;
             }
-            if (k < NP) mref[k] = -INFINITY;
-            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            float lpart[NP];
+            float mr[HQ], lpart[HQ];
 #pragma unroll
-            for (int c = 0; c < NP; ++c) lpart[c] = 0.f;
+            for (int c = 0; c < HQ; ++c) {
+                mr[c] = -INFINITY;
+                lpart[c] = 0.f;
+            }
             for (int t = 0; t < nt; ++t, ++g) {
                 const int b = g & 1;
                 bool masked;
@@ -560,18 +561,26 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
 #pragma unroll
                     for (int c = 0; c < NP; ++c) s[c] = masked ? -INFINITY : __uint_as_float(r[c]) * sl2;
                 }
-                bool exceed = false;
+                // A row's first tile always takes the exact max (its references
+                // are -inf); later tiles only when a score crosses its reference.
+                bool any = t == 0;
+                if (!any) {
+                    bool exceed = false;
 #pragma unroll
-                for (int c = 0; c < HQ; ++c)
-                    if (c < nh) exceed |= s[c] > mref[c] + RESCALE_THRESHOLD;
-                const unsigned vote = __ballot_sync(0xffffffffu, exceed);
-                volatile int* fl = flags + (g & 1) * 4;
-                if (lane == 0) fl[wq] = vote != 0;
-                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                const bool any = fl[0] | fl[1] | fl[2] | fl[3];
+                    for (int c = 0; c < HQ; ++c)
+                        if (c < nh) exceed |= s[c] > mr[c] + RESCALE_THRESHOLD;
+                    const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                    volatile int* fl = flags + (g & 1) * 4;
+                    if (lane == 0) fl[wq] = vote != 0;
+                    ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    any = fl[0] | fl[1] | fl[2] | fl[3];
+                }
                 if (any) {
+                    // The tile's max per head: warp maxima -> red (its slot of
+                    // this tile parity) -> one barrier -> every thread.
+                    float* rd = red + (g & 1) * (4 * NP);
 #pragma unroll
                     for (int c = 0; c < HQ; ++c) {
                         if (c >= nh) break;
@@ -579,27 +588,26 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
                             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                        if (lane == 0) red[wq * NP + c] = m;
+                        if (lane == 0) rd[wq * NP + c] = m;
                     }
                     ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    if (k < nh) {
-                        const int c = k;
-                        const float tmax = fmaxf(fmaxf(red[c], red[NP + c]),
-                                                 fmaxf(red[2 * NP + c], red[3 * NP + c]));
-                        const float old = mref[c];
-                        float f = 1.0f;
-                        if (tmax > old + RESCALE_THRESHOLD) {
-                            f = (old == -INFINITY) ? 0.f : ex2(old - tmax);
-                            mref[c] = tmax;
+                    float f[HQ];
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) {
+                        f[c] = 1.0f;
+                        if (c < nh) {
+                            const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
+                                                     fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
+                            if (tmax > mr[c] + RESCALE_THRESHOLD) {
+                                f[c] = (mr[c] == -INFINITY) ? 0.f : ex2(mr[c] - tmax);
+                                mr[c] = tmax;
+                            }
                         }
-                        fac[c] = f;
                     }
-                    ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
                     if (t > 0) {
+                        // O^T must hold every earlier P.V of the row before it is rescaled.
                         const uint32_t x = g - 1;
                         ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
                         ok = __all_sync(0xffffffffu, ok);
@@ -612,13 +620,13 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
                             tmem_ld_wait<NP>(r);
 #pragma unroll
                             for (int c = 0; c < HQ; ++c)
-                                r[c] = __float_as_uint(__uint_as_float(r[c]) * fac[c]);
+                                r[c] = __float_as_uint(__uint_as_float(r[c]) * f[c]);
                             tmem_st16(t_lane + O_COL + h * NP, r);
                         }
                         tmem_st_wait();
                     }
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) lpart[c] *= fac[c];
+                    for (int c = 0; c < HQ; ++c) lpart[c] *= f[c];
                 }
                 ok = mbar_wait(bar(B_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
@@ -628,10 +636,10 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
 #pragma unroll
                 for (int c = 0; c < NP; ++c) {
                     float p = 0.f;
-                    if (c < nh) {
-                        const float m = mref[c];
+                    if (c < HQ && c < nh) {
+                        const float m = mr[c < HQ ? c : 0];
                         p = ex2(s[c] - (m == -INFINITY ? 0.f : m));
-                        lpart[c] += p;
+                        lpart[c < HQ ? c : 0] += p;
                     }
                     const uint32_t off = kc * (NP * 128) + sw128(c, kin >> 3) + (kin & 7) * 2;
                     *reinterpret_cast<__half*>(pt + off) = __float2half_rn(p);
@@ -646,13 +654,18 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            // Row sums: warp sums -> redl (its slot of this row parity) -> one
+            // barrier.  The next write to the same slot comes two rows later,
+            // behind barriers every thread passes after its reads here.
+            float* rl = redl + rpar * (4 * NP);
+            rpar ^= 1;
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
                 if (c >= nh) break;
                 float v = lpart[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) red[wq * NP + c] = v;
+                if (lane == 0) rl[wq * NP + c] = v;
             }
             ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
@@ -660,7 +673,7 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
             float inv[HQ];
 #pragma unroll
             for (int c = 0; c < HQ; ++c) {
-                const float l = (red[c] + red[NP + c]) + (red[2 * NP + c] + red[3 * NP + c]);
+                const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
                 inv[c] = l > 0.f ? 1.0f / l : 0.f;
             }
 #pragma unroll
@@ -675,10 +688,6 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
                         P.out[(size_t)i * q_stride + c * DH + d] =
                             __float2half_rn(__uint_as_float(r[c]) * inv[c]);
             }
-            // red / mref are rewritten by the next row only after this barrier.
-            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
         }
     }
 
