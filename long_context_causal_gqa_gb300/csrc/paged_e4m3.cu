@@ -61,6 +61,7 @@
 #include <stdint.h>
 #include <type_traits>
 
+#include "e4m3_umma.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -75,8 +76,6 @@ __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; 
 constexpr float RESCALE_THRESHOLD = 8.0f;
 // A moved reference sits this far below the tile's max (log2 units).
 constexpr float REF_SHIFT = 6.0f;
-// Ratio between consecutive terms of the three-term E4M3 expansions.
-constexpr float XRATIO = 32.0f;
 
 struct Params {
     const uint8_t* kcache;
@@ -173,44 +172,6 @@ static_assert(NUM_BARRIERS <= 40, "mbarrier slots");
 __device__ __forceinline__ int item_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int item_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
-// FP8 UMMA: D (+)= A . B with E4M3 operands from shared memory, f32 accumulator.
-__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Two floats -> two E4M3 bytes (round to nearest even, saturating), low byte = a.
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
-    return r;
-}
-// Value of an E4M3 byte pair (low byte first) as two floats.
-__device__ __forceinline__ void e4m3x2_val(uint32_t v, float& a, float& b) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
-    const __half2 hh = *reinterpret_cast<const __half2*>(&h2);
-    a = __low2float(hh);
-    b = __high2float(hh);
-}
-// x ~= t1 + t2 / 32 + t3 / 1024 with t1, t2, t3 E4M3, for two values at
-// once, |x| <= 256 (each result holds the pair's two bytes in its low 16 bits).
-__device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& t1, uint32_t& t2,
-                                              uint32_t& t3) {
-    float a0, a1;
-    t1 = e4m3x2(x0, x1);
-    e4m3x2_val(t1, a0, a1);
-    const float r0 = (x0 - a0) * XRATIO, r1 = (x1 - a1) * XRATIO;
-    t2 = e4m3x2(r0, r1);
-    e4m3x2_val(t2, a0, a1);
-    t3 = e4m3x2((r0 - a0) * XRATIO, (r1 - a1) * XRATIO);
-}
-
 // Byte offset of 16-byte unit u (0..7) of row r inside a 128B-swizzled block.
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t u) {
     return r * 128u + ((u ^ (r & 7u)) << 4);
@@ -232,56 +193,6 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volati
     const bool ok = mbar_wait(bar, phase, abort, err);
     phase ^= 1u;
     return ok;
-}
-
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-                   "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-// N consecutive columns (N a multiple of 4, at most 32) of this thread's TMEM lane.
-template <int N>
-__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t* r) {
-    static_assert(N % 4 == 0 && N > 0 && N <= 32, "column count");
-    if constexpr (N >= 16) {
-        tmem_ld16(taddr, r);
-        if constexpr (N > 16) tmem_ldn<N - 16>(taddr + 16, r + 16);
-    } else if constexpr (N >= 8) {
-        tmem_ld8(taddr, r);
-        if constexpr (N > 8) tmem_ldn<N - 8>(taddr + 8, r + 8);
-    } else {
-        tmem_ld4(taddr, r);
-    }
-}
-template <int N>
-__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t* r) {
-    static_assert(N % 4 == 0 && N > 0 && N <= 32, "column count");
-    if constexpr (N >= 16) {
-        tmem_st16(taddr, r);
-        if constexpr (N > 16) tmem_stn<N - 16>(taddr + 16, r + 16);
-    } else if constexpr (N >= 8) {
-        tmem_st8(taddr, r);
-        if constexpr (N > 8) tmem_stn<N - 8>(taddr + 8, r + 8);
-    } else {
-        tmem_st4(taddr, r);
-    }
 }
 
 // Which sequence, and which of its splits, CTA `split` works on.  With one
@@ -752,9 +663,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     }
 #pragma unroll
                     for (int c = 0; c < NH; ++c)
-                        s[c] = fmaf(__uint_as_float(r3[c]), 1.0f / (XRATIO * XRATIO),
-                                    fmaf(__uint_as_float(r2[c]), 1.0f / XRATIO,
-                                         __uint_as_float(r1[c]))) *
+                        s[c] = combine3(r1[c], r2[c], r3[c]) *
                                (kSl2InRegs ? sl2[kSl2InRegs ? c : 0] : sl2k * qs[c0 + c]);
                 }
                 const int key = (t_begin + jj) * TILE + k;
@@ -916,9 +825,7 @@ paged_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     for (int c = 0; c < NH; ++c)
                         if (c0 + c < P.nq)
                             P.ws_o[((size_t)split * P.nq + c0 + c) * DH + d] =
-                                fmaf(__uint_as_float(r3[c]), 1.0f / (XRATIO * XRATIO),
-                                     fmaf(__uint_as_float(r2[c]), 1.0f / XRATIO,
-                                          __uint_as_float(r1[c])));
+                                combine3(r1[c], r2[c], r3[c]);
                 }
             }
             if (ntl == 0 && k < NH && c0 + k < P.nq) {
