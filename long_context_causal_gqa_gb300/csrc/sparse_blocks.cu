@@ -121,7 +121,7 @@ struct SL {
 enum {
     B_KFULL = 0,
     B_KEMPTY = 1,
-    B_VFULL = 2,   // [2] (one slot with an E4M3 cache)
+    B_VFULL = 2,   // [2]
     B_VEMPTY = 4,  // [2]
     B_QFULL = 6,   // [2]
     B_QEMPTY = 8,  // [2]
