@@ -177,6 +177,10 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 }
 
 __device__ __forceinline__ int row_tiles(int cnt) { return (cnt * BLK + TILE - 1) / TILE; }
+// Selected blocks of row i, clamped to [0, max_sel]; 0 past the last row.
+__device__ __forceinline__ int sel_count(const Params& P, int i) {
+    return i < P.rows ? min(max(__ldg(P.sel_cnt + i), 0), P.max_sel) : 0;
+}
 
 // ------------------------------------------------------------ token index warp
 // (both kernels).  idx: the ring of NI slots of TILE token rows; seen: the
@@ -264,6 +268,66 @@ __device__ __forceinline__ void index_warp(const Params& P, int* idx, uint32_t* 
             __syncwarp();   // the set's bits are read by every lane in the next tile
             mbar_arrive(ifull + 8u * slot);
         }
+    }
+}
+
+// Token-index warp for units of two rows (PAIR; every row selects at most 16
+// blocks): lanes 0 .. 15 resolve row 2u's positions 0 .. 15 (keys 0 .. 63 of
+// the unit's one tile), lanes 16 .. 31 row 2u + 1's (keys 64 .. 127).  A row's
+// whole selection is in this tile, so a repeat is found among the lanes of
+// its half alone and no bitmap is needed.
+__device__ __forceinline__ void index_warp_pairs(const Params& P, int* idx, uint32_t ifull,
+                                                 uint32_t iempty, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4, li = lane & 15;
+    const int lp = P.log2_page, pmask = (1 << P.log2_page) - 1;
+    const int nu = (P.rows + 1) / 2;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nu && ok; u += P.G) {
+        const int i = 2 * u + half;            // this half's row (i = rows: none)
+        const int cnt = sel_count(P, i);
+        if (!__any_sync(0xffffffffu, cnt > 0)) continue;   // the unit has no tile
+        const int slot = (int)(g % NI);
+        if (!mbar_wait(iempty + 8u * slot, ((g / NI) & 1) ^ 1, abort_flag, P.err)) {
+            ok = false;
+            break;
+        }
+        const int p = P.ctx_len - P.rows + i;
+        const int own = p / BLK;                   // the row's own block
+        int b = -1;
+        bool valid = false;
+        if (li < cnt) {
+            b = __ldg(P.sel_idx + (size_t)i * P.max_sel + li);
+            valid = b >= 0 && b <= own;
+        }
+        const unsigned bad = __ballot_sync(0xffffffffu, li < cnt && !valid);
+        if (bad && lane == 0) atomicOr(P.err, kErrBadBlockId);
+        // A repeat: a lower lane of the same row holds the same id.
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        bool dup = false;
+        if (valid) {
+            const unsigned same = __match_any_sync(vmask, (b << 1) | half);
+            dup = (same & ((1u << lane) - 1u)) != 0u;
+        }
+        if (__ballot_sync(0xffffffffu, dup) && lane == 0) atomicOr(P.err, kErrDupBlockId);
+        const bool use = valid && !dup;
+        const int tok0 = b * BLK;
+        int pg = use ? __ldg(P.table + (tok0 >> lp)) : 0;   // a block never straddles a page
+        if (use && (pg < 0 || pg >= P.num_pages)) {
+            atomicOr(P.err, kErrBadPageId);
+            pg = 0;
+        }
+        const int r0 = (pg << lp) + (tok0 & pmask);
+        int4 r;
+        r.x = (use && tok0 + 0 <= p) ? r0 + 0 : -1;
+        r.y = (use && tok0 + 1 <= p) ? r0 + 1 : -1;
+        r.z = (use && tok0 + 2 <= p) ? r0 + 2 : -1;
+        r.w = (use && tok0 + 3 <= p) ? r0 + 3 : -1;
+        reinterpret_cast<int4*>(idx + slot * TILE)[lane] = r;
+        __syncwarp();
+        mbar_arrive(ifull + 8u * slot);
+        ++g;
     }
 }
 
@@ -726,12 +790,26 @@ constexpr float REF_SHIFT = 6.0f;
 constexpr int F8_QWARPS = 2;
 constexpr int F8_NKB = 2, F8_NVB = 2;   // K / V tile buffers
 constexpr int F8_NQB = 2;               // Q expansion buffers
-// Rows per expansion term (the heads of the launch, padded to 8) and the UMMA
-// N: three terms, rounded up to the N granule of 16.
-template <int HQ>
-constexpr int f8_ts() { return HQ == NP ? NP : 8; }
-template <int HQ>
-constexpr int f8_n() { return (3 * f8_ts<HQ>() + 15) / 16 * 16; }
+// Rows per expansion term (the heads of the launch, padded to 8; with PAIR
+// the heads of two rows, 8 columns each) and the UMMA N: three terms, rounded
+// up to the N granule of 16.
+template <int HQ, bool PAIR>
+constexpr int f8_ts() { return (HQ == NP || PAIR) ? NP : 8; }
+template <int HQ, bool PAIR>
+constexpr int f8_n() { return (3 * f8_ts<HQ, PAIR>() + 15) / 16 * 16; }
+// Work units.  Without PAIR a unit is one row.  With PAIR (every row selects
+// at most 16 blocks, i.e. 64 keys) unit u is rows 2u and 2u + 1 sharing one
+// tile: row 2u's keys are keys 0 .. 63 and its heads columns 0 .. 7 of S^T /
+// O^T, row 2u + 1's keys 64 .. 127 and columns 8 .. 15; a score of one row's
+// head against the other row's key is masked.  Half as many tiles, each
+// full, where a row alone would fill half of one.
+template <bool PAIR>
+__device__ __forceinline__ int num_units(const Params& P) { return PAIR ? (P.rows + 1) / 2 : P.rows; }
+template <bool PAIR>
+__device__ __forceinline__ int unit_tiles(const Params& P, int u) {
+    if (!PAIR) return row_tiles(sel_count(P, u));
+    return (sel_count(P, 2 * u) > 0 || sel_count(P, 2 * u + 1) > 0) ? 1 : 0;
+}
 // Half the bytes of the fp16 rows: eight gather warps move a tile's codes in
 // about the time sixteen take for fp16.
 template <int HQ, int DH>
@@ -756,10 +834,10 @@ enum {
 };
 static_assert(F8_NKB <= 2 && F8_NVB <= 3 && F8_NQB <= 3, "barrier slots");
 // smem layout (offsets from a 1024-aligned base)
-template <int HQ, int DH>
+template <int HQ, int DH, bool PAIR>
 struct SL8 {
-    static constexpr int TS = f8_ts<HQ>();
-    static constexpr int N3 = f8_n<HQ>();
+    static constexpr int TS = f8_ts<HQ, PAIR>();
+    static constexpr int N3 = f8_n<HQ, PAIR>();
     static constexpr int RAW_TILE = TILE * DH;                     // 32 / 16 KB of codes
     static constexpr int OFF_K = 0;                                // [F8_NKB][DH / 128][TILE][128]
     static constexpr int OFF_V = OFF_K + F8_NKB * RAW_TILE;        // [F8_NVB][DH / 128][TILE][128]
@@ -784,9 +862,11 @@ struct SL8 {
 };
 constexpr uint32_t F8_TMEM_COLS = 256;
 
-template <int HQ, int DH>
+template <int HQ, int DH, bool PAIR>
 __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(const Params P) {
-    using L = SL8<HQ, DH>;
+    static_assert(!PAIR || HQ <= 8, "two rows' heads in 16 columns");
+    using L = SL8<HQ, DH, PAIR>;
+    const int NU = num_units<PAIR>(P);
     constexpr int HALVES = DH / 128;
     constexpr int TS = L::TS, N3 = L::N3, RAW_TILE = L::RAW_TILE;
     constexpr int NGW = f8_gather_warps<HQ, DH>();
@@ -871,8 +951,8 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
         const uint8_t* cache = kg ? P.kcache8 : P.vcache8;
         uint32_t g = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-            const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+        for (int u = blockIdx.x; u < NU && ok; u += P.G) {
+            const int nt = unit_tiles<PAIR>(P, u);
             for (int t = 0; t < nt && ok; ++t, ++g) {
                 const int slot = (int)(g % NI);
                 if (!mbar_wait(bar(F_IFULL + slot), (g / NI) & 1, abort_flag, P.err)) {
@@ -947,8 +1027,8 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
             };
             uint32_t g = 0;
             int rloc = 0;
-            for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-                const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+            for (int u = blockIdx.x; u < NU && ok; u += P.G) {
+                const int nt = unit_tiles<PAIR>(P, u);
                 if (nt == 0) continue;
                 const int qb = rloc % F8_NQB;
                 if (!mbar_wait(bar(F_QFULL + qb), (rloc / F8_NQB) & 1, abort_flag, P.err)) {
@@ -1006,28 +1086,27 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
         uint32_t gphase = 0;
         int rloc = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-            const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
-            if (nt == 0) {
-                // Nothing selected: the row's output is zero.
-                for (int u = k; u < nh * (DH / 8); u += 128)
-                    reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
-                continue;
-            }
-            const int qb = rloc % F8_NQB;
-            ok = mbar_wait(bar(F_QFULL + qb), (rloc / F8_NQB) & 1, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ++rloc;
-            // Score scale per head (log2 units): scale * kscale * the head's Q scale.
-            float sl2[HQ], mr[HQ], lpart[HQ];
+        if constexpr (PAIR) {
+            // Units of two rows, one tile each: S^T column c is head c & 7 of
+            // row 2u + (c >> 3); key k belongs to row 2u + (k >> 6).
+            for (int u = blockIdx.x; u < NU && ok; u += P.G) {
+                const int i0 = 2 * u;
+                if (unit_tiles<PAIR>(P, u) == 0) {
+                    // Nothing selected in either row: both outputs are zero.
+                    for (int sr = 0; sr < 2 && i0 + sr < P.rows; ++sr)
+                        for (int v = k; v < HQ * (DH / 8); v += 128)
+                            reinterpret_cast<uint4*>(P.out + (size_t)(i0 + sr) * q_stride)[v] =
+                                make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                const int qb = rloc % F8_NQB;
+                ok = mbar_wait(bar(F_QFULL + qb), (rloc / F8_NQB) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++rloc;
+                float sl2[NP];
 #pragma unroll
-            for (int c = 0; c < HQ; ++c) {
-                sl2[c] = c < nh ? sl2k * qs[qb * NP + c] : 0.f;
-                mr[c] = -INFINITY;
-                lpart[c] = 0.f;
-            }
-            for (int t = 0; t < nt; ++t, ++g) {
+                for (int c = 0; c < NP; ++c) sl2[c] = (c & 7) < HQ ? sl2k * qs[qb * NP + c] : 0.f;
                 const int b = g & 1;
                 bool masked;
                 {
@@ -1043,7 +1122,8 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                float s[HQ];
+                const int kr = k >> 6;   // the unit's row this key belongs to
+                float s[NP];
                 {
                     uint32_t r1[TS], r2[TS], r3[TS];
                     const uint32_t sc = t_lane + L::S_COL + b * N3;
@@ -1054,95 +1134,46 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                     tmem_ld_wait<TS>(r2);
                     tmem_ld_wait<TS>(r3);
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c)
-                        s[c] = masked ? -INFINITY : combine3(r1[c], r2[c], r3[c]) * sl2[c];
+                    for (int c = 0; c < NP; ++c)
+                        s[c] = (masked || (c >> 3) != kr || (c & 7) >= HQ)
+                                   ? -INFINITY
+                                   : combine3(r1[c], r2[c], r3[c]) * sl2[c];
                 }
-                // A row's first tile always takes the exact max (its references
-                // are -inf); later tiles only when a score crosses its reference.
-                bool any = t == 0;
-                if (!any) {
-                    bool exceed = false;
+                // The unit's one tile: each column's exact max, the reference
+                // REF_SHIFT below it.
+                float* rd = red + (g & 1) * (4 * NP);
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c)
-                        if (c < nh) exceed |= s[c] > mr[c] + RESCALE_THRESHOLD;
-                    const unsigned vote = __ballot_sync(0xffffffffu, exceed);
-                    volatile int* fl = flags + (g & 1) * 4;
-                    if (lane == 0) fl[wq] = vote != 0;
-                    ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    any = fl[0] | fl[1] | fl[2] | fl[3];
+                for (int c = 0; c < NP; ++c) {
+                    if ((c & 7) >= HQ) continue;
+                    float m = s[c];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0) rd[wq * NP + c] = m;
                 }
-                if (any) {
-                    // The tile's max per head: warp maxima -> red (its slot of
-                    // this tile parity) -> one barrier -> every thread.
-                    float* rd = red + (g & 1) * (4 * NP);
+                ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                float mr[NP];
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) {
-                        if (c >= nh) break;
-                        float m = s[c];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1)
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                        if (lane == 0) rd[wq * NP + c] = m;
-                    }
-                    ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    float f[HQ];
-#pragma unroll
-                    for (int c = 0; c < HQ; ++c) {
-                        f[c] = 1.0f;
-                        if (c < nh) {
-                            const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
-                                                     fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
-                            if (tmax > mr[c] + RESCALE_THRESHOLD) {
-                                const float ref = tmax - REF_SHIFT;
-                                f[c] = (mr[c] == -INFINITY) ? 0.f : ex2(mr[c] - ref);
-                                mr[c] = ref;
-                            }
-                        }
-                    }
-                    if (t > 0) {
-                        // O^T must hold every earlier P.V of the row before it is rescaled.
-                        const uint32_t x = g - 1;
-                        ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int g6 = 0; g6 < 3 * HALVES; ++g6) {   // (d half, expansion term)
-                            const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * TS;
-                            uint32_t r[TS];
-                            tmem_ldn<TS>(t_lane + col, r);
-                            tmem_ld_wait<TS>(r);
-#pragma unroll
-                            for (int c = 0; c < HQ; ++c)
-                                r[c] = __float_as_uint(__uint_as_float(r[c]) * f[c]);
-                            tmem_stn<TS>(t_lane + col, r);
-                        }
-                        tmem_st_wait();
-                    }
-#pragma unroll
-                    for (int c = 0; c < HQ; ++c) lpart[c] *= f[c];
+                for (int c = 0; c < NP; ++c) {
+                    const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]), fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
+                    mr[c] = ((c & 7) >= HQ || tmax == -INFINITY) ? 0.f : tmax - REF_SHIFT;
                 }
                 // P^T buffer b is free once the P.V two tiles back has completed.
                 ok = mbar_wait(bar(F_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+                float pl[NP];
                 {
-                    // [P1 | P2 | P3]^T, K-major: row = term * TS + head, byte = key.
                     uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
 #pragma unroll
-                    for (int c = 0; c < HQ; c += 2) {
-                        if (c >= nh) break;
-                        const float p0 = ex2(s[c] - (mr[c] == -INFINITY ? 0.f : mr[c]));
-                        const float p1 = c + 1 < nh ? ex2(s[c + 1] - (mr[c + 1] == -INFINITY ? 0.f : mr[c + 1]))
-                                                    : 0.f;
-                        lpart[c] += p0;
-                        lpart[c + 1] += p1;
+                    for (int c = 0; c < NP; c += 2) {
+                        pl[c] = pl[c + 1] = 0.f;
+                        if ((c & 7) >= HQ) continue;
+                        pl[c] = ex2(s[c] - mr[c]);
+                        pl[c + 1] = (c & 7) + 1 < HQ ? ex2(s[c + 1] - mr[c + 1]) : 0.f;
                         uint32_t t3[3];
-                        split3_e4m3x2(p0, p1, t3[0], t3[1], t3[2]);
+                        split3_e4m3x2(pl[c], pl[c + 1], t3[0], t3[1], t3[2]);
 #pragma unroll
                         for (int e = 0; e < 3; ++e) {
                             pt[pofs(e * TS + c)] = (uint8_t)(t3[e] & 0xFF);
@@ -1152,84 +1183,299 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
                 }
                 fence_async_shared();
                 mbar_arrive(bar(F_PREADY + b));
+                // Row sums per column (this tile is the unit's only one), while
+                // the P.V runs: warp sums -> redl (slot of this unit's parity).
+                float* rl = redl + (rloc & 1) * (4 * NP);
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    if ((c & 7) >= HQ) continue;
+                    float v = pl[c];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) rl[wq * NP + c] = v;
+                }
+                // ---------------------------------------------------------- unit epilogue
+                const uint32_t x = g++;
+                ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                // Every thread has read the unit's Q scales: the buffer may be refilled.
+                if (k == 0) mbar_arrive(bar(F_QEMPTY + qb));
+                float inv[NP];
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
+                    inv[c] = ((c & 7) < HQ && l > 0.f) ? vsc / l : 0.f;
+                }
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    uint32_t r1[TS], r2[TS], r3[TS];
+                    const uint32_t oc = t_lane + L::O_COL + h * N3;
+                    tmem_ldn<TS>(oc, r1);
+                    tmem_ldn<TS>(oc + TS, r2);
+                    tmem_ldn<TS>(oc + 2 * TS, r3);
+                    tmem_ld_wait<TS>(r1);
+                    tmem_ld_wait<TS>(r2);
+                    tmem_ld_wait<TS>(r3);
+                    const int d = h * 128 + k;
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) {
+                        const int row = i0 + (c >> 3);
+                        if ((c & 7) < HQ && row < P.rows)
+                            P.out[(size_t)row * q_stride + (c & 7) * DH + d] =
+                                __float2half_rn(combine3(r1[c], r2[c], r3[c]) * inv[c]);
+                    }
+                }
             }
-            if (!ok) break;
-            // ---------------------------------------------------------- row epilogue
-            const uint32_t x = g - 1;
-            ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            // Row sums: warp sums -> redl (its slot of this row parity) -> one
-            // barrier.  The next write to the same slot comes two rows later,
-            // behind barriers every thread passes after its reads here.
-            float* rl = redl + (rloc & 1) * (4 * NP);
-#pragma unroll
-            for (int c = 0; c < HQ; ++c) {
-                if (c >= nh) break;
-                float v = lpart[c];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) rl[wq * NP + c] = v;
-            }
-            ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            // Every thread has read this row's Q scales (row start) and passed
-            // the barrier above: the Q buffer may be refilled.
-            if (k == 0) mbar_arrive(bar(F_QEMPTY + qb));
-            float inv[HQ];
-#pragma unroll
-            for (int c = 0; c < HQ; ++c) {
-                const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
-                inv[c] = l > 0.f ? vsc / l : 0.f;
-            }
-#pragma unroll
-            for (int h = 0; h < HALVES; ++h) {
-                uint32_t r1[TS], r2[TS], r3[TS];
-                const uint32_t oc = t_lane + L::O_COL + h * N3;
-                tmem_ldn<TS>(oc, r1);
-                tmem_ldn<TS>(oc + TS, r2);
-                tmem_ldn<TS>(oc + 2 * TS, r3);
-                tmem_ld_wait<TS>(r1);
-                tmem_ld_wait<TS>(r2);
-                tmem_ld_wait<TS>(r3);
-                const int d = h * 128 + k;
-#pragma unroll
-                for (int c = 0; c < HQ; ++c)
-                    if (c < nh)
-                        P.out[(size_t)i * q_stride + c * DH + d] =
-                            __float2half_rn(combine3(r1[c], r2[c], r3[c]) * inv[c]);
+        } else {
+            for (int u = blockIdx.x; u < NU && ok; u += P.G) {
+                const int nt = unit_tiles<PAIR>(P, u);
+                const int i = u;   // the row (without PAIR)
+                if (nt == 0) {
+                    // Nothing selected: the row's output is zero.
+                    for (int u = k; u < nh * (DH / 8); u += 128)
+                        reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                const int qb = rloc % F8_NQB;
+                ok = mbar_wait(bar(F_QFULL + qb), (rloc / F8_NQB) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++rloc;
+                // Score scale per head (log2 units): scale * kscale * the head's Q scale.
+                float sl2[HQ], mr[HQ], lpart[HQ];
+    #pragma unroll
+                for (int c = 0; c < HQ; ++c) {
+                    sl2[c] = c < nh ? sl2k * qs[qb * NP + c] : 0.f;
+                    mr[c] = -INFINITY;
+                    lpart[c] = 0.f;
+                }
+                for (int t = 0; t < nt; ++t, ++g) {
+                    const int b = g & 1;
+                    bool masked;
+                    {
+                        // The index warp's verdict on this key (-1: masked).
+                        const int slot = (int)(g % NI);
+                        ok = mbar_wait(bar(F_IFULL + slot), (g / NI) & 1, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        masked = reinterpret_cast<const int*>(gbase + L::OFF_IDX)[slot * TILE + k] < 0;
+                        mbar_arrive(bar(F_IEMPTY + slot));
+                    }
+                    ok = mbar_wait(bar(F_SFULL + b), (g >> 1) & 1, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    float s[HQ];
+                    {
+                        uint32_t r1[TS], r2[TS], r3[TS];
+                        const uint32_t sc = t_lane + L::S_COL + b * N3;
+                        tmem_ldn<TS>(sc, r1);
+                        tmem_ldn<TS>(sc + TS, r2);
+                        tmem_ldn<TS>(sc + 2 * TS, r3);
+                        tmem_ld_wait<TS>(r1);
+                        tmem_ld_wait<TS>(r2);
+                        tmem_ld_wait<TS>(r3);
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c)
+                            s[c] = masked ? -INFINITY : combine3(r1[c], r2[c], r3[c]) * sl2[c];
+                    }
+                    // A row's first tile always takes the exact max (its references
+                    // are -inf); later tiles only when a score crosses its reference.
+                    bool any = t == 0;
+                    if (!any) {
+                        bool exceed = false;
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c)
+                            if (c < nh) exceed |= s[c] > mr[c] + RESCALE_THRESHOLD;
+                        const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                        volatile int* fl = flags + (g & 1) * 4;
+                        if (lane == 0) fl[wq] = vote != 0;
+                        ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        any = fl[0] | fl[1] | fl[2] | fl[3];
+                    }
+                    if (any) {
+                        // The tile's max per head: warp maxima -> red (its slot of
+                        // this tile parity) -> one barrier -> every thread.
+                        float* rd = red + (g & 1) * (4 * NP);
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c) {
+                            if (c >= nh) break;
+                            float m = s[c];
+    #pragma unroll
+                            for (int o = 16; o > 0; o >>= 1)
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                            if (lane == 0) rd[wq * NP + c] = m;
+                        }
+                        ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        float f[HQ];
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c) {
+                            f[c] = 1.0f;
+                            if (c < nh) {
+                                const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
+                                                         fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
+                                if (tmax > mr[c] + RESCALE_THRESHOLD) {
+                                    const float ref = tmax - REF_SHIFT;
+                                    f[c] = (mr[c] == -INFINITY) ? 0.f : ex2(mr[c] - ref);
+                                    mr[c] = ref;
+                                }
+                            }
+                        }
+                        if (t > 0) {
+                            // O^T must hold every earlier P.V of the row before it is rescaled.
+                            const uint32_t x = g - 1;
+                            ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                            ok = __all_sync(0xffffffffu, ok);
+                            if (!ok) break;
+                            tc_fence_after();
+    #pragma unroll
+                            for (int g6 = 0; g6 < 3 * HALVES; ++g6) {   // (d half, expansion term)
+                                const uint32_t col = L::O_COL + (g6 / 3) * N3 + (g6 % 3) * TS;
+                                uint32_t r[TS];
+                                tmem_ldn<TS>(t_lane + col, r);
+                                tmem_ld_wait<TS>(r);
+    #pragma unroll
+                                for (int c = 0; c < HQ; ++c)
+                                    r[c] = __float_as_uint(__uint_as_float(r[c]) * f[c]);
+                                tmem_stn<TS>(t_lane + col, r);
+                            }
+                            tmem_st_wait();
+                        }
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c) lpart[c] *= f[c];
+                    }
+                    // P^T buffer b is free once the P.V two tiles back has completed.
+                    ok = mbar_wait(bar(F_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    {
+                        // [P1 | P2 | P3]^T, K-major: row = term * TS + head, byte = key.
+                        uint8_t* pt = gbase + L::OFF_PT + b * L::PT_BYTES;
+    #pragma unroll
+                        for (int c = 0; c < HQ; c += 2) {
+                            if (c >= nh) break;
+                            const float p0 = ex2(s[c] - (mr[c] == -INFINITY ? 0.f : mr[c]));
+                            const float p1 = c + 1 < nh ? ex2(s[c + 1] - (mr[c + 1] == -INFINITY ? 0.f : mr[c + 1]))
+                                                        : 0.f;
+                            lpart[c] += p0;
+                            lpart[c + 1] += p1;
+                            uint32_t t3[3];
+                            split3_e4m3x2(p0, p1, t3[0], t3[1], t3[2]);
+    #pragma unroll
+                            for (int e = 0; e < 3; ++e) {
+                                pt[pofs(e * TS + c)] = (uint8_t)(t3[e] & 0xFF);
+                                pt[pofs(e * TS + c + 1)] = (uint8_t)(t3[e] >> 8);
+                            }
+                        }
+                    }
+                    fence_async_shared();
+                    mbar_arrive(bar(F_PREADY + b));
+                }
+                if (!ok) break;
+                // ---------------------------------------------------------- row epilogue
+                const uint32_t x = g - 1;
+                ok = mbar_wait(bar(F_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                // Row sums: warp sums -> redl (its slot of this row parity) -> one
+                // barrier.  The next write to the same slot comes two rows later,
+                // behind barriers every thread passes after its reads here.
+                float* rl = redl + (rloc & 1) * (4 * NP);
+    #pragma unroll
+                for (int c = 0; c < HQ; ++c) {
+                    if (c >= nh) break;
+                    float v = lpart[c];
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) rl[wq * NP + c] = v;
+                }
+                ok = group_sync(bar(F_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                // Every thread has read this row's Q scales (row start) and passed
+                // the barrier above: the Q buffer may be refilled.
+                if (k == 0) mbar_arrive(bar(F_QEMPTY + qb));
+                float inv[HQ];
+    #pragma unroll
+                for (int c = 0; c < HQ; ++c) {
+                    const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
+                    inv[c] = l > 0.f ? vsc / l : 0.f;
+                }
+    #pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    uint32_t r1[TS], r2[TS], r3[TS];
+                    const uint32_t oc = t_lane + L::O_COL + h * N3;
+                    tmem_ldn<TS>(oc, r1);
+                    tmem_ldn<TS>(oc + TS, r2);
+                    tmem_ldn<TS>(oc + 2 * TS, r3);
+                    tmem_ld_wait<TS>(r1);
+                    tmem_ld_wait<TS>(r2);
+                    tmem_ld_wait<TS>(r3);
+                    const int d = h * 128 + k;
+    #pragma unroll
+                    for (int c = 0; c < HQ; ++c)
+                        if (c < nh)
+                            P.out[(size_t)i * q_stride + c * DH + d] =
+                                __float2half_rn(combine3(r1[c], r2[c], r3[c]) * inv[c]);
+                }
             }
         }
     } else if (warp == IDX_WARP) {
-        index_warp(P, reinterpret_cast<int*>(gbase + L::OFF_IDX),
-                   reinterpret_cast<uint32_t*>(gbase + L::OFF_SEEN), bar(F_IFULL), bar(F_IEMPTY),
-                   abort_flag);
+        if constexpr (PAIR)
+            index_warp_pairs(P, reinterpret_cast<int*>(gbase + L::OFF_IDX), bar(F_IFULL),
+                             bar(F_IEMPTY), abort_flag);
+        else
+            index_warp(P, reinterpret_cast<int*>(gbase + L::OFF_IDX),
+                       reinterpret_cast<uint32_t*>(gbase + L::OFF_SEEN), bar(F_IFULL),
+                       bar(F_IEMPTY), abort_flag);
     } else {
         // ------------------------------------------------------------ Q expansion
-        // Warp qw takes heads qw, qw + F8_QWARPS, ...: each lane loads EPL
-        // values of a head's row (all of the row's loads issued before the
-        // wait for the buffer), the head's scale is its absolute max / 256, and
-        // the three E4M3 terms of x / scale go to rows head, TS + head and
-        // 2 TS + head of the K-major, 128B-swizzled expansion.
+        // A unit's head rows (its row's heads, or with PAIR both rows' heads,
+        // entry e = row * HQ + head) are dealt to the warps: warp qw takes
+        // entries qw, qw + F8_QWARPS, ...  Each lane loads EPL values of an
+        // entry's head row (all of the unit's loads issued before the wait
+        // for the buffer), the head's scale is its absolute max / 256, and the
+        // three E4M3 terms of x / scale go to rows col, TS + col and 2 TS + col
+        // of the K-major, 128B-swizzled expansion (col: the head's S^T column).
         const int qw = warp - Q_WARP0;
-        constexpr int RPW = (HQ + F8_QWARPS - 1) / F8_QWARPS;
+        constexpr int NE_MAX = PAIR ? 2 * HQ : HQ;
+        const int ne = PAIR ? 2 * HQ : nh;
+        constexpr int RPW = (NE_MAX + F8_QWARPS - 1) / F8_QWARPS;
         constexpr int EPL = DH / 32;   // elements of a row per lane: 8 or 4
         using QV = typename std::conditional<EPL == 8, uint4, uint2>::type;
         const int d0 = lane * EPL;
         int rloc = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-            const int nt = row_tiles(min(max(__ldg(P.sel_cnt + i), 0), P.max_sel));
+        for (int u = blockIdx.x; u < NU && ok; u += P.G) {
+            const int nt = unit_tiles<PAIR>(P, u);
             if (nt == 0) continue;
             const int qb = rloc % F8_NQB;
+            // Entry e: row, head and S^T column.
+            auto entry = [&](int e, int& row, int& head, int& col) {
+                const int sr = PAIR ? e / HQ : 0;
+                head = e - sr * HQ;
+                row = PAIR ? 2 * u + sr : u;
+                col = sr * 8 + head;
+            };
             QV raw[RPW];
 #pragma unroll
             for (int j = 0; j < RPW; ++j) {
-                const int c = qw + F8_QWARPS * j;
-                raw[j] = c < nh ? *reinterpret_cast<const QV*>(P.q + (size_t)i * q_stride + c * DH + d0)
-                                : QV{};
+                const int e = qw + F8_QWARPS * j;
+                int row, head, col;
+                entry(e, row, head, col);
+                raw[j] = (e < ne && row < P.rows)
+                             ? *reinterpret_cast<const QV*>(P.q + (size_t)row * q_stride + head * DH + d0)
+                             : QV{};
             }
             ok = mbar_wait(bar(F_QEMPTY + qb), ((rloc / F8_NQB) & 1) ^ 1, abort_flag, P.err);
             ok = __all_sync(0xffffffffu, ok);
@@ -1237,8 +1483,11 @@ __global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(con
             uint8_t* qbuf = gbase + L::OFF_Q + qb * L::Q_BYTES;
 #pragma unroll
             for (int j = 0; j < RPW; ++j) {
-                const int c = qw + F8_QWARPS * j;
-                if (c >= nh) break;
+                const int e = qw + F8_QWARPS * j;
+                if (e >= ne) break;
+                int row, head, c;
+                entry(e, row, head, c);
+                if (row >= P.rows) continue;   // the missing second row of the last unit
                 float x[EPL];
                 const __half* hx = reinterpret_cast<const __half*>(&raw[j]);
 #pragma unroll
@@ -1323,14 +1572,25 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
     KernelFn fn;
     int smem, threads;
     if (e4m3) {
+        // The 6-head family takes two rows per tile when every row's selection
+        // fits half a tile (at most 64 keys); the grid then walks row pairs.
+        const bool pair = six && max_sel * BLK <= TILE / 2;
+        if (pair) {
+            const int units = (rows + 1) / 2;
+            P.G = units < di->num_sms ? units : di->num_sms;
+        }
         if (Dh == 128) {
-            fn = six ? sparse_f8_kernel<kHq, 128> : sparse_f8_kernel<NP, 128>;
+            fn = pair ? sparse_f8_kernel<kHq, 128, true>
+                      : (six ? sparse_f8_kernel<kHq, 128, false> : sparse_f8_kernel<NP, 128, false>);
             threads = six ? f8_nthreads<kHq, 128>() : f8_nthreads<NP, 128>();
-            smem = six ? SL8<kHq, 128>::SMEM : SL8<NP, 128>::SMEM;
+            smem = pair ? SL8<kHq, 128, true>::SMEM
+                        : (six ? SL8<kHq, 128, false>::SMEM : SL8<NP, 128, false>::SMEM);
         } else {
-            fn = six ? sparse_f8_kernel<kHq, 256> : sparse_f8_kernel<NP, 256>;
+            fn = pair ? sparse_f8_kernel<kHq, 256, true>
+                      : (six ? sparse_f8_kernel<kHq, 256, false> : sparse_f8_kernel<NP, 256, false>);
             threads = six ? f8_nthreads<kHq, 256>() : f8_nthreads<NP, 256>();
-            smem = six ? SL8<kHq, 256>::SMEM : SL8<NP, 256>::SMEM;
+            smem = pair ? SL8<kHq, 256, true>::SMEM
+                        : (six ? SL8<kHq, 256, false>::SMEM : SL8<NP, 256, false>::SMEM);
         }
     } else if (Dh == 128) {
         fn = six ? sparse_kernel<kHq, 128> : sparse_kernel<NP, 128>;
