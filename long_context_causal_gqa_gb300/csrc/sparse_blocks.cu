@@ -32,6 +32,11 @@
 //   entering as three-term E4M3 expansions (see e4m3_umma.cuh); the K scale
 //   joins the score scale and the V scale the final 1 / l.
 //
+// * Short selections: when every row selects at most 16 blocks (64 keys, half
+//   a tile), the 6-head kernels take two rows per tile (num_units), their
+//   heads side by side in the 16 columns and cross-row scores masked, so the
+//   per-row chain of softmax, P.V and epilogue is paid once per two rows.
+//
 // * Token index warp: block-table lookups (a selected id, then a page id, two
 //   dependent loads per key) are taken off the gather warps' path: the index warp
 //   resolves each tile's keys to cache token rows ahead of them, through a
@@ -180,6 +185,20 @@ __device__ __forceinline__ int row_tiles(int cnt) { return (cnt * BLK + TILE - 1
 // Selected blocks of row i, clamped to [0, max_sel]; 0 past the last row.
 __device__ __forceinline__ int sel_count(const Params& P, int i) {
     return i < P.rows ? min(max(__ldg(P.sel_cnt + i), 0), P.max_sel) : 0;
+}
+
+// Work units.  Without PAIR a unit is one row.  With PAIR (every row selects
+// at most 16 blocks, i.e. 64 keys) unit u is rows 2u and 2u + 1 sharing one
+// tile: row 2u's keys are keys 0 .. 63 and its heads columns 0 .. 7 of S^T /
+// O^T, row 2u + 1's keys 64 .. 127 and columns 8 .. 15; a score of one row's
+// head against the other row's key is masked.  Half as many tiles, each
+// full, where a row alone would fill half of one.
+template <bool PAIR>
+__device__ __forceinline__ int num_units(const Params& P) { return PAIR ? (P.rows + 1) / 2 : P.rows; }
+template <bool PAIR>
+__device__ __forceinline__ int unit_tiles(const Params& P, int u) {
+    if (!PAIR) return row_tiles(sel_count(P, u));
+    return (sel_count(P, 2 * u) > 0 || sel_count(P, 2 * u + 1) > 0) ? 1 : 0;
 }
 
 // ------------------------------------------------------------ token index warp
@@ -333,10 +352,12 @@ __device__ __forceinline__ void index_warp_pairs(const Params& P, int* idx, uint
 
 // fp16 cache.  HQ: heads per launch known at compile time (6), or NP with the
 // count read from P.nh (any grouping up to 16 query heads per KV head).  DH:
-// head size, 256 or 128.
-template <int HQ, int DH>
+// head size, 256 or 128.  PAIR: units of two rows per tile (see num_units).
+template <int HQ, int DH, bool PAIR>
 __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Params P) {
+    static_assert(!PAIR || HQ <= 8, "two rows' heads in 16 columns");
     using L = SL<DH>;
+    const int NU = num_units<PAIR>(P);
     constexpr int HALVES = DH / 128;   // 128-d halves of a row (one M = 128 P.V each)
     constexpr int KV_TILE_BYTES = L::KV_TILE_BYTES;
     constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, Q_BYTES = L::Q_BYTES, OFF_Q = L::OFF_Q;
@@ -424,23 +445,29 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
         uint32_t g = 0;                     // global tile counter
         int rloc = 0;                       // non-empty rows handled so far
         bool ok = true;
-        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-            const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
-            const int nt = row_tiles(cnt);
+        for (int un = blockIdx.x; un < NU && ok; un += P.G) {
+            const int nt = unit_tiles<PAIR>(P, un);
+            const int i = un;   // the row (without PAIR)
             if (nt == 0) continue;
-            // Q row i (nh heads x DH d) -> Q buffer rloc & 1, rows 0 .. nh - 1,
-            // by the NQLOAD threads that count on QFULL (the first gather warps).
+            // Q row i (nh heads x DH d) -> Q buffer rloc & 1, rows 0 .. nh - 1
+            // (with PAIR rows 2un and 2un + 1, head h of row r at Q row
+            // 8 r + h), by the NQLOAD threads that count on QFULL (the first
+            // gather warps).
             const int qb = rloc & 1;
             if (gt < NQLOAD) {
                 if (!mbar_wait(bar(B_QEMPTY + qb), ((rloc >> 1) & 1) ^ 1, abort_flag, P.err)) {
                     ok = false;
                     break;
                 }
-                for (int u = gt; u < nh * (DH / 8); u += NQLOAD) {
-                    const int h = u / (DH / 8), c16 = u % (DH / 8);
+                const int ne = PAIR ? 2 * HQ : nh;   // head rows to load
+                for (int v = gt; v < ne * (DH / 8); v += NQLOAD) {
+                    const int e = v / (DH / 8), c16 = v % (DH / 8);
+                    const int sr = PAIR ? e / HQ : 0, h = e - sr * HQ;
+                    const int row = PAIR ? 2 * un + sr : i;
+                    if (row >= P.rows) continue;   // the missing second row of the last unit
                     const uint32_t dst = sbase + OFF_Q + qb * Q_BYTES + (c16 / 8) * (NP * 128) +
-                                         sw128(h, c16 % 8);
-                    cp_async16(dst, P.q + (size_t)i * q_stride + h * DH + c16 * 8, 16);
+                                         sw128(sr * 8 + h, c16 % 8);
+                    cp_async16(dst, P.q + (size_t)row * q_stride + h * DH + c16 * 8, 16);
                 }
                 cp_async_arrive(bar(B_QFULL + qb));
             }
@@ -531,9 +558,8 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
                 umma_commit(bar(B_VEMPTY + vb));
                 return true;
             };
-            for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-                const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
-                const int nt = row_tiles(cnt);
+            for (int un = blockIdx.x; un < NU && ok; un += P.G) {
+                const int nt = unit_tiles<PAIR>(P, un);
                 if (nt == 0) continue;
                 const int qb = rloc & 1;
                 if (!mbar_wait(bar(B_QFULL + qb), (rloc >> 1) & 1, abort_flag, P.err)) {
@@ -586,22 +612,19 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
         uint32_t gphase = 0;
         int rpar = 0;   // parity of the non-empty rows handled (row-sum slot)
         bool ok = true;
-        for (int i = blockIdx.x; i < P.rows && ok; i += P.G) {
-            const int cnt = min(max(__ldg(P.sel_cnt + i), 0), P.max_sel);
-            const int nt = row_tiles(cnt);
-            if (nt == 0) {
-                // Nothing selected: the row's output is zero.
-                for (int u = k; u < nh * (DH / 8); u += 128)
-                    reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
-                continue;
-            }
-            float mr[HQ], lpart[HQ];
-#pragma unroll
-            for (int c = 0; c < HQ; ++c) {
-                mr[c] = -INFINITY;
-                lpart[c] = 0.f;
-            }
-            for (int t = 0; t < nt; ++t, ++g) {
+        if constexpr (PAIR) {
+            // Units of two rows, one tile each: S^T column c is head c & 7 of
+            // row 2un + (c >> 3); key k belongs to row 2un + (k >> 6).
+            for (int un = blockIdx.x; un < NU && ok; un += P.G) {
+                const int i0 = 2 * un;
+                if (unit_tiles<PAIR>(P, un) == 0) {
+                    // Nothing selected in either row: both outputs are zero.
+                    for (int sr = 0; sr < 2 && i0 + sr < P.rows; ++sr)
+                        for (int v = k; v < HQ * (DH / 8); v += 128)
+                            reinterpret_cast<uint4*>(P.out + (size_t)(i0 + sr) * q_stride)[v] =
+                                make_uint4(0, 0, 0, 0);
+                    continue;
+                }
                 const int b = g & 1;
                 bool masked;
                 {
@@ -617,148 +640,274 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
+                const int kr = k >> 6;   // the unit's row this key belongs to
                 float s[NP];
                 {
                     uint32_t r[NP];
                     tmem_ld16(t_lane + S_COL + b * NP, r);
                     tmem_ld_wait<NP>(r);
 #pragma unroll
-                    for (int c = 0; c < NP; ++c) s[c] = masked ? -INFINITY : __uint_as_float(r[c]) * sl2;
+                    for (int c = 0; c < NP; ++c)
+                        s[c] = (masked || (c >> 3) != kr || (c & 7) >= HQ) ? -INFINITY
+                                                                           : __uint_as_float(r[c]) * sl2;
                 }
-                // A row's first tile always takes the exact max (its references
-                // are -inf); later tiles only when a score crosses its reference.
-                bool any = t == 0;
-                if (!any) {
-                    bool exceed = false;
+                // The unit's one tile: each column's exact max is its reference.
+                float* rd = red + (g & 1) * (4 * NP);
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c)
-                        if (c < nh) exceed |= s[c] > mr[c] + RESCALE_THRESHOLD;
-                    const unsigned vote = __ballot_sync(0xffffffffu, exceed);
-                    volatile int* fl = flags + (g & 1) * 4;
-                    if (lane == 0) fl[wq] = vote != 0;
-                    ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    any = fl[0] | fl[1] | fl[2] | fl[3];
+                for (int c = 0; c < NP; ++c) {
+                    if ((c & 7) >= HQ) continue;
+                    float m = s[c];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0) rd[wq * NP + c] = m;
                 }
-                if (any) {
-                    // The tile's max per head: warp maxima -> red (its slot of
-                    // this tile parity) -> one barrier -> every thread.
-                    float* rd = red + (g & 1) * (4 * NP);
-#pragma unroll
-                    for (int c = 0; c < HQ; ++c) {
-                        if (c >= nh) break;
-                        float m = s[c];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1)
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                        if (lane == 0) rd[wq * NP + c] = m;
-                    }
-                    ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    float f[HQ];
-#pragma unroll
-                    for (int c = 0; c < HQ; ++c) {
-                        f[c] = 1.0f;
-                        if (c < nh) {
-                            const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
-                                                     fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
-                            if (tmax > mr[c] + RESCALE_THRESHOLD) {
-                                f[c] = (mr[c] == -INFINITY) ? 0.f : ex2(mr[c] - tmax);
-                                mr[c] = tmax;
-                            }
-                        }
-                    }
-                    if (t > 0) {
-                        // O^T must hold every earlier P.V of the row before it is rescaled.
-                        const uint32_t x = g - 1;
-                        ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int h = 0; h < HALVES; ++h) {
-                            uint32_t r[NP];
-                            tmem_ld16(t_lane + O_COL + h * NP, r);
-                            tmem_ld_wait<NP>(r);
-#pragma unroll
-                            for (int c = 0; c < HQ; ++c)
-                                r[c] = __float_as_uint(__uint_as_float(r[c]) * f[c]);
-                            tmem_st16(t_lane + O_COL + h * NP, r);
-                        }
-                        tmem_st_wait();
-                    }
-#pragma unroll
-                    for (int c = 0; c < HQ; ++c) lpart[c] *= f[c];
-                }
+                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                // P^T buffer b is free once the P.V two tiles back has completed.
                 ok = mbar_wait(bar(B_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                uint8_t* pt = gbase + OFF_PT + b * PT_BYTES;
-                const int kc = k >> 6, kin = k & 63;
+                float pl[NP];
+                {
+                    uint8_t* pt = gbase + OFF_PT + b * PT_BYTES;
+                    const int kc = k >> 6, kin = k & 63;
 #pragma unroll
-                for (int c = 0; c < NP; ++c) {
-                    float p = 0.f;
-                    if (c < HQ && c < nh) {
-                        const float m = mr[c < HQ ? c : 0];
-                        p = ex2(s[c] - (m == -INFINITY ? 0.f : m));
-                        lpart[c < HQ ? c : 0] += p;
+                    for (int c = 0; c < NP; ++c) {
+                        pl[c] = 0.f;
+                        if ((c & 7) < HQ) {
+                            const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
+                                                     fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
+                            pl[c] = ex2(s[c] - (tmax == -INFINITY ? 0.f : tmax));
+                        }
+                        const uint32_t off = kc * (NP * 128) + sw128(c, kin >> 3) + (kin & 7) * 2;
+                        *reinterpret_cast<__half*>(pt + off) = __float2half_rn(pl[c]);
                     }
-                    const uint32_t off = kc * (NP * 128) + sw128(c, kin >> 3) + (kin & 7) * 2;
-                    *reinterpret_cast<__half*>(pt + off) = __float2half_rn(p);
                 }
                 fence_async_shared();
                 mbar_arrive(bar(B_PREADY + b));
+                // Row sums per column (this tile is the unit's only one), while
+                // the P.V runs: warp sums -> redl (slot of this unit's parity).
+                float* rl = redl + rpar * (4 * NP);
+                rpar ^= 1;
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    if ((c & 7) >= HQ) continue;
+                    float v = pl[c];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) rl[wq * NP + c] = v;
+                }
+                // ---------------------------------------------------------- unit epilogue
+                const uint32_t x = g++;
+                ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                float inv[NP];
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
+                    inv[c] = ((c & 7) < HQ && l > 0.f) ? 1.0f / l : 0.f;
+                }
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    uint32_t r[NP];
+                    tmem_ld16(t_lane + O_COL + h * NP, r);
+                    tmem_ld_wait<NP>(r);
+                    const int d = h * 128 + k;
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) {
+                        const int row = i0 + (c >> 3);
+                        if ((c & 7) < HQ && row < P.rows)
+                            P.out[(size_t)row * q_stride + (c & 7) * DH + d] =
+                                __float2half_rn(__uint_as_float(r[c]) * inv[c]);
+                    }
+                }
             }
-            if (!ok) break;
-            // ---------------------------------------------------------- row epilogue
-            const uint32_t x = g - 1;
-            ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            // Row sums: warp sums -> redl (its slot of this row parity) -> one
-            // barrier.  The next write to the same slot comes two rows later,
-            // behind barriers every thread passes after its reads here.
-            float* rl = redl + rpar * (4 * NP);
-            rpar ^= 1;
-#pragma unroll
-            for (int c = 0; c < HQ; ++c) {
-                if (c >= nh) break;
-                float v = lpart[c];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) rl[wq * NP + c] = v;
-            }
-            ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            float inv[HQ];
-#pragma unroll
-            for (int c = 0; c < HQ; ++c) {
-                const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
-                inv[c] = l > 0.f ? 1.0f / l : 0.f;
-            }
-#pragma unroll
-            for (int h = 0; h < HALVES; ++h) {
-                uint32_t r[NP];
-                tmem_ld16(t_lane + O_COL + h * NP, r);
-                tmem_ld_wait<NP>(r);
-                const int d = h * 128 + k;
-#pragma unroll
-                for (int c = 0; c < HQ; ++c)
-                    if (c < nh)
-                        P.out[(size_t)i * q_stride + c * DH + d] =
-                            __float2half_rn(__uint_as_float(r[c]) * inv[c]);
+        } else {
+            for (int un = blockIdx.x; un < NU && ok; un += P.G) {
+                const int nt = unit_tiles<PAIR>(P, un);
+                const int i = un;   // the row (without PAIR)
+                if (nt == 0) {
+                    // Nothing selected: the row's output is zero.
+                    for (int u = k; u < nh * (DH / 8); u += 128)
+                        reinterpret_cast<uint4*>(P.out + (size_t)i * q_stride)[u] = make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                float mr[HQ], lpart[HQ];
+    #pragma unroll
+                for (int c = 0; c < HQ; ++c) {
+                    mr[c] = -INFINITY;
+                    lpart[c] = 0.f;
+                }
+                for (int t = 0; t < nt; ++t, ++g) {
+                    const int b = g & 1;
+                    bool masked;
+                    {
+                        // The index warp's verdict on this key (-1: masked).
+                        const int slot = (int)(g % NI);
+                        ok = mbar_wait(bar(B_IFULL + slot), (g / NI) & 1, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        masked = reinterpret_cast<const int*>(gbase + OFF_IDX)[slot * TILE + k] < 0;
+                        mbar_arrive(bar(B_IEMPTY + slot));
+                    }
+                    ok = mbar_wait(bar(B_SFULL + b), (g >> 1) & 1, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    float s[NP];
+                    {
+                        uint32_t r[NP];
+                        tmem_ld16(t_lane + S_COL + b * NP, r);
+                        tmem_ld_wait<NP>(r);
+    #pragma unroll
+                        for (int c = 0; c < NP; ++c) s[c] = masked ? -INFINITY : __uint_as_float(r[c]) * sl2;
+                    }
+                    // A row's first tile always takes the exact max (its references
+                    // are -inf); later tiles only when a score crosses its reference.
+                    bool any = t == 0;
+                    if (!any) {
+                        bool exceed = false;
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c)
+                            if (c < nh) exceed |= s[c] > mr[c] + RESCALE_THRESHOLD;
+                        const unsigned vote = __ballot_sync(0xffffffffu, exceed);
+                        volatile int* fl = flags + (g & 1) * 4;
+                        if (lane == 0) fl[wq] = vote != 0;
+                        ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        any = fl[0] | fl[1] | fl[2] | fl[3];
+                    }
+                    if (any) {
+                        // The tile's max per head: warp maxima -> red (its slot of
+                        // this tile parity) -> one barrier -> every thread.
+                        float* rd = red + (g & 1) * (4 * NP);
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c) {
+                            if (c >= nh) break;
+                            float m = s[c];
+    #pragma unroll
+                            for (int o = 16; o > 0; o >>= 1)
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                            if (lane == 0) rd[wq * NP + c] = m;
+                        }
+                        ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        float f[HQ];
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c) {
+                            f[c] = 1.0f;
+                            if (c < nh) {
+                                const float tmax = fmaxf(fmaxf(rd[c], rd[NP + c]),
+                                                         fmaxf(rd[2 * NP + c], rd[3 * NP + c]));
+                                if (tmax > mr[c] + RESCALE_THRESHOLD) {
+                                    f[c] = (mr[c] == -INFINITY) ? 0.f : ex2(mr[c] - tmax);
+                                    mr[c] = tmax;
+                                }
+                            }
+                        }
+                        if (t > 0) {
+                            // O^T must hold every earlier P.V of the row before it is rescaled.
+                            const uint32_t x = g - 1;
+                            ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                            ok = __all_sync(0xffffffffu, ok);
+                            if (!ok) break;
+                            tc_fence_after();
+    #pragma unroll
+                            for (int h = 0; h < HALVES; ++h) {
+                                uint32_t r[NP];
+                                tmem_ld16(t_lane + O_COL + h * NP, r);
+                                tmem_ld_wait<NP>(r);
+    #pragma unroll
+                                for (int c = 0; c < HQ; ++c)
+                                    r[c] = __float_as_uint(__uint_as_float(r[c]) * f[c]);
+                                tmem_st16(t_lane + O_COL + h * NP, r);
+                            }
+                            tmem_st_wait();
+                        }
+    #pragma unroll
+                        for (int c = 0; c < HQ; ++c) lpart[c] *= f[c];
+                    }
+                    ok = mbar_wait(bar(B_PTEMPTY + b), ((g >> 1) & 1) ^ 1, abort_flag, P.err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    uint8_t* pt = gbase + OFF_PT + b * PT_BYTES;
+                    const int kc = k >> 6, kin = k & 63;
+    #pragma unroll
+                    for (int c = 0; c < NP; ++c) {
+                        float p = 0.f;
+                        if (c < HQ && c < nh) {
+                            const float m = mr[c < HQ ? c : 0];
+                            p = ex2(s[c] - (m == -INFINITY ? 0.f : m));
+                            lpart[c < HQ ? c : 0] += p;
+                        }
+                        const uint32_t off = kc * (NP * 128) + sw128(c, kin >> 3) + (kin & 7) * 2;
+                        *reinterpret_cast<__half*>(pt + off) = __float2half_rn(p);
+                    }
+                    fence_async_shared();
+                    mbar_arrive(bar(B_PREADY + b));
+                }
+                if (!ok) break;
+                // ---------------------------------------------------------- row epilogue
+                const uint32_t x = g - 1;
+                ok = mbar_wait(bar(B_PTEMPTY + (x & 1)), (x >> 1) & 1, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                // Row sums: warp sums -> redl (its slot of this row parity) -> one
+                // barrier.  The next write to the same slot comes two rows later,
+                // behind barriers every thread passes after its reads here.
+                float* rl = redl + rpar * (4 * NP);
+                rpar ^= 1;
+    #pragma unroll
+                for (int c = 0; c < HQ; ++c) {
+                    if (c >= nh) break;
+                    float v = lpart[c];
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) rl[wq * NP + c] = v;
+                }
+                ok = group_sync(bar(B_GROUP), gphase, abort_flag, P.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                float inv[HQ];
+    #pragma unroll
+                for (int c = 0; c < HQ; ++c) {
+                    const float l = (rl[c] + rl[NP + c]) + (rl[2 * NP + c] + rl[3 * NP + c]);
+                    inv[c] = l > 0.f ? 1.0f / l : 0.f;
+                }
+    #pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    uint32_t r[NP];
+                    tmem_ld16(t_lane + O_COL + h * NP, r);
+                    tmem_ld_wait<NP>(r);
+                    const int d = h * 128 + k;
+    #pragma unroll
+                    for (int c = 0; c < HQ; ++c)
+                        if (c < nh)
+                            P.out[(size_t)i * q_stride + c * DH + d] =
+                                __float2half_rn(__uint_as_float(r[c]) * inv[c]);
+                }
             }
         }
     }
 
-    if (warp == IDX_WARP)
-        index_warp(P, reinterpret_cast<int*>(gbase + OFF_IDX),
-                   reinterpret_cast<uint32_t*>(gbase + OFF_SEEN), bar(B_IFULL), bar(B_IEMPTY),
-                   abort_flag);
+    if (warp == IDX_WARP) {
+        if constexpr (PAIR)
+            index_warp_pairs(P, reinterpret_cast<int*>(gbase + OFF_IDX), bar(B_IFULL),
+                             bar(B_IEMPTY), abort_flag);
+        else
+            index_warp(P, reinterpret_cast<int*>(gbase + OFF_IDX),
+                       reinterpret_cast<uint32_t*>(gbase + OFF_SEEN), bar(B_IFULL), bar(B_IEMPTY),
+                       abort_flag);
+    }
 
     tc_fence_before();
     __syncthreads();
@@ -797,19 +946,6 @@ template <int HQ, bool PAIR>
 constexpr int f8_ts() { return (HQ == NP || PAIR) ? NP : 8; }
 template <int HQ, bool PAIR>
 constexpr int f8_n() { return (3 * f8_ts<HQ, PAIR>() + 15) / 16 * 16; }
-// Work units.  Without PAIR a unit is one row.  With PAIR (every row selects
-// at most 16 blocks, i.e. 64 keys) unit u is rows 2u and 2u + 1 sharing one
-// tile: row 2u's keys are keys 0 .. 63 and its heads columns 0 .. 7 of S^T /
-// O^T, row 2u + 1's keys 64 .. 127 and columns 8 .. 15; a score of one row's
-// head against the other row's key is masked.  Half as many tiles, each
-// full, where a row alone would fill half of one.
-template <bool PAIR>
-__device__ __forceinline__ int num_units(const Params& P) { return PAIR ? (P.rows + 1) / 2 : P.rows; }
-template <bool PAIR>
-__device__ __forceinline__ int unit_tiles(const Params& P, int u) {
-    if (!PAIR) return row_tiles(sel_count(P, u));
-    return (sel_count(P, 2 * u) > 0 || sel_count(P, 2 * u + 1) > 0) ? 1 : 0;
-}
 // Half the bytes of the fp16 rows: eight gather warps move a tile's codes in
 // about the time sixteen take for fp16.
 template <int HQ, int DH>
@@ -1592,14 +1728,24 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
             smem = pair ? SL8<kHq, 256, true>::SMEM
                         : (six ? SL8<kHq, 256, false>::SMEM : SL8<NP, 256, false>::SMEM);
         }
-    } else if (Dh == 128) {
-        fn = six ? sparse_kernel<kHq, 128> : sparse_kernel<NP, 128>;
-        threads = six ? nthreads<kHq, 128>() : nthreads<NP, 128>();
-        smem = smem_bytes<128>();
     } else {
-        fn = six ? sparse_kernel<kHq, 256> : sparse_kernel<NP, 256>;
-        threads = six ? nthreads<kHq, 256>() : nthreads<NP, 256>();
-        smem = smem_bytes<256>();
+        // As above: two rows per tile for the 6-head family when they fit.
+        const bool pair = six && max_sel * BLK <= TILE / 2;
+        if (pair) {
+            const int units = (rows + 1) / 2;
+            P.G = units < di->num_sms ? units : di->num_sms;
+        }
+        if (Dh == 128) {
+            fn = pair ? sparse_kernel<kHq, 128, true>
+                      : (six ? sparse_kernel<kHq, 128, false> : sparse_kernel<NP, 128, false>);
+            threads = six ? nthreads<kHq, 128>() : nthreads<NP, 128>();
+            smem = smem_bytes<128>();
+        } else {
+            fn = pair ? sparse_kernel<kHq, 256, true>
+                      : (six ? sparse_kernel<kHq, 256, false> : sparse_kernel<NP, 256, false>);
+            threads = six ? nthreads<kHq, 256>() : nthreads<NP, 256>();
+            smem = smem_bytes<256>();
+        }
     }
     if (ensure_smem_limit(reinterpret_cast<const void*>(fn), smem) != GQA_OK)
         return GQA_ERR_CUDA;

@@ -265,8 +265,8 @@ def _sparse_ref(s, e4m3, rows=None):
 @pytest.mark.parametrize("e4m3", [False, True])
 @pytest.mark.parametrize("T", [512, 64])
 def test_sparse_edge_cases(cuda_lib, kind, e4m3, T):
-    """T = 64 (16 blocks per row) runs the E4M3 kernel's two-rows-per-tile
-    form: one row's heads against the other row's keys must stay masked."""
+    """T = 64 (16 blocks per row) runs the kernels' two-rows-per-tile form:
+    one row's heads against the other row's keys must stay masked."""
     rows, ctx = 201, 4096
     q, k, v, scale = structured(kind, rows, ctx, seed=SEEDS[kind] + e4m3, dominant_rows_tail=True)
     s = inputs.sparse_from_values(q.half(), k if e4m3 else k.half(), v if e4m3 else v.half(),

@@ -197,7 +197,8 @@ def _with_duplicates(sel, cnt, seed, extra=8):
 
 
 @pytest.mark.parametrize("ctx,e4m3,T,extra", [(4096, False, 512, 8), (4096, True, 512, 8),
-                                              (70000, False, 512, 8), (4096, True, 40, 6)])
+                                              (70000, False, 512, 8), (4096, True, 40, 6),
+                                              (4096, False, 40, 6)])
 def test_sparse_duplicate_ids_are_masked_and_flagged(cuda_lib, ctx, e4m3, T, extra):
     """Selection has set semantics ("[Kernel][SM70] Repair #378 on latest
     main", Changes: stale or repeated entries are masked, not attended): a
@@ -206,8 +207,8 @@ def test_sparse_duplicate_ids_are_masked_and_flagged(cuda_lib, ctx, e4m3, T, ext
     builds each row's visible set) and the error bit is set.  At ctx 70000
     the later rows' block ids exceed the kernel's exact 16384-bit set, so its
     hashed set with confirmation is exercised.  At T = 40 with 6 repeats (16
-    positions) the E4M3 kernel runs two rows per tile and finds repeats
-    within each half of the tile."""
+    positions) the kernels run two rows per tile and find repeats within
+    each half of the tile."""
     rows = 301
     mk = inputs.sparse_e4m3_inputs if e4m3 else inputs.sparse_inputs
     s = mk(rows=rows, ctx_len=ctx, tokens=T, seed=31 + e4m3)
@@ -242,6 +243,7 @@ def test_sparse_duplicate_ids_are_masked_and_flagged(cuda_lib, ctx, e4m3, T, ext
     (6, 1, 200, 4096, 512, 16, False),
     (6, 1, 200, 4096, 512, 16, True),
     (6, 1, 301, 4096, 64, 16, True),
+    (6, 1, 301, 4096, 64, 16, False),
     (6, 1, 1, 4, 4, 16, False),          # one row, one block
     (6, 2, 100, 3001, 256, 32, False),   # two KV heads
     (8, 1, 120, 4096, 128, 8, True),     # generic 16-column instantiation
