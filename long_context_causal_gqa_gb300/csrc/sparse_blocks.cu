@@ -931,12 +931,15 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
 // A moved reference max sits REF_SHIFT below the tile's max, so that P stays
 // far above the expansion's floor of 2^-19 (the paged tail's rule).
 // Warps: gather warps (half K, half V), the UMMA issuer, four key warps, the
-// token index warp, then F8_QWARPS warps that build each row's Q expansion
-// one row ahead (two Q buffers).  Two K and two V buffers: the gather of
+// token index warp, then the warps that build each unit's Q expansion one
+// unit ahead (two Q buffers).  Two K and two V buffers: the gather of
 // tile t + 1 never waits for the Q.K^T of tile t.
 // ======================================================================
 constexpr float REF_SHIFT = 6.0f;
-constexpr int F8_QWARPS = 2;
+// Warps that build the Q expansions: two for a row's heads, four for a
+// unit of two rows (twelve head rows per unit).
+template <bool PAIR>
+constexpr int f8_qwarps() { return PAIR ? 4 : 2; }
 constexpr int F8_NKB = 2, F8_NVB = 2;   // K / V tile buffers
 constexpr int F8_NQB = 2;               // Q expansion buffers
 // Rows per expansion term (the heads of the launch, padded to 8; with PAIR
@@ -950,8 +953,8 @@ constexpr int f8_n() { return (3 * f8_ts<HQ, PAIR>() + 15) / 16 * 16; }
 // about the time sixteen take for fp16.
 template <int HQ, int DH>
 constexpr int f8_gather_warps() { return 8; }
-template <int HQ, int DH>
-constexpr int f8_nthreads() { return 32 * (f8_gather_warps<HQ, DH>() + 6 + F8_QWARPS); }
+template <int HQ, int DH, bool PAIR>
+constexpr int f8_nthreads() { return 32 * (f8_gather_warps<HQ, DH>() + 6 + f8_qwarps<PAIR>()); }
 enum {
     F_KFULL = 0,      // [F8_NKB]
     F_KEMPTY = 2,     // [F8_NKB]
@@ -999,14 +1002,15 @@ struct SL8 {
 constexpr uint32_t F8_TMEM_COLS = 256;
 
 template <int HQ, int DH, bool PAIR>
-__global__ void __launch_bounds__(f8_nthreads<HQ, DH>(), 1) sparse_f8_kernel(const Params P) {
+__global__ void __launch_bounds__(f8_nthreads<HQ, DH, PAIR>(), 1) sparse_f8_kernel(const Params P) {
     static_assert(!PAIR || HQ <= 8, "two rows' heads in 16 columns");
     using L = SL8<HQ, DH, PAIR>;
     const int NU = num_units<PAIR>(P);
     constexpr int HALVES = DH / 128;
     constexpr int TS = L::TS, N3 = L::N3, RAW_TILE = L::RAW_TILE;
     constexpr int NGW = f8_gather_warps<HQ, DH>();
-    constexpr int NTHREADS = f8_nthreads<HQ, DH>();
+    constexpr int NTHREADS = f8_nthreads<HQ, DH, PAIR>();
+    constexpr int F8_QWARPS = f8_qwarps<PAIR>();
     constexpr int MMA_WARP = NGW, KEY_WARP0 = NGW + 1, IDX_WARP = NGW + 5, Q_WARP0 = NGW + 6;
     constexpr int NGATHER = 32 * (NGW / 2);   // arrivals per K or V tile
     // E4M3 x E4M3 -> f32 (format fields 0 = E4M3 for kind::f8f6f4); A = K
@@ -1718,13 +1722,15 @@ int sparse_launch(const void* q, const void* kcache, const void* vcache, const f
         if (Dh == 128) {
             fn = pair ? sparse_f8_kernel<kHq, 128, true>
                       : (six ? sparse_f8_kernel<kHq, 128, false> : sparse_f8_kernel<NP, 128, false>);
-            threads = six ? f8_nthreads<kHq, 128>() : f8_nthreads<NP, 128>();
+            threads = pair ? f8_nthreads<kHq, 128, true>()
+                           : (six ? f8_nthreads<kHq, 128, false>() : f8_nthreads<NP, 128, false>());
             smem = pair ? SL8<kHq, 128, true>::SMEM
                         : (six ? SL8<kHq, 128, false>::SMEM : SL8<NP, 128, false>::SMEM);
         } else {
             fn = pair ? sparse_f8_kernel<kHq, 256, true>
                       : (six ? sparse_f8_kernel<kHq, 256, false> : sparse_f8_kernel<NP, 256, false>);
-            threads = six ? f8_nthreads<kHq, 256>() : f8_nthreads<NP, 256>();
+            threads = pair ? f8_nthreads<kHq, 256, true>()
+                           : (six ? f8_nthreads<kHq, 256, false>() : f8_nthreads<NP, 256, false>());
             smem = pair ? SL8<kHq, 256, true>::SMEM
                         : (six ? SL8<kHq, 256, false>::SMEM : SL8<NP, 256, false>::SMEM);
         }
