@@ -25,6 +25,13 @@ namespace gqa {
 // Ratio between consecutive terms of a three-term E4M3 expansion.
 constexpr float XRATIO = 32.0f;
 
+// A softmax whose P enters such an expansion keeps P <= 256 (a score may
+// exceed its row's reference by at most 8 in log2 units before the reference
+// moves) and, when the reference moves, sets it this far below the tile's
+// max (log2 units): right after a move the largest P is 2^6, and the
+// expansion's floor of 2^-19 sits at least 25 binades below the row's max.
+constexpr float REF_SHIFT = 6.0f;
+
 // FP8 UMMA: D (+)= A . B with E4M3 operands from shared memory, f32 accumulator
 // (the instruction descriptor's A / B format fields 0 select E4M3 here).
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,

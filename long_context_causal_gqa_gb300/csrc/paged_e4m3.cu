@@ -74,8 +74,6 @@ constexpr int TILE = 128;        // keys per tile
 // then 4 * NWG softmax warps.
 __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
 constexpr float RESCALE_THRESHOLD = 8.0f;
-// A moved reference sits this far below the tile's max (log2 units).
-constexpr float REF_SHIFT = 6.0f;
 
 struct Params {
     const uint8_t* kcache;

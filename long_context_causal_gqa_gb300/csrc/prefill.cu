@@ -444,7 +444,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr bool TWO_ISSUERS = NSB == 3;
     constexpr uint32_t IDESC_PV = idesc_f16_f32(256, DH, false, true);
     using C = Cfg<F8, DH>;
-    constexpr int NK = C::NK, NV = C::NV, NRING = C::NRING;
+    constexpr int NK = C::NK, NRING = C::NRING;
     constexpr int RING_BYTES = C::RING_BYTES, NUM_BARS = C::NUM_BARS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;

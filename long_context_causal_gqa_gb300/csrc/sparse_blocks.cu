@@ -935,7 +935,6 @@ __global__ void __launch_bounds__(nthreads<HQ, DH>(), 1) sparse_kernel(const Par
 // unit ahead (two Q buffers).  Two K and two V buffers: the gather of
 // tile t + 1 never waits for the Q.K^T of tile t.
 // ======================================================================
-constexpr float REF_SHIFT = 6.0f;
 // Warps that build the Q expansions: two for a row's heads, four for a
 // unit of two rows (twelve head rows per unit).
 template <bool PAIR>
