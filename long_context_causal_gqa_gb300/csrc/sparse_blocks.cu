@@ -23,8 +23,9 @@
 //     S^T[128 x 16] = K[128 x 256] . Q^T,  O^T[256 x 16] += V^T . P^T.
 // * Softmax across TMEM lanes with a lazily moved per-head reference max
 //   (exact cross-lane max only on a row's first tile or when a score exceeds
-//   the reference by more than 8 in log2 units); row sums stay per thread
-//   until the row ends.  The epilogue writes out[i] directly (no split).
+//   the reference by more than 8 in log2 units; every key thread holds the
+//   references in registers); row sums stay per thread until the row ends.
+//   The epilogue writes out[i] directly (no split).
 //
 // * An E4M3 cache (the tail's storage applied to this workload) halves the
 //   gathered bytes and has a kernel of its own (sparse_f8_kernel): the codes
@@ -50,7 +51,8 @@
 //
 // Warp roles: gather warps, then the TMEM owner + UMMA issuer, four key warps
 // (softmax + epilogue; thread = TMEM lane) and the token index warp (and, in
-// the E4M3 kernel, two warps that build the Q expansions).
+// the E4M3 kernel, the warps that build the Q expansions: two, or four for
+// two-row units).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
