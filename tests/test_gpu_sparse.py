@@ -169,13 +169,16 @@ def test_sparse_bitwise_reproducible_and_graph_replay(cuda_lib):
 
 
 @pytest.mark.parametrize("page", [8, 32, 64, 256])
-def test_sparse_other_page_sizes(cuda_lib, page):
-    """Page sizes other than the pages' 16 (any power of two in [8, 256])."""
-    s = inputs.sparse_inputs(rows=96, ctx_len=3000, tokens=128, seed=page, page=page)
+@pytest.mark.parametrize("T", [128, 60])
+def test_sparse_other_page_sizes(cuda_lib, page, T):
+    """Page sizes other than the pages' 16 (any power of two in [8, 256]);
+    T = 60 (15 blocks per row) runs the two-rows-per-tile form, 97 rows the
+    last unit with one row."""
+    s = inputs.sparse_inputs(rows=97, ctx_len=3000, tokens=T, seed=page + T, page=page)
     out = _run(cuda_lib, s)
     ref = oracle.sparse_blocks(s.q, s.kcache, s.vcache, s.block_table, s.sel_idx, s.sel_cnt,
                                s.ctx_len, s.scale)
-    _check(out, ref, f"page={page}")
+    _check(out, ref, f"page={page} T={T}")
 
 
 def _with_duplicates(sel, cnt, seed, extra=8):

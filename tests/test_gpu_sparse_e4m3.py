@@ -50,6 +50,7 @@ def _ref(s, rows=None):
 @pytest.mark.parametrize("rows,ctx,T,page", [
     (1, 4, 4, 16), (5, 41, 12, 16), (64, 2048, 64, 16), (100, 3001, 512, 16),
     (300, 5000, 200, 16), (200, 4096, 2048, 16), (77, 2000, 300, 8), (90, 3000, 256, 64),
+    (77, 2000, 60, 8), (91, 3000, 64, 64), (33, 1500, 48, 256),
 ])
 def test_sparse_e4m3_matches_oracle(cuda_lib, rows, ctx, T, page):
     s = inputs.sparse_e4m3_inputs(rows=rows, ctx_len=ctx, tokens=T, seed=rows + T, page=page,
