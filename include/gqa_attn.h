@@ -272,6 +272,16 @@ int gqa_set_workspace(int device, void* ptr, size_t bytes);
  * themselves failed. */
 int gqa_get_device_error(struct CUstream_st* stream);
 
+/* Diagnostic (an addition of this library): queues on `stream` a one-warp
+ * kernel that runs the bounded wait every pipeline barrier of the library's
+ * kernels uses, on an mbarrier that nothing ever arrives on.  After the
+ * wait's limit (about 2 s) it gives up, sets GQA_DEVERR_WAIT_TIMEOUT in the
+ * device error word and the kernel returns, so the context stays usable: a
+ * caller can check that a stalled pipeline reports an error instead of
+ * hanging.  Read the result with gqa_get_device_error.  Returns GQA_OK once
+ * queued, GQA_ERR_CUDA if the launch failed. */
+int gqa_check_wait_limit(struct CUstream_st* stream);
+
 /* Number of SM pairs (two-CTA clusters) gqa_attn_prefill runs on for the
  * current device: the clusters of its kernel that can be resident at once,
  * which the GPC layout can put below half the SM count.  Returns -1 on a CUDA

@@ -42,7 +42,7 @@ EXPORTED = ("gqa_attn_prefill", "gqa_attn_prefill_e4m3", "gqa_attn_paged_e4m3", 
             "gqa_attn_paged_e4m3_noalloc",
             "gqa_attn_sparse_blocks", "gqa_attn_sparse_blocks_e4m3",
             "gqa_workspace_bytes", "gqa_set_workspace", "gqa_get_device_error",
-            "gqa_prefill_sm_pairs", "gqa_status_string")
+            "gqa_check_wait_limit", "gqa_prefill_sm_pairs", "gqa_status_string")
 
 
 class GQAError(RuntimeError):
@@ -92,6 +92,8 @@ def load():
             lib.gqa_set_workspace.restype = I
             lib.gqa_get_device_error.argtypes = [P]
             lib.gqa_get_device_error.restype = I
+            lib.gqa_check_wait_limit.argtypes = [P]
+            lib.gqa_check_wait_limit.restype = I
             lib.gqa_prefill_sm_pairs.argtypes = []
             lib.gqa_prefill_sm_pairs.restype = I
             lib.gqa_status_string.argtypes = [I]
@@ -164,6 +166,15 @@ def device_error(stream=None) -> int:
     if v < 0:
         raise GQAError(GQA_ERR_CUDA, "gqa_get_device_error")
     return v
+
+
+def check_wait_limit(stream=None) -> None:
+    """Queue the bounded-wait diagnostic (gqa_check_wait_limit): a wait on an
+    mbarrier nothing arrives on, which gives up after its limit and sets
+    DEVERR_WAIT_TIMEOUT; read it with device_error()."""
+    st = load().gqa_check_wait_limit(_stream_ptr(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_check_wait_limit")
 
 
 def prefill_sm_pairs() -> int:

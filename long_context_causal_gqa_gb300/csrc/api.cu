@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace gqa {
 
@@ -20,6 +21,20 @@ __device__ unsigned g_err_snapshot;
 
 // Reads and clears the error word in one atomic step.
 __global__ void err_exchange_kernel() { g_err_snapshot = atomicExch(&g_err_word, 0u); }
+
+// The kernels' bounded pipeline wait on an mbarrier that nothing arrives on:
+// it gives up after its limit, records the timeout in *err and returns.
+__global__ void wait_limit_kernel(unsigned* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
+}
 
 namespace {
 
@@ -388,6 +403,13 @@ int gqa_get_device_error(struct CUstream_st* stream) {
         return -1;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
     return (int)v;
+}
+
+int gqa_check_wait_limit(struct CUstream_st* stream) {
+    const DeviceInfo* di = device_info();
+    if (!di) return GQA_ERR_CUDA;
+    wait_limit_kernel<<<1, 32, 0, stream>>>(di->err_word);
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 int gqa_prefill_sm_pairs(void) { return prefill_resident_pairs(); }
